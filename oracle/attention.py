@@ -1,0 +1,190 @@
+"""Exact vs compressed decode attention, total variation, and the two-tier meter (oracle; test infrastructure).
+
+Everything is float64 and follows WitCert (arXiv 2607.28699):
+
+* §3 "Setup and notation": p and p~ are the softmax attention distributions over
+  the S cached tokens from exact and compressed keys; the metered quantity is
+  TV(p, p~) = 1/2 sum_t |p_t - p~_t|, reported as min(1, .) because TV <= 1.
+* §3 Theorem 1: with A = E_p~[e^{c}] and |eps_t| <= c_t, TV <= 1/2 (A^2 - 1).
+  "evaluate A in the log domain and return the trivial bound 1 on overflow;
+  we never truncate the error parameter": here the meter state is ln(A - 1),
+  computed by log-sum-exp, so it never overflows.
+* §4.1 Theorem 2: c_t = (1/sqrt(d)) sum_b ||q_b|| w_{t,b} (the kernel form uses
+  sm_scale in place of 1/sqrt(d)); w is the stored fp16 witness.
+* §4.2: Tier B radius u_t = sqrt(2 varsigma_t^2 log(2S/delta_loc)) with
+  varsigma_t^2 = (1/d) sum_c q_c^2 s_{c,t}^2 / 12, delta_loc = delta_req/(L*H*T);
+  with one scale per (token, kv head) this is
+  u_t = sm_scale * ||q|| * s_t * sqrt(2 ln(2S/delta_loc) / 12) (§6.2.2 hoists the sqrt).
+* §4.3: meter = min(1, 1/2 (A^2 - 1)); the raw value (kept as a log score
+  ln(1/2 (A^2 - 1))) is a risk score with no guarantee above 1.
+* "Compress the shared cartridge", "One kernel spans cartridge and live KV":
+  the shared prefix and the request's live suffix form one logical sequence
+  under one softmax (the caller concatenates them before calling this module).
+
+The output is o = sum_t p~_t v_hat_t with the dequantized values.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+from .quant import HEAD_DIM, N_BANDS
+
+__all__ = [
+    "DecodeResult",
+    "logsumexp",
+    "log_expm1",
+    "softmax",
+    "total_variation",
+    "band_q_norms",
+    "tier_a_radius",
+    "tier_b_radius",
+    "log_a_minus_1",
+    "meter_from_log_am1",
+    "raw_log_score",
+    "decode_head",
+    "flawed_dispersion_bound",
+    "two_sided_bound",
+]
+
+
+def logsumexp(a: np.ndarray, axis=-1) -> np.ndarray:
+    a = np.asarray(a, dtype=np.float64)
+    m = np.max(a, axis=axis, keepdims=True)
+    m = np.where(np.isfinite(m), m, 0.0)
+    with np.errstate(divide="ignore"):
+        out = np.log(np.sum(np.exp(a - m), axis=axis, keepdims=True)) + m
+    return np.squeeze(out, axis=axis)
+
+
+def log_expm1(c: np.ndarray) -> np.ndarray:
+    """ln(e^c - 1) for c >= 0, accurate for tiny and huge c (-inf at c = 0)."""
+    c = np.asarray(c, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        small = np.log(np.expm1(np.minimum(c, 1.0)))
+        large = c + np.log1p(-np.exp(-np.maximum(c, 1.0)))
+    return np.where(c < 1.0, small, large)
+
+
+def softmax(x: np.ndarray) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float64)
+    return np.exp(x - logsumexp(x)[..., None])
+
+
+def total_variation(p: np.ndarray, p_t: np.ndarray) -> np.ndarray:
+    """TV(p, p~) = 1/2 sum_t |p_t - p~_t| (WitCert §3)."""
+    return 0.5 * np.sum(np.abs(p - p_t), axis=-1)
+
+
+def band_q_norms(q: np.ndarray) -> np.ndarray:
+    """||q_b|| over the 16 half-split RoPE bands, q [..., 128] -> [..., 16]."""
+    q = np.asarray(q, dtype=np.float64)
+    half = HEAD_DIM // 2
+    per = half // N_BANDS
+    lo = q[..., :half].reshape(q.shape[:-1] + (N_BANDS, per))
+    hi = q[..., half:].reshape(q.shape[:-1] + (N_BANDS, per))
+    return np.sqrt(np.sum(lo * lo, -1) + np.sum(hi * hi, -1))
+
+
+def tier_a_radius(q: np.ndarray, w: np.ndarray, sm_scale: float) -> np.ndarray:
+    """c_t = sm_scale * sum_b ||q_b|| w_{t,b} (WitCert §4.1, Theorem 2).  q [128], w [S, 16] -> [S]."""
+    return sm_scale * (np.asarray(w, dtype=np.float64) @ band_q_norms(q))
+
+
+def tier_b_radius(q: np.ndarray, s_k: np.ndarray, sm_scale: float, seq_len: int,
+                  delta_req: float, n_layers: int, n_q_heads: int, n_steps: int) -> np.ndarray:
+    """u_t = sm_scale ||q|| s_t sqrt(2 ln(2S/delta_loc)/12), delta_loc = delta_req/(L H T) (WitCert §4.2)."""
+    delta_loc = delta_req / (n_layers * n_q_heads * n_steps)
+    kappa = math.sqrt(2.0 * math.log(2.0 * seq_len / delta_loc) / 12.0)
+    qn = float(np.sqrt(np.sum(np.asarray(q, dtype=np.float64) ** 2)))
+    return sm_scale * qn * kappa * np.asarray(s_k, dtype=np.float64)
+
+
+def log_a_minus_1(log_p: np.ndarray, radius: np.ndarray) -> float:
+    """ln(A - 1) with A - 1 = sum_t p~_t (e^{c_t} - 1), evaluated in the log domain (WitCert §3)."""
+    terms = np.asarray(log_p, dtype=np.float64) + log_expm1(radius)
+    if not np.any(np.isfinite(terms)):
+        return -math.inf
+    return float(logsumexp(terms))
+
+
+def meter_from_log_am1(lam1) -> np.ndarray:
+    """min(1, 1/2 (A^2 - 1)) from ln(A - 1) (WitCert §4.3); A - 1 >= e^0 = 1 always saturates."""
+    lam1 = np.asarray(lam1, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        am1 = np.exp(np.minimum(lam1, 1.0))
+    return np.minimum(1.0, 0.5 * am1 * (am1 + 2.0))
+
+
+def raw_log_score(lam1) -> np.ndarray:
+    """ln(1/2 (A^2 - 1)) = ln(A-1) + ln(A+1) - ln 2, finite for any finite ln(A-1) (WitCert §4.3)."""
+    lam1 = np.asarray(lam1, dtype=np.float64)
+    return lam1 + np.logaddexp(math.log(2.0), lam1) - math.log(2.0)
+
+
+@dataclass
+class DecodeResult:
+    out: np.ndarray          # [H, 128] compressed-attention output
+    lse: np.ndarray          # [H] log-sum-exp of the compressed logits
+    tv: np.ndarray           # [H] exact total variation between p and p~
+    log_am1_a: np.ndarray    # [H] ln(A - 1), Tier A
+    meter_a: np.ndarray      # [H] min(1, 1/2 (A^2 - 1)), Tier A
+    raw_a: np.ndarray        # [H] ln(1/2 (A^2 - 1)), Tier A
+    log_am1_b: np.ndarray    # [H] ln(A_B - 1), Tier B (nan when not requested)
+    cert_b: np.ndarray       # [H] min(1, 1/2 (A_B^2 - 1)) (nan when not requested)
+    c_max: np.ndarray        # [H] max_t c_t (diagnostic)
+
+
+def decode_head(q: np.ndarray, k_exact: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray,
+                w: np.ndarray, sm_scale: float, s_k: np.ndarray | None = None,
+                tier_b: dict | None = None) -> DecodeResult:
+    """Decode attention of H query heads that share one kv head's cache.
+
+    q [H, 128] (the query values exactly as the kernel reads them), k_exact
+    [S, 128] (the binary32 post-RoPE keys), k_hat / v_hat [S, 128] (exact
+    dequantized cache), w [S, 16] (witness values), s_k [S] (key scales, Tier B),
+    tier_b = dict(delta_req, n_layers, n_q_heads, n_steps) or None.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    H = q.shape[0]
+    S = k_hat.shape[0]
+    x_exact = sm_scale * (q @ np.asarray(k_exact, dtype=np.float64).T)   # [H, S]
+    x_comp = sm_scale * (q @ np.asarray(k_hat, dtype=np.float64).T)
+    lse = logsumexp(x_comp)
+    log_pt = x_comp - lse[:, None]
+    p_t = np.exp(log_pt)
+    p = softmax(x_exact)
+    out = p_t @ np.asarray(v_hat, dtype=np.float64)
+    tv = total_variation(p, p_t)
+    la = np.empty(H)
+    lb = np.full(H, np.nan)
+    cmax = np.empty(H)
+    for h in range(H):
+        c = tier_a_radius(q[h], w, sm_scale)
+        cmax[h] = float(np.max(c)) if S else 0.0
+        la[h] = log_a_minus_1(log_pt[h], c)
+        if tier_b is not None:
+            u = tier_b_radius(q[h], s_k, sm_scale, S, **tier_b)
+            lb[h] = log_a_minus_1(log_pt[h], u)
+    return DecodeResult(out=out, lse=lse, tv=tv, log_am1_a=la, meter_a=meter_from_log_am1(la),
+                        raw_a=raw_log_score(la), log_am1_b=lb,
+                        cert_b=np.where(np.isnan(lb), np.nan, meter_from_log_am1(lb)), c_max=cmax)
+
+
+def flawed_dispersion_bound(p_t: np.ndarray, c: np.ndarray) -> float:
+    """WitCert §3 eq. (1), the plausible but unsound certificate (kept as a regression guard).
+
+    1/2 e^{2 c_max} ( E_p~|c - c_bar| + c_bar (e^{c_max} - 1) ), c_bar = E_p~[c].
+    """
+    p_t = np.asarray(p_t, dtype=np.float64)
+    c = np.asarray(c, dtype=np.float64)
+    cbar = float(p_t @ c)
+    cmax = float(np.max(c))
+    return 0.5 * math.exp(2 * cmax) * (float(p_t @ np.abs(c - cbar)) + cbar * (math.exp(cmax) - 1.0))
+
+
+def two_sided_bound(a: float, a_minus: float) -> float:
+    """WitCert §4.3 Proposition 1: TV <= 1/2 (A/A^- - A^-/A) with A^- = E_p~[e^{-c}]."""
+    return 0.5 * (a / a_minus - a_minus / a)

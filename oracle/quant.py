@@ -1,0 +1,150 @@
+"""Quantize-on-append, dequantization and the band-norm witness (oracle; test infrastructure).
+
+Layouts ("Compress the shared cartridge", table "Keys carry the cartridge
+quantization loss"; WitCert §4.2 and §6.2.3):
+
+  'bf16'   BF16 code, round-to-nearest-even (the K16 half of K16/V8 and K16/V16)
+  'e4m3'   raw FP8 E4M3 cast, no scale (the K8/V8 raw-cast layout)
+  'e4m3s'  FP8 E4M3 with one fp16 scale per (token, kv head): s = fp16(amax/448)
+  'int8'   subtractively dithered INT8 with one fp16 scale per (token, kv head):
+           s = fp16(amax/126.5), code = rint(x/s + xi), x_hat = s*(code - xi)
+
+Rules taken from the pages
+--------------------------
+* WitCert §4.2 "Subtractive dither": x_hat = s*(round(x/s + xi) - xi), xi uniform
+  on [-1/2, 1/2), s = amax/(Q - 1/2) with Q = 127, i.e. amax/126.5, chosen so that
+  no code clips.
+* WitCert §6.2.1: quantization must use the *stored* fp16 scale, not the fp32
+  one it was rounded from.
+* WitCert §6.2.3: with token-granular paging the scale is per token (per
+  channel group); the workloads here use one group of 128 channels per
+  (token, kv head).
+* WitCert §4.1, eq. (2): the witness w_{t,b} = ||r_{t,b}|| is the Euclidean
+  norm of the key residual r = k_hat - k over band b, stored in fp16.  Bands are
+  B = 16 contiguous groups of RoPE frequency pairs (4 pairs = 8 coordinates each).
+
+Readings where the pages are silent (listed in the design doc)
+-------------------------------------------------------
+* RoPE pairs are half-split: pair j = coordinates (j, j + 64).  Band b therefore
+  holds coordinates 4b..4b+3 and 64+4b..64+4b+3.
+* Every scalar step is the binary32 operation (evaluated in float64 and rounded
+  once): t = fp32(amax / 126.5) (or / 448), s = fp16_rn(t), y = fp32(x / s),
+  y2 = fp32(y + xi), code = clamp(round_half_even(y2), -127, 127).
+* amax = 0 (or a scale that rounds to fp16 zero) stores scale 0 and all-zero codes.
+* The fp16 witness is rounded up, so it never under-states the residual norm.
+* FP8-scaled values use s = fp16_rn(fp32(amax / 448)) and code = e4m3(fp32(v / s))
+  (round-to-nearest-even, saturating at +-448).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .encoders import (
+    bf16_bits_rne,
+    bf16_value,
+    e4m3_bits_rne_satfinite,
+    e4m3_value,
+    f32,
+    fp16_bits,
+    fp16_value,
+)
+
+__all__ = [
+    "FORMATS",
+    "HEAD_DIM",
+    "N_BANDS",
+    "band_of_channel",
+    "quantize",
+    "dequantize",
+    "witness_bits",
+    "band_norms",
+]
+
+HEAD_DIM = 128
+N_BANDS = 16
+FORMATS = ("bf16", "e4m3", "e4m3s", "int8")
+INT8_QMAX = 127
+INT8_DIVISOR = 126.5  # Q - 1/2 with Q = 127
+E4M3_DIVISOR = 448.0
+
+
+def band_of_channel(c):
+    """Band index of head-dim coordinate ``c`` under half-split RoPE pairing with 16 bands."""
+    c = np.asarray(c)
+    return (c % (HEAD_DIM // 2)) // ((HEAD_DIM // 2) // N_BANDS)
+
+
+def _scale_bits(amax32: np.ndarray, divisor: float) -> np.ndarray:
+    t = f32(amax32.astype(np.float64) / divisor)
+    return fp16_bits(t.astype(np.float64), "rne")
+
+
+def quantize(x32: np.ndarray, fmt: str, xi: np.ndarray | None = None):
+    """Quantize rows of 128 binary32 values.
+
+    ``x32``: [..., 128] float32.  ``xi``: [..., 128] dither (float64, exact) for
+    'int8'.  Returns ``(codes, scale_bits, valid)``: codes as uint16 (bf16
+    patterns), uint8 (e4m3 patterns) or int8 (INT8 codes); scale_bits [...]
+    uint16 fp16 patterns or None; ``valid`` [...] False where the row holds a
+    non-finite value or its scale overflows fp16 (the library flags those rows).
+    """
+    x = np.asarray(x32, dtype=np.float32)
+    assert x.shape[-1] == HEAD_DIM
+    finite = np.all(np.isfinite(x), axis=-1)
+    if fmt == "bf16":
+        return bf16_bits_rne(x), None, finite
+    if fmt == "e4m3":
+        return e4m3_bits_rne_satfinite(x), None, finite
+    amax = np.max(np.abs(x), axis=-1)
+    if fmt == "e4m3s":
+        s_bits = _scale_bits(amax, E4M3_DIVISOR)
+        s = fp16_value(s_bits)
+        valid = finite & np.isfinite(s)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            y = f32(x.astype(np.float64) / s[..., None])
+        codes = e4m3_bits_rne_satfinite(y)
+        codes = np.where((s == 0)[..., None], np.uint8(0), codes).astype(np.uint8)
+        return codes, s_bits, valid
+    if fmt == "int8":
+        assert xi is not None and xi.shape == x.shape
+        s_bits = _scale_bits(amax, INT8_DIVISOR)
+        s = fp16_value(s_bits)
+        valid = finite & np.isfinite(s)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            y = f32(x.astype(np.float64) / s[..., None])
+            y2 = f32(y.astype(np.float64) + xi)
+            code = np.clip(np.rint(y2.astype(np.float64)), -INT8_QMAX, INT8_QMAX)
+        code = np.where((s == 0)[..., None] | ~np.isfinite(code), 0, code)
+        return code.astype(np.int8), s_bits, valid
+    raise ValueError(fmt)
+
+
+def dequantize(codes: np.ndarray, scale_bits: np.ndarray | None, fmt: str, xi: np.ndarray | None = None):
+    """Exact float64 reconstruction x_hat of stored codes."""
+    if fmt == "bf16":
+        return bf16_value(codes)
+    if fmt == "e4m3":
+        return e4m3_value(codes)
+    s = fp16_value(scale_bits)[..., None]
+    if fmt == "e4m3s":
+        return s * e4m3_value(codes)
+    if fmt == "int8":
+        # s (11 bits) * (code - xi) (at most 31 bits) is exact in float64
+        return s * (codes.astype(np.float64) - xi)
+    raise ValueError(fmt)
+
+
+def band_norms(r: np.ndarray) -> np.ndarray:
+    """Per-band Euclidean norms of residual rows r [..., 128] -> [..., 16] float64."""
+    r = np.asarray(r, dtype=np.float64)
+    half = HEAD_DIM // 2
+    per = half // N_BANDS
+    lo = r[..., :half].reshape(r.shape[:-1] + (N_BANDS, per))
+    hi = r[..., half:].reshape(r.shape[:-1] + (N_BANDS, per))
+    return np.sqrt(np.sum(lo * lo, axis=-1) + np.sum(hi * hi, axis=-1))
+
+
+def witness_bits(k_hat: np.ndarray, k32: np.ndarray) -> np.ndarray:
+    """fp16 (round-up) patterns of the band norms of r = k_hat - k (WitCert §4.1, eq. (2))."""
+    r = np.asarray(k_hat, dtype=np.float64) - np.asarray(k32, dtype=np.float32).astype(np.float64)
+    return fp16_bits(band_norms(r), "ru")

@@ -1,0 +1,140 @@
+"""Pins of the oracle's Philox4x32-10 stream and dither (CPU).
+
+Agreement with an external Philox implementation is checked on the GPU (cuRAND's
+Philox4x32-10, tests/test_gpu_philox_pin.py).  Here the generator is pinned by
+properties that a plausible mistake (a wrong multiplier, a swapped word, a
+missing key bump, a wrong output-word mapping) breaks:
+
+* bijectivity: an independently written inverse recovers the counter;
+* the inverse uses the key schedule and multipliers in the opposite order, so
+  a round written with swapped output words fails it;
+* uniformity, independence and avalanche statistics;
+* the dither values lie on the documented grid and are symmetric.
+"""
+import numpy as np
+import pytest
+
+from oracle import philox as P
+
+
+def _inv_mod_2_32(m):
+    return pow(int(m), -1, 1 << 32)
+
+
+def _philox_inverse(y, key, rounds=10):
+    """Invert Philox4x32-``rounds`` written from the round definition (not from philox4x32_10)."""
+    y0, y1, y2, y3 = (np.asarray(v, dtype=np.uint64) for v in y)
+    mask = np.uint64(0xFFFFFFFF)
+    keys = []
+    k0, k1 = int(key[0]), int(key[1])
+    for r in range(rounds):
+        keys.append((k0, k1))
+        k0 = (k0 + 0x9E3779B9) & 0xFFFFFFFF
+        k1 = (k1 + 0xBB67AE85) & 0xFFFFFFFF
+    inv0 = np.uint64(_inv_mod_2_32(0xD2511F53))
+    inv1 = np.uint64(_inv_mod_2_32(0xCD9E8D57))
+    for r in reversed(range(rounds)):
+        kk0, kk1 = keys[r]
+        # forward: y1 = lo(M1*x2), y3 = lo(M0*x0), y0 = hi(M1*x2)^x1^k0, y2 = hi(M0*x0)^x3^k1
+        x2 = (y1 * inv1) & mask
+        x0 = (y3 * inv0) & mask
+        hi1 = (np.uint64(0xCD9E8D57) * x2) >> np.uint64(32)
+        hi0 = (np.uint64(0xD2511F53) * x0) >> np.uint64(32)
+        x1 = y0 ^ hi1 ^ np.uint64(kk0)
+        x3 = y2 ^ hi0 ^ np.uint64(kk1)
+        y0, y1, y2, y3 = x0, x1, x2, x3
+    return y0, y1, y2, y3
+
+
+def test_constants_are_the_published_ones():
+    # Weyl constants: floor(2^32 * (golden ratio - 1)) and floor(2^32 * (sqrt(3) - 1))
+    import math
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    phi = (1 + Decimal(5).sqrt()) / 2
+    assert P.PHILOX_W0 == int((phi - 1) * (1 << 32))
+    assert P.PHILOX_W1 == int((Decimal(3).sqrt() - 1) * (1 << 32))
+    assert P.PHILOX_M0 % 2 == 1 and P.PHILOX_M1 % 2 == 1  # odd, hence invertible mod 2^32
+    assert math.gcd(P.PHILOX_M0, 1 << 32) == 1
+
+
+def test_bijective_via_independent_inverse():
+    rng = np.random.default_rng(11)
+    ctr = [rng.integers(0, 2**32, 10_000, dtype=np.uint64) for _ in range(4)]
+    key = (0x1234ABCD, 0xDEADBEEF)
+    y = P.philox4x32_10(ctr, key)
+    back = _philox_inverse(y, key)
+    for a, b in zip(ctr, back):
+        assert np.array_equal(a, b)
+
+
+def test_single_round_structure():
+    # one round with key (0, 0) on counter (1, 0, 0, 0): only the first product is non-zero
+    y = P.philox4x32_10(([1], [0], [0], [0]), (0, 0), rounds=1)
+    assert [int(v[0]) for v in y] == [0, 0, 0, P.PHILOX_M0]
+    y = P.philox4x32_10(([0], [0], [1], [0]), (0, 0), rounds=1)
+    assert [int(v[0]) for v in y] == [0, P.PHILOX_M1, 0, 0]
+    y = P.philox4x32_10(([0], [5], [0], [7]), (3, 9), rounds=1)
+    assert [int(v[0]) for v in y] == [5 ^ 3, 0, 7 ^ 9, 0]
+
+
+def test_uniform_and_independent_words():
+    n = 1 << 18
+    slots = np.arange(n, dtype=np.uint64)
+    w = P.philox4x32_10((slots, np.uint64(3), np.uint64(1), np.uint64(7)), (42, 0))
+    allw = np.concatenate([v for v in w]).astype(np.float64) / 2**32
+    # chi-square on 256 bins
+    hist = np.bincount((allw * 256).astype(int), minlength=256)
+    exp = allw.size / 256
+    chi2 = np.sum((hist - exp) ** 2 / exp)
+    assert chi2 < 255 + 6 * np.sqrt(2 * 255)
+    # words of one call are uncorrelated
+    c = np.corrcoef(np.stack([v.astype(np.float64) for v in w]))
+    assert np.max(np.abs(c - np.eye(4))) < 0.01
+
+
+def test_avalanche():
+    rng = np.random.default_rng(12)
+    ctr = [rng.integers(0, 2**32, 4096, dtype=np.uint64) for _ in range(4)]
+    base = P.philox4x32_10(ctr, (7, 8))
+    flipped = [c.copy() for c in ctr]
+    flipped[2] ^= np.uint64(1 << 13)
+    out = P.philox4x32_10(flipped, (7, 8))
+    diff = sum(np.unpackbits((a ^ b).astype(np.uint32).view(np.uint8)).sum() for a, b in zip(base, out))
+    frac = diff / (4096 * 128)
+    assert abs(frac - 0.5) < 0.01
+
+
+def test_dither_grid_range_and_moments():
+    slots = np.arange(20_000)[:, None]
+    ch = np.arange(128)[None, :]
+    xi = P.dither(0xABCDEF0123, layer=5, kv_head=2, slot=slots, channel=ch)
+    assert xi.shape == (20_000, 128)
+    assert np.all(xi > -0.5) and np.all(xi < 0.5)
+    n = (xi + 0.5) * 2**24 - 0.5
+    assert np.array_equal(n, np.round(n))          # on the mid-point grid
+    assert np.all(np.float32(xi) == xi)             # exact in binary32
+    assert abs(xi.mean()) < 3 * np.sqrt(1 / 12 / xi.size)
+    assert abs(xi.var() - 1 / 12) < 0.002
+    # the grid is symmetric: the extreme values are +-(1/2 - 2^-25)
+    assert (0.5 - 2**-25) in {abs(v) for v in (-0.5 + 2**-25, 0.5 - 2**-25)}
+
+
+def test_dither_stream_is_keyed_by_every_coordinate():
+    base = P.dither(99, 1, 0, np.arange(1000), 0)
+    assert not np.array_equal(base, P.dither(100, 1, 0, np.arange(1000), 0))   # seed
+    assert not np.array_equal(base, P.dither(99, 2, 0, np.arange(1000), 0))   # layer
+    assert not np.array_equal(base, P.dither(99, 1, 1, np.arange(1000), 0))   # kv head
+    assert not np.array_equal(base, P.dither(99, 1, 0, np.arange(1, 1001), 0))  # slot
+    # the four channels of one call come from the four output words, in order
+    w = P.philox4x32_10((np.arange(5, dtype=np.uint64), np.uint64(1), np.uint64(0), np.uint64(0)), (99, 0))
+    for c in range(4):
+        xi = P.dither(99, 1, 0, np.arange(5), c)
+        assert np.array_equal(xi, ((w[c] >> np.uint64(8)).astype(np.float64) + 0.5) * 2**-24 - 0.5)
+    # stream uniqueness: distinct (slot, layer, head, channel-group) tuples give distinct words
+    slots = np.repeat(np.arange(64), 32 * 2)
+    heads = np.tile(np.repeat(np.arange(2), 32), 64)
+    groups = np.tile(np.arange(32), 128)
+    words = P.philox4x32_10((slots.astype(np.uint64), np.uint64(3), heads.astype(np.uint64), groups.astype(np.uint64)), (5, 6))
+    packed = set(zip(*(v.tolist() for v in words)))
+    assert len(packed) == slots.size

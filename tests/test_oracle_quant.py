@@ -1,0 +1,140 @@
+"""Pins of the oracle's quantizers and witness (CPU).
+
+What pins what:
+* INT8 dither: |x_hat - x| <= s/2 (up to the binary32 rounding of x/s + xi)
+  and no code clips (WitCert §4.2, §6.2.1 "zero clipping", "|err| <= s/2");
+  the scale is the fp16 rounding of amax/126.5 (closed form); the stored scale
+  is the one quantized with (a row whose amax makes fp32 and fp16 scales differ).
+* E4M3 scaled: reconstruction error <= half an E4M3 step at each value.
+* BF16 keys: residual <= 2^-9 relative; bf16-representable keys give witness 0.
+* Witness: the smallest fp16 at or above the exact band norm (checked with
+  exact rational arithmetic on a sample); band membership by RoPE pairs.
+* Lemma 1 (RoPE band unitarity): the band norms of a rotated residual equal
+  those of the unrotated one.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle.encoders import e4m3_value, fp16_value
+from oracle.philox import dither
+from oracle.quant import band_norms, band_of_channel, dequantize, quantize, witness_bits
+from workloads import apply_rope
+
+
+def _rows(n, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((n, 128)) * scale).astype(np.float32)
+
+
+def test_band_membership_half_split():
+    b = band_of_channel(np.arange(128))
+    for band in range(16):
+        idx = np.where(b == band)[0]
+        assert list(idx) == [4 * band + i for i in range(4)] + [64 + 4 * band + i for i in range(4)]
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.01, 37.0])
+def test_int8_dither_error_bound_and_no_clipping(scale):
+    x = _rows(4096, 1, scale)
+    xi = dither(7, 0, 0, np.arange(4096)[:, None], np.arange(128)[None, :])
+    codes, sb, valid = quantize(x, "int8", xi)
+    assert valid.all()
+    s = fp16_value(sb)
+    # scale closed form: fp16(fp32(amax / 126.5))
+    amax = np.abs(x).max(axis=1).astype(np.float64)
+    t = (amax / 126.5).astype(np.float32).astype(np.float64)
+    assert np.array_equal(s, t.astype(np.float16).astype(np.float64))
+    xh = dequantize(codes, sb, "int8", xi)
+    err = np.abs(xh - x.astype(np.float64)) / s[:, None]
+    # fp32 rounding of x/s and of + xi can move the rounding point by ~2^-17 code units
+    assert err.max() <= 0.5 + 2**-16
+    # no clipping: the unclamped nearest integer of x/s + xi is inside [-127, 127]
+    y2 = (x.astype(np.float64) / s[:, None]).astype(np.float32).astype(np.float64) + xi
+    assert np.abs(np.rint(y2)).max() <= 127
+
+
+def test_int8_zero_row_and_stored_scale_rule():
+    x = np.zeros((2, 128), dtype=np.float32)
+    x[1, 5] = 1.0
+    xi = dither(1, 0, 0, np.arange(2)[:, None], np.arange(128)[None, :])
+    codes, sb, _ = quantize(x, "int8", xi)
+    assert sb[0] == 0 and np.all(codes[0] == 0)
+    # amax = 1: fp32(1/126.5) differs from its fp16 rounding; codes use the fp16 value
+    s16 = fp16_value(sb[1])
+    assert s16 != np.float32(1 / 126.5)
+    y = np.float32(np.float64(np.float32(1.0)) / s16)
+    assert codes[1, 5] == int(np.clip(np.rint(np.float64(np.float32(np.float64(y) + xi[1, 5]))), -127, 127))
+
+
+def test_e4m3_scaled_error_and_scale():
+    v = _rows(2048, 2, 3.0)
+    codes, sb, valid = quantize(v, "e4m3s")
+    assert valid.all()
+    s = fp16_value(sb)
+    amax = np.abs(v).max(axis=1).astype(np.float64)
+    assert np.array_equal(s, (amax / 448).astype(np.float32).astype(np.float64).astype(np.float16).astype(np.float64))
+    vh = dequantize(codes, sb, "e4m3s")
+    y = v.astype(np.float64) / s[:, None]
+    # half an E4M3 step at |y| (step 2^(e-3), e = exponent of |y|, at least 2^-9)
+    e = np.floor(np.log2(np.maximum(np.abs(y), 2.0**-6)))
+    step = 2.0 ** (e - 3)
+    assert np.all(np.abs(vh / s[:, None] - y) <= step / 2 * (1 + 1e-6) + np.maximum(np.abs(y) - 448, 0))
+
+
+def test_bf16_residual_and_identity_quantizer():
+    k = _rows(1024, 3)
+    codes, _, _ = quantize(k, "bf16")
+    kh = dequantize(codes, None, "bf16")
+    assert np.all(np.abs(kh - k) <= np.abs(k) * 2.0**-8 + 1e-45)
+    # keys that are already bfloat16 values have zero residual and zero witness
+    w = witness_bits(kh, kh.astype(np.float32))
+    assert np.all(fp16_value(w) == 0.0)
+
+
+def test_witness_is_round_up_of_exact_band_norm():
+    k = _rows(64, 4)
+    xi = dither(3, 1, 0, np.arange(64)[:, None], np.arange(128)[None, :])
+    for fmt in ("bf16", "e4m3", "int8"):
+        codes, sb, _ = quantize(k, fmt, xi if fmt == "int8" else None)
+        kh = dequantize(codes, sb, fmt, xi if fmt == "int8" else None)
+        w = witness_bits(kh, k)
+        wv = fp16_value(w)
+        for t in range(0, 64, 7):
+            r = [Fraction(float(a)) - Fraction(float(b)) for a, b in zip(kh[t], k[t].astype(np.float64))]
+            for b in range(16):
+                idx = [4 * b + i for i in range(4)] + [64 + 4 * b + i for i in range(4)]
+                n2 = sum(r[i] * r[i] for i in idx)
+                up = Fraction(float(wv[t, b]))
+                assert up * up >= n2, (fmt, t, b)
+                below = np.nextafter(np.float16(wv[t, b]), np.float16(0)).astype(np.float64)
+                if wv[t, b] > 0:
+                    assert Fraction(float(below)) ** 2 < n2, (fmt, t, b)
+
+
+def test_lemma1_band_norms_invariant_under_rope():
+    rng = np.random.default_rng(5)
+    r = rng.standard_normal((32, 128))
+    base = band_norms(r)
+    for pos in (0, 1, 517, 131071):
+        # rotate the residual in float64 (apply_rope rounds to binary32, so use its float64 math here)
+        from workloads import rope_tables
+        cos, sin = rope_tables(np.full(32, pos))
+        a, b = r[:, :64], r[:, 64:]
+        rr = np.concatenate([a * cos - b * sin, b * cos + a * sin], axis=-1)
+        assert np.allclose(band_norms(rr), base, rtol=1e-13, atol=0)
+    # and the binary32 rotation used for the inputs changes them only at binary32 precision
+    assert np.allclose(band_norms(apply_rope(r, np.full(32, 99))), base, rtol=1e-6)
+
+
+def test_nonfinite_and_overflow_rows_flagged():
+    x = _rows(3, 6)
+    x[0, 0] = np.nan
+    x[1, 0] = 3.0e7  # amax / 126.5 overflows fp16
+    xi = np.zeros((3, 128))
+    _, _, valid = quantize(x, "int8", xi)
+    assert list(valid) == [False, False, True]
+    _, _, valid = quantize(x, "e4m3s")
+    # 3e7 / 448 = 66,964 is past the fp16 round-to-nearest overflow threshold 65,520
+    assert list(valid) == [False, False, True]
