@@ -1,0 +1,232 @@
+/*
+ * kvq.h -- C ABI of libkvq: single-token decode attention over a paged,
+ * quantized KV cache, with the WitCert runtime error meter fused into the
+ * attention pass.
+ *
+ * Sources (cited by page title and section):
+ *   [W]  "WitCert: Sound Runtime Risk Observability and Gating for KV-Cache
+ *        Quantization" (arXiv 2607.28699).
+ *   [C]  "Compress the shared cartridge. Keep the keys." (knlp.io, cartridge
+ *        asymmetric quantization).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: the caller owns every buffer.  Pointers named *_dev are device
+ *   pointers; the library never allocates, frees or resizes memory.
+ * - Streams: work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *   default stream) and the call returns without synchronising.  No entry
+ *   point performs a host<->device copy or a host synchronisation, so the
+ *   sequence append -> decode -> meter can be captured in a CUDA graph.
+ * - Errors: argument errors are detected on the host and returned at once
+ *   (nothing is enqueued).  Errors that only the device can see (a block-table
+ *   entry or slot outside the cache, a non-finite input, a scale out of range,
+ *   an asynchronous copy that never completed) are written to the caller's
+ *   `err_word_dev` (a device int32 the caller zeroes) as the first kvq_status
+ *   code observed (atomic compare-and-swap from 0); the kernels never trap and
+ *   never spin without a bound.  Read it after synchronising the stream.
+ * - Shapes: head_dim is 128, page size 16 tokens, 16 witness bands, at most 8
+ *   query heads per kv head (GQA group G = num_q_heads / num_kv_heads <= 8).
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_HEAD_DIM 128
+#define KVQ_PAGE_SIZE 16
+#define KVQ_N_BANDS 16
+#define KVQ_MAX_GROUP 8
+#define KVQ_VERSION 1
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* kvq_stream_t;
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,         /* bad pointer, size, alignment or shape (host-detected)          */
+  KVQ_ERR_UNSUPPORTED_LAYOUT = 2,  /* format / GQA group combination this build does not provide     */
+  KVQ_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < kvq_decode_workspace_size(...)                       */
+  KVQ_ERR_CUDA = 4,                /* a CUDA runtime call or kernel launch failed                      */
+  KVQ_ERR_DEVICE_BOUNDS = 5,       /* device: slot / block-table entry outside [0, num_pages*16)       */
+  KVQ_ERR_NONFINITE_INPUT = 6,     /* device: non-finite key/value, or a scale that overflows fp16     */
+  KVQ_ERR_RANGE = 7,               /* device: a value scale above KVQ_MAX_VALUE_SCALE (see kvq_append) */
+  KVQ_ERR_TIMEOUT = 8              /* device: a bounded wait for an asynchronous copy gave up          */
+} kvq_status;
+
+/* Storage formats of one plane ([C] table "Keys carry the cartridge quantization loss"; [W] Sec. 4.2). */
+typedef enum kvq_fmt {
+  KVQ_FMT_BF16 = 0,        /* bfloat16, round-to-nearest-even; no scale                                  */
+  KVQ_FMT_E4M3 = 1,        /* FP8 E4M3 raw cast, round-to-nearest-even, saturating at +-448; no scale     */
+  KVQ_FMT_E4M3_SCALED = 2, /* FP8 E4M3 of x / s, s = fp16(amax / 448) per (token, kv head)               */
+  KVQ_FMT_INT8_DITHER = 3  /* subtractively dithered INT8: code = rint(x/s + xi), s = fp16(amax / 126.5) */
+} kvq_fmt;
+
+/* Element type of the key / value / query inputs. */
+typedef enum kvq_dtype { KVQ_DTYPE_F32 = 0, KVQ_DTYPE_BF16 = 1 } kvq_dtype;
+
+/* Largest per-token value scale the decode kernel accepts (the fp16 P*s*2^8 operand stays finite). */
+#define KVQ_MAX_VALUE_SCALE 255.875f
+
+/*
+ * One layer's paged cache: planes of tiles, one tile per (page, kv head).
+ * Tile index of (page p, kv head h) is p * num_kv_heads + h; a tile holds the
+ * 16 tokens (slots p*16 .. p*16+15) of that page.  All planes are device
+ * memory, 16-byte aligned, owned by the caller.
+ *
+ * Tile layouts (byte offset of token t in 0..15, channel c in 0..127, band b
+ * in 0..15; they place each lane's tensor-core fragment in contiguous 16-byte
+ * words so one bulk copy of a tile feeds the decode kernel with conflict-free
+ * shared-memory loads):
+ *   K, 16-bit (4096 B):  16 * ((((t>>3)*4 + (c>>5)) * 32) + (t&7)*4 + ((c>>3)&3)) + 2*(c&7)
+ *   K,  8-bit (2048 B):  16 * ((((t>>3)*2 + (c>>6)) * 32) + (t&7)*4 + ((c>>4)&3)) + (c&15)
+ *   V, 16-bit (4096 B):  16 * (((c>>4) * 32) + 4*(c&7) + ((t&7)>>1)) + 8*((c>>3)&1) + 2*i(t)
+ *   V,  8-bit (2048 B):  16 * (((c>>5) * 32) + 4*(c&7) + ((t&7)>>1)) + 4*((c>>3)&3) +   i(t)
+ *   witness (512 B, fp16 bits):  16 * (4*(t&7) + (b>>2)) + 8*(t>>3) + 2*(b&3)
+ *   scale   (32 B,  fp16 bits):   2 * (4*((t&7)>>1) + i(t))
+ * with i(t) = (t&1) + 2*(t>>3).  Band b holds the RoPE frequency pairs
+ * 4b..4b+3 of the half-split pairing (pair j = channels j and j+64), i.e.
+ * channels 4b..4b+3 and 64+4b..64+4b+3 ([W] Sec. 4.1, eq. (2)).
+ */
+typedef struct kvq_cache {
+  int32_t k_fmt;          /* kvq_fmt of the key plane                                  */
+  int32_t v_fmt;          /* kvq_fmt of the value plane                                */
+  int32_t num_kv_heads;   /* kv heads per layer                                        */
+  int32_t num_pages;      /* pages in every plane                                      */
+  int32_t layer;          /* layer index: a word of the dither counter                 */
+  int32_t reserved;       /* must be 0                                                 */
+  uint64_t dither_seed;   /* Philox key of the INT8 dither stream                      */
+  void* k_data;           /* K tiles                                                   */
+  void* v_data;           /* V tiles                                                   */
+  uint16_t* k_scale;      /* K scale tiles (fp16 bits); non-NULL iff the K format has a scale */
+  uint16_t* v_scale;      /* V scale tiles (fp16 bits); non-NULL iff the V format has a scale */
+  uint16_t* witness;      /* witness tiles (fp16 bits); required by kvq_append, and by
+                             kvq_decode_attn when the meter is on                      */
+} kvq_cache;
+
+/* Meter configuration ([W] Sec. 4.2 request-level budget, Sec. 4.3 saturation). */
+typedef struct kvq_meter_params {
+  uint32_t tiers;     /* bit 0: Tier A witness bound; bit 1: Tier B dither certificate (INT8 keys only) */
+  int32_t n_layers;   /* L in delta_loc = delta_req / (L * H * T)                                      */
+  int32_t n_q_heads;  /* H (query heads)                                                               */
+  int32_t n_steps;    /* T (decode steps the request budget covers; 256 in [W])                         */
+  double delta_req;   /* request-level failure budget of Tier B                                        */
+  float tau;          /* gate threshold for the coverage counts of kvq_meter                           */
+  int32_t reserved;   /* must be 0                                                                     */
+} kvq_meter_params;
+
+#define KVQ_TIER_A 1u
+#define KVQ_TIER_B 2u
+
+/* Bytes of one tile of a plane: plane 0 = K, 1 = V, 2 = K scale, 3 = V scale, 4 = witness.
+   Returns 0 for a plane the format does not store. */
+size_t kvq_tile_bytes(int32_t fmt, int32_t plane);
+
+/*
+ * kvq_append -- quantize-on-append ([W] Sec. 4.2 "Subtractive dither",
+ * Sec. 6.2.1 and 6.2.3; [C] "One kernel spans cartridge and live KV" for the
+ * K16/V8 layout).
+ *
+ * k_dev, v_dev: [num_tokens][num_kv_heads][128] post-RoPE keys and values,
+ *   element type in_dtype (KVQ_DTYPE_F32 or KVQ_DTYPE_BF16).
+ * slot_mapping_dev: [num_tokens] int32 physical slot (page * 16 + offset) of
+ *   each token; a negative slot skips the token.
+ * For each (token, kv head) the kernel writes the K and V codes, the fp16
+ * scales of scaled formats, and the 16 fp16 witness values: the band norms of
+ * the key residual k_hat - k, rounded up ([W] Sec. 4.1, eq. (2)).  Scales:
+ *   E4M3_SCALED: s = fp16_rn(fp32(amax / 448)),  code = e4m3_rn_satfinite(fp32(x / s))
+ *   INT8_DITHER: s = fp16_rn(fp32(amax / 126.5)), code = clamp(rint(fp32(fp32(x / s) + xi)), -127, 127)
+ * (amax = 0 stores scale 0 and zero codes).  The dither xi comes from
+ * Philox4x32-10 with key (seed low 32 bits, seed high 32 bits), counter
+ * (slot, layer, kv_head, c >> 2), output word c & 3, xi = ((w >> 8) + 1/2) *
+ * 2^-24 - 1/2; the K and V planes of a token share it ([W] Sec. 6.2.1, 6.2.3).
+ * Device errors: KVQ_ERR_DEVICE_BOUNDS (slot beyond the cache; the token is
+ * skipped), KVQ_ERR_NONFINITE_INPUT (non-finite input or fp16 scale overflow;
+ * the token is written), KVQ_ERR_RANGE (a value scale above
+ * KVQ_MAX_VALUE_SCALE; the token is written but decode would lose it).
+ */
+kvq_status kvq_append(const kvq_cache* cache, const void* k_dev, const void* v_dev, int32_t in_dtype,
+                      const int32_t* slot_mapping_dev, int32_t num_tokens, int32_t* err_word_dev,
+                      kvq_stream_t stream);
+
+/* Workspace bytes kvq_decode_attn needs for (batch, num_kv_heads, num_q_heads) on the current device. */
+size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads);
+
+/*
+ * kvq_decode_attn -- one decode step of one layer: split-KV paged GQA
+ * attention over [shared prefix ++ live suffix] with one online-softmax state
+ * per sequence and query head, the meter accumulated in the same pass, and a
+ * log-sum-exp merge of the splits ([W] Sec. 6.2.2 "the certificate shares the
+ * split-KV reduction with the output"; [C] "One kernel spans cartridge and
+ * live KV").
+ *
+ * cache: the layer's live paged cache.  prefix (nullable): a shared dense
+ *   prefix of prefix_len tokens stored in pages 0, 1, ... of its own cache
+ *   (same num_kv_heads); every sequence attends to it before its suffix.
+ * q_dev: [batch][num_q_heads][128] post-RoPE queries (q_dtype F32 or BF16);
+ *   query head h reads kv head h / (num_q_heads / num_kv_heads).
+ * block_table_dev: [batch][max_pages_per_seq] int32 physical pages of each
+ *   sequence's live suffix; seq_lens_dev: [batch] int32 live token counts.
+ * sm_scale: softmax scale (1/sqrt(128) for standard attention).
+ * meter (nullable => meter off): tiers to accumulate.  With the meter off the
+ *   witness is not read and `out` is bit-identical to the meter-on output.
+ * out_dev: [batch][num_q_heads][128] fp32 attention output sum_t p~_t v_hat_t.
+ * meter_state_dev (nullable iff meter off): [batch][num_q_heads][4] fp32:
+ *   [0] ln(A - 1) of Tier A, A = sum_t p~_t e^{c_t}, c_t = sm_scale *
+ *       sum_b ||q_b|| w_{t,b} ([W] Thm. 1, Thm. 2); -inf when A = 1;
+ *   [1] ln(A_B - 1) of Tier B, u_t = sm_scale ||q|| s_t sqrt(2 ln(2S/delta_loc)/12)
+ *       ([W] Sec. 4.2), NaN when Tier B is off;
+ *   [2] log-sum-exp of the compressed logits (natural log); [3] tokens attended S.
+ * workspace_dev / ws_bytes: scratch of at least kvq_decode_workspace_size().
+ * An empty sequence (no prefix, seq_len 0) yields out = 0 and ln(A-1) = -inf.
+ */
+kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int32_t prefix_len,
+                           const void* q_dev, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
+                           const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                           const int32_t* seq_lens_dev, float sm_scale, const kvq_meter_params* meter,
+                           float* out_dev, float* meter_state_dev, void* workspace_dev, size_t ws_bytes,
+                           int32_t* err_word_dev, kvq_stream_t stream);
+
+/*
+ * kvq_meter -- meter finalisation and telemetry on the device ([W] Sec. 4.3;
+ * Sec. 6.2.4 "Certificate telemetry in production": aggregate on the GPU,
+ * count non-finite values separately).
+ *
+ * meter_state_dev: [n_layers][batch][num_q_heads][4] as written by kvq_decode_attn.
+ * meter_a_dev:  [n_layers][batch][num_q_heads] min(1, 1/2 (A^2 - 1)) of Tier A.
+ * raw_a_dev:    same shape, the raw log score ln(1/2 (A^2 - 1)) (finite for finite inputs).
+ * cert_b_dev (nullable): same shape, min(1, 1/2 (A_B^2 - 1)).
+ * counts_dev:   int32[4]: cells with meter_a < tau, cells with cert_b < tau,
+ *               non-finite cells, total cells (zeroed and filled by the call).
+ * ranking_dev (nullable): [batch][n_layers * num_q_heads] int32 flat cell
+ *   indices (layer * num_q_heads + head) of each request, highest raw score
+ *   first, ties to the lower index (requires n_layers * num_q_heads <= 8192).
+ */
+kvq_status kvq_meter(const float* meter_state_dev, int32_t n_layers, int32_t batch, int32_t num_q_heads,
+                     const kvq_meter_params* meter, float* meter_a_dev, float* raw_a_dev, float* cert_b_dev,
+                     int32_t* counts_dev, int32_t* ranking_dev, kvq_stream_t stream);
+
+/* Test hook: the dither xi of (seed, layer, kv_head, slots[i], channel c) into xi_dev[i * 128 + c]. */
+kvq_status kvq_debug_dither(uint64_t seed, int32_t layer, int32_t kv_head, const int32_t* slots_dev, int32_t n,
+                            float* xi_dev, kvq_stream_t stream);
+
+/* Test hook: the device conversions kvq_append uses, applied to n fp32 values.
+   kind 0: bf16 RNE (uint16 out); 1: e4m3 RNE satfinite (uint8 out); 2: fp16 RNE
+   (uint16 out); 3: fp16 round-up (uint16 out). */
+kvq_status kvq_debug_encode(int32_t kind, const float* x_dev, int64_t n, void* out_dev, kvq_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* kvq_status_string(int32_t status);
+
+/* KVQ_VERSION of the loaded library. */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

@@ -1,0 +1,245 @@
+"""Python binding of libkvq (argument marshalling only).
+
+Every step of the decode path runs in the CUDA library: this module allocates
+device memory with torch, packs the C structs of ``include/kvq.h`` and calls
+the C ABI with the current torch stream.  There is no CPU fallback: importing
+works without a GPU (so the library can be inspected), but every compute call
+needs the built ``libkvq.so`` and a CUDA device, and raises otherwise.
+
+Entry points mirror the C names: ``append``, ``decode_attn``, ``meter``,
+``decode_workspace_size``, ``debug_dither``, ``debug_encode``, plus the
+``PagedCache`` helper that owns one layer's planes.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from ctypes import POINTER, c_double, c_float, c_int32, c_int64, c_size_t, c_uint32, c_uint64, c_void_p
+
+import torch
+
+__all__ = [
+    "FMT",
+    "KvqError",
+    "lib",
+    "load",
+    "PagedCache",
+    "MeterParams",
+    "append",
+    "decode_attn",
+    "decode_workspace_size",
+    "meter",
+    "debug_dither",
+    "debug_encode",
+    "tile_bytes",
+    "status_string",
+    "read_err",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+FMT = {"bf16": 0, "e4m3": 1, "e4m3s": 2, "int8": 3}
+DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+TIER_A, TIER_B = 1, 2
+HEAD_DIM, PAGE, N_BANDS = 128, 16, 16
+
+STATUS = {
+    0: "KVQ_OK",
+    1: "KVQ_ERR_INVALID_ARG",
+    2: "KVQ_ERR_UNSUPPORTED_LAYOUT",
+    3: "KVQ_ERR_WORKSPACE_TOO_SMALL",
+    4: "KVQ_ERR_CUDA",
+    5: "KVQ_ERR_DEVICE_BOUNDS",
+    6: "KVQ_ERR_NONFINITE_INPUT",
+    7: "KVQ_ERR_RANGE",
+    8: "KVQ_ERR_TIMEOUT",
+}
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [
+        ("k_fmt", c_int32),
+        ("v_fmt", c_int32),
+        ("num_kv_heads", c_int32),
+        ("num_pages", c_int32),
+        ("layer", c_int32),
+        ("reserved", c_int32),
+        ("dither_seed", c_uint64),
+        ("k_data", c_void_p),
+        ("v_data", c_void_p),
+        ("k_scale", c_void_p),
+        ("v_scale", c_void_p),
+        ("witness", c_void_p),
+    ]
+
+
+class MeterParams(ctypes.Structure):
+    _fields_ = [
+        ("tiers", c_uint32),
+        ("n_layers", c_int32),
+        ("n_q_heads", c_int32),
+        ("n_steps", c_int32),
+        ("delta_req", c_double),
+        ("tau", c_float),
+        ("reserved", c_int32),
+    ]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libkvq.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libkvq.so not built ({path}); run __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    L.kvq_tile_bytes.restype = c_size_t
+    L.kvq_tile_bytes.argtypes = [c_int32, c_int32]
+    L.kvq_append.restype = c_int32
+    L.kvq_append.argtypes = [POINTER(_Cache), c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_void_p]
+    L.kvq_decode_workspace_size.restype = c_size_t
+    L.kvq_decode_workspace_size.argtypes = [c_int32, c_int32, c_int32]
+    L.kvq_decode_attn.restype = c_int32
+    L.kvq_decode_attn.argtypes = [
+        POINTER(_Cache), POINTER(_Cache), c_int32, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32,
+        c_void_p, c_float, POINTER(MeterParams), c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p,
+    ]
+    L.kvq_meter.restype = c_int32
+    L.kvq_meter.argtypes = [c_void_p, c_int32, c_int32, c_int32, POINTER(MeterParams), c_void_p, c_void_p,
+                            c_void_p, c_void_p, c_void_p, c_void_p]
+    L.kvq_debug_dither.restype = c_int32
+    L.kvq_debug_dither.argtypes = [c_uint64, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p]
+    L.kvq_debug_encode.restype = c_int32
+    L.kvq_debug_encode.argtypes = [c_int32, c_void_p, c_int64, c_void_p, c_void_p]
+    L.kvq_status_string.restype = ctypes.c_char_p
+    L.kvq_status_string.argtypes = [c_int32]
+    L.kvq_version.restype = c_int32
+    L.kvq_version.argtypes = []
+    _lib = L
+    return L
+
+
+def lib():
+    return load()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise KvqError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def tile_bytes(fmt: str, plane: int) -> int:
+    return int(lib().kvq_tile_bytes(FMT[fmt], plane))
+
+
+def status_string(status: int) -> str:
+    return lib().kvq_status_string(status).decode()
+
+
+class PagedCache:
+    """One layer's paged planes (device memory owned by torch tensors)."""
+
+    def __init__(self, k_fmt: str, v_fmt: str, num_kv_heads: int, num_pages: int, layer: int = 0,
+                 seed: int = 0, device="cuda", witness: bool = True):
+        self.k_fmt, self.v_fmt = k_fmt, v_fmt
+        self.num_kv_heads, self.num_pages, self.layer, self.seed = num_kv_heads, num_pages, layer, seed
+        n = num_pages * num_kv_heads
+        kb = 4096 if k_fmt == "bf16" else 2048
+        vb = 4096 if v_fmt == "bf16" else 2048
+        z = dict(dtype=torch.uint8, device=device)
+        self.k = torch.zeros((n, kb), **z)
+        self.v = torch.zeros((n, vb), **z)
+        self.k_scale = torch.zeros((n, 32), **z) if k_fmt in ("e4m3s", "int8") else None
+        self.v_scale = torch.zeros((n, 32), **z) if v_fmt in ("e4m3s", "int8") else None
+        self.witness = torch.zeros((n, 512), **z) if witness else None
+
+    def desc(self) -> _Cache:
+        return _Cache(FMT[self.k_fmt], FMT[self.v_fmt], self.num_kv_heads, self.num_pages, self.layer, 0,
+                      self.seed & 0xFFFFFFFFFFFFFFFF, _ptr(self.k), _ptr(self.v), _ptr(self.k_scale),
+                      _ptr(self.v_scale), _ptr(self.witness))
+
+    def nbytes(self) -> int:
+        return sum(t.numel() for t in (self.k, self.v, self.k_scale, self.v_scale, self.witness) if t is not None)
+
+
+def read_err(err: torch.Tensor) -> int:
+    return int(err.item())
+
+
+def append(cache: PagedCache, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+           err: torch.Tensor | None = None, stream=None):
+    """kvq_append: quantize k, v [n, Hkv, 128] (fp32 or bf16) into the slots of ``cache``."""
+    assert k.is_contiguous() and v.is_contiguous() and k.dtype == v.dtype and k.shape == v.shape
+    assert slot_mapping.dtype == torch.int32 and slot_mapping.is_contiguous()
+    d = cache.desc()
+    _check(lib().kvq_append(ctypes.byref(d), k.data_ptr(), v.data_ptr(), DTYPE[k.dtype], slot_mapping.data_ptr(),
+                            int(k.shape[0]), _ptr(err), _stream(stream)), "kvq_append")
+
+
+def decode_workspace_size(batch: int, num_kv_heads: int, num_q_heads: int) -> int:
+    return int(lib().kvq_decode_workspace_size(batch, num_kv_heads, num_q_heads))
+
+
+def meter_params(tiers: int = TIER_A, n_layers: int = 1, n_q_heads: int = 1, n_steps: int = 256,
+                 delta_req: float = 1e-2, tau: float = 0.2) -> MeterParams:
+    return MeterParams(tiers, n_layers, n_q_heads, n_steps, delta_req, tau, 0)
+
+
+def decode_attn(cache: PagedCache, q: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                out: torch.Tensor, workspace: torch.Tensor, *, prefix: PagedCache | None = None,
+                prefix_len: int = 0, sm_scale: float | None = None, meter: MeterParams | None = None,
+                meter_state: torch.Tensor | None = None, err: torch.Tensor | None = None, stream=None):
+    """kvq_decode_attn for one layer: q [B, Hq, 128] -> out [B, Hq, 128] (+ meter_state [B, Hq, 4])."""
+    B, Hq, D = q.shape
+    assert D == HEAD_DIM and q.is_contiguous() and out.is_contiguous()
+    assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    d = cache.desc()
+    pd = prefix.desc() if prefix is not None else None
+    _check(lib().kvq_decode_attn(
+        ctypes.byref(d), ctypes.byref(pd) if pd is not None else None, int(prefix_len), q.data_ptr(), DTYPE[q.dtype],
+        B, Hq, block_table.data_ptr(), int(block_table.shape[1]) if block_table.dim() == 2 else 0,
+        seq_lens.data_ptr(), float(sm_scale), ctypes.byref(meter) if meter is not None else None,
+        out.data_ptr(), _ptr(meter_state), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _ptr(err), _stream(stream)), "kvq_decode_attn")
+
+
+def meter(meter_state: torch.Tensor, n_layers: int, batch: int, num_q_heads: int, params: MeterParams,
+          meter_a: torch.Tensor, raw_a: torch.Tensor, counts: torch.Tensor, cert_b: torch.Tensor | None = None,
+          ranking: torch.Tensor | None = None, stream=None):
+    """kvq_meter over meter_state [L, B, Hq, 4]."""
+    _check(lib().kvq_meter(meter_state.data_ptr(), n_layers, batch, num_q_heads, ctypes.byref(params),
+                           meter_a.data_ptr(), raw_a.data_ptr(), _ptr(cert_b), counts.data_ptr(), _ptr(ranking),
+                           _stream(stream)), "kvq_meter")
+
+
+def debug_dither(seed: int, layer: int, kv_head: int, slots: torch.Tensor, out: torch.Tensor, stream=None):
+    _check(lib().kvq_debug_dither(seed & 0xFFFFFFFFFFFFFFFF, layer, kv_head, slots.data_ptr(), int(slots.numel()),
+                                  out.data_ptr(), _stream(stream)), "kvq_debug_dither")
+
+
+def debug_encode(kind: int, x: torch.Tensor, out: torch.Tensor, stream=None):
+    _check(lib().kvq_debug_encode(kind, x.data_ptr(), int(x.numel()), out.data_ptr(), _stream(stream)),
+           "kvq_debug_encode")

@@ -1,0 +1,268 @@
+// decode.cu -- kvq_decode_attn / kvq_decode_workspace_size: argument checks, workspace layout,
+// shared-memory stage sizing, and dispatch to the decode and merge kernels.
+#include <cmath>
+
+#include "decode_kernel.cuh"
+
+#define KVQ_X(KF, VF, PKF, PVF) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, false) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, true)
+#include "decode_instances.inc"
+#undef KVQ_X
+
+namespace kvq {
+namespace dec {
+
+// ------------------------------------------------------------------------------------------------
+// Merge of the (warp, unit) pieces: one warp per (sequence, query head).
+__global__ void __launch_bounds__(128) merge_kernel(const Args a, int meter_on, float* __restrict__ out,
+                                                    float* __restrict__ meter_state) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= static_cast<long long>(a.B) * a.Hq) return;
+  const int seq = static_cast<int>(gw / a.Hq), qh = static_cast<int>(gw % a.Hq);
+  const int kvh = qh / a.G, row = qh % a.G;
+  const int32_t* cum = a.ws_cum;
+  const long long T = static_cast<long long>(a.Hkv) * cum[a.B];
+  const int P = cum[seq + 1] - cum[seq];
+  const int unit = seq * a.Hkv + kvh;
+  float* o = out + static_cast<size_t>(gw) * kHeadDim;
+  const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
+  if (P == 0 || T == 0) {
+    *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (meter_state && lane == 0)
+      *reinterpret_cast<float4*>(meter_state + gw * 4) =
+          make_float4(-INFINITY, a.tier_b ? -INFINITY : NAN, -INFINITY, static_cast<float>(total));
+    return;
+  }
+  const long long W = min(static_cast<long long>(a.w_max), T);
+  const long long b_u = static_cast<long long>(a.Hkv) * cum[seq] + static_cast<long long>(kvh) * P;
+  const long long e_u = b_u + P;
+  auto warp_of = [&](long long x) { return ((x + 1) * W - 1) / T; };
+  const long long w_lo = warp_of(b_u), w_hi = warp_of(e_u - 1);
+  float M = -INFINITY, Mc = -INFINITY, Mu = -INFINITY;
+  for (long long w = w_lo; w <= w_hi; ++w) {
+    const float* st = a.ws_stats + ((static_cast<size_t>(w) + unit) * a.G + row) * 8;
+    M = fmaxf(M, st[0]);
+    Mc = fmaxf(Mc, st[2]);
+    Mu = fmaxf(Mu, st[4]);
+  }
+  float Ls = 0.f, Sc = 0.f, Su = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long w = w_lo; w <= w_hi; ++w) {
+    const size_t slot = static_cast<size_t>(w) + unit;
+    const float* st = a.ws_stats + (slot * a.G + row) * 8;
+    const float wt = (st[0] == -INFINITY) ? 0.f : exp2f(st[0] - M);
+    Ls += st[1] * wt;
+    if (st[2] != -INFINITY) Sc += st[3] * exp2f(st[2] - Mc);
+    if (st[4] != -INFINITY) Su += st[5] * exp2f(st[4] - Mu);
+    const float4 v = *reinterpret_cast<const float4*>(a.ws_acc + (slot * a.G + row) * kHeadDim + 4 * lane);
+    acc.x += v.x * wt; acc.y += v.y * wt; acc.z += v.z * wt; acc.w += v.w * wt;
+  }
+  const float inv = kPvShiftInv / Ls;
+  *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (meter_state && lane == 0) {
+    const float lse2 = M + log2f(Ls);
+    const float la = (meter_on && Sc > 0.f) ? (Mc + log2f(Sc) - lse2) * kLn2 : -INFINITY;
+    const float lb = a.tier_b ? ((Su > 0.f) ? (Mu + log2f(Su) - lse2) * kLn2 : -INFINITY) : NAN;
+    *reinterpret_cast<float4*>(meter_state + gw * 4) = make_float4(la, lb, lse2 * kLn2, static_cast<float>(total));
+  }
+}
+
+}  // namespace dec
+}  // namespace kvq
+
+using namespace kvq;
+using namespace kvq::dec;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int device_sm_count() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int device_smem_optin() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t cum, stats, acc, total;
+};
+
+WsLayout ws_layout(int batch, int hkv, int hq, int w_max) {
+  const int G = hq / hkv;
+  const size_t slots = static_cast<size_t>(w_max) + static_cast<size_t>(batch) * hkv;
+  WsLayout l;
+  l.cum = 0;
+  l.stats = align256(static_cast<size_t>(batch + 1) * 4);
+  l.acc = l.stats + align256(slots * G * 8 * sizeof(float));
+  l.total = l.acc + align256(slots * G * kHeadDim * sizeof(float));
+  return l;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int page_bytes(int kf, int vf, bool meter) {
+  return tile_bytes_k(kf) + tile_bytes_v(vf) + (meter ? kTileBytesW : 0) + (fmt_has_scale(kf) ? kTileBytesS : 0) +
+         (fmt_has_scale(vf) ? kTileBytesS : 0);
+}
+
+kvq_status check_cache(const kvq_cache* c, bool meter) {
+  if (!c) return KVQ_ERR_INVALID_ARG;
+  if (c->k_fmt < 0 || c->k_fmt > 3 || c->v_fmt < 0 || c->v_fmt > 3) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  if (c->num_kv_heads <= 0 || c->num_pages < 0 || c->reserved != 0) return KVQ_ERR_INVALID_ARG;
+  if (!c->k_data || !c->v_data || !aligned16(c->k_data) || !aligned16(c->v_data)) return KVQ_ERR_INVALID_ARG;
+  if (fmt_has_scale(c->k_fmt) && (!c->k_scale || !aligned16(c->k_scale))) return KVQ_ERR_INVALID_ARG;
+  if (fmt_has_scale(c->v_fmt) && (!c->v_scale || !aligned16(c->v_scale))) return KVQ_ERR_INVALID_ARG;
+  if (meter && (!c->witness || !aligned16(c->witness))) return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+Planes planes_of(const kvq_cache* c) {
+  Planes p{};
+  if (!c) return p;
+  p.k = static_cast<const uint8_t*>(c->k_data);
+  p.v = static_cast<const uint8_t*>(c->v_data);
+  p.ks = reinterpret_cast<const uint8_t*>(c->k_scale);
+  p.vs = reinterpret_cast<const uint8_t*>(c->v_scale);
+  p.w = reinterpret_cast<const uint8_t*>(c->witness);
+  p.num_pages = c->num_pages;
+  p.layer = static_cast<uint32_t>(c->layer);
+  p.seed_lo = static_cast<uint32_t>(c->dither_seed);
+  p.seed_hi = static_cast<uint32_t>(c->dither_seed >> 32);
+  return p;
+}
+
+using Launcher = cudaError_t (*)(const Args&, int, size_t, cudaStream_t);
+
+Launcher pick(int kf, int vf, int pkf, int pvf, bool meter) {
+#define KVQ_X(KF, VF, PKF, PVF)                                   \
+  if (kf == (KF) && vf == (VF) && pkf == (PKF) && pvf == (PVF))   \
+    return meter ? &launch_decode<KF, VF, PKF, PVF, true> : &launch_decode<KF, VF, PKF, PVF, false>;
+#include "decode_instances.inc"
+#undef KVQ_X
+  return nullptr;
+}
+
+}  // namespace
+
+extern "C" size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads) {
+  if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  return ws_layout(batch, num_kv_heads, num_q_heads, sms * kWarps).total;
+}
+
+extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int32_t prefix_len,
+                                      const void* q, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
+                                      const int32_t* block_table, int32_t max_pages_per_seq,
+                                      const int32_t* seq_lens, float sm_scale, const kvq_meter_params* mp,
+                                      float* out, float* meter_state, void* workspace, size_t ws_bytes,
+                                      int32_t* err_word, kvq_stream_t stream) {
+  const bool meter = mp != nullptr;
+  kvq_status st = check_cache(cache, meter);
+  if (st != KVQ_OK) return st;
+  if (prefix && prefix_len > 0) {
+    if ((st = check_cache(prefix, meter)) != KVQ_OK) return st;
+    if (prefix->num_kv_heads != cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
+    if (static_cast<long long>(prefix->num_pages) * kPage < prefix_len) return KVQ_ERR_INVALID_ARG;
+    if (fmt_is_16bit(prefix->k_fmt) != fmt_is_16bit(cache->k_fmt)) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  }
+  if (prefix_len < 0 || (prefix_len > 0 && !prefix)) return KVQ_ERR_INVALID_ARG;
+  const int hkv = cache->num_kv_heads;
+  if (batch < 0 || batch > kMaxBatch || num_q_heads <= 0 || num_q_heads % hkv) return KVQ_ERR_INVALID_ARG;
+  const int G = num_q_heads / hkv;
+  if (G > kMaxGroup) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  if (q_dtype != KVQ_DTYPE_F32 && q_dtype != KVQ_DTYPE_BF16) return KVQ_ERR_INVALID_ARG;
+  if (max_pages_per_seq < 0 || !std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
+  if (meter) {
+    if (!(mp->tiers & KVQ_TIER_A) || (mp->tiers & ~3u) || mp->reserved != 0) return KVQ_ERR_INVALID_ARG;
+    if (mp->tiers & KVQ_TIER_B) {
+      if (cache->k_fmt != KVQ_FMT_INT8_DITHER || (prefix && prefix_len > 0)) return KVQ_ERR_INVALID_ARG;
+      if (!(mp->delta_req > 0.0 && mp->delta_req < 1.0) || mp->n_layers <= 0 || mp->n_q_heads <= 0 || mp->n_steps <= 0)
+        return KVQ_ERR_INVALID_ARG;
+    }
+    if (!meter_state) return KVQ_ERR_INVALID_ARG;
+  }
+  if (batch == 0) return KVQ_OK;
+  if (!q || !seq_lens || !out || !workspace || (max_pages_per_seq > 0 && !block_table)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(workspace) || (meter_state && !aligned16(meter_state))) return KVQ_ERR_INVALID_ARG;
+  const int sms = device_sm_count();
+  const int smem_max = device_smem_optin();
+  if (sms <= 0 || smem_max <= 0) return KVQ_ERR_CUDA;
+  const int w_max = sms * kWarps;
+  const WsLayout wl = ws_layout(batch, hkv, num_q_heads, w_max);
+  if (ws_bytes < wl.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+
+  const bool has_prefix = prefix && prefix_len > 0;
+  const int pkf = has_prefix ? prefix->k_fmt : kNoPrefix;
+  const int pvf = has_prefix ? prefix->v_fmt : kNoPrefix;
+  Launcher launch = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter);
+  if (!launch) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+
+  Args a{};
+  a.live = planes_of(cache);
+  a.pre = planes_of(has_prefix ? prefix : nullptr);
+  a.prefix_len = has_prefix ? prefix_len : 0;
+  a.prefix_pages = (a.prefix_len + kPage - 1) / kPage;
+  a.Hkv = hkv;
+  a.G = G;
+  a.Hq = num_q_heads;
+  a.B = batch;
+  a.q = q;
+  a.q_bf16 = q_dtype == KVQ_DTYPE_BF16;
+  a.bt = block_table;
+  a.max_pages = max_pages_per_seq;
+  a.seq_lens = seq_lens;
+  a.sm_scale = sm_scale;
+  a.tier_b = meter && (mp->tiers & KVQ_TIER_B) ? 1 : 0;
+  a.ln_delta_loc = 0.f;
+  if (a.tier_b)
+    a.ln_delta_loc = static_cast<float>(
+        std::log(mp->delta_req / (static_cast<double>(mp->n_layers) * mp->n_q_heads * mp->n_steps)));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.ws_cum = reinterpret_cast<int32_t*>(ws + wl.cum);
+  a.ws_stats = reinterpret_cast<float*>(ws + wl.stats);
+  a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
+  a.w_max = w_max;
+  a.err = err_word;
+
+  // stage size: the larger of the two segments' page footprints (16-byte multiple by construction)
+  int sb = page_bytes(cache->k_fmt, cache->v_fmt, meter);
+  if (has_prefix) sb = std::max(sb, page_bytes(prefix->k_fmt, prefix->v_fmt, meter));
+  const bool xi = cache->k_fmt == KVQ_FMT_INT8_DITHER && cache->v_fmt == KVQ_FMT_INT8_DITHER;
+  const int cum_bytes = ((batch + 1) * 4 + 127) & ~127;
+  const int fixed = cum_bytes + kWarps * ((xi ? kXiScratch : 0) + kMaxStages * 8);
+  const int budget = smem_max - 1024 - fixed;
+  int stages = budget / (kWarps * sb);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  a.stages = stages;
+  a.stage_bytes = sb;
+  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(kWarps) * stages * sb;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch(a, sms, smem, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  const long long merge_threads = static_cast<long long>(batch) * num_q_heads * 32;
+  merge_kernel<<<static_cast<unsigned>((merge_threads + 127) / 128), 128, 0, s>>>(a, meter ? 1 : 0, out, meter_state);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  return KVQ_OK;
+}

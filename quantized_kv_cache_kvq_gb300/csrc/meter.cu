@@ -1,0 +1,131 @@
+// meter.cu -- meter finalisation and device telemetry (kvq_meter), status strings.
+//
+// WitCert (arXiv 2607.28699) Sec. 4.3: the sound meter is min(1, 1/2 (A^2 - 1)); above saturation
+// the raw value is a risk score (certified gating at tau < 1, risk-ranked gating at tau >= 1).
+// Sec. 6.2.4 ("Certificate telemetry in production"): reduce certificates on the GPU without a host
+// synchronisation per layer, and count non-finite values separately from the finite statistics.
+#include "kvq_common.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr int kMaxRankCells = 8192;
+
+// meter = min(1, 1/2 (A-1)(A+1)) and raw = ln(1/2 (A^2 - 1)) from la = ln(A - 1)
+__device__ __forceinline__ void finalize_one(float la, float& meter, float& raw) {
+  if (isnan(la)) { meter = NAN; raw = NAN; return; }
+  if (la == -INFINITY) { meter = 0.f; raw = -INFINITY; return; }
+  // ln(A + 1) = ln(2 + e^la)
+  const float lap1 = la < 0.f ? kLn2 + log1pf(0.5f * expf(la)) : la + log1pf(2.f * expf(-la));
+  raw = la + lap1 - kLn2;
+  if (la > 1.f) { meter = 1.f; return; }
+  const float am1 = expf(la);
+  meter = fminf(1.f, 0.5f * am1 * (am1 + 2.f));
+}
+
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ state, long long n, float tau,
+                                                       float* __restrict__ meter_a, float* __restrict__ raw_a,
+                                                       float* __restrict__ cert_b, int32_t* __restrict__ counts) {
+  int cov_a = 0, cov_b = 0, nonfinite = 0, cells = 0;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 s = reinterpret_cast<const float4*>(state)[i];
+    float m, r;
+    finalize_one(s.x, m, r);
+    meter_a[i] = m;
+    raw_a[i] = r;
+    cells += 1;
+    if (isnan(s.x) || s.x == INFINITY) nonfinite += 1;
+    else if (m < tau) cov_a += 1;
+    if (cert_b) {
+      float mb, rb;
+      finalize_one(s.y, mb, rb);
+      cert_b[i] = mb;
+      if (!isnan(mb) && mb < tau) cov_b += 1;
+    }
+  }
+  // block reduction, then one atomic per counter per block
+  __shared__ int red[4][8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int v[4] = {cov_a, cov_b, nonfinite, cells};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+    if (lane == 0) red[k][warp] = v[k];
+  }
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    int t = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[threadIdx.x][w];
+    if (t) atomicAdd(&counts[threadIdx.x], t);
+  }
+}
+
+// Rank the L*H cells of one request by raw score (highest first, ties to the lower flat index).
+__global__ void __launch_bounds__(512) rank_kernel(const float* __restrict__ raw_a, int n_layers, int batch, int hq,
+                                                   int32_t* __restrict__ ranking) {
+  __shared__ float key[kMaxRankCells];
+  const int b = blockIdx.x;
+  const int n = n_layers * hq;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int l = i / hq, h = i % hq;
+    const float r = raw_a[(static_cast<size_t>(l) * batch + b) * hq + h];
+    key[i] = isnan(r) ? INFINITY : r;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float ki = key[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) {
+      const float kj = key[j];
+      rank += (kj > ki) || (kj == ki && j < i);
+    }
+    ranking[static_cast<size_t>(b) * n + rank] = i;
+  }
+}
+
+}  // namespace
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" kvq_status kvq_meter(const float* state, int32_t n_layers, int32_t batch, int32_t hq,
+                                const kvq_meter_params* mp, float* meter_a, float* raw_a, float* cert_b,
+                                int32_t* counts, int32_t* ranking, kvq_stream_t stream) {
+  if (!mp || n_layers < 0 || batch < 0 || hq <= 0) return KVQ_ERR_INVALID_ARG;
+  if (!state || !meter_a || !raw_a || !counts) return KVQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(state) & 15u) != 0) return KVQ_ERR_INVALID_ARG;
+  if (ranking && static_cast<long long>(n_layers) * hq > kMaxRankCells) return KVQ_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(counts, 0, 4 * sizeof(int32_t), s) != cudaSuccess) return KVQ_ERR_CUDA;
+  const long long n = static_cast<long long>(n_layers) * batch * hq;
+  if (n == 0) return KVQ_OK;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(state, n, mp->tau, meter_a, raw_a, cert_b, counts);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  if (ranking) {
+    rank_kernel<<<batch, 512, 0, s>>>(raw_a, n_layers, batch, hq, ranking);
+    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  }
+  return KVQ_OK;
+}
+
+extern "C" const char* kvq_status_string(int32_t status) {
+  switch (status) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_INVALID_ARG: return "KVQ_ERR_INVALID_ARG";
+    case KVQ_ERR_UNSUPPORTED_LAYOUT: return "KVQ_ERR_UNSUPPORTED_LAYOUT";
+    case KVQ_ERR_WORKSPACE_TOO_SMALL: return "KVQ_ERR_WORKSPACE_TOO_SMALL";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA";
+    case KVQ_ERR_DEVICE_BOUNDS: return "KVQ_ERR_DEVICE_BOUNDS";
+    case KVQ_ERR_NONFINITE_INPUT: return "KVQ_ERR_NONFINITE_INPUT";
+    case KVQ_ERR_RANGE: return "KVQ_ERR_RANGE";
+    case KVQ_ERR_TIMEOUT: return "KVQ_ERR_TIMEOUT";
+  }
+  return "KVQ_ERR_UNKNOWN";
+}
+
+extern "C" int32_t kvq_version(void) { return KVQ_VERSION; }

@@ -1,0 +1,72 @@
+"""Tile layouts of the paged planes (the byte-offset formulas documented in include/kvq.h).
+
+Used to read a cache back into logical [page, kv head, token, channel] order
+(tests, inspection); the kernels use the same formulas in kvq_common.cuh.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = ["k_offsets", "v_offsets", "w_offsets", "s_offsets", "unpack_k", "unpack_v", "unpack_w", "unpack_s"]
+
+
+def _i(t):
+    return (t & 1) + 2 * (t >> 3)
+
+
+def k_offsets(fmt: str) -> np.ndarray:
+    """[16 tokens, 128 channels] byte offsets in a K tile."""
+    t = np.arange(16)[:, None]
+    c = np.arange(128)[None, :]
+    if fmt == "bf16":
+        return 16 * ((((t >> 3) * 4 + (c >> 5)) * 32) + (t & 7) * 4 + ((c >> 3) & 3)) + 2 * (c & 7)
+    return 16 * ((((t >> 3) * 2 + (c >> 6)) * 32) + (t & 7) * 4 + ((c >> 4) & 3)) + (c & 15)
+
+
+def v_offsets(fmt: str) -> np.ndarray:
+    t = np.arange(16)[:, None]
+    c = np.arange(128)[None, :]
+    if fmt == "bf16":
+        return 16 * (((c >> 4) * 32) + 4 * (c & 7) + ((t & 7) >> 1)) + 8 * ((c >> 3) & 1) + 2 * _i(t)
+    return 16 * (((c >> 5) * 32) + 4 * (c & 7) + ((t & 7) >> 1)) + 4 * ((c >> 3) & 3) + _i(t)
+
+
+def w_offsets() -> np.ndarray:
+    t = np.arange(16)[:, None]
+    b = np.arange(16)[None, :]
+    return 16 * (4 * (t & 7) + (b >> 2)) + 8 * (t >> 3) + 2 * (b & 3)
+
+
+def s_offsets() -> np.ndarray:
+    t = np.arange(16)
+    return 2 * (4 * ((t & 7) >> 1) + _i(t))
+
+
+def _gather16(tiles: np.ndarray, offs: np.ndarray) -> np.ndarray:
+    u16 = np.ascontiguousarray(tiles).view(np.uint16)
+    return u16[..., offs // 2]
+
+
+def unpack_k(tiles: np.ndarray, fmt: str, num_kv_heads: int) -> np.ndarray:
+    """K plane bytes [pages*heads, tile] -> codes [pages, heads, 16, 128] (uint16 bf16 bits / uint8)."""
+    tiles = tiles.reshape(-1, num_kv_heads, tiles.shape[-1])
+    offs = k_offsets(fmt)
+    return _gather16(tiles, offs) if fmt == "bf16" else tiles[..., offs]
+
+
+def unpack_v(tiles: np.ndarray, fmt: str, num_kv_heads: int) -> np.ndarray:
+    tiles = tiles.reshape(-1, num_kv_heads, tiles.shape[-1])
+    offs = v_offsets(fmt)
+    return _gather16(tiles, offs) if fmt == "bf16" else tiles[..., offs]
+
+
+def unpack_w(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:
+    """witness plane -> fp16 bits [pages, heads, 16 tokens, 16 bands]."""
+    tiles = tiles.reshape(-1, num_kv_heads, tiles.shape[-1])
+    return _gather16(tiles, w_offsets())
+
+
+def unpack_s(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:
+    """scale plane -> fp16 bits [pages, heads, 16 tokens]."""
+    tiles = tiles.reshape(-1, num_kv_heads, tiles.shape[-1])
+    return _gather16(tiles, s_offsets())

@@ -1,0 +1,145 @@
+"""Host-side checks of the C ABI and of the tile layouts (no GPU needed).
+
+* libkvq.so builds, loads, and exports every function include/kvq.h declares;
+* the pure host entry points answer (tile sizes, status strings, version);
+* the ctypes structs match the C struct sizes;
+* every tile layout is a bijection onto its tile bytes, and the decode
+  kernel's per-lane 16-byte reads are contiguous and bank-conflict free.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_kv_cache_kvq_gb300 import build as b
+
+    b.build()
+    import quantized_kv_cache_kvq_gb300 as kvq
+
+    return kvq.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s+(kvq_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"kvq_append", "kvq_decode_attn", "kvq_meter", "kvq_decode_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_host_entry_points(lib):
+    import quantized_kv_cache_kvq_gb300 as kvq
+
+    assert lib.kvq_version() == 1
+    assert kvq.status_string(0) == "KVQ_OK"
+    assert kvq.status_string(8) == "KVQ_ERR_TIMEOUT"
+    assert kvq.tile_bytes("bf16", 0) == 4096 and kvq.tile_bytes("e4m3", 0) == 2048
+    assert kvq.tile_bytes("int8", 1) == 2048 and kvq.tile_bytes("bf16", 1) == 4096
+    assert kvq.tile_bytes("int8", 2) == 32 and kvq.tile_bytes("bf16", 2) == 0
+    assert kvq.tile_bytes("e4m3s", 3) == 32 and kvq.tile_bytes("e4m3", 4) == 512
+
+
+def test_struct_sizes_match_c():
+    import quantized_kv_cache_kvq_gb300 as kvq
+
+    assert ctypes.sizeof(kvq._Cache) == 6 * 4 + 8 + 5 * 8
+    assert ctypes.sizeof(kvq.MeterParams) == 32
+    assert kvq.MeterParams.delta_req.offset == 16
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    import quantized_kv_cache_kvq_gb300 as kvq
+
+    # a NULL cache and a bad format are argument errors detected before any device work
+    assert lib.kvq_append(None, None, None, 0, None, 1, None, None) == 1
+    c = kvq._Cache(9, 0, 8, 1, 0, 0, 0, 16, 16, None, None, 16)
+    assert lib.kvq_append(ctypes.byref(c), 16, 16, 0, 16, 1, None, None) == 2
+    assert lib.kvq_decode_workspace_size(1, 3, 8) == 0  # 8 % 3 != 0
+
+
+@pytest.mark.parametrize("plane,fmt,nbytes,elem", [
+    ("k", "bf16", 4096, 2), ("k", "e4m3", 2048, 1), ("v", "bf16", 4096, 2), ("v", "e4m3", 2048, 1)])
+def test_layouts_are_bijections(plane, fmt, nbytes, elem):
+    from quantized_kv_cache_kvq_gb300 import layout as L
+
+    offs = (L.k_offsets if plane == "k" else L.v_offsets)(fmt)
+    assert offs.shape == (16, 128)
+    assert np.all(offs % elem == 0)
+    assert sorted((offs // elem).ravel().tolist()) == list(range(nbytes // elem))
+
+
+def test_witness_and_scale_layouts_are_bijections():
+    from quantized_kv_cache_kvq_gb300 import layout as L
+
+    assert sorted((L.w_offsets() // 2).ravel().tolist()) == list(range(256))
+    assert sorted((L.s_offsets() // 2).tolist()) == list(range(16))
+
+
+def _bank_conflict_free(chunk_idx):
+    """32 lanes read 16-byte chunks; the hardware serves 8 lanes per phase: the 8 chunks of a phase
+    must fall into 8 distinct 16-byte bank groups (chunk index mod 8)."""
+    for ph in range(4):
+        grp = [c % 8 for c in chunk_idx[8 * ph:8 * ph + 8]]
+        if len(set(grp)) != 8:
+            return False
+    return True
+
+
+def test_decode_fragment_reads_are_contiguous_and_conflict_free():
+    from quantized_kv_cache_kvq_gb300 import layout as L
+
+    lanes = np.arange(32)
+    g, c = lanes >> 2, lanes & 3
+    # K 16-bit: read (nt, j) gives lane (g, c) token 8nt+g, channels 32j+8c .. +7
+    ko = L.k_offsets("bf16")
+    for nt in range(2):
+        for j in range(4):
+            starts = [ko[8 * nt + gg, 32 * j + 8 * cc] for gg, cc in zip(g, c)]
+            assert all(ko[8 * nt + gg, 32 * j + 8 * cc + e] == s + 2 * e for gg, cc, s in zip(g, c, starts) for e in range(8))
+            assert starts == [((nt * 4 + j) * 32 + L_) * 16 for L_ in lanes]
+            assert _bank_conflict_free([s // 16 for s in starts])
+    # K 8-bit: read (nt, jj): token 8nt+g, channels 64jj+16c .. +15
+    ko8 = L.k_offsets("e4m3")
+    for nt in range(2):
+        for jj in range(2):
+            starts = [ko8[8 * nt + gg, 64 * jj + 16 * cc] for gg, cc in zip(g, c)]
+            assert starts == [((nt * 2 + jj) * 32 + L_) * 16 for L_ in lanes]
+            assert all(ko8[8 * nt + gg, 64 * jj + 16 * cc + e] == s + e for gg, cc, s in zip(g, c, starts) for e in range(16))
+    # V 8-bit: read m gives lane (g, c), n-tile 4m+r, channel 8(4m+r)+g, tokens 2c, 2c+1, 2c+8, 2c+9
+    vo = L.v_offsets("e4m3")
+    toks = lambda cc: [2 * cc, 2 * cc + 1, 2 * cc + 8, 2 * cc + 9]
+    for m in range(4):
+        for r in range(4):
+            for gg, cc, L_ in zip(g, c, lanes):
+                ch = 8 * (4 * m + r) + gg
+                assert [vo[t, ch] for t in toks(cc)] == [(m * 32 + L_) * 16 + 4 * r + i for i in range(4)]
+    # V 16-bit: read m gives n-tiles 2m, 2m+1
+    vo16 = L.v_offsets("bf16")
+    for m in range(8):
+        for r in range(2):
+            for gg, cc, L_ in zip(g, c, lanes):
+                ch = 8 * (2 * m + r) + gg
+                assert [vo16[t, ch] for t in toks(cc)] == [(m * 32 + L_) * 16 + 8 * r + 2 * i for i in range(4)]
+    # witness: lane reads chunk L: tokens g (+8 for the second half), bands 4c..4c+3
+    wo = L.w_offsets()
+    for gg, cc, L_ in zip(g, c, lanes):
+        for nt in range(2):
+            assert [wo[8 * nt + gg, 4 * cc + i] for i in range(4)] == [L_ * 16 + 8 * nt + 2 * i for i in range(4)]
+    # scales: lane c reads 8 bytes at 8c: tokens 2c, 2c+1, 2c+8, 2c+9
+    so = L.s_offsets()
+    for cc in range(4):
+        assert [so[t] for t in toks(cc)] == [8 * cc + 2 * i for i in range(4)]
