@@ -1,0 +1,495 @@
+#!/usr/bin/env python
+"""Decode-step benchmark: KV GB/s of quantized-cache decode attention with the fused meter.
+
+A step is one decode step of the whole model: for every layer, append the new
+token's K/V (kvq_append) and run kvq_decode_attn over [shared prefix ++ live
+suffix]; then kvq_meter finalises the meter of every (layer, sequence, head).
+The default workload is the Qwen3-8B-shaped cartridge decode (batch 16, 36
+layers, 8 kv heads, 32 q heads, 632-token K16/V8 shared prefix with a x10 sink,
+11,996-token BF16 live suffix = 12,628 attended tokens).
+
+value = algorithmic bytes of the step (every live token's K, V, scales and
+witness once per (layer, kv head); the shared prefix once per layer) / step
+time.  Inputs are resident in HBM before the timed region and larger than L2
+(no flush needed).  `e2e` is the same metric through the public API with host
+buffers: pinned host->device copies of the step's queries and new K/V, and a
+device->host read of the outputs and meter, inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "decode-attn KV GB/s (% of GB300 HBM peak) with meter on; attended tok/s"
+SM_SCALE = float(np.float32(1.0 / math.sqrt(128)))
+KERNEL_SOURCES = ["quantized_kv_cache_kvq_gb300/csrc/decode_kernel.cuh", "quantized_kv_cache_kvq_gb300/csrc/decode.cu",
+                  "quantized_kv_cache_kvq_gb300/csrc/kvq_common.cuh"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="qwen3_8b_cartridge", choices=sorted(W.WORKLOADS))
+    p.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layers", type=int, default=0, help="override layer count (profiling only; not a bench line)")
+    return p.parse_args()
+
+
+CODE_BYTES = {"bf16": 2, "e4m3": 1, "e4m3s": 1, "int8": 1}
+HAS_SCALE = {"bf16": 0, "e4m3": 0, "e4m3s": 1, "int8": 1}
+
+
+def token_head_bytes(k_fmt, v_fmt, meter=True) -> int:
+    """Bytes one token of one kv head costs the decode: K and V codes, fp16 scales, 32-byte witness."""
+    return 128 * (CODE_BYTES[k_fmt] + CODE_BYTES[v_fmt]) + 2 * (HAS_SCALE[k_fmt] + HAS_SCALE[v_fmt]) + 32 * meter
+
+
+def step_bytes(w, lens) -> int:
+    """Algorithmic bytes of one decode step: live tokens once per (layer, kv head), the prefix once per layer."""
+    live = int(np.sum(lens)) * token_head_bytes(w.k_fmt, w.v_fmt)
+    pre = w.prefix_len * token_head_bytes(w.prefix_k_fmt, w.prefix_v_fmt) if w.prefix_len else 0
+    return w.n_layers * w.n_kv_heads * (live + pre)
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record(workload: str):
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(workload)
+    if not rec or rec.get("kernel_hash") != kernel_hash():
+        return None
+    return rec
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sms.append(float(parts[0]))
+                    mx = float(parts[1])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------------------------------------ GPU arm
+class Model:
+    """All layers' caches of one workload, filled through kvq_append, plus the step's buffers."""
+
+    def __init__(self, w, device, seed_base=0, n_layers=None):
+        import torch
+
+        import quantized_kv_cache_kvq_gb300 as kvq
+
+        self.kvq, self.torch, self.w, self.dev = kvq, torch, w, device
+        self.L = n_layers or w.n_layers
+        B, Hkv, Hq = w.batch, w.n_kv_heads, w.n_q_heads
+        self.lens = W.seq_lengths(w)
+        pages = (self.lens + W.PAGE - 1) // W.PAGE
+        max_pages = int(pages.max())
+        if w.random_pages:
+            bt = W.permuted_block_table(self.lens, W.unit_seed(w, 424_242), max_pages)
+        else:
+            bt = W.identity_block_table(self.lens, max_pages)
+        self.num_pages = int(pages.sum())
+        self.bt = torch.from_numpy(bt).to(device)
+        self.seq_lens = torch.from_numpy(self.lens.astype(np.int32)).to(device)
+        # the step's new token sits at the last position of every sequence
+        last = self.lens - 1
+        self.new_slots = torch.from_numpy(np.array([W.slot_mapping(bt, s, [last[s]])[0] for s in range(B)],
+                                                   dtype=np.int32)).to(device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        g = torch.Generator(device=device)
+        self.caches, self.prefixes = [], []
+        theta = w.rope_theta
+        inv = torch.tensor(theta ** (-2.0 * np.arange(64) / 128), dtype=torch.float64, device=device)
+        total = int(self.lens.sum())
+        pos = torch.cat([torch.arange(w.prefix_len, w.prefix_len + int(n), device=device) for n in self.lens])
+        slots = torch.cat([torch.from_numpy(W.slot_mapping(bt, s, np.arange(n))) for s, n in
+                           enumerate(self.lens)]).to(device)
+        for l in range(self.L):
+            g.manual_seed(W.unit_seed(w, 100_000 + 1000 * seed_base + l))
+            c = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, self.num_pages, layer=l,
+                               seed=(0x5EED << 20) + 97 * l + seed_base)
+            chunk = 1 << 20
+            for a in range(0, total, chunk):
+                b = min(total, a + chunk)
+                k, v = self._gen(g, b - a, pos[a:b], inv, l)
+                kvq.append(c, k, v, slots[a:b].contiguous(), self.err)
+            self.caches.append(c)
+            if w.prefix_len:
+                p = kvq.PagedCache(w.prefix_k_fmt, w.prefix_v_fmt, Hkv, (w.prefix_len + 15) // 16, layer=l,
+                                   seed=(0xCA47 << 20) + l)
+                k, v = self._gen(g, w.prefix_len, torch.arange(w.prefix_len, device=device), inv, l, sink=True)
+                kvq.append(p, k, v, torch.arange(w.prefix_len, dtype=torch.int32, device=device), self.err)
+                self.prefixes.append(p)
+            else:
+                self.prefixes.append(None)
+        # the step's inputs: queries and new K/V of every layer
+        qd = torch.bfloat16 if w.q_dtype == "bf16" else torch.float32
+        g.manual_seed(W.unit_seed(w, 200_000 + seed_base))
+        self.q = torch.randn((self.L, B, Hq, 128), generator=g, device=device).to(qd).contiguous()
+        self.k_new = torch.randn((self.L, B, Hkv, 128), generator=g, device=device)
+        self.v_new = torch.randn((self.L, B, Hkv, 128), generator=g, device=device)
+        self.out = torch.empty((self.L, B, Hq, 128), device=device)
+        self.state = torch.empty((self.L, B, Hq, 4), device=device)
+        self.meter_a = torch.empty((self.L, B, Hq), device=device)
+        self.raw_a = torch.empty((self.L, B, Hq), device=device)
+        self.cert_b = torch.empty((self.L, B, Hq), device=device) if w.tier_b else None
+        self.counts = torch.zeros(4, dtype=torch.int32, device=device)
+        self.ranking = (torch.empty((B, self.L * Hq), dtype=torch.int32, device=device)
+                        if w.n_outliers else None)
+        self.ws = torch.empty(kvq.decode_workspace_size(B, Hkv, Hq), dtype=torch.uint8, device=device)
+        tiers = kvq.TIER_A | (kvq.TIER_B if w.tier_b else 0)
+        self.mp = kvq.meter_params(tiers, w.n_layers, Hq, w.n_steps, w.delta_req, w.tau)
+        torch.cuda.synchronize()
+        if self.err.item() != 0:
+            raise RuntimeError(f"append reported {kvq.STATUS.get(self.err.item())}")
+
+    def _gen(self, g, n, pos, inv, layer, sink=False):
+        torch, w = self.torch, self.w
+        Hkv = w.n_kv_heads
+        k = torch.randn((n, Hkv, 128), generator=g, device=self.dev, dtype=torch.float32)
+        v = torch.randn((n, Hkv, 128), generator=g, device=self.dev, dtype=torch.float32)
+        if sink and w.sink_scale != 1.0:
+            k[0] *= w.sink_scale
+            v[0] *= w.sink_scale
+        for h in range(Hkv):
+            ch = W.outlier_channels(w, layer, h)
+            if ch.size:
+                k[:, h, torch.from_numpy(ch).to(self.dev)] *= w.outlier_scale
+        ang = pos.to(torch.float64)[:, None] * inv[None, :]
+        cos, sin = torch.cos(ang).float()[:, None, :], torch.sin(ang).float()[:, None, :]
+        a, b = k[..., :64], k[..., 64:]
+        k = torch.cat([a * cos - b * sin, b * cos + a * sin], dim=-1).contiguous()
+        return k, v
+
+    def step(self, q=None, k_new=None, v_new=None, events=None):
+        kvq, w = self.kvq, self.w
+        q = self.q if q is None else q
+        k_new = self.k_new if k_new is None else k_new
+        v_new = self.v_new if v_new is None else v_new
+        for l in range(self.L):
+            kvq.append(self.caches[l], k_new[l], v_new[l], self.new_slots, self.err)
+            if events is not None:
+                events[l][0].record()
+            kvq.decode_attn(self.caches[l], q[l], self.bt, self.seq_lens, self.out[l], self.ws,
+                            prefix=self.prefixes[l], prefix_len=w.prefix_len, sm_scale=SM_SCALE, meter=self.mp,
+                            meter_state=self.state[l], err=self.err)
+            if events is not None:
+                events[l][1].record()
+        kvq.meter(self.state, self.L, w.batch, w.n_q_heads, self.mp, self.meter_a, self.raw_a, self.counts,
+                  cert_b=self.cert_b, ranking=self.ranking)
+
+    def launches_per_step(self) -> int:
+        return self.L * 3 + 1 + (1 if self.ranking is not None else 0)
+
+
+def run_gpu(args, w):
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import quantized_kv_cache_kvq_gb300 as kvq
+
+    kvq.load()
+    m = Model(w, dev, seed_base=rank, n_layers=args.layers or None)
+    per_step_bytes = step_bytes(w, m.lens) * m.L // w.n_layers
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        m.step()
+    barrier()
+    events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(m.L)]
+              for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        start.record()
+        for s in range(args.steps):
+            m.step(events=events[s])
+        stop.record()
+        barrier()
+    ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    if m.err.item() != 0:
+        raise RuntimeError(f"device error {kvq.STATUS.get(m.err.item())}")
+    ms_step = ms / args.steps
+    value = per_step_bytes * world / (ms_step * 1e-3) / 1e9
+    layer_ms = [e[0].elapsed_time(e[1]) for st in events for e in st]
+    layer_bytes = per_step_bytes / m.L
+    achieved = layer_bytes / (statistics.mean(layer_ms) * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    tr = traffic_record(w.name)
+    attended = float(np.sum(m.lens) + w.prefix_len * w.batch) * m.L * w.n_kv_heads
+    res = dict(value=value, ms_step=ms_step, achieved=achieved, layer_ms_mean=statistics.mean(layer_ms),
+               layer_ms_median=statistics.median(layer_ms), peak=peak, peak_kind=peak_kind, traffic=tr,
+               clocks=clk.summary(), launches=m.launches_per_step() * args.steps, attended=attended,
+               per_step_bytes=per_step_bytes, world=world, rank=rank, counts=m.counts.cpu().tolist())
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, m, per_step_bytes, world)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return res
+
+
+def run_e2e(args, m, per_step_bytes, world):
+    """Same metric through the public API with pinned host buffers and copies in the timed region."""
+    torch = m.torch
+    hq = torch.empty(m.q.shape, dtype=m.q.dtype, pin_memory=True).copy_(m.q)
+    hk = torch.empty(m.k_new.shape, dtype=m.k_new.dtype, pin_memory=True).copy_(m.k_new)
+    hv = torch.empty(m.v_new.shape, dtype=m.v_new.dtype, pin_memory=True).copy_(m.v_new)
+    ho = torch.empty(m.out.shape, dtype=m.out.dtype, pin_memory=True)
+    hm = torch.empty(m.meter_a.shape, dtype=m.meter_a.dtype, pin_memory=True)
+    hc = torch.empty(4, dtype=torch.int32, pin_memory=True)
+    dq, dk, dv = torch.empty_like(m.q), torch.empty_like(m.k_new), torch.empty_like(m.v_new)
+
+    def one():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        m.step(dq, dk, dv)
+        ho.copy_(m.out, non_blocking=True)
+        hm.copy_(m.meter_a, non_blocking=True)
+        hc.copy_(m.counts, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+        torch.cuda.current_stream().synchronize()  # the host reads the step's result
+    el = (time.perf_counter() - t0) / args.steps
+    h2d = (hq.numel() * hq.element_size() + hk.numel() * 4 + hv.numel() * 4)
+    d2h = ho.numel() * 4 + hm.numel() * 4 + 16
+    return {"value": per_step_bytes * world / el / 1e9, "unit": "GB/s", "ms_per_step": el * 1e3,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------------------------------ CPU oracle
+def oracle_units(w, n_units: int, seed_base: int = 0):
+    """Time the float64 oracle's decode of n (sequence, kv head) units of layer 0 at full context."""
+    from oracle import attention as OA
+    from oracle.encoders import fp16_value
+    from tests.parity import oracle_cache_rows
+
+    lens = W.seq_lengths(w)
+    bts = W.identity_block_table(lens)
+    total_bytes, elapsed = 0, 0.0
+    for u in range(n_units):
+        s = (u + seed_base) % w.batch
+        n = int(lens[s])
+        k32, v32, q = W.gen_unit_cpu(w, s, 0, n, first_pos=w.prefix_len)
+        g = u % w.n_kv_heads
+        k1, v1 = k32[:, g:g + 1], v32[:, g:g + 1]
+        slots = W.slot_mapping(bts, s, np.arange(n))
+        pre = None
+        if w.prefix_len:
+            pk, pv, _ = W.gen_unit_cpu(w, 0, 0, w.prefix_len, seed_unit=777_777)
+            pre = (pk[:, g:g + 1], pv[:, g:g + 1])
+        t0 = time.perf_counter()
+        rows = oracle_cache_rows(k1, v1, slots, w.k_fmt, w.v_fmt, 1234, 0)
+        kk, kh, vh, ww = k1[:, 0], rows["kh"][:, 0], rows["vh"][:, 0], fp16_value(rows["w16"][:, 0])
+        sk = fp16_value(rows["ksb"][:, 0]) if rows["ksb"] is not None else None
+        if pre is not None:
+            pr = oracle_cache_rows(pre[0], pre[1], np.arange(w.prefix_len), w.prefix_k_fmt, w.prefix_v_fmt, 99, 0)
+            kk = np.concatenate([pre[0][:, 0], kk])
+            kh = np.concatenate([pr["kh"][:, 0], kh])
+            vh = np.concatenate([pr["vh"][:, 0], vh])
+            ww = np.concatenate([fp16_value(pr["w16"][:, 0]), ww])
+        G = w.group
+        tb = dict(delta_req=w.delta_req, n_layers=w.n_layers, n_q_heads=w.n_q_heads, n_steps=w.n_steps) \
+            if w.tier_b else None
+        OA.decode_head(q[g * G:(g + 1) * G].astype(np.float64), kk, kh, vh, ww, SM_SCALE, s_k=sk, tier_b=tb)
+        elapsed += time.perf_counter() - t0
+        total_bytes += n * token_head_bytes(w.k_fmt, w.v_fmt)
+        if w.prefix_len:
+            total_bytes += w.prefix_len * token_head_bytes(w.prefix_k_fmt, w.prefix_v_fmt)
+    return total_bytes, elapsed
+
+
+def host_threads() -> int:
+    try:
+        import threadpoolctl
+
+        info = threadpoolctl.threadpool_info()
+        n = max([i.get("num_threads", 1) for i in info] or [1])
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, budget_s: float = 15.0):
+    """Oracle GB/s on a bounded sample: as many full-context units as fit in ~budget_s."""
+    b1, t1 = oracle_units(w, 1)
+    n = max(1, min(4 * w.n_kv_heads, int(budget_s / max(t1, 1e-3))))
+    b, t = oracle_units(w, n, seed_base=1)
+    return {"value": b / t / 1e9, "unit": "GB/s", "cores": host_threads(), "kind": "oracle",
+            "sample": f"{n} (sequence, kv head) units of layer 0 at full context ({w.name}): float64 oracle "
+                      f"dequantize + compressed/exact attention + TV + meter; {b / 1e6:.1f} MB of KV in {t:.1f} s"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_units(w, 1)
+    b, t = 0, 0.0
+    for s in range(args.steps):
+        bb, tt = oracle_units(w, 1, seed_base=s)
+        b += bb
+        t += tt
+    value = b / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": host_threads(), "kind": "oracle",
+                             "sample": f"each step: one (sequence, kv head) unit of layer 0 at full context"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def workload_config(w):
+    lens = W.seq_lengths(w)
+    cfg = {"workload": w.name, "batch": w.batch, "layers": w.n_layers, "kv_heads": w.n_kv_heads,
+           "q_heads": w.n_q_heads, "head_dim": 128, "page_size": 16,
+           "layout": f"K {w.k_fmt} / V {w.v_fmt}", "meter": "tier A" + (" + tier B" if w.tier_b else ""),
+           "context_tokens": int(lens.mean()) + w.prefix_len, "l2": "inputs larger than L2 (no flush)"}
+    if w.prefix_len:
+        cfg["prefix"] = f"{w.prefix_len} shared tokens, K {w.prefix_k_fmt} / V {w.prefix_v_fmt}, sink x{w.sink_scale:g}"
+    return cfg
+
+
+def main():
+    args = parse()
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+    r = run_gpu(args, w)
+    if r["rank"] != 0:
+        return
+    line = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": r["world"], "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
+            "pct_of_hbm_peak": 100.0 * r["value"] / r["world"] / r["peak"],
+            "attended_kv_tok_per_s": r["attended"] * r["world"] / (r["ms_step"] * 1e-3),
+            "seq_tok_per_s": w.batch * r["world"] / (r["ms_step"] * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
+                         "frac": r["achieved"] / r["peak"],
+                         "traffic": (r["traffic"]["bytes_per_launch"] if r["traffic"] else None),
+                         "kernel": "kvq_decode_attn (decode_split_kernel + merge_kernel)",
+                         "peak_source": f"{r['peak_kind']} hbm_gbs",
+                         "algorithmic_bytes_per_launch": r["per_step_bytes"] // (args.layers or w.n_layers),
+                         "launch_ms_mean": r["layer_ms_mean"]},
+            "gpu_launches": r["launches"], "clocks": r["clocks"], "meter_counts": r["counts"]}
+    if "e2e" in r:
+        line["e2e"] = r["e2e"]
+    if args.layers:
+        line["note"] = f"profiling run with {args.layers} layers: not a bench line"
+    if r["world"] == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
