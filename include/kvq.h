@@ -82,15 +82,16 @@ typedef enum kvq_dtype { KVQ_DTYPE_F32 = 0, KVQ_DTYPE_BF16 = 1 } kvq_dtype;
  * in 0..15; they place each lane's tensor-core fragment in contiguous 16-byte
  * words so one bulk copy of a tile feeds the decode kernel with conflict-free
  * shared-memory loads):
- *   K, 16-bit (4096 B):  16 * ((((t>>3)*4 + (c>>5)) * 32) + (t&7)*4 + ((c>>3)&3)) + 2*(c&7)
- *   K,  8-bit (2048 B):  16 * ((((t>>3)*2 + (c>>6)) * 32) + (t&7)*4 + ((c>>4)&3)) + (c&15)
- *   V, 16-bit (4096 B):  16 * (((c>>4) * 32) + 4*(c&7) + ((t&7)>>1)) + 8*((c>>3)&1) + 2*i(t)
- *   V,  8-bit (2048 B):  16 * (((c>>5) * 32) + 4*(c&7) + ((t&7)>>1)) + 4*((c>>3)&3) +   i(t)
- *   witness (512 B, fp16 bits):  16 * (4*(t&7) + (b>>2)) + 8*(t>>3) + 2*(b&3)
- *   scale   (32 B,  fp16 bits):   2 * (4*((t&7)>>1) + i(t))
- * with i(t) = (t&1) + 2*(t>>3).  Band b holds the RoPE frequency pairs
- * 4b..4b+3 of the half-split pairing (pair j = channels j and j+64), i.e.
- * channels 4b..4b+3 and 64+4b..64+4b+3 ([W] Sec. 4.1, eq. (2)).
+ *   K, 16-bit (4096 B):  16*(((t>>3)*4 + (c>>5))*32 + (t&7)*4 + ((c>>3)&3)) + 2*(c&7)
+ *   K,  8-bit (2048 B):  16*(((t>>3)*2 + (c>>6))*32 + (t&7)*4 + ((c>>4)&3)) + (c&15)
+ *   V, 16-bit (4096 B):  16*(32*(c>>4) + 4*(c&7) + ((t&7)>>1)) + 4*(2*(t>>3) + ((c>>3)&1)) + 2*(t&1)
+ *   V,  8-bit (2048 B):  16*(32*(c>>5) + 4*(c&7) + ((t&7)>>1)) + 8*((c>>4)&1)
+ *                        + 2*(2*(t>>3) + ((c>>3)&1)) + (t&1)
+ *   witness (512 B, fp16 bits):  16*(4*(t&7) + (b>>2)) + 8*(t>>3) + 2*(b&3)
+ *   scale   (32 B,  fp16 bits):  2*(2*(t&7) + (t>>3))
+ * Band b holds the RoPE frequency pairs 4b..4b+3 of the half-split pairing
+ * (pair j = channels j and j+64), i.e. channels 4b..4b+3 and 64+4b..64+4b+3
+ * ([W] Sec. 4.1, eq. (2)).
  */
 typedef struct kvq_cache {
   int32_t k_fmt;          /* kvq_fmt of the key plane                                  */

@@ -38,7 +38,7 @@ __all__ = [
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvq.so")
+LIB_PATH = os.environ.get("KVQ_LIB") or os.path.join(_HERE, "libkvq.so")
 
 FMT = {"bf16": 0, "e4m3": 1, "e4m3s": 2, "int8": 3}
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}

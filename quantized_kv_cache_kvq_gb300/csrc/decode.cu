@@ -12,9 +12,19 @@ namespace kvq {
 namespace dec {
 
 // ------------------------------------------------------------------------------------------------
-// Merge of the (warp, unit) pieces: one warp per (sequence, query head).
-__global__ void __launch_bounds__(128) merge_kernel(const Args a, int meter_on, float* __restrict__ out,
-                                                    float* __restrict__ meter_state) {
+// Merge of the (warp, unit) pieces: one warp per (sequence, query head).  Piece statistics are
+// loaded lane-parallel and combined by shuffles; the O^T partials are read with independent
+// loads.  WitCert Sec. 6.2.2: the certificate A is a p~-weighted average, so per-piece sums
+// merged under the same log-sum-exp weights give the global A exactly.
+__device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
+  const float mm = fmaxf(m, m2);
+  if (mm == -INFINITY) return;
+  s = (m == -INFINITY ? 0.f : s * ex2(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * ex2(m2 - mm));
+  m = mm;
+}
+
+__global__ void __launch_bounds__(256) merge_kernel(const Args a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's pieces are complete and visible
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (gw >= static_cast<long long>(a.B) * a.Hq) return;
@@ -24,46 +34,67 @@ __global__ void __launch_bounds__(128) merge_kernel(const Args a, int meter_on, 
   const long long T = static_cast<long long>(a.Hkv) * cum[a.B];
   const int P = cum[seq + 1] - cum[seq];
   const int unit = seq * a.Hkv + kvh;
-  float* o = out + static_cast<size_t>(gw) * kHeadDim;
+  float* o = a.out + static_cast<size_t>(gw) * kHeadDim;
   const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
-  if (P == 0 || T == 0) {
+  if (P == 0) {
     *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (meter_state && lane == 0)
-      *reinterpret_cast<float4*>(meter_state + gw * 4) =
+    if (a.meter_state && lane == 0)
+      *reinterpret_cast<float4*>(a.meter_state + gw * 4) =
           make_float4(-INFINITY, a.tier_b ? -INFINITY : NAN, -INFINITY, static_cast<float>(total));
     return;
   }
   const long long W = min(static_cast<long long>(a.w_max), T);
   const long long b_u = static_cast<long long>(a.Hkv) * cum[seq] + static_cast<long long>(kvh) * P;
   const long long e_u = b_u + P;
-  auto warp_of = [&](long long x) { return ((x + 1) * W - 1) / T; };
-  const long long w_lo = warp_of(b_u), w_hi = warp_of(e_u - 1);
-  float M = -INFINITY, Mc = -INFINITY, Mu = -INFINITY;
-  for (long long w = w_lo; w <= w_hi; ++w) {
-    const float* st = a.ws_stats + ((static_cast<size_t>(w) + unit) * a.G + row) * 8;
-    M = fmaxf(M, st[0]);
-    Mc = fmaxf(Mc, st[2]);
-    Mu = fmaxf(Mu, st[4]);
+  // warp w covers pages [T w / W, T (w + 1) / W): the warp holding page x is ((x + 1) W - 1) / T
+  const long long w_lo = ((b_u + 1) * W - 1) / T, w_hi = (e_u * W - 1) / T;
+  const int np = static_cast<int>(w_hi - w_lo + 1);
+  auto stats = [&](int i) { return a.ws_stats + ((static_cast<size_t>(w_lo) + i + unit) * a.G + row) * 8; };
+  float m = -INFINITY, l = 0.f, mc = -INFINITY, sc = 0.f, mu = -INFINITY, su = 0.f;
+  for (int i = lane; i < np; i += 32) {
+    const float4 s4 = *reinterpret_cast<const float4*>(stats(i));
+    const float2 s2 = *reinterpret_cast<const float2*>(stats(i) + 4);
+    lse_combine(m, l, s4.x, s4.y);
+    lse_combine(mc, sc, s4.z, s4.w);
+    lse_combine(mu, su, s2.x, s2.y);
   }
-  float Ls = 0.f, Sc = 0.f, Su = 0.f;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float m2 = __shfl_xor_sync(kFull, m, off), l2 = __shfl_xor_sync(kFull, l, off);
+    const float c2 = __shfl_xor_sync(kFull, mc, off), s2 = __shfl_xor_sync(kFull, sc, off);
+    const float u2 = __shfl_xor_sync(kFull, mu, off), v2 = __shfl_xor_sync(kFull, su, off);
+    lse_combine(m, l, m2, l2);
+    lse_combine(mc, sc, c2, s2);
+    lse_combine(mu, su, u2, v2);
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long w = w_lo; w <= w_hi; ++w) {
-    const size_t slot = static_cast<size_t>(w) + unit;
-    const float* st = a.ws_stats + (slot * a.G + row) * 8;
-    const float wt = (st[0] == -INFINITY) ? 0.f : exp2f(st[0] - M);
-    Ls += st[1] * wt;
-    if (st[2] != -INFINITY) Sc += st[3] * exp2f(st[2] - Mc);
-    if (st[4] != -INFINITY) Su += st[5] * exp2f(st[4] - Mu);
-    const float4 v = *reinterpret_cast<const float4*>(a.ws_acc + (slot * a.G + row) * kHeadDim + 4 * lane);
-    acc.x += v.x * wt; acc.y += v.y * wt; acc.z += v.z * wt; acc.w += v.w * wt;
+  constexpr int kU = 8;
+  for (int i0 = 0; i0 < np; i0 += kU) {
+    float mi[kU];
+    float4 v[kU];
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      if (i0 + k < np) {
+        mi[k] = stats(i0 + k)[0];
+        v[k] = *reinterpret_cast<const float4*>(
+            a.ws_acc + ((static_cast<size_t>(w_lo) + i0 + k + unit) * a.G + row) * kHeadDim + 4 * lane);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      if (i0 + k < np && mi[k] != -INFINITY) {
+        const float wt = ex2(mi[k] - m);
+        acc.x += v[k].x * wt; acc.y += v[k].y * wt; acc.z += v[k].z * wt; acc.w += v[k].w * wt;
+      }
+    }
   }
-  const float inv = kPvShiftInv / Ls;
+  const float inv = kPvShiftInv / l;
   *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (meter_state && lane == 0) {
-    const float lse2 = M + log2f(Ls);
-    const float la = (meter_on && Sc > 0.f) ? (Mc + log2f(Sc) - lse2) * kLn2 : -INFINITY;
-    const float lb = a.tier_b ? ((Su > 0.f) ? (Mu + log2f(Su) - lse2) * kLn2 : -INFINITY) : NAN;
-    *reinterpret_cast<float4*>(meter_state + gw * 4) = make_float4(la, lb, lse2 * kLn2, static_cast<float>(total));
+  if (a.meter_state && lane == 0) {
+    const float lse2 = m + log2f(l);
+    const float la = (a.meter_on && sc > 0.f) ? (mc + log2f(sc) - lse2) * kLn2 : -INFINITY;
+    const float lb = a.tier_b ? ((su > 0.f) ? (mu + log2f(su) - lse2) * kLn2 : -INFINITY) : NAN;
+    *reinterpret_cast<float4*>(a.meter_state + gw * 4) = make_float4(la, lb, lse2 * kLn2, static_cast<float>(total));
   }
 }
 
@@ -240,6 +271,9 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* p
         std::log(mp->delta_req / (static_cast<double>(mp->n_layers) * mp->n_q_heads * mp->n_steps)));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.ws_cum = reinterpret_cast<int32_t*>(ws + wl.cum);
+  a.out = out;
+  a.meter_state = meter_state;
+  a.meter_on = meter ? 1 : 0;
   a.ws_stats = reinterpret_cast<float*>(ws + wl.stats);
   a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
   a.w_max = w_max;
@@ -261,8 +295,18 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* p
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (launch(a, sms, smem, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  // merge: programmatic dependent launch, so its launch overlaps the decode grid's tail
   const long long merge_threads = static_cast<long long>(batch) * num_q_heads * 32;
-  merge_kernel<<<static_cast<unsigned>((merge_threads + 127) / 128), 128, 0, s>>>(a, meter ? 1 : 0, out, meter_state);
-  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((merge_threads + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, merge_kernel, a) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
 }

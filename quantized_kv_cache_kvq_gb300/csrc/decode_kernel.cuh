@@ -26,8 +26,13 @@
 namespace kvq {
 namespace dec {
 
-constexpr int kWarps = 8;        // warps per CTA (one CTA per SM)
-constexpr int kMaxStages = 8;
+#ifndef KVQ_DECODE_WARPS
+#define KVQ_DECODE_WARPS 12
+#endif
+// Warps per CTA (one CTA per SM).  Each warp owns a ring of page stages; the decode is bound by
+// the bytes in flight, so few warps with deep rings beat many warps with shallow ones.
+constexpr int kWarps = KVQ_DECODE_WARPS;
+constexpr int kMaxStages = 16;
 constexpr int kMaxBatch = 1024;  // sequences per call (prefix sums live in shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
@@ -60,6 +65,9 @@ struct Args {
   int tier_b;
   float ln_delta_loc;
   int32_t* ws_cum;   // [B + 1] prefix sums of pages per sequence (written by CTA 0)
+  float* out;        // [B][Hq][128]
+  float* meter_state;  // [B][Hq][4] or nullptr
+  int meter_on;
   float* ws_stats;   // [slots][G][8]
   float* ws_acc;     // [slots][G][128]
   int w_max;
@@ -208,63 +216,118 @@ __device__ __forceinline__ float one_minus_exp_neg(float c) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Per-warp state
-struct QFrag {
-  uint32_t hi[8][2];  // A fragment words a0, a2 per k-step (rows g; rows g+8 are zero)
-  uint32_t lo[8][2];  // low parts (q - hi) when q is not exactly representable in the MMA type
-  uint32_t qn_hi[2], qn_lo[2];  // band-norm A fragment (meter)
-  bool has_lo;
-  float cm_scale;   // c_t = cm_scale * (QN . W)  (natural units)
-  float alpha_b;    // Tier B: u_t = alpha_b * s_t (natural units)
-};
+// Fragment orientation.  The page's 16 tokens are the M dimension of every tensor-core product:
+//   S^T [16 tok x 8 heads]  = K [16 x 128]      . Q^T [128 x 8]    (8 k-steps)
+//   C^T [16 tok x 8 heads]  = W [16 x 16 bands] . QN^T [16 x 8]    (1 k-step; QN = band norms)
+//   O^T [128 ch x 8 heads] += V^T [128 x 16 tok] . P^T [16 x 8]    (8 m-tiles of 16 channels)
+// Lane (g, c) (g = lane / 4, c = lane % 4) holds S^T / C^T for tokens g and g+8 and query heads
+// 2c and 2c+1 (heads >= G are padding), and O^T for channels 16mt+g, 16mt+g+8 of those heads.
+// P^T, the B operand of the third product, is S^T's fragment transposed 8x8 by movmatrix.
 
-struct SoftState {
-  float m;      // running max of the logits (log2 units), per row g
-  float l;      // lane-partial sum of 2^{x - m}
-  float mc, sc; // Tier A: running max of x + c*log2e, lane-partial sum
-  float mu, su; // Tier B
-  float o[16][4];
-};
-
-__device__ __forceinline__ void reset_state(SoftState& s) {
-  s.m = -INFINITY; s.l = 0.f; s.mc = -INFINITY; s.sc = 0.f; s.mu = -INFINITY; s.su = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) { s.o[i][0] = 0.f; s.o[i][1] = 0.f; s.o[i][2] = 0.f; s.o[i][3] = 0.f; }
+__device__ __forceinline__ void mma_bf16_4(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16_4(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
 }
 
-__device__ __forceinline__ float row_max4(float v) {
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 1));
-  v = fmaxf(v, __shfl_xor_sync(kFull, v, 2));
-  return v;
-}
+// sum over the 4 lanes of one fragment row (lanes with the same g)
 __device__ __forceinline__ float row_sum4(float v) {
   v += __shfl_xor_sync(kFull, v, 1);
   v += __shfl_xor_sync(kFull, v, 2);
   return v;
 }
+// max over the 8 lanes of one fragment column (lanes with the same c)
+__device__ __forceinline__ float col_max8(float v) {
+  v = fmaxf(v, __shfl_xor_sync(kFull, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(kFull, v, 8));
+  v = fmaxf(v, __shfl_xor_sync(kFull, v, 16));
+  return v;
+}
+__device__ __forceinline__ float col_sum8(float v) {
+  v += __shfl_xor_sync(kFull, v, 4);
+  v += __shfl_xor_sync(kFull, v, 8);
+  v += __shfl_xor_sync(kFull, v, 16);
+  return v;
+}
 
-// Build the q fragments of unit (seq, kv head).  K16 family: k-step kb = 2j + s covers channels
-// 32j + 8c + 4s + {0,1} (slots 2c, 2c+1) and + {2,3} (slots 2c+8, 2c+9).  K8 family: kb = 4jj + s
-// covers 64jj + 16c + 4s + {0..3}.  Band norms: slots (2c, 2c+1) <-> bands 4c, 4c+1 and
-// (2c+8, 2c+9) <-> 4c+2, 4c+3.
+struct QFrag {
+  uint32_t hi[8][2];  // Q^T B fragments (b0, b1) per k-step: head g, channels of the K tile word order
+  uint32_t lo[8][2];  // q - hi, when q is not exactly representable in the MMA input type
+  uint32_t qn_hi[2], qn_lo[2];  // QN^T B fragment: band norms of head g (normalised by 2^-e)
+  bool has_lo;
+  float cm_scale;    // c_t = cm_scale * (W . QN)  (natural units)
+  float alpha_b[2];  // Tier B: u_t = alpha_b[h] * s_t for heads 2c, 2c+1 (natural units)
+};
+
+struct SoftState {
+  float m[2], l[2];    // per head (2c, 2c+1): running max (log2 units), lane-partial sum
+  float mc[2], sc[2];  // Tier A accumulator (max of x + c log2e, scaled sum)
+  float mu[2], su[2];  // Tier B accumulator
+  float o[8][4];       // O^T fragments of the 8 channel blocks
+};
+
+__device__ __forceinline__ void reset_state(SoftState& s) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    s.m[h] = -INFINITY; s.l[h] = 0.f; s.mc[h] = -INFINITY; s.sc[h] = 0.f; s.mu[h] = -INFINITY; s.su[h] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { s.o[i][0] = 0.f; s.o[i][1] = 0.f; s.o[i][2] = 0.f; s.o[i][3] = 0.f; }
+}
+
+// Build the fragments of unit (seq, kv head).  Lane (g, c) supplies the B fragments of query head g:
+// K16 family, k-step kb = 2j + s: b0 <- channels 32j + 8c + 4s + {0,1}, b1 <- + {2,3};
+// K8 family, kb = 4jj + s: channels 64jj + 16c + 4s + {0,1} / {2,3}.  Band norms: b0 <- bands 4c, 4c+1,
+// b1 <- 4c+2, 4c+3 (the witness tile's word order).
 template <bool K16, bool METER>
 __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const bool real = g < a.G;
   const int qh = kvh * a.G + (real ? g : 0);
   const size_t qbase = (static_cast<size_t>(seq) * a.Hq + qh) * kHeadDim;
-  auto qv = [&](int ch) -> float {
-    if (!real) return 0.f;
-    if (a.q_bf16) return bf16_bits_to_f32(static_cast<const uint16_t*>(a.q)[qbase + ch]);
-    return static_cast<const float*>(a.q)[qbase + ch];
-  };
-  bool any_lo = false;
+  // 8 consecutive channels of this lane's head (ch % 8 == 0): one 16-byte (bf16) or two (fp32) loads
+  auto load8 = [&](int ch, float (&v)[8]) {
+    if (!real) {
 #pragma unroll
-  for (int kb = 0; kb < 8; ++kb) {
-    const int ch0 = K16 ? (32 * (kb >> 1) + 8 * c + 4 * (kb & 1)) : (64 * (kb >> 2) + 16 * c + 4 * (kb & 3));
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+      return;
+    }
+    if (a.q_bf16) {
+      const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + qbase + ch);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { v[2 * i] = __uint_as_float(ws[i] << 16); v[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u); }
+    } else {
+      const float4 x0 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + qbase + ch);
+      const float4 x1 = *reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + qbase + ch + 4);
+      v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+    }
+  };
+  auto put = [&](int kb, const float* x) {  // channels x[0..3] of k-step kb: b0 <- x0, x1; b1 <- x2, x3
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const float x0 = qv(ch0 + 2 * h), x1 = qv(ch0 + 2 * h + 1);
+      const float x0 = x[2 * h], x1 = x[2 * h + 1];
       if (K16) {
         f.hi[kb][h] = pack_bf16(x0, x1);
         const float2 r = unpack_bf16(f.hi[kb][h]);
@@ -274,39 +337,68 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
         const float2 r = unpack_f16(f.hi[kb][h]);
         f.lo[kb][h] = pack_f16(x0 - r.x, x1 - r.y);
       }
-      any_lo |= (f.lo[kb][h] & 0x7FFF7FFFu) != 0u;
+    }
+  };
+  if (K16) {
+    // k-step 2j + s <- channels 32j + 8c + 4s + {0..3}
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float v[8];
+      load8(32 * j + 8 * c, v);
+      put(2 * j, v);
+      put(2 * j + 1, v + 4);
+    }
+  } else {
+    // k-step 4jj + s <- channels 64jj + 16c + 4s + {0..3}
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      float v0[8], v1[8];
+      load8(64 * jj + 16 * c, v0);
+      load8(64 * jj + 16 * c + 8, v1);
+      put(4 * jj, v0);
+      put(4 * jj + 1, v0 + 4);
+      put(4 * jj + 2, v1);
+      put(4 * jj + 3, v1 + 4);
     }
   }
+  bool any_lo = false;
+#pragma unroll
+  for (int kb = 0; kb < 8; ++kb) any_lo |= ((f.lo[kb][0] | f.lo[kb][1]) & 0x7FFF7FFFu) != 0u;
   f.has_lo = __any_sync(kFull, any_lo);
-  // band norms of q (for Tier A) and ||q|| (Tier B)
-  float qn[4];
-  float sq_all = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int b = 4 * c + i;
-    float s = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float u = qv(4 * b + e), w = qv(64 + 4 * b + e);
-      s = __fmaf_rn(u, u, s);
-      s = __fmaf_rn(w, w, s);
-    }
-    qn[i] = sqrtf(s);
-    sq_all += s;
-  }
   if (METER) {
-    // normalise the row's band norms by a power of two so that max < 2 (fp16 range), split hi/lo
+    // band b = 4c + i holds channels 16c + 4i + {0..3} and 64 + 16c + 4i + {0..3}
+    float u0[8], u1[8], w0[8], w1[8];
+    load8(16 * c, u0);
+    load8(16 * c + 8, u1);
+    load8(64 + 16 * c, w0);
+    load8(64 + 16 * c + 8, w1);
+    float qn[4];
+    float sq_all = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float* u = (i < 2) ? (u0 + 4 * i) : (u1 + 4 * (i - 2));
+      const float* w = (i < 2) ? (w0 + 4 * i) : (w1 + 4 * (i - 2));
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s = __fmaf_rn(u[e], u[e], s);
+        s = __fmaf_rn(w[e], w[e], s);
+      }
+      qn[i] = sqrtf(s);
+      sq_all += s;
+    }
+    // one power-of-two normalisation for the unit (max over heads and bands < 2), hi/lo fp16 split
     float mx = fmaxf(fmaxf(qn[0], qn[1]), fmaxf(qn[2], qn[3]));
-    mx = row_max4(mx);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
     int e2 = 0;
-    if (mx > 0.f) frexpf(mx, &e2);  // mx = f * 2^e2, f in [0.5, 1)
+    if (mx > 0.f) frexpf(mx, &e2);
     const float inv = ldexpf(1.f, -e2);
     float hv[4], lv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float v = qn[i] * inv;
-      const __half h = __float2half_rn(v);
-      hv[i] = __half2float(h);
+      hv[i] = __half2float(__float2half_rn(v));
       lv[i] = v - hv[i];
     }
     f.qn_hi[0] = pack_f16(hv[0], hv[1]);
@@ -314,10 +406,12 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     f.qn_lo[0] = pack_f16(lv[0], lv[1]);
     f.qn_lo[1] = pack_f16(lv[2], lv[3]);
     f.cm_scale = a.sm_scale * ldexpf(1.f, e2);
-    const float qnorm = sqrtf(row_sum4(sq_all));
-    // kappa = sqrt(2 ln(2S / delta_loc) / 12)
+    // ||q_g|| lives on the lanes of row g; the C fragment needs heads 2c and 2c+1
+    const float qnorm_g = sqrtf(row_sum4(sq_all));
     const float kappa = sqrtf(2.f * (logf(2.f * static_cast<float>(seq_total)) - a.ln_delta_loc) / 12.f);
-    f.alpha_b = a.sm_scale * qnorm * kappa;
+    const float q0 = __shfl_sync(kFull, qnorm_g, 8 * c), q1 = __shfl_sync(kFull, qnorm_g, 8 * c + 4);
+    f.alpha_b[0] = a.sm_scale * q0 * kappa;
+    f.alpha_b[1] = a.sm_scale * q1 * kappa;
   }
 }
 
@@ -333,213 +427,218 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   constexpr bool KDITHER = KF == KVQ_FMT_INT8_DITHER;
   constexpr bool VDITHER = VF == KVQ_FMT_INT8_DITHER;
 
-  // ---------------- logits S = q . k (tensor cores); columns are tokens 8nt + 2c, 8nt + 2c + 1
-  float S[2][4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) { S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f; }
+  // ---------------- S^T = K . Q^T: rows are tokens g (a0, a2) and g + 8 (a1, a3)
+  float S[4] = {0.f, 0.f, 0.f, 0.f};
   if (K16) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 kb = lds128(st + L::kOff + ((nt * 4 + j) * 32 + lane) * 16);
-        mma_bf16(S[nt], f.hi[2 * j][0], f.hi[2 * j][1], kb.x, kb.y);
-        mma_bf16(S[nt], f.hi[2 * j + 1][0], f.hi[2 * j + 1][1], kb.z, kb.w);
-        if (f.has_lo) {
-          mma_bf16(S[nt], f.lo[2 * j][0], f.lo[2 * j][1], kb.x, kb.y);
-          mma_bf16(S[nt], f.lo[2 * j + 1][0], f.lo[2 * j + 1][1], kb.z, kb.w);
-        }
+    for (int j = 0; j < 4; ++j) {
+      const uint4 k0 = lds128(st + L::kOff + (j * 32 + lane) * 16);
+      const uint4 k1 = lds128(st + L::kOff + ((4 + j) * 32 + lane) * 16);
+      mma_bf16_4(S, k0.x, k1.x, k0.y, k1.y, f.hi[2 * j][0], f.hi[2 * j][1]);
+      mma_bf16_4(S, k0.z, k1.z, k0.w, k1.w, f.hi[2 * j + 1][0], f.hi[2 * j + 1][1]);
+      if (f.has_lo) {
+        mma_bf16_4(S, k0.x, k1.x, k0.y, k1.y, f.lo[2 * j][0], f.lo[2 * j][1]);
+        mma_bf16_4(S, k0.z, k1.z, k0.w, k1.w, f.lo[2 * j + 1][0], f.lo[2 * j + 1][1]);
       }
     }
   } else {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int jj = 0; jj < 2; ++jj) {
+      const uint4 k0 = lds128(st + L::kOff + (jj * 32 + lane) * 16);
+      const uint4 k1 = lds128(st + L::kOff + ((2 + jj) * 32 + lane) * 16);
+      const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
+      const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const uint4 kb = lds128(st + L::kOff + ((nt * 2 + jj) * 32 + lane) * 16);
-        const uint32_t words[4] = {kb.x, kb.y, kb.z, kb.w};
-#pragma unroll
-        for (int sidx = 0; sidx < 4; ++sidx) {
-          uint32_t b0, b1;
-          if (KDITHER) {
-            const uint32_t wx = words[sidx] ^ 0x80808080u;
-            b0 = s8x2_to_f16x2(wx, 0);
-            b1 = s8x2_to_f16x2(wx, 1);
-          } else {
-            b0 = e4m3x2_to_f16x2(words[sidx] & 0xFFFFu);
-            b1 = e4m3x2_to_f16x2(words[sidx] >> 16);
-          }
-          const int kb_i = 4 * jj + sidx;
-          mma_f16(S[nt], f.hi[kb_i][0], f.hi[kb_i][1], b0, b1);
-          if (f.has_lo) mma_f16(S[nt], f.lo[kb_i][0], f.lo[kb_i][1], b0, b1);
-          if (KDITHER) {
-            // subtract q . xi: dither of token 8nt + g, channels 64jj + 16c + 4sidx + {0..3}
-            const uint32_t slot = phys * kPage + 8 * nt + g;
-            const uint32_t grp = 16 * jj + 4 * c + sidx;
-            const float4 d = dither4(slot, pl.layer, static_cast<uint32_t>(kvh), grp, pl.seed_lo, pl.seed_hi);
-            const uint32_t nb0 = pack_f16(-d.x, -d.y), nb1 = pack_f16(-d.z, -d.w);
-            mma_f16(S[nt], f.hi[kb_i][0], f.hi[kb_i][1], nb0, nb1);
-            if (VDITHER) {
-              // stage the dither for the value side (token-major fp16 tile, 16-byte chunks xor-swizzled)
-              const int row = 8 * nt + g;
-              const int ch = 64 * jj + 16 * c + 4 * sidx;
-              const int chunk = (ch >> 3) ^ (row & 7);
-              uint2 w2;
-              w2.x = pack_f16(d.x, d.y);
-              w2.y = pack_f16(d.z, d.w);
-              *reinterpret_cast<uint2*>(xi_tile + row * 256 + chunk * 16 + (ch & 7) * 2) = w2;
-            }
+      for (int sidx = 0; sidx < 4; ++sidx) {
+        uint32_t a0, a1, a2, a3;
+        if (KDITHER) {
+          const uint32_t x0 = w0[sidx] ^ 0x80808080u, x1 = w1[sidx] ^ 0x80808080u;
+          a0 = s8x2_to_f16x2(x0, 0); a2 = s8x2_to_f16x2(x0, 1);
+          a1 = s8x2_to_f16x2(x1, 0); a3 = s8x2_to_f16x2(x1, 1);
+        } else {
+          a0 = e4m3x2_to_f16x2(w0[sidx] & 0xFFFFu); a2 = e4m3x2_to_f16x2(w0[sidx] >> 16);
+          a1 = e4m3x2_to_f16x2(w1[sidx] & 0xFFFFu); a3 = e4m3x2_to_f16x2(w1[sidx] >> 16);
+        }
+        const int kb = 4 * jj + sidx;
+        mma_f16_4(S, a0, a1, a2, a3, f.hi[kb][0], f.hi[kb][1]);
+        if (f.has_lo) mma_f16_4(S, a0, a1, a2, a3, f.lo[kb][0], f.lo[kb][1]);
+        if (KDITHER) {
+          // subtract xi . q: the dither of tokens g and g + 8, channels 64jj + 16c + 4sidx + {0..3}
+          const uint32_t grp = 16 * jj + 4 * c + sidx;
+          const float4 d0 = dither4(phys * kPage + g, pl.layer, static_cast<uint32_t>(kvh), grp, pl.seed_lo,
+                                    pl.seed_hi);
+          const float4 d1 = dither4(phys * kPage + g + 8, pl.layer, static_cast<uint32_t>(kvh), grp, pl.seed_lo,
+                                    pl.seed_hi);
+          mma_f16_4(S, pack_f16(-d0.x, -d0.y), pack_f16(-d1.x, -d1.y), pack_f16(-d0.z, -d0.w),
+                    pack_f16(-d1.z, -d1.w), f.hi[kb][0], f.hi[kb][1]);
+          if (VDITHER) {
+            // stage the dither for the value side: token-major fp16 tile, 16-byte chunks xor-swizzled
+            const int ch = 64 * jj + 16 * c + 4 * sidx;
+            uint2 w2;
+            w2.x = pack_f16(d0.x, d0.y);
+            w2.y = pack_f16(d0.z, d0.w);
+            *reinterpret_cast<uint2*>(xi_tile + g * 256 + (((ch >> 3) ^ g) << 4) + (ch & 7) * 2) = w2;
+            w2.x = pack_f16(d1.x, d1.y);
+            w2.y = pack_f16(d1.z, d1.w);
+            *reinterpret_cast<uint2*>(xi_tile + (g + 8) * 256 + (((ch >> 3) ^ g) << 4) + (ch & 7) * 2) = w2;
           }
         }
       }
     }
   }
 
-  // ---------------- per-token scales of the lane's four columns (tokens 2c, 2c+1, 2c+8, 2c+9)
-  float sk[4] = {1.f, 1.f, 1.f, 1.f}, sv[4] = {1.f, 1.f, 1.f, 1.f};
+  // ---------------- per-token scales of tokens g and g + 8
+  float sk[2] = {1.f, 1.f}, sv[2] = {1.f, 1.f};
   if (fmt_has_scale(KF)) {
-    const uint2 w = lds64(st + L::ksOff + c * 8);
-    const float2 a0 = unpack_f16(w.x), a1 = unpack_f16(w.y);
-    sk[0] = a0.x; sk[1] = a0.y; sk[2] = a1.x; sk[3] = a1.y;
+    const float2 a = unpack_f16(*reinterpret_cast<const uint32_t*>(st + L::ksOff + 4 * g));
+    sk[0] = a.x; sk[1] = a.y;
   }
   if (fmt_has_scale(VF)) {
-    const uint2 w = lds64(st + L::vsOff + c * 8);
-    const float2 a0 = unpack_f16(w.x), a1 = unpack_f16(w.y);
-    sv[0] = a0.x; sv[1] = a0.y; sv[2] = a1.x; sv[3] = a1.y;
+    const float2 a = unpack_f16(*reinterpret_cast<const uint32_t*>(st + L::vsOff + 4 * g));
+    sv[0] = a.x; sv[1] = a.y;
   }
 
-  // ---------------- online softmax (log2 domain); v = 2 nt + e <-> token 8nt + 2c + e
-  bool valid[4];
+  // ---------------- online softmax (log2 domain).  v = 2r + h: token g + 8r, head 2c + h
+  const bool valid[2] = {g < nvalid, g + 8 < nvalid};
   float x[4];
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
-    const int tok = 8 * (v >> 1) + 2 * c + (v & 1);
-    valid[v] = tok < nvalid;
     float sc = qk_scale;
-    if (fmt_has_scale(KF)) sc *= sk[v];
-    x[v] = valid[v] ? S[v >> 1][v & 1] * sc : -INFINITY;
+    if (fmt_has_scale(KF)) sc *= sk[v >> 1];
+    x[v] = valid[v >> 1] ? S[v] * sc : -INFINITY;
   }
-  const float mx = row_max4(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
-  const float m_new = fmaxf(s.m, mx);
-  const float alpha = (m_new == -INFINITY) ? 1.f : ex2(s.m - m_new);
+  float alpha[2], mnew[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float mx = col_max8(fmaxf(x[h], x[2 + h]));
+    mnew[h] = fmaxf(s.m[h], mx);
+    alpha[h] = (mnew[h] == -INFINITY) ? 1.f : ex2(s.m[h] - mnew[h]);
+  }
   float p[4];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) p[v] = valid[v] ? ex2(x[v] - m_new) : 0.f;
-  s.l = s.l * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
-  if (__any_sync(kFull, alpha != 1.f)) {
+  for (int v = 0; v < 4; ++v) p[v] = valid[v >> 1] ? ex2(x[v] - mnew[v & 1]) : 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) { s.o[i][0] *= alpha; s.o[i][1] *= alpha; }
+  for (int h = 0; h < 2; ++h) {
+    s.l[h] = s.l[h] * alpha[h] + (p[h] + p[2 + h]);
+    s.m[h] = mnew[h];
   }
-  s.m = m_new;
+  if (__any_sync(kFull, (alpha[0] != 1.f) | (alpha[1] != 1.f))) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s.o[i][0] *= alpha[0]; s.o[i][1] *= alpha[1]; s.o[i][2] *= alpha[0]; s.o[i][3] *= alpha[1];
+    }
+  }
 
   // ---------------- meter (Tier A witness bound; Tier B dither certificate)
   if (METER) {
-    float Cm[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) { Cm[nt][0] = Cm[nt][1] = Cm[nt][2] = Cm[nt][3] = 0.f; }
+    float C[4] = {0.f, 0.f, 0.f, 0.f};
     const uint4 wb = lds128(st + L::wOff + lane * 16);
-    mma_f16(Cm[0], f.qn_hi[0], f.qn_hi[1], wb.x, wb.y);
-    mma_f16(Cm[0], f.qn_lo[0], f.qn_lo[1], wb.x, wb.y);
-    mma_f16(Cm[1], f.qn_hi[0], f.qn_hi[1], wb.z, wb.w);
-    mma_f16(Cm[1], f.qn_lo[0], f.qn_lo[1], wb.z, wb.w);
-    float cz[4], cv[4];
+    mma_f16_4(C, wb.x, wb.z, wb.y, wb.w, f.qn_hi[0], f.qn_hi[1]);
+    mma_f16_4(C, wb.x, wb.z, wb.y, wb.w, f.qn_lo[0], f.qn_lo[1]);
+    float cv[4], cz[4];
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      cv[v] = valid[v] ? Cm[v >> 1][v & 1] * f.cm_scale : 0.f;
-      cz[v] = valid[v] ? __fmaf_rn(cv[v], kLog2e, x[v]) : -INFINITY;
+      cv[v] = valid[v >> 1] ? C[v] * f.cm_scale : 0.f;
+      cz[v] = valid[v >> 1] ? __fmaf_rn(cv[v], kLog2e, x[v]) : -INFINITY;
     }
-    const float mz = row_max4(fmaxf(fmaxf(cz[0], cz[1]), fmaxf(cz[2], cz[3])));
-    const float mc_new = fmaxf(s.mc, mz);
-    if (mc_new != -INFINITY) {
-      float acc = 0.f;
 #pragma unroll
-      for (int v = 0; v < 4; ++v) acc += valid[v] ? ex2(cz[v] - mc_new) * one_minus_exp_neg(cv[v]) : 0.f;
-      s.sc = s.sc * ex2(s.mc - mc_new) + acc;
-      s.mc = mc_new;
+    for (int h = 0; h < 2; ++h) {
+      const float mz = col_max8(fmaxf(cz[h], cz[2 + h]));
+      const float mc_new = fmaxf(s.mc[h], mz);
+      if (mc_new != -INFINITY) {
+        const float t0 = valid[0] ? ex2(cz[h] - mc_new) * one_minus_exp_neg(cv[h]) : 0.f;
+        const float t1 = valid[1] ? ex2(cz[2 + h] - mc_new) * one_minus_exp_neg(cv[2 + h]) : 0.f;
+        s.sc[h] = s.sc[h] * ex2(s.mc[h] - mc_new) + (t0 + t1);
+        s.mc[h] = mc_new;
+      }
     }
     if (KDITHER && tier_b) {
-      float uz[4], uv[4];
+      float uv[4], uz[4];
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        uv[v] = valid[v] ? f.alpha_b * sk[v] : 0.f;
-        uz[v] = valid[v] ? __fmaf_rn(uv[v], kLog2e, x[v]) : -INFINITY;
+        uv[v] = valid[v >> 1] ? f.alpha_b[v & 1] * sk[v >> 1] : 0.f;
+        uz[v] = valid[v >> 1] ? __fmaf_rn(uv[v], kLog2e, x[v]) : -INFINITY;
       }
-      const float mu = row_max4(fmaxf(fmaxf(uz[0], uz[1]), fmaxf(uz[2], uz[3])));
-      const float mu_new = fmaxf(s.mu, mu);
-      if (mu_new != -INFINITY) {
-        float acc = 0.f;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) acc += valid[v] ? ex2(uz[v] - mu_new) * one_minus_exp_neg(uv[v]) : 0.f;
-        s.su = s.su * ex2(s.mu - mu_new) + acc;
-        s.mu = mu_new;
+      for (int h = 0; h < 2; ++h) {
+        const float mz = col_max8(fmaxf(uz[h], uz[2 + h]));
+        const float mu_new = fmaxf(s.mu[h], mz);
+        if (mu_new != -INFINITY) {
+          const float t0 = valid[0] ? ex2(uz[h] - mu_new) * one_minus_exp_neg(uv[h]) : 0.f;
+          const float t1 = valid[1] ? ex2(uz[2 + h] - mu_new) * one_minus_exp_neg(uv[2 + h]) : 0.f;
+          s.su[h] = s.su[h] * ex2(s.mu[h] - mu_new) + (t0 + t1);
+          s.mu[h] = mu_new;
+        }
       }
     }
   }
 
-  // ---------------- P . V (tensor cores).  A rows g = query heads, k = the page's 16 tokens.
+  // ---------------- O^T += V^T . P^T.  P'^T (B operand) = movmatrix of the S^T-shaped weights.
   float pw[4];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) pw[v] = valid[v] ? p[v] * (kPvShift * sv[v]) : 0.f;
-  // partial pages: zero the value codes of invalid tokens (their bytes may hold NaN patterns)
+  for (int v = 0; v < 4; ++v) pw[v] = valid[v >> 1] ? p[v] * (kPvShift * sv[v >> 1]) : 0.f;
+  // the A fragments carry tokens 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3): zero invalid ones
   const bool partial = nvalid < kPage;
+  const bool vt[4] = {2 * c < nvalid, 2 * c + 1 < nvalid, 2 * c + 8 < nvalid, 2 * c + 9 < nvalid};
   if (!fmt_is_16bit(VF)) {
-    const uint32_t a0 = pack_f16(pw[0], pw[1]), a2 = pack_f16(pw[2], pw[3]);
-    uint32_t mask = 0xFFFFFFFFu;
+    const uint32_t b0 = movmatrix_trans(pack_f16(pw[0], pw[1]));
+    const uint32_t b1 = movmatrix_trans(pack_f16(pw[2], pw[3]));
+    uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
     if (partial) {
-      mask = (valid[0] ? 0xFFu : 0u) | (valid[1] ? 0xFF00u : 0u) | (valid[2] ? 0xFF0000u : 0u) |
-             (valid[3] ? 0xFF000000u : 0u);
+      mlo = (vt[0] ? 0x00FF00FFu : 0u) | (vt[1] ? 0xFF00FF00u : 0u);
+      mhi = (vt[2] ? 0x00FF00FFu : 0u) | (vt[3] ? 0xFF00FF00u : 0u);
     }
 #pragma unroll
-    for (int m4 = 0; m4 < 4; ++m4) {
-      const uint4 vb = lds128(st + L::vOff + (m4 * 32 + lane) * 16);
-      const uint32_t words[4] = {vb.x & mask, vb.y & mask, vb.z & mask, vb.w & mask};
+    for (int mm = 0; mm < 4; ++mm) {
+      const uint4 vb = lds128(st + L::vOff + (mm * 32 + lane) * 16);
+      const uint32_t words[4] = {vb.x & mlo, vb.y & mhi, vb.z & mlo, vb.w & mhi};
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        uint32_t b0, b1;
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t u0 = words[2 * half], u1 = words[2 * half + 1];
+        uint32_t a0, a1, a2, a3;
         if (VDITHER) {
-          const uint32_t wx = words[r] ^ 0x80808080u;
-          b0 = s8x2_to_f16x2(wx, 0);
-          b1 = s8x2_to_f16x2(wx, 1);
+          const uint32_t x0 = u0 ^ 0x80808080u, x1 = u1 ^ 0x80808080u;
+          a0 = s8x2_to_f16x2(x0, 0); a1 = s8x2_to_f16x2(x0, 1);
+          a2 = s8x2_to_f16x2(x1, 0); a3 = s8x2_to_f16x2(x1, 1);
         } else {
-          b0 = e4m3x2_to_f16x2(words[r] & 0xFFFFu);
-          b1 = e4m3x2_to_f16x2(words[r] >> 16);
+          a0 = e4m3x2_to_f16x2(u0 & 0xFFFFu); a1 = e4m3x2_to_f16x2(u0 >> 16);
+          a2 = e4m3x2_to_f16x2(u1 & 0xFFFFu); a3 = e4m3x2_to_f16x2(u1 >> 16);
         }
-        mma_f16(s.o[4 * m4 + r], a0, a2, b0, b1);
+        mma_f16_4(s.o[2 * mm + half], a0, a1, a2, a3, b0, b1);
       }
     }
     if (VDITHER) {
-      // subtract p' . xi: B fragments of the dither tile via transposed 8x8 loads
+      // subtract xi^T . P'^T: A fragments of the dither tile by transposed 8x8 loads
       __syncwarp();
-      const uint32_t na0 = a0 ^ 0x80008000u, na2 = a2 ^ 0x80008000u;
+      const uint32_t nb0 = b0 ^ 0x80008000u, nb1 = b1 ^ 0x80008000u;
 #pragma unroll
-      for (int np = 0; np < 8; ++np) {
-        // matrices: (tokens 0-7, chunk 2np), (8-15, 2np), (0-7, 2np+1), (8-15, 2np+1)
+      for (int mt = 0; mt < 8; ++mt) {
+        // matrices: (tok 0-7, ch 16mt..+7), (tok 0-7, ch 16mt+8..), (tok 8-15, ch 16mt..), (tok 8-15, ch +8..)
         const int mat = lane >> 3, r8 = lane & 7;
-        const int row = ((mat & 1) << 3) + r8;
-        const int chunk = (2 * np + (mat >> 1)) ^ (row & 7);
+        const int row = ((mat >> 1) << 3) + r8;
+        const int chunk = (2 * mt + (mat & 1)) ^ (row & 7);
         uint32_t fr[4];
         ldmatrix_x4_trans(fr, xi_tile + row * 256 + chunk * 16);
-        mma_f16(s.o[2 * np], na0, na2, fr[0], fr[1]);
-        mma_f16(s.o[2 * np + 1], na0, na2, fr[2], fr[3]);
+        mma_f16_4(s.o[mt], fr[0], fr[1], fr[2], fr[3], nb0, nb1);
       }
     }
   } else {
-    const uint32_t h0 = pack_bf16(pw[0], pw[1]), h2 = pack_bf16(pw[2], pw[3]);
-    const float2 r0 = unpack_bf16(h0), r2 = unpack_bf16(h2);
-    const uint32_t l0 = pack_bf16(pw[0] - r0.x, pw[1] - r0.y), l2 = pack_bf16(pw[2] - r2.x, pw[3] - r2.y);
+    const uint32_t h01 = pack_bf16(pw[0], pw[1]), h23 = pack_bf16(pw[2], pw[3]);
+    const float2 r01 = unpack_bf16(h01), r23 = unpack_bf16(h23);
+    const uint32_t l01 = pack_bf16(pw[0] - r01.x, pw[1] - r01.y), l23 = pack_bf16(pw[2] - r23.x, pw[3] - r23.y);
+    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+    const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
     uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
     if (partial) {
-      mlo = (valid[0] ? 0xFFFFu : 0u) | (valid[1] ? 0xFFFF0000u : 0u);
-      mhi = (valid[2] ? 0xFFFFu : 0u) | (valid[3] ? 0xFFFF0000u : 0u);
+      mlo = (vt[0] ? 0xFFFFu : 0u) | (vt[1] ? 0xFFFF0000u : 0u);
+      mhi = (vt[2] ? 0xFFFFu : 0u) | (vt[3] ? 0xFFFF0000u : 0u);
     }
 #pragma unroll
-    for (int m8 = 0; m8 < 8; ++m8) {
-      const uint4 vb = lds128(st + L::vOff + (m8 * 32 + lane) * 16);
-      const uint32_t b00 = vb.x & mlo, b01 = vb.y & mhi, b10 = vb.z & mlo, b11 = vb.w & mhi;
-      mma_bf16(s.o[2 * m8], h0, h2, b00, b01);
-      mma_bf16(s.o[2 * m8], l0, l2, b00, b01);
-      mma_bf16(s.o[2 * m8 + 1], h0, h2, b10, b11);
-      mma_bf16(s.o[2 * m8 + 1], l0, l2, b10, b11);
+    for (int mt = 0; mt < 8; ++mt) {
+      const uint4 vb = lds128(st + L::vOff + (mt * 32 + lane) * 16);
+      const uint32_t a0 = vb.x & mlo, a1 = vb.y & mlo, a2 = vb.z & mhi, a3 = vb.w & mhi;
+      mma_bf16_4(s.o[mt], a0, a1, a2, a3, bh0, bh1);
+      mma_bf16_4(s.o[mt], a0, a1, a2, a3, bl0, bl1);
     }
   }
 }
@@ -622,19 +721,31 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
   }
 }
 
-__device__ __forceinline__ void flush(const Args& a, int warp_id, int unit, SoftState& s) {
+// Partial of one (warp, unit) piece: per real head, (m, l, mc, sc, mu, su) and the 128 O^T values.
+__device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftState& s) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const float l = row_sum4(s.l), sc = row_sum4(s.sc), su = row_sum4(s.su);
-  const size_t slot = static_cast<size_t>(warp_id) + unit;
-  if (g < a.G) {
-    float* acc = a.ws_acc + (slot * a.G + g) * kHeadDim;
+  float l[2], sc[2], su[2];
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-      *reinterpret_cast<float2*>(acc + 8 * nt + 2 * c) = make_float2(s.o[nt][0], s.o[nt][1]);
-    if (c == 0) {
-      float* st = a.ws_stats + (slot * a.G + g) * 8;
-      *reinterpret_cast<float4*>(st) = make_float4(s.m, l, s.mc, sc);
-      *reinterpret_cast<float4*>(st + 4) = make_float4(s.mu, su, 0.f, 0.f);
+  for (int h = 0; h < 2; ++h) {
+    l[h] = col_sum8(s.l[h]);
+    sc[h] = col_sum8(s.sc[h]);
+    su[h] = col_sum8(s.su[h]);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int head = 2 * c + h;
+    if (head < a.G) {
+      float* acc = a.ws_acc + (slot * a.G + head) * kHeadDim;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        acc[16 * mt + g] = s.o[mt][h];
+        acc[16 * mt + g + 8] = s.o[mt][2 + h];
+      }
+      if (g == 0) {
+        float* st = a.ws_stats + (slot * a.G + head) * 8;
+        *reinterpret_cast<float4*>(st) = make_float4(s.m[h], l[h], s.mc[h], sc[h]);
+        *reinterpret_cast<float4*>(st + 4) = make_float4(s.mu[h], su[h], 0.f, 0.f);
+      }
     }
   }
 }
@@ -642,6 +753,8 @@ __device__ __forceinline__ void flush(const Args& a, int warp_id, int unit, Soft
 template <int KF, int VF, int PKF, int PVF, bool METER>
 __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // let the merge grid (programmatic dependent launch) be scheduled as soon as SMs free up
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr bool K16 = fmt_is_16bit(KF);
   constexpr bool XI = (KF == KVQ_FMT_INT8_DITHER && VF == KVQ_FMT_INT8_DITHER);
   int32_t* cum = reinterpret_cast<int32_t*>(smem);
@@ -734,7 +847,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args
     const uint32_t info = __shfl_sync(kFull, cur.info, j & 31);
     const int u = d_unit(info);
     if (u != unit) {
-      if (unit >= 0) { flush(a, wid, unit, s); reset_state(s); }
+      if (unit >= 0) { write_piece(a, static_cast<size_t>(wid) + unit, s); reset_state(s); }
       unit = u;
       const int seq = u / a.Hkv, kvh = u % a.Hkv;
       const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
@@ -777,7 +890,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args
       (void)mbar_wait(&bars[k % a.stages], static_cast<uint32_t>((k / a.stages) & 1));
     return;
   }
-  if (unit >= 0) flush(a, wid, unit, s);
+  if (unit >= 0) write_piece(a, static_cast<size_t>(wid) + unit, s);
 }
 
 }  // namespace dec

@@ -34,9 +34,10 @@ constexpr int kTileBytesS = 32;
 
 // ---------------------------------------------------------------------------------------------
 // Tile layouts (byte offsets inside one (page, kv head) tile; see include/kvq.h).
-// i(t) orders the four tokens a tensor-core lane holds in a P*V fragment: 2c, 2c+1, 2c+8, 2c+9.
-__host__ __device__ __forceinline__ int tok_quad_index(int t) { return (t & 1) + 2 * (t >> 3); }
-
+// K tiles hold, per 16-byte word, one token and 8 (16-bit) or 16 (8-bit) consecutive channels:
+// the A fragments of S^T = K . Q^T.  V tiles hold, per lane of a 16-channel block, the tokens
+// 2c, 2c+1, 2c+8, 2c+9 of channels g and g+8: the A fragments of O^T = V^T . P^T.  Scales hold
+// tokens t and t+8 side by side (the two tokens a lane owns in S^T).
 __host__ __device__ __forceinline__ int k16_offset(int t, int c) {
   return 16 * ((((t >> 3) * 4 + (c >> 5)) * 32) + (t & 7) * 4 + ((c >> 3) & 3)) + 2 * (c & 7);
 }
@@ -44,15 +45,16 @@ __host__ __device__ __forceinline__ int k8_offset(int t, int c) {
   return 16 * ((((t >> 3) * 2 + (c >> 6)) * 32) + (t & 7) * 4 + ((c >> 4) & 3)) + (c & 15);
 }
 __host__ __device__ __forceinline__ int v16_offset(int t, int c) {
-  return 16 * (((c >> 4) * 32) + 4 * (c & 7) + ((t & 7) >> 1)) + 8 * ((c >> 3) & 1) + 2 * tok_quad_index(t);
+  return 16 * (32 * (c >> 4) + 4 * (c & 7) + ((t & 7) >> 1)) + 4 * (2 * (t >> 3) + ((c >> 3) & 1)) + 2 * (t & 1);
 }
 __host__ __device__ __forceinline__ int v8_offset(int t, int c) {
-  return 16 * (((c >> 5) * 32) + 4 * (c & 7) + ((t & 7) >> 1)) + 4 * ((c >> 3) & 3) + tok_quad_index(t);
+  return 16 * (32 * (c >> 5) + 4 * (c & 7) + ((t & 7) >> 1)) + 8 * ((c >> 4) & 1) +
+         2 * (2 * (t >> 3) + ((c >> 3) & 1)) + (t & 1);
 }
 __host__ __device__ __forceinline__ int w_offset(int t, int b) {
   return 16 * (4 * (t & 7) + (b >> 2)) + 8 * (t >> 3) + 2 * (b & 3);
 }
-__host__ __device__ __forceinline__ int s_offset(int t) { return 2 * (4 * ((t & 7) >> 1) + tok_quad_index(t)); }
+__host__ __device__ __forceinline__ int s_offset(int t) { return 2 * (2 * (t & 7) + (t >> 3)); }
 
 // ---------------------------------------------------------------------------------------------
 // Device error word: the first error code wins.

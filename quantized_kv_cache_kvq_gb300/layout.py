@@ -10,10 +10,6 @@ import numpy as np
 __all__ = ["k_offsets", "v_offsets", "w_offsets", "s_offsets", "unpack_k", "unpack_v", "unpack_w", "unpack_s"]
 
 
-def _i(t):
-    return (t & 1) + 2 * (t >> 3)
-
-
 def k_offsets(fmt: str) -> np.ndarray:
     """[16 tokens, 128 channels] byte offsets in a K tile."""
     t = np.arange(16)[:, None]
@@ -27,8 +23,9 @@ def v_offsets(fmt: str) -> np.ndarray:
     t = np.arange(16)[:, None]
     c = np.arange(128)[None, :]
     if fmt == "bf16":
-        return 16 * (((c >> 4) * 32) + 4 * (c & 7) + ((t & 7) >> 1)) + 8 * ((c >> 3) & 1) + 2 * _i(t)
-    return 16 * (((c >> 5) * 32) + 4 * (c & 7) + ((t & 7) >> 1)) + 4 * ((c >> 3) & 3) + _i(t)
+        return 16 * (32 * (c >> 4) + 4 * (c & 7) + ((t & 7) >> 1)) + 4 * (2 * (t >> 3) + ((c >> 3) & 1)) + 2 * (t & 1)
+    return (16 * (32 * (c >> 5) + 4 * (c & 7) + ((t & 7) >> 1)) + 8 * ((c >> 4) & 1)
+            + 2 * (2 * (t >> 3) + ((c >> 3) & 1)) + (t & 1))
 
 
 def w_offsets() -> np.ndarray:
@@ -39,7 +36,7 @@ def w_offsets() -> np.ndarray:
 
 def s_offsets() -> np.ndarray:
     t = np.arange(16)
-    return 2 * (4 * ((t & 7) >> 1) + _i(t))
+    return 2 * (2 * (t & 7) + (t >> 3))
 
 
 def _gather16(tiles: np.ndarray, offs: np.ndarray) -> np.ndarray:

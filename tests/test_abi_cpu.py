@@ -119,27 +119,33 @@ def test_decode_fragment_reads_are_contiguous_and_conflict_free():
             starts = [ko8[8 * nt + gg, 64 * jj + 16 * cc] for gg, cc in zip(g, c)]
             assert starts == [((nt * 2 + jj) * 32 + L_) * 16 for L_ in lanes]
             assert all(ko8[8 * nt + gg, 64 * jj + 16 * cc + e] == s + e for gg, cc, s in zip(g, c, starts) for e in range(16))
-    # V 8-bit: read m gives lane (g, c), n-tile 4m+r, channel 8(4m+r)+g, tokens 2c, 2c+1, 2c+8, 2c+9
+    # V 8-bit: read mm gives lane (g, c) the A fragments of V^T for channel blocks 2mm and 2mm+1:
+    # per block, tokens (2c, 2c+1) then (2c+8, 2c+9), each at channel g then g + 8
     vo = L.v_offsets("e4m3")
-    toks = lambda cc: [2 * cc, 2 * cc + 1, 2 * cc + 8, 2 * cc + 9]
-    for m in range(4):
-        for r in range(4):
+    for mm in range(4):
+        for half in range(2):
+            mt = 2 * mm + half
             for gg, cc, L_ in zip(g, c, lanes):
-                ch = 8 * (4 * m + r) + gg
-                assert [vo[t, ch] for t in toks(cc)] == [(m * 32 + L_) * 16 + 4 * r + i for i in range(4)]
-    # V 16-bit: read m gives n-tiles 2m, 2m+1
+                base = (mm * 32 + L_) * 16 + 8 * half
+                order = [(2 * cc, 16 * mt + gg), (2 * cc + 1, 16 * mt + gg), (2 * cc, 16 * mt + gg + 8),
+                         (2 * cc + 1, 16 * mt + gg + 8), (2 * cc + 8, 16 * mt + gg), (2 * cc + 9, 16 * mt + gg),
+                         (2 * cc + 8, 16 * mt + gg + 8), (2 * cc + 9, 16 * mt + gg + 8)]
+                assert [vo[t, ch] for t, ch in order] == [base + i for i in range(8)]
+    # V 16-bit: read mt gives the same eight values of channel block mt as 16-bit elements
     vo16 = L.v_offsets("bf16")
-    for m in range(8):
-        for r in range(2):
-            for gg, cc, L_ in zip(g, c, lanes):
-                ch = 8 * (2 * m + r) + gg
-                assert [vo16[t, ch] for t in toks(cc)] == [(m * 32 + L_) * 16 + 8 * r + 2 * i for i in range(4)]
+    for mt in range(8):
+        for gg, cc, L_ in zip(g, c, lanes):
+            base = (mt * 32 + L_) * 16
+            order = [(2 * cc, 16 * mt + gg), (2 * cc + 1, 16 * mt + gg), (2 * cc, 16 * mt + gg + 8),
+                     (2 * cc + 1, 16 * mt + gg + 8), (2 * cc + 8, 16 * mt + gg), (2 * cc + 9, 16 * mt + gg),
+                     (2 * cc + 8, 16 * mt + gg + 8), (2 * cc + 9, 16 * mt + gg + 8)]
+            assert [vo16[t, ch] for t, ch in order] == [base + 2 * i for i in range(8)]
     # witness: lane reads chunk L: tokens g (+8 for the second half), bands 4c..4c+3
     wo = L.w_offsets()
     for gg, cc, L_ in zip(g, c, lanes):
         for nt in range(2):
             assert [wo[8 * nt + gg, 4 * cc + i] for i in range(4)] == [L_ * 16 + 8 * nt + 2 * i for i in range(4)]
-    # scales: lane c reads 8 bytes at 8c: tokens 2c, 2c+1, 2c+8, 2c+9
+    # scales: lane (g, c) reads 4 bytes at 4g: tokens g and g + 8
     so = L.s_offsets()
-    for cc in range(4):
-        assert [so[t] for t in toks(cc)] == [8 * cc + 2 * i for i in range(4)]
+    for gg in range(8):
+        assert [so[gg], so[gg + 8]] == [4 * gg, 4 * gg + 2]
