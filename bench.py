@@ -51,6 +51,7 @@ def parse():
     p.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
     p.add_argument("--layers", type=int, default=0, help="override layer count (profiling only; not a bench line)")
     return p.parse_args()
 
@@ -293,17 +294,35 @@ def run_gpu(args, w):
     for _ in range(args.warmup):
         m.step()
     barrier()
-    events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(m.L)]
-              for _ in range(args.steps)]
+    graph = None
+    if not args.eager:
+        # the whole step (append + decode + merge per layer, meter) as one CUDA graph
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            m.step()
+        for _ in range(args.warmup):
+            graph.replay()
+        barrier()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
         start.record()
         for s in range(args.steps):
-            m.step(events=events[s])
+            if graph is not None:
+                graph.replay()
+            else:
+                m.step()
         stop.record()
         barrier()
     ms = start.elapsed_time(stop)
+    # per-launch duration of kvq_decode_attn: CUDA events around every layer's call, eager steps
+    n_ev = max(1, min(args.steps, 20))
+    events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(m.L)]
+              for _ in range(n_ev)]
+    barrier()
+    for s in range(n_ev):
+        m.step(events=events[s])
+    barrier()
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -318,18 +337,18 @@ def run_gpu(args, w):
     peak, peak_kind = measured_peaks()
     tr = traffic_record(w.name)
     attended = float(np.sum(m.lens) + w.prefix_len * w.batch) * m.L * w.n_kv_heads
-    res = dict(value=value, ms_step=ms_step, achieved=achieved, layer_ms_mean=statistics.mean(layer_ms),
+    res = dict(value=value, ms_step=ms_step, achieved=achieved, graph=graph is not None, layer_ms_mean=statistics.mean(layer_ms),
                layer_ms_median=statistics.median(layer_ms), peak=peak, peak_kind=peak_kind, traffic=tr,
                clocks=clk.summary(), launches=m.launches_per_step() * args.steps, attended=attended,
                per_step_bytes=per_step_bytes, world=world, rank=rank, counts=m.counts.cpu().tolist())
     if not args.no_e2e:
-        res["e2e"] = run_e2e(args, m, per_step_bytes, world)
+        res["e2e"] = run_e2e(args, m, per_step_bytes, world, use_graph=graph is not None)
     if world > 1:
         torch.distributed.destroy_process_group()
     return res
 
 
-def run_e2e(args, m, per_step_bytes, world):
+def run_e2e(args, m, per_step_bytes, world, use_graph=True):
     """Same metric through the public API with pinned host buffers and copies in the timed region."""
     torch = m.torch
     hq = torch.empty(m.q.shape, dtype=m.q.dtype, pin_memory=True).copy_(m.q)
@@ -339,12 +358,20 @@ def run_e2e(args, m, per_step_bytes, world):
     hm = torch.empty(m.meter_a.shape, dtype=m.meter_a.dtype, pin_memory=True)
     hc = torch.empty(4, dtype=torch.int32, pin_memory=True)
     dq, dk, dv = torch.empty_like(m.q), torch.empty_like(m.k_new), torch.empty_like(m.v_new)
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            m.step(dq, dk, dv)
 
     def one():
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
-        m.step(dq, dk, dv)
+        if graph is not None:
+            graph.replay()
+        else:
+            m.step(dq, dk, dv)
         ho.copy_(m.out, non_blocking=True)
         hm.copy_(m.meter_a, non_blocking=True)
         hc.copy_(m.counts, non_blocking=True)
@@ -481,7 +508,8 @@ def main():
                          "peak_source": f"{r['peak_kind']} hbm_gbs",
                          "algorithmic_bytes_per_launch": r["per_step_bytes"] // (args.layers or w.n_layers),
                          "launch_ms_mean": r["layer_ms_mean"]},
-            "gpu_launches": r["launches"], "clocks": r["clocks"], "meter_counts": r["counts"]}
+            "gpu_launches": r["launches"], "clocks": r["clocks"], "meter_counts": r["counts"],
+            "launch_mode": "cuda_graph" if r["graph"] else "eager"}
     if "e2e" in r:
         line["e2e"] = r["e2e"]
     if args.layers:
