@@ -193,6 +193,36 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int3
                            int32_t* err_word_dev, kvq_stream_t stream);
 
 /*
+ * kvq_decode_attn_noalloc -- kvq_decode_attn without a caller-provided
+ * workspace.  No counterpart on the source pages: it exists for callers that
+ * cannot allocate device memory for scratch -- a plugin or embedding host
+ * that owns every device allocation and passes the library only its inputs
+ * and outputs, or a serving loop whose memory is planned up front and that
+ * must not allocate on the request path.
+ *
+ * Arguments, outputs and device errors are those of kvq_decode_attn.  The
+ * scratch is a file-scope device array of KVQ_STATIC_WORKSPACE_BYTES (16 MiB)
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  The first call on a device looks up that array's device
+ * address (with that device current), so make the first call on each device
+ * before any stream capture.  Calls whose workspace need
+ * (kvq_decode_workspace_size) exceeds KVQ_STATIC_WORKSPACE_BYTES return
+ * KVQ_ERR_WORKSPACE_TOO_SMALL without enqueuing work.  The call itself
+ * allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
+ * All calls share the one array and it keeps the last call's contents; the
+ * decode writes every scratch value before reading it, so nothing needs
+ * clearing between calls.  Calls that overlap on the GPU (different streams,
+ * or different host threads) race on the array: serialise them.
+ */
+#define KVQ_STATIC_WORKSPACE_BYTES (16u << 20)
+kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_cache* prefix, int32_t prefix_len,
+                                   const void* q_dev, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
+                                   const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                                   const int32_t* seq_lens_dev, float sm_scale, const kvq_meter_params* meter,
+                                   float* out_dev, float* meter_state_dev, int32_t* err_word_dev,
+                                   kvq_stream_t stream);
+
+/*
  * kvq_meter -- meter finalisation and telemetry on the device ([W] Sec. 4.3;
  * Sec. 6.2.4 "Certificate telemetry in production": aggregate on the GPU,
  * count non-finite values separately).

@@ -1,6 +1,7 @@
 // decode.cu -- kvq_decode_attn / kvq_decode_workspace_size: argument checks, workspace layout,
 // shared-memory stage sizing, and dispatch to the decode and merge kernels.
 #include <cmath>
+#include <mutex>
 
 #include "decode_kernel.cuh"
 
@@ -309,4 +310,44 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* p
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, merge_kernel, a) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+// kvq_decode_attn_noalloc: kvq_decode_attn with its scratch in a file-scope device array, for
+// callers that can hand the library only inputs and outputs (see include/kvq.h).  The array is a
+// device symbol: its host-side name is not a device address, so the address is looked up once per
+// device with cudaGetSymbolAddress while that device is current, and that address is what the
+// kernels receive.
+static __device__ __align__(256) uint8_t g_kvq_static_workspace[KVQ_STATIC_WORKSPACE_BYTES];
+
+namespace {
+void* g_static_ws_addr[kMaxDevices] = {nullptr};
+std::mutex g_static_ws_mutex;
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_cache* prefix, int32_t prefix_len,
+                                              const void* q, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
+                                              const int32_t* block_table, int32_t max_pages_per_seq,
+                                              const int32_t* seq_lens, float sm_scale, const kvq_meter_params* mp,
+                                              float* out, float* meter_state, int32_t* err_word, kvq_stream_t stream) {
+  if (!cache || cache->num_kv_heads <= 0) return KVQ_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+    if (!g_static_ws_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_kvq_static_workspace) != cudaSuccess || !p) return KVQ_ERR_CUDA;
+      g_static_ws_addr[dev] = p;
+    }
+    ws = g_static_ws_addr[dev];
+  }
+  if (batch > 0) {
+    const size_t need = kvq_decode_workspace_size(batch, cache->num_kv_heads, num_q_heads);
+    if (need == 0) return KVQ_ERR_INVALID_ARG;
+    if (need > KVQ_STATIC_WORKSPACE_BYTES) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  }
+  return kvq_decode_attn(cache, prefix, prefix_len, q, q_dtype, batch, num_q_heads, block_table, max_pages_per_seq,
+                         seq_lens, sm_scale, mp, out, meter_state, ws, KVQ_STATIC_WORKSPACE_BYTES, err_word, stream);
 }
