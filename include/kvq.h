@@ -161,9 +161,9 @@ size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t nu
  * kvq_decode_attn -- one decode step of one layer: split-KV paged GQA
  * attention over [shared prefix ++ live suffix] with one online-softmax state
  * per sequence and query head, the meter accumulated in the same pass, and a
- * log-sum-exp merge of the splits ([W] Sec. 6.2.2 "the certificate shares the
- * split-KV reduction with the output"; [C] "One kernel spans cartridge and
- * live KV").
+ * log-sum-exp merge of the splits ([W] Sec. 6.2.2: the certificate, like the
+ * output, is a p~-weighted average, so both merge under the same weights;
+ * [C] "One kernel spans cartridge and live KV").
  *
  * cache: the layer's live paged cache.  prefix (nullable): a shared dense
  *   prefix of prefix_len tokens stored in pages 0, 1, ... of its own cache

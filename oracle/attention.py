@@ -6,9 +6,9 @@ Everything is float64 and follows WitCert (arXiv 2607.28699):
   the S cached tokens from exact and compressed keys; the metered quantity is
   TV(p, p~) = 1/2 sum_t |p_t - p~_t|, reported as min(1, .) because TV <= 1.
 * §3 Theorem 1: with A = E_p~[e^{c}] and |eps_t| <= c_t, TV <= 1/2 (A^2 - 1).
-  "evaluate A in the log domain and return the trivial bound 1 on overflow;
-  we never truncate the error parameter": here the meter state is ln(A - 1),
-  computed by log-sum-exp, so it never overflows.
+  The page evaluates A in the log domain, returns 1 when it overflows and
+  leaves c itself untouched: here the meter state is ln(A - 1), computed by
+  log-sum-exp, so it never overflows and c is never clipped.
 * §4.1 Theorem 2: c_t = (1/sqrt(d)) sum_b ||q_b|| w_{t,b} (the kernel form uses
   sm_scale in place of 1/sqrt(d)); w is the stored fp16 witness.
 * §4.2: Tier B radius u_t = sqrt(2 varsigma_t^2 log(2S/delta_loc)) with

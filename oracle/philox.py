@@ -5,9 +5,9 @@ Source passages
 * WitCert §6.2.1: the dither of the quantizer is drawn by Philox4x32-10 [Salmon
   et al., SC'11] from a counter built from the cache coordinates, so that the
   read side regenerates exactly the dither the write side used.
-* WitCert §6.2.3 ("The dither counter uses the slot, not the sequence
-  position"): the tuple is (layer, kv_head, slot, channel); slots are stable
-  under paging and prefix sharing.
+* WitCert §6.2.3 (storage side): the counter tuple is (layer, kv_head, slot,
+  channel) -- the physical slot rather than the sequence position, because a
+  written slot never changes under paging or prefix sharing.
 * WitCert §4.2: the dither is uniform on [-1/2, 1/2).
 
 Generator (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as

@@ -17,7 +17,7 @@
 // logit, c_t = sm_scale * sum_b ||q_b|| w_{t,b}, the kernel accumulates
 //     A - 1 = sum_t e^{x_t} (e^{c_t} - 1) / sum_t e^{x_t} = sum_t e^{x_t + c_t} (1 - e^{-c_t}) / sum_t e^{x_t}
 // as a running maximum and a scaled sum of e^{x_t + c_t - max} (1 - e^{-c_t}), i.e. in the log
-// domain ("we never truncate the error parameter"); Tier B does the same with
+// domain, so c is never clipped and A never overflows; Tier B does the same with
 // u_t = sm_scale ||q|| s_t sqrt(2 ln(2S/delta_loc) / 12).
 #pragma once
 

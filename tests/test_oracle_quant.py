@@ -2,7 +2,7 @@
 
 What pins what:
 * INT8 dither: |x_hat - x| <= s/2 (up to the binary32 rounding of x/s + xi)
-  and no code clips (WitCert §4.2, §6.2.1 "zero clipping", "|err| <= s/2");
+  and no code clips (WitCert §4.2 and the §6.2.1 acceptance items);
   the scale is the fp16 rounding of amax/126.5 (closed form); the stored scale
   is the one quantized with (a row whose amax makes fp32 and fp16 scales differ).
 * E4M3 scaled: reconstruction error <= half an E4M3 step at each value.
