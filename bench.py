@@ -169,11 +169,7 @@ class Model:
         B, Hkv, Hq = w.batch, w.n_kv_heads, w.n_q_heads
         self.lens = W.seq_lengths(w)
         pages = (self.lens + W.PAGE - 1) // W.PAGE
-        max_pages = int(pages.max())
-        if w.random_pages:
-            bt = W.permuted_block_table(self.lens, W.unit_seed(w, 424_242), max_pages)
-        else:
-            bt = W.identity_block_table(self.lens, max_pages)
+        bt = W.block_table_for(w, self.lens)
         self.num_pages = int(pages.sum())
         self.bt = torch.from_numpy(bt).to(device)
         self.seq_lens = torch.from_numpy(self.lens.astype(np.int32)).to(device)
@@ -184,8 +180,6 @@ class Model:
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         g = torch.Generator(device=device)
         self.caches, self.prefixes = [], []
-        theta = w.rope_theta
-        inv = torch.tensor(theta ** (-2.0 * np.arange(64) / 128), dtype=torch.float64, device=device)
         total = int(self.lens.sum())
         pos = torch.cat([torch.arange(w.prefix_len, w.prefix_len + int(n), device=device) for n in self.lens])
         slots = torch.cat([torch.from_numpy(W.slot_mapping(bt, s, np.arange(n))) for s, n in
@@ -194,16 +188,16 @@ class Model:
             g.manual_seed(W.unit_seed(w, 100_000 + 1000 * seed_base + l))
             c = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, self.num_pages, layer=l,
                                seed=(0x5EED << 20) + 97 * l + seed_base)
-            chunk = 1 << 20
+            chunk = 1 << 18
             for a in range(0, total, chunk):
                 b = min(total, a + chunk)
-                k, v = self._gen(g, b - a, pos[a:b], inv, l)
+                k, v = W.gen_tokens_gpu(w, l, pos[a:b], g, device)
                 kvq.append(c, k, v, slots[a:b].contiguous(), self.err)
             self.caches.append(c)
             if w.prefix_len:
                 p = kvq.PagedCache(w.prefix_k_fmt, w.prefix_v_fmt, Hkv, (w.prefix_len + 15) // 16, layer=l,
                                    seed=(0xCA47 << 20) + l)
-                k, v = self._gen(g, w.prefix_len, torch.arange(w.prefix_len, device=device), inv, l, sink=True)
+                k, v = W.gen_tokens_gpu(w, l, torch.arange(w.prefix_len, device=device), g, device, sink=True)
                 kvq.append(p, k, v, torch.arange(w.prefix_len, dtype=torch.int32, device=device), self.err)
                 self.prefixes.append(p)
             else:
@@ -228,24 +222,6 @@ class Model:
         torch.cuda.synchronize()
         if self.err.item() != 0:
             raise RuntimeError(f"append reported {kvq.STATUS.get(self.err.item())}")
-
-    def _gen(self, g, n, pos, inv, layer, sink=False):
-        torch, w = self.torch, self.w
-        Hkv = w.n_kv_heads
-        k = torch.randn((n, Hkv, 128), generator=g, device=self.dev, dtype=torch.float32)
-        v = torch.randn((n, Hkv, 128), generator=g, device=self.dev, dtype=torch.float32)
-        if sink and w.sink_scale != 1.0:
-            k[0] *= w.sink_scale
-            v[0] *= w.sink_scale
-        for h in range(Hkv):
-            ch = W.outlier_channels(w, layer, h)
-            if ch.size:
-                k[:, h, torch.from_numpy(ch).to(self.dev)] *= w.outlier_scale
-        ang = pos.to(torch.float64)[:, None] * inv[None, :]
-        cos, sin = torch.cos(ang).float()[:, None, :], torch.sin(ang).float()[:, None, :]
-        a, b = k[..., :64], k[..., 64:]
-        k = torch.cat([a * cos - b * sin, b * cos + a * sin], dim=-1).contiguous()
-        return k, v
 
     def step(self, q=None, k_new=None, v_new=None, events=None):
         kvq, w = self.kvq, self.w

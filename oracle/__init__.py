@@ -23,7 +23,7 @@ meter      meter finalisation, coverage and per-request risk ranking
 bytes      byte account per layout and per workload
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in
-``tests/test_oracle_*.py`` except the Philox stream's agreement with an external
-implementation, which is pinned only where the CUDA toolkit's own Philox
-generator can be run (a GPU test); see ``oracle/philox.py``.
+``tests/test_oracle_*.py``; the Philox generator is additionally pinned word for
+word to the CUDA toolkit's own Philox4x32-10 by a GPU test (see
+``oracle/philox.py``).
 """

@@ -35,11 +35,11 @@ so each call serves four consecutive channels, xi lies on the 2**24-point
 mid-point grid of (-1/2, 1/2) (symmetric, mean exactly 0, every value exact in
 binary32), and the key and value planes of a token share the same xi.
 
-Parity status: agreement of ``philox4x32_10`` with an implementation outside
-this repository is pinned only by a GPU test against the CUDA toolkit's own
-Philox4x32-10 generator (cuRAND device API); on CPU it is pinned by properties
-(bijectivity through an independently written inverse, uniformity and
-independence statistics, avalanche).
+Parity status: pinned.  ``philox4x32_10`` agrees word for word with the CUDA
+toolkit's own Philox4x32-10 generator (cuRAND device API, four seeds, seven
+subsequences; tests/test_gpu_philox_pin.py).  On CPU it is further pinned by
+properties (bijectivity through an independently written inverse, uniformity
+and independence statistics, avalanche).
 """
 from __future__ import annotations
 

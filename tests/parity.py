@@ -56,10 +56,12 @@ def _oracle_quant_rows(x32, fmt, xi):
     return codes, sb, xh, valid
 
 
-def oracle_cache_rows(k32, v32, slots, k_fmt, v_fmt, seed, layer):
-    """Oracle quantization of tokens [n, Hkv, 128] written at ``slots`` [n]."""
+def oracle_cache_rows(k32, v32, slots, k_fmt, v_fmt, seed, layer, heads=None):
+    """Oracle quantization of tokens [n, Hkv, 128] written at ``slots`` [n].
+
+    ``heads``: kv-head index of each column of the inputs (defaults to 0..Hkv-1); it keys the dither."""
     n, Hkv, _ = k32.shape
-    heads = np.arange(Hkv)[None, :, None]
+    heads = (np.arange(Hkv) if heads is None else np.asarray(heads))[None, :, None]
     xi = dither(seed, layer, heads, np.asarray(slots)[:, None, None], np.arange(128)[None, None, :])
     kc, ksb, kh, kval = _oracle_quant_rows(k32, k_fmt, xi)
     vc, vsb, vh, vval = _oracle_quant_rows(v32, v_fmt, xi)

@@ -41,6 +41,8 @@ __all__ = [
     "identity_block_table",
     "permuted_block_table",
     "slot_mapping",
+    "gen_tokens_gpu",
+    "block_table_for",
 ]
 
 HEAD_DIM = 128
@@ -202,3 +204,41 @@ def slot_mapping(block_table: np.ndarray, seq: int, positions: np.ndarray) -> np
 def reduced(w: Workload, **kw) -> Workload:
     """A smaller copy of a workload (parity cases that the oracle finishes in seconds)."""
     return replace(w, **kw)
+
+
+def block_table_for(w: Workload, lens, layer_seed: int = 0) -> np.ndarray:
+    """The block table a workload uses: identity, or a seeded permutation of the physical pages."""
+    pages = (np.asarray(lens) + PAGE - 1) // PAGE
+    max_pages = max(1, int(pages.max(initial=1)))
+    if w.random_pages:
+        return permuted_block_table(lens, unit_seed(w, 424_242 + layer_seed), max_pages)
+    return identity_block_table(lens, max_pages)
+
+
+def gen_tokens_gpu(w: Workload, layer: int, positions, generator, device, sink: bool = False):
+    """Binary32 post-RoPE K and V [n, Hkv, 128] on the GPU for the given absolute positions.
+
+    Same recipe as ``gen_unit_cpu`` (N(0,1) pre-RoPE, optional x10 sink at position 0, outlier key
+    channels, half-split RoPE theta = 1e6 evaluated in float64 and rounded once), drawn from torch's
+    seeded GPU generator.
+    """
+    import torch
+
+    pos = torch.as_tensor(positions, device=device)
+    n, H = int(pos.numel()), w.n_kv_heads
+    k = torch.randn((n, H, HEAD_DIM), generator=generator, device=device, dtype=torch.float32)
+    v = torch.randn((n, H, HEAD_DIM), generator=generator, device=device, dtype=torch.float32)
+    if sink and w.sink_scale != 1.0 and n > 0:
+        k[0] *= w.sink_scale
+        v[0] *= w.sink_scale
+    for h in range(H):
+        ch = outlier_channels(w, layer, h)
+        if ch.size:
+            k[:, h, torch.from_numpy(ch).to(device)] *= w.outlier_scale
+    j = torch.arange(HEAD_DIM // 2, device=device, dtype=torch.float64)
+    inv = w.rope_theta ** (-2.0 * j / HEAD_DIM)
+    ang = pos.to(torch.float64)[:, None] * inv[None, :]
+    cos, sin = torch.cos(ang)[:, None, :], torch.sin(ang)[:, None, :]
+    a, b = k[..., : HEAD_DIM // 2].double(), k[..., HEAD_DIM // 2:].double()
+    k = torch.cat([a * cos - b * sin, b * cos + a * sin], dim=-1).float().contiguous()
+    return k, v
