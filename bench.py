@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
     p.add_argument("--layers", type=int, default=0, help="override layer count (profiling only; not a bench line)")
+    p.add_argument("--resident-layers", type=int, default=0,
+                   help="keep only this many layers' caches in HBM and run every layer call on cache l %% R "
+                        "(for workloads whose caches exceed HBM; each call still streams a full layer)")
     return p.parse_args()
 
 
@@ -159,13 +162,14 @@ class ClockSampler:
 class Model:
     """All layers' caches of one workload, filled through kvq_append, plus the step's buffers."""
 
-    def __init__(self, w, device, seed_base=0, n_layers=None):
+    def __init__(self, w, device, seed_base=0, n_layers=None, resident=0):
         import torch
 
         import quantized_kv_cache_kvq_gb300 as kvq
 
         self.kvq, self.torch, self.w, self.dev = kvq, torch, w, device
         self.L = n_layers or w.n_layers
+        self.R = min(self.L, resident) if resident else self.L   # caches resident in HBM
         B, Hkv, Hq = w.batch, w.n_kv_heads, w.n_q_heads
         self.lens = W.seq_lengths(w)
         pages = (self.lens + W.PAGE - 1) // W.PAGE
@@ -184,7 +188,7 @@ class Model:
         pos = torch.cat([torch.arange(w.prefix_len, w.prefix_len + int(n), device=device) for n in self.lens])
         slots = torch.cat([torch.from_numpy(W.slot_mapping(bt, s, np.arange(n))) for s, n in
                            enumerate(self.lens)]).to(device)
-        for l in range(self.L):
+        for l in range(self.R):
             g.manual_seed(W.unit_seed(w, 100_000 + 1000 * seed_base + l))
             c = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, self.num_pages, layer=l,
                                seed=(0x5EED << 20) + 97 * l + seed_base)
@@ -229,11 +233,12 @@ class Model:
         k_new = self.k_new if k_new is None else k_new
         v_new = self.v_new if v_new is None else v_new
         for l in range(self.L):
-            kvq.append(self.caches[l], k_new[l], v_new[l], self.new_slots, self.err)
+            c = l % self.R
+            kvq.append(self.caches[c], k_new[l], v_new[l], self.new_slots, self.err)
             if events is not None:
                 events[l][0].record()
-            kvq.decode_attn(self.caches[l], q[l], self.bt, self.seq_lens, self.out[l], self.ws,
-                            prefix=self.prefixes[l], prefix_len=w.prefix_len, sm_scale=SM_SCALE, meter=self.mp,
+            kvq.decode_attn(self.caches[c], q[l], self.bt, self.seq_lens, self.out[l], self.ws,
+                            prefix=self.prefixes[c], prefix_len=w.prefix_len, sm_scale=SM_SCALE, meter=self.mp,
                             meter_state=self.state[l], err=self.err)
             if events is not None:
                 events[l][1].record()
@@ -259,7 +264,10 @@ def run_gpu(args, w):
     import quantized_kv_cache_kvq_gb300 as kvq
 
     kvq.load()
-    m = Model(w, dev, seed_base=rank, n_layers=args.layers or None)
+    resident = args.resident_layers
+    if not resident and w.name == "ragged_paged":
+        resident = 4  # 36 layers of this workload need ~413 GB of cache: rotate 4 resident layers
+    m = Model(w, dev, seed_base=rank, n_layers=args.layers or None, resident=resident)
     per_step_bytes = step_bytes(w, m.lens) * m.L // w.n_layers
 
     def barrier():
@@ -316,7 +324,8 @@ def run_gpu(args, w):
     res = dict(value=value, ms_step=ms_step, achieved=achieved, graph=graph is not None, layer_ms_mean=statistics.mean(layer_ms),
                layer_ms_median=statistics.median(layer_ms), peak=peak, peak_kind=peak_kind, traffic=tr,
                clocks=clk.summary(), launches=m.launches_per_step() * args.steps, attended=attended,
-               per_step_bytes=per_step_bytes, world=world, rank=rank, counts=m.counts.cpu().tolist())
+               per_step_bytes=per_step_bytes, world=world, rank=rank, counts=m.counts.cpu().tolist(),
+               resident=m.R)
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, m, per_step_bytes, world, use_graph=graph is not None)
     if world > 1:
@@ -486,6 +495,8 @@ def main():
                          "launch_ms_mean": r["layer_ms_mean"]},
             "gpu_launches": r["launches"], "clocks": r["clocks"], "meter_counts": r["counts"],
             "launch_mode": "cuda_graph" if r["graph"] else "eager"}
+    if r["resident"] < (args.layers or w.n_layers):
+        line["config"]["resident_layers"] = r["resident"]
     if "e2e" in r:
         line["e2e"] = r["e2e"]
     if args.layers:
