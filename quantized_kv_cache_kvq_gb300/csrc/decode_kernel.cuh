@@ -215,6 +215,23 @@ __device__ __forceinline__ float one_minus_exp_neg(float c) {
   return c < 0.5f ? small : large;
 }
 
+// e^c - 1 for 0 <= c: Taylor series to c^8 below 1/2 (truncation < c^9/9! * e^c), else via exp2.
+__device__ __forceinline__ float expm1_pos(float c, bool all_small) {
+  float p = 2.48015873015873e-05f;            // 1/8!
+  p = __fmaf_rn(p, c, 1.98412698412698e-04f);  // 1/7!
+  p = __fmaf_rn(p, c, 1.38888888888889e-03f);  // 1/6!
+  p = __fmaf_rn(p, c, 8.33333333333333e-03f);  // 1/5!
+  p = __fmaf_rn(p, c, 4.16666666666667e-02f);  // 1/4!
+  p = __fmaf_rn(p, c, 1.66666666666667e-01f);  // 1/3!
+  p = __fmaf_rn(p, c, 0.5f);                   // 1/2!
+  p = __fmaf_rn(p, c, 1.0f);
+  const float small = p * c;
+  if (all_small) return small;
+  const float large = ex2(c * kLog2e) - 1.0f;
+  return c < 0.5f ? small : large;
+}
+constexpr float kFastRadius = 60.f;  // e^60 * 2^17 tokens stays far below the fp32 range
+
 // ------------------------------------------------------------------------------------------------
 // Fragment orientation.  The page's 16 tokens are the M dimension of every tensor-core product:
 //   S^T [16 tok x 8 heads]  = K [16 x 128]      . Q^T [128 x 8]    (8 k-steps)
@@ -282,9 +299,13 @@ struct QFrag {
 
 struct SoftState {
   float m[2], l[2];    // per head (2c, 2c+1): running max (log2 units), lane-partial sum
-  float mc[2], sc[2];  // Tier A accumulator (max of x + c log2e, scaled sum)
+  float mc[2], sc[2];  // Tier A accumulator: reference max (log2 units) and scaled sum
   float mu[2], su[2];  // Tier B accumulator
   float o[8][4];       // O^T fragments of the 8 channel blocks
+  // While every radius seen in the unit is <= kFastRadius the meter sums share the softmax's
+  // reference max (mc == m): sum p_t (e^{c_t} - 1).  The first larger radius switches the unit to
+  // the general form with its own running max (warp-uniform, sticky until the unit ends).
+  bool slow_a, slow_b;
 };
 
 __device__ __forceinline__ void reset_state(SoftState& s) {
@@ -292,6 +313,8 @@ __device__ __forceinline__ void reset_state(SoftState& s) {
   for (int h = 0; h < 2; ++h) {
     s.m[h] = -INFINITY; s.l[h] = 0.f; s.mc[h] = -INFINITY; s.sc[h] = 0.f; s.mu[h] = -INFINITY; s.su[h] = 0.f;
   }
+  s.slow_a = false;
+  s.slow_b = false;
 #pragma unroll
   for (int i = 0; i < 8; ++i) { s.o[i][0] = 0.f; s.o[i][1] = 0.f; s.o[i][2] = 0.f; s.o[i][3] = 0.f; }
 }
@@ -415,10 +438,48 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
   }
 }
 
+// One page of a meter sum.  r[v]: radius (c_t or u_t, natural units) of token g + 8(v >> 1) for head
+// 2c + (v & 1); x[v]: its logit (log2 units, -inf for padding); p[v] = 2^{x - mnew}.
+// Fast form (mc == m): sum += sum_v p (e^r - 1), rescaled with the softmax's alpha.
+// General form: own running max of x + r log2e, terms 2^{x + r log2e - max} (1 - e^{-r}).
+__device__ __forceinline__ void accumulate_meter(const float (&r)[4], const float (&x)[4], const float (&p)[4],
+                                                 const float (&alpha)[2], const float (&mnew)[2], float (&mc)[2],
+                                                 float (&sc)[2], bool& slow) {
+  const float rmax = __uint_as_float(__reduce_max_sync(
+      kFull, __float_as_uint(fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3])))));  // r >= 0: bit order = value order
+  slow = slow || !(rmax <= kFastRadius);
+  if (!slow) {
+    const bool small = rmax < 0.5f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      sc[h] = sc[h] * alpha[h] + (p[h] * expm1_pos(r[h], small) + p[2 + h] * expm1_pos(r[2 + h], small));
+      mc[h] = mnew[h];
+    }
+    return;
+  }
+  float z[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) z[v] = __fmaf_rn(r[v], kLog2e, x[v]);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float mz = col_max8(fmaxf(z[h], z[2 + h]));
+    const float mc_new = fmaxf(mc[h], mz);
+    if (mc_new != -INFINITY) {
+      const float t0 = ex2(z[h] - mc_new) * one_minus_exp_neg(r[h]);
+      const float t1 = ex2(z[2 + h] - mc_new) * one_minus_exp_neg(r[2 + h]);
+      sc[h] = sc[h] * ex2(mc[h] - mc_new) + (t0 + t1);
+      mc[h] = mc_new;
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------------------
 // One page of 16 tokens for one kv head.  `st` is the stage holding the page's tiles.
+// Tokens past the end of the sequence (a partial last page) have had their K, V, witness and scale
+// bytes zeroed in the stage; `xb0` / `xb1` are 0 for valid tokens g / g + 8 and -inf otherwise, added
+// to the logits, so no per-element masking is needed here.
 template <int KF, int VF, bool METER>
-__device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile, int nvalid, uint32_t phys,
+__device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile, float xb0, float xb1, uint32_t phys,
                                              const Planes& pl, int kvh, const QFrag& f, SoftState& s,
                                              float qk_scale, bool tier_b) {
   using L = Layout<KF, VF, METER>;
@@ -499,29 +560,25 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   }
 
   // ---------------- online softmax (log2 domain).  v = 2r + h: token g + 8r, head 2c + h
-  const bool valid[2] = {g < nvalid, g + 8 < nvalid};
+  const float xb[2] = {xb0, xb1};
   float x[4];
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
-    float sc = qk_scale;
-    if (fmt_has_scale(KF)) sc *= sk[v >> 1];
-    x[v] = valid[v >> 1] ? S[v] * sc : -INFINITY;
+    const float sc = fmt_has_scale(KF) ? qk_scale * sk[v >> 1] : qk_scale;
+    x[v] = __fmaf_rn(S[v], sc, xb[v >> 1]);
   }
   float alpha[2], mnew[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const float mx = col_max8(fmaxf(x[h], x[2 + h]));
     mnew[h] = fmaxf(s.m[h], mx);
-    alpha[h] = (mnew[h] == -INFINITY) ? 1.f : ex2(s.m[h] - mnew[h]);
+    alpha[h] = ex2(s.m[h] - mnew[h]);  // 0 on the first page (m = -inf); every page has a valid token
   }
   float p[4];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) p[v] = valid[v >> 1] ? ex2(x[v] - mnew[v & 1]) : 0.f;
+  for (int v = 0; v < 4; ++v) p[v] = ex2(x[v] - mnew[v & 1]);  // 0 for -inf logits
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    s.l[h] = s.l[h] * alpha[h] + (p[h] + p[2 + h]);
-    s.m[h] = mnew[h];
-  }
+  for (int h = 0; h < 2; ++h) s.l[h] = s.l[h] * alpha[h] + (p[h] + p[2 + h]);
   if (__any_sync(kFull, (alpha[0] != 1.f) | (alpha[1] != 1.f))) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -535,63 +592,31 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     const uint4 wb = lds128(st + L::wOff + lane * 16);
     mma_f16_4(C, wb.x, wb.z, wb.y, wb.w, f.qn_hi[0], f.qn_hi[1]);
     mma_f16_4(C, wb.x, wb.z, wb.y, wb.w, f.qn_lo[0], f.qn_lo[1]);
-    float cv[4], cz[4];
+    float cv[4];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      cv[v] = valid[v >> 1] ? C[v] * f.cm_scale : 0.f;
-      cz[v] = valid[v >> 1] ? __fmaf_rn(cv[v], kLog2e, x[v]) : -INFINITY;
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float mz = col_max8(fmaxf(cz[h], cz[2 + h]));
-      const float mc_new = fmaxf(s.mc[h], mz);
-      if (mc_new != -INFINITY) {
-        const float t0 = valid[0] ? ex2(cz[h] - mc_new) * one_minus_exp_neg(cv[h]) : 0.f;
-        const float t1 = valid[1] ? ex2(cz[2 + h] - mc_new) * one_minus_exp_neg(cv[2 + h]) : 0.f;
-        s.sc[h] = s.sc[h] * ex2(s.mc[h] - mc_new) + (t0 + t1);
-        s.mc[h] = mc_new;
-      }
-    }
+    for (int v = 0; v < 4; ++v) cv[v] = fmaxf(C[v] * f.cm_scale, 0.f);
+    accumulate_meter(cv, x, p, alpha, mnew, s.mc, s.sc, s.slow_a);
     if (KDITHER && tier_b) {
-      float uv[4], uz[4];
+      float uv[4];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uv[v] = valid[v >> 1] ? f.alpha_b[v & 1] * sk[v >> 1] : 0.f;
-        uz[v] = valid[v >> 1] ? __fmaf_rn(uv[v], kLog2e, x[v]) : -INFINITY;
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float mz = col_max8(fmaxf(uz[h], uz[2 + h]));
-        const float mu_new = fmaxf(s.mu[h], mz);
-        if (mu_new != -INFINITY) {
-          const float t0 = valid[0] ? ex2(uz[h] - mu_new) * one_minus_exp_neg(uv[h]) : 0.f;
-          const float t1 = valid[1] ? ex2(uz[2 + h] - mu_new) * one_minus_exp_neg(uv[2 + h]) : 0.f;
-          s.su[h] = s.su[h] * ex2(s.mu[h] - mu_new) + (t0 + t1);
-          s.mu[h] = mu_new;
-        }
-      }
+      for (int v = 0; v < 4; ++v) uv[v] = f.alpha_b[v & 1] * sk[v >> 1];
+      accumulate_meter(uv, x, p, alpha, mnew, s.mu, s.su, s.slow_b);
     }
   }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) s.m[h] = mnew[h];
 
   // ---------------- O^T += V^T . P^T.  P'^T (B operand) = movmatrix of the S^T-shaped weights.
   float pw[4];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) pw[v] = valid[v >> 1] ? p[v] * (kPvShift * sv[v >> 1]) : 0.f;
-  // the A fragments carry tokens 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3): zero invalid ones
-  const bool partial = nvalid < kPage;
-  const bool vt[4] = {2 * c < nvalid, 2 * c + 1 < nvalid, 2 * c + 8 < nvalid, 2 * c + 9 < nvalid};
+  for (int v = 0; v < 4; ++v) pw[v] = p[v] * (kPvShift * sv[v >> 1]);
   if (!fmt_is_16bit(VF)) {
     const uint32_t b0 = movmatrix_trans(pack_f16(pw[0], pw[1]));
     const uint32_t b1 = movmatrix_trans(pack_f16(pw[2], pw[3]));
-    uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
-    if (partial) {
-      mlo = (vt[0] ? 0x00FF00FFu : 0u) | (vt[1] ? 0xFF00FF00u : 0u);
-      mhi = (vt[2] ? 0x00FF00FFu : 0u) | (vt[3] ? 0xFF00FF00u : 0u);
-    }
 #pragma unroll
     for (int mm = 0; mm < 4; ++mm) {
       const uint4 vb = lds128(st + L::vOff + (mm * 32 + lane) * 16);
-      const uint32_t words[4] = {vb.x & mlo, vb.y & mhi, vb.z & mlo, vb.w & mhi};
+      const uint32_t words[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const uint32_t u0 = words[2 * half], u1 = words[2 * half + 1];
@@ -628,17 +653,11 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     const uint32_t l01 = pack_bf16(pw[0] - r01.x, pw[1] - r01.y), l23 = pack_bf16(pw[2] - r23.x, pw[3] - r23.y);
     const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
     const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-    uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
-    if (partial) {
-      mlo = (vt[0] ? 0xFFFFu : 0u) | (vt[1] ? 0xFFFF0000u : 0u);
-      mhi = (vt[2] ? 0xFFFFu : 0u) | (vt[3] ? 0xFFFF0000u : 0u);
-    }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       const uint4 vb = lds128(st + L::vOff + (mt * 32 + lane) * 16);
-      const uint32_t a0 = vb.x & mlo, a1 = vb.y & mlo, a2 = vb.z & mhi, a3 = vb.w & mhi;
-      mma_bf16_4(s.o[mt], a0, a1, a2, a3, bh0, bh1);
-      mma_bf16_4(s.o[mt], a0, a1, a2, a3, bl0, bl1);
+      mma_bf16_4(s.o[mt], vb.x, vb.y, vb.z, vb.w, bh0, bh1);
+      mma_bf16_4(s.o[mt], vb.x, vb.y, vb.z, vb.w, bl0, bl1);
     }
   }
 }
@@ -750,6 +769,32 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
   }
 }
 
+// Zero the bytes of tokens nvalid..15 in a stage (a partial last page): the slots past the end of a
+// sequence may hold anything, and zeros make their logit exactly the -inf bias, their value and
+// radius exactly 0.  Runs once per unit at most; all lanes take part.
+template <int KF, int VF, bool METER>
+__device__ void zero_tail(uint8_t* st, int nvalid) {
+  using L = Layout<KF, VF, METER>;
+  const int lane = threadIdx.x & 31;
+  const int n = (kPage - nvalid) * kHeadDim;
+  for (int e = lane; e < n; e += 32) {
+    const int t = nvalid + e / kHeadDim, c = e % kHeadDim;
+    if (fmt_is_16bit(KF)) *reinterpret_cast<uint16_t*>(st + L::kOff + k16_offset(t, c)) = 0;
+    else st[L::kOff + k8_offset(t, c)] = 0;
+    if (fmt_is_16bit(VF)) *reinterpret_cast<uint16_t*>(st + L::vOff + v16_offset(t, c)) = 0;
+    else st[L::vOff + v8_offset(t, c)] = 0;
+  }
+  for (int e = lane; e < (kPage - nvalid) * kBands; e += 32) {
+    const int t = nvalid + e / kBands, b = e % kBands;
+    if (METER) *reinterpret_cast<uint16_t*>(st + L::wOff + w_offset(t, b)) = 0;
+  }
+  for (int t = nvalid + lane; t < kPage; t += 32) {
+    if (fmt_has_scale(KF)) *reinterpret_cast<uint16_t*>(st + L::ksOff + s_offset(t)) = 0;
+    if (fmt_has_scale(VF)) *reinterpret_cast<uint16_t*>(st + L::vsOff + s_offset(t)) = 0;
+  }
+  __syncwarp();
+}
+
 template <int KF, int VF, int PKF, int PVF, bool METER>
 __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -838,6 +883,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args
   bool ok = true;
   int timeout_at = 0;
 
+  const int g8 = lane >> 2;
+  int stage = 0;
+  uint32_t parity = 0;
   for (int j = 0; j < n; ++j) {
     if (j > 0 && (j & 31) == 0) {
       cur = nxt;
@@ -853,19 +901,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args
       const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
       load_q<K16, METER>(a, seq, kvh, total, f);
     }
-    const int stage = j % a.stages;
-    const uint32_t parity = static_cast<uint32_t>((j / a.stages) & 1);
     // every lane polls; the verdict is made warp-uniform before anyone leaves the loop
     if (!__all_sync(kFull, mbar_wait(&bars[stage], parity))) { ok = false; timeout_at = j; break; }
+    uint8_t* st = wbase + stage * a.stage_bytes;
     if (phys >= 0) {
-      const uint8_t* st = wbase + stage * a.stage_bytes;
       const int kvh = u % a.Hkv;
+      const int nvalid = d_nvalid(info);
+      const float xb0 = g8 < nvalid ? 0.f : -INFINITY, xb1 = g8 + 8 < nvalid ? 0.f : -INFINITY;
       if (PKF != kNoPrefix && d_prefix(info)) {
         constexpr int pk = (PKF < 0 ? 0 : PKF), pv = (PVF < 0 ? 0 : PVF);
-        process_page<pk, pv, METER>(st, xi_tile, d_nvalid(info), static_cast<uint32_t>(phys), a.pre, kvh, f, s,
+        if (nvalid < kPage) zero_tail<pk, pv, METER>(st, nvalid);
+        process_page<pk, pv, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.pre, kvh, f, s,
                                     qk_scale, a.tier_b != 0);
       } else {
-        process_page<KF, VF, METER>(st, xi_tile, d_nvalid(info), static_cast<uint32_t>(phys), a.live, kvh, f, s,
+        if (nvalid < kPage) zero_tail<KF, VF, METER>(st, nvalid);
+        process_page<KF, VF, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f, s,
                                     qk_scale, a.tier_b != 0);
       }
     }
@@ -877,10 +927,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args
       const uint32_t ic = __shfl_sync(kFull, cur.info, jn & 31), inx = __shfl_sync(kFull, nxt.info, jn & 31);
       if (lane == 0) {
         fence_proxy_async();
-        issue_page<KF, VF, PKF, PVF, METER>(a, wbase + stage * a.stage_bytes, &bars[stage],
-                                            in_cur ? Desc{pc, ic} : Desc{pn, inx});
+        issue_page<KF, VF, PKF, PVF, METER>(a, st, &bars[stage], in_cur ? Desc{pc, ic} : Desc{pn, inx});
       }
     }
+    if (++stage == a.stages) { stage = 0; parity ^= 1u; }
   }
   if (!ok) {
     if (lane == 0) report(a.err, KVQ_ERR_TIMEOUT);
