@@ -5,7 +5,7 @@
 
 #include "decode_kernel.cuh"
 
-#define KVQ_X(KF, VF, PKF, PVF) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, false) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, true)
+#define KVQ_X(KF, VF, PKF, PVF, NW) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, false) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, true)
 #include "decode_instances.inc"
 #undef KVQ_X
 
@@ -180,18 +180,27 @@ Planes planes_of(const kvq_cache* c) {
   p.layer = static_cast<uint32_t>(c->layer);
   p.seed_lo = static_cast<uint32_t>(c->dither_seed);
   p.seed_hi = static_cast<uint32_t>(c->dither_seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    p.rk0[r] = p.seed_lo + static_cast<uint32_t>(r) * kPhiloxW0;
+    p.rk1[r] = p.seed_hi + static_cast<uint32_t>(r) * kPhiloxW1;
+  }
   return p;
 }
 
 using Launcher = cudaError_t (*)(const Args&, int, size_t, cudaStream_t);
 
-Launcher pick(int kf, int vf, int pkf, int pvf, bool meter) {
-#define KVQ_X(KF, VF, PKF, PVF)                                   \
-  if (kf == (KF) && vf == (VF) && pkf == (PKF) && pvf == (PVF))   \
-    return meter ? &launch_decode<KF, VF, PKF, PVF, true> : &launch_decode<KF, VF, PKF, PVF, false>;
+struct Pick {
+  Launcher launch;
+  int warps;
+};
+
+Pick pick(int kf, int vf, int pkf, int pvf, bool meter) {
+#define KVQ_X(KF, VF, PKF, PVF, NW)                                                                       \
+  if (kf == (KF) && vf == (VF) && pkf == (PKF) && pvf == (PVF))                                           \
+    return Pick{meter ? &launch_decode<KF, VF, PKF, PVF, NW, true> : &launch_decode<KF, VF, PKF, PVF, NW, false>, NW};
 #include "decode_instances.inc"
 #undef KVQ_X
-  return nullptr;
+  return Pick{nullptr, 0};
 }
 
 }  // namespace
@@ -200,7 +209,7 @@ extern "C" size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads,
   if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads) return 0;
   const int sms = device_sm_count();
   if (sms <= 0) return 0;
-  return ws_layout(batch, num_kv_heads, num_q_heads, sms * kWarps).total;
+  return ws_layout(batch, num_kv_heads, num_q_heads, sms * kMaxWarps).total;
 }
 
 extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int32_t prefix_len,
@@ -240,15 +249,16 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* p
   const int sms = device_sm_count();
   const int smem_max = device_smem_optin();
   if (sms <= 0 || smem_max <= 0) return KVQ_ERR_CUDA;
-  const int w_max = sms * kWarps;
-  const WsLayout wl = ws_layout(batch, hkv, num_q_heads, w_max);
+  const WsLayout wl = ws_layout(batch, hkv, num_q_heads, sms * kMaxWarps);
   if (ws_bytes < wl.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
 
   const bool has_prefix = prefix && prefix_len > 0;
   const int pkf = has_prefix ? prefix->k_fmt : kNoPrefix;
   const int pvf = has_prefix ? prefix->v_fmt : kNoPrefix;
-  Launcher launch = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter);
-  if (!launch) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter);
+  if (!pk.launch) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  const int nw = pk.warps;
+  const int w_max = sms * nw;
 
   Args a{};
   a.live = planes_of(cache);
@@ -285,17 +295,18 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* p
   if (has_prefix) sb = std::max(sb, page_bytes(prefix->k_fmt, prefix->v_fmt, meter));
   const bool xi = cache->k_fmt == KVQ_FMT_INT8_DITHER && cache->v_fmt == KVQ_FMT_INT8_DITHER;
   const int cum_bytes = ((batch + 1) * 4 + 127) & ~127;
-  const int fixed = cum_bytes + kWarps * ((xi ? kXiScratch : 0) + kMaxStages * 8);
+  const int lo_bytes = q_dtype == KVQ_DTYPE_F32 ? kQloBytes : 0;
+  const int fixed = cum_bytes + nw * ((xi ? kXiScratch : 0) + lo_bytes + kMaxStages * 8);
   const int budget = smem_max - 1024 - fixed;
-  int stages = budget / (kWarps * sb);
+  int stages = budget / (nw * sb);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return KVQ_ERR_UNSUPPORTED_LAYOUT;
   a.stages = stages;
   a.stage_bytes = sb;
-  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(kWarps) * stages * sb;
+  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(nw) * stages * sb;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch(a, sms, smem, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (pk.launch(a, sms, smem, s) != cudaSuccess) return KVQ_ERR_CUDA;
   // merge: programmatic dependent launch, so its launch overlaps the decode grid's tail
   const long long merge_threads = static_cast<long long>(batch) * num_q_heads * 32;
   cudaLaunchConfig_t cfg = {};

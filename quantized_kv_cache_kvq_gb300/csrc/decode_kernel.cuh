@@ -26,12 +26,10 @@
 namespace kvq {
 namespace dec {
 
-#ifndef KVQ_DECODE_WARPS
-#define KVQ_DECODE_WARPS 12
-#endif
-// Warps per CTA (one CTA per SM).  Each warp owns a ring of page stages; the decode is bound by
-// the bytes in flight, so few warps with deep rings beat many warps with shallow ones.
-constexpr int kWarps = KVQ_DECODE_WARPS;
+// Warps per CTA (one CTA per SM) is a per-layout template parameter (decode_instances.inc); this is
+// the largest value any layout uses, which sizes the workspace.
+constexpr int kMaxWarps = 16;
+constexpr int kQloBytes = 8 * 2 * 32 * 4;  // per-warp low parts of an fp32 query (only when q is fp32)
 constexpr int kMaxStages = 16;
 constexpr int kMaxBatch = 1024;  // sequences per call (prefix sums live in shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -50,6 +48,7 @@ struct Planes {
   int num_pages;
   uint32_t layer;
   uint32_t seed_lo, seed_hi;
+  uint32_t rk0[10], rk1[10];  // Philox round keys of the dither stream (host-precomputed)
 };
 
 struct Args {
@@ -290,7 +289,7 @@ __device__ __forceinline__ float col_sum8(float v) {
 
 struct QFrag {
   uint32_t hi[8][2];  // Q^T B fragments (b0, b1) per k-step: head g, channels of the K tile word order
-  uint32_t lo[8][2];  // q - hi, when q is not exactly representable in the MMA input type
+  uint32_t* lo;       // q - hi per (k-step, word, lane) in the warp's shared memory (fp32 queries only)
   uint32_t qn_hi[2], qn_lo[2];  // QN^T B fragment: band norms of head g (normalised by 2^-e)
   bool has_lo;
   float cm_scale;    // c_t = cm_scale * (W . QN)  (natural units)
@@ -347,18 +346,26 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
       v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
     }
   };
+  const bool fp32q = !a.q_bf16;
+  bool any_lo = false;
   auto put = [&](int kb, const float* x) {  // channels x[0..3] of k-step kb: b0 <- x0, x1; b1 <- x2, x3
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const float x0 = x[2 * h], x1 = x[2 * h + 1];
+      uint32_t lo;
       if (K16) {
         f.hi[kb][h] = pack_bf16(x0, x1);
         const float2 r = unpack_bf16(f.hi[kb][h]);
-        f.lo[kb][h] = pack_bf16(x0 - r.x, x1 - r.y);
+        lo = pack_bf16(x0 - r.x, x1 - r.y);
       } else {
+        // bf16 queries are exact in fp16 down to 2^-14 and within 2^-25 below it: no low part needed
         f.hi[kb][h] = pack_f16(x0, x1);
         const float2 r = unpack_f16(f.hi[kb][h]);
-        f.lo[kb][h] = pack_f16(x0 - r.x, x1 - r.y);
+        lo = pack_f16(x0 - r.x, x1 - r.y);
+      }
+      if (fp32q) {
+        f.lo[(kb * 2 + h) * 32 + lane] = lo;
+        any_lo |= (lo & 0x7FFF7FFFu) != 0u;
       }
     }
   };
@@ -384,10 +391,8 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
       put(4 * jj + 3, v1 + 4);
     }
   }
-  bool any_lo = false;
-#pragma unroll
-  for (int kb = 0; kb < 8; ++kb) any_lo |= ((f.lo[kb][0] | f.lo[kb][1]) & 0x7FFF7FFFu) != 0u;
   f.has_lo = __any_sync(kFull, any_lo);
+  __syncwarp();
   if (METER) {
     // band b = 4c + i holds channels 16c + 4i + {0..3} and 64 + 16c + 4i + {0..3}
     float u0[8], u1[8], w0[8], w1[8];
@@ -498,8 +503,9 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       mma_bf16_4(S, k0.x, k1.x, k0.y, k1.y, f.hi[2 * j][0], f.hi[2 * j][1]);
       mma_bf16_4(S, k0.z, k1.z, k0.w, k1.w, f.hi[2 * j + 1][0], f.hi[2 * j + 1][1]);
       if (f.has_lo) {
-        mma_bf16_4(S, k0.x, k1.x, k0.y, k1.y, f.lo[2 * j][0], f.lo[2 * j][1]);
-        mma_bf16_4(S, k0.z, k1.z, k0.w, k1.w, f.lo[2 * j + 1][0], f.lo[2 * j + 1][1]);
+        const uint32_t* lo = f.lo + lane;
+        mma_bf16_4(S, k0.x, k1.x, k0.y, k1.y, lo[(4 * j + 0) * 32], lo[(4 * j + 1) * 32]);
+        mma_bf16_4(S, k0.z, k1.z, k0.w, k1.w, lo[(4 * j + 2) * 32], lo[(4 * j + 3) * 32]);
       }
     }
   } else {
@@ -522,26 +528,23 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         }
         const int kb = 4 * jj + sidx;
         mma_f16_4(S, a0, a1, a2, a3, f.hi[kb][0], f.hi[kb][1]);
-        if (f.has_lo) mma_f16_4(S, a0, a1, a2, a3, f.lo[kb][0], f.lo[kb][1]);
+        if (f.has_lo) mma_f16_4(S, a0, a1, a2, a3, f.lo[(2 * kb) * 32 + lane], f.lo[(2 * kb + 1) * 32 + lane]);
         if (KDITHER) {
           // subtract xi . q: the dither of tokens g and g + 8, channels 64jj + 16c + 4sidx + {0..3}
           const uint32_t grp = 16 * jj + 4 * c + sidx;
-          const float4 d0 = dither4(phys * kPage + g, pl.layer, static_cast<uint32_t>(kvh), grp, pl.seed_lo,
-                                    pl.seed_hi);
-          const float4 d1 = dither4(phys * kPage + g + 8, pl.layer, static_cast<uint32_t>(kvh), grp, pl.seed_lo,
-                                    pl.seed_hi);
-          mma_f16_4(S, pack_f16(-d0.x, -d0.y), pack_f16(-d1.x, -d1.y), pack_f16(-d0.z, -d0.w),
-                    pack_f16(-d1.z, -d1.w), f.hi[kb][0], f.hi[kb][1]);
+          const uint4 w0 = philox4x32_10_rk(make_uint4(phys * kPage + g, pl.layer, static_cast<uint32_t>(kvh), grp),
+                                            pl.rk0, pl.rk1);
+          const uint4 w1 = philox4x32_10_rk(make_uint4(phys * kPage + g + 8, pl.layer, static_cast<uint32_t>(kvh), grp),
+                                            pl.rk0, pl.rk1);
+          const uint32_t n00 = neg_dither_f16x2(w0.x, w0.y), n01 = neg_dither_f16x2(w0.z, w0.w);
+          const uint32_t n10 = neg_dither_f16x2(w1.x, w1.y), n11 = neg_dither_f16x2(w1.z, w1.w);
+          mma_f16_4(S, n00, n10, n01, n11, f.hi[kb][0], f.hi[kb][1]);
           if (VDITHER) {
-            // stage the dither for the value side: token-major fp16 tile, 16-byte chunks xor-swizzled
+            // stage minus the dither for the value side: token-major fp16 tile, 16-byte chunks xor-swizzled
             const int ch = 64 * jj + 16 * c + 4 * sidx;
-            uint2 w2;
-            w2.x = pack_f16(d0.x, d0.y);
-            w2.y = pack_f16(d0.z, d0.w);
-            *reinterpret_cast<uint2*>(xi_tile + g * 256 + (((ch >> 3) ^ g) << 4) + (ch & 7) * 2) = w2;
-            w2.x = pack_f16(d1.x, d1.y);
-            w2.y = pack_f16(d1.z, d1.w);
-            *reinterpret_cast<uint2*>(xi_tile + (g + 8) * 256 + (((ch >> 3) ^ g) << 4) + (ch & 7) * 2) = w2;
+            const int off = (((ch >> 3) ^ g) << 4) + (ch & 7) * 2;
+            *reinterpret_cast<uint2*>(xi_tile + g * 256 + off) = make_uint2(n00, n01);
+            *reinterpret_cast<uint2*>(xi_tile + (g + 8) * 256 + off) = make_uint2(n10, n11);
           }
         }
       }
@@ -633,9 +636,8 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       }
     }
     if (VDITHER) {
-      // subtract xi^T . P'^T: A fragments of the dither tile by transposed 8x8 loads
+      // add (-xi)^T . P'^T: A fragments of the (negated) dither tile by transposed 8x8 loads
       __syncwarp();
-      const uint32_t nb0 = b0 ^ 0x80008000u, nb1 = b1 ^ 0x80008000u;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         // matrices: (tok 0-7, ch 16mt..+7), (tok 0-7, ch 16mt+8..), (tok 8-15, ch 16mt..), (tok 8-15, ch +8..)
@@ -644,7 +646,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         const int chunk = (2 * mt + (mat & 1)) ^ (row & 7);
         uint32_t fr[4];
         ldmatrix_x4_trans(fr, xi_tile + row * 256 + chunk * 16);
-        mma_f16_4(s.o[mt], fr[0], fr[1], fr[2], fr[3], nb0, nb1);
+        mma_f16_4(s.o[mt], fr[0], fr[1], fr[2], fr[3], b0, b1);
       }
     }
   } else {
@@ -795,8 +797,8 @@ __device__ void zero_tail(uint8_t* st, int nvalid) {
   __syncwarp();
 }
 
-template <int KF, int VF, int PKF, int PVF, bool METER>
-__global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args a) {
+template <int KF, int VF, int PKF, int PVF, int NW, bool METER>
+__global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   // let the merge grid (programmatic dependent launch) be scheduled as soon as SMs free up
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -808,7 +810,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args
 
   // ---- prefix sums of pages per sequence (block-wide scan)
   {
-    __shared__ int32_t warp_tot[kWarps];
+    __shared__ int32_t warp_tot[NW];
     const int per = (a.B + blockDim.x - 1) / blockDim.x;
     const int s0 = threadIdx.x * per;
     int loc = 0;
@@ -850,16 +852,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args
 
   const long long T = static_cast<long long>(a.Hkv) * cum[a.B];
   const long long W = min(static_cast<long long>(a.w_max), T);
-  const int wid = blockIdx.x * kWarps + warp;
+  const int wid = blockIdx.x * NW + warp;
   if (wid >= W) return;
   const long long x_begin = T * wid / W, x_end = T * (wid + 1) / W;
   const int n = static_cast<int>(x_end - x_begin);
 
-  // ---- per-warp shared memory: stages, dither tile, barriers
-  const int per_warp = a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + kMaxStages * 8;
+  // ---- per-warp shared memory: stages, dither tile, query low parts, barriers
+  const int lo_bytes = a.q_bf16 ? 0 : kQloBytes;
+  const int per_warp = a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes + kMaxStages * 8;
   uint8_t* wbase = smem + cum_bytes + warp * per_warp;
   uint8_t* xi_tile = wbase + a.stages * a.stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + a.stages * a.stage_bytes + (XI ? kXiScratch : 0));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes);
   if (lane == 0) {
     for (int i = 0; i < a.stages; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
@@ -876,6 +879,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_split_kernel(const Args
   }
 
   QFrag f;
+  f.lo = reinterpret_cast<uint32_t*>(wbase + a.stages * a.stage_bytes + (XI ? kXiScratch : 0));
+  f.has_lo = false;
   SoftState s;
   reset_state(s);
   int unit = -1;
@@ -950,16 +955,16 @@ namespace kvq {
 namespace dec {
 
 // Host launcher of one instantiation (the dynamic shared-memory limit is raised once per kernel).
-template <int KF, int VF, int PKF, int PVF, bool METER>
+template <int KF, int VF, int PKF, int PVF, int NW, bool METER>
 cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s) {
-  auto kern = decode_split_kernel<KF, VF, PKF, PVF, METER>;
+  auto kern = decode_split_kernel<KF, VF, PKF, PVF, NW, METER>;
   static size_t configured = 0;  // largest dynamic smem size set so far
   if (smem > configured) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<grid, kWarps * 32, smem, s>>>(a);
+  kern<<<grid, NW * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -968,7 +973,7 @@ cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s) 
 
 // Explicit instantiations are listed once, in decode_instances.inc, and split across translation
 // units so they compile in parallel.
-#define KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, M) \
-  template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, M>(const kvq::dec::Args&, int, size_t, cudaStream_t);
-#define KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, M) \
-  extern template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, M>(const kvq::dec::Args&, int, size_t, cudaStream_t);
+#define KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, M) \
+  template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M>(const kvq::dec::Args&, int, size_t, cudaStream_t);
+#define KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, M) \
+  extern template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M>(const kvq::dec::Args&, int, size_t, cudaStream_t);

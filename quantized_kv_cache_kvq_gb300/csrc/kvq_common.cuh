@@ -91,10 +91,32 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1
   return x;
 }
 
+// Philox4x32-10 with the ten round keys precomputed (k0[r] = key0 + r * W0, k1[r] = key1 + r * W1);
+// kernel-parameter arrays make every round key a constant operand.
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 x, const uint32_t (&k0)[10], const uint32_t (&k1)[10]) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    uint32_t hi0, lo0, hi1, lo1;
+    mul_wide(kPhiloxM0, x.x, hi0, lo0);
+    mul_wide(kPhiloxM1, x.z, hi1, lo1);
+    x = make_uint4(hi1 ^ x.y ^ k0[r], lo1, hi0 ^ x.w ^ k1[r], lo0);
+  }
+  return x;
+}
+
 // Dither value of a Philox output word: ((w >> 8) + 1/2) * 2^-24 - 1/2, exact in binary32.
 __device__ __forceinline__ float dither_from_word(uint32_t w) {
   return __fmaf_rn(static_cast<float>(w >> 8), 5.9604644775390625e-8f /* 2^-24 */,
                    -0.49999997019767761f /* 2^-25 - 1/2 */);
+}
+
+// Minus the dither of two words, rounded to an fp16 pair (low half from w0): the decode's tensor-core
+// operand; -xi = 1/2 - 2^-25 - (w >> 8) * 2^-24 is exact in binary32 before the fp16 rounding.
+__device__ __forceinline__ uint32_t neg_dither_f16x2(uint32_t w0, uint32_t w1) {
+  const float a = __fmaf_rn(static_cast<float>(w0 >> 8), -5.9604644775390625e-8f, 0.49999997019767761f);
+  const float b = __fmaf_rn(static_cast<float>(w1 >> 8), -5.9604644775390625e-8f, 0.49999997019767761f);
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // The four dithers of channels 4*group .. 4*group+3 of (slot, layer, kv_head).
