@@ -250,6 +250,11 @@ kvq_status kvq_debug_dither(uint64_t seed, int32_t layer, int32_t kv_head, const
    (uint16 out); 3: fp16 round-up (uint16 out). */
 kvq_status kvq_debug_encode(int32_t kind, const float* x_dev, int64_t n, void* out_dev, kvq_stream_t stream);
 
+/* Test hook: one warp runs the decode kernel's bounded wait (at most limit_ns <= 2 s of wall clock)
+   on an mbarrier that nothing completes, then writes KVQ_ERR_TIMEOUT to err_word_dev; the context
+   stays usable.  Exercises the failure path without faulting or hanging the GPU. */
+kvq_status kvq_debug_wait_timeout(uint64_t limit_ns, int32_t* err_word_dev, kvq_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* kvq_status_string(int32_t status);
 

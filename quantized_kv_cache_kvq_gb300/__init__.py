@@ -128,6 +128,8 @@ def load(path: str = LIB_PATH):
     L.kvq_debug_dither.argtypes = [c_uint64, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p]
     L.kvq_debug_encode.restype = c_int32
     L.kvq_debug_encode.argtypes = [c_int32, c_void_p, c_int64, c_void_p, c_void_p]
+    L.kvq_debug_wait_timeout.restype = c_int32
+    L.kvq_debug_wait_timeout.argtypes = [c_uint64, c_void_p, c_void_p]
     L.kvq_status_string.restype = ctypes.c_char_p
     L.kvq_status_string.argtypes = [c_int32]
     L.kvq_version.restype = c_int32
@@ -266,6 +268,11 @@ def meter(meter_state: torch.Tensor, n_layers: int, batch: int, num_q_heads: int
 def debug_dither(seed: int, layer: int, kv_head: int, slots: torch.Tensor, out: torch.Tensor, stream=None):
     _check(lib().kvq_debug_dither(seed & 0xFFFFFFFFFFFFFFFF, layer, kv_head, slots.data_ptr(), int(slots.numel()),
                                   out.data_ptr(), _stream(stream)), "kvq_debug_dither")
+
+
+def debug_wait_timeout(limit_ns: int, err: torch.Tensor, stream=None):
+    """kvq_debug_wait_timeout: a bounded wait that runs out; err receives KVQ_ERR_TIMEOUT."""
+    _check(lib().kvq_debug_wait_timeout(int(limit_ns), err.data_ptr(), _stream(stream)), "kvq_debug_wait_timeout")
 
 
 def debug_encode(kind: int, x: torch.Tensor, out: torch.Tensor, stream=None):

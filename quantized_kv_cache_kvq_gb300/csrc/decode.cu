@@ -362,3 +362,25 @@ extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_
   return kvq_decode_attn(cache, prefix, prefix_len, q, q_dtype, batch, num_q_heads, block_table, max_pages_per_seq,
                          seq_lens, sm_scale, mp, out, meter_state, ws, KVQ_STATIC_WORKSPACE_BYTES, err_word, stream);
 }
+
+// ------------------------------------------------------------------------------------------------
+// Test hook: the decode kernel's bounded mbarrier wait on a barrier that nothing completes.
+namespace kvq {
+namespace dec {
+__global__ void wait_timeout_kernel(unsigned long long limit_ns, int32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (!__all_sync(kFull, mbar_wait(&bar, 0, limit_ns)) && threadIdx.x == 0) report(err, KVQ_ERR_TIMEOUT);
+}
+}  // namespace dec
+}  // namespace kvq
+
+extern "C" kvq_status kvq_debug_wait_timeout(uint64_t limit_ns, int32_t* err_word, kvq_stream_t stream) {
+  if (!err_word || limit_ns > 2000000000ull) return KVQ_ERR_INVALID_ARG;
+  kvq::dec::wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, err_word);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
