@@ -74,9 +74,12 @@ typedef enum kvq_dtype { KVQ_DTYPE_F32 = 0, KVQ_DTYPE_BF16 = 1 } kvq_dtype;
 
 /*
  * One layer's paged cache: planes of tiles, one tile per (page, kv head).
- * Tile index of (page p, kv head h) is p * num_kv_heads + h; a tile holds the
- * 16 tokens (slots p*16 .. p*16+15) of that page.  All planes are device
- * memory, 16-byte aligned, owned by the caller.
+ * Tile index of (page p, kv head h) is p * num_kv_heads + h in the K, V and
+ * witness planes and h * num_pages + p in the two scale planes (head-major, so
+ * that the 32-byte scale tiles of consecutive pages of one head share a
+ * 128-byte memory line); a tile holds the 16 tokens (slots p*16 .. p*16+15)
+ * of that page.  All planes are device memory, 16-byte aligned, owned by the
+ * caller.
  *
  * Tile layouts (byte offset of token t in 0..15, channel c in 0..127, band b
  * in 0..15; they place each lane's tensor-core fragment in contiguous 16-byte

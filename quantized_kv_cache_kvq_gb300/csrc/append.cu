@@ -175,9 +175,11 @@ __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __
   store_k4<KF>(static_cast<uint8_t*>(c.k_data) + tile * tile_bytes_k(KF), t, c0, kc);
   store_v4<VF>(static_cast<uint8_t*>(c.v_data) + tile * tile_bytes_v(VF), t, c0, vc);
   if (lane == 0) {
-    if (fmt_has_scale(KF)) *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(c.k_scale) + tile * kTileBytesS + s_offset(t)) = ks;
+    // scale planes are head-major: tile (page, head) at head * num_pages + page
+    const size_t stile = static_cast<size_t>(head) * c.num_pages + page;
+    if (fmt_has_scale(KF)) *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(c.k_scale) + stile * kTileBytesS + s_offset(t)) = ks;
     if (fmt_has_scale(VF)) {
-      *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(c.v_scale) + tile * kTileBytesS + s_offset(t)) = vs;
+      *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(c.v_scale) + stile * kTileBytesS + s_offset(t)) = vs;
       if (__half2float(__ushort_as_half(vs)) > KVQ_MAX_VALUE_SCALE) flags |= 2;
     }
   }

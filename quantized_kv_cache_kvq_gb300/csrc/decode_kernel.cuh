@@ -509,6 +509,13 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       }
     }
   } else {
+    PhiloxHead ph{};
+    PhiloxSlot pt0{}, pt1{};
+    if (KDITHER) {
+      ph = philox_head(pl.layer, static_cast<uint32_t>(kvh), pl.rk0, pl.rk1);
+      pt0 = philox_slot(phys * kPage + g, ph, pl.rk0, pl.rk1);
+      pt1 = philox_slot(phys * kPage + g + 8, ph, pl.rk0, pl.rk1);
+    }
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
       const uint4 k0 = lds128(st + L::kOff + (jj * 32 + lane) * 16);
@@ -532,10 +539,8 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         if (KDITHER) {
           // subtract xi . q: the dither of tokens g and g + 8, channels 64jj + 16c + 4sidx + {0..3}
           const uint32_t grp = 16 * jj + 4 * c + sidx;
-          const uint4 w0 = philox4x32_10_rk(make_uint4(phys * kPage + g, pl.layer, static_cast<uint32_t>(kvh), grp),
-                                            pl.rk0, pl.rk1);
-          const uint4 w1 = philox4x32_10_rk(make_uint4(phys * kPage + g + 8, pl.layer, static_cast<uint32_t>(kvh), grp),
-                                            pl.rk0, pl.rk1);
+          const uint4 w0 = philox_finish(grp, pt0, ph, pl.rk0, pl.rk1);
+          const uint4 w1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
           const uint32_t n00 = neg_dither_f16x2(w0.x, w0.y), n01 = neg_dither_f16x2(w0.z, w0.w);
           const uint32_t n10 = neg_dither_f16x2(w1.x, w1.y), n11 = neg_dither_f16x2(w1.z, w1.w);
           mma_f16_4(S, n00, n10, n01, n11, f.hi[kb][0], f.hi[kb][1]);
@@ -728,8 +733,9 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     bulk_g2s(stage + L::kOff, a.pre.k + tile * L::kBytes, L::kBytes, bar);
     bulk_g2s(stage + L::vOff, a.pre.v + tile * L::vBytes, L::vBytes, bar);
     if (METER) bulk_g2s(stage + L::wOff, a.pre.w + tile * kTileBytesW, kTileBytesW, bar);
-    if (fmt_has_scale(pk)) bulk_g2s(stage + L::ksOff, a.pre.ks + tile * kTileBytesS, kTileBytesS, bar);
-    if (fmt_has_scale(pv)) bulk_g2s(stage + L::vsOff, a.pre.vs + tile * kTileBytesS, kTileBytesS, bar);
+    const size_t stile = static_cast<size_t>(kvh) * a.pre.num_pages + d.phys;
+    if (fmt_has_scale(pk)) bulk_g2s(stage + L::ksOff, a.pre.ks + stile * kTileBytesS, kTileBytesS, bar);
+    if (fmt_has_scale(pv)) bulk_g2s(stage + L::vsOff, a.pre.vs + stile * kTileBytesS, kTileBytesS, bar);
   } else {
     using L = Layout<KF, VF, METER>;
     const size_t tile = static_cast<size_t>(d.phys) * a.Hkv + kvh;
@@ -737,8 +743,10 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     bulk_g2s(stage + L::kOff, a.live.k + tile * L::kBytes, L::kBytes, bar);
     bulk_g2s(stage + L::vOff, a.live.v + tile * L::vBytes, L::vBytes, bar);
     if (METER) bulk_g2s(stage + L::wOff, a.live.w + tile * kTileBytesW, kTileBytesW, bar);
-    if (fmt_has_scale(KF)) bulk_g2s(stage + L::ksOff, a.live.ks + tile * kTileBytesS, kTileBytesS, bar);
-    if (fmt_has_scale(VF)) bulk_g2s(stage + L::vsOff, a.live.vs + tile * kTileBytesS, kTileBytesS, bar);
+    // scale planes are head-major, so consecutive pages of a unit share a 128-byte line
+    const size_t stile = static_cast<size_t>(kvh) * a.live.num_pages + d.phys;
+    if (fmt_has_scale(KF)) bulk_g2s(stage + L::ksOff, a.live.ks + stile * kTileBytesS, kTileBytesS, bar);
+    if (fmt_has_scale(VF)) bulk_g2s(stage + L::vsOff, a.live.vs + stile * kTileBytesS, kTileBytesS, bar);
   }
 }
 

@@ -71,9 +71,9 @@ constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
 constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
 constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
 
+// 32 x 32 -> 64-bit product, written as plain arithmetic so the compiler can share equal products.
 __device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& hi, uint32_t& lo) {
-  uint64_t p;
-  asm("mul.wide.u32 %0, %1, %2;" : "=l"(p) : "r"(a), "r"(b));
+  const uint64_t p = static_cast<uint64_t>(a) * b;
   lo = static_cast<uint32_t>(p);
   hi = static_cast<uint32_t>(p >> 32);
 }
@@ -104,6 +104,60 @@ __device__ __forceinline__ uint4 philox4x32_10_rk(uint4 x, const uint32_t (&k0)[
   return x;
 }
 
+// The decode regenerates, per page and lane, Philox4x32-10 of the counters (slot, layer, kv_head,
+// grp) for two slots and eight channel groups.  In the first three rounds several products depend
+// only on (layer, kv_head) or only on the slot; they are computed once (PhiloxHead per page,
+// PhiloxSlot per token) and each call finishes with two products in rounds 1-2 and seven full
+// rounds.  With (H, L) the high and low words of a product and y, z, w the counters after rounds
+// 0, 1, 2:
+//   y = (H(M1 kvh) ^ layer ^ k0[0], L(M1 kvh), H(M0 slot) ^ grp ^ k1[0], L(M0 slot))
+//   z = (H(M1 y2) ^ y1 ^ k0[1], L(M1 y2), H(M0 y0) ^ y3 ^ k1[1], L(M0 y0))
+//   w = (H(M1 z2) ^ z1 ^ k0[2], L(M1 z2), H(M0 z0) ^ z3 ^ k1[2], L(M0 z0))
+// where y0, y1, L(M0 y0) depend on (layer, kv_head) only and y3, z2, H(M1 z2), L(M1 z2) on the slot.
+struct PhiloxHead {
+  uint32_t c1;  // y1 ^ k0[1]
+  uint32_t uB;  // H(M0 y0) ^ k1[1]
+  uint32_t uD;  // L(M0 y0) ^ k1[2] = z3 ^ k1[2]
+};
+struct PhiloxSlot {
+  uint32_t tA;  // H(M0 slot) ^ k1[0]            (y2 = tA ^ grp)
+  uint32_t tC;  // H(M1 z2) ^ k0[2]              (w0 = tC ^ z1)
+  uint32_t w1;  // L(M1 z2)
+};
+
+__device__ __forceinline__ PhiloxHead philox_head(uint32_t layer, uint32_t kv_head, const uint32_t (&k0)[10],
+                                                  const uint32_t (&k1)[10]) {
+  uint32_t h1, l1, h0, l0;
+  mul_wide(kPhiloxM1, kv_head, h1, l1);
+  mul_wide(kPhiloxM0, h1 ^ layer ^ k0[0], h0, l0);
+  return PhiloxHead{l1 ^ k0[1], h0 ^ k1[1], l0 ^ k1[2]};
+}
+
+__device__ __forceinline__ PhiloxSlot philox_slot(uint32_t slot, const PhiloxHead& h, const uint32_t (&k0)[10],
+                                                  const uint32_t (&k1)[10]) {
+  uint32_t h0, l0, h1, l1;
+  mul_wide(kPhiloxM0, slot, h0, l0);
+  mul_wide(kPhiloxM1, l0 ^ h.uB, h1, l1);  // z2 = y3 ^ H(M0 y0) ^ k1[1]
+  return PhiloxSlot{h0 ^ k1[0], h1 ^ k0[2], l1};
+}
+
+// Philox4x32-10 of (slot, layer, kv_head, grp) from its PhiloxHead / PhiloxSlot parts.
+__device__ __forceinline__ uint4 philox_finish(uint32_t grp, const PhiloxSlot& t, const PhiloxHead& h,
+                                               const uint32_t (&k0)[10], const uint32_t (&k1)[10]) {
+  uint32_t ah, al, bh, bl;
+  mul_wide(kPhiloxM1, t.tA ^ grp, ah, al);  // round 1: M1 y2
+  mul_wide(kPhiloxM0, ah ^ h.c1, bh, bl);   // round 2: M0 z0
+  uint4 x = make_uint4(t.tC ^ al, t.w1, bh ^ h.uD, bl);
+#pragma unroll
+  for (int r = 3; r < 10; ++r) {
+    uint32_t hi0, lo0, hi1, lo1;
+    mul_wide(kPhiloxM0, x.x, hi0, lo0);
+    mul_wide(kPhiloxM1, x.z, hi1, lo1);
+    x = make_uint4(hi1 ^ x.y ^ k0[r], lo1, hi0 ^ x.w ^ k1[r], lo0);
+  }
+  return x;
+}
+
 // Dither value of a Philox output word: ((w >> 8) + 1/2) * 2^-24 - 1/2, exact in binary32.
 __device__ __forceinline__ float dither_from_word(uint32_t w) {
   return __fmaf_rn(static_cast<float>(w >> 8), 5.9604644775390625e-8f /* 2^-24 */,
@@ -111,10 +165,12 @@ __device__ __forceinline__ float dither_from_word(uint32_t w) {
 }
 
 // Minus the dither of two words, rounded to an fp16 pair (low half from w0): the decode's tensor-core
-// operand; -xi = 1/2 - 2^-25 - (w >> 8) * 2^-24 is exact in binary32 before the fp16 rounding.
+// operand.  The top 23 bits m = w >> 9 are placed in the mantissa of a float f = 1 + m 2^-23 (no
+// int-to-float conversion); 3/2 - f is exact and exceeds -xi = 1/2 - ((w >> 8) + 1/2) 2^-24 by
+// (bit 8 of w + 1/2) 2^-24 <= 1.5 * 2^-24, far below the fp16 rounding that follows.
 __device__ __forceinline__ uint32_t neg_dither_f16x2(uint32_t w0, uint32_t w1) {
-  const float a = __fmaf_rn(static_cast<float>(w0 >> 8), -5.9604644775390625e-8f, 0.49999997019767761f);
-  const float b = __fmaf_rn(static_cast<float>(w1 >> 8), -5.9604644775390625e-8f, 0.49999997019767761f);
+  const float a = 1.5f - __uint_as_float((w0 >> 9) + 0x3F800000u);
+  const float b = 1.5f - __uint_as_float((w1 >> 9) + 0x3F800000u);
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
 }

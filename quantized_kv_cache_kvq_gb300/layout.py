@@ -64,6 +64,6 @@ def unpack_w(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:
 
 
 def unpack_s(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:
-    """scale plane -> fp16 bits [pages, heads, 16 tokens]."""
-    tiles = tiles.reshape(-1, num_kv_heads, tiles.shape[-1])
+    """scale plane (head-major tiles: head * num_pages + page) -> fp16 bits [pages, heads, 16 tokens]."""
+    tiles = tiles.reshape(num_kv_heads, -1, tiles.shape[-1]).transpose(1, 0, 2)
     return _gather16(tiles, s_offsets())
