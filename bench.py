@@ -2,8 +2,10 @@
 """Decode-step benchmark: KV GB/s of quantized-cache decode attention with the fused meter.
 
 A step is one decode step of the whole model: for every layer, append the new
-token's K/V (kvq_append) and run kvq_decode_attn over [shared prefix ++ live
-suffix]; then kvq_meter finalises the meter of every (layer, sequence, head).
+token's K/V and run the decode attention over [shared prefix ++ live suffix]
+(one kvq_decode_attn_append call, which does the append inside the decode
+kernel; --separate-append times kvq_append + kvq_decode_attn instead); then
+kvq_meter finalises the meter of every (layer, sequence, head).
 The default workload is the Qwen3-8B-shaped cartridge decode (batch 16, 36
 layers, 8 kv heads, 32 q heads, 632-token K16/V8 shared prefix with a x10 sink,
 11,996-token BF16 live suffix = 12,628 attended tokens).
@@ -52,6 +54,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
+    p.add_argument("--separate-append", action="store_true",
+                   help="kvq_append + kvq_decode_attn per layer instead of the fused kvq_decode_attn_append")
     p.add_argument("--layers", type=int, default=0, help="override layer count (profiling only; not a bench line)")
     p.add_argument("--resident-layers", type=int, default=0,
                    help="keep only this many layers' caches in HBM and run every layer call on cache l %% R "
@@ -163,6 +167,7 @@ class Model:
     """All layers' caches of one workload, filled through kvq_append, plus the step's buffers."""
 
     def __init__(self, w, device, seed_base=0, n_layers=None, resident=0):
+        self.separate_append = False
         import torch
 
         import quantized_kv_cache_kvq_gb300 as kvq
@@ -234,19 +239,24 @@ class Model:
         v_new = self.v_new if v_new is None else v_new
         for l in range(self.L):
             c = l % self.R
-            kvq.append(self.caches[c], k_new[l], v_new[l], self.new_slots, self.err)
+            kw = dict(prefix=self.prefixes[c], prefix_len=w.prefix_len, sm_scale=SM_SCALE, meter=self.mp,
+                      meter_state=self.state[l], err=self.err)
+            if self.separate_append:
+                kvq.append(self.caches[c], k_new[l], v_new[l], self.new_slots, self.err)
             if events is not None:
                 events[l][0].record()
-            kvq.decode_attn(self.caches[c], q[l], self.bt, self.seq_lens, self.out[l], self.ws,
-                            prefix=self.prefixes[c], prefix_len=w.prefix_len, sm_scale=SM_SCALE, meter=self.mp,
-                            meter_state=self.state[l], err=self.err)
+            if self.separate_append:
+                kvq.decode_attn(self.caches[c], q[l], self.bt, self.seq_lens, self.out[l], self.ws, **kw)
+            else:
+                kvq.decode_attn_append(self.caches[c], k_new[l], v_new[l], q[l], self.bt, self.seq_lens, self.out[l],
+                                       self.ws, **kw)
             if events is not None:
                 events[l][1].record()
         kvq.meter(self.state, self.L, w.batch, w.n_q_heads, self.mp, self.meter_a, self.raw_a, self.counts,
                   cert_b=self.cert_b, ranking=self.ranking)
 
     def launches_per_step(self) -> int:
-        return self.L * 3 + 1 + (1 if self.ranking is not None else 0)
+        return self.L * (3 if self.separate_append else 2) + 1 + (1 if self.ranking is not None else 0)
 
 
 def run_gpu(args, w):
@@ -268,6 +278,7 @@ def run_gpu(args, w):
     if not resident and w.name == "ragged_paged":
         resident = 4  # 36 layers of this workload need ~413 GB of cache: rotate 4 resident layers
     m = Model(w, dev, seed_base=rank, n_layers=args.layers or None, resident=resident)
+    m.separate_append = args.separate_append
     per_step_bytes = step_bytes(w, m.lens) * m.L // w.n_layers
 
     def barrier():

@@ -196,6 +196,34 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int3
                            int32_t* err_word_dev, kvq_stream_t stream);
 
 /*
+ * kvq_decode_attn_append -- one decode step's append and attention in one
+ * call: kvq_append of each sequence's newest token followed by
+ * kvq_decode_attn, with the append done inside the decode kernel by the warp
+ * that attends the page holding that token ([W] Sec. 6.2.1: the read kernel
+ * shares one data load with attention; here the write of the new token shares
+ * it too).
+ *
+ * k_new_dev, v_new_dev: [batch][num_kv_heads][128] post-RoPE key and value of
+ *   the newest token of each sequence, element type kv_dtype (KVQ_DTYPE_F32 or
+ *   KVQ_DTYPE_BF16), 16-byte aligned.  The token is live position
+ *   seq_lens[s] - 1 of sequence s; it is written at the slot the block table
+ *   gives for that position (page block_table[s][(seq_lens[s] - 1) / 16],
+ *   offset (seq_lens[s] - 1) % 16), exactly the bytes kvq_append would write
+ *   for that slot, and is attended in the same call.  Sequences with
+ *   seq_lens[s] == 0 append nothing.  The cache's witness plane is required.
+ * Every other argument, output and error is that of kvq_decode_attn; input
+ *   errors of the appended token are reported as kvq_append reports them
+ *   (KVQ_ERR_NONFINITE_INPUT, KVQ_ERR_RANGE).
+ */
+kvq_status kvq_decode_attn_append(const kvq_cache* cache, const void* k_new_dev, const void* v_new_dev,
+                                  int32_t kv_dtype, const kvq_cache* prefix, int32_t prefix_len,
+                                  const void* q_dev, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
+                                  const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                                  const int32_t* seq_lens_dev, float sm_scale, const kvq_meter_params* meter,
+                                  float* out_dev, float* meter_state_dev, void* workspace_dev, size_t ws_bytes,
+                                  int32_t* err_word_dev, kvq_stream_t stream);
+
+/*
  * kvq_decode_attn_noalloc -- kvq_decode_attn without a caller-provided
  * workspace.  No counterpart on the source pages: it exists for callers that
  * cannot allocate device memory for scratch -- a plugin or embedding host

@@ -116,6 +116,12 @@ def load(path: str = LIB_PATH):
         POINTER(_Cache), POINTER(_Cache), c_int32, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32,
         c_void_p, c_float, POINTER(MeterParams), c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p,
     ]
+    L.kvq_decode_attn_append.restype = c_int32
+    L.kvq_decode_attn_append.argtypes = [
+        POINTER(_Cache), c_void_p, c_void_p, c_int32, POINTER(_Cache), c_int32, c_void_p, c_int32, c_int32, c_int32,
+        c_void_p, c_int32, c_void_p, c_float, POINTER(MeterParams), c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
+        c_void_p,
+    ]
     L.kvq_decode_attn_noalloc.restype = c_int32
     L.kvq_decode_attn_noalloc.argtypes = [
         POINTER(_Cache), POINTER(_Cache), c_int32, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32,
@@ -232,6 +238,29 @@ def decode_attn(cache: PagedCache, q: torch.Tensor, block_table: torch.Tensor, s
         seq_lens.data_ptr(), float(sm_scale), ctypes.byref(meter) if meter is not None else None,
         out.data_ptr(), _ptr(meter_state), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _ptr(err), _stream(stream)), "kvq_decode_attn")
+
+
+def decode_attn_append(cache: PagedCache, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                       block_table: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor, *,
+                       prefix: PagedCache | None = None, prefix_len: int = 0, sm_scale: float | None = None,
+                       meter: MeterParams | None = None, meter_state: torch.Tensor | None = None,
+                       err: torch.Tensor | None = None, stream=None):
+    """kvq_decode_attn_append: append each sequence's newest token (k_new, v_new [B, Hkv, 128]) and decode."""
+    B, Hq, D = q.shape
+    assert D == HEAD_DIM and q.is_contiguous() and out.is_contiguous()
+    assert k_new.is_contiguous() and v_new.is_contiguous() and k_new.dtype == v_new.dtype and k_new.shape == v_new.shape
+    assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    d = cache.desc()
+    pd = prefix.desc() if prefix is not None else None
+    _check(lib().kvq_decode_attn_append(
+        ctypes.byref(d), k_new.data_ptr(), v_new.data_ptr(), DTYPE[k_new.dtype],
+        ctypes.byref(pd) if pd is not None else None, int(prefix_len), q.data_ptr(), DTYPE[q.dtype],
+        B, Hq, block_table.data_ptr(), int(block_table.shape[1]) if block_table.dim() == 2 else 0,
+        seq_lens.data_ptr(), float(sm_scale), ctypes.byref(meter) if meter is not None else None,
+        out.data_ptr(), _ptr(meter_state), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _ptr(err), _stream(stream)), "kvq_decode_attn_append")
 
 
 def decode_attn_noalloc(cache: PagedCache, q: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,

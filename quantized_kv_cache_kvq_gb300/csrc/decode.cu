@@ -25,18 +25,20 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float 
 }
 
 __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's pieces are complete and visible
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (gw >= static_cast<long long>(a.B) * a.Hq) return;
   const int seq = static_cast<int>(gw / a.Hq), qh = static_cast<int>(gw % a.Hq);
   const int kvh = qh / a.G, row = qh % a.G;
-  const int32_t* cum = a.ws_cum;
-  const long long T = static_cast<long long>(a.Hkv) * cum[a.B];
-  const int P = cum[seq + 1] - cum[seq];
   const int unit = seq * a.Hkv + kvh;
-  float* o = a.out + static_cast<size_t>(gw) * kHeadDim;
+  // inputs of the call are read before the wait; the decode grid's outputs only after it
   const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
+  float* o = a.out + static_cast<size_t>(gw) * kHeadDim;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's pieces are complete and visible
+  const int32_t* cum = a.ws_cum;
+  const int c0 = cum[seq], c1 = cum[seq + 1], cB = cum[a.B];
+  const long long T = static_cast<long long>(a.Hkv) * cB;
+  const int P = c1 - c0;
   if (P == 0) {
     *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
     if (a.meter_state && lane == 0)
@@ -45,16 +47,28 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
     return;
   }
   const long long W = min(static_cast<long long>(a.w_max), T);
-  const long long b_u = static_cast<long long>(a.Hkv) * cum[seq] + static_cast<long long>(kvh) * P;
+  const long long b_u = static_cast<long long>(a.Hkv) * c0 + static_cast<long long>(kvh) * P;
   const long long e_u = b_u + P;
   // warp w covers pages [T w / W, T (w + 1) / W): the warp holding page x is ((x + 1) W - 1) / T
   const long long w_lo = ((b_u + 1) * W - 1) / T, w_hi = (e_u * W - 1) / T;
   const int np = static_cast<int>(w_hi - w_lo + 1);
-  auto stats = [&](int i) { return a.ws_stats + ((static_cast<size_t>(w_lo) + i + unit) * a.G + row) * 8; };
+  const size_t p0 = static_cast<size_t>(w_lo) + unit;  // piece slot of the unit's first piece
+  auto stats = [&](int i) { return a.ws_stats + ((p0 + i) * a.G + row) * 8; };
+  auto accp = [&](int i) { return a.ws_acc + ((p0 + i) * a.G + row) * kHeadDim + 4 * lane; };
+
+  // one round of loads: every piece's statistics (lane-parallel) and the first kU pieces' partial
+  // outputs (this lane's four channels), all independent of each other
+  constexpr int kU = 16;
+  float4 v[kU];
+#pragma unroll
+  for (int k = 0; k < kU; ++k)
+    if (k < np) v[k] = *reinterpret_cast<const float4*>(accp(k));
   float m = -INFINITY, l = 0.f, mc = -INFINITY, sc = 0.f, mu = -INFINITY, su = 0.f;
+  float m_mine = -INFINITY;  // the running max of piece `lane` (pieces < 32), for the weights below
   for (int i = lane; i < np; i += 32) {
     const float4 s4 = *reinterpret_cast<const float4*>(stats(i));
     const float2 s2 = *reinterpret_cast<const float2*>(stats(i) + 4);
+    if (i < 32) m_mine = s4.x;
     lse_combine(m, l, s4.x, s4.y);
     lse_combine(mc, sc, s4.z, s4.w);
     lse_combine(mu, su, s2.x, s2.y);
@@ -69,24 +83,20 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
     lse_combine(mu, su, u2, v2);
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int kU = 8;
-  for (int i0 = 0; i0 < np; i0 += kU) {
-    float mi[kU];
-    float4 v[kU];
 #pragma unroll
-    for (int k = 0; k < kU; ++k) {
-      if (i0 + k < np) {
-        mi[k] = stats(i0 + k)[0];
-        v[k] = *reinterpret_cast<const float4*>(
-            a.ws_acc + ((static_cast<size_t>(w_lo) + i0 + k + unit) * a.G + row) * kHeadDim + 4 * lane);
-      }
+  for (int k = 0; k < kU; ++k) {
+    const float mk = __shfl_sync(kFull, m_mine, k);
+    if (k < np && mk != -INFINITY) {
+      const float wt = ex2(mk - m);
+      acc.x += v[k].x * wt; acc.y += v[k].y * wt; acc.z += v[k].z * wt; acc.w += v[k].w * wt;
     }
-#pragma unroll
-    for (int k = 0; k < kU; ++k) {
-      if (i0 + k < np && mi[k] != -INFINITY) {
-        const float wt = ex2(mi[k] - m);
-        acc.x += v[k].x * wt; acc.y += v[k].y * wt; acc.z += v[k].z * wt; acc.w += v[k].w * wt;
-      }
+  }
+  for (int i = kU; i < np; ++i) {  // units split over more than kU warps (few, long sequences)
+    const float mi = stats(i)[0];
+    if (mi != -INFINITY) {
+      const float4 vi = *reinterpret_cast<const float4*>(accp(i));
+      const float wt = ex2(mi - m);
+      acc.x += vi.x * wt; acc.y += vi.y * wt; acc.z += vi.z * wt; acc.w += vi.w * wt;
     }
   }
   const float inv = kPvShiftInv / l;
@@ -212,15 +222,22 @@ extern "C" size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads,
   return ws_layout(batch, num_kv_heads, num_q_heads, sms * kMaxWarps).total;
 }
 
-extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int32_t prefix_len,
-                                      const void* q, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
-                                      const int32_t* block_table, int32_t max_pages_per_seq,
-                                      const int32_t* seq_lens, float sm_scale, const kvq_meter_params* mp,
-                                      float* out, float* meter_state, void* workspace, size_t ws_bytes,
-                                      int32_t* err_word, kvq_stream_t stream) {
+namespace {
+
+kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_new, int32_t kv_dtype,
+                       const kvq_cache* prefix, int32_t prefix_len, const void* q, int32_t q_dtype, int32_t batch,
+                       int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
+                       const int32_t* seq_lens, float sm_scale, const kvq_meter_params* mp, float* out,
+                       float* meter_state, void* workspace, size_t ws_bytes, int32_t* err_word, cudaStream_t s) {
   const bool meter = mp != nullptr;
   kvq_status st = check_cache(cache, meter);
   if (st != KVQ_OK) return st;
+  const bool fused_append = k_new != nullptr || v_new != nullptr;
+  if (fused_append) {
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+    if (kv_dtype != KVQ_DTYPE_F32 && kv_dtype != KVQ_DTYPE_BF16) return KVQ_ERR_INVALID_ARG;
+    if (!cache->witness || !aligned16(cache->witness)) return KVQ_ERR_INVALID_ARG;
+  }
   if (prefix && prefix_len > 0) {
     if ((st = check_cache(prefix, meter)) != KVQ_OK) return st;
     if (prefix->num_kv_heads != cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
@@ -271,6 +288,9 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* p
   a.B = batch;
   a.q = q;
   a.q_bf16 = q_dtype == KVQ_DTYPE_BF16;
+  a.k_new = fused_append ? k_new : nullptr;
+  a.v_new = fused_append ? v_new : nullptr;
+  a.kv_bf16 = kv_dtype == KVQ_DTYPE_BF16;
   a.bt = block_table;
   a.max_pages = max_pages_per_seq;
   a.seq_lens = seq_lens;
@@ -305,7 +325,6 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* p
   a.stage_bytes = sb;
   const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(nw) * stages * sb;
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (pk.launch(a, sms, smem, s) != cudaSuccess) return KVQ_ERR_CUDA;
   // merge: programmatic dependent launch, so its launch overlaps the decode grid's tail
   const long long merge_threads = static_cast<long long>(batch) * num_q_heads * 32;
@@ -321,6 +340,32 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* p
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, merge_kernel, a) != cudaSuccess) return KVQ_ERR_CUDA;
   return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int32_t prefix_len,
+                                      const void* q, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
+                                      const int32_t* block_table, int32_t max_pages_per_seq,
+                                      const int32_t* seq_lens, float sm_scale, const kvq_meter_params* mp,
+                                      float* out, float* meter_state, void* workspace, size_t ws_bytes,
+                                      int32_t* err_word, kvq_stream_t stream) {
+  return decode_impl(cache, nullptr, nullptr, KVQ_DTYPE_F32, prefix, prefix_len, q, q_dtype, batch, num_q_heads,
+                     block_table, max_pages_per_seq, seq_lens, sm_scale, mp, out, meter_state, workspace, ws_bytes,
+                     err_word, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvq_status kvq_decode_attn_append(const kvq_cache* cache, const void* k_new, const void* v_new,
+                                             int32_t kv_dtype, const kvq_cache* prefix, int32_t prefix_len,
+                                             const void* q, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
+                                             const int32_t* block_table, int32_t max_pages_per_seq,
+                                             const int32_t* seq_lens, float sm_scale, const kvq_meter_params* mp,
+                                             float* out, float* meter_state, void* workspace, size_t ws_bytes,
+                                             int32_t* err_word, kvq_stream_t stream) {
+  if (!k_new || !v_new) return KVQ_ERR_INVALID_ARG;
+  return decode_impl(cache, k_new, v_new, kv_dtype, prefix, prefix_len, q, q_dtype, batch, num_q_heads, block_table,
+                     max_pages_per_seq, seq_lens, sm_scale, mp, out, meter_state, workspace, ws_bytes, err_word,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -21,7 +21,7 @@
 // u_t = sm_scale ||q|| s_t sqrt(2 ln(2S/delta_loc) / 12).
 #pragma once
 
-#include "kvq_common.cuh"
+#include "quant_row.cuh"
 
 namespace kvq {
 namespace dec {
@@ -63,6 +63,9 @@ struct Args {
   float sm_scale;
   int tier_b;
   float ln_delta_loc;
+  const void* k_new;  // [B][Hkv][128] newest token of each sequence (fused append) or nullptr
+  const void* v_new;
+  int kv_bf16;
   int32_t* ws_cum;   // [B + 1] prefix sums of pages per sequence (written by CTA 0)
   float* out;        // [B][Hq][128]
   float* meter_state;  // [B][Hq][4] or nullptr
@@ -674,11 +677,13 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
 struct Desc {
   int32_t phys;   // physical page in its cache (-1: out of range, skipped)
   uint32_t info;  // unit (bits 0..22) | nvalid (bits 23..27) | prefix segment (bit 28) | present (bit 29)
+                  // | last live page of the unit (bit 30)
 };
 __device__ __forceinline__ int d_unit(uint32_t i) { return static_cast<int>(i & 0x7FFFFFu); }
 __device__ __forceinline__ int d_nvalid(uint32_t i) { return static_cast<int>((i >> 23) & 31u); }
 __device__ __forceinline__ bool d_prefix(uint32_t i) { return (i >> 28) & 1u; }
 __device__ __forceinline__ bool d_present(uint32_t i) { return (i >> 29) & 1u; }
+__device__ __forceinline__ bool d_last(uint32_t i) { return (i >> 30) & 1u; }
 
 __device__ __forceinline__ Desc make_desc(const Args& a, const int32_t* cum, long long x, long long x_end) {
   Desc d{-1, 0u};
@@ -711,8 +716,9 @@ __device__ __forceinline__ Desc make_desc(const Args& a, const int32_t* cum, lon
       phys = -1;
     }
   }
+  const uint32_t last = (!pre && p == P - 1) ? 1u : 0u;
   d.phys = phys;
-  d.info = static_cast<uint32_t>(unit) | (static_cast<uint32_t>(nvalid) << 23) | (pre << 28) | (1u << 29);
+  d.info = static_cast<uint32_t>(unit) | (static_cast<uint32_t>(nvalid) << 23) | (pre << 28) | (1u << 29) | (last << 30);
   return d;
 }
 
@@ -777,6 +783,33 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
       }
     }
   }
+}
+
+// Fused append: the warp that holds a unit's last live page quantizes the sequence's newest token
+// (position seq_len - 1, token t of the page) for its kv head, writes it to the cache and into the
+// staged copy of the page, so the page is attended with the token in place.  The same per-row
+// quantizer as kvq_append, so the stored bytes are identical.
+template <int KF, int VF, bool METER>
+__device__ __noinline__ void append_newest(const Args& a, uint8_t* st, int phys, int unit, int t) {
+  using L = Layout<KF, VF, METER>;
+  const int lane = threadIdx.x & 31;
+  const int kvh = unit % a.Hkv;
+  float k[4], v[4];
+  load_row4(a.k_new, a.v_new, a.kv_bf16, static_cast<size_t>(unit) * kHeadDim + lane * 4, k, v);
+  const uint64_t seed = (static_cast<uint64_t>(a.live.seed_hi) << 32) | a.live.seed_lo;
+  const RowCodes rc = quantize_row<KF, VF>(k, v, static_cast<uint32_t>(phys) * kPage + t, a.live.layer,
+                                           static_cast<uint32_t>(kvh), seed);
+  const size_t tile = static_cast<size_t>(phys) * a.Hkv + kvh;
+  const size_t stile = static_cast<size_t>(kvh) * a.live.num_pages + phys;  // scale planes: head-major
+  store_row<KF, VF>(rc, t, const_cast<uint8_t*>(a.live.k) + tile * L::kBytes,
+                    const_cast<uint8_t*>(a.live.v) + tile * L::vBytes,
+                    fmt_has_scale(KF) ? const_cast<uint8_t*>(a.live.ks) + stile * kTileBytesS : nullptr,
+                    fmt_has_scale(VF) ? const_cast<uint8_t*>(a.live.vs) + stile * kTileBytesS : nullptr,
+                    const_cast<uint8_t*>(a.live.w) + tile * kTileBytesW);
+  store_row<KF, VF>(rc, t, st + L::kOff, st + L::vOff, fmt_has_scale(KF) ? st + L::ksOff : nullptr,
+                    fmt_has_scale(VF) ? st + L::vsOff : nullptr, METER ? st + L::wOff : nullptr);
+  if (lane == 0) report_row(rc, a.err);
+  __syncwarp();
 }
 
 // Zero the bytes of tokens nvalid..15 in a stage (a partial last page): the slots past the end of a
@@ -928,6 +961,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
                                     qk_scale, a.tier_b != 0);
       } else {
         if (nvalid < kPage) zero_tail<KF, VF, METER>(st, nvalid);
+        if (a.k_new && d_last(info)) append_newest<KF, VF, METER>(a, st, phys, u, nvalid - 1);
         process_page<KF, VF, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f, s,
                                     qk_scale, a.tier_b != 0);
       }
