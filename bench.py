@@ -41,7 +41,8 @@ import workloads as W  # noqa: E402
 METRIC = "decode-attn KV GB/s (% of GB300 HBM peak) with meter on; attended tok/s"
 SM_SCALE = float(np.float32(1.0 / math.sqrt(128)))
 KERNEL_SOURCES = ["quantized_kv_cache_kvq_gb300/csrc/decode_kernel.cuh", "quantized_kv_cache_kvq_gb300/csrc/decode.cu",
-                  "quantized_kv_cache_kvq_gb300/csrc/kvq_common.cuh"]
+                  "quantized_kv_cache_kvq_gb300/csrc/kvq_common.cuh", "quantized_kv_cache_kvq_gb300/csrc/quant_row.cuh",
+                  "quantized_kv_cache_kvq_gb300/csrc/decode_instances.inc"]
 
 
 def parse():

@@ -198,10 +198,11 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int3
 /*
  * kvq_decode_attn_append -- one decode step's append and attention in one
  * call: kvq_append of each sequence's newest token followed by
- * kvq_decode_attn, with the append done inside the decode kernel by the warp
- * that attends the page holding that token ([W] Sec. 6.2.1: the read kernel
- * shares one data load with attention; here the write of the new token shares
- * it too).
+ * kvq_decode_attn.  The append runs as a small grid ahead of the decode; the
+ * decode is launched as its programmatic dependent, runs alongside it, and
+ * waits for it only before loading a page that holds a new token, so the
+ * append costs no separate step on the GPU timeline ([W] Sec. 6.2.1: quantize
+ * on write with the dither the read side regenerates).
  *
  * k_new_dev, v_new_dev: [batch][num_kv_heads][128] post-RoPE key and value of
  *   the newest token of each sequence, element type kv_dtype (KVQ_DTYPE_F32 or

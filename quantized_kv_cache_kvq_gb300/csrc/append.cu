@@ -44,6 +44,57 @@ __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __
   if (lane == 0) report_row(rc, err);
 }
 
+// The newest token of every sequence (live position seq_lens[s] - 1, its slot from the block
+// table), one warp per (sequence, kv head); launched ahead of a decode that waits for it only where
+// it reads those pages (programmatic dependent launch).
+template <int KF, int VF>
+__global__ void __launch_bounds__(256) append_newest_kernel(kvq_cache c, const void* __restrict__ kin,
+                                                            const void* __restrict__ vin, int in_bf16,
+                                                            const int32_t* __restrict__ block_table, int max_pages,
+                                                            const int32_t* __restrict__ seq_lens, int batch,
+                                                            int32_t* err) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int H = c.num_kv_heads;
+  if (row >= static_cast<long long>(batch) * H) return;
+  const int seq = static_cast<int>(row / H);
+  const int head = static_cast<int>(row % H);
+  const int len = seq_lens[seq];
+  if (len <= 0) return;
+  if (len > max_pages * kPage) {
+    if (lane == 0) report(err, KVQ_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int pos = len - 1;
+  const int page = block_table[static_cast<size_t>(seq) * max_pages + pos / kPage];
+  const int t = pos % kPage;
+  if (page < 0 || page >= c.num_pages) {
+    if (lane == 0) report(err, KVQ_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int slot = page * kPage + t;
+  float k[4], v[4];
+  load_row4(kin, vin, in_bf16, static_cast<size_t>(row) * kHeadDim + lane * 4, k, v);
+  const RowCodes rc = quantize_row<KF, VF>(k, v, static_cast<uint32_t>(slot), static_cast<uint32_t>(c.layer),
+                                           static_cast<uint32_t>(head), c.dither_seed);
+  const size_t tile = static_cast<size_t>(page) * H + head;
+  const size_t stile = static_cast<size_t>(head) * c.num_pages + page;
+  store_row<KF, VF>(rc, t, static_cast<uint8_t*>(c.k_data) + tile * tile_bytes_k(KF),
+                    static_cast<uint8_t*>(c.v_data) + tile * tile_bytes_v(VF),
+                    fmt_has_scale(KF) ? reinterpret_cast<uint8_t*>(c.k_scale) + stile * kTileBytesS : nullptr,
+                    fmt_has_scale(VF) ? reinterpret_cast<uint8_t*>(c.v_scale) + stile * kTileBytesS : nullptr,
+                    reinterpret_cast<uint8_t*>(c.witness) + tile * kTileBytesW);
+  if (lane == 0) report_row(rc, err);
+}
+
+struct NewestArgs {
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  int batch;
+};
+
 template <int KF, int VF>
 cudaError_t launch_append(const kvq_cache& c, const void* k, const void* v, int in_bf16, const int32_t* slots,
                           int n, int32_t* err, cudaStream_t s) {
@@ -54,14 +105,28 @@ cudaError_t launch_append(const kvq_cache& c, const void* k, const void* v, int 
   return cudaGetLastError();
 }
 
+template <int KF, int VF>
+cudaError_t launch_any(const kvq_cache& c, const void* k, const void* v, int in_bf16, const int32_t* slots, int n,
+                       int32_t* err, cudaStream_t s, const NewestArgs* newest) {
+  const int threads = 256;
+  if (newest) {
+    const long long rows = static_cast<long long>(newest->batch) * c.num_kv_heads;
+    const long long blocks = (rows * 32 + threads - 1) / threads;
+    append_newest_kernel<KF, VF><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+        c, k, v, in_bf16, newest->block_table, newest->max_pages, newest->seq_lens, newest->batch, err);
+    return cudaGetLastError();
+  }
+  return launch_append<KF, VF>(c, k, v, in_bf16, slots, n, err, s);
+}
+
 template <int KF>
 cudaError_t dispatch_v(int vf, const kvq_cache& c, const void* k, const void* v, int b, const int32_t* sl, int n,
-                       int32_t* e, cudaStream_t s) {
+                       int32_t* e, cudaStream_t s, const NewestArgs* nw = nullptr) {
   switch (vf) {
-    case KVQ_FMT_BF16: return launch_append<KF, KVQ_FMT_BF16>(c, k, v, b, sl, n, e, s);
-    case KVQ_FMT_E4M3: return launch_append<KF, KVQ_FMT_E4M3>(c, k, v, b, sl, n, e, s);
-    case KVQ_FMT_E4M3_SCALED: return launch_append<KF, KVQ_FMT_E4M3_SCALED>(c, k, v, b, sl, n, e, s);
-    case KVQ_FMT_INT8_DITHER: return launch_append<KF, KVQ_FMT_INT8_DITHER>(c, k, v, b, sl, n, e, s);
+    case KVQ_FMT_BF16: return launch_any<KF, KVQ_FMT_BF16>(c, k, v, b, sl, n, e, s, nw);
+    case KVQ_FMT_E4M3: return launch_any<KF, KVQ_FMT_E4M3>(c, k, v, b, sl, n, e, s, nw);
+    case KVQ_FMT_E4M3_SCALED: return launch_any<KF, KVQ_FMT_E4M3_SCALED>(c, k, v, b, sl, n, e, s, nw);
+    case KVQ_FMT_INT8_DITHER: return launch_any<KF, KVQ_FMT_INT8_DITHER>(c, k, v, b, sl, n, e, s, nw);
   }
   return cudaErrorInvalidValue;
 }
@@ -130,6 +195,22 @@ extern "C" kvq_status kvq_append(const kvq_cache* c, const void* k, const void* 
   }
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
+
+namespace kvq {
+// Library-internal: the append kernel of kvq_decode_attn_append (arguments checked by the caller).
+cudaError_t launch_append_newest(const kvq_cache& c, const void* k, const void* v, int in_bf16,
+                                 const int32_t* block_table, int max_pages, const int32_t* seq_lens, int batch,
+                                 int32_t* err, cudaStream_t s) {
+  const NewestArgs nw{block_table, max_pages, seq_lens, batch};
+  switch (c.k_fmt) {
+    case KVQ_FMT_BF16: return dispatch_v<KVQ_FMT_BF16>(c.v_fmt, c, k, v, in_bf16, nullptr, 0, err, s, &nw);
+    case KVQ_FMT_E4M3: return dispatch_v<KVQ_FMT_E4M3>(c.v_fmt, c, k, v, in_bf16, nullptr, 0, err, s, &nw);
+    case KVQ_FMT_E4M3_SCALED: return dispatch_v<KVQ_FMT_E4M3_SCALED>(c.v_fmt, c, k, v, in_bf16, nullptr, 0, err, s, &nw);
+    case KVQ_FMT_INT8_DITHER: return dispatch_v<KVQ_FMT_INT8_DITHER>(c.v_fmt, c, k, v, in_bf16, nullptr, 0, err, s, &nw);
+  }
+  return cudaErrorInvalidValue;
+}
+}  // namespace kvq
 
 extern "C" kvq_status kvq_debug_dither(uint64_t seed, int32_t layer, int32_t kv_head, const int32_t* slots, int32_t n,
                                        float* xi, kvq_stream_t stream) {

@@ -10,6 +10,10 @@
 #undef KVQ_X
 
 namespace kvq {
+cudaError_t launch_append_newest(const kvq_cache& c, const void* k, const void* v, int in_bf16,
+                                 const int32_t* block_table, int max_pages, const int32_t* seq_lens, int batch,
+                                 int32_t* err, cudaStream_t s);  // append.cu
+
 namespace dec {
 
 // ------------------------------------------------------------------------------------------------
@@ -197,7 +201,7 @@ Planes planes_of(const kvq_cache* c) {
   return p;
 }
 
-using Launcher = cudaError_t (*)(const Args&, int, size_t, cudaStream_t);
+using Launcher = cudaError_t (*)(const Args&, int, size_t, cudaStream_t, bool);
 
 struct Pick {
   Launcher launch;
@@ -288,9 +292,7 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   a.B = batch;
   a.q = q;
   a.q_bf16 = q_dtype == KVQ_DTYPE_BF16;
-  a.k_new = fused_append ? k_new : nullptr;
-  a.v_new = fused_append ? v_new : nullptr;
-  a.kv_bf16 = kv_dtype == KVQ_DTYPE_BF16;
+  a.wait_append = fused_append ? 1 : 0;
   a.bt = block_table;
   a.max_pages = max_pages_per_seq;
   a.seq_lens = seq_lens;
@@ -325,7 +327,14 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   a.stage_bytes = sb;
   const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(nw) * stages * sb;
 
-  if (pk.launch(a, sms, smem, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (fused_append) {
+    // the newest tokens first; the decode is a programmatic dependent of that grid and waits for it
+    // only before it loads a page that holds one of them
+    if (launch_append_newest(*cache, k_new, v_new, kv_dtype == KVQ_DTYPE_BF16, block_table, max_pages_per_seq,
+                             seq_lens, batch, err_word, s) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+  }
+  if (pk.launch(a, sms, smem, s, fused_append) != cudaSuccess) return KVQ_ERR_CUDA;
   // merge: programmatic dependent launch, so its launch overlaps the decode grid's tail
   const long long merge_threads = static_cast<long long>(batch) * num_q_heads * 32;
   cudaLaunchConfig_t cfg = {};

@@ -21,7 +21,7 @@
 // u_t = sm_scale ||q|| s_t sqrt(2 ln(2S/delta_loc) / 12).
 #pragma once
 
-#include "quant_row.cuh"
+#include "kvq_common.cuh"
 
 namespace kvq {
 namespace dec {
@@ -63,9 +63,7 @@ struct Args {
   float sm_scale;
   int tier_b;
   float ln_delta_loc;
-  const void* k_new;  // [B][Hkv][128] newest token of each sequence (fused append) or nullptr
-  const void* v_new;
-  int kv_bf16;
+  int wait_append;   // the preceding grid appends each sequence's newest token (programmatic launch)
   int32_t* ws_cum;   // [B + 1] prefix sums of pages per sequence (written by CTA 0)
   float* out;        // [B][Hq][128]
   float* meter_state;  // [B][Hq][4] or nullptr
@@ -745,6 +743,11 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
   } else {
     using L = Layout<KF, VF, METER>;
     const size_t tile = static_cast<size_t>(d.phys) * a.Hkv + kvh;
+    if (a.wait_append && d_last(d.info)) {
+      // the page holding the sequence's newest token: the append grid must have completed
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
     mbar_arrive_expect_tx(bar, L::total);
     bulk_g2s(stage + L::kOff, a.live.k + tile * L::kBytes, L::kBytes, bar);
     bulk_g2s(stage + L::vOff, a.live.v + tile * L::vBytes, L::vBytes, bar);
@@ -783,33 +786,6 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
       }
     }
   }
-}
-
-// Fused append: the warp that holds a unit's last live page quantizes the sequence's newest token
-// (position seq_len - 1, token t of the page) for its kv head, writes it to the cache and into the
-// staged copy of the page, so the page is attended with the token in place.  The same per-row
-// quantizer as kvq_append, so the stored bytes are identical.
-template <int KF, int VF, bool METER>
-__device__ __noinline__ void append_newest(const Args& a, uint8_t* st, int phys, int unit, int t) {
-  using L = Layout<KF, VF, METER>;
-  const int lane = threadIdx.x & 31;
-  const int kvh = unit % a.Hkv;
-  float k[4], v[4];
-  load_row4(a.k_new, a.v_new, a.kv_bf16, static_cast<size_t>(unit) * kHeadDim + lane * 4, k, v);
-  const uint64_t seed = (static_cast<uint64_t>(a.live.seed_hi) << 32) | a.live.seed_lo;
-  const RowCodes rc = quantize_row<KF, VF>(k, v, static_cast<uint32_t>(phys) * kPage + t, a.live.layer,
-                                           static_cast<uint32_t>(kvh), seed);
-  const size_t tile = static_cast<size_t>(phys) * a.Hkv + kvh;
-  const size_t stile = static_cast<size_t>(kvh) * a.live.num_pages + phys;  // scale planes: head-major
-  store_row<KF, VF>(rc, t, const_cast<uint8_t*>(a.live.k) + tile * L::kBytes,
-                    const_cast<uint8_t*>(a.live.v) + tile * L::vBytes,
-                    fmt_has_scale(KF) ? const_cast<uint8_t*>(a.live.ks) + stile * kTileBytesS : nullptr,
-                    fmt_has_scale(VF) ? const_cast<uint8_t*>(a.live.vs) + stile * kTileBytesS : nullptr,
-                    const_cast<uint8_t*>(a.live.w) + tile * kTileBytesW);
-  store_row<KF, VF>(rc, t, st + L::kOff, st + L::vOff, fmt_has_scale(KF) ? st + L::ksOff : nullptr,
-                    fmt_has_scale(VF) ? st + L::vsOff : nullptr, METER ? st + L::wOff : nullptr);
-  if (lane == 0) report_row(rc, a.err);
-  __syncwarp();
 }
 
 // Zero the bytes of tokens nvalid..15 in a stage (a partial last page): the slots past the end of a
@@ -961,7 +937,6 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
                                     qk_scale, a.tier_b != 0);
       } else {
         if (nvalid < kPage) zero_tail<KF, VF, METER>(st, nvalid);
-        if (a.k_new && d_last(info)) append_newest<KF, VF, METER>(a, st, phys, u, nvalid - 1);
         process_page<KF, VF, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f, s,
                                     qk_scale, a.tier_b != 0);
       }
@@ -997,8 +972,10 @@ namespace kvq {
 namespace dec {
 
 // Host launcher of one instantiation (the dynamic shared-memory limit is raised once per kernel).
+// `programmatic`: launch as a programmatic dependent of the preceding grid in the stream (the
+// fused append), which the kernel waits for where it reads that grid's output.
 template <int KF, int VF, int PKF, int PVF, int NW, bool METER>
-cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s, bool programmatic) {
   auto kern = decode_split_kernel<KF, VF, PKF, PVF, NW, METER>;
   static size_t configured = 0;  // largest dynamic smem size set so far
   if (smem > configured) {
@@ -1006,8 +983,21 @@ cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<grid, NW * 32, smem, s>>>(a);
-  return cudaGetLastError();
+  if (!programmatic) {
+    kern<<<grid, NW * 32, smem, s>>>(a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace dec
@@ -1016,6 +1006,8 @@ cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s) 
 // Explicit instantiations are listed once, in decode_instances.inc, and split across translation
 // units so they compile in parallel.
 #define KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, M) \
-  template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M>(const kvq::dec::Args&, int, size_t, cudaStream_t);
+  template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M>(const kvq::dec::Args&, int, size_t, cudaStream_t, \
+                                                                         bool);
 #define KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, M) \
-  extern template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M>(const kvq::dec::Args&, int, size_t, cudaStream_t);
+  extern template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M>(const kvq::dec::Args&, int, size_t, \
+                                                                                cudaStream_t, bool);
