@@ -40,8 +40,9 @@ import workloads as W  # noqa: E402
 
 METRIC = "decode-attn KV GB/s (% of GB300 HBM peak) with meter on; attended tok/s"
 SM_SCALE = float(np.float32(1.0 / math.sqrt(128)))
-KERNEL_SOURCES = ["quantized_kv_cache_kvq_gb300/csrc/decode_kernel.cuh", "quantized_kv_cache_kvq_gb300/csrc/decode.cu",
-                  "quantized_kv_cache_kvq_gb300/csrc/kvq_common.cuh", "quantized_kv_cache_kvq_gb300/csrc/quant_row.cuh",
+# device sources of decode_split_kernel (the roofline kernel): its recorded DRAM traffic is valid only
+# for the exact sources it was captured from
+KERNEL_SOURCES = ["quantized_kv_cache_kvq_gb300/csrc/decode_kernel.cuh", "quantized_kv_cache_kvq_gb300/csrc/kvq_common.cuh",
                   "quantized_kv_cache_kvq_gb300/csrc/decode_instances.inc"]
 
 
@@ -246,6 +247,7 @@ class Model:
                 kvq.append(self.caches[c], k_new[l], v_new[l], self.new_slots, self.err)
             if events is not None:
                 events[l][0].record()
+                kvq.debug_time_decode(events[l][2], events[l][3])
             if self.separate_append:
                 kvq.decode_attn(self.caches[c], q[l], self.bt, self.seq_lens, self.out[l], self.ws, **kw)
             else:
@@ -253,6 +255,7 @@ class Model:
                                        self.ws, **kw)
             if events is not None:
                 events[l][1].record()
+                kvq.debug_time_decode(None, None)
         kvq.meter(self.state, self.L, w.batch, w.n_q_heads, self.mp, self.meter_a, self.raw_a, self.counts,
                   cert_b=self.cert_b, ranking=self.ranking)
 
@@ -311,10 +314,17 @@ def run_gpu(args, w):
         stop.record()
         barrier()
     ms = start.elapsed_time(stop)
-    # per-launch duration of kvq_decode_attn: CUDA events around every layer's call, eager steps
+    # per-launch duration of the decode kernel (the dominant one): CUDA events the library records on
+    # the call's stream right before and after that kernel's launch (kvq_debug_time_decode), eager
+    # steps; plus events around each whole call (append + decode + merge)
     n_ev = max(1, min(args.steps, 20))
-    events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(m.L)]
+    events = [[tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(m.L)]
               for _ in range(n_ev)]
+    for st in events:
+        for e4 in st:
+            for e in e4:
+                e.record()  # creates the underlying CUDA event
+    torch.cuda.synchronize()
     barrier()
     for s in range(n_ev):
         m.step(events=events[s])
@@ -327,13 +337,15 @@ def run_gpu(args, w):
         raise RuntimeError(f"device error {kvq.STATUS.get(m.err.item())}")
     ms_step = ms / args.steps
     value = per_step_bytes * world / (ms_step * 1e-3) / 1e9
-    layer_ms = [e[0].elapsed_time(e[1]) for st in events for e in st]
+    layer_ms = [e[2].elapsed_time(e[3]) for st in events for e in st]
+    call_ms = [e[0].elapsed_time(e[1]) for st in events for e in st]
     layer_bytes = per_step_bytes / m.L
     achieved = layer_bytes / (statistics.mean(layer_ms) * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     tr = traffic_record(w.name)
     attended = float(np.sum(m.lens) + w.prefix_len * w.batch) * m.L * w.n_kv_heads
     res = dict(value=value, ms_step=ms_step, achieved=achieved, graph=graph is not None, layer_ms_mean=statistics.mean(layer_ms),
+               call_ms_mean=statistics.mean(call_ms),
                layer_ms_median=statistics.median(layer_ms), peak=peak, peak_kind=peak_kind, traffic=tr,
                clocks=clk.summary(), launches=m.launches_per_step() * args.steps, attended=attended,
                per_step_bytes=per_step_bytes, world=world, rank=rank, counts=m.counts.cpu().tolist(),
@@ -501,10 +513,11 @@ def main():
             "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
                          "frac": r["achieved"] / r["peak"],
                          "traffic": (r["traffic"]["bytes_per_launch"] if r["traffic"] else None),
-                         "kernel": "kvq_decode_attn (decode_split_kernel + merge_kernel)",
+                         "kernel": "decode_split_kernel (CUDA events around its launch, eager steps)",
                          "peak_source": f"{r['peak_kind']} hbm_gbs",
                          "algorithmic_bytes_per_launch": r["per_step_bytes"] // (args.layers or w.n_layers),
-                         "launch_ms_mean": r["layer_ms_mean"]},
+                         "launch_ms_mean": r["layer_ms_mean"],
+                         "call_ms_mean": r["call_ms_mean"]},
             "gpu_launches": r["launches"], "clocks": r["clocks"], "meter_counts": r["counts"],
             "launch_mode": "cuda_graph" if r["graph"] else "eager"}
     if r["resident"] < (args.layers or w.n_layers):

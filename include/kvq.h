@@ -287,6 +287,13 @@ kvq_status kvq_debug_encode(int32_t kind, const float* x_dev, int64_t n, void* o
    stays usable.  Exercises the failure path without faulting or hanging the GPU. */
 kvq_status kvq_debug_wait_timeout(uint64_t limit_ns, int32_t* err_word_dev, kvq_stream_t stream);
 
+/* Measurement hook: while set (both non-NULL, cudaEvent_t handles), every decode call made from
+   this host thread records start_event immediately before the decode kernel's launch and
+   stop_event immediately after it, on the call's stream, so the kernel's own duration can be timed
+   apart from the append and merge launches around it (a fused call then launches the decode after
+   its append instead of overlapping them).  NULL, NULL clears it. */
+kvq_status kvq_debug_time_decode(void* start_event, void* stop_event);
+
 /* Human-readable name of a status code (static storage). */
 const char* kvq_status_string(int32_t status);
 

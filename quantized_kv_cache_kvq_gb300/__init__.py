@@ -134,6 +134,8 @@ def load(path: str = LIB_PATH):
     L.kvq_debug_dither.argtypes = [c_uint64, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p]
     L.kvq_debug_encode.restype = c_int32
     L.kvq_debug_encode.argtypes = [c_int32, c_void_p, c_int64, c_void_p, c_void_p]
+    L.kvq_debug_time_decode.restype = c_int32
+    L.kvq_debug_time_decode.argtypes = [c_void_p, c_void_p]
     L.kvq_debug_wait_timeout.restype = c_int32
     L.kvq_debug_wait_timeout.argtypes = [c_uint64, c_void_p, c_void_p]
     L.kvq_status_string.restype = ctypes.c_char_p
@@ -297,6 +299,14 @@ def meter(meter_state: torch.Tensor, n_layers: int, batch: int, num_q_heads: int
 def debug_dither(seed: int, layer: int, kv_head: int, slots: torch.Tensor, out: torch.Tensor, stream=None):
     _check(lib().kvq_debug_dither(seed & 0xFFFFFFFFFFFFFFFF, layer, kv_head, slots.data_ptr(), int(slots.numel()),
                                   out.data_ptr(), _stream(stream)), "kvq_debug_dither")
+
+
+def debug_time_decode(start: "torch.cuda.Event | None", stop: "torch.cuda.Event | None"):
+    """kvq_debug_time_decode: record these events around every decode kernel launch (None, None clears)."""
+    if start is None or stop is None:
+        _check(lib().kvq_debug_time_decode(None, None), "kvq_debug_time_decode")
+        return
+    _check(lib().kvq_debug_time_decode(start.cuda_event, stop.cuda_event), "kvq_debug_time_decode")
 
 
 def debug_wait_timeout(limit_ns: int, err: torch.Tensor, stream=None):

@@ -228,6 +228,9 @@ extern "C" size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads,
 
 namespace {
 
+// Measurement hook (kvq_debug_time_decode): events recorded around the decode kernel's launch.
+thread_local cudaEvent_t g_time_start = nullptr, g_time_stop = nullptr;
+
 kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_new, int32_t kv_dtype,
                        const kvq_cache* prefix, int32_t prefix_len, const void* q, int32_t q_dtype, int32_t batch,
                        int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
@@ -334,7 +337,9 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
                              seq_lens, batch, err_word, s) != cudaSuccess)
       return KVQ_ERR_CUDA;
   }
-  if (pk.launch(a, sms, smem, s, fused_append) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (g_time_start && cudaEventRecord(g_time_start, s) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (pk.launch(a, sms, smem, s, fused_append && !g_time_start) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (g_time_stop && cudaEventRecord(g_time_stop, s) != cudaSuccess) return KVQ_ERR_CUDA;
   // merge: programmatic dependent launch, so its launch overlaps the decode grid's tail
   const long long merge_threads = static_cast<long long>(batch) * num_q_heads * 32;
   cudaLaunchConfig_t cfg = {};
@@ -352,6 +357,13 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
 }
 
 }  // namespace
+
+extern "C" kvq_status kvq_debug_time_decode(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return KVQ_ERR_INVALID_ARG;
+  g_time_start = static_cast<cudaEvent_t>(start_event);
+  g_time_stop = static_cast<cudaEvent_t>(stop_event);
+  return KVQ_OK;
+}
 
 extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int32_t prefix_len,
                                       const void* q, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
