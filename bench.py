@@ -98,6 +98,16 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# Issue roofline of a path bound by integer arithmetic and instruction issue (the INT8-dithered decode
+# regenerates every element's dither with Philox4x32-10): each of a GB300's 152 SMs has 4 schedulers
+# that each issue at most one warp-instruction per clock, at most 2070 MHz.
+GB300_SMS, GB300_SCHEDULERS_PER_SM, GB300_MAX_SM_MHZ = 152, 4, 2070.0
+
+
+def issue_peak_winst_per_s(sm_mhz: float = GB300_MAX_SM_MHZ) -> float:
+    return GB300_SMS * GB300_SCHEDULERS_PER_SM * sm_mhz * 1e6
+
+
 def traffic_record(workload: str):
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(p):
@@ -357,6 +367,33 @@ def run_gpu(args, w):
     return res
 
 
+def roofline_of(r, w, args) -> dict:
+    """Roofline object of the dominant kernel (decode_split_kernel): HBM-bound layouts against the measured
+    copy peak; the INT8-dithered layout (record marked "alu") against the issue peak, with its HBM figures
+    alongside."""
+    rec = r["traffic"]
+    launch_s = r["layer_ms_mean"] * 1e-3
+    hbm = {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
+           "frac": r["achieved"] / r["peak"], "traffic": (rec["bytes_per_launch"] if rec else None),
+           "kernel": "decode_split_kernel (CUDA events around its launch, eager steps)",
+           "peak_source": f"{r['peak_kind']} hbm_gbs",
+           "algorithmic_bytes_per_launch": r["per_step_bytes"] // (args.layers or w.n_layers),
+           "launch_ms_mean": r["layer_ms_mean"], "call_ms_mean": r["call_ms_mean"]}
+    if not rec or rec.get("bound") != "alu":
+        return hbm
+    achieved = rec["warp_inst_per_launch"] / launch_s
+    peak = issue_peak_winst_per_s()
+    out = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "warp-instructions/s", "frac": achieved / peak,
+           "traffic": rec["bytes_per_launch"], "kernel": hbm["kernel"],
+           "peak_source": f"{GB300_SMS} SMs x {GB300_SCHEDULERS_PER_SM} schedulers x 1 warp-instruction/clock x "
+                          f"{GB300_MAX_SM_MHZ:.0f} MHz",
+           "warp_inst_per_launch": rec["warp_inst_per_launch"],
+           "hbm_achieved_gbs": r["achieved"], "hbm_frac": r["achieved"] / r["peak"],
+           "algorithmic_bytes_per_launch": hbm["algorithmic_bytes_per_launch"],
+           "launch_ms_mean": r["layer_ms_mean"], "call_ms_mean": r["call_ms_mean"]}
+    return out
+
+
 def run_e2e(args, m, per_step_bytes, world, use_graph=True):
     """Same metric through the public API with pinned host buffers and copies in the timed region."""
     torch = m.torch
@@ -510,14 +547,7 @@ def main():
             "pct_of_hbm_peak": 100.0 * r["value"] / r["world"] / r["peak"],
             "attended_kv_tok_per_s": r["attended"] * r["world"] / (r["ms_step"] * 1e-3),
             "seq_tok_per_s": w.batch * r["world"] / (r["ms_step"] * 1e-3),
-            "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
-                         "frac": r["achieved"] / r["peak"],
-                         "traffic": (r["traffic"]["bytes_per_launch"] if r["traffic"] else None),
-                         "kernel": "decode_split_kernel (CUDA events around its launch, eager steps)",
-                         "peak_source": f"{r['peak_kind']} hbm_gbs",
-                         "algorithmic_bytes_per_launch": r["per_step_bytes"] // (args.layers or w.n_layers),
-                         "launch_ms_mean": r["layer_ms_mean"],
-                         "call_ms_mean": r["call_ms_mean"]},
+            "roofline": roofline_of(r, w, args),
             "gpu_launches": r["launches"], "clocks": r["clocks"], "meter_counts": r["counts"],
             "launch_mode": "cuda_graph" if r["graph"] else "eager"}
     if r["resident"] < (args.layers or w.n_layers):
