@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -130,7 +131,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"kvq_clocks_{os.getpid()}_{index}.csv")
 
     def __enter__(self):
         try:
@@ -170,6 +171,10 @@ class ClockSampler:
                 for n, v in zip(names, parts[4:8]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sms)}
 

@@ -22,6 +22,16 @@ Everything is float64 and follows WitCert (arXiv 2607.28699):
   under one softmax (the caller concatenates them before calling this module).
 
 The output is o = sum_t p~_t v_hat_t with the dequantized values.
+
+Value side (WitCert §3, the statement that TV propagates linearly to the output):
+with y = sum_t p_t v_t the exact output and y_hat = sum_t p~_t v_hat_t,
+
+    ||y - y_hat|| <= 2 TV max_t ||v_t|| + sum_t p~_t rho^v_t,   rho^v_t = ||v_hat_t - v_t||,
+
+(split y - y_hat = sum_t (p_t - p~_t) v_t + sum_t p~_t (v_t - v_hat_t) and bound each sum by
+the triangle inequality).  With the meter in place of TV and the stored fp16 round-up
+value witness (rho^v_t, ||v_t||), the output-error bound is
+2 min(1, 1/2 (A^2 - 1)) Vmax + R with R = sum_t p~_t rho^v_t and Vmax = max_t ||v_t||.
 """
 from __future__ import annotations
 
@@ -47,6 +57,8 @@ __all__ = [
     "decode_head",
     "flawed_dispersion_bound",
     "two_sided_bound",
+    "value_side",
+    "output_error_bound",
 ]
 
 
@@ -135,17 +147,23 @@ class DecodeResult:
     log_am1_b: np.ndarray    # [H] ln(A_B - 1), Tier B (nan when not requested)
     cert_b: np.ndarray       # [H] min(1, 1/2 (A_B^2 - 1)) (nan when not requested)
     c_max: np.ndarray        # [H] max_t c_t (diagnostic)
+    value_r: np.ndarray | None = None      # [H] R = sum_t p~_t rho^v_t (value witness given)
+    value_vmax: float | None = None        # max_t ||v_t|| (value witness given)
+    out_bound_a: np.ndarray | None = None  # [H] 2 meter_a Vmax + R
+    out_err: np.ndarray | None = None      # [H] ||y - y_hat|| with exact keys and values (v_exact given)
 
 
 def decode_head(q: np.ndarray, k_exact: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray,
                 w: np.ndarray, sm_scale: float, s_k: np.ndarray | None = None,
-                tier_b: dict | None = None) -> DecodeResult:
+                tier_b: dict | None = None, vw: np.ndarray | None = None,
+                v_exact: np.ndarray | None = None) -> DecodeResult:
     """Decode attention of H query heads that share one kv head's cache.
 
     q [H, 128] (the query values exactly as the kernel reads them), k_exact
     [S, 128] (the binary32 post-RoPE keys), k_hat / v_hat [S, 128] (exact
     dequantized cache), w [S, 16] (witness values), s_k [S] (key scales, Tier B),
-    tier_b = dict(delta_req, n_layers, n_q_heads, n_steps) or None.
+    tier_b = dict(delta_req, n_layers, n_q_heads, n_steps) or None, vw [S, 2] (value witness
+    values: rho^v, ||v||) or None, v_exact [S, 128] (the binary32 values) or None.
     """
     q = np.asarray(q, dtype=np.float64)
     H = q.shape[0]
@@ -168,9 +186,30 @@ def decode_head(q: np.ndarray, k_exact: np.ndarray, k_hat: np.ndarray, v_hat: np
         if tier_b is not None:
             u = tier_b_radius(q[h], s_k, sm_scale, S, **tier_b)
             lb[h] = log_a_minus_1(log_pt[h], u)
-    return DecodeResult(out=out, lse=lse, tv=tv, log_am1_a=la, meter_a=meter_from_log_am1(la),
-                        raw_a=raw_log_score(la), log_am1_b=lb,
-                        cert_b=np.where(np.isnan(lb), np.nan, meter_from_log_am1(lb)), c_max=cmax)
+    res = DecodeResult(out=out, lse=lse, tv=tv, log_am1_a=la, meter_a=meter_from_log_am1(la),
+                       raw_a=raw_log_score(la), log_am1_b=lb,
+                       cert_b=np.where(np.isnan(lb), np.nan, meter_from_log_am1(lb)), c_max=cmax)
+    if vw is not None:
+        res.value_r, res.value_vmax = value_side(p_t, vw)
+        res.out_bound_a = output_error_bound(res.meter_a, res.value_r, res.value_vmax)
+    if v_exact is not None:
+        y = p @ np.asarray(v_exact, dtype=np.float64)
+        res.out_err = np.sqrt(np.sum((y - out) ** 2, axis=-1))
+    return res
+
+
+def value_side(p_t: np.ndarray, vw: np.ndarray):
+    """R = sum_t p~_t rho^v_t per head (p_t [H, S]) and Vmax = max_t ||v_t|| from value witness values
+    vw [S, 2] = (rho^v_t, ||v_t||).  Vmax is 0 for an empty sequence."""
+    vw = np.asarray(vw, dtype=np.float64)
+    r = np.asarray(p_t, dtype=np.float64) @ vw[:, 0]
+    vmax = float(np.max(vw[:, 1])) if vw.shape[0] else 0.0
+    return r, vmax
+
+
+def output_error_bound(tv_bound, r, vmax):
+    """WitCert §3: ||y - y_hat|| <= 2 TV max_t ||v_t|| + sum_t p~_t rho^v_t, with a TV bound for TV."""
+    return 2.0 * np.asarray(tv_bound, dtype=np.float64) * vmax + np.asarray(r, dtype=np.float64)
 
 
 def flawed_dispersion_bound(p_t: np.ndarray, c: np.ndarray) -> float:

@@ -22,9 +22,12 @@ Rules taken from the pages
 * WitCert §4.1, eq. (2): the witness w_{t,b} = ||r_{t,b}|| is the Euclidean
   norm of the key residual r = k_hat - k over band b, stored in fp16.  Bands are
   B = 16 contiguous groups of RoPE frequency pairs (4 pairs = 8 coordinates each).
+* WitCert §3 (the output bound ||y - y_hat|| <= 2 TV max_t ||v_t|| + sum_t p~_t rho^v_t):
+  the value side needs, per token, rho^v_t = ||v_hat_t - v_t|| and ||v_t||; stored
+  here as a value witness of two fp16 numbers per (token, kv head).
 
-Readings where the pages are silent (listed in the design doc)
--------------------------------------------------------
+Readings where the pages are silent
+-----------------------------------
 * RoPE pairs are half-split: pair j = coordinates (j, j + 64).  Band b therefore
   holds coordinates 4b..4b+3 and 64+4b..64+4b+3.
 * Every scalar step is the binary32 operation (evaluated in float64 and rounded
@@ -57,6 +60,7 @@ __all__ = [
     "quantize",
     "dequantize",
     "witness_bits",
+    "value_witness_bits",
     "band_norms",
 ]
 
@@ -142,6 +146,18 @@ def band_norms(r: np.ndarray) -> np.ndarray:
     lo = r[..., :half].reshape(r.shape[:-1] + (N_BANDS, per))
     hi = r[..., half:].reshape(r.shape[:-1] + (N_BANDS, per))
     return np.sqrt(np.sum(lo * lo, axis=-1) + np.sum(hi * hi, axis=-1))
+
+
+def value_witness_bits(v_hat: np.ndarray, v32: np.ndarray) -> np.ndarray:
+    """Value witness [..., 2] fp16 (round-up) patterns: (||v_hat - v||, ||v||) over the 128 channels.
+
+    Rounded up so that neither the value reconstruction error nor the value norm is under-stated.
+    """
+    v = np.asarray(v32, dtype=np.float32).astype(np.float64)
+    r = np.asarray(v_hat, dtype=np.float64) - v
+    rho = np.sqrt(np.sum(r * r, axis=-1))
+    vn = np.sqrt(np.sum(v * v, axis=-1))
+    return np.stack([fp16_bits(rho, "ru"), fp16_bits(vn, "ru")], axis=-1)
 
 
 def witness_bits(k_hat: np.ndarray, k32: np.ndarray) -> np.ndarray:
