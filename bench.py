@@ -57,6 +57,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
+    p.add_argument("--value-side", action="store_true",
+                   help="meter the value side too (value witness read, output-error bound from kvq_meter)")
     p.add_argument("--separate-append", action="store_true",
                    help="kvq_append + kvq_decode_attn per layer instead of the fused kvq_decode_attn_append")
     p.add_argument("--layers", type=int, default=0, help="override layer count (profiling only; not a bench line)")
@@ -70,15 +72,18 @@ CODE_BYTES = {"bf16": 2, "e4m3": 1, "e4m3s": 1, "int8": 1}
 HAS_SCALE = {"bf16": 0, "e4m3": 0, "e4m3s": 1, "int8": 1}
 
 
-def token_head_bytes(k_fmt, v_fmt, meter=True) -> int:
-    """Bytes one token of one kv head costs the decode: K and V codes, fp16 scales, 32-byte witness."""
-    return 128 * (CODE_BYTES[k_fmt] + CODE_BYTES[v_fmt]) + 2 * (HAS_SCALE[k_fmt] + HAS_SCALE[v_fmt]) + 32 * meter
+def token_head_bytes(k_fmt, v_fmt, meter=True, value_side=False) -> int:
+    """Bytes one token of one kv head costs the decode: K and V codes, fp16 scales, 32-byte witness
+    (+ the 4-byte value witness with the value side of the output bound)."""
+    return (128 * (CODE_BYTES[k_fmt] + CODE_BYTES[v_fmt]) + 2 * (HAS_SCALE[k_fmt] + HAS_SCALE[v_fmt]) + 32 * meter
+            + 4 * value_side)
 
 
-def step_bytes(w, lens) -> int:
+def step_bytes(w, lens, value_side=False) -> int:
     """Algorithmic bytes of one decode step: live tokens once per (layer, kv head), the prefix once per layer."""
-    live = int(np.sum(lens)) * token_head_bytes(w.k_fmt, w.v_fmt)
-    pre = w.prefix_len * token_head_bytes(w.prefix_k_fmt, w.prefix_v_fmt) if w.prefix_len else 0
+    live = int(np.sum(lens)) * token_head_bytes(w.k_fmt, w.v_fmt, value_side=value_side)
+    pre = (w.prefix_len * token_head_bytes(w.prefix_k_fmt, w.prefix_v_fmt, value_side=value_side)
+           if w.prefix_len else 0)
     return w.n_layers * w.n_kv_heads * (live + pre)
 
 
@@ -183,8 +188,9 @@ class ClockSampler:
 class Model:
     """All layers' caches of one workload, filled through kvq_append, plus the step's buffers."""
 
-    def __init__(self, w, device, seed_base=0, n_layers=None, resident=0):
+    def __init__(self, w, device, seed_base=0, n_layers=None, resident=0, value_side=False):
         self.separate_append = False
+        self.value_side = value_side
         import torch
 
         import quantized_kv_cache_kvq_gb300 as kvq
@@ -213,7 +219,7 @@ class Model:
         for l in range(self.R):
             g.manual_seed(W.unit_seed(w, 100_000 + 1000 * seed_base + l))
             c = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, self.num_pages, layer=l,
-                               seed=(0x5EED << 20) + 97 * l + seed_base)
+                               seed=(0x5EED << 20) + 97 * l + seed_base, value_witness=value_side)
             chunk = 1 << 18
             for a in range(0, total, chunk):
                 b = min(total, a + chunk)
@@ -222,7 +228,7 @@ class Model:
             self.caches.append(c)
             if w.prefix_len:
                 p = kvq.PagedCache(w.prefix_k_fmt, w.prefix_v_fmt, Hkv, (w.prefix_len + 15) // 16, layer=l,
-                                   seed=(0xCA47 << 20) + l)
+                                   seed=(0xCA47 << 20) + l, value_witness=value_side)
                 k, v = W.gen_tokens_gpu(w, l, torch.arange(w.prefix_len, device=device), g, device, sink=True)
                 kvq.append(p, k, v, torch.arange(w.prefix_len, dtype=torch.int32, device=device), self.err)
                 self.prefixes.append(p)
@@ -235,7 +241,7 @@ class Model:
         self.k_new = torch.randn((self.L, B, Hkv, 128), generator=g, device=device)
         self.v_new = torch.randn((self.L, B, Hkv, 128), generator=g, device=device)
         self.out = torch.empty((self.L, B, Hq, 128), device=device)
-        self.state = torch.empty((self.L, B, Hq, 4), device=device)
+        self.state = torch.empty((self.L, B, Hq, 8), device=device)
         self.meter_a = torch.empty((self.L, B, Hq), device=device)
         self.raw_a = torch.empty((self.L, B, Hq), device=device)
         self.cert_b = torch.empty((self.L, B, Hq), device=device) if w.tier_b else None
@@ -243,7 +249,8 @@ class Model:
         self.ranking = (torch.empty((B, self.L * Hq), dtype=torch.int32, device=device)
                         if w.n_outliers else None)
         self.ws = torch.empty(kvq.decode_workspace_size(B, Hkv, Hq), dtype=torch.uint8, device=device)
-        tiers = kvq.TIER_A | (kvq.TIER_B if w.tier_b else 0)
+        tiers = kvq.TIER_A | (kvq.TIER_B if w.tier_b else 0) | (kvq.TIER_V if value_side else 0)
+        self.out_bound = torch.empty((self.L, B, Hq), device=device) if value_side else None
         self.mp = kvq.meter_params(tiers, w.n_layers, Hq, w.n_steps, w.delta_req, w.tau)
         torch.cuda.synchronize()
         if self.err.item() != 0:
@@ -272,7 +279,7 @@ class Model:
                 events[l][1].record()
                 kvq.debug_time_decode(None, None)
         kvq.meter(self.state, self.L, w.batch, w.n_q_heads, self.mp, self.meter_a, self.raw_a, self.counts,
-                  cert_b=self.cert_b, ranking=self.ranking)
+                  cert_b=self.cert_b, ranking=self.ranking, out_bound=self.out_bound)
 
     def launches_per_step(self) -> int:
         return self.L * (3 if self.separate_append else 2) + 1 + (1 if self.ranking is not None else 0)
@@ -296,9 +303,9 @@ def run_gpu(args, w):
     resident = args.resident_layers
     if not resident and w.name == "ragged_paged":
         resident = 4  # 36 layers of this workload need ~413 GB of cache: rotate 4 resident layers
-    m = Model(w, dev, seed_base=rank, n_layers=args.layers or None, resident=resident)
+    m = Model(w, dev, seed_base=rank, n_layers=args.layers or None, resident=resident, value_side=args.value_side)
     m.separate_append = args.separate_append
-    per_step_bytes = step_bytes(w, m.lens) * m.L // w.n_layers
+    per_step_bytes = step_bytes(w, m.lens, value_side=args.value_side) * m.L // w.n_layers
 
     def barrier():
         if world > 1:
@@ -555,6 +562,8 @@ def main():
             "roofline": roofline_of(r, w, args),
             "gpu_launches": r["launches"], "clocks": r["clocks"], "meter_counts": r["counts"],
             "launch_mode": "cuda_graph" if r["graph"] else "eager"}
+    if args.value_side:
+        line["config"]["meter"] += " + value side (output-error bound)"
     if r["resident"] < (args.layers or w.n_layers):
         line["config"]["resident_layers"] = r["resident"]
     if "e2e" in r:

@@ -75,11 +75,11 @@ typedef enum kvq_dtype { KVQ_DTYPE_F32 = 0, KVQ_DTYPE_BF16 = 1 } kvq_dtype;
 /*
  * One layer's paged cache: planes of tiles, one tile per (page, kv head).
  * Tile index of (page p, kv head h) is p * num_kv_heads + h in the K, V and
- * witness planes and h * num_pages + p in the two scale planes (head-major, so
- * that the 32-byte scale tiles of consecutive pages of one head share a
- * 128-byte memory line); a tile holds the 16 tokens (slots p*16 .. p*16+15)
- * of that page.  All planes are device memory, 16-byte aligned, owned by the
- * caller.
+ * witness planes and h * num_pages + p in the two scale planes and the value
+ * witness plane (head-major, so that the small tiles of consecutive pages of
+ * one head share a 128-byte memory line); a tile holds the 16 tokens (slots
+ * p*16 .. p*16+15) of that page.  All planes are device memory, 16-byte
+ * aligned, owned by the caller.
  *
  * Tile layouts (byte offset of token t in 0..15, channel c in 0..127, band b
  * in 0..15; they place each lane's tensor-core fragment in contiguous 16-byte
@@ -92,6 +92,9 @@ typedef enum kvq_dtype { KVQ_DTYPE_F32 = 0, KVQ_DTYPE_BF16 = 1 } kvq_dtype;
  *                        + 2*(2*(t>>3) + ((c>>3)&1)) + (t&1)
  *   witness (512 B, fp16 bits):  16*(4*(t&7) + (b>>2)) + 8*(t>>3) + 2*(b&3)
  *   scale   (32 B,  fp16 bits):  2*(2*(t&7) + (t>>3))
+ *   value witness (64 B, fp16 bits):  8*(t&7) + 4*k + 2*(t>>3), k = 0: rho^v_t =
+ *                        ||v_hat_t - v_t||, k = 1: ||v_t|| (both rounded up; [W] Sec. 3,
+ *                        the output bound ||y - y_hat|| <= 2 TV max_t ||v_t|| + sum_t p~_t rho^v_t)
  * Band b holds the RoPE frequency pairs 4b..4b+3 of the half-split pairing
  * (pair j = channels j and j+64), i.e. channels 4b..4b+3 and 64+4b..64+4b+3
  * ([W] Sec. 4.1, eq. (2)).
@@ -110,11 +113,14 @@ typedef struct kvq_cache {
   uint16_t* v_scale;      /* V scale tiles (fp16 bits); non-NULL iff the V format has a scale */
   uint16_t* witness;      /* witness tiles (fp16 bits); required by kvq_append, and by
                              kvq_decode_attn when the meter is on                      */
+  uint16_t* v_witness;    /* value witness tiles (fp16 bits) or NULL; written by kvq_append
+                             when non-NULL, required by kvq_decode_attn with KVQ_TIER_V */
 } kvq_cache;
 
 /* Meter configuration ([W] Sec. 4.2 request-level budget, Sec. 4.3 saturation). */
 typedef struct kvq_meter_params {
-  uint32_t tiers;     /* bit 0: Tier A witness bound; bit 1: Tier B dither certificate (INT8 keys only) */
+  uint32_t tiers;     /* bit 0: Tier A witness bound; bit 1: Tier B dither certificate (INT8 keys only);
+                         bit 2: value side of the output-error bound (requires Tier A)               */
   int32_t n_layers;   /* L in delta_loc = delta_req / (L * H * T)                                      */
   int32_t n_q_heads;  /* H (query heads)                                                               */
   int32_t n_steps;    /* T (decode steps the request budget covers; 256 in [W])                         */
@@ -125,10 +131,18 @@ typedef struct kvq_meter_params {
 
 #define KVQ_TIER_A 1u
 #define KVQ_TIER_B 2u
+#define KVQ_TIER_V 4u
 
-/* Bytes of one tile of a plane: plane 0 = K, 1 = V, 2 = K scale, 3 = V scale, 4 = witness.
-   Returns 0 for a plane the format does not store. */
+/* Floats per (sequence, query head) cell of meter_state. */
+#define KVQ_METER_STATE_FLOATS 8
+
+/* Bytes of one tile of a plane: plane 0 = K, 1 = V, 2 = K scale, 3 = V scale, 4 = witness,
+   5 = value witness.  Returns 0 for a plane the format does not store. */
 size_t kvq_tile_bytes(int32_t fmt, int32_t plane);
+
+/* sizeof of the ABI structs as this library was compiled: which 0 = kvq_cache,
+   1 = kvq_meter_params (0 for other values); lets bindings check their layouts. */
+size_t kvq_sizeof(int32_t which);
 
 /*
  * kvq_append -- quantize-on-append ([W] Sec. 4.2 "Subtractive dither",
@@ -179,12 +193,16 @@ size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t nu
  * meter (nullable => meter off): tiers to accumulate.  With the meter off the
  *   witness is not read and `out` is bit-identical to the meter-on output.
  * out_dev: [batch][num_q_heads][128] fp32 attention output sum_t p~_t v_hat_t.
- * meter_state_dev (nullable iff meter off): [batch][num_q_heads][4] fp32:
+ * meter_state_dev (nullable iff meter off): [batch][num_q_heads][8] fp32
+ *   (KVQ_METER_STATE_FLOATS):
  *   [0] ln(A - 1) of Tier A, A = sum_t p~_t e^{c_t}, c_t = sm_scale *
  *       sum_b ||q_b|| w_{t,b} ([W] Thm. 1, Thm. 2); -inf when A = 1;
  *   [1] ln(A_B - 1) of Tier B, u_t = sm_scale ||q|| s_t sqrt(2 ln(2S/delta_loc)/12)
  *       ([W] Sec. 4.2), NaN when Tier B is off;
- *   [2] log-sum-exp of the compressed logits (natural log); [3] tokens attended S.
+ *   [2] log-sum-exp of the compressed logits (natural log); [3] tokens attended S;
+ *   [4] R = sum_t p~_t rho^v_t and [5] Vmax = max_t ||v_t|| from the value
+ *       witness ([W] Sec. 3), NaN when KVQ_TIER_V is off (0 for an empty sequence);
+ *   [6], [7] 0.
  * workspace_dev / ws_bytes: scratch of at least kvq_decode_workspace_size().
  * An empty sequence (no prefix, seq_len 0) yields out = 0 and ln(A-1) = -inf.
  */
@@ -259,10 +277,13 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_cache* pref
  * Sec. 6.2.4 "Certificate telemetry in production": aggregate on the GPU,
  * count non-finite values separately).
  *
- * meter_state_dev: [n_layers][batch][num_q_heads][4] as written by kvq_decode_attn.
+ * meter_state_dev: [n_layers][batch][num_q_heads][8] as written by kvq_decode_attn.
  * meter_a_dev:  [n_layers][batch][num_q_heads] min(1, 1/2 (A^2 - 1)) of Tier A.
  * raw_a_dev:    same shape, the raw log score ln(1/2 (A^2 - 1)) (finite for finite inputs).
  * cert_b_dev (nullable): same shape, min(1, 1/2 (A_B^2 - 1)).
+ * out_bound_dev (nullable): same shape, the output-error bound 2 meter_a Vmax + R
+ *   of ||y - y_hat|| ([W] Sec. 3 with Tier A's meter for TV); NaN where the state
+ *   has no value side.
  * counts_dev:   int32[4]: cells with meter_a < tau, cells with cert_b < tau,
  *               non-finite cells, total cells (zeroed and filled by the call).
  * ranking_dev (nullable): [batch][n_layers * num_q_heads] int32 flat cell
@@ -271,7 +292,7 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_cache* pref
  */
 kvq_status kvq_meter(const float* meter_state_dev, int32_t n_layers, int32_t batch, int32_t num_q_heads,
                      const kvq_meter_params* meter, float* meter_a_dev, float* raw_a_dev, float* cert_b_dev,
-                     int32_t* counts_dev, int32_t* ranking_dev, kvq_stream_t stream);
+                     float* out_bound_dev, int32_t* counts_dev, int32_t* ranking_dev, kvq_stream_t stream);
 
 /* Test hook: the dither xi of (seed, layer, kv_head, slots[i], channel c) into xi_dev[i * 128 + c]. */
 kvq_status kvq_debug_dither(uint64_t seed, int32_t layer, int32_t kv_head, const int32_t* slots_dev, int32_t n,

@@ -43,7 +43,8 @@ LIB_PATH = os.environ.get("KVQ_LIB") or os.path.join(_HERE, "libkvq.so")
 
 FMT = {"bf16": 0, "e4m3": 1, "e4m3s": 2, "int8": 3}
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
-TIER_A, TIER_B = 1, 2
+TIER_A, TIER_B, TIER_V = 1, 2, 4
+METER_STATE_FLOATS = 8  # floats per (sequence, query head) cell of meter_state
 HEAD_DIM, PAGE, N_BANDS = 128, 16, 16
 
 STATUS = {
@@ -79,6 +80,7 @@ class _Cache(ctypes.Structure):
         ("k_scale", c_void_p),
         ("v_scale", c_void_p),
         ("witness", c_void_p),
+        ("v_witness", c_void_p),
     ]
 
 
@@ -129,7 +131,9 @@ def load(path: str = LIB_PATH):
     ]
     L.kvq_meter.restype = c_int32
     L.kvq_meter.argtypes = [c_void_p, c_int32, c_int32, c_int32, POINTER(MeterParams), c_void_p, c_void_p,
-                            c_void_p, c_void_p, c_void_p, c_void_p]
+                            c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    L.kvq_sizeof.restype = c_size_t
+    L.kvq_sizeof.argtypes = [c_int32]
     L.kvq_debug_dither.restype = c_int32
     L.kvq_debug_dither.argtypes = [c_uint64, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p]
     L.kvq_debug_encode.restype = c_int32
@@ -177,7 +181,7 @@ class PagedCache:
     """One layer's paged planes (device memory owned by torch tensors)."""
 
     def __init__(self, k_fmt: str, v_fmt: str, num_kv_heads: int, num_pages: int, layer: int = 0,
-                 seed: int = 0, device="cuda", witness: bool = True):
+                 seed: int = 0, device="cuda", witness: bool = True, value_witness: bool = False):
         self.k_fmt, self.v_fmt = k_fmt, v_fmt
         self.num_kv_heads, self.num_pages, self.layer, self.seed = num_kv_heads, num_pages, layer, seed
         n = num_pages * num_kv_heads
@@ -189,14 +193,16 @@ class PagedCache:
         self.k_scale = torch.zeros((n, 32), **z) if k_fmt in ("e4m3s", "int8") else None
         self.v_scale = torch.zeros((n, 32), **z) if v_fmt in ("e4m3s", "int8") else None
         self.witness = torch.zeros((n, 512), **z) if witness else None
+        self.v_witness = torch.zeros((n, 64), **z) if value_witness else None
 
     def desc(self) -> _Cache:
         return _Cache(FMT[self.k_fmt], FMT[self.v_fmt], self.num_kv_heads, self.num_pages, self.layer, 0,
                       self.seed & 0xFFFFFFFFFFFFFFFF, _ptr(self.k), _ptr(self.v), _ptr(self.k_scale),
-                      _ptr(self.v_scale), _ptr(self.witness))
+                      _ptr(self.v_scale), _ptr(self.witness), _ptr(self.v_witness))
 
     def nbytes(self) -> int:
-        return sum(t.numel() for t in (self.k, self.v, self.k_scale, self.v_scale, self.witness) if t is not None)
+        return sum(t.numel() for t in (self.k, self.v, self.k_scale, self.v_scale, self.witness, self.v_witness)
+                   if t is not None)
 
 
 def read_err(err: torch.Tensor) -> int:
@@ -226,7 +232,7 @@ def decode_attn(cache: PagedCache, q: torch.Tensor, block_table: torch.Tensor, s
                 out: torch.Tensor, workspace: torch.Tensor, *, prefix: PagedCache | None = None,
                 prefix_len: int = 0, sm_scale: float | None = None, meter: MeterParams | None = None,
                 meter_state: torch.Tensor | None = None, err: torch.Tensor | None = None, stream=None):
-    """kvq_decode_attn for one layer: q [B, Hq, 128] -> out [B, Hq, 128] (+ meter_state [B, Hq, 4])."""
+    """kvq_decode_attn for one layer: q [B, Hq, 128] -> out [B, Hq, 128] (+ meter_state [B, Hq, 8])."""
     B, Hq, D = q.shape
     assert D == HEAD_DIM and q.is_contiguous() and out.is_contiguous()
     assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
@@ -289,11 +295,11 @@ def decode_attn_noalloc(cache: PagedCache, q: torch.Tensor, block_table: torch.T
 
 def meter(meter_state: torch.Tensor, n_layers: int, batch: int, num_q_heads: int, params: MeterParams,
           meter_a: torch.Tensor, raw_a: torch.Tensor, counts: torch.Tensor, cert_b: torch.Tensor | None = None,
-          ranking: torch.Tensor | None = None, stream=None):
-    """kvq_meter over meter_state [L, B, Hq, 4]."""
+          ranking: torch.Tensor | None = None, out_bound: torch.Tensor | None = None, stream=None):
+    """kvq_meter over meter_state [L, B, Hq, 8]."""
     _check(lib().kvq_meter(meter_state.data_ptr(), n_layers, batch, num_q_heads, ctypes.byref(params),
-                           meter_a.data_ptr(), raw_a.data_ptr(), _ptr(cert_b), counts.data_ptr(), _ptr(ranking),
-                           _stream(stream)), "kvq_meter")
+                           meter_a.data_ptr(), raw_a.data_ptr(), _ptr(cert_b), _ptr(out_bound), counts.data_ptr(),
+                           _ptr(ranking), _stream(stream)), "kvq_meter")
 
 
 def debug_dither(seed: int, layer: int, kv_head: int, slots: torch.Tensor, out: torch.Tensor, stream=None):

@@ -40,7 +40,8 @@ __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __
                     static_cast<uint8_t*>(c.v_data) + tile * tile_bytes_v(VF),
                     fmt_has_scale(KF) ? reinterpret_cast<uint8_t*>(c.k_scale) + stile * kTileBytesS : nullptr,
                     fmt_has_scale(VF) ? reinterpret_cast<uint8_t*>(c.v_scale) + stile * kTileBytesS : nullptr,
-                    reinterpret_cast<uint8_t*>(c.witness) + tile * kTileBytesW);
+                    reinterpret_cast<uint8_t*>(c.witness) + tile * kTileBytesW,
+                    c.v_witness ? reinterpret_cast<uint8_t*>(c.v_witness) + stile * kTileBytesVW : nullptr);
   if (lane == 0) report_row(rc, err);
 }
 
@@ -84,7 +85,8 @@ __global__ void __launch_bounds__(256) append_newest_kernel(kvq_cache c, const v
                     static_cast<uint8_t*>(c.v_data) + tile * tile_bytes_v(VF),
                     fmt_has_scale(KF) ? reinterpret_cast<uint8_t*>(c.k_scale) + stile * kTileBytesS : nullptr,
                     fmt_has_scale(VF) ? reinterpret_cast<uint8_t*>(c.v_scale) + stile * kTileBytesS : nullptr,
-                    reinterpret_cast<uint8_t*>(c.witness) + tile * kTileBytesW);
+                    reinterpret_cast<uint8_t*>(c.witness) + tile * kTileBytesW,
+                    c.v_witness ? reinterpret_cast<uint8_t*>(c.v_witness) + stile * kTileBytesVW : nullptr);
   if (lane == 0) report_row(rc, err);
 }
 
@@ -168,6 +170,15 @@ extern "C" size_t kvq_tile_bytes(int32_t fmt, int32_t plane) {
     case 2:
     case 3: return fmt_has_scale(fmt) ? static_cast<size_t>(kTileBytesS) : 0;
     case 4: return static_cast<size_t>(kTileBytesW);
+    case 5: return static_cast<size_t>(kTileBytesVW);
+  }
+  return 0;
+}
+
+extern "C" size_t kvq_sizeof(int32_t which) {
+  switch (which) {
+    case 0: return sizeof(kvq_cache);
+    case 1: return sizeof(kvq_meter_params);
   }
   return 0;
 }
@@ -184,6 +195,7 @@ extern "C" kvq_status kvq_append(const kvq_cache* c, const void* k, const void* 
     return KVQ_ERR_INVALID_ARG;
   if (fmt_has_scale(c->k_fmt) && (!c->k_scale || !aligned16(c->k_scale))) return KVQ_ERR_INVALID_ARG;
   if (fmt_has_scale(c->v_fmt) && (!c->v_scale || !aligned16(c->v_scale))) return KVQ_ERR_INVALID_ARG;
+  if (c->v_witness && !aligned16(c->v_witness)) return KVQ_ERR_INVALID_ARG;
   const int in_bf16 = in_dtype == KVQ_DTYPE_BF16;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;

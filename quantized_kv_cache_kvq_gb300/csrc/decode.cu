@@ -5,7 +5,7 @@
 
 #include "decode_kernel.cuh"
 
-#define KVQ_X(KF, VF, PKF, PVF, NW) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, false) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, true)
+#define KVQ_X(KF, VF, PKF, PVF, NW) KVQ_DECODE_EXTERNS(KF, VF, PKF, PVF, NW)
 #include "decode_instances.inc"
 #undef KVQ_X
 
@@ -28,6 +28,16 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float 
   m = mm;
 }
 
+// (m, l, r): r is merged with the same weights as l (the value side's sum_t e^{x_t} rho^v_t)
+__device__ __forceinline__ void lse_combine2(float& m, float& l, float& r, float m2, float l2, float r2) {
+  const float mm = fmaxf(m, m2);
+  if (mm == -INFINITY) return;
+  const float a = m == -INFINITY ? 0.f : ex2(m - mm), b = m2 == -INFINITY ? 0.f : ex2(m2 - mm);
+  l = l * a + l2 * b;
+  r = r * a + r2 * b;
+  m = mm;
+}
+
 __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -45,9 +55,12 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
   const int P = c1 - c0;
   if (P == 0) {
     *reinterpret_cast<float4*>(o + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.meter_state && lane == 0)
-      *reinterpret_cast<float4*>(a.meter_state + gw * 4) =
-          make_float4(-INFINITY, a.tier_b ? -INFINITY : NAN, -INFINITY, static_cast<float>(total));
+    if (a.meter_state && lane == 0) {
+      float* ms = a.meter_state + gw * KVQ_METER_STATE_FLOATS;
+      *reinterpret_cast<float4*>(ms) = make_float4(-INFINITY, a.tier_b ? -INFINITY : NAN, -INFINITY,
+                                                   static_cast<float>(total));
+      *reinterpret_cast<float4*>(ms + 4) = make_float4(a.value_on ? 0.f : NAN, a.value_on ? 0.f : NAN, 0.f, 0.f);
+    }
     return;
   }
   const long long W = min(static_cast<long long>(a.w_max), T);
@@ -67,24 +80,27 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
 #pragma unroll
   for (int k = 0; k < kU; ++k)
     if (k < np) v[k] = *reinterpret_cast<const float4*>(accp(k));
-  float m = -INFINITY, l = 0.f, mc = -INFINITY, sc = 0.f, mu = -INFINITY, su = 0.f;
+  float m = -INFINITY, l = 0.f, mc = -INFINITY, sc = 0.f, mu = -INFINITY, su = 0.f, vr = 0.f, vmax = 0.f;
   float m_mine = -INFINITY;  // the running max of piece `lane` (pieces < 32), for the weights below
   for (int i = lane; i < np; i += 32) {
     const float4 s4 = *reinterpret_cast<const float4*>(stats(i));
-    const float2 s2 = *reinterpret_cast<const float2*>(stats(i) + 4);
+    const float4 t4 = *reinterpret_cast<const float4*>(stats(i) + 4);
     if (i < 32) m_mine = s4.x;
-    lse_combine(m, l, s4.x, s4.y);
+    lse_combine2(m, l, vr, s4.x, s4.y, t4.z);
     lse_combine(mc, sc, s4.z, s4.w);
-    lse_combine(mu, su, s2.x, s2.y);
+    lse_combine(mu, su, t4.x, t4.y);
+    vmax = fmaxf(vmax, t4.w);
   }
 #pragma unroll
   for (int off = 16; off; off >>= 1) {
     const float m2 = __shfl_xor_sync(kFull, m, off), l2 = __shfl_xor_sync(kFull, l, off);
+    const float r2 = __shfl_xor_sync(kFull, vr, off), x2 = __shfl_xor_sync(kFull, vmax, off);
     const float c2 = __shfl_xor_sync(kFull, mc, off), s2 = __shfl_xor_sync(kFull, sc, off);
     const float u2 = __shfl_xor_sync(kFull, mu, off), v2 = __shfl_xor_sync(kFull, su, off);
-    lse_combine(m, l, m2, l2);
+    lse_combine2(m, l, vr, m2, l2, r2);
     lse_combine(mc, sc, c2, s2);
     lse_combine(mu, su, u2, v2);
+    vmax = fmaxf(vmax, x2);
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -109,7 +125,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
     const float lse2 = m + log2f(l);
     const float la = (a.meter_on && sc > 0.f) ? (mc + log2f(sc) - lse2) * kLn2 : -INFINITY;
     const float lb = a.tier_b ? ((su > 0.f) ? (mu + log2f(su) - lse2) * kLn2 : -INFINITY) : NAN;
-    *reinterpret_cast<float4*>(a.meter_state + gw * 4) = make_float4(la, lb, lse2 * kLn2, static_cast<float>(total));
+    float* ms = a.meter_state + gw * KVQ_METER_STATE_FLOATS;
+    *reinterpret_cast<float4*>(ms) = make_float4(la, lb, lse2 * kLn2, static_cast<float>(total));
+    *reinterpret_cast<float4*>(ms + 4) =
+        make_float4(a.value_on ? vr / l : NAN, a.value_on ? vmax : NAN, 0.f, 0.f);
   }
 }
 
@@ -166,9 +185,10 @@ WsLayout ws_layout(int batch, int hkv, int hq, int w_max) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int page_bytes(int kf, int vf, bool meter) {
-  return tile_bytes_k(kf) + tile_bytes_v(vf) + (meter ? kTileBytesW : 0) + (fmt_has_scale(kf) ? kTileBytesS : 0) +
-         (fmt_has_scale(vf) ? kTileBytesS : 0);
+// Stage bytes of a page: Layout<kf, vf, meter>::total with the value side on, ::unvalued without it.
+int page_bytes(int kf, int vf, bool meter, bool value) {
+  return tile_bytes_k(kf) + tile_bytes_v(vf) + (meter ? kTileBytesW : 0) + (value ? kTileBytesVW : 0) +
+         (fmt_has_scale(kf) ? kTileBytesS : 0) + (fmt_has_scale(vf) ? kTileBytesS : 0);
 }
 
 kvq_status check_cache(const kvq_cache* c, bool meter) {
@@ -190,6 +210,7 @@ Planes planes_of(const kvq_cache* c) {
   p.ks = reinterpret_cast<const uint8_t*>(c->k_scale);
   p.vs = reinterpret_cast<const uint8_t*>(c->v_scale);
   p.w = reinterpret_cast<const uint8_t*>(c->witness);
+  p.vw = reinterpret_cast<const uint8_t*>(c->v_witness);
   p.num_pages = c->num_pages;
   p.layer = static_cast<uint32_t>(c->layer);
   p.seed_lo = static_cast<uint32_t>(c->dither_seed);
@@ -208,10 +229,13 @@ struct Pick {
   int warps;
 };
 
-Pick pick(int kf, int vf, int pkf, int pvf, bool meter) {
+Pick pick(int kf, int vf, int pkf, int pvf, bool meter, bool value) {
 #define KVQ_X(KF, VF, PKF, PVF, NW)                                                                       \
   if (kf == (KF) && vf == (VF) && pkf == (PKF) && pvf == (PVF))                                           \
-    return Pick{meter ? &launch_decode<KF, VF, PKF, PVF, NW, true> : &launch_decode<KF, VF, PKF, PVF, NW, false>, NW};
+    return Pick{!meter  ? &launch_decode<KF, VF, PKF, PVF, NW, false, false>                               \
+                : value ? &launch_decode<KF, VF, PKF, PVF, NW, true, true>                                 \
+                        : &launch_decode<KF, VF, PKF, PVF, NW, true, false>,                               \
+                NW};
 #include "decode_instances.inc"
 #undef KVQ_X
   return Pick{nullptr, 0};
@@ -259,7 +283,12 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   if (q_dtype != KVQ_DTYPE_F32 && q_dtype != KVQ_DTYPE_BF16) return KVQ_ERR_INVALID_ARG;
   if (max_pages_per_seq < 0 || !std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
   if (meter) {
-    if (!(mp->tiers & KVQ_TIER_A) || (mp->tiers & ~3u) || mp->reserved != 0) return KVQ_ERR_INVALID_ARG;
+    if (!(mp->tiers & KVQ_TIER_A) || (mp->tiers & ~7u) || mp->reserved != 0) return KVQ_ERR_INVALID_ARG;
+    if (mp->tiers & KVQ_TIER_V) {
+      if (!cache->v_witness || !aligned16(cache->v_witness)) return KVQ_ERR_INVALID_ARG;
+      if (prefix && prefix_len > 0 && (!prefix->v_witness || !aligned16(prefix->v_witness)))
+        return KVQ_ERR_INVALID_ARG;
+    }
     if (mp->tiers & KVQ_TIER_B) {
       if (cache->k_fmt != KVQ_FMT_INT8_DITHER || (prefix && prefix_len > 0)) return KVQ_ERR_INVALID_ARG;
       if (!(mp->delta_req > 0.0 && mp->delta_req < 1.0) || mp->n_layers <= 0 || mp->n_q_heads <= 0 || mp->n_steps <= 0)
@@ -279,7 +308,7 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   const bool has_prefix = prefix && prefix_len > 0;
   const int pkf = has_prefix ? prefix->k_fmt : kNoPrefix;
   const int pvf = has_prefix ? prefix->v_fmt : kNoPrefix;
-  const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter);
+  const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter, meter && (mp->tiers & KVQ_TIER_V));
   if (!pk.launch) return KVQ_ERR_UNSUPPORTED_LAYOUT;
   const int nw = pk.warps;
   const int w_max = sms * nw;
@@ -310,18 +339,20 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   a.out = out;
   a.meter_state = meter_state;
   a.meter_on = meter ? 1 : 0;
+  a.value_on = meter && (mp->tiers & KVQ_TIER_V) ? 1 : 0;
   a.ws_stats = reinterpret_cast<float*>(ws + wl.stats);
   a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
   a.w_max = w_max;
   a.err = err_word;
 
   // stage size: the larger of the two segments' page footprints (16-byte multiple by construction)
-  int sb = page_bytes(cache->k_fmt, cache->v_fmt, meter);
-  if (has_prefix) sb = std::max(sb, page_bytes(prefix->k_fmt, prefix->v_fmt, meter));
+  int sb = page_bytes(cache->k_fmt, cache->v_fmt, meter, a.value_on);
+  if (has_prefix) sb = std::max(sb, page_bytes(prefix->k_fmt, prefix->v_fmt, meter, a.value_on));
   const bool xi = cache->k_fmt == KVQ_FMT_INT8_DITHER && cache->v_fmt == KVQ_FMT_INT8_DITHER;
   const int cum_bytes = ((batch + 1) * 4 + 127) & ~127;
   const int lo_bytes = q_dtype == KVQ_DTYPE_F32 ? kQloBytes : 0;
-  const int fixed = cum_bytes + nw * ((xi ? kXiScratch : 0) + lo_bytes + kMaxStages * 8);
+  const int fixed = cum_bytes + nw * ((xi ? kXiScratch : 0) + lo_bytes + (a.value_on ? kVStateBytes : 0) +
+                                       kMaxStages * 8);
   const int budget = smem_max - 1024 - fixed;
   int stages = budget / (nw * sb);
   if (stages > kMaxStages) stages = kMaxStages;

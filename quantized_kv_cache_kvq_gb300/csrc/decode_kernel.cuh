@@ -36,6 +36,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr int kNoPrefix = -1;
 constexpr int kXiScratch = 16 * 128 * 2;  // per-warp fp16 dither tile (INT8 values)
+// Value side of the output bound: per lane (sum_t e^{x_t - m} rho^v_t for heads 2c and 2c + 1, rescaled
+// with l; max_t ||v_t||; unused) in shared memory, so it costs no registers in the page loop.
+constexpr int kVStateBytes = 32 * 16;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // a copy not landed after 2 s is reported as a timeout
 
@@ -45,6 +48,7 @@ struct Planes {
   const uint8_t* ks;
   const uint8_t* vs;
   const uint8_t* w;
+  const uint8_t* vw;  // value witness plane (head-major) or nullptr
   int num_pages;
   uint32_t layer;
   uint32_t seed_lo, seed_hi;
@@ -68,6 +72,7 @@ struct Args {
   float* out;        // [B][Hq][128]
   float* meter_state;  // [B][Hq][4] or nullptr
   int meter_on;
+  int value_on;      // value side of the output bound (value witness read, R and Vmax accumulated)
   float* ws_stats;   // [slots][G][8]
   float* ws_acc;     // [slots][G][128]
   int w_max;
@@ -85,7 +90,11 @@ struct Layout {
   static constexpr int wOff = kBytes + vBytes;
   static constexpr int ksOff = wOff + (METER ? kTileBytesW : 0);
   static constexpr int vsOff = ksOff + (fmt_has_scale(KF) ? kTileBytesS : 0);
-  static constexpr int total = vsOff + (fmt_has_scale(VF) ? kTileBytesS : 0);
+  // the value witness tile follows; it is copied (and the stage sized for it) only with the value
+  // side on, so stages without it keep their size
+  static constexpr int vwOff = vsOff + (fmt_has_scale(VF) ? kTileBytesS : 0);
+  static constexpr int total = vwOff + (METER ? kTileBytesVW : 0);
+  static constexpr int unvalued = vwOff;  // bytes copied when the value side is off
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -487,7 +496,7 @@ __device__ __forceinline__ void accumulate_meter(const float (&r)[4], const floa
 template <int KF, int VF, bool METER>
 __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile, float xb0, float xb1, uint32_t phys,
                                              const Planes& pl, int kvh, const QFrag& f, SoftState& s,
-                                             float qk_scale, bool tier_b) {
+                                             float qk_scale, bool tier_b, float* vstate) {
   using L = Layout<KF, VF, METER>;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   constexpr bool K16 = fmt_is_16bit(KF);
@@ -588,6 +597,16 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   for (int v = 0; v < 4; ++v) p[v] = ex2(x[v] - mnew[v & 1]);  // 0 for -inf logits
 #pragma unroll
   for (int h = 0; h < 2; ++h) s.l[h] = s.l[h] * alpha[h] + (p[h] + p[2 + h]);
+  if (METER && vstate) {
+    // value side: rho^v and ||v|| of tokens g and g + 8 (WitCert Sec. 3 output bound)
+    const uint2 vw = lds64(st + L::vwOff + 8 * g);
+    const float2 rho = unpack_f16(vw.x), vn = unpack_f16(vw.y);
+    float4 v4 = *reinterpret_cast<const float4*>(vstate + 4 * lane);
+    v4.x = __fmaf_rn(p[2], rho.y, __fmaf_rn(p[0], rho.x, v4.x * alpha[0]));
+    v4.y = __fmaf_rn(p[3], rho.y, __fmaf_rn(p[1], rho.x, v4.y * alpha[1]));
+    v4.z = fmaxf(v4.z, fmaxf(vn.x, vn.y));
+    *reinterpret_cast<float4*>(vstate + 4 * lane) = v4;
+  }
   if (__any_sync(kFull, (alpha[0] != 1.f) | (alpha[1] != 1.f))) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -720,7 +739,7 @@ __device__ __forceinline__ Desc make_desc(const Args& a, const int32_t* cum, lon
   return d;
 }
 
-template <int KF, int VF, int PKF, int PVF, bool METER>
+template <int KF, int VF, int PKF, int PVF, bool METER, bool VALUE>
 __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64_t* bar, Desc d) {
   // lane 0 only
   if (d.phys < 0) {
@@ -733,13 +752,14 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     using L = Layout<(PKF < 0 ? 0 : PKF), (PVF < 0 ? 0 : PVF), METER>;
     constexpr int pk = (PKF < 0 ? 0 : PKF), pv = (PVF < 0 ? 0 : PVF);
     const size_t tile = static_cast<size_t>(d.phys) * a.Hkv + kvh;
-    mbar_arrive_expect_tx(bar, L::total);
+    mbar_arrive_expect_tx(bar, VALUE ? L::total : L::unvalued);
     bulk_g2s(stage + L::kOff, a.pre.k + tile * L::kBytes, L::kBytes, bar);
     bulk_g2s(stage + L::vOff, a.pre.v + tile * L::vBytes, L::vBytes, bar);
     if (METER) bulk_g2s(stage + L::wOff, a.pre.w + tile * kTileBytesW, kTileBytesW, bar);
     const size_t stile = static_cast<size_t>(kvh) * a.pre.num_pages + d.phys;
     if (fmt_has_scale(pk)) bulk_g2s(stage + L::ksOff, a.pre.ks + stile * kTileBytesS, kTileBytesS, bar);
     if (fmt_has_scale(pv)) bulk_g2s(stage + L::vsOff, a.pre.vs + stile * kTileBytesS, kTileBytesS, bar);
+    if (METER && VALUE) bulk_g2s(stage + L::vwOff, a.pre.vw + stile * kTileBytesVW, kTileBytesVW, bar);
   } else {
     using L = Layout<KF, VF, METER>;
     const size_t tile = static_cast<size_t>(d.phys) * a.Hkv + kvh;
@@ -748,7 +768,7 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
       asm volatile("griddepcontrol.wait;" ::: "memory");
       asm volatile("fence.proxy.async.global;" ::: "memory");
     }
-    mbar_arrive_expect_tx(bar, L::total);
+    mbar_arrive_expect_tx(bar, VALUE ? L::total : L::unvalued);
     bulk_g2s(stage + L::kOff, a.live.k + tile * L::kBytes, L::kBytes, bar);
     bulk_g2s(stage + L::vOff, a.live.v + tile * L::vBytes, L::vBytes, bar);
     if (METER) bulk_g2s(stage + L::wOff, a.live.w + tile * kTileBytesW, kTileBytesW, bar);
@@ -756,18 +776,29 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     const size_t stile = static_cast<size_t>(kvh) * a.live.num_pages + d.phys;
     if (fmt_has_scale(KF)) bulk_g2s(stage + L::ksOff, a.live.ks + stile * kTileBytesS, kTileBytesS, bar);
     if (fmt_has_scale(VF)) bulk_g2s(stage + L::vsOff, a.live.vs + stile * kTileBytesS, kTileBytesS, bar);
+    if (METER && VALUE) bulk_g2s(stage + L::vwOff, a.live.vw + stile * kTileBytesVW, kTileBytesVW, bar);
   }
 }
 
 // Partial of one (warp, unit) piece: per real head, (m, l, mc, sc, mu, su) and the 128 O^T values.
-__device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftState& s) {
+__device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftState& s, float* vstate) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  float l[2], sc[2], su[2];
+  float l[2], sc[2], su[2], vr[2] = {0.f, 0.f};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     l[h] = col_sum8(s.l[h]);
     sc[h] = col_sum8(s.sc[h]);
     su[h] = col_sum8(s.su[h]);
+  }
+  float vmax = 0.f;
+  if (vstate) {
+    const float4 v4 = *reinterpret_cast<const float4*>(vstate + 4 * lane);
+    vr[0] = col_sum8(v4.x);
+    vr[1] = col_sum8(v4.y);
+    vmax = v4.z;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, o));
+    *reinterpret_cast<float4*>(vstate + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);  // next unit starts empty
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -782,7 +813,7 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
       if (g == 0) {
         float* st = a.ws_stats + (slot * a.G + head) * 8;
         *reinterpret_cast<float4*>(st) = make_float4(s.m[h], l[h], s.mc[h], sc[h]);
-        *reinterpret_cast<float4*>(st + 4) = make_float4(s.mu[h], su[h], 0.f, 0.f);
+        *reinterpret_cast<float4*>(st + 4) = make_float4(s.mu[h], su[h], vr[h], vmax);
       }
     }
   }
@@ -791,7 +822,8 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
 // Zero the bytes of tokens nvalid..15 in a stage (a partial last page): the slots past the end of a
 // sequence may hold anything, and zeros make their logit exactly the -inf bias, their value and
 // radius exactly 0.  Runs once per unit at most; all lanes take part.
-template <int KF, int VF, bool METER>
+// VALUE: the stage holds a value witness tile (only then does the stage have room for it).
+template <int KF, int VF, bool METER, bool VALUE>
 __device__ void zero_tail(uint8_t* st, int nvalid) {
   using L = Layout<KF, VF, METER>;
   const int lane = threadIdx.x & 31;
@@ -810,11 +842,17 @@ __device__ void zero_tail(uint8_t* st, int nvalid) {
   for (int t = nvalid + lane; t < kPage; t += 32) {
     if (fmt_has_scale(KF)) *reinterpret_cast<uint16_t*>(st + L::ksOff + s_offset(t)) = 0;
     if (fmt_has_scale(VF)) *reinterpret_cast<uint16_t*>(st + L::vsOff + s_offset(t)) = 0;
+    if (METER && VALUE) {
+      *reinterpret_cast<uint16_t*>(st + L::vwOff + vw_offset(t, 0)) = 0;
+      *reinterpret_cast<uint16_t*>(st + L::vwOff + vw_offset(t, 1)) = 0;
+    }
   }
   __syncwarp();
 }
 
-template <int KF, int VF, int PKF, int PVF, int NW, bool METER>
+// VALUE: the value side of the output bound is compiled in (value witness staged and accumulated);
+// without it no trace of the value side is left in the kernel.
+template <int KF, int VF, int PKF, int PVF, int NW, bool METER, bool VALUE>
 __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   // let the merge grid (programmatic dependent launch) be scheduled as soon as SMs free up
@@ -876,10 +914,15 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
 
   // ---- per-warp shared memory: stages, dither tile, query low parts, barriers
   const int lo_bytes = a.q_bf16 ? 0 : kQloBytes;
-  const int per_warp = a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes + kMaxStages * 8;
+  static_assert(METER || !VALUE, "the value side rides on the meter");
+  const int v_bytes = VALUE ? kVStateBytes : 0;
+  const int per_warp = a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes + v_bytes + kMaxStages * 8;
   uint8_t* wbase = smem + cum_bytes + warp * per_warp;
   uint8_t* xi_tile = wbase + a.stages * a.stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes);
+  float* vstate = VALUE ? reinterpret_cast<float*>(xi_tile + (XI ? kXiScratch : 0) + lo_bytes) : nullptr;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(wbase + a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes + v_bytes);
+  if (vstate) *reinterpret_cast<float4*>(vstate + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane == 0) {
     for (int i = 0; i < a.stages; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
@@ -892,7 +935,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   for (int j = 0; j < a.stages && j < n; ++j) {
     const int32_t ph = __shfl_sync(kFull, cur.phys, j);
     const uint32_t in = __shfl_sync(kFull, cur.info, j);
-    if (lane == 0) issue_page<KF, VF, PKF, PVF, METER>(a, wbase + j * a.stage_bytes, &bars[j], Desc{ph, in});
+    if (lane == 0) issue_page<KF, VF, PKF, PVF, METER, VALUE>(a, wbase + j * a.stage_bytes, &bars[j], Desc{ph, in});
   }
 
   QFrag f;
@@ -917,7 +960,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
     const uint32_t info = __shfl_sync(kFull, cur.info, j & 31);
     const int u = d_unit(info);
     if (u != unit) {
-      if (unit >= 0) { write_piece(a, static_cast<size_t>(wid) + unit, s); reset_state(s); }
+      if (unit >= 0) { write_piece(a, static_cast<size_t>(wid) + unit, s, vstate); reset_state(s); }
       unit = u;
       const int seq = u / a.Hkv, kvh = u % a.Hkv;
       const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
@@ -932,13 +975,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       const float xb0 = g8 < nvalid ? 0.f : -INFINITY, xb1 = g8 + 8 < nvalid ? 0.f : -INFINITY;
       if (PKF != kNoPrefix && d_prefix(info)) {
         constexpr int pk = (PKF < 0 ? 0 : PKF), pv = (PVF < 0 ? 0 : PVF);
-        if (nvalid < kPage) zero_tail<pk, pv, METER>(st, nvalid);
+        if (nvalid < kPage) zero_tail<pk, pv, METER, VALUE>(st, nvalid);
         process_page<pk, pv, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.pre, kvh, f, s,
-                                    qk_scale, a.tier_b != 0);
+                                    qk_scale, a.tier_b != 0, vstate);
       } else {
-        if (nvalid < kPage) zero_tail<KF, VF, METER>(st, nvalid);
+        if (nvalid < kPage) zero_tail<KF, VF, METER, VALUE>(st, nvalid);
         process_page<KF, VF, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f, s,
-                                    qk_scale, a.tier_b != 0);
+                                    qk_scale, a.tier_b != 0, vstate);
       }
     }
     __syncwarp();
@@ -949,7 +992,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       const uint32_t ic = __shfl_sync(kFull, cur.info, jn & 31), inx = __shfl_sync(kFull, nxt.info, jn & 31);
       if (lane == 0) {
         fence_proxy_async();
-        issue_page<KF, VF, PKF, PVF, METER>(a, st, &bars[stage], in_cur ? Desc{pc, ic} : Desc{pn, inx});
+        issue_page<KF, VF, PKF, PVF, METER, VALUE>(a, st, &bars[stage], in_cur ? Desc{pc, ic} : Desc{pn, inx});
       }
     }
     if (++stage == a.stages) { stage = 0; parity ^= 1u; }
@@ -962,7 +1005,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       (void)mbar_wait(&bars[k % a.stages], static_cast<uint32_t>((k / a.stages) & 1));
     return;
   }
-  if (unit >= 0) write_piece(a, static_cast<size_t>(wid) + unit, s);
+  if (unit >= 0) write_piece(a, static_cast<size_t>(wid) + unit, s, vstate);
 }
 
 }  // namespace dec
@@ -974,9 +1017,9 @@ namespace dec {
 // Host launcher of one instantiation (the dynamic shared-memory limit is raised once per kernel).
 // `programmatic`: launch as a programmatic dependent of the preceding grid in the stream (the
 // fused append), which the kernel waits for where it reads that grid's output.
-template <int KF, int VF, int PKF, int PVF, int NW, bool METER>
+template <int KF, int VF, int PKF, int PVF, int NW, bool METER, bool VALUE>
 cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s, bool programmatic) {
-  auto kern = decode_split_kernel<KF, VF, PKF, PVF, NW, METER>;
+  auto kern = decode_split_kernel<KF, VF, PKF, PVF, NW, METER, VALUE>;
   static size_t configured = 0;  // largest dynamic smem size set so far
   if (smem > configured) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -1005,9 +1048,16 @@ cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s, 
 
 // Explicit instantiations are listed once, in decode_instances.inc, and split across translation
 // units so they compile in parallel.
-#define KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, M) \
-  template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M>(const kvq::dec::Args&, int, size_t, cudaStream_t, \
-                                                                         bool);
-#define KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, M) \
-  extern template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M>(const kvq::dec::Args&, int, size_t, \
-                                                                                cudaStream_t, bool);
+#define KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, M, V)                                                        \
+  template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M, V>(const kvq::dec::Args&, int, size_t, \
+                                                                            cudaStream_t, bool);
+#define KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, M, V)                                                        \
+  extern template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M, V>(const kvq::dec::Args&, int, \
+                                                                                   size_t, cudaStream_t, bool);
+// meter off, meter on, meter with the value side
+#define KVQ_DECODE_INSTANCES(KF, VF, PKF, PVF, NW)                                                    \
+  KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, false, false) KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, true, false) \
+  KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, true, true)
+#define KVQ_DECODE_EXTERNS(KF, VF, PKF, PVF, NW)                                                      \
+  KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, false, false) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, true, false) \
+  KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, true, true)

@@ -31,6 +31,7 @@ __host__ __device__ constexpr int tile_bytes_k(int f) { return fmt_is_16bit(f) ?
 __host__ __device__ constexpr int tile_bytes_v(int f) { return fmt_is_16bit(f) ? 4096 : 2048; }
 constexpr int kTileBytesW = 512;
 constexpr int kTileBytesS = 32;
+constexpr int kTileBytesVW = 64;  // value witness: (rho^v, ||v||) per token
 
 // ---------------------------------------------------------------------------------------------
 // Tile layouts (byte offsets inside one (page, kv head) tile; see include/kvq.h).
@@ -55,6 +56,8 @@ __host__ __device__ __forceinline__ int w_offset(int t, int b) {
   return 16 * (4 * (t & 7) + (b >> 2)) + 8 * (t >> 3) + 2 * (b & 3);
 }
 __host__ __device__ __forceinline__ int s_offset(int t) { return 2 * (2 * (t & 7) + (t >> 3)); }
+// value witness: k = 0 rho^v, k = 1 ||v||; lane g of the decode reads tokens g and g + 8 as one 8-byte word
+__host__ __device__ __forceinline__ int vw_offset(int t, int k) { return 8 * (t & 7) + 4 * k + 2 * (t >> 3); }
 
 // ---------------------------------------------------------------------------------------------
 // Device error word: the first error code wins.

@@ -4,6 +4,8 @@
 // the raw value is a risk score (certified gating at tau < 1, risk-ranked gating at tau >= 1).
 // Sec. 6.2.4 ("Certificate telemetry in production"): reduce certificates on the GPU without a host
 // synchronisation per layer, and count non-finite values separately from the finite statistics.
+// Sec. 3: the output moves by at most 2 TV max_t ||v_t|| + sum_t p~_t rho^v_t; with the meter for TV
+// that is the output-error bound 2 meter Vmax + R.
 #include "kvq_common.cuh"
 
 namespace kvq {
@@ -26,15 +28,21 @@ __device__ __forceinline__ void finalize_one(float la, float& meter, float& raw)
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ state, long long n, float tau,
                                                        float* __restrict__ meter_a, float* __restrict__ raw_a,
-                                                       float* __restrict__ cert_b, int32_t* __restrict__ counts) {
+                                                       float* __restrict__ cert_b, float* __restrict__ out_bound,
+                                                       int32_t* __restrict__ counts) {
   int cov_a = 0, cov_b = 0, nonfinite = 0, cells = 0;
+  static_assert(KVQ_METER_STATE_FLOATS == 8, "two float4 per cell");
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 s = reinterpret_cast<const float4*>(state)[i];
+    const float4 s = reinterpret_cast<const float4*>(state)[2 * i];
     float m, r;
     finalize_one(s.x, m, r);
     meter_a[i] = m;
     raw_a[i] = r;
+    if (out_bound) {
+      const float4 v = reinterpret_cast<const float4*>(state)[2 * i + 1];  // (R, Vmax, 0, 0)
+      out_bound[i] = (isnan(v.x) || isnan(m)) ? NAN : __fmaf_rn(2.f * m, v.y, v.x);
+    }
     cells += 1;
     if (isnan(s.x) || s.x == INFINITY) nonfinite += 1;
     else if (m < tau) cov_a += 1;
@@ -93,7 +101,7 @@ using namespace kvq;
 
 extern "C" kvq_status kvq_meter(const float* state, int32_t n_layers, int32_t batch, int32_t hq,
                                 const kvq_meter_params* mp, float* meter_a, float* raw_a, float* cert_b,
-                                int32_t* counts, int32_t* ranking, kvq_stream_t stream) {
+                                float* out_bound, int32_t* counts, int32_t* ranking, kvq_stream_t stream) {
   if (!mp || n_layers < 0 || batch < 0 || hq <= 0) return KVQ_ERR_INVALID_ARG;
   if (!state || !meter_a || !raw_a || !counts) return KVQ_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(state) & 15u) != 0) return KVQ_ERR_INVALID_ARG;
@@ -104,7 +112,8 @@ extern "C" kvq_status kvq_meter(const float* state, int32_t n_layers, int32_t ba
   if (n == 0) return KVQ_OK;
   long long blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(state, n, mp->tau, meter_a, raw_a, cert_b, counts);
+  finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(state, n, mp->tau, meter_a, raw_a, cert_b, out_bound,
+                                                                counts);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   if (ranking) {
     rank_kernel<<<batch, 512, 0, s>>>(raw_a, n_layers, batch, hq, ranking);

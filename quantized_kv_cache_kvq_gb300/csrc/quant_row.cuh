@@ -138,6 +138,7 @@ struct RowCodes {
   uint32_t kc[4], vc[4];  // this lane's four K and V codes
   uint16_t ks, vs;        // scale bits (formats with a scale)
   uint16_t wb;            // witness bits of band `lane` (lanes 0..15)
+  uint16_t vrho, vnorm;   // value witness bits: ||v_hat - v|| and ||v||, rounded up (warp-uniform)
   bool nonfinite;         // non-finite input or scale overflow (warp-uniform)
   bool range;             // value scale above KVQ_MAX_VALUE_SCALE (warp-uniform)
 };
@@ -165,7 +166,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
   rc.ks = 0;
   rc.vs = 0;
   quantize4<KF, true>(k, kamax, xi, rc.kc, rc.ks, qk, flags);
-  quantize4<VF, false>(v, vamax, xi, rc.vc, rc.vs, qv, flags);
+  quantize4<VF, true>(v, vamax, xi, rc.vc, rc.vs, qv, flags);
   if (fmt_has_scale(VF) && __half2float(__ushort_as_half(rc.vs)) > KVQ_MAX_VALUE_SCALE) flags |= 2;
   // Witness: upper bound of each band norm.  Lane l holds channels 4l..4l+3, all in band l % 16;
   // lanes l and l + 16 share a band (channels 4b..4b+3 and 64+4b..64+4b+3).
@@ -177,6 +178,21 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
   }
   ss = __fadd_ru(ss, __shfl_xor_sync(0xffffffffu, ss, 16));
   rc.wb = __half_as_ushort(__float2half_ru(__fsqrt_ru(ss)));
+  // Value witness: upper bounds of ||v_hat - v|| and ||v|| over all 128 channels (sums rounded up)
+  float rv = 0.0f, vv = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = fmaxf(qv.hi[i], -qv.lo[i]);
+    rv = __fmaf_ru(a, a, rv);
+    vv = __fmaf_ru(v[i], v[i], vv);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    rv = __fadd_ru(rv, __shfl_xor_sync(0xffffffffu, rv, o));
+    vv = __fadd_ru(vv, __shfl_xor_sync(0xffffffffu, vv, o));
+  }
+  rc.vrho = __half_as_ushort(__float2half_ru(__fsqrt_ru(rv)));
+  rc.vnorm = __half_as_ushort(__float2half_ru(__fsqrt_ru(vv)));
   rc.nonfinite = !finite || (flags & 1);  // flags are warp-uniform: amax and the scales are
   rc.range = (flags & 2) != 0;
   return rc;
@@ -186,7 +202,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
 // pointers may be null (plane absent).
 template <int KF, int VF>
 __device__ __forceinline__ void store_row(const RowCodes& rc, int t, uint8_t* ktile, uint8_t* vtile, uint8_t* kstile,
-                                          uint8_t* vstile, uint8_t* wtile) {
+                                          uint8_t* vstile, uint8_t* wtile, uint8_t* vwtile) {
   const int lane = threadIdx.x & 31;
   store_k4<KF>(ktile, t, lane * 4, rc.kc);
   store_v4<VF>(vtile, t, lane * 4, rc.vc);
@@ -195,6 +211,10 @@ __device__ __forceinline__ void store_row(const RowCodes& rc, int t, uint8_t* kt
     if (fmt_has_scale(VF) && vstile) *reinterpret_cast<uint16_t*>(vstile + s_offset(t)) = rc.vs;
   }
   if (wtile && lane < 16) *reinterpret_cast<uint16_t*>(wtile + w_offset(t, lane)) = rc.wb;
+  if (vwtile && lane == 0) {
+    *reinterpret_cast<uint16_t*>(vwtile + vw_offset(t, 0)) = rc.vrho;
+    *reinterpret_cast<uint16_t*>(vwtile + vw_offset(t, 1)) = rc.vnorm;
+  }
 }
 
 __device__ __forceinline__ void report_row(const RowCodes& rc, int32_t* err) {

@@ -7,7 +7,8 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["k_offsets", "v_offsets", "w_offsets", "s_offsets", "unpack_k", "unpack_v", "unpack_w", "unpack_s"]
+__all__ = ["k_offsets", "v_offsets", "w_offsets", "s_offsets", "vw_offsets", "unpack_k", "unpack_v", "unpack_w",
+           "unpack_s", "unpack_vw"]
 
 
 def k_offsets(fmt: str) -> np.ndarray:
@@ -39,6 +40,13 @@ def s_offsets() -> np.ndarray:
     return 2 * (2 * (t & 7) + (t >> 3))
 
 
+def vw_offsets() -> np.ndarray:
+    """[16 tokens, 2] byte offsets in a value-witness tile: k = 0 rho^v, k = 1 ||v||."""
+    t = np.arange(16)[:, None]
+    k = np.arange(2)[None, :]
+    return 8 * (t & 7) + 4 * k + 2 * (t >> 3)
+
+
 def _gather16(tiles: np.ndarray, offs: np.ndarray) -> np.ndarray:
     u16 = np.ascontiguousarray(tiles).view(np.uint16)
     return u16[..., offs // 2]
@@ -67,3 +75,9 @@ def unpack_s(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:
     """scale plane (head-major tiles: head * num_pages + page) -> fp16 bits [pages, heads, 16 tokens]."""
     tiles = tiles.reshape(num_kv_heads, -1, tiles.shape[-1]).transpose(1, 0, 2)
     return _gather16(tiles, s_offsets())
+
+
+def unpack_vw(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:
+    """value-witness plane (head-major tiles) -> fp16 bits [pages, heads, 16 tokens, 2]."""
+    tiles = tiles.reshape(num_kv_heads, -1, tiles.shape[-1]).transpose(1, 0, 2)
+    return _gather16(tiles, vw_offsets())

@@ -16,7 +16,7 @@ import workloads as W
 from oracle import attention as OA
 from oracle.encoders import fp16_value
 from oracle.philox import dither
-from oracle.quant import dequantize, quantize, witness_bits
+from oracle.quant import dequantize, quantize, value_witness_bits, witness_bits
 
 SM_SCALE = float(np.float32(1.0 / math.sqrt(128)))
 PREFIX_SEED_UNIT = 777_777
@@ -66,7 +66,8 @@ def oracle_cache_rows(k32, v32, slots, k_fmt, v_fmt, seed, layer, heads=None):
     kc, ksb, kh, kval = _oracle_quant_rows(k32, k_fmt, xi)
     vc, vsb, vh, vval = _oracle_quant_rows(v32, v_fmt, xi)
     w16 = witness_bits(kh, k32)
-    return dict(kc=kc, ksb=ksb, kh=kh, vc=vc, vsb=vsb, vh=vh, w16=w16, valid=kval & vval)
+    vw16 = value_witness_bits(vh, v32)
+    return dict(kc=kc, ksb=ksb, kh=kh, vc=vc, vsb=vsb, vh=vh, w16=w16, vw16=vw16, valid=kval & vval)
 
 
 def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
@@ -81,7 +82,8 @@ def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
                                      inp["prefix_seed"], layer)
     res = {k: np.zeros((B, w.n_q_heads) + sh) for k, sh in
            (("out", (128,)), ("lse", ()), ("tv", ()), ("log_am1", ()), ("meter", ()), ("raw", ()),
-            ("log_am1_b", ()), ("cert_b", ()))}
+            ("log_am1_b", ()), ("cert_b", ()), ("value_r", ()), ("value_vmax", ()), ("out_bound", ()),
+            ("out_err", ()))}
     rows_all = []
     for s in range(B):
         k32, v32, q = inp["seqs"][s]
@@ -91,13 +93,16 @@ def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
         rows_all.append((slots, rows))
         for g in range(Hkv):
             kk, kh, vh, ww = k32[:, g], rows["kh"][:, g], rows["vh"][:, g], fp16_value(rows["w16"][:, g])
+            vv, vw = v32[:, g], fp16_value(rows["vw16"][:, g])
             sk = fp16_value(rows["ksb"][:, g]) if rows["ksb"] is not None else None
             if pre_rows is not None:
-                pk, _ = inp["prefix"]
+                pk, pv = inp["prefix"]
                 kk = np.concatenate([pk[:, g], kk])
                 kh = np.concatenate([pre_rows["kh"][:, g], kh])
                 vh = np.concatenate([pre_rows["vh"][:, g], vh])
                 ww = np.concatenate([fp16_value(pre_rows["w16"][:, g]), ww])
+                vv = np.concatenate([pv[:, g], vv])
+                vw = np.concatenate([fp16_value(pre_rows["vw16"][:, g]), vw])
             qs = q[g * G:(g + 1) * G].astype(np.float64)
             S = kh.shape[0]
             if S == 0:
@@ -105,7 +110,7 @@ def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
                 continue
             tb = dict(delta_req=w.delta_req, n_layers=w.n_layers, n_q_heads=w.n_q_heads,
                       n_steps=w.n_steps) if tier_b else None
-            r = OA.decode_head(qs, kk, kh, vh, ww, SM_SCALE, s_k=sk, tier_b=tb)
+            r = OA.decode_head(qs, kk, kh, vh, ww, SM_SCALE, s_k=sk, tier_b=tb, vw=vw, v_exact=vv)
             sl = slice(g * G, (g + 1) * G)
             res["out"][s, sl] = r.out
             res["lse"][s, sl] = r.lse
@@ -115,13 +120,17 @@ def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
             res["raw"][s, sl] = r.raw_a
             res["log_am1_b"][s, sl] = r.log_am1_b
             res["cert_b"][s, sl] = r.cert_b
+            res["value_r"][s, sl] = r.value_r
+            res["value_vmax"][s, sl] = r.value_vmax
+            res["out_bound"][s, sl] = r.out_bound_a
+            res["out_err"][s, sl] = r.out_err
     res["rows"] = rows_all
     res["prefix_rows"] = pre_rows
     return res
 
 
 def run_case_gpu(w, layer: int = 0, inputs=None, meter: bool = True, tier_b: bool | None = None,
-                 q_dtype=None, device="cuda"):
+                 q_dtype=None, device="cuda", value: bool = False):
     """Append + decode (+ meter) of the case through the C ABI; returns host arrays and the caches."""
     import torch
 
@@ -132,7 +141,8 @@ def run_case_gpu(w, layer: int = 0, inputs=None, meter: bool = True, tier_b: boo
     B, Hkv, Hq = w.batch, w.n_kv_heads, w.n_q_heads
     dev = torch.device(device)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    cache = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, inp["num_pages"], layer=layer, seed=inp["seed"], device=dev)
+    cache = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, inp["num_pages"], layer=layer, seed=inp["seed"], device=dev,
+                           value_witness=value)
     for s in range(B):
         k32, v32, _ = inp["seqs"][s]
         n = k32.shape[0]
@@ -146,7 +156,7 @@ def run_case_gpu(w, layer: int = 0, inputs=None, meter: bool = True, tier_b: boo
         pk, pv = inp["prefix"]
         npp = (w.prefix_len + W.PAGE - 1) // W.PAGE
         prefix = kvq.PagedCache(w.prefix_k_fmt, w.prefix_v_fmt, Hkv, npp, layer=layer, seed=inp["prefix_seed"],
-                                device=dev)
+                                device=dev, value_witness=value)
         kvq.append(prefix, torch.from_numpy(pk).to(dev), torch.from_numpy(pv).to(dev),
                    torch.arange(w.prefix_len, dtype=torch.int32, device=dev), err)
     qd = q_dtype or (torch.bfloat16 if w.q_dtype == "bf16" else torch.float32)
@@ -154,12 +164,12 @@ def run_case_gpu(w, layer: int = 0, inputs=None, meter: bool = True, tier_b: boo
     bt = torch.from_numpy(inp["bt"]).to(dev)
     lens = torch.from_numpy(inp["lens"].astype(np.int32)).to(dev)
     out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
-    ms = torch.empty((B, Hq, 4), dtype=torch.float32, device=dev)
+    ms = torch.empty((B, Hq, 8), dtype=torch.float32, device=dev)
     ws = torch.empty(kvq.decode_workspace_size(B, Hkv, Hq), dtype=torch.uint8, device=dev)
     mp = None
     if meter:
-        mp = kvq.meter_params(kvq.TIER_A | (kvq.TIER_B if tier_b else 0), w.n_layers, w.n_q_heads, w.n_steps,
-                              w.delta_req, w.tau)
+        mp = kvq.meter_params(kvq.TIER_A | (kvq.TIER_B if tier_b else 0) | (kvq.TIER_V if value else 0), w.n_layers,
+                              w.n_q_heads, w.n_steps, w.delta_req, w.tau)
     kvq.decode_attn(cache, q, bt, lens, out, ws, prefix=prefix, prefix_len=w.prefix_len, sm_scale=SM_SCALE,
                     meter=mp, meter_state=ms if meter else None, err=err)
     res = dict(out=out.cpu().numpy().astype(np.float64), err=int(err.item()), cache=cache, prefix=prefix,
@@ -171,4 +181,8 @@ def run_case_gpu(w, layer: int = 0, inputs=None, meter: bool = True, tier_b: boo
         res["log_am1_b"] = msn[..., 1]
         res["lse"] = msn[..., 2]
         res["meter"] = OA.meter_from_log_am1(msn[..., 0])
+        res["value_r"] = msn[..., 4]
+        res["value_vmax"] = msn[..., 5]
+        res["mp"] = mp
+        res["ms_dev"] = ms
     return res

@@ -56,8 +56,11 @@ def test_host_entry_points(lib):
 def test_struct_sizes_match_c():
     import quantized_kv_cache_kvq_gb300 as kvq
 
-    assert ctypes.sizeof(kvq._Cache) == 6 * 4 + 8 + 5 * 8
+    assert ctypes.sizeof(kvq._Cache) == 6 * 4 + 8 + 6 * 8
     assert ctypes.sizeof(kvq.MeterParams) == 32
+    lib = kvq.load()
+    assert lib.kvq_sizeof(0) == ctypes.sizeof(kvq._Cache)  # as the C compiler laid them out
+    assert lib.kvq_sizeof(1) == ctypes.sizeof(kvq.MeterParams)
     assert kvq.MeterParams.delta_req.offset == 16
 
 

@@ -70,7 +70,7 @@ def test_fullsize_sampled_parity(name):
     qd = torch.bfloat16 if w.q_dtype == "bf16" else torch.float32
     q = torch.randn((B, Hq, 128), generator=g, device=dev).to(qd).contiguous()
     out = torch.empty((B, Hq, 128), device=dev)
-    ms = torch.empty((B, Hq, 4), device=dev)
+    ms = torch.empty((B, Hq, 8), device=dev)
     ws = torch.empty(kvq.decode_workspace_size(B, Hkv, Hq), dtype=torch.uint8, device=dev)
     tiers = kvq.TIER_A | (kvq.TIER_B if w.tier_b else 0)
     mp = kvq.meter_params(tiers, w.n_layers, Hq, w.n_steps, w.delta_req, w.tau)

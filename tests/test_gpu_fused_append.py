@@ -1,10 +1,11 @@
-"""kvq_decode_attn_append: the decode step's append done inside the decode kernel (GPU).
+"""kvq_decode_attn_append: the decode step's append and attention in one call (GPU).
 
-The fused call must leave the cache byte-identical to kvq_append of the same tokens (WitCert
-Sec. 6.2.1: the write side and the read side share one dither stream and one stored form), and its
-outputs and meter state must equal those of kvq_append followed by kvq_decode_attn bit for bit:
-the decode attends the staged page with the new token written into it, the same bytes it would
-have loaded.
+The append of each sequence's newest token runs as its own grid, which the decode overlaps and waits
+for only before loading the pages that hold those tokens.  The fused call must leave the cache
+byte-identical to kvq_append of the same tokens (WitCert Sec. 6.2.1: the write side and the read
+side share one dither stream and one stored form) in every plane, the value witness included, and
+its outputs and meter state (value side on) must equal those of kvq_append followed by
+kvq_decode_attn bit for bit.
 """
 import numpy as np
 import pytest
@@ -50,7 +51,7 @@ def _run(kvq, w, inp, fused):
     dev = torch.device("cuda")
     B, Hkv, Hq = w.batch, w.n_kv_heads, w.n_q_heads
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    cache = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, inp["num_pages"], seed=inp["seed"], device=dev)
+    cache = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, inp["num_pages"], seed=inp["seed"], device=dev, value_witness=True)
     k_new = torch.zeros((B, Hkv, 128), device=dev)
     v_new = torch.zeros((B, Hkv, 128), device=dev)
     for s in range(B):
@@ -69,23 +70,25 @@ def _run(kvq, w, inp, fused):
     if w.prefix_len:
         pk, pv = inp["prefix"]
         prefix = kvq.PagedCache(w.prefix_k_fmt, w.prefix_v_fmt, Hkv, (w.prefix_len + 15) // 16,
-                                seed=inp["prefix_seed"], device=dev)
+                                seed=inp["prefix_seed"], device=dev, value_witness=True)
         kvq.append(prefix, torch.from_numpy(pk).to(dev), torch.from_numpy(pv).to(dev),
                    torch.arange(w.prefix_len, dtype=torch.int32, device=dev), err)
     q = torch.from_numpy(inp["q"]).to(dev).to(torch.bfloat16 if w.q_dtype == "bf16" else torch.float32).contiguous()
     bt = torch.from_numpy(inp["bt"]).to(dev)
     lens = torch.from_numpy(inp["lens"].astype(np.int32)).to(dev)
     out = torch.full((B, Hq, 128), float("nan"), device=dev)
-    ms = torch.full((B, Hq, 4), float("nan"), device=dev)
+    ms = torch.full((B, Hq, 8), float("nan"), device=dev)
     ws = torch.empty(kvq.decode_workspace_size(B, Hkv, Hq), dtype=torch.uint8, device=dev)
-    mp = kvq.meter_params(kvq.TIER_A | (kvq.TIER_B if w.tier_b else 0), w.n_layers, Hq, w.n_steps, w.delta_req, w.tau)
+    mp = kvq.meter_params(kvq.TIER_A | kvq.TIER_V | (kvq.TIER_B if w.tier_b else 0), w.n_layers, Hq, w.n_steps,
+                          w.delta_req, w.tau)
     kw = dict(prefix=prefix, prefix_len=w.prefix_len, sm_scale=SM_SCALE, meter=mp, meter_state=ms, err=err)
     if fused:
         kvq.decode_attn_append(cache, k_new, v_new, q, bt, lens, out, ws, **kw)
     else:
         kvq.decode_attn(cache, q, bt, lens, out, ws, **kw)
     torch.cuda.synchronize()
-    planes = [t.cpu().numpy() for t in (cache.k, cache.v, cache.k_scale, cache.v_scale, cache.witness) if t is not None]
+    planes = [t.cpu().numpy() for t in (cache.k, cache.v, cache.k_scale, cache.v_scale, cache.witness, cache.v_witness)
+              if t is not None]
     return dict(err=int(err.item()), planes=planes, out=out.cpu().numpy(), ms=ms.cpu().numpy())
 
 

@@ -36,7 +36,7 @@ def test_meter_finalize_counts_and_ranking(kvq):
     lb = rng.uniform(-15, 2, (L, B, H))
     la = la.astype(np.float32).astype(np.float64)
     lb = lb.astype(np.float32).astype(np.float64)
-    state = np.zeros((L, B, H, 4), dtype=np.float32)
+    state = np.zeros((L, B, H, 8), dtype=np.float32)
     state[..., 0] = la
     state[..., 1] = lb
     tau = 0.2

@@ -61,7 +61,7 @@ def test_graph_replay_bit_identical_to_eager(kvq, name):
     tiers = kvq.TIER_A | (kvq.TIER_B if w.tier_b else 0)
     mp = kvq.meter_params(tiers, w.n_layers, Hq, w.n_steps, w.delta_req, w.tau)
     out = torch.empty((B, Hq, 128), device=dev)
-    ms = torch.empty((B, Hq, 4), device=dev)
+    ms = torch.empty((B, Hq, 8), device=dev)
     meter_a = torch.empty((1, B, Hq), device=dev)
     raw_a = torch.empty((1, B, Hq), device=dev)
     counts = torch.zeros(4, dtype=torch.int32, device=dev)
@@ -75,7 +75,7 @@ def test_graph_replay_bit_identical_to_eager(kvq, name):
         kvq.append(cache, k_new, v_new, slots, err)
         kvq.decode_attn(cache, q, bt, lens, out, ws, prefix=prefix, prefix_len=w.prefix_len, sm_scale=SM_SCALE,
                         meter=mp, meter_state=ms, err=err)
-        kvq.meter(ms.view(1, B, Hq, 4), 1, B, Hq, mp, meter_a, raw_a, counts)
+        kvq.meter(ms.view(1, B, Hq, 8), 1, B, Hq, mp, meter_a, raw_a, counts)
 
     step()
     torch.cuda.synchronize()
@@ -111,7 +111,7 @@ def test_split_count_invariance(kvq):
         bt = torch.from_numpy(inp["bt"][idx]).to(dev)
         lens = torch.from_numpy(inp["lens"][idx].astype(np.int32)).to(dev)
         out = torch.empty((B, Hq, 128), device=dev)
-        ms = torch.empty((B, Hq, 4), device=dev)
+        ms = torch.empty((B, Hq, 8), device=dev)
         ws = torch.empty(kvq.decode_workspace_size(B, Hkv, Hq), dtype=torch.uint8, device=dev)
         kvq.decode_attn(cache, q_all[idx].contiguous(), bt, lens, out, ws, sm_scale=SM_SCALE, meter=mp,
                         meter_state=ms, err=err)

@@ -53,13 +53,13 @@ def test_noalloc_matches_workspace_entry_point_twice():
     B, Hq = w.batch, w.n_q_heads
     mp = kvq.meter_params(kvq.TIER_A, w.n_layers, Hq, w.n_steps, w.delta_req, w.tau)
     out_ref = torch.empty((B, Hq, 128), device="cuda")
-    ms_ref = torch.empty((B, Hq, 4), device="cuda")
+    ms_ref = torch.empty((B, Hq, 8), device="cuda")
     ws = torch.empty(kvq.decode_workspace_size(B, w.n_kv_heads, Hq), dtype=torch.uint8, device="cuda")
     kvq.decode_attn(c["cache"], c["q"], c["bt"], c["lens"], out_ref, ws, prefix=c["prefix"], prefix_len=w.prefix_len,
                     sm_scale=SM_SCALE, meter=mp, meter_state=ms_ref, err=c["err"])
     for _ in range(2):
         out = torch.full((B, Hq, 128), float("nan"), device="cuda")
-        ms = torch.full((B, Hq, 4), float("nan"), device="cuda")
+        ms = torch.full((B, Hq, 8), float("nan"), device="cuda")
         kvq.decode_attn_noalloc(c["cache"], c["q"], c["bt"], c["lens"], out, prefix=c["prefix"],
                                 prefix_len=w.prefix_len, sm_scale=SM_SCALE, meter=mp, meter_state=ms, err=c["err"])
         torch.cuda.synchronize()
