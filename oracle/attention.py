@@ -32,6 +32,11 @@ with y = sum_t p_t v_t the exact output and y_hat = sum_t p~_t v_hat_t,
 the triangle inequality).  With the meter in place of TV and the stored fp16 round-up
 value witness (rho^v_t, ||v_t||), the output-error bound is
 2 min(1, 1/2 (A^2 - 1)) Vmax + R with R = sum_t p~_t rho^v_t and Vmax = max_t ||v_t||.
+
+Alternative bound shapes (WitCert §4.3 Proposition 1 and the det-tanh shape of its comparison):
+* two-sided: with A^- = E_p~[e^{-c}], TV <= 1/2 (A/A^- - A^-/A); neither this nor 1/2 (A^2 - 1) dominates,
+  so the bound is the minimum of the two (and of 1);
+* det-tanh: with every |eps_t| <= c_t, TV <= tanh(max_t c_t), a data-independent worst case merged by max.
 """
 from __future__ import annotations
 
@@ -59,6 +64,9 @@ __all__ = [
     "two_sided_bound",
     "value_side",
     "output_error_bound",
+    "one_minus_a_minus",
+    "two_sided_meter",
+    "det_tanh_bound",
 ]
 
 
@@ -151,6 +159,9 @@ class DecodeResult:
     value_vmax: float | None = None        # max_t ||v_t|| (value witness given)
     out_bound_a: np.ndarray | None = None  # [H] 2 meter_a Vmax + R
     out_err: np.ndarray | None = None      # [H] ||y - y_hat|| with exact keys and values (v_exact given)
+    one_minus_a_minus: np.ndarray | None = None  # [H] 1 - A^- = E_p~[1 - e^{-c}] (Tier A radius)
+    meter_two_sided: np.ndarray | None = None    # [H] min(1, 1/2 (A^2 - 1), 1/2 (A/A^- - A^-/A))
+    meter_tanh: np.ndarray | None = None         # [H] tanh(max_t c_t)
 
 
 def decode_head(q: np.ndarray, k_exact: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray,
@@ -179,16 +190,21 @@ def decode_head(q: np.ndarray, k_exact: np.ndarray, k_hat: np.ndarray, v_hat: np
     la = np.empty(H)
     lb = np.full(H, np.nan)
     cmax = np.empty(H)
+    om = np.empty(H)
     for h in range(H):
         c = tier_a_radius(q[h], w, sm_scale)
         cmax[h] = float(np.max(c)) if S else 0.0
         la[h] = log_a_minus_1(log_pt[h], c)
+        om[h] = one_minus_a_minus(p_t[h], c)
         if tier_b is not None:
             u = tier_b_radius(q[h], s_k, sm_scale, S, **tier_b)
             lb[h] = log_a_minus_1(log_pt[h], u)
     res = DecodeResult(out=out, lse=lse, tv=tv, log_am1_a=la, meter_a=meter_from_log_am1(la),
                        raw_a=raw_log_score(la), log_am1_b=lb,
                        cert_b=np.where(np.isnan(lb), np.nan, meter_from_log_am1(lb)), c_max=cmax)
+    res.one_minus_a_minus = om
+    res.meter_two_sided = two_sided_meter(la, om)
+    res.meter_tanh = det_tanh_bound(cmax)
     if vw is not None:
         res.value_r, res.value_vmax = value_side(p_t, vw)
         res.out_bound_a = output_error_bound(res.meter_a, res.value_r, res.value_vmax)
@@ -227,3 +243,27 @@ def flawed_dispersion_bound(p_t: np.ndarray, c: np.ndarray) -> float:
 def two_sided_bound(a: float, a_minus: float) -> float:
     """WitCert §4.3 Proposition 1: TV <= 1/2 (A/A^- - A^-/A) with A^- = E_p~[e^{-c}]."""
     return 0.5 * (a / a_minus - a_minus / a)
+
+
+def one_minus_a_minus(p_t: np.ndarray, c: np.ndarray) -> float:
+    """1 - A^- = E_p~[1 - e^{-c}] (WitCert §4.3 Proposition 1), computed without cancellation."""
+    c = np.asarray(c, dtype=np.float64)
+    return float(np.asarray(p_t, dtype=np.float64) @ (-np.expm1(-c))) if c.size else 0.0
+
+
+def two_sided_meter(lam1, om) -> np.ndarray:
+    """min(1, 1/2 (A^2 - 1), 1/2 (A/A^- - A^-/A)) from ln(A - 1) and 1 - A^- (Proposition 1 and Theorem 1)."""
+    lam1 = np.asarray(lam1, dtype=np.float64)
+    om = np.asarray(om, dtype=np.float64)
+    one_sided = meter_from_log_am1(lam1)
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        a = 1.0 + np.exp(lam1)
+        am = 1.0 - om
+        ts = 0.5 * (a / am - am / a)
+    ts = np.where(np.isfinite(ts), ts, 1.0)
+    return np.minimum(one_sided, np.minimum(1.0, ts))
+
+
+def det_tanh_bound(c_max) -> np.ndarray:
+    """tanh(max_t c_t): the data-independent worst-case shape TV <= tanh(max |eps|)."""
+    return np.tanh(np.asarray(c_max, dtype=np.float64))
