@@ -120,7 +120,8 @@ typedef struct kvq_cache {
 /* Meter configuration ([W] Sec. 4.2 request-level budget, Sec. 4.3 saturation). */
 typedef struct kvq_meter_params {
   uint32_t tiers;     /* bit 0: Tier A witness bound; bit 1: Tier B dither certificate (INT8 keys only);
-                         bit 2: value side of the output-error bound (requires Tier A)               */
+                         bit 2: value side of the output-error bound; bit 3: alternative bound shapes
+                         (two-sided, det-tanh); bits 2 and 3 require Tier A                          */
   int32_t n_layers;   /* L in delta_loc = delta_req / (L * H * T)                                      */
   int32_t n_q_heads;  /* H (query heads)                                                               */
   int32_t n_steps;    /* T (decode steps the request budget covers; 256 in [W])                         */
@@ -132,6 +133,7 @@ typedef struct kvq_meter_params {
 #define KVQ_TIER_A 1u
 #define KVQ_TIER_B 2u
 #define KVQ_TIER_V 4u
+#define KVQ_TIER_S 8u
 
 /* Floats per (sequence, query head) cell of meter_state. */
 #define KVQ_METER_STATE_FLOATS 8
@@ -202,7 +204,8 @@ size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t nu
  *   [2] log-sum-exp of the compressed logits (natural log); [3] tokens attended S;
  *   [4] R = sum_t p~_t rho^v_t and [5] Vmax = max_t ||v_t|| from the value
  *       witness ([W] Sec. 3), NaN when KVQ_TIER_V is off (0 for an empty sequence);
- *   [6], [7] 0.
+ *   [6] max_t c_t and [7] 1 - A^- = sum_t p~_t (1 - e^{-c_t}) of Tier A's radii
+ *       ([W] Sec. 4.3 Prop. 1 and the det-tanh shape), NaN when KVQ_TIER_S is off.
  * workspace_dev / ws_bytes: scratch of at least kvq_decode_workspace_size().
  * An empty sequence (no prefix, seq_len 0) yields out = 0 and ln(A-1) = -inf.
  */
@@ -284,6 +287,9 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_cache* pref
  * out_bound_dev (nullable): same shape, the output-error bound 2 meter_a Vmax + R
  *   of ||y - y_hat|| ([W] Sec. 3 with Tier A's meter for TV); NaN where the state
  *   has no value side.
+ * two_sided_dev (nullable): same shape, min(meter_a, 1/2 (A/A^- - A^-/A)) ([W] Sec. 4.3
+ *   Prop. 1: neither form dominates, so the minimum); NaN without KVQ_TIER_S.
+ * tanh_dev (nullable): same shape, tanh(max_t c_t) (TV <= tanh(max |eps|)); NaN without KVQ_TIER_S.
  * counts_dev:   int32[4]: cells with meter_a < tau, cells with cert_b < tau,
  *               non-finite cells, total cells (zeroed and filled by the call).
  * ranking_dev (nullable): [batch][n_layers * num_q_heads] int32 flat cell
@@ -292,7 +298,8 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache* cache, const kvq_cache* pref
  */
 kvq_status kvq_meter(const float* meter_state_dev, int32_t n_layers, int32_t batch, int32_t num_q_heads,
                      const kvq_meter_params* meter, float* meter_a_dev, float* raw_a_dev, float* cert_b_dev,
-                     float* out_bound_dev, int32_t* counts_dev, int32_t* ranking_dev, kvq_stream_t stream);
+                     float* out_bound_dev, float* two_sided_dev, float* tanh_dev, int32_t* counts_dev,
+                     int32_t* ranking_dev, kvq_stream_t stream);
 
 /* Test hook: the dither xi of (seed, layer, kv_head, slots[i], channel c) into xi_dev[i * 128 + c]. */
 kvq_status kvq_debug_dither(uint64_t seed, int32_t layer, int32_t kv_head, const int32_t* slots_dev, int32_t n,

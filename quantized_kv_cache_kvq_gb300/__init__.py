@@ -43,7 +43,7 @@ LIB_PATH = os.environ.get("KVQ_LIB") or os.path.join(_HERE, "libkvq.so")
 
 FMT = {"bf16": 0, "e4m3": 1, "e4m3s": 2, "int8": 3}
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
-TIER_A, TIER_B, TIER_V = 1, 2, 4
+TIER_A, TIER_B, TIER_V, TIER_S = 1, 2, 4, 8
 METER_STATE_FLOATS = 8  # floats per (sequence, query head) cell of meter_state
 HEAD_DIM, PAGE, N_BANDS = 128, 16, 16
 
@@ -131,7 +131,7 @@ def load(path: str = LIB_PATH):
     ]
     L.kvq_meter.restype = c_int32
     L.kvq_meter.argtypes = [c_void_p, c_int32, c_int32, c_int32, POINTER(MeterParams), c_void_p, c_void_p,
-                            c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+                            c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     L.kvq_sizeof.restype = c_size_t
     L.kvq_sizeof.argtypes = [c_int32]
     L.kvq_debug_dither.restype = c_int32
@@ -295,11 +295,12 @@ def decode_attn_noalloc(cache: PagedCache, q: torch.Tensor, block_table: torch.T
 
 def meter(meter_state: torch.Tensor, n_layers: int, batch: int, num_q_heads: int, params: MeterParams,
           meter_a: torch.Tensor, raw_a: torch.Tensor, counts: torch.Tensor, cert_b: torch.Tensor | None = None,
-          ranking: torch.Tensor | None = None, out_bound: torch.Tensor | None = None, stream=None):
+          ranking: torch.Tensor | None = None, out_bound: torch.Tensor | None = None,
+          two_sided: torch.Tensor | None = None, det_tanh: torch.Tensor | None = None, stream=None):
     """kvq_meter over meter_state [L, B, Hq, 8]."""
     _check(lib().kvq_meter(meter_state.data_ptr(), n_layers, batch, num_q_heads, ctypes.byref(params),
-                           meter_a.data_ptr(), raw_a.data_ptr(), _ptr(cert_b), _ptr(out_bound), counts.data_ptr(),
-                           _ptr(ranking), _stream(stream)), "kvq_meter")
+                           meter_a.data_ptr(), raw_a.data_ptr(), _ptr(cert_b), _ptr(out_bound), _ptr(two_sided),
+                           _ptr(det_tanh), counts.data_ptr(), _ptr(ranking), _stream(stream)), "kvq_meter")
 
 
 def debug_dither(seed: int, layer: int, kv_head: int, slots: torch.Tensor, out: torch.Tensor, stream=None):

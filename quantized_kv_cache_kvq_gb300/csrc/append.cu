@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __
   float k[4], v[4];
   load_row4(kin, vin, in_bf16, static_cast<size_t>(row) * kHeadDim + lane * 4, k, v);
   const RowCodes rc = quantize_row<KF, VF>(k, v, static_cast<uint32_t>(slot), static_cast<uint32_t>(c.layer),
-                                           static_cast<uint32_t>(head), c.dither_seed);
+                                           static_cast<uint32_t>(head), c.dither_seed, c.v_witness != nullptr);
   const size_t tile = static_cast<size_t>(page) * H + head;
   const size_t stile = static_cast<size_t>(head) * c.num_pages + page;  // scale planes are head-major
   store_row<KF, VF>(rc, t, static_cast<uint8_t*>(c.k_data) + tile * tile_bytes_k(KF),
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(256) append_newest_kernel(kvq_cache c, const v
   float k[4], v[4];
   load_row4(kin, vin, in_bf16, static_cast<size_t>(row) * kHeadDim + lane * 4, k, v);
   const RowCodes rc = quantize_row<KF, VF>(k, v, static_cast<uint32_t>(slot), static_cast<uint32_t>(c.layer),
-                                           static_cast<uint32_t>(head), c.dither_seed);
+                                           static_cast<uint32_t>(head), c.dither_seed, c.v_witness != nullptr);
   const size_t tile = static_cast<size_t>(page) * H + head;
   const size_t stile = static_cast<size_t>(head) * c.num_pages + page;
   store_row<KF, VF>(rc, t, static_cast<uint8_t*>(c.k_data) + tile * tile_bytes_k(KF),

@@ -28,13 +28,16 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float 
   m = mm;
 }
 
-// (m, l, r): r is merged with the same weights as l (the value side's sum_t e^{x_t} rho^v_t)
-__device__ __forceinline__ void lse_combine2(float& m, float& l, float& r, float m2, float l2, float r2) {
+// (m, l, r, u): r and u are merged with the same weights as l (the extended meter's p~-weighted sums:
+// sum_t e^{x_t} rho^v_t and sum_t e^{x_t} (1 - e^{-c_t}))
+__device__ __forceinline__ void lse_combine3(float& m, float& l, float& r, float& u, float m2, float l2, float r2,
+                                             float u2) {
   const float mm = fmaxf(m, m2);
   if (mm == -INFINITY) return;
   const float a = m == -INFINITY ? 0.f : ex2(m - mm), b = m2 == -INFINITY ? 0.f : ex2(m2 - mm);
   l = l * a + l2 * b;
   r = r * a + r2 * b;
+  u = u * a + u2 * b;
   m = mm;
 }
 
@@ -59,7 +62,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
       float* ms = a.meter_state + gw * KVQ_METER_STATE_FLOATS;
       *reinterpret_cast<float4*>(ms) = make_float4(-INFINITY, a.tier_b ? -INFINITY : NAN, -INFINITY,
                                                    static_cast<float>(total));
-      *reinterpret_cast<float4*>(ms + 4) = make_float4(a.value_on ? 0.f : NAN, a.value_on ? 0.f : NAN, 0.f, 0.f);
+      *reinterpret_cast<float4*>(ms + 4) = make_float4(a.value_on ? 0.f : NAN, a.value_on ? 0.f : NAN,
+                                                       a.shapes_on ? 0.f : NAN, a.shapes_on ? 0.f : NAN);
     }
     return;
   }
@@ -70,7 +74,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
   const long long w_lo = ((b_u + 1) * W - 1) / T, w_hi = (e_u * W - 1) / T;
   const int np = static_cast<int>(w_hi - w_lo + 1);
   const size_t p0 = static_cast<size_t>(w_lo) + unit;  // piece slot of the unit's first piece
-  auto stats = [&](int i) { return a.ws_stats + ((p0 + i) * a.G + row) * 8; };
+  auto stats = [&](int i) { return a.ws_stats + ((p0 + i) * a.G + row) * kStatsFloats; };
   auto accp = [&](int i) { return a.ws_acc + ((p0 + i) * a.G + row) * kHeadDim + 4 * lane; };
 
   // one round of loads: every piece's statistics (lane-parallel) and the first kU pieces' partial
@@ -81,26 +85,53 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
   for (int k = 0; k < kU; ++k)
     if (k < np) v[k] = *reinterpret_cast<const float4*>(accp(k));
   float m = -INFINITY, l = 0.f, mc = -INFINITY, sc = 0.f, mu = -INFINITY, su = 0.f, vr = 0.f, vmax = 0.f;
+  float cmax = 0.f, om = 0.f;
   float m_mine = -INFINITY;  // the running max of piece `lane` (pieces < 32), for the weights below
-  for (int i = lane; i < np; i += 32) {
-    const float4 s4 = *reinterpret_cast<const float4*>(stats(i));
-    const float4 t4 = *reinterpret_cast<const float4*>(stats(i) + 4);
-    if (i < 32) m_mine = s4.x;
-    lse_combine2(m, l, vr, s4.x, s4.y, t4.z);
-    lse_combine(mc, sc, s4.z, s4.w);
-    lse_combine(mu, su, t4.x, t4.y);
-    vmax = fmaxf(vmax, t4.w);
-  }
+  // both branches combine (m, l) with the same arithmetic (lse_combine3), so the output does not depend
+  // on whether the extended meter is on
+  if (!(a.value_on | a.shapes_on)) {
+    for (int i = lane; i < np; i += 32) {
+      const float4 s4 = *reinterpret_cast<const float4*>(stats(i));
+      const float2 t2 = *reinterpret_cast<const float2*>(stats(i) + 4);
+      if (i < 32) m_mine = s4.x;
+      lse_combine3(m, l, vr, om, s4.x, s4.y, 0.f, 0.f);
+      lse_combine(mc, sc, s4.z, s4.w);
+      lse_combine(mu, su, t2.x, t2.y);
+    }
 #pragma unroll
-  for (int off = 16; off; off >>= 1) {
-    const float m2 = __shfl_xor_sync(kFull, m, off), l2 = __shfl_xor_sync(kFull, l, off);
-    const float r2 = __shfl_xor_sync(kFull, vr, off), x2 = __shfl_xor_sync(kFull, vmax, off);
-    const float c2 = __shfl_xor_sync(kFull, mc, off), s2 = __shfl_xor_sync(kFull, sc, off);
-    const float u2 = __shfl_xor_sync(kFull, mu, off), v2 = __shfl_xor_sync(kFull, su, off);
-    lse_combine2(m, l, vr, m2, l2, r2);
-    lse_combine(mc, sc, c2, s2);
-    lse_combine(mu, su, u2, v2);
-    vmax = fmaxf(vmax, x2);
+    for (int off = 16; off; off >>= 1) {
+      const float m2 = __shfl_xor_sync(kFull, m, off), l2 = __shfl_xor_sync(kFull, l, off);
+      const float c2 = __shfl_xor_sync(kFull, mc, off), s2 = __shfl_xor_sync(kFull, sc, off);
+      const float u2 = __shfl_xor_sync(kFull, mu, off), v2 = __shfl_xor_sync(kFull, su, off);
+      lse_combine3(m, l, vr, om, m2, l2, 0.f, 0.f);
+      lse_combine(mc, sc, c2, s2);
+      lse_combine(mu, su, u2, v2);
+    }
+  } else {  // extended meter: the value side's and the shapes' sums ride on l's weights
+    for (int i = lane; i < np; i += 32) {
+      const float4 s4 = *reinterpret_cast<const float4*>(stats(i));
+      const float4 t4 = *reinterpret_cast<const float4*>(stats(i) + 4);
+      const float2 e2 = *reinterpret_cast<const float2*>(stats(i) + 8);
+      if (i < 32) m_mine = s4.x;
+      lse_combine3(m, l, vr, om, s4.x, s4.y, t4.z, e2.y);
+      lse_combine(mc, sc, s4.z, s4.w);
+      lse_combine(mu, su, t4.x, t4.y);
+      vmax = fmaxf(vmax, t4.w);
+      cmax = fmaxf(cmax, e2.x);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      const float m2 = __shfl_xor_sync(kFull, m, off), l2 = __shfl_xor_sync(kFull, l, off);
+      const float r2 = __shfl_xor_sync(kFull, vr, off), x2 = __shfl_xor_sync(kFull, vmax, off);
+      const float o2 = __shfl_xor_sync(kFull, om, off), y2 = __shfl_xor_sync(kFull, cmax, off);
+      const float c2 = __shfl_xor_sync(kFull, mc, off), s2 = __shfl_xor_sync(kFull, sc, off);
+      const float u2 = __shfl_xor_sync(kFull, mu, off), v2 = __shfl_xor_sync(kFull, su, off);
+      lse_combine3(m, l, vr, om, m2, l2, r2, o2);
+      lse_combine(mc, sc, c2, s2);
+      lse_combine(mu, su, u2, v2);
+      vmax = fmaxf(vmax, x2);
+      cmax = fmaxf(cmax, y2);
+    }
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -127,8 +158,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
     const float lb = a.tier_b ? ((su > 0.f) ? (mu + log2f(su) - lse2) * kLn2 : -INFINITY) : NAN;
     float* ms = a.meter_state + gw * KVQ_METER_STATE_FLOATS;
     *reinterpret_cast<float4*>(ms) = make_float4(la, lb, lse2 * kLn2, static_cast<float>(total));
-    *reinterpret_cast<float4*>(ms + 4) =
-        make_float4(a.value_on ? vr / l : NAN, a.value_on ? vmax : NAN, 0.f, 0.f);
+    *reinterpret_cast<float4*>(ms + 4) = make_float4(a.value_on ? vr / l : NAN, a.value_on ? vmax : NAN,
+                                                     a.shapes_on ? cmax : NAN, a.shapes_on ? om / l : NAN);
   }
 }
 
@@ -178,7 +209,7 @@ WsLayout ws_layout(int batch, int hkv, int hq, int w_max) {
   WsLayout l;
   l.cum = 0;
   l.stats = align256(static_cast<size_t>(batch + 1) * 4);
-  l.acc = l.stats + align256(slots * G * 8 * sizeof(float));
+  l.acc = l.stats + align256(slots * G * kStatsFloats * sizeof(float));
   l.total = l.acc + align256(slots * G * kHeadDim * sizeof(float));
   return l;
 }
@@ -283,7 +314,7 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   if (q_dtype != KVQ_DTYPE_F32 && q_dtype != KVQ_DTYPE_BF16) return KVQ_ERR_INVALID_ARG;
   if (max_pages_per_seq < 0 || !std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARG;
   if (meter) {
-    if (!(mp->tiers & KVQ_TIER_A) || (mp->tiers & ~7u) || mp->reserved != 0) return KVQ_ERR_INVALID_ARG;
+    if (!(mp->tiers & KVQ_TIER_A) || (mp->tiers & ~15u) || mp->reserved != 0) return KVQ_ERR_INVALID_ARG;
     if (mp->tiers & KVQ_TIER_V) {
       if (!cache->v_witness || !aligned16(cache->v_witness)) return KVQ_ERR_INVALID_ARG;
       if (prefix && prefix_len > 0 && (!prefix->v_witness || !aligned16(prefix->v_witness)))
@@ -308,7 +339,7 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   const bool has_prefix = prefix && prefix_len > 0;
   const int pkf = has_prefix ? prefix->k_fmt : kNoPrefix;
   const int pvf = has_prefix ? prefix->v_fmt : kNoPrefix;
-  const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter, meter && (mp->tiers & KVQ_TIER_V));
+  const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter, meter && (mp->tiers & (KVQ_TIER_V | KVQ_TIER_S)));
   if (!pk.launch) return KVQ_ERR_UNSUPPORTED_LAYOUT;
   const int nw = pk.warps;
   const int w_max = sms * nw;
@@ -340,6 +371,7 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   a.meter_state = meter_state;
   a.meter_on = meter ? 1 : 0;
   a.value_on = meter && (mp->tiers & KVQ_TIER_V) ? 1 : 0;
+  a.shapes_on = meter && (mp->tiers & KVQ_TIER_S) ? 1 : 0;
   a.ws_stats = reinterpret_cast<float*>(ws + wl.stats);
   a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
   a.w_max = w_max;
@@ -351,8 +383,8 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   const bool xi = cache->k_fmt == KVQ_FMT_INT8_DITHER && cache->v_fmt == KVQ_FMT_INT8_DITHER;
   const int cum_bytes = ((batch + 1) * 4 + 127) & ~127;
   const int lo_bytes = q_dtype == KVQ_DTYPE_F32 ? kQloBytes : 0;
-  const int fixed = cum_bytes + nw * ((xi ? kXiScratch : 0) + lo_bytes + (a.value_on ? kVStateBytes : 0) +
-                                       kMaxStages * 8);
+  const bool ext = a.value_on || a.shapes_on;  // the extended-meter kernel variant and its per-lane state
+  const int fixed = cum_bytes + nw * ((xi ? kXiScratch : 0) + lo_bytes + (ext ? kVStateBytes : 0) + kMaxStages * 8);
   const int budget = smem_max - 1024 - fixed;
   int stages = budget / (nw * sb);
   if (stages > kMaxStages) stages = kMaxStages;

@@ -36,9 +36,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr int kNoPrefix = -1;
 constexpr int kXiScratch = 16 * 128 * 2;  // per-warp fp16 dither tile (INT8 values)
-// Value side of the output bound: per lane (sum_t e^{x_t - m} rho^v_t for heads 2c and 2c + 1, rescaled
-// with l; max_t ||v_t||; unused) in shared memory, so it costs no registers in the page loop.
-constexpr int kVStateBytes = 32 * 16;
+// Extended meter state per lane in shared memory (so it costs no registers in the page loop), 8 floats:
+// value side (sum_t e^{x_t - m} rho^v_t for heads 2c and 2c + 1, rescaled with l; max_t ||v_t||; 0) and
+// alternative bound shapes (max_t c_t for heads 2c, 2c + 1; sum_t e^{x_t - m} (1 - e^{-c_t}) for both heads).
+constexpr int kVStateBytes = 32 * 32;
+constexpr int kExtValue = 1, kExtShapes = 2;
+constexpr int kStatsFloats = 12;  // per (piece, head): m l mc sc | mu su vr vmax | cmax om 0 0
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // a copy not landed after 2 s is reported as a timeout
 
@@ -73,6 +76,7 @@ struct Args {
   float* meter_state;  // [B][Hq][4] or nullptr
   int meter_on;
   int value_on;      // value side of the output bound (value witness read, R and Vmax accumulated)
+  int shapes_on;     // alternative bound shapes (max radius, 1 - A^-)
   float* ws_stats;   // [slots][G][8]
   float* ws_acc;     // [slots][G][128]
   int w_max;
@@ -496,7 +500,7 @@ __device__ __forceinline__ void accumulate_meter(const float (&r)[4], const floa
 template <int KF, int VF, bool METER>
 __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile, float xb0, float xb1, uint32_t phys,
                                              const Planes& pl, int kvh, const QFrag& f, SoftState& s,
-                                             float qk_scale, bool tier_b, float* vstate) {
+                                             float qk_scale, bool tier_b, float* vstate, int ext) {
   using L = Layout<KF, VF, METER>;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   constexpr bool K16 = fmt_is_16bit(KF);
@@ -597,15 +601,15 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   for (int v = 0; v < 4; ++v) p[v] = ex2(x[v] - mnew[v & 1]);  // 0 for -inf logits
 #pragma unroll
   for (int h = 0; h < 2; ++h) s.l[h] = s.l[h] * alpha[h] + (p[h] + p[2 + h]);
-  if (METER && vstate) {
+  if (METER && vstate && (ext & kExtValue)) {
     // value side: rho^v and ||v|| of tokens g and g + 8 (WitCert Sec. 3 output bound)
     const uint2 vw = lds64(st + L::vwOff + 8 * g);
     const float2 rho = unpack_f16(vw.x), vn = unpack_f16(vw.y);
-    float4 v4 = *reinterpret_cast<const float4*>(vstate + 4 * lane);
+    float4 v4 = *reinterpret_cast<const float4*>(vstate + 8 * lane);
     v4.x = __fmaf_rn(p[2], rho.y, __fmaf_rn(p[0], rho.x, v4.x * alpha[0]));
     v4.y = __fmaf_rn(p[3], rho.y, __fmaf_rn(p[1], rho.x, v4.y * alpha[1]));
     v4.z = fmaxf(v4.z, fmaxf(vn.x, vn.y));
-    *reinterpret_cast<float4*>(vstate + 4 * lane) = v4;
+    *reinterpret_cast<float4*>(vstate + 8 * lane) = v4;
   }
   if (__any_sync(kFull, (alpha[0] != 1.f) | (alpha[1] != 1.f))) {
 #pragma unroll
@@ -624,6 +628,15 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
 #pragma unroll
     for (int v = 0; v < 4; ++v) cv[v] = fmaxf(C[v] * f.cm_scale, 0.f);
     accumulate_meter(cv, x, p, alpha, mnew, s.mc, s.sc, s.slow_a);
+    if (vstate && (ext & kExtShapes)) {
+      // alternative shapes (WitCert Sec. 4.3 Prop. 1; det-tanh): max_t c_t and sum_t e^{x_t - m} (1 - e^{-c_t})
+      float4 w4 = *reinterpret_cast<const float4*>(vstate + 8 * lane + 4);
+      w4.x = fmaxf(w4.x, fmaxf(cv[0], cv[2]));
+      w4.y = fmaxf(w4.y, fmaxf(cv[1], cv[3]));
+      w4.z = __fmaf_rn(p[2], one_minus_exp_neg(cv[2]), __fmaf_rn(p[0], one_minus_exp_neg(cv[0]), w4.z * alpha[0]));
+      w4.w = __fmaf_rn(p[3], one_minus_exp_neg(cv[3]), __fmaf_rn(p[1], one_minus_exp_neg(cv[1]), w4.w * alpha[1]));
+      *reinterpret_cast<float4*>(vstate + 8 * lane + 4) = w4;
+    }
     if (KDITHER && tier_b) {
       float uv[4];
 #pragma unroll
@@ -752,14 +765,14 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     using L = Layout<(PKF < 0 ? 0 : PKF), (PVF < 0 ? 0 : PVF), METER>;
     constexpr int pk = (PKF < 0 ? 0 : PKF), pv = (PVF < 0 ? 0 : PVF);
     const size_t tile = static_cast<size_t>(d.phys) * a.Hkv + kvh;
-    mbar_arrive_expect_tx(bar, VALUE ? L::total : L::unvalued);
+    mbar_arrive_expect_tx(bar, VALUE && a.value_on ? L::total : L::unvalued);
     bulk_g2s(stage + L::kOff, a.pre.k + tile * L::kBytes, L::kBytes, bar);
     bulk_g2s(stage + L::vOff, a.pre.v + tile * L::vBytes, L::vBytes, bar);
     if (METER) bulk_g2s(stage + L::wOff, a.pre.w + tile * kTileBytesW, kTileBytesW, bar);
     const size_t stile = static_cast<size_t>(kvh) * a.pre.num_pages + d.phys;
     if (fmt_has_scale(pk)) bulk_g2s(stage + L::ksOff, a.pre.ks + stile * kTileBytesS, kTileBytesS, bar);
     if (fmt_has_scale(pv)) bulk_g2s(stage + L::vsOff, a.pre.vs + stile * kTileBytesS, kTileBytesS, bar);
-    if (METER && VALUE) bulk_g2s(stage + L::vwOff, a.pre.vw + stile * kTileBytesVW, kTileBytesVW, bar);
+    if (METER && VALUE && a.value_on) bulk_g2s(stage + L::vwOff, a.pre.vw + stile * kTileBytesVW, kTileBytesVW, bar);
   } else {
     using L = Layout<KF, VF, METER>;
     const size_t tile = static_cast<size_t>(d.phys) * a.Hkv + kvh;
@@ -768,7 +781,7 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
       asm volatile("griddepcontrol.wait;" ::: "memory");
       asm volatile("fence.proxy.async.global;" ::: "memory");
     }
-    mbar_arrive_expect_tx(bar, VALUE ? L::total : L::unvalued);
+    mbar_arrive_expect_tx(bar, VALUE && a.value_on ? L::total : L::unvalued);
     bulk_g2s(stage + L::kOff, a.live.k + tile * L::kBytes, L::kBytes, bar);
     bulk_g2s(stage + L::vOff, a.live.v + tile * L::vBytes, L::vBytes, bar);
     if (METER) bulk_g2s(stage + L::wOff, a.live.w + tile * kTileBytesW, kTileBytesW, bar);
@@ -776,7 +789,7 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     const size_t stile = static_cast<size_t>(kvh) * a.live.num_pages + d.phys;
     if (fmt_has_scale(KF)) bulk_g2s(stage + L::ksOff, a.live.ks + stile * kTileBytesS, kTileBytesS, bar);
     if (fmt_has_scale(VF)) bulk_g2s(stage + L::vsOff, a.live.vs + stile * kTileBytesS, kTileBytesS, bar);
-    if (METER && VALUE) bulk_g2s(stage + L::vwOff, a.live.vw + stile * kTileBytesVW, kTileBytesVW, bar);
+    if (METER && VALUE && a.value_on) bulk_g2s(stage + L::vwOff, a.live.vw + stile * kTileBytesVW, kTileBytesVW, bar);
   }
 }
 
@@ -790,15 +803,22 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
     sc[h] = col_sum8(s.sc[h]);
     su[h] = col_sum8(s.su[h]);
   }
-  float vmax = 0.f;
+  float vmax = 0.f, cmax[2] = {0.f, 0.f}, om[2] = {0.f, 0.f};
   if (vstate) {
-    const float4 v4 = *reinterpret_cast<const float4*>(vstate + 4 * lane);
+    const float4 v4 = *reinterpret_cast<const float4*>(vstate + 8 * lane);
+    const float4 w4 = *reinterpret_cast<const float4*>(vstate + 8 * lane + 4);
     vr[0] = col_sum8(v4.x);
     vr[1] = col_sum8(v4.y);
     vmax = v4.z;
 #pragma unroll
     for (int o = 16; o; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, o));
-    *reinterpret_cast<float4*>(vstate + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);  // next unit starts empty
+    cmax[0] = col_max8(w4.x);
+    cmax[1] = col_max8(w4.y);
+    om[0] = col_sum8(w4.z);
+    om[1] = col_sum8(w4.w);
+    // the next unit starts empty
+    *reinterpret_cast<float4*>(vstate + 8 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(vstate + 8 * lane + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -811,9 +831,10 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
         acc[16 * mt + g + 8] = s.o[mt][2 + h];
       }
       if (g == 0) {
-        float* st = a.ws_stats + (slot * a.G + head) * 8;
+        float* st = a.ws_stats + (slot * a.G + head) * kStatsFloats;
         *reinterpret_cast<float4*>(st) = make_float4(s.m[h], l[h], s.mc[h], sc[h]);
         *reinterpret_cast<float4*>(st + 4) = make_float4(s.mu[h], su[h], vr[h], vmax);
+        *reinterpret_cast<float4*>(st + 8) = make_float4(cmax[h], om[h], 0.f, 0.f);
       }
     }
   }
@@ -822,9 +843,9 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
 // Zero the bytes of tokens nvalid..15 in a stage (a partial last page): the slots past the end of a
 // sequence may hold anything, and zeros make their logit exactly the -inf bias, their value and
 // radius exactly 0.  Runs once per unit at most; all lanes take part.
-// VALUE: the stage holds a value witness tile (only then does the stage have room for it).
+// vw_on: the stage holds a value witness tile (only then does the stage have room for it).
 template <int KF, int VF, bool METER, bool VALUE>
-__device__ void zero_tail(uint8_t* st, int nvalid) {
+__device__ void zero_tail(uint8_t* st, int nvalid, bool vw_on) {
   using L = Layout<KF, VF, METER>;
   const int lane = threadIdx.x & 31;
   const int n = (kPage - nvalid) * kHeadDim;
@@ -842,7 +863,7 @@ __device__ void zero_tail(uint8_t* st, int nvalid) {
   for (int t = nvalid + lane; t < kPage; t += 32) {
     if (fmt_has_scale(KF)) *reinterpret_cast<uint16_t*>(st + L::ksOff + s_offset(t)) = 0;
     if (fmt_has_scale(VF)) *reinterpret_cast<uint16_t*>(st + L::vsOff + s_offset(t)) = 0;
-    if (METER && VALUE) {
+    if (METER && VALUE && vw_on) {
       *reinterpret_cast<uint16_t*>(st + L::vwOff + vw_offset(t, 0)) = 0;
       *reinterpret_cast<uint16_t*>(st + L::vwOff + vw_offset(t, 1)) = 0;
     }
@@ -850,8 +871,9 @@ __device__ void zero_tail(uint8_t* st, int nvalid) {
   __syncwarp();
 }
 
-// VALUE: the value side of the output bound is compiled in (value witness staged and accumulated);
-// without it no trace of the value side is left in the kernel.
+// VALUE: the extended meter is compiled in (value side of the output bound and alternative bound
+// shapes, chosen at run time; the value witness is staged only when the value side is on); without it
+// no trace of either is left in the kernel.
 template <int KF, int VF, int PKF, int PVF, int NW, bool METER, bool VALUE>
 __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -914,7 +936,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
 
   // ---- per-warp shared memory: stages, dither tile, query low parts, barriers
   const int lo_bytes = a.q_bf16 ? 0 : kQloBytes;
-  static_assert(METER || !VALUE, "the value side rides on the meter");
+  static_assert(METER || !VALUE, "the extended meter rides on the meter");
   const int v_bytes = VALUE ? kVStateBytes : 0;
   const int per_warp = a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes + v_bytes + kMaxStages * 8;
   uint8_t* wbase = smem + cum_bytes + warp * per_warp;
@@ -922,7 +944,11 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   float* vstate = VALUE ? reinterpret_cast<float*>(xi_tile + (XI ? kXiScratch : 0) + lo_bytes) : nullptr;
   uint64_t* bars =
       reinterpret_cast<uint64_t*>(wbase + a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes + v_bytes);
-  if (vstate) *reinterpret_cast<float4*>(vstate + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (vstate) {
+    *reinterpret_cast<float4*>(vstate + 8 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(vstate + 8 * lane + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int ext = (a.value_on ? kExtValue : 0) | (a.shapes_on ? kExtShapes : 0);
   if (lane == 0) {
     for (int i = 0; i < a.stages; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
@@ -975,13 +1001,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       const float xb0 = g8 < nvalid ? 0.f : -INFINITY, xb1 = g8 + 8 < nvalid ? 0.f : -INFINITY;
       if (PKF != kNoPrefix && d_prefix(info)) {
         constexpr int pk = (PKF < 0 ? 0 : PKF), pv = (PVF < 0 ? 0 : PVF);
-        if (nvalid < kPage) zero_tail<pk, pv, METER, VALUE>(st, nvalid);
+        if (nvalid < kPage) zero_tail<pk, pv, METER, VALUE>(st, nvalid, a.value_on != 0);
         process_page<pk, pv, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.pre, kvh, f, s,
-                                    qk_scale, a.tier_b != 0, vstate);
+                                    qk_scale, a.tier_b != 0, vstate, ext);
       } else {
-        if (nvalid < kPage) zero_tail<KF, VF, METER, VALUE>(st, nvalid);
+        if (nvalid < kPage) zero_tail<KF, VF, METER, VALUE>(st, nvalid, a.value_on != 0);
         process_page<KF, VF, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f, s,
-                                    qk_scale, a.tier_b != 0, vstate);
+                                    qk_scale, a.tier_b != 0, vstate, ext);
       }
     }
     __syncwarp();

@@ -5,7 +5,9 @@
 // Sec. 6.2.4 ("Certificate telemetry in production"): reduce certificates on the GPU without a host
 // synchronisation per layer, and count non-finite values separately from the finite statistics.
 // Sec. 3: the output moves by at most 2 TV max_t ||v_t|| + sum_t p~_t rho^v_t; with the meter for TV
-// that is the output-error bound 2 meter Vmax + R.
+// that is the output-error bound 2 meter Vmax + R.  Sec. 4.3 Prop. 1: TV <= 1/2 (A/A^- - A^-/A), and
+// neither this nor 1/2 (A^2 - 1) dominates, so the two-sided meter is the minimum; the det-tanh shape
+// TV <= tanh(max |eps|) uses the largest radius.
 #include "kvq_common.cuh"
 
 namespace kvq {
@@ -29,6 +31,7 @@ __device__ __forceinline__ void finalize_one(float la, float& meter, float& raw)
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ state, long long n, float tau,
                                                        float* __restrict__ meter_a, float* __restrict__ raw_a,
                                                        float* __restrict__ cert_b, float* __restrict__ out_bound,
+                                                       float* __restrict__ two_sided, float* __restrict__ det_tanh,
                                                        int32_t* __restrict__ counts) {
   int cov_a = 0, cov_b = 0, nonfinite = 0, cells = 0;
   static_assert(KVQ_METER_STATE_FLOATS == 8, "two float4 per cell");
@@ -39,9 +42,23 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
     finalize_one(s.x, m, r);
     meter_a[i] = m;
     raw_a[i] = r;
-    if (out_bound) {
-      const float4 v = reinterpret_cast<const float4*>(state)[2 * i + 1];  // (R, Vmax, 0, 0)
-      out_bound[i] = (isnan(v.x) || isnan(m)) ? NAN : __fmaf_rn(2.f * m, v.y, v.x);
+    if (out_bound || two_sided || det_tanh) {
+      const float4 v = reinterpret_cast<const float4*>(state)[2 * i + 1];  // (R, Vmax, max c, 1 - A^-)
+      if (out_bound) out_bound[i] = (isnan(v.x) || isnan(m)) ? NAN : __fmaf_rn(2.f * m, v.y, v.x);
+      if (det_tanh) det_tanh[i] = isnan(v.z) ? NAN : tanhf(v.z);
+      if (two_sided) {
+        float t = NAN;
+        if (!isnan(v.w) && !isnan(m)) {
+          t = m;
+          if (s.x != -INFINITY && s.x < 80.f && v.w < 1.f) {
+            // 1/2 (A/A^- - A^-/A) with x = A - 1 = e^{la}, y = 1 - A^-, free of cancellation:
+            // A/A^- - A^-/A = (A - A^-)(A + A^-) / (A A^-) = (x + y)(2 + x - y) / ((1 + x)(1 - y))
+            const float x = expf(s.x), y = v.w;
+            t = fminf(t, 0.5f * ((x + y) * (2.f + x - y)) / ((1.f + x) * (1.f - y)));
+          }
+        }
+        two_sided[i] = t;
+      }
     }
     cells += 1;
     if (isnan(s.x) || s.x == INFINITY) nonfinite += 1;
@@ -101,7 +118,8 @@ using namespace kvq;
 
 extern "C" kvq_status kvq_meter(const float* state, int32_t n_layers, int32_t batch, int32_t hq,
                                 const kvq_meter_params* mp, float* meter_a, float* raw_a, float* cert_b,
-                                float* out_bound, int32_t* counts, int32_t* ranking, kvq_stream_t stream) {
+                                float* out_bound, float* two_sided, float* det_tanh, int32_t* counts, int32_t* ranking,
+                                kvq_stream_t stream) {
   if (!mp || n_layers < 0 || batch < 0 || hq <= 0) return KVQ_ERR_INVALID_ARG;
   if (!state || !meter_a || !raw_a || !counts) return KVQ_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(state) & 15u) != 0) return KVQ_ERR_INVALID_ARG;
@@ -113,7 +131,7 @@ extern "C" kvq_status kvq_meter(const float* state, int32_t n_layers, int32_t ba
   long long blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
   finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(state, n, mp->tau, meter_a, raw_a, cert_b, out_bound,
-                                                                counts);
+                                                                two_sided, det_tanh, counts);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   if (ranking) {
     rank_kernel<<<batch, 512, 0, s>>>(raw_a, n_layers, batch, hq, ranking);

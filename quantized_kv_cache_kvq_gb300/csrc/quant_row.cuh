@@ -143,9 +143,10 @@ struct RowCodes {
   bool range;             // value scale above KVQ_MAX_VALUE_SCALE (warp-uniform)
 };
 
+// want_vw: compute the value witness (the cache has a value witness plane).
 template <int KF, int VF>
 __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v[4], uint32_t slot, uint32_t layer,
-                                                 uint32_t head, uint64_t seed) {
+                                                 uint32_t head, uint64_t seed, bool want_vw) {
   const int lane = threadIdx.x & 31;
   RowCodes rc;
   bool finite = true;
@@ -179,20 +180,24 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
   ss = __fadd_ru(ss, __shfl_xor_sync(0xffffffffu, ss, 16));
   rc.wb = __half_as_ushort(__float2half_ru(__fsqrt_ru(ss)));
   // Value witness: upper bounds of ||v_hat - v|| and ||v|| over all 128 channels (sums rounded up)
-  float rv = 0.0f, vv = 0.0f;
+  rc.vrho = 0;
+  rc.vnorm = 0;
+  if (want_vw) {  // warp-uniform
+    float rv = 0.0f, vv = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float a = fmaxf(qv.hi[i], -qv.lo[i]);
-    rv = __fmaf_ru(a, a, rv);
-    vv = __fmaf_ru(v[i], v[i], vv);
-  }
+    for (int i = 0; i < 4; ++i) {
+      const float a = fmaxf(qv.hi[i], -qv.lo[i]);
+      rv = __fmaf_ru(a, a, rv);
+      vv = __fmaf_ru(v[i], v[i], vv);
+    }
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    rv = __fadd_ru(rv, __shfl_xor_sync(0xffffffffu, rv, o));
-    vv = __fadd_ru(vv, __shfl_xor_sync(0xffffffffu, vv, o));
+    for (int o = 16; o; o >>= 1) {
+      rv = __fadd_ru(rv, __shfl_xor_sync(0xffffffffu, rv, o));
+      vv = __fadd_ru(vv, __shfl_xor_sync(0xffffffffu, vv, o));
+    }
+    rc.vrho = __half_as_ushort(__float2half_ru(__fsqrt_ru(rv)));
+    rc.vnorm = __half_as_ushort(__float2half_ru(__fsqrt_ru(vv)));
   }
-  rc.vrho = __half_as_ushort(__float2half_ru(__fsqrt_ru(rv)));
-  rc.vnorm = __half_as_ushort(__float2half_ru(__fsqrt_ru(vv)));
   rc.nonfinite = !finite || (flags & 1);  // flags are warp-uniform: amax and the scales are
   rc.range = (flags & 2) != 0;
   return rc;

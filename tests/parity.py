@@ -83,7 +83,7 @@ def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
     res = {k: np.zeros((B, w.n_q_heads) + sh) for k, sh in
            (("out", (128,)), ("lse", ()), ("tv", ()), ("log_am1", ()), ("meter", ()), ("raw", ()),
             ("log_am1_b", ()), ("cert_b", ()), ("value_r", ()), ("value_vmax", ()), ("out_bound", ()),
-            ("out_err", ()))}
+            ("out_err", ()), ("c_max", ()), ("om", ()), ("meter_2s", ()), ("meter_tanh", ()))}
     rows_all = []
     for s in range(B):
         k32, v32, q = inp["seqs"][s]
@@ -124,13 +124,17 @@ def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
             res["value_vmax"][s, sl] = r.value_vmax
             res["out_bound"][s, sl] = r.out_bound_a
             res["out_err"][s, sl] = r.out_err
+            res["c_max"][s, sl] = r.c_max
+            res["om"][s, sl] = r.one_minus_a_minus
+            res["meter_2s"][s, sl] = r.meter_two_sided
+            res["meter_tanh"][s, sl] = r.meter_tanh
     res["rows"] = rows_all
     res["prefix_rows"] = pre_rows
     return res
 
 
 def run_case_gpu(w, layer: int = 0, inputs=None, meter: bool = True, tier_b: bool | None = None,
-                 q_dtype=None, device="cuda", value: bool = False):
+                 q_dtype=None, device="cuda", value: bool = False, shapes: bool = False):
     """Append + decode (+ meter) of the case through the C ABI; returns host arrays and the caches."""
     import torch
 
@@ -168,8 +172,8 @@ def run_case_gpu(w, layer: int = 0, inputs=None, meter: bool = True, tier_b: boo
     ws = torch.empty(kvq.decode_workspace_size(B, Hkv, Hq), dtype=torch.uint8, device=dev)
     mp = None
     if meter:
-        mp = kvq.meter_params(kvq.TIER_A | (kvq.TIER_B if tier_b else 0) | (kvq.TIER_V if value else 0), w.n_layers,
-                              w.n_q_heads, w.n_steps, w.delta_req, w.tau)
+        mp = kvq.meter_params(kvq.TIER_A | (kvq.TIER_B if tier_b else 0) | (kvq.TIER_V if value else 0)
+                              | (kvq.TIER_S if shapes else 0), w.n_layers, w.n_q_heads, w.n_steps, w.delta_req, w.tau)
     kvq.decode_attn(cache, q, bt, lens, out, ws, prefix=prefix, prefix_len=w.prefix_len, sm_scale=SM_SCALE,
                     meter=mp, meter_state=ms if meter else None, err=err)
     res = dict(out=out.cpu().numpy().astype(np.float64), err=int(err.item()), cache=cache, prefix=prefix,
@@ -183,6 +187,8 @@ def run_case_gpu(w, layer: int = 0, inputs=None, meter: bool = True, tier_b: boo
         res["meter"] = OA.meter_from_log_am1(msn[..., 0])
         res["value_r"] = msn[..., 4]
         res["value_vmax"] = msn[..., 5]
+        res["c_max"] = msn[..., 6]
+        res["om"] = msn[..., 7]
         res["mp"] = mp
         res["ms_dev"] = ms
     return res
