@@ -56,6 +56,7 @@ __all__ = [
     "band_q_norms",
     "tier_a_radius",
     "tier_b_radius",
+    "tier_b_radius_bypass",
     "log_a_minus_1",
     "meter_from_log_am1",
     "raw_log_score",
@@ -122,6 +123,29 @@ def tier_b_radius(q: np.ndarray, s_k: np.ndarray, sm_scale: float, seq_len: int,
     return sm_scale * qn * kappa * np.asarray(s_k, dtype=np.float64)
 
 
+FP16_REL = 2.0 ** -11   # |RN_fp16(x) - x| <= 2^-11 |RN_fp16(x)| for normal results ...
+FP16_ABS = 2.0 ** -25   # ... and <= 2^-25 in the subnormal range
+
+
+def tier_b_radius_bypass(q: np.ndarray, s_k: np.ndarray, k_hat_bypass: np.ndarray, channels, sm_scale: float,
+                         seq_len: int, delta_req: float, n_layers: int, n_q_heads: int, n_steps: int) -> np.ndarray:
+    """Tier B radius with the fixed-channel bypass (WitCert §6.2.5, §4.2).
+
+    The dither (probabilistic) term uses the query restricted to the INT8 channels (the bypassed
+    channels leave the variance term); the bypassed channels' fp16 rounding is deterministic and
+    added by Cauchy-Schwarz: |q_O . r_O| <= ||q_O|| (2^-11 ||k_hat_O|| + sqrt(2m) 2^-25).
+    ``k_hat_bypass`` [S, 2m]: the stored fp16 values of the bypassed channels.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    ch = np.asarray(channels)
+    keep = np.ones(q.shape[-1], dtype=bool)
+    keep[ch] = False
+    u = tier_b_radius(q[keep], s_k, sm_scale, seq_len, delta_req, n_layers, n_q_heads, n_steps)
+    qo = float(np.sqrt(np.sum(q[ch] ** 2)))
+    ko = np.sqrt(np.sum(np.asarray(k_hat_bypass, dtype=np.float64) ** 2, axis=-1))
+    return u + sm_scale * qo * (FP16_REL * ko + math.sqrt(len(ch)) * FP16_ABS)
+
+
 def log_a_minus_1(log_p: np.ndarray, radius: np.ndarray) -> float:
     """ln(A - 1) with A - 1 = sum_t p~_t (e^{c_t} - 1), evaluated in the log domain (WitCert §3)."""
     terms = np.asarray(log_p, dtype=np.float64) + log_expm1(radius)
@@ -167,14 +191,15 @@ class DecodeResult:
 def decode_head(q: np.ndarray, k_exact: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray,
                 w: np.ndarray, sm_scale: float, s_k: np.ndarray | None = None,
                 tier_b: dict | None = None, vw: np.ndarray | None = None,
-                v_exact: np.ndarray | None = None) -> DecodeResult:
+                v_exact: np.ndarray | None = None, bypass: dict | None = None) -> DecodeResult:
     """Decode attention of H query heads that share one kv head's cache.
 
     q [H, 128] (the query values exactly as the kernel reads them), k_exact
     [S, 128] (the binary32 post-RoPE keys), k_hat / v_hat [S, 128] (exact
     dequantized cache), w [S, 16] (witness values), s_k [S] (key scales, Tier B),
     tier_b = dict(delta_req, n_layers, n_q_heads, n_steps) or None, vw [S, 2] (value witness
-    values: rho^v, ||v||) or None, v_exact [S, 128] (the binary32 values) or None.
+    values: rho^v, ||v||) or None, v_exact [S, 128] (the binary32 values) or None, bypass =
+    dict(channels [2m], values [S, 2m]) for keys stored with the fixed-channel outlier bypass (Tier B).
     """
     q = np.asarray(q, dtype=np.float64)
     H = q.shape[0]
@@ -197,7 +222,10 @@ def decode_head(q: np.ndarray, k_exact: np.ndarray, k_hat: np.ndarray, v_hat: np
         la[h] = log_a_minus_1(log_pt[h], c)
         om[h] = one_minus_a_minus(p_t[h], c)
         if tier_b is not None:
-            u = tier_b_radius(q[h], s_k, sm_scale, S, **tier_b)
+            if bypass is not None:
+                u = tier_b_radius_bypass(q[h], s_k, bypass["values"], bypass["channels"], sm_scale, S, **tier_b)
+            else:
+                u = tier_b_radius(q[h], s_k, sm_scale, S, **tier_b)
             lb[h] = log_a_minus_1(log_pt[h], u)
     res = DecodeResult(out=out, lse=lse, tv=tv, log_am1_a=la, meter_a=meter_from_log_am1(la),
                        raw_a=raw_log_score(la), log_am1_b=lb,

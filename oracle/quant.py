@@ -22,6 +22,11 @@ Rules taken from the pages
 * WitCert §4.1, eq. (2): the witness w_{t,b} = ||r_{t,b}|| is the Euclidean
   norm of the key residual r = k_hat - k over band b, stored in fp16.  Bands are
   B = 16 contiguous groups of RoPE frequency pairs (4 pairs = 8 coordinates each).
+* WitCert §6.2.5 (fixed-channel outlier bypass): a fixed set of m RoPE pairs per
+  (layer, kv head) keeps its 2m key channels in fp16, and those channels are
+  excluded from the group amax (bypassing without the exclusion leaves the scale,
+  and so the error of every other channel, unchanged).  Here the INT8 code of a
+  bypassed channel is 0 and its value is the fp16 one (round to nearest even).
 * WitCert §3 (the output bound ||y - y_hat|| <= 2 TV max_t ||v_t|| + sum_t p~_t rho^v_t):
   the value side needs, per token, rho^v_t = ||v_hat_t - v_t|| and ||v_t||; stored
   here as a value witness of two fp16 numbers per (token, kv head).
@@ -61,6 +66,9 @@ __all__ = [
     "dequantize",
     "witness_bits",
     "value_witness_bits",
+    "bypass_channels",
+    "quantize_int8_bypass",
+    "dequantize_int8_bypass",
     "band_norms",
 ]
 
@@ -121,6 +129,47 @@ def quantize(x32: np.ndarray, fmt: str, xi: np.ndarray | None = None):
         code = np.where((s == 0)[..., None] | ~np.isfinite(code), 0, code)
         return code.astype(np.int8), s_bits, valid
     raise ValueError(fmt)
+
+
+def bypass_channels(pairs) -> np.ndarray:
+    """Key channels of outlier RoPE pairs j (half-split pairing: channels j and j + 64), in the stored
+    column order: column 2i -> channel pairs[i], column 2i + 1 -> channel pairs[i] + 64."""
+    pairs = np.asarray(pairs, dtype=np.int64)
+    assert pairs.ndim == 1 and np.all((pairs >= 0) & (pairs < HEAD_DIM // 2)) and len(set(pairs.tolist())) == len(pairs)
+    return np.stack([pairs, pairs + HEAD_DIM // 2], axis=-1).reshape(-1)
+
+
+def quantize_int8_bypass(x32: np.ndarray, xi: np.ndarray, pairs, exclude_from_amax: bool = True):
+    """Subtractively dithered INT8 with the fixed-channel outlier bypass (WitCert §6.2.5).
+
+    Returns ``(codes, scale_bits, outlier_bits, valid)``: INT8 codes (0 at bypassed channels), the fp16
+    scale of amax over the other channels (over all channels when ``exclude_from_amax`` is False, the
+    page's "bypass, amax unchanged" control), the fp16 patterns [..., 2m] of the bypassed channels in
+    column order, and ``valid`` (False for non-finite input or an fp16 overflow of scale or outlier).
+    """
+    x = np.asarray(x32, dtype=np.float32)
+    ch = bypass_channels(pairs)
+    keep = np.ones(HEAD_DIM, dtype=bool)
+    keep[ch] = False
+    finite = np.all(np.isfinite(x), axis=-1)
+    amax = np.max(np.abs(np.where(keep, x, 0.0) if exclude_from_amax else x), axis=-1).astype(np.float32)
+    s_bits = _scale_bits(amax, INT8_DIVISOR)
+    s = fp16_value(s_bits)
+    out_bits = fp16_bits(x[..., ch].astype(np.float64), "rne")
+    valid = finite & np.isfinite(s) & np.all(np.isfinite(fp16_value(out_bits)), axis=-1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = f32(x.astype(np.float64) / s[..., None])
+        y2 = f32(y.astype(np.float64) + xi)
+        code = np.clip(np.rint(y2.astype(np.float64)), -INT8_QMAX, INT8_QMAX)
+    code = np.where((s == 0)[..., None] | ~np.isfinite(code) | ~keep, 0, code)
+    return code.astype(np.int8), s_bits, out_bits, valid
+
+
+def dequantize_int8_bypass(codes, scale_bits, outlier_bits, xi, pairs) -> np.ndarray:
+    """x_hat: s (code - xi) on the INT8 channels, the fp16 value on the bypassed ones."""
+    xh = dequantize(codes, scale_bits, "int8", xi)
+    xh[..., bypass_channels(pairs)] = fp16_value(outlier_bits)
+    return xh
 
 
 def dequantize(codes: np.ndarray, scale_bits: np.ndarray | None, fmt: str, xi: np.ndarray | None = None):
