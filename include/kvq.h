@@ -95,6 +95,13 @@ typedef enum kvq_dtype { KVQ_DTYPE_F32 = 0, KVQ_DTYPE_BF16 = 1 } kvq_dtype;
  *   value witness (64 B, fp16 bits):  8*(t&7) + 4*k + 2*(t>>3), k = 0: rho^v_t =
  *                        ||v_hat_t - v_t||, k = 1: ||v_t|| (both rounded up; [W] Sec. 3,
  *                        the output bound ||y - y_hat|| <= 2 TV max_t ||v_t|| + sum_t p~_t rho^v_t)
+ *   key outliers (fp16 bits, column col in 0..2m-1; column 2i holds channel pairs[i],
+ *                 column 2i+1 channel pairs[i] + 64; unused columns 0):
+ *       m <= 4 (256 B):  8*(4*(t&7) + (col>>1)) + 4*(t>>3) + 2*(col&1)
+ *       m <= 8 (512 B):  16*(4*(t&7) + ((col&7)>>1)) + 8*(col>>3) + 4*(t>>3) + 2*(col&1)
+ *     ([W] Sec. 6.2.5 fixed-channel outlier bypass: a fixed set of m RoPE pairs per
+ *     (layer, kv head) is stored in fp16 (round to nearest even) and left out of the
+ *     INT8 amax; the INT8 code of a bypassed channel is 0).  Head-major like the scales.
  * Band b holds the RoPE frequency pairs 4b..4b+3 of the half-split pairing
  * (pair j = channels j and j+64), i.e. channels 4b..4b+3 and 64+4b..64+4b+3
  * ([W] Sec. 4.1, eq. (2)).
@@ -115,6 +122,12 @@ typedef struct kvq_cache {
                              kvq_decode_attn when the meter is on                      */
   uint16_t* v_witness;    /* value witness tiles (fp16 bits) or NULL; written by kvq_append
                              when non-NULL, required by kvq_decode_attn with KVQ_TIER_V */
+  const int32_t* outlier_pairs; /* [num_kv_heads][n_outlier_pairs] RoPE pair indices j in 0..63
+                             (channels j and j+64) bypassed in fp16, device memory; NULL iff
+                             n_outlier_pairs == 0.  INT8-dithered keys only. */
+  int32_t n_outlier_pairs;  /* m in 0..8 (0: no bypass); pairs of one head are distinct   */
+  int32_t reserved2;        /* must be 0                                                 */
+  uint16_t* k_outlier;      /* key outlier tiles (fp16 bits); non-NULL iff m > 0         */
 } kvq_cache;
 
 /* Meter configuration ([W] Sec. 4.2 request-level budget, Sec. 4.3 saturation). */
@@ -139,7 +152,8 @@ typedef struct kvq_meter_params {
 #define KVQ_METER_STATE_FLOATS 8
 
 /* Bytes of one tile of a plane: plane 0 = K, 1 = V, 2 = K scale, 3 = V scale, 4 = witness,
-   5 = value witness.  Returns 0 for a plane the format does not store. */
+   5 = value witness, 6 = key outliers with m <= 4 pairs, 7 = key outliers with m <= 8 pairs.
+   Returns 0 for a plane the format does not store. */
 size_t kvq_tile_bytes(int32_t fmt, int32_t plane);
 
 /* sizeof of the ABI structs as this library was compiled: which 0 = kvq_cache,

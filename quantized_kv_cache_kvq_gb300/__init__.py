@@ -81,6 +81,10 @@ class _Cache(ctypes.Structure):
         ("v_scale", c_void_p),
         ("witness", c_void_p),
         ("v_witness", c_void_p),
+        ("outlier_pairs", c_void_p),
+        ("n_outlier_pairs", c_int32),
+        ("reserved2", c_int32),
+        ("k_outlier", c_void_p),
     ]
 
 
@@ -181,7 +185,8 @@ class PagedCache:
     """One layer's paged planes (device memory owned by torch tensors)."""
 
     def __init__(self, k_fmt: str, v_fmt: str, num_kv_heads: int, num_pages: int, layer: int = 0,
-                 seed: int = 0, device="cuda", witness: bool = True, value_witness: bool = False):
+                 seed: int = 0, device="cuda", witness: bool = True, value_witness: bool = False,
+                 outlier_pairs: torch.Tensor | None = None):
         self.k_fmt, self.v_fmt = k_fmt, v_fmt
         self.num_kv_heads, self.num_pages, self.layer, self.seed = num_kv_heads, num_pages, layer, seed
         n = num_pages * num_kv_heads
@@ -194,15 +199,24 @@ class PagedCache:
         self.v_scale = torch.zeros((n, 32), **z) if v_fmt in ("e4m3s", "int8") else None
         self.witness = torch.zeros((n, 512), **z) if witness else None
         self.v_witness = torch.zeros((n, 64), **z) if value_witness else None
+        # fixed-channel key outlier bypass: [num_kv_heads, m] int32 RoPE pairs (INT8-dithered keys)
+        self.n_out = 0 if outlier_pairs is None else int(outlier_pairs.shape[1])
+        self.outlier_pairs = None
+        self.k_outlier = None
+        if self.n_out:
+            assert outlier_pairs.shape[0] == num_kv_heads and outlier_pairs.dtype == torch.int32
+            self.outlier_pairs = outlier_pairs.to(device).contiguous()
+            self.k_outlier = torch.zeros((n, 256 if self.n_out <= 4 else 512), **z)
 
     def desc(self) -> _Cache:
         return _Cache(FMT[self.k_fmt], FMT[self.v_fmt], self.num_kv_heads, self.num_pages, self.layer, 0,
                       self.seed & 0xFFFFFFFFFFFFFFFF, _ptr(self.k), _ptr(self.v), _ptr(self.k_scale),
-                      _ptr(self.v_scale), _ptr(self.witness), _ptr(self.v_witness))
+                      _ptr(self.v_scale), _ptr(self.witness), _ptr(self.v_witness), _ptr(self.outlier_pairs),
+                      self.n_out, 0, _ptr(self.k_outlier))
 
     def nbytes(self) -> int:
-        return sum(t.numel() for t in (self.k, self.v, self.k_scale, self.v_scale, self.witness, self.v_witness)
-                   if t is not None)
+        return sum(t.numel() for t in (self.k, self.v, self.k_scale, self.v_scale, self.witness, self.v_witness,
+                                       self.k_outlier) if t is not None)
 
 
 def read_err(err: torch.Tensor) -> int:

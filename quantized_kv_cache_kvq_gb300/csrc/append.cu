@@ -33,7 +33,9 @@ __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __
   float k[4], v[4];
   load_row4(kin, vin, in_bf16, static_cast<size_t>(row) * kHeadDim + lane * 4, k, v);
   const RowCodes rc = quantize_row<KF, VF>(k, v, static_cast<uint32_t>(slot), static_cast<uint32_t>(c.layer),
-                                           static_cast<uint32_t>(head), c.dither_seed, c.v_witness != nullptr);
+                                           static_cast<uint32_t>(head), c.dither_seed, c.v_witness != nullptr,
+                                           c.n_outlier_pairs > 0 ? c.outlier_pairs + head * c.n_outlier_pairs : nullptr,
+                                           c.n_outlier_pairs);
   const size_t tile = static_cast<size_t>(page) * H + head;
   const size_t stile = static_cast<size_t>(head) * c.num_pages + page;  // scale planes are head-major
   store_row<KF, VF>(rc, t, static_cast<uint8_t*>(c.k_data) + tile * tile_bytes_k(KF),
@@ -41,7 +43,11 @@ __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __
                     fmt_has_scale(KF) ? reinterpret_cast<uint8_t*>(c.k_scale) + stile * kTileBytesS : nullptr,
                     fmt_has_scale(VF) ? reinterpret_cast<uint8_t*>(c.v_scale) + stile * kTileBytesS : nullptr,
                     reinterpret_cast<uint8_t*>(c.witness) + tile * kTileBytesW,
-                    c.v_witness ? reinterpret_cast<uint8_t*>(c.v_witness) + stile * kTileBytesVW : nullptr);
+                    c.v_witness ? reinterpret_cast<uint8_t*>(c.v_witness) + stile * kTileBytesVW : nullptr,
+                    c.n_outlier_pairs > 0
+                        ? reinterpret_cast<uint8_t*>(c.k_outlier) + stile * outlier_tile_bytes(c.n_outlier_pairs)
+                        : nullptr,
+                    c.n_outlier_pairs > 4);
   if (lane == 0) report_row(rc, err);
 }
 
@@ -78,7 +84,9 @@ __global__ void __launch_bounds__(256) append_newest_kernel(kvq_cache c, const v
   float k[4], v[4];
   load_row4(kin, vin, in_bf16, static_cast<size_t>(row) * kHeadDim + lane * 4, k, v);
   const RowCodes rc = quantize_row<KF, VF>(k, v, static_cast<uint32_t>(slot), static_cast<uint32_t>(c.layer),
-                                           static_cast<uint32_t>(head), c.dither_seed, c.v_witness != nullptr);
+                                           static_cast<uint32_t>(head), c.dither_seed, c.v_witness != nullptr,
+                                           c.n_outlier_pairs > 0 ? c.outlier_pairs + head * c.n_outlier_pairs : nullptr,
+                                           c.n_outlier_pairs);
   const size_t tile = static_cast<size_t>(page) * H + head;
   const size_t stile = static_cast<size_t>(head) * c.num_pages + page;
   store_row<KF, VF>(rc, t, static_cast<uint8_t*>(c.k_data) + tile * tile_bytes_k(KF),
@@ -86,7 +94,11 @@ __global__ void __launch_bounds__(256) append_newest_kernel(kvq_cache c, const v
                     fmt_has_scale(KF) ? reinterpret_cast<uint8_t*>(c.k_scale) + stile * kTileBytesS : nullptr,
                     fmt_has_scale(VF) ? reinterpret_cast<uint8_t*>(c.v_scale) + stile * kTileBytesS : nullptr,
                     reinterpret_cast<uint8_t*>(c.witness) + tile * kTileBytesW,
-                    c.v_witness ? reinterpret_cast<uint8_t*>(c.v_witness) + stile * kTileBytesVW : nullptr);
+                    c.v_witness ? reinterpret_cast<uint8_t*>(c.v_witness) + stile * kTileBytesVW : nullptr,
+                    c.n_outlier_pairs > 0
+                        ? reinterpret_cast<uint8_t*>(c.k_outlier) + stile * outlier_tile_bytes(c.n_outlier_pairs)
+                        : nullptr,
+                    c.n_outlier_pairs > 4);
   if (lane == 0) report_row(rc, err);
 }
 
@@ -171,6 +183,8 @@ extern "C" size_t kvq_tile_bytes(int32_t fmt, int32_t plane) {
     case 3: return fmt_has_scale(fmt) ? static_cast<size_t>(kTileBytesS) : 0;
     case 4: return static_cast<size_t>(kTileBytesW);
     case 5: return static_cast<size_t>(kTileBytesVW);
+    case 6: return fmt == KVQ_FMT_INT8_DITHER ? static_cast<size_t>(outlier_tile_bytes(4)) : 0;
+    case 7: return fmt == KVQ_FMT_INT8_DITHER ? static_cast<size_t>(outlier_tile_bytes(8)) : 0;
   }
   return 0;
 }
@@ -196,6 +210,11 @@ extern "C" kvq_status kvq_append(const kvq_cache* c, const void* k, const void* 
   if (fmt_has_scale(c->k_fmt) && (!c->k_scale || !aligned16(c->k_scale))) return KVQ_ERR_INVALID_ARG;
   if (fmt_has_scale(c->v_fmt) && (!c->v_scale || !aligned16(c->v_scale))) return KVQ_ERR_INVALID_ARG;
   if (c->v_witness && !aligned16(c->v_witness)) return KVQ_ERR_INVALID_ARG;
+  if (c->n_outlier_pairs < 0 || c->n_outlier_pairs > kMaxOutlierPairs || c->reserved2 != 0) return KVQ_ERR_INVALID_ARG;
+  if (c->n_outlier_pairs > 0) {
+    if (c->k_fmt != KVQ_FMT_INT8_DITHER) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+    if (!c->outlier_pairs || !c->k_outlier || !aligned16(c->k_outlier)) return KVQ_ERR_INVALID_ARG;
+  }
   const int in_bf16 = in_dtype == KVQ_DTYPE_BF16;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;

@@ -8,6 +8,7 @@
 #define KVQ_X(KF, VF, PKF, PVF, NW) KVQ_DECODE_EXTERNS(KF, VF, PKF, PVF, NW)
 #include "decode_instances.inc"
 #undef KVQ_X
+KVQ_DECODE_EXTERNS3(KVQ_FMT_INT8_DITHER, KVQ_FMT_INT8_DITHER, -1, -1, 12, true)
 
 namespace kvq {
 cudaError_t launch_append_newest(const kvq_cache& c, const void* k, const void* v, int in_bf16,
@@ -216,10 +217,12 @@ WsLayout ws_layout(int batch, int hkv, int hq, int w_max) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Stage bytes of a page: Layout<kf, vf, meter>::total with the value side on, ::unvalued without it.
-int page_bytes(int kf, int vf, bool meter, bool value) {
+// Stage bytes of a page: the Layout<kf, vf, meter, outl> bytes up to the value witness, plus the value
+// witness tile with the value side on.
+int page_bytes(int kf, int vf, bool meter, bool value, bool outl = false) {
   return tile_bytes_k(kf) + tile_bytes_v(vf) + (meter ? kTileBytesW : 0) + (value ? kTileBytesVW : 0) +
-         (fmt_has_scale(kf) ? kTileBytesS : 0) + (fmt_has_scale(vf) ? kTileBytesS : 0);
+         (fmt_has_scale(kf) ? kTileBytesS : 0) + (fmt_has_scale(vf) ? kTileBytesS : 0) +
+         (outl ? outlier_tile_bytes(kMaxOutlierPairs) : 0);
 }
 
 kvq_status check_cache(const kvq_cache* c, bool meter) {
@@ -230,6 +233,11 @@ kvq_status check_cache(const kvq_cache* c, bool meter) {
   if (fmt_has_scale(c->k_fmt) && (!c->k_scale || !aligned16(c->k_scale))) return KVQ_ERR_INVALID_ARG;
   if (fmt_has_scale(c->v_fmt) && (!c->v_scale || !aligned16(c->v_scale))) return KVQ_ERR_INVALID_ARG;
   if (meter && (!c->witness || !aligned16(c->witness))) return KVQ_ERR_INVALID_ARG;
+  if (c->n_outlier_pairs < 0 || c->n_outlier_pairs > kMaxOutlierPairs || c->reserved2 != 0) return KVQ_ERR_INVALID_ARG;
+  if (c->n_outlier_pairs > 0) {
+    if (c->k_fmt != KVQ_FMT_INT8_DITHER) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+    if (!c->outlier_pairs || !c->k_outlier || !aligned16(c->k_outlier)) return KVQ_ERR_INVALID_ARG;
+  }
   return KVQ_OK;
 }
 
@@ -242,6 +250,9 @@ Planes planes_of(const kvq_cache* c) {
   p.vs = reinterpret_cast<const uint8_t*>(c->v_scale);
   p.w = reinterpret_cast<const uint8_t*>(c->witness);
   p.vw = reinterpret_cast<const uint8_t*>(c->v_witness);
+  p.ko = reinterpret_cast<const uint8_t*>(c->k_outlier);
+  p.opairs = c->outlier_pairs;
+  p.n_out = c->n_outlier_pairs;
   p.num_pages = c->num_pages;
   p.layer = static_cast<uint32_t>(c->layer);
   p.seed_lo = static_cast<uint32_t>(c->dither_seed);
@@ -260,12 +271,20 @@ struct Pick {
   int warps;
 };
 
-Pick pick(int kf, int vf, int pkf, int pvf, bool meter, bool value) {
+Pick pick(int kf, int vf, int pkf, int pvf, bool meter, bool value, bool outl) {
+  if (outl) {  // the fixed-channel key outlier bypass exists for the INT8-dithered layout without a prefix
+    constexpr int I8 = KVQ_FMT_INT8_DITHER;
+    if (kf != I8 || vf != I8 || pkf != kNoPrefix || pvf != kNoPrefix) return Pick{nullptr, 0};
+    return Pick{!meter  ? &launch_decode<I8, I8, -1, -1, 12, false, false, true>
+                : value ? &launch_decode<I8, I8, -1, -1, 12, true, true, true>
+                        : &launch_decode<I8, I8, -1, -1, 12, true, false, true>,
+                12};
+  }
 #define KVQ_X(KF, VF, PKF, PVF, NW)                                                                       \
   if (kf == (KF) && vf == (VF) && pkf == (PKF) && pvf == (PVF))                                           \
-    return Pick{!meter  ? &launch_decode<KF, VF, PKF, PVF, NW, false, false>                               \
-                : value ? &launch_decode<KF, VF, PKF, PVF, NW, true, true>                                 \
-                        : &launch_decode<KF, VF, PKF, PVF, NW, true, false>,                               \
+    return Pick{!meter  ? &launch_decode<KF, VF, PKF, PVF, NW, false, false, false>                        \
+                : value ? &launch_decode<KF, VF, PKF, PVF, NW, true, true, false>                          \
+                        : &launch_decode<KF, VF, PKF, PVF, NW, true, false, false>,                        \
                 NW};
 #include "decode_instances.inc"
 #undef KVQ_X
@@ -339,7 +358,9 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   const bool has_prefix = prefix && prefix_len > 0;
   const int pkf = has_prefix ? prefix->k_fmt : kNoPrefix;
   const int pvf = has_prefix ? prefix->v_fmt : kNoPrefix;
-  const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter, meter && (mp->tiers & (KVQ_TIER_V | KVQ_TIER_S)));
+  const bool outl = cache->n_outlier_pairs > 0;
+  const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter, meter && (mp->tiers & (KVQ_TIER_V | KVQ_TIER_S)),
+                       outl);
   if (!pk.launch) return KVQ_ERR_UNSUPPORTED_LAYOUT;
   const int nw = pk.warps;
   const int w_max = sms * nw;
@@ -378,7 +399,7 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   a.err = err_word;
 
   // stage size: the larger of the two segments' page footprints (16-byte multiple by construction)
-  int sb = page_bytes(cache->k_fmt, cache->v_fmt, meter, a.value_on);
+  int sb = page_bytes(cache->k_fmt, cache->v_fmt, meter, a.value_on, outl);
   if (has_prefix) sb = std::max(sb, page_bytes(prefix->k_fmt, prefix->v_fmt, meter, a.value_on));
   const bool xi = cache->k_fmt == KVQ_FMT_INT8_DITHER && cache->v_fmt == KVQ_FMT_INT8_DITHER;
   const int cum_bytes = ((batch + 1) * 4 + 127) & ~127;

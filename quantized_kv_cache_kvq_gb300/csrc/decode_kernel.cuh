@@ -52,6 +52,9 @@ struct Planes {
   const uint8_t* vs;
   const uint8_t* w;
   const uint8_t* vw;  // value witness plane (head-major) or nullptr
+  const uint8_t* ko;  // key outlier plane (head-major) or nullptr
+  const int32_t* opairs;  // [Hkv][n_out] bypassed RoPE pairs
+  int n_out;          // bypassed pairs per head (0: none)
   int num_pages;
   uint32_t layer;
   uint32_t seed_lo, seed_hi;
@@ -85,7 +88,8 @@ struct Args {
   int32_t* err;
 };
 
-template <int KF, int VF, bool METER>
+// OUTL: the stage has room for a key outlier tile (fixed-channel bypass), 512 bytes reserved.
+template <int KF, int VF, bool METER, bool OUTL = false>
 struct Layout {
   static constexpr int kBytes = tile_bytes_k(KF);
   static constexpr int vBytes = tile_bytes_v(VF);
@@ -94,9 +98,10 @@ struct Layout {
   static constexpr int wOff = kBytes + vBytes;
   static constexpr int ksOff = wOff + (METER ? kTileBytesW : 0);
   static constexpr int vsOff = ksOff + (fmt_has_scale(KF) ? kTileBytesS : 0);
+  static constexpr int koOff = vsOff + (fmt_has_scale(VF) ? kTileBytesS : 0);
   // the value witness tile follows; it is copied (and the stage sized for it) only with the value
   // side on, so stages without it keep their size
-  static constexpr int vwOff = vsOff + (fmt_has_scale(VF) ? kTileBytesS : 0);
+  static constexpr int vwOff = koOff + (OUTL ? outlier_tile_bytes(kMaxOutlierPairs) : 0);
   static constexpr int total = vwOff + (METER ? kTileBytesVW : 0);
   static constexpr int unvalued = vwOff;  // bytes copied when the value side is off
 };
@@ -270,6 +275,17 @@ __device__ __forceinline__ void mma_f16_4(float (&d)[4], uint32_t a0, uint32_t a
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// m16n8k8 (fp16 inputs, fp32 accumulate): the key-outlier product of up to 8 bypassed channels
+__device__ __forceinline__ void mma_f16_k8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(b0));
+}
+// sum of squares of an fp16 pair, rounded up
+__device__ __forceinline__ float sq2_ru(uint32_t h2, float acc) {
+  const float2 v = unpack_f16(h2);
+  return __fmaf_ru(v.y, v.y, __fmaf_ru(v.x, v.x, acc));
+}
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
@@ -308,6 +324,10 @@ struct QFrag {
   bool has_lo;
   float cm_scale;    // c_t = cm_scale * (W . QN)  (natural units)
   float alpha_b[2];  // Tier B: u_t = alpha_b[h] * s_t for heads 2c, 2c+1 (natural units)
+  // fixed-channel outlier bypass: B fragment of the bypassed channels (head g; fp16 hi / lo), and the
+  // Tier B terms of heads 2c, 2c+1: u_t += beta_o[h] ||k_hat_{t,O}|| + gamma_o[h]
+  uint32_t qo_hi[2], qo_lo[2];
+  float beta_o[2], gamma_o[2];
 };
 
 struct SoftState {
@@ -336,12 +356,33 @@ __device__ __forceinline__ void reset_state(SoftState& s) {
 // K16 family, k-step kb = 2j + s: b0 <- channels 32j + 8c + 4s + {0,1}, b1 <- + {2,3};
 // K8 family, kb = 4jj + s: channels 64jj + 16c + 4s + {0,1} / {2,3}.  Band norms: b0 <- bands 4c, 4c+1,
 // b1 <- 4c+2, 4c+3 (the witness tile's word order).
-template <bool K16, bool METER>
+// OUTL: the live cache bypasses a fixed set of key channels (INT8 keys): those channels are zeroed in
+// the INT8 fragments, gathered into qo_hi / qo_lo (column 2i <- channel pairs[i], 2i + 1 <- pairs[i] + 64;
+// B fragment of m16n8k8, or m16n8k16 when m > 4), and Tier B splits ||q|| into the INT8 part (alpha_b)
+// and the bypassed part (beta_o, gamma_o: the deterministic bound of the fp16 rounding).
+template <bool K16, bool METER, bool OUTL = false>
 __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const bool real = g < a.G;
   const int qh = kvh * a.G + (real ? g : 0);
   const size_t qbase = (static_cast<size_t>(seq) * a.Hq + qh) * kHeadDim;
+  // bypassed channels among this lane's channels 64 jj + 16 c + (0..15): bit e of omask[jj]
+  uint32_t omask[2] = {0u, 0u};
+  const int m_out = OUTL ? a.live.n_out : 0;
+  const int32_t* pairs = OUTL ? a.live.opairs + static_cast<size_t>(kvh) * m_out : nullptr;
+  if (OUTL) {
+    for (int i = 0; i < m_out; ++i) {
+      const int j = pairs[i];
+      if (j < 0 || j >= kHeadDim / 2) continue;  // reported by the append
+      if ((j >> 4) == c) omask[0] |= 1u << (j & 15);        // channel j < 64: jj = 0
+      if (((j >> 4) & 3) == c) omask[1] |= 1u << (j & 15);  // channel j + 64: jj = 1, same 16-block
+    }
+  }
+  auto q_at = [&](int ch) -> float {  // one channel of this lane's head
+    if (!real) return 0.f;
+    return a.q_bf16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(a.q)[qbase + ch]) << 16)
+                    : static_cast<const float*>(a.q)[qbase + ch];
+  };
   // 8 consecutive channels of this lane's head (ch % 8 == 0): one 16-byte (bf16) or two (fp32) loads
   auto load8 = [&](int ch, float (&v)[8]) {
     if (!real) {
@@ -399,6 +440,13 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
       float v0[8], v1[8];
       load8(64 * jj + 16 * c, v0);
       load8(64 * jj + 16 * c + 8, v1);
+      if (OUTL) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if ((omask[jj] >> e) & 1u) v0[e] = 0.f;
+          if ((omask[jj] >> (8 + e)) & 1u) v1[e] = 0.f;
+        }
+      }
       put(4 * jj, v0);
       put(4 * jj + 1, v0 + 4);
       put(4 * jj + 2, v1);
@@ -415,19 +463,25 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     load8(64 + 16 * c, w0);
     load8(64 + 16 * c + 8, w1);
     float qn[4];
-    float sq_all = 0.f;
+    float sq_all = 0.f, sq_int8 = 0.f;  // ||q||^2 and, with the bypass, its INT8-channel part
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float* u = (i < 2) ? (u0 + 4 * i) : (u1 + 4 * (i - 2));
       const float* w = (i < 2) ? (w0 + 4 * i) : (w1 + 4 * (i - 2));
-      float s = 0.f;
+      float s = 0.f, s8 = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         s = __fmaf_rn(u[e], u[e], s);
         s = __fmaf_rn(w[e], w[e], s);
+        if (OUTL) {
+          const int bit = 4 * i + e;  // channel 16c + bit (u) and 64 + 16c + bit (w)
+          if (!((omask[0] >> bit) & 1u)) s8 = __fmaf_rn(u[e], u[e], s8);
+          if (!((omask[1] >> bit) & 1u)) s8 = __fmaf_rn(w[e], w[e], s8);
+        }
       }
       qn[i] = sqrtf(s);
       sq_all += s;
+      sq_int8 += s8;
     }
     // one power-of-two normalisation for the unit (max over heads and bands < 2), hi/lo fp16 split
     float mx = fmaxf(fmaxf(qn[0], qn[1]), fmaxf(qn[2], qn[3]));
@@ -449,11 +503,43 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     f.qn_lo[1] = pack_f16(lv[2], lv[3]);
     f.cm_scale = a.sm_scale * ldexpf(1.f, e2);
     // ||q_g|| lives on the lanes of row g; the C fragment needs heads 2c and 2c+1
-    const float qnorm_g = sqrtf(row_sum4(sq_all));
+    // the dither term uses the query on the INT8 channels only (the bypassed ones leave the variance)
+    const float qnorm_g = sqrtf(row_sum4(OUTL ? sq_int8 : sq_all));
     const float kappa = sqrtf(2.f * (logf(2.f * static_cast<float>(seq_total)) - a.ln_delta_loc) / 12.f);
     const float q0 = __shfl_sync(kFull, qnorm_g, 8 * c), q1 = __shfl_sync(kFull, qnorm_g, 8 * c + 4);
     f.alpha_b[0] = a.sm_scale * q0 * kappa;
     f.alpha_b[1] = a.sm_scale * q1 * kappa;
+  }
+  if (OUTL) {
+    // bypassed channels: B fragment columns 2c, 2c + 1 (pair c) and, when m > 4, 2c + 8, 2c + 9 (pair c + 4)
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int i = c + 4 * k2;
+      if (i < m_out) {
+        const int j = pairs[i];
+        if (j >= 0 && j < kHeadDim / 2) { x[2 * k2] = q_at(j); x[2 * k2 + 1] = q_at(j + kHeadDim / 2); }
+      }
+    }
+    f.qo_hi[0] = pack_f16(x[0], x[1]);
+    f.qo_hi[1] = pack_f16(x[2], x[3]);
+    const float2 r0 = unpack_f16(f.qo_hi[0]), r1 = unpack_f16(f.qo_hi[1]);
+    f.qo_lo[0] = pack_f16(x[0] - r0.x, x[1] - r0.y);
+    f.qo_lo[1] = pack_f16(x[2] - r1.x, x[3] - r1.y);
+    // ||q_O|| of head g (rounded up), for the deterministic fp16 term of Tier B:
+    // |q_O . r_O| <= ||q_O|| (2^-11 ||k_hat_O|| + sqrt(2m) 2^-25)
+    float so = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) so = __fmaf_ru(x[e], x[e], so);
+    so = __fadd_ru(so, __shfl_xor_sync(kFull, so, 1));
+    so = __fadd_ru(so, __shfl_xor_sync(kFull, so, 2));
+    const float qo_g = __fsqrt_ru(so);
+    const float o0 = __shfl_sync(kFull, qo_g, 8 * c), o1 = __shfl_sync(kFull, qo_g, 8 * c + 4);
+    const float rt = sqrtf(2.f * static_cast<float>(m_out)) * 1.0000001f;
+    f.beta_o[0] = a.sm_scale * o0 * 0x1p-11f;
+    f.beta_o[1] = a.sm_scale * o1 * 0x1p-11f;
+    f.gamma_o[0] = a.sm_scale * o0 * rt * 0x1p-25f;
+    f.gamma_o[1] = a.sm_scale * o1 * rt * 0x1p-25f;
   }
 }
 
@@ -497,11 +583,11 @@ __device__ __forceinline__ void accumulate_meter(const float (&r)[4], const floa
 // Tokens past the end of the sequence (a partial last page) have had their K, V, witness and scale
 // bytes zeroed in the stage; `xb0` / `xb1` are 0 for valid tokens g / g + 8 and -inf otherwise, added
 // to the logits, so no per-element masking is needed here.
-template <int KF, int VF, bool METER>
+template <int KF, int VF, bool METER, bool OUTL = false>
 __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile, float xb0, float xb1, uint32_t phys,
                                              const Planes& pl, int kvh, const QFrag& f, SoftState& s,
                                              float qk_scale, bool tier_b, float* vstate, int ext) {
-  using L = Layout<KF, VF, METER>;
+  using L = Layout<KF, VF, METER, OUTL>;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   constexpr bool K16 = fmt_is_16bit(KF);
   constexpr bool KDITHER = KF == KVQ_FMT_INT8_DITHER;
@@ -570,6 +656,35 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     }
   }
 
+  // ---------------- bypassed key channels (fixed-channel outlier bypass, WitCert Sec. 6.2.5): fp16 values
+  // times the query's bypassed channels; kon = ||k_hat_O|| of tokens g and g + 8 (Tier B, rounded up)
+  float So[4] = {0.f, 0.f, 0.f, 0.f};
+  float kon[2] = {0.f, 0.f};
+  if (OUTL) {
+    float s0 = 0.f, s1 = 0.f;
+    if (pl.n_out > 4) {
+      const uint4 ko = lds128(st + L::koOff + lane * 16);
+      mma_f16_4(So, ko.x, ko.y, ko.z, ko.w, f.qo_hi[0], f.qo_hi[1]);
+      if (f.has_lo) mma_f16_4(So, ko.x, ko.y, ko.z, ko.w, f.qo_lo[0], f.qo_lo[1]);
+      s0 = sq2_ru(ko.z, sq2_ru(ko.x, 0.f));
+      s1 = sq2_ru(ko.w, sq2_ru(ko.y, 0.f));
+    } else {
+      const uint2 ko = lds64(st + L::koOff + lane * 8);
+      mma_f16_k8(So, ko.x, ko.y, f.qo_hi[0]);
+      if (f.has_lo) mma_f16_k8(So, ko.x, ko.y, f.qo_lo[0]);
+      s0 = sq2_ru(ko.x, 0.f);
+      s1 = sq2_ru(ko.y, 0.f);
+    }
+    if (METER && tier_b) {
+      s0 = __fadd_ru(s0, __shfl_xor_sync(kFull, s0, 1));
+      s0 = __fadd_ru(s0, __shfl_xor_sync(kFull, s0, 2));
+      s1 = __fadd_ru(s1, __shfl_xor_sync(kFull, s1, 1));
+      s1 = __fadd_ru(s1, __shfl_xor_sync(kFull, s1, 2));
+      kon[0] = __fsqrt_ru(s0);
+      kon[1] = __fsqrt_ru(s1);
+    }
+  }
+
   // ---------------- per-token scales of tokens g and g + 8
   float sk[2] = {1.f, 1.f}, sv[2] = {1.f, 1.f};
   if (fmt_has_scale(KF)) {
@@ -587,7 +702,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const float sc = fmt_has_scale(KF) ? qk_scale * sk[v >> 1] : qk_scale;
-    x[v] = __fmaf_rn(S[v], sc, xb[v >> 1]);
+    x[v] = __fmaf_rn(S[v], sc, OUTL ? __fmaf_rn(So[v], qk_scale, xb[v >> 1]) : xb[v >> 1]);
   }
   float alpha[2], mnew[2];
 #pragma unroll
@@ -640,7 +755,10 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     if (KDITHER && tier_b) {
       float uv[4];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) uv[v] = f.alpha_b[v & 1] * sk[v >> 1];
+      for (int v = 0; v < 4; ++v) {
+        uv[v] = f.alpha_b[v & 1] * sk[v >> 1];
+        if (OUTL) uv[v] = __fmaf_ru(f.beta_o[v & 1], kon[v >> 1], uv[v]) + f.gamma_o[v & 1];
+      }
       accumulate_meter(uv, x, p, alpha, mnew, s.mu, s.su, s.slow_b);
     }
   }
@@ -752,7 +870,7 @@ __device__ __forceinline__ Desc make_desc(const Args& a, const int32_t* cum, lon
   return d;
 }
 
-template <int KF, int VF, int PKF, int PVF, bool METER, bool VALUE>
+template <int KF, int VF, int PKF, int PVF, bool METER, bool VALUE, bool OUTL>
 __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64_t* bar, Desc d) {
   // lane 0 only
   if (d.phys < 0) {
@@ -774,14 +892,15 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     if (fmt_has_scale(pv)) bulk_g2s(stage + L::vsOff, a.pre.vs + stile * kTileBytesS, kTileBytesS, bar);
     if (METER && VALUE && a.value_on) bulk_g2s(stage + L::vwOff, a.pre.vw + stile * kTileBytesVW, kTileBytesVW, bar);
   } else {
-    using L = Layout<KF, VF, METER>;
+    using L = Layout<KF, VF, METER, OUTL>;
     const size_t tile = static_cast<size_t>(d.phys) * a.Hkv + kvh;
     if (a.wait_append && d_last(d.info)) {
       // the page holding the sequence's newest token: the append grid must have completed
       asm volatile("griddepcontrol.wait;" ::: "memory");
       asm volatile("fence.proxy.async.global;" ::: "memory");
     }
-    mbar_arrive_expect_tx(bar, VALUE && a.value_on ? L::total : L::unvalued);
+    const int ko_bytes = OUTL ? outlier_tile_bytes(a.live.n_out) : 0;
+    mbar_arrive_expect_tx(bar, L::koOff + ko_bytes + (VALUE && a.value_on ? kTileBytesVW : 0));
     bulk_g2s(stage + L::kOff, a.live.k + tile * L::kBytes, L::kBytes, bar);
     bulk_g2s(stage + L::vOff, a.live.v + tile * L::vBytes, L::vBytes, bar);
     if (METER) bulk_g2s(stage + L::wOff, a.live.w + tile * kTileBytesW, kTileBytesW, bar);
@@ -789,6 +908,7 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     const size_t stile = static_cast<size_t>(kvh) * a.live.num_pages + d.phys;
     if (fmt_has_scale(KF)) bulk_g2s(stage + L::ksOff, a.live.ks + stile * kTileBytesS, kTileBytesS, bar);
     if (fmt_has_scale(VF)) bulk_g2s(stage + L::vsOff, a.live.vs + stile * kTileBytesS, kTileBytesS, bar);
+    if (OUTL) bulk_g2s(stage + L::koOff, a.live.ko + stile * ko_bytes, ko_bytes, bar);
     if (METER && VALUE && a.value_on) bulk_g2s(stage + L::vwOff, a.live.vw + stile * kTileBytesVW, kTileBytesVW, bar);
   }
 }
@@ -843,10 +963,11 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
 // Zero the bytes of tokens nvalid..15 in a stage (a partial last page): the slots past the end of a
 // sequence may hold anything, and zeros make their logit exactly the -inf bias, their value and
 // radius exactly 0.  Runs once per unit at most; all lanes take part.
-// vw_on: the stage holds a value witness tile (only then does the stage have room for it).
-template <int KF, int VF, bool METER, bool VALUE>
-__device__ void zero_tail(uint8_t* st, int nvalid, bool vw_on) {
-  using L = Layout<KF, VF, METER>;
+// vw_on: the stage holds a value witness tile (only then does the stage have room for it); OUTL: a key
+// outlier tile of 8 (ko_wide: 16) columns.
+template <int KF, int VF, bool METER, bool VALUE, bool OUTL = false>
+__device__ void zero_tail(uint8_t* st, int nvalid, bool vw_on, bool ko_wide = false) {
+  using L = Layout<KF, VF, METER, OUTL>;
   const int lane = threadIdx.x & 31;
   const int n = (kPage - nvalid) * kHeadDim;
   for (int e = lane; e < n; e += 32) {
@@ -867,6 +988,9 @@ __device__ void zero_tail(uint8_t* st, int nvalid, bool vw_on) {
       *reinterpret_cast<uint16_t*>(st + L::vwOff + vw_offset(t, 0)) = 0;
       *reinterpret_cast<uint16_t*>(st + L::vwOff + vw_offset(t, 1)) = 0;
     }
+    if (OUTL)
+      for (int col = 0; col < (ko_wide ? 16 : 8); ++col)
+        *reinterpret_cast<uint16_t*>(st + L::koOff + ko_offset(t, col, ko_wide)) = 0;
   }
   __syncwarp();
 }
@@ -874,7 +998,8 @@ __device__ void zero_tail(uint8_t* st, int nvalid, bool vw_on) {
 // VALUE: the extended meter is compiled in (value side of the output bound and alternative bound
 // shapes, chosen at run time; the value witness is staged only when the value side is on); without it
 // no trace of either is left in the kernel.
-template <int KF, int VF, int PKF, int PVF, int NW, bool METER, bool VALUE>
+// OUTL: the live cache stores a fixed set of key channels in fp16 (outlier bypass, INT8 keys).
+template <int KF, int VF, int PKF, int PVF, int NW, bool METER, bool VALUE, bool OUTL>
 __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   // let the merge grid (programmatic dependent launch) be scheduled as soon as SMs free up
@@ -961,7 +1086,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   for (int j = 0; j < a.stages && j < n; ++j) {
     const int32_t ph = __shfl_sync(kFull, cur.phys, j);
     const uint32_t in = __shfl_sync(kFull, cur.info, j);
-    if (lane == 0) issue_page<KF, VF, PKF, PVF, METER, VALUE>(a, wbase + j * a.stage_bytes, &bars[j], Desc{ph, in});
+    if (lane == 0) issue_page<KF, VF, PKF, PVF, METER, VALUE, OUTL>(a, wbase + j * a.stage_bytes, &bars[j], Desc{ph, in});
   }
 
   QFrag f;
@@ -990,7 +1115,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       unit = u;
       const int seq = u / a.Hkv, kvh = u % a.Hkv;
       const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
-      load_q<K16, METER>(a, seq, kvh, total, f);
+      load_q<K16, METER, OUTL>(a, seq, kvh, total, f);
     }
     // every lane polls; the verdict is made warp-uniform before anyone leaves the loop
     if (!__all_sync(kFull, mbar_wait(&bars[stage], parity))) { ok = false; timeout_at = j; break; }
@@ -1005,8 +1130,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
         process_page<pk, pv, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.pre, kvh, f, s,
                                     qk_scale, a.tier_b != 0, vstate, ext);
       } else {
-        if (nvalid < kPage) zero_tail<KF, VF, METER, VALUE>(st, nvalid, a.value_on != 0);
-        process_page<KF, VF, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f, s,
+        if (nvalid < kPage) zero_tail<KF, VF, METER, VALUE, OUTL>(st, nvalid, a.value_on != 0, a.live.n_out > 4);
+        process_page<KF, VF, METER, OUTL>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f, s,
                                     qk_scale, a.tier_b != 0, vstate, ext);
       }
     }
@@ -1018,7 +1143,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       const uint32_t ic = __shfl_sync(kFull, cur.info, jn & 31), inx = __shfl_sync(kFull, nxt.info, jn & 31);
       if (lane == 0) {
         fence_proxy_async();
-        issue_page<KF, VF, PKF, PVF, METER, VALUE>(a, st, &bars[stage], in_cur ? Desc{pc, ic} : Desc{pn, inx});
+        issue_page<KF, VF, PKF, PVF, METER, VALUE, OUTL>(a, st, &bars[stage], in_cur ? Desc{pc, ic} : Desc{pn, inx});
       }
     }
     if (++stage == a.stages) { stage = 0; parity ^= 1u; }
@@ -1043,9 +1168,9 @@ namespace dec {
 // Host launcher of one instantiation (the dynamic shared-memory limit is raised once per kernel).
 // `programmatic`: launch as a programmatic dependent of the preceding grid in the stream (the
 // fused append), which the kernel waits for where it reads that grid's output.
-template <int KF, int VF, int PKF, int PVF, int NW, bool METER, bool VALUE>
+template <int KF, int VF, int PKF, int PVF, int NW, bool METER, bool VALUE, bool OUTL>
 cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s, bool programmatic) {
-  auto kern = decode_split_kernel<KF, VF, PKF, PVF, NW, METER, VALUE>;
+  auto kern = decode_split_kernel<KF, VF, PKF, PVF, NW, METER, VALUE, OUTL>;
   static size_t configured = 0;  // largest dynamic smem size set so far
   if (smem > configured) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -1074,16 +1199,18 @@ cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s, 
 
 // Explicit instantiations are listed once, in decode_instances.inc, and split across translation
 // units so they compile in parallel.
-#define KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, M, V)                                                        \
-  template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M, V>(const kvq::dec::Args&, int, size_t, \
-                                                                            cudaStream_t, bool);
-#define KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, M, V)                                                        \
-  extern template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M, V>(const kvq::dec::Args&, int, \
-                                                                                   size_t, cudaStream_t, bool);
-// meter off, meter on, meter with the value side
-#define KVQ_DECODE_INSTANCES(KF, VF, PKF, PVF, NW)                                                    \
-  KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, false, false) KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, true, false) \
-  KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, true, true)
-#define KVQ_DECODE_EXTERNS(KF, VF, PKF, PVF, NW)                                                      \
-  KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, false, false) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, true, false) \
-  KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, true, true)
+#define KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, M, V, O)                                                      \
+  template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M, V, O>(const kvq::dec::Args&, int, size_t, \
+                                                                               cudaStream_t, bool);
+#define KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, M, V, O)                                                      \
+  extern template cudaError_t kvq::dec::launch_decode<KF, VF, PKF, PVF, NW, M, V, O>(const kvq::dec::Args&, int, \
+                                                                                      size_t, cudaStream_t, bool);
+// meter off, meter on, meter with the extended meter (O: with the key outlier bypass)
+#define KVQ_DECODE_INSTANCES3(KF, VF, PKF, PVF, NW, O)                                                     \
+  KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, false, false, O)                                              \
+  KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, true, false, O) KVQ_DECODE_INSTANCE(KF, VF, PKF, PVF, NW, true, true, O)
+#define KVQ_DECODE_EXTERNS3(KF, VF, PKF, PVF, NW, O)                                                       \
+  KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, false, false, O)                                                \
+  KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, true, false, O) KVQ_DECODE_EXTERN(KF, VF, PKF, PVF, NW, true, true, O)
+#define KVQ_DECODE_INSTANCES(KF, VF, PKF, PVF, NW) KVQ_DECODE_INSTANCES3(KF, VF, PKF, PVF, NW, false)
+#define KVQ_DECODE_EXTERNS(KF, VF, PKF, PVF, NW) KVQ_DECODE_EXTERNS3(KF, VF, PKF, PVF, NW, false)

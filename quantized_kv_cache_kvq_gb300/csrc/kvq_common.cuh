@@ -32,6 +32,9 @@ __host__ __device__ constexpr int tile_bytes_v(int f) { return fmt_is_16bit(f) ?
 constexpr int kTileBytesW = 512;
 constexpr int kTileBytesS = 32;
 constexpr int kTileBytesVW = 64;  // value witness: (rho^v, ||v||) per token
+constexpr int kMaxOutlierPairs = 8;
+// key outlier tile: 16 tokens x 8 fp16 columns (m <= 4) or x 16 (m <= 8), tensor-core A-fragment order
+__host__ __device__ constexpr int outlier_tile_bytes(int m) { return m <= 0 ? 0 : (m <= 4 ? 256 : 512); }
 
 // ---------------------------------------------------------------------------------------------
 // Tile layouts (byte offsets inside one (page, kv head) tile; see include/kvq.h).
@@ -56,6 +59,11 @@ __host__ __device__ __forceinline__ int w_offset(int t, int b) {
   return 16 * (4 * (t & 7) + (b >> 2)) + 8 * (t >> 3) + 2 * (b & 3);
 }
 __host__ __device__ __forceinline__ int s_offset(int t) { return 2 * (2 * (t & 7) + (t >> 3)); }
+// key outlier column col of token t (m16n8k8 A fragment for m <= 4, m16n8k16 for m <= 8)
+__host__ __device__ __forceinline__ int ko_offset(int t, int col, bool wide) {
+  return wide ? 16 * (4 * (t & 7) + ((col & 7) >> 1)) + 8 * (col >> 3) + 4 * (t >> 3) + 2 * (col & 1)
+              : 8 * (4 * (t & 7) + (col >> 1)) + 4 * (t >> 3) + 2 * (col & 1);
+}
 // value witness: k = 0 rho^v, k = 1 ||v||; lane g of the decode reads tokens g and g + 8 as one 8-byte word
 __host__ __device__ __forceinline__ int vw_offset(int t, int k) { return 8 * (t & 7) + 4 * k + 2 * (t >> 3); }
 

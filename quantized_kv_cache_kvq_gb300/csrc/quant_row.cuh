@@ -139,14 +139,19 @@ struct RowCodes {
   uint16_t ks, vs;        // scale bits (formats with a scale)
   uint16_t wb;            // witness bits of band `lane` (lanes 0..15)
   uint16_t vrho, vnorm;   // value witness bits: ||v_hat - v|| and ||v||, rounded up (warp-uniform)
+  uint16_t kob[4];        // fp16 bits of this lane's bypassed key channels ...
+  int8_t kocol[4];        // ... and their outlier columns (-1: not bypassed)
   bool nonfinite;         // non-finite input or scale overflow (warp-uniform)
   bool range;             // value scale above KVQ_MAX_VALUE_SCALE (warp-uniform)
+  bool bad_pair;          // a bypassed pair index outside 0..63 (warp-uniform)
 };
 
-// want_vw: compute the value witness (the cache has a value witness plane).
+// want_vw: compute the value witness (the cache has a value witness plane).  opairs / m: the head's
+// bypassed RoPE pairs (INT8-dithered keys; WitCert Sec. 6.2.5), m = 0 for none.
 template <int KF, int VF>
 __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v[4], uint32_t slot, uint32_t layer,
-                                                 uint32_t head, uint64_t seed, bool want_vw) {
+                                                 uint32_t head, uint64_t seed, bool want_vw,
+                                                 const int32_t* opairs = nullptr, int m = 0) {
   const int lane = threadIdx.x & 31;
   RowCodes rc;
   bool finite = true;
@@ -159,8 +164,25 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
                              static_cast<uint32_t>(seed >> 32));
     xi[0] = d.x; xi[1] = d.y; xi[2] = d.z; xi[3] = d.w;
   }
+  // bypassed channels of this lane: column 2i <- channel pairs[i], column 2i + 1 <- pairs[i] + 64
+  bool bad_pair = false;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) rc.kocol[e] = -1;
+  if (KF == KVQ_FMT_INT8_DITHER) {
+    for (int i = 0; i < m; ++i) {
+      const int j = opairs[i];
+      if (j < 0 || j >= kHeadDim / 2) { bad_pair = true; continue; }
+      if ((j >> 2) == lane) rc.kocol[j & 3] = static_cast<int8_t>(2 * i);
+      if (((j + kHeadDim / 2) >> 2) == lane) rc.kocol[j & 3] = static_cast<int8_t>(2 * i + 1);
+    }
+  }
   float kamax = 0.f, vamax = 0.f;
-  if (fmt_has_scale(KF)) kamax = warp_max(fmaxf(fmaxf(fabsf(k[0]), fabsf(k[1])), fmaxf(fabsf(k[2]), fabsf(k[3]))));
+  if (fmt_has_scale(KF)) {
+    float a = 0.f;  // bypassed channels are left out of the amax
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a = rc.kocol[e] < 0 ? fmaxf(a, fabsf(k[e])) : a;
+    kamax = warp_max(a);
+  }
   if (fmt_has_scale(VF)) vamax = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
   int flags = 0;
   Quantized4 qk, qv;
@@ -168,6 +190,21 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
   rc.vs = 0;
   quantize4<KF, true>(k, kamax, xi, rc.kc, rc.ks, qk, flags);
   quantize4<VF, true>(v, vamax, xi, rc.vc, rc.vs, qv, flags);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    rc.kob[e] = 0;
+    if (rc.kocol[e] >= 0) {  // bypassed: code 0, fp16 value, residual of the fp16 rounding
+      const __half h = __float2half_rn(k[e]);
+      const float hv = __half2float(h);
+      rc.kob[e] = __half_as_ushort(h);
+      rc.kc[e] = 0;
+      qk.hi[e] = __fsub_ru(hv, k[e]);
+      qk.lo[e] = __fsub_rd(hv, k[e]);
+      if (!isfinite(hv)) flags |= 1;
+    }
+  }
+  if (__any_sync(0xffffffffu, (flags & 1) != 0)) flags |= 1;  // an overflowing bypassed channel flags the row
+  if (bad_pair) flags |= 4;
   if (fmt_has_scale(VF) && __half2float(__ushort_as_half(rc.vs)) > KVQ_MAX_VALUE_SCALE) flags |= 2;
   // Witness: upper bound of each band norm.  Lane l holds channels 4l..4l+3, all in band l % 16;
   // lanes l and l + 16 share a band (channels 4b..4b+3 and 64+4b..64+4b+3).
@@ -198,6 +235,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
     rc.vrho = __half_as_ushort(__float2half_ru(__fsqrt_ru(rv)));
     rc.vnorm = __half_as_ushort(__float2half_ru(__fsqrt_ru(vv)));
   }
+  rc.bad_pair = (flags & 4) != 0;
   rc.nonfinite = !finite || (flags & 1);  // flags are warp-uniform: amax and the scales are
   rc.range = (flags & 2) != 0;
   return rc;
@@ -207,7 +245,8 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
 // pointers may be null (plane absent).
 template <int KF, int VF>
 __device__ __forceinline__ void store_row(const RowCodes& rc, int t, uint8_t* ktile, uint8_t* vtile, uint8_t* kstile,
-                                          uint8_t* vstile, uint8_t* wtile, uint8_t* vwtile) {
+                                          uint8_t* vstile, uint8_t* wtile, uint8_t* vwtile, uint8_t* kotile = nullptr,
+                                          bool ko_wide = false) {
   const int lane = threadIdx.x & 31;
   store_k4<KF>(ktile, t, lane * 4, rc.kc);
   store_v4<VF>(vtile, t, lane * 4, rc.vc);
@@ -220,10 +259,16 @@ __device__ __forceinline__ void store_row(const RowCodes& rc, int t, uint8_t* kt
     *reinterpret_cast<uint16_t*>(vwtile + vw_offset(t, 0)) = rc.vrho;
     *reinterpret_cast<uint16_t*>(vwtile + vw_offset(t, 1)) = rc.vnorm;
   }
+  if (kotile) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (rc.kocol[e] >= 0) *reinterpret_cast<uint16_t*>(kotile + ko_offset(t, rc.kocol[e], ko_wide)) = rc.kob[e];
+  }
 }
 
 __device__ __forceinline__ void report_row(const RowCodes& rc, int32_t* err) {
-  if (rc.nonfinite) report(err, KVQ_ERR_NONFINITE_INPUT);
+  if (rc.bad_pair) report(err, KVQ_ERR_DEVICE_BOUNDS);
+  else if (rc.nonfinite) report(err, KVQ_ERR_NONFINITE_INPUT);
   else if (rc.range) report(err, KVQ_ERR_RANGE);
 }
 

@@ -7,8 +7,8 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["k_offsets", "v_offsets", "w_offsets", "s_offsets", "vw_offsets", "unpack_k", "unpack_v", "unpack_w",
-           "unpack_s", "unpack_vw"]
+__all__ = ["k_offsets", "v_offsets", "w_offsets", "s_offsets", "vw_offsets", "ko_offsets", "unpack_k", "unpack_v",
+           "unpack_w", "unpack_s", "unpack_vw", "unpack_ko"]
 
 
 def k_offsets(fmt: str) -> np.ndarray:
@@ -47,6 +47,15 @@ def vw_offsets() -> np.ndarray:
     return 8 * (t & 7) + 4 * k + 2 * (t >> 3)
 
 
+def ko_offsets(m: int) -> np.ndarray:
+    """[16 tokens, 2m] byte offsets in a key outlier tile (8 columns for m <= 4, 16 for m <= 8)."""
+    t = np.arange(16)[:, None]
+    col = np.arange(2 * m)[None, :]
+    if m <= 4:
+        return 8 * (4 * (t & 7) + (col >> 1)) + 4 * (t >> 3) + 2 * (col & 1)
+    return 16 * (4 * (t & 7) + ((col & 7) >> 1)) + 8 * (col >> 3) + 4 * (t >> 3) + 2 * (col & 1)
+
+
 def _gather16(tiles: np.ndarray, offs: np.ndarray) -> np.ndarray:
     u16 = np.ascontiguousarray(tiles).view(np.uint16)
     return u16[..., offs // 2]
@@ -81,3 +90,9 @@ def unpack_vw(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:
     """value-witness plane (head-major tiles) -> fp16 bits [pages, heads, 16 tokens, 2]."""
     tiles = tiles.reshape(num_kv_heads, -1, tiles.shape[-1]).transpose(1, 0, 2)
     return _gather16(tiles, vw_offsets())
+
+
+def unpack_ko(tiles: np.ndarray, num_kv_heads: int, m: int) -> np.ndarray:
+    """key outlier plane (head-major tiles) -> fp16 bits [pages, heads, 16 tokens, 2m] in column order."""
+    tiles = tiles.reshape(num_kv_heads, -1, tiles.shape[-1]).transpose(1, 0, 2)
+    return _gather16(tiles, ko_offsets(m))

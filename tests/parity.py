@@ -16,7 +16,8 @@ import workloads as W
 from oracle import attention as OA
 from oracle.encoders import fp16_value
 from oracle.philox import dither
-from oracle.quant import dequantize, quantize, value_witness_bits, witness_bits
+from oracle.quant import (bypass_channels, dequantize, dequantize_int8_bypass, quantize, quantize_int8_bypass,
+                          value_witness_bits, witness_bits)
 
 SM_SCALE = float(np.float32(1.0 / math.sqrt(128)))
 PREFIX_SEED_UNIT = 777_777
@@ -46,8 +47,9 @@ def make_inputs(w, layer: int = 0):
         pk, pv, _ = W.gen_unit_cpu(w, 0, layer, w.prefix_len, first_pos=0, seed_unit=PREFIX_SEED_UNIT + layer)
         pre = (pk, pv)
     q = np.stack([sq[2] for sq in seqs]) if B else np.zeros((0, w.n_q_heads, 128), np.float32)
+    pairs = W.bypass_pair_table(w, layer) if w.bypass_pairs else None
     return dict(lens=lens, seqs=seqs, bt=bt, num_pages=max(num_pages, 1), prefix=pre, q=q, layer=layer,
-                seed=cache_seed(w, layer), prefix_seed=cache_seed(w, 10_000 + layer))
+                seed=cache_seed(w, layer), prefix_seed=cache_seed(w, 10_000 + layer), pairs=pairs)
 
 
 def _oracle_quant_rows(x32, fmt, xi):
@@ -56,18 +58,33 @@ def _oracle_quant_rows(x32, fmt, xi):
     return codes, sb, xh, valid
 
 
-def oracle_cache_rows(k32, v32, slots, k_fmt, v_fmt, seed, layer, heads=None):
+def oracle_cache_rows(k32, v32, slots, k_fmt, v_fmt, seed, layer, heads=None, pairs=None):
     """Oracle quantization of tokens [n, Hkv, 128] written at ``slots`` [n].
 
-    ``heads``: kv-head index of each column of the inputs (defaults to 0..Hkv-1); it keys the dither."""
+    ``heads``: kv-head index of each column of the inputs (defaults to 0..Hkv-1); it keys the dither.
+    ``pairs``: [Hkv, m] fixed-channel bypass of INT8 keys (per column of the inputs), or None."""
     n, Hkv, _ = k32.shape
     heads = (np.arange(Hkv) if heads is None else np.asarray(heads))[None, :, None]
     xi = dither(seed, layer, heads, np.asarray(slots)[:, None, None], np.arange(128)[None, None, :])
-    kc, ksb, kh, kval = _oracle_quant_rows(k32, k_fmt, xi)
+    kob = None
+    if pairs is not None and np.asarray(pairs).shape[1] > 0:
+        assert k_fmt == "int8"
+        m = np.asarray(pairs).shape[1]
+        kc = np.zeros((n, Hkv, 128), np.int8)
+        ksb = np.zeros((n, Hkv), np.uint16)
+        kh = np.zeros((n, Hkv, 128))
+        kob = np.zeros((n, Hkv, 2 * m), np.uint16)
+        kval = np.ones((n, Hkv), bool)
+        for h in range(Hkv):
+            c_, s_, o_, v_ = quantize_int8_bypass(k32[:, h], xi[:, h], pairs[h])
+            kc[:, h], ksb[:, h], kob[:, h], kval[:, h] = c_, s_, o_, v_
+            kh[:, h] = dequantize_int8_bypass(c_, s_, o_, xi[:, h], pairs[h])
+    else:
+        kc, ksb, kh, kval = _oracle_quant_rows(k32, k_fmt, xi)
     vc, vsb, vh, vval = _oracle_quant_rows(v32, v_fmt, xi)
     w16 = witness_bits(kh, k32)
     vw16 = value_witness_bits(vh, v32)
-    return dict(kc=kc, ksb=ksb, kh=kh, vc=vc, vsb=vsb, vh=vh, w16=w16, vw16=vw16, valid=kval & vval)
+    return dict(kc=kc, ksb=ksb, kh=kh, vc=vc, vsb=vsb, vh=vh, w16=w16, vw16=vw16, kob=kob, valid=kval & vval)
 
 
 def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
@@ -89,7 +106,7 @@ def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
         k32, v32, q = inp["seqs"][s]
         n = k32.shape[0]
         slots = W.slot_mapping(inp["bt"], s, np.arange(n)) if n else np.zeros(0, np.int32)
-        rows = oracle_cache_rows(k32, v32, slots, w.k_fmt, w.v_fmt, inp["seed"], layer)
+        rows = oracle_cache_rows(k32, v32, slots, w.k_fmt, w.v_fmt, inp["seed"], layer, pairs=inp.get("pairs"))
         rows_all.append((slots, rows))
         for g in range(Hkv):
             kk, kh, vh, ww = k32[:, g], rows["kh"][:, g], rows["vh"][:, g], fp16_value(rows["w16"][:, g])
@@ -110,7 +127,10 @@ def reference_case(w, layer: int = 0, inputs=None, tier_b: bool | None = None):
                 continue
             tb = dict(delta_req=w.delta_req, n_layers=w.n_layers, n_q_heads=w.n_q_heads,
                       n_steps=w.n_steps) if tier_b else None
-            r = OA.decode_head(qs, kk, kh, vh, ww, SM_SCALE, s_k=sk, tier_b=tb, vw=vw, v_exact=vv)
+            byp = None
+            if rows["kob"] is not None:
+                byp = dict(channels=bypass_channels(inp["pairs"][g]), values=fp16_value(rows["kob"][:, g]))
+            r = OA.decode_head(qs, kk, kh, vh, ww, SM_SCALE, s_k=sk, tier_b=tb, vw=vw, v_exact=vv, bypass=byp)
             sl = slice(g * G, (g + 1) * G)
             res["out"][s, sl] = r.out
             res["lse"][s, sl] = r.lse
@@ -145,8 +165,10 @@ def run_case_gpu(w, layer: int = 0, inputs=None, meter: bool = True, tier_b: boo
     B, Hkv, Hq = w.batch, w.n_kv_heads, w.n_q_heads
     dev = torch.device(device)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
+    pairs = inp.get("pairs")
     cache = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, inp["num_pages"], layer=layer, seed=inp["seed"], device=dev,
-                           value_witness=value)
+                           value_witness=value,
+                           outlier_pairs=torch.from_numpy(pairs).to(dev) if pairs is not None else None)
     for s in range(B):
         k32, v32, _ = inp["seqs"][s]
         n = k32.shape[0]

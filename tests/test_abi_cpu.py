@@ -56,7 +56,7 @@ def test_host_entry_points(lib):
 def test_struct_sizes_match_c():
     import quantized_kv_cache_kvq_gb300 as kvq
 
-    assert ctypes.sizeof(kvq._Cache) == 6 * 4 + 8 + 6 * 8
+    assert ctypes.sizeof(kvq._Cache) == 6 * 4 + 8 + 6 * 8 + 8 + 2 * 4 + 8
     assert ctypes.sizeof(kvq.MeterParams) == 32
     lib = kvq.load()
     assert lib.kvq_sizeof(0) == ctypes.sizeof(kvq._Cache)  # as the C compiler laid them out
@@ -152,3 +152,23 @@ def test_decode_fragment_reads_are_contiguous_and_conflict_free():
     so = L.s_offsets()
     for gg in range(8):
         assert [so[gg], so[gg + 8]] == [4 * gg, 4 * gg + 2]
+
+
+@pytest.mark.parametrize("m", [4, 8])
+def test_key_outlier_tile_layout(m):
+    """The key outlier tile is a bijection onto its fp16 slots, and lane (g, c) of the decode reads its
+    tensor-core A fragment (tokens g and g + 8, columns 2c, 2c + 1 [and 2c + 8, 2c + 9]) as one word."""
+    from quantized_kv_cache_kvq_gb300 import layout as L
+
+    cols = 8 if m <= 4 else 16
+    offs = L.ko_offsets(cols // 2)
+    assert sorted(offs.reshape(-1).tolist()) == list(range(0, 2 * 16 * cols, 2))
+    word = 8 if cols == 8 else 16
+    for g in range(8):
+        for c in range(4):
+            lane = 4 * g + c
+            base = word * lane
+            assert offs[g, 2 * c] == base and offs[g, 2 * c + 1] == base + 2
+            assert offs[g + 8, 2 * c] == base + 4 and offs[g + 8, 2 * c + 1] == base + 6
+            if cols == 16:
+                assert offs[g, 2 * c + 8] == base + 8 and offs[g + 8, 2 * c + 9] == base + 14

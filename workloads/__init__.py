@@ -67,6 +67,9 @@ class Workload:
     sink_scale: float = 1.0          # scale of the pre-RoPE K and V at absolute position 0
     n_outliers: int = 0              # outlier pre-RoPE key channels per (layer, kv head)
     outlier_scale: float = 1.0
+    massive_pairs: int = 0           # RoPE pairs (channels j, j + 64) of the pre-RoPE key scaled per (layer, kv head)
+    massive_scale: float = 1.0
+    bypass_pairs: int = 0            # fixed-channel bypass: the cache stores the massive pairs in fp16
     q_dtype: str = "bf16"            # 'bf16' or 'f32' query as handed to the kernel
     tier_b: bool = False
     delta_req: float = 1e-2
@@ -118,6 +121,24 @@ def outlier_channels(w: Workload, layer: int, kv_head: int) -> np.ndarray:
     return np.sort(rng.choice(HEAD_DIM, size=w.n_outliers, replace=False))
 
 
+def massive_pairs(w: Workload, layer: int, kv_head: int) -> np.ndarray:
+    """The seeded set of RoPE pairs j (pre-RoPE key channels j and j + 64 scaled) of (layer, kv_head);
+    the fixed-channel bypass of the cache uses the same set (a calibration that found them)."""
+    if not w.massive_pairs:
+        return np.zeros(0, dtype=np.int64)
+    rng = np.random.default_rng(unit_seed(w, 600_000 + layer * 64 + kv_head))
+    return np.sort(rng.choice(HEAD_DIM // 2, size=w.massive_pairs, replace=False))
+
+
+def bypass_pair_table(w: Workload, layer: int) -> np.ndarray:
+    """[Hkv, m] int32 bypassed pairs of a layer (m = w.bypass_pairs), or an empty [Hkv, 0] table."""
+    m = w.bypass_pairs
+    t = np.zeros((w.n_kv_heads, m), dtype=np.int32)
+    for h in range(w.n_kv_heads):
+        t[h] = massive_pairs(w, layer, h)[:m]
+    return t
+
+
 def rope_tables(positions: np.ndarray, theta: float = 1e6):
     """cos/sin [n, 64] in float64 for half-split RoPE: angle = pos * theta**(-2j/128)."""
     j = np.arange(HEAD_DIM // 2, dtype=np.float64)
@@ -157,6 +178,9 @@ def gen_unit_cpu(w: Workload, seq: int, layer: int, n_tokens: int, first_pos: in
         ch = outlier_channels(w, layer, h)
         if ch.size:
             k[:, h, ch] *= w.outlier_scale
+        pj = massive_pairs(w, layer, h)
+        if pj.size:
+            k[:, h, np.concatenate([pj, pj + HEAD_DIM // 2])] *= w.massive_scale
     k32 = apply_rope(k, pos, w.rope_theta)
     v32 = v.astype(np.float32)
     q32 = apply_rope(q, np.array([first_pos + n_tokens]), w.rope_theta)[0]
@@ -235,6 +259,9 @@ def gen_tokens_gpu(w: Workload, layer: int, positions, generator, device, sink: 
         ch = outlier_channels(w, layer, h)
         if ch.size:
             k[:, h, torch.from_numpy(ch).to(device)] *= w.outlier_scale
+        pj = massive_pairs(w, layer, h)
+        if pj.size:
+            k[:, h, torch.from_numpy(np.concatenate([pj, pj + HEAD_DIM // 2])).to(device)] *= w.massive_scale
     j = torch.arange(HEAD_DIM // 2, device=device, dtype=torch.float64)
     inv = w.rope_theta ** (-2.0 * j / HEAD_DIM)
     ang = pos.to(torch.float64)[:, None] * inv[None, :]
