@@ -259,6 +259,58 @@ kvq_status kvq_decode_attn_append(const kvq_cache* cache, const void* k_new_dev,
                                   float* out_dev, float* meter_state_dev, void* workspace_dev, size_t ws_bytes,
                                   int32_t* err_word_dev, kvq_stream_t stream);
 
+/* Optional outputs of kvq_decode_attn_ex. */
+typedef struct kvq_decode_extras {
+  float* page_log_contrib;  /* [batch][num_q_heads][contrib_stride] or NULL: per page of a sequence's
+                               page list (the prefix pages, then the live pages) the natural log of
+                               sum_{t in page} e^{x_t} (e^{c_t} - 1), x_t the compressed logit, c_t the
+                               Tier A radius (-inf where every c_t is 0); exp(value - lse) is the page's
+                               contribution to A - 1 ([W] Sec. 6.3.5: A decomposes over blocks and paging
+                               in a block's exact values removes its contribution).  Requires the meter. */
+  int32_t contrib_stride;   /* >= ceil(prefix_len / 16) + max_pages_per_seq                            */
+  int32_t reserved;         /* must be 0                                                               */
+} kvq_decode_extras;
+
+/*
+ * kvq_decode_attn_ex -- kvq_decode_attn_append with the newest tokens optional (k_new_dev and
+ * v_new_dev both NULL: no append) and the optional outputs of `extras` (nullable).  Everything
+ * else is that of kvq_decode_attn_append / kvq_decode_attn.
+ */
+kvq_status kvq_decode_attn_ex(const kvq_cache* cache, const void* k_new_dev, const void* v_new_dev, int32_t kv_dtype,
+                              const kvq_cache* prefix, int32_t prefix_len, const void* q_dev, int32_t q_dtype,
+                              int32_t batch, int32_t num_q_heads, const int32_t* block_table_dev,
+                              int32_t max_pages_per_seq, const int32_t* seq_lens_dev, float sm_scale,
+                              const kvq_meter_params* meter, const kvq_decode_extras* extras, float* out_dev,
+                              float* meter_state_dev, void* workspace_dev, size_t ws_bytes, int32_t* err_word_dev,
+                              kvq_stream_t stream);
+
+/*
+ * kvq_gate -- greedy block page-in plan from the page contributions ([W] Sec. 6.3.5, Sec. 6.1 "Gate"):
+ * per (sequence, query head), the shortest list of pages, taken in decreasing order of contribution
+ * (ties to the lower page index), whose removal brings A - 1 (the state's ln(A - 1)) down to
+ * sqrt(1 + 2 tau) - 1, i.e. the meter 1/2 (A^2 - 1) to at most tau (the compressed distribution held
+ * fixed, as on the page).
+ * page_log_contrib_dev / contrib_stride: as written by kvq_decode_attn_ex; meter_state_dev:
+ *   [batch][num_q_heads][8] of the same call; seq_lens_dev, prefix_len: that call's.  A sequence
+ *   has ceil(prefix_len / 16) + ceil(seq_len / 16) pages; at most 16384.
+ * n_page_in_dev: [batch][num_q_heads] int32, the list's length (0 when the meter is already <= tau).
+ * page_list_dev (nullable): [batch][num_q_heads][max_list] int32, the first min(n, max_list) pages of
+ *   the list in order, -1 after them.
+ */
+kvq_status kvq_gate(const float* page_log_contrib_dev, int32_t contrib_stride, const float* meter_state_dev,
+                    int32_t batch, int32_t num_q_heads, const int32_t* seq_lens_dev, int32_t prefix_len, float tau,
+                    int32_t* n_page_in_dev, int32_t* page_list_dev, int32_t max_list, kvq_stream_t stream);
+
+/*
+ * kvq_zero_witness -- after a repair (the pages' exact values written back into the cache), zero
+ * the witness (and the value witness, if the cache has one) of the repaired slots, so the meter
+ * stops charging them ([W] Sec. 6.1: "write back, zero the witness").
+ * slots_dev: [n] int32 physical slots; negative slots are skipped; a slot past the cache is reported
+ * as KVQ_ERR_DEVICE_BOUNDS through err_word_dev (nullable).
+ */
+kvq_status kvq_zero_witness(const kvq_cache* cache, const int32_t* slots_dev, int32_t n, int32_t* err_word_dev,
+                            kvq_stream_t stream);
+
 /*
  * kvq_decode_attn_noalloc -- kvq_decode_attn without a caller-provided
  * workspace.  No counterpart on the source pages: it exists for callers that

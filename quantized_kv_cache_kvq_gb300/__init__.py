@@ -88,6 +88,10 @@ class _Cache(ctypes.Structure):
     ]
 
 
+class DecodeExtras(ctypes.Structure):
+    _fields_ = [("page_log_contrib", c_void_p), ("contrib_stride", c_int32), ("reserved", c_int32)]
+
+
 class MeterParams(ctypes.Structure):
     _fields_ = [
         ("tiers", c_uint32),
@@ -128,6 +132,17 @@ def load(path: str = LIB_PATH):
         c_void_p, c_int32, c_void_p, c_float, POINTER(MeterParams), c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
         c_void_p,
     ]
+    L.kvq_decode_attn_ex.restype = c_int32
+    L.kvq_decode_attn_ex.argtypes = [
+        POINTER(_Cache), c_void_p, c_void_p, c_int32, POINTER(_Cache), c_int32, c_void_p, c_int32, c_int32, c_int32,
+        c_void_p, c_int32, c_void_p, c_float, POINTER(MeterParams), POINTER(DecodeExtras), c_void_p, c_void_p,
+        c_void_p, c_size_t, c_void_p, c_void_p,
+    ]
+    L.kvq_gate.restype = c_int32
+    L.kvq_gate.argtypes = [c_void_p, c_int32, c_void_p, c_int32, c_int32, c_void_p, c_int32, c_float, c_void_p,
+                           c_void_p, c_int32, c_void_p]
+    L.kvq_zero_witness.restype = c_int32
+    L.kvq_zero_witness.argtypes = [POINTER(_Cache), c_void_p, c_int32, c_void_p, c_void_p]
     L.kvq_decode_attn_noalloc.restype = c_int32
     L.kvq_decode_attn_noalloc.argtypes = [
         POINTER(_Cache), POINTER(_Cache), c_int32, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32,
@@ -283,6 +298,49 @@ def decode_attn_append(cache: PagedCache, k_new: torch.Tensor, v_new: torch.Tens
         seq_lens.data_ptr(), float(sm_scale), ctypes.byref(meter) if meter is not None else None,
         out.data_ptr(), _ptr(meter_state), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _ptr(err), _stream(stream)), "kvq_decode_attn_append")
+
+
+def decode_attn_ex(cache: PagedCache, q: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                   out: torch.Tensor, workspace: torch.Tensor, *, k_new: torch.Tensor | None = None,
+                   v_new: torch.Tensor | None = None, prefix: PagedCache | None = None, prefix_len: int = 0,
+                   sm_scale: float | None = None, meter: MeterParams | None = None,
+                   meter_state: torch.Tensor | None = None, page_log_contrib: torch.Tensor | None = None,
+                   err: torch.Tensor | None = None, stream=None):
+    """kvq_decode_attn_ex: decode (with the optional newest-token append) and the optional per-page
+    log contributions page_log_contrib [B, Hq, stride] (fp32) for kvq_gate."""
+    B, Hq, D = q.shape
+    assert D == HEAD_DIM and q.is_contiguous() and out.is_contiguous()
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    d = cache.desc()
+    pd = prefix.desc() if prefix is not None else None
+    ex = None
+    if page_log_contrib is not None:
+        assert page_log_contrib.dtype == torch.float32 and page_log_contrib.is_contiguous()
+        ex = DecodeExtras(page_log_contrib.data_ptr(), int(page_log_contrib.shape[-1]), 0)
+    _check(lib().kvq_decode_attn_ex(
+        ctypes.byref(d), _ptr(k_new), _ptr(v_new), DTYPE[k_new.dtype] if k_new is not None else 0,
+        ctypes.byref(pd) if pd is not None else None, int(prefix_len), q.data_ptr(), DTYPE[q.dtype], B, Hq,
+        block_table.data_ptr(), int(block_table.shape[1]) if block_table.dim() == 2 else 0, seq_lens.data_ptr(),
+        float(sm_scale), ctypes.byref(meter) if meter is not None else None, ctypes.byref(ex) if ex is not None else None,
+        out.data_ptr(), _ptr(meter_state), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _ptr(err), _stream(stream)), "kvq_decode_attn_ex")
+
+
+def gate(page_log_contrib: torch.Tensor, meter_state: torch.Tensor, seq_lens: torch.Tensor, prefix_len: int,
+         tau: float, n_page_in: torch.Tensor, page_list: torch.Tensor | None = None, stream=None):
+    """kvq_gate: greedy page-in plan per (sequence, query head)."""
+    B, Hq, stride = page_log_contrib.shape
+    _check(lib().kvq_gate(page_log_contrib.data_ptr(), stride, meter_state.data_ptr(), B, Hq, seq_lens.data_ptr(),
+                          int(prefix_len), float(tau), n_page_in.data_ptr(), _ptr(page_list),
+                          int(page_list.shape[-1]) if page_list is not None else 0, _stream(stream)), "kvq_gate")
+
+
+def zero_witness(cache: PagedCache, slots: torch.Tensor, err: torch.Tensor | None = None, stream=None):
+    """kvq_zero_witness: zero the witness (and value witness) of repaired slots."""
+    d = cache.desc()
+    _check(lib().kvq_zero_witness(ctypes.byref(d), slots.data_ptr(), int(slots.numel()), _ptr(err), _stream(stream)),
+           "kvq_zero_witness")
 
 
 def decode_attn_noalloc(cache: PagedCache, q: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,

@@ -145,6 +145,28 @@ cudaError_t dispatch_v(int vf, const kvq_cache& c, const void* k, const void* v,
   return cudaErrorInvalidValue;
 }
 
+// zero the witness (and value witness) of repaired slots: one thread per (slot, kv head)
+__global__ void zero_witness_kernel(kvq_cache c, const int32_t* __restrict__ slots, int n, int32_t* err) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int H = c.num_kv_heads;
+  if (i >= static_cast<long long>(n) * H) return;
+  const int slot = slots[i / H], head = static_cast<int>(i % H);
+  if (slot < 0) return;
+  const int page = slot >> 4, t = slot & 15;
+  if (page >= c.num_pages) {
+    report(err, KVQ_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  uint8_t* w = reinterpret_cast<uint8_t*>(c.witness) + (static_cast<size_t>(page) * H + head) * kTileBytesW;
+#pragma unroll
+  for (int b = 0; b < 16; ++b) *reinterpret_cast<uint16_t*>(w + w_offset(t, b)) = 0;
+  if (c.v_witness) {
+    uint8_t* vw = reinterpret_cast<uint8_t*>(c.v_witness) + (static_cast<size_t>(head) * c.num_pages + page) * kTileBytesVW;
+    *reinterpret_cast<uint16_t*>(vw + vw_offset(t, 0)) = 0;
+    *reinterpret_cast<uint16_t*>(vw + vw_offset(t, 1)) = 0;
+  }
+}
+
 __global__ void debug_dither_kernel(uint64_t seed, int layer, int head, const int32_t* slots, int n, float* out) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;  // one thread per group
   if (i >= static_cast<long long>(n) * 32) return;
@@ -242,6 +264,17 @@ cudaError_t launch_append_newest(const kvq_cache& c, const void* k, const void* 
   return cudaErrorInvalidValue;
 }
 }  // namespace kvq
+
+extern "C" kvq_status kvq_zero_witness(const kvq_cache* c, const int32_t* slots, int32_t n, int32_t* err,
+                                       kvq_stream_t stream) {
+  if (!c || n < 0 || c->num_kv_heads <= 0 || c->num_pages < 0) return KVQ_ERR_INVALID_ARG;
+  if (n == 0) return KVQ_OK;
+  if (!slots || !c->witness) return KVQ_ERR_INVALID_ARG;
+  const long long threads = static_cast<long long>(n) * c->num_kv_heads;
+  zero_witness_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      *c, slots, n, err);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
 
 extern "C" kvq_status kvq_debug_dither(uint64_t seed, int32_t layer, int32_t kv_head, const int32_t* slots, int32_t n,
                                        float* xi, kvq_stream_t stream) {

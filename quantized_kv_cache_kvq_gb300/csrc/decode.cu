@@ -309,8 +309,17 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
                        const kvq_cache* prefix, int32_t prefix_len, const void* q, int32_t q_dtype, int32_t batch,
                        int32_t num_q_heads, const int32_t* block_table, int32_t max_pages_per_seq,
                        const int32_t* seq_lens, float sm_scale, const kvq_meter_params* mp, float* out,
-                       float* meter_state, void* workspace, size_t ws_bytes, int32_t* err_word, cudaStream_t s) {
+                       float* meter_state, void* workspace, size_t ws_bytes, int32_t* err_word, cudaStream_t s,
+                       const kvq_decode_extras* extras = nullptr) {
   const bool meter = mp != nullptr;
+  const bool contrib = extras && extras->page_log_contrib;
+  if (extras && extras->reserved != 0) return KVQ_ERR_INVALID_ARG;
+  if (contrib) {
+    if (!meter) return KVQ_ERR_INVALID_ARG;
+    const long long need = (static_cast<long long>(prefix && prefix_len > 0 ? prefix_len : 0) + kPage - 1) / kPage +
+                           max_pages_per_seq;
+    if (extras->contrib_stride < need) return KVQ_ERR_INVALID_ARG;
+  }
   kvq_status st = check_cache(cache, meter);
   if (st != KVQ_OK) return st;
   const bool fused_append = k_new != nullptr || v_new != nullptr;
@@ -359,8 +368,8 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   const int pkf = has_prefix ? prefix->k_fmt : kNoPrefix;
   const int pvf = has_prefix ? prefix->v_fmt : kNoPrefix;
   const bool outl = cache->n_outlier_pairs > 0;
-  const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter, meter && (mp->tiers & (KVQ_TIER_V | KVQ_TIER_S)),
-                       outl);
+  const bool ext_meter = meter && ((mp->tiers & (KVQ_TIER_V | KVQ_TIER_S)) || contrib);
+  const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter, ext_meter, outl);
   if (!pk.launch) return KVQ_ERR_UNSUPPORTED_LAYOUT;
   const int nw = pk.warps;
   const int w_max = sms * nw;
@@ -393,6 +402,8 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   a.meter_on = meter ? 1 : 0;
   a.value_on = meter && (mp->tiers & KVQ_TIER_V) ? 1 : 0;
   a.shapes_on = meter && (mp->tiers & KVQ_TIER_S) ? 1 : 0;
+  a.page_contrib = contrib ? extras->page_log_contrib : nullptr;
+  a.contrib_stride = contrib ? extras->contrib_stride : 0;
   a.ws_stats = reinterpret_cast<float*>(ws + wl.stats);
   a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
   a.w_max = w_max;
@@ -404,7 +415,7 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   const bool xi = cache->k_fmt == KVQ_FMT_INT8_DITHER && cache->v_fmt == KVQ_FMT_INT8_DITHER;
   const int cum_bytes = ((batch + 1) * 4 + 127) & ~127;
   const int lo_bytes = q_dtype == KVQ_DTYPE_F32 ? kQloBytes : 0;
-  const bool ext = a.value_on || a.shapes_on;  // the extended-meter kernel variant and its per-lane state
+  const bool ext = ext_meter;  // the extended-meter kernel variant and its per-lane state
   const int fixed = cum_bytes + nw * ((xi ? kXiScratch : 0) + lo_bytes + (ext ? kVStateBytes : 0) + kMaxStages * 8);
   const int budget = smem_max - 1024 - fixed;
   int stages = budget / (nw * sb);
@@ -458,6 +469,19 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* p
   return decode_impl(cache, nullptr, nullptr, KVQ_DTYPE_F32, prefix, prefix_len, q, q_dtype, batch, num_q_heads,
                      block_table, max_pages_per_seq, seq_lens, sm_scale, mp, out, meter_state, workspace, ws_bytes,
                      err_word, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvq_status kvq_decode_attn_ex(const kvq_cache* cache, const void* k_new, const void* v_new, int32_t kv_dtype,
+                                         const kvq_cache* prefix, int32_t prefix_len, const void* q, int32_t q_dtype,
+                                         int32_t batch, int32_t num_q_heads, const int32_t* block_table,
+                                         int32_t max_pages_per_seq, const int32_t* seq_lens, float sm_scale,
+                                         const kvq_meter_params* mp, const kvq_decode_extras* extras, float* out,
+                                         float* meter_state, void* workspace, size_t ws_bytes, int32_t* err_word,
+                                         kvq_stream_t stream) {
+  if ((k_new == nullptr) != (v_new == nullptr)) return KVQ_ERR_INVALID_ARG;
+  return decode_impl(cache, k_new, v_new, kv_dtype, prefix, prefix_len, q, q_dtype, batch, num_q_heads, block_table,
+                     max_pages_per_seq, seq_lens, sm_scale, mp, out, meter_state, workspace, ws_bytes, err_word,
+                     reinterpret_cast<cudaStream_t>(stream), extras);
 }
 
 extern "C" kvq_status kvq_decode_attn_append(const kvq_cache* cache, const void* k_new, const void* v_new,

@@ -40,7 +40,7 @@ constexpr int kXiScratch = 16 * 128 * 2;  // per-warp fp16 dither tile (INT8 val
 // value side (sum_t e^{x_t - m} rho^v_t for heads 2c and 2c + 1, rescaled with l; max_t ||v_t||; 0) and
 // alternative bound shapes (max_t c_t for heads 2c, 2c + 1; sum_t e^{x_t - m} (1 - e^{-c_t}) for both heads).
 constexpr int kVStateBytes = 32 * 32;
-constexpr int kExtValue = 1, kExtShapes = 2;
+constexpr int kExtValue = 1, kExtShapes = 2, kExtContrib = 4;
 constexpr int kStatsFloats = 12;  // per (piece, head): m l mc sc | mu su vr vmax | cmax om 0 0
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitNs = 2000000000ull;  // a copy not landed after 2 s is reported as a timeout
@@ -80,6 +80,8 @@ struct Args {
   int meter_on;
   int value_on;      // value side of the output bound (value witness read, R and Vmax accumulated)
   int shapes_on;     // alternative bound shapes (max radius, 1 - A^-)
+  float* page_contrib;  // [B][Hq][contrib_stride] per-page log contributions to A - 1, or nullptr
+  int contrib_stride;
   float* ws_stats;   // [slots][G][8]
   float* ws_acc;     // [slots][G][128]
   int w_max;
@@ -586,7 +588,8 @@ __device__ __forceinline__ void accumulate_meter(const float (&r)[4], const floa
 template <int KF, int VF, bool METER, bool OUTL = false>
 __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile, float xb0, float xb1, uint32_t phys,
                                              const Planes& pl, int kvh, const QFrag& f, SoftState& s,
-                                             float qk_scale, bool tier_b, float* vstate, int ext) {
+                                             float qk_scale, bool tier_b, float* vstate, int ext,
+                                             float* cdst = nullptr, int cstride = 0, int G = 0) {
   using L = Layout<KF, VF, METER, OUTL>;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   constexpr bool K16 = fmt_is_16bit(KF);
@@ -751,6 +754,21 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       w4.z = __fmaf_rn(p[2], one_minus_exp_neg(cv[2]), __fmaf_rn(p[0], one_minus_exp_neg(cv[0]), w4.z * alpha[0]));
       w4.w = __fmaf_rn(p[3], one_minus_exp_neg(cv[3]), __fmaf_rn(p[1], one_minus_exp_neg(cv[1]), w4.w * alpha[1]));
       *reinterpret_cast<float4*>(vstate + 8 * lane + 4) = w4;
+    }
+    if (vstate && cdst) {
+      // gate support (WitCert Sec. 6.3.5): ln sum_{t in page} e^{x_t} (e^{c_t} - 1) for heads 2c, 2c + 1
+      float t[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        t[v] = (x[v] == -INFINITY || cv[v] <= 0.f) ? -INFINITY : x[v] * kLn2 + cv[v] + logf(one_minus_exp_neg(cv[v]));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float mx = col_max8(fmaxf(t[h], t[2 + h]));
+        const float sum = col_sum8(mx == -INFINITY ? 0.f : expf(t[h] - mx) + expf(t[2 + h] - mx));
+        const int head = 2 * (lane & 3) + h;
+        if ((lane >> 2) == 0 && head < G) cdst[static_cast<size_t>(head) * cstride] = mx == -INFINITY ? -INFINITY
+                                                                                              : mx + logf(sum);
+      }
     }
     if (KDITHER && tier_b) {
       float uv[4];
@@ -1095,6 +1113,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   SoftState s;
   reset_state(s);
   int unit = -1;
+  long long unit_x0 = 0;   // gate support: global index of the current unit's first page
+  float* crow = nullptr;   // gate support: the current unit's contribution row
   const float qk_scale = a.sm_scale * kLog2e;
   bool ok = true;
   int timeout_at = 0;
@@ -1116,6 +1136,11 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       const int seq = u / a.Hkv, kvh = u % a.Hkv;
       const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
       load_q<K16, METER, OUTL>(a, seq, kvh, total, f);
+      if (VALUE && a.page_contrib) {
+        // this unit's row of contributions, and the global index of its first page
+        unit_x0 = static_cast<long long>(a.Hkv) * cum[seq] + static_cast<long long>(kvh) * (cum[seq + 1] - cum[seq]);
+        crow = a.page_contrib + (static_cast<size_t>(seq) * a.Hq + static_cast<size_t>(kvh) * a.G) * a.contrib_stride;
+      }
     }
     // every lane polls; the verdict is made warp-uniform before anyone leaves the loop
     if (!__all_sync(kFull, mbar_wait(&bars[stage], parity))) { ok = false; timeout_at = j; break; }
@@ -1128,11 +1153,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
         constexpr int pk = (PKF < 0 ? 0 : PKF), pv = (PVF < 0 ? 0 : PVF);
         if (nvalid < kPage) zero_tail<pk, pv, METER, VALUE>(st, nvalid, a.value_on != 0);
         process_page<pk, pv, METER>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.pre, kvh, f, s,
-                                    qk_scale, a.tier_b != 0, vstate, ext);
+                                    qk_scale, a.tier_b != 0, vstate, ext,
+                                    crow ? crow + (x_begin + j - unit_x0) : nullptr, a.contrib_stride, a.G);
       } else {
         if (nvalid < kPage) zero_tail<KF, VF, METER, VALUE, OUTL>(st, nvalid, a.value_on != 0, a.live.n_out > 4);
         process_page<KF, VF, METER, OUTL>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f, s,
-                                    qk_scale, a.tier_b != 0, vstate, ext);
+                                    qk_scale, a.tier_b != 0, vstate, ext,
+                                    crow ? crow + (x_begin + j - unit_x0) : nullptr, a.contrib_stride, a.G);
       }
     }
     __syncwarp();

@@ -111,10 +111,87 @@ __global__ void __launch_bounds__(512) rank_kernel(const float* __restrict__ raw
   }
 }
 
+constexpr int kMaxGatePages = 16384;
+
+// Greedy block page-in (WitCert Sec. 6.3.5): one block per (sequence, query head) cell.  The cell's
+// page contributions exp(lc - lse) are sorted in shared memory (bitonic; descending, ties to the lower
+// page index) and walked in double precision until A - 1 is at most sqrt(1 + 2 tau) - 1.
+__global__ void __launch_bounds__(512) gate_kernel(const float* __restrict__ lc, int stride,
+                                                   const float* __restrict__ state, int hq,
+                                                   const int32_t* __restrict__ seq_lens, int prefix_pages, float tau,
+                                                   int32_t* __restrict__ n_out, int32_t* __restrict__ list,
+                                                   int max_list) {
+  extern __shared__ __align__(16) float key[];
+  const int cell = blockIdx.x, seq = cell / hq;
+  const int len = max(seq_lens[seq], 0);
+  const int P = min(min(prefix_pages + (len + 15) / 16, kMaxGatePages), stride);  // never past the row
+  int n2 = 1;
+  while (n2 < P) n2 <<= 1;
+  int* idx = reinterpret_cast<int*>(key + n2);
+  const float lse = state[static_cast<size_t>(cell) * KVQ_METER_STATE_FLOATS + 2];
+  const float la = state[static_cast<size_t>(cell) * KVQ_METER_STATE_FLOATS];
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    float k = -1.f;  // padding sorts last
+    if (i < P) {
+      const float v = lc[static_cast<size_t>(cell) * stride + i];
+      k = v == -INFINITY ? 0.f : expf(v - lse);
+    }
+    key[i] = k;
+    idx[i] = i;
+  }
+  __syncthreads();
+  auto before = [&](int a, int b) { return key[a] > key[b] || (key[a] == key[b] && idx[a] < idx[b]); };
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int half = size >> 1; half > 0; half >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int j = i ^ half;
+        if (j > i && ((i & size) == 0 ? before(j, i) : before(i, j))) {
+          const float tk = key[i]; key[i] = key[j]; key[j] = tk;
+          const int ti = idx[i]; idx[i] = idx[j]; idx[j] = ti;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  __shared__ int k_shared;
+  if (threadIdx.x == 0) {
+    const double target = sqrt(1.0 + 2.0 * static_cast<double>(tau)) - 1.0;
+    double rest = la == -INFINITY ? 0.0 : exp(static_cast<double>(la));
+    int k = 0;
+    while (rest > target && k < P) rest -= static_cast<double>(key[k++]);
+    k_shared = k;
+    n_out[cell] = k;
+  }
+  __syncthreads();
+  if (list)
+    for (int i = threadIdx.x; i < max_list; i += blockDim.x)
+      list[static_cast<size_t>(cell) * max_list + i] = i < k_shared ? idx[i] : -1;
+}
+
 }  // namespace
 }  // namespace kvq
 
 using namespace kvq;
+
+extern "C" kvq_status kvq_gate(const float* lc, int32_t stride, const float* state, int32_t batch, int32_t hq,
+                               const int32_t* seq_lens, int32_t prefix_len, float tau, int32_t* n_page_in,
+                               int32_t* page_list, int32_t max_list, kvq_stream_t stream) {
+  if (batch < 0 || hq <= 0 || prefix_len < 0 || stride <= 0 || !(tau >= 0.f) || max_list < 0) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0) return KVQ_OK;
+  if (!lc || !state || !seq_lens || !n_page_in || (page_list && max_list == 0)) return KVQ_ERR_INVALID_ARG;
+  static int configured = 0;
+  const int smem = kMaxGatePages * 8;  // keys and indices
+  if (!configured) {
+    if (cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    configured = 1;
+  }
+  const int prefix_pages = (prefix_len + 15) / 16;
+  gate_kernel<<<static_cast<unsigned>(static_cast<long long>(batch) * hq), 512, smem,
+                reinterpret_cast<cudaStream_t>(stream)>>>(lc, stride, state, hq, seq_lens, prefix_pages, tau, n_page_in,
+                                                           page_list, max_list);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
 
 extern "C" kvq_status kvq_meter(const float* state, int32_t n_layers, int32_t batch, int32_t hq,
                                 const kvq_meter_params* mp, float* meter_a, float* raw_a, float* cert_b,
