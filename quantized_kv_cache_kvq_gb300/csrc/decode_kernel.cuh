@@ -171,6 +171,40 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed binary32 pairs (lane 0 in the low word).  sm_100-family SMs issue add / sub / mul / fma on two
+// binary32 values as one instruction and round each one exactly like the scalar instruction, so the
+// pair forms below halve the issue cost of the per-lane arithmetic without changing any result bit.
+using f2x = unsigned long long;
+__device__ __forceinline__ f2x f2_pack(float lo, float hi) {
+  f2x r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ f2x f2_splat(float v) { return f2_pack(v, v); }
+__device__ __forceinline__ void f2_unpack(f2x x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ f2x f2_fma(f2x a, f2x b, f2x c) {
+  f2x d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2x f2_mul(f2x a, f2x b) {
+  f2x d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2x f2_add(f2x a, f2x b) {
+  f2x d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2x f2_sub(f2x a, f2x b) {
+  f2x d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -249,6 +283,22 @@ __device__ __forceinline__ float expm1_pos(float c, bool all_small) {
   if (all_small) return small;
   const float large = ex2(c * kLog2e) - 1.0f;
   return c < 0.5f ? small : large;
+}
+// The same for a pair: the Taylor polynomial in packed arithmetic.
+__device__ __forceinline__ f2x expm1_pos2(f2x c, bool all_small) {
+  f2x p = f2_fma(f2_splat(2.48015873015873e-05f), c, f2_splat(1.98412698412698e-04f));
+  p = f2_fma(p, c, f2_splat(1.38888888888889e-03f));
+  p = f2_fma(p, c, f2_splat(8.33333333333333e-03f));
+  p = f2_fma(p, c, f2_splat(4.16666666666667e-02f));
+  p = f2_fma(p, c, f2_splat(1.66666666666667e-01f));
+  p = f2_fma(p, c, f2_splat(0.5f));
+  p = f2_fma(p, c, f2_splat(1.0f));
+  const f2x small = f2_mul(p, c);
+  if (all_small) return small;
+  float s0, s1, c0, c1;
+  f2_unpack(small, s0, s1);
+  f2_unpack(c, c0, c1);
+  return f2_pack(c0 < 0.5f ? s0 : ex2(c0 * kLog2e) - 1.0f, c1 < 0.5f ? s1 : ex2(c1 * kLog2e) - 1.0f);
 }
 constexpr float kFastRadius = 60.f;  // e^60 * 2^17 tokens stays far below the fp32 range
 
@@ -556,12 +606,13 @@ __device__ __forceinline__ void accumulate_meter(const float (&r)[4], const floa
       kFull, __float_as_uint(fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3])))));  // r >= 0: bit order = value order
   slow = slow || !(rmax <= kFastRadius);
   if (!slow) {
+    // both heads at once: sc = sc alpha + (p_g (e^{r_g} - 1) + p_{g+8} (e^{r_{g+8}} - 1))
     const bool small = rmax < 0.5f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      sc[h] = sc[h] * alpha[h] + (p[h] * expm1_pos(r[h], small) + p[2 + h] * expm1_pos(r[2 + h], small));
-      mc[h] = mnew[h];
-    }
+    const f2x e0 = expm1_pos2(f2_pack(r[0], r[1]), small), e1 = expm1_pos2(f2_pack(r[2], r[3]), small);
+    const f2x t = f2_fma(f2_pack(p[2], p[3]), e1, f2_mul(f2_pack(p[0], p[1]), e0));
+    f2_unpack(f2_fma(f2_pack(sc[0], sc[1]), f2_pack(alpha[0], alpha[1]), t), sc[0], sc[1]);
+    mc[0] = mnew[0];
+    mc[1] = mnew[1];
     return;
   }
   float z[4];
@@ -700,13 +751,18 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   }
 
   // ---------------- online softmax (log2 domain).  v = 2r + h: token g + 8r, head 2c + h
-  const float xb[2] = {xb0, xb1};
-  float x[4];
+  // pair r holds token g + 8r for heads 2c, 2c + 1
+  f2x xp[2];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const float sc = fmt_has_scale(KF) ? qk_scale * sk[v >> 1] : qk_scale;
-    x[v] = __fmaf_rn(S[v], sc, OUTL ? __fmaf_rn(So[v], qk_scale, xb[v >> 1]) : xb[v >> 1]);
+  for (int r = 0; r < 2; ++r) {
+    const float sc = fmt_has_scale(KF) ? qk_scale * sk[r] : qk_scale;
+    f2x base = f2_splat(r ? xb1 : xb0);
+    if (OUTL) base = f2_fma(f2_pack(So[2 * r], So[2 * r + 1]), f2_splat(qk_scale), base);
+    xp[r] = f2_fma(f2_pack(S[2 * r], S[2 * r + 1]), f2_splat(sc), base);
   }
+  float x[4];
+  f2_unpack(xp[0], x[0], x[1]);
+  f2_unpack(xp[1], x[2], x[3]);
   float alpha[2], mnew[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -715,10 +771,16 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     alpha[h] = ex2(s.m[h] - mnew[h]);  // 0 on the first page (m = -inf); every page has a valid token
   }
   float p[4];
+  {
+    const f2x mn = f2_pack(mnew[0], mnew[1]);
+    float d[4];
+    f2_unpack(f2_sub(xp[0], mn), d[0], d[1]);
+    f2_unpack(f2_sub(xp[1], mn), d[2], d[3]);
 #pragma unroll
-  for (int v = 0; v < 4; ++v) p[v] = ex2(x[v] - mnew[v & 1]);  // 0 for -inf logits
-#pragma unroll
-  for (int h = 0; h < 2; ++h) s.l[h] = s.l[h] * alpha[h] + (p[h] + p[2 + h]);
+    for (int v = 0; v < 4; ++v) p[v] = ex2(d[v]);  // 0 for -inf logits
+    f2_unpack(f2_fma(f2_pack(s.l[0], s.l[1]), f2_pack(alpha[0], alpha[1]),
+                     f2_add(f2_pack(p[0], p[1]), f2_pack(p[2], p[3]))), s.l[0], s.l[1]);
+  }
   if (METER && vstate && (ext & kExtValue)) {
     // value side: rho^v and ||v|| of tokens g and g + 8 (WitCert Sec. 3 output bound)
     const uint2 vw = lds64(st + L::vwOff + 8 * g);
@@ -730,9 +792,11 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     *reinterpret_cast<float4*>(vstate + 8 * lane) = v4;
   }
   if (__any_sync(kFull, (alpha[0] != 1.f) | (alpha[1] != 1.f))) {
+    const f2x al = f2_pack(alpha[0], alpha[1]);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      s.o[i][0] *= alpha[0]; s.o[i][1] *= alpha[1]; s.o[i][2] *= alpha[0]; s.o[i][3] *= alpha[1];
+      f2_unpack(f2_mul(f2_pack(s.o[i][0], s.o[i][1]), al), s.o[i][0], s.o[i][1]);
+      f2_unpack(f2_mul(f2_pack(s.o[i][2], s.o[i][3]), al), s.o[i][2], s.o[i][3]);
     }
   }
 
@@ -743,8 +807,10 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     mma_f16_4(C, wb.x, wb.z, wb.y, wb.w, f.qn_hi[0], f.qn_hi[1]);
     mma_f16_4(C, wb.x, wb.z, wb.y, wb.w, f.qn_lo[0], f.qn_lo[1]);
     float cv[4];
+    f2_unpack(f2_mul(f2_pack(C[0], C[1]), f2_splat(f.cm_scale)), cv[0], cv[1]);
+    f2_unpack(f2_mul(f2_pack(C[2], C[3]), f2_splat(f.cm_scale)), cv[2], cv[3]);
 #pragma unroll
-    for (int v = 0; v < 4; ++v) cv[v] = fmaxf(C[v] * f.cm_scale, 0.f);
+    for (int v = 0; v < 4; ++v) cv[v] = fmaxf(cv[v], 0.f);
     accumulate_meter(cv, x, p, alpha, mnew, s.mc, s.sc, s.slow_a);
     if (vstate && (ext & kExtShapes)) {
       // alternative shapes (WitCert Sec. 4.3 Prop. 1; det-tanh): max_t c_t and sum_t e^{x_t - m} (1 - e^{-c_t})
@@ -772,10 +838,12 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     }
     if (KDITHER && tier_b) {
       float uv[4];
+      const f2x ab = f2_pack(f.alpha_b[0], f.alpha_b[1]);
+      f2_unpack(f2_mul(ab, f2_splat(sk[0])), uv[0], uv[1]);
+      f2_unpack(f2_mul(ab, f2_splat(sk[1])), uv[2], uv[3]);
+      if (OUTL) {
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uv[v] = f.alpha_b[v & 1] * sk[v >> 1];
-        if (OUTL) uv[v] = __fmaf_ru(f.beta_o[v & 1], kon[v >> 1], uv[v]) + f.gamma_o[v & 1];
+        for (int v = 0; v < 4; ++v) uv[v] = __fmaf_ru(f.beta_o[v & 1], kon[v >> 1], uv[v]) + f.gamma_o[v & 1];
       }
       accumulate_meter(uv, x, p, alpha, mnew, s.mu, s.su, s.slow_b);
     }
@@ -785,8 +853,8 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
 
   // ---------------- O^T += V^T . P^T.  P'^T (B operand) = movmatrix of the S^T-shaped weights.
   float pw[4];
-#pragma unroll
-  for (int v = 0; v < 4; ++v) pw[v] = p[v] * (kPvShift * sv[v >> 1]);
+  f2_unpack(f2_mul(f2_pack(p[0], p[1]), f2_splat(kPvShift * sv[0])), pw[0], pw[1]);
+  f2_unpack(f2_mul(f2_pack(p[2], p[3]), f2_splat(kPvShift * sv[1])), pw[2], pw[3]);
   if (!fmt_is_16bit(VF)) {
     const uint32_t b0 = movmatrix_trans(pack_f16(pw[0], pw[1]));
     const uint32_t b1 = movmatrix_trans(pack_f16(pw[2], pw[3]));

@@ -179,11 +179,14 @@ __device__ __forceinline__ float dither_from_word(uint32_t w) {
 // operand.  The top 23 bits m = w >> 9 are placed in the mantissa of a float f = 1 + m 2^-23 (no
 // int-to-float conversion); 3/2 - f is exact and exceeds -xi = 1/2 - ((w >> 8) + 1/2) 2^-24 by
 // (bit 8 of w + 1/2) 2^-24 <= 1.5 * 2^-24, far below the fp16 rounding that follows.
+// Both subtractions run as one packed binary32 instruction (each lane rounded like the scalar one).
 __device__ __forceinline__ uint32_t neg_dither_f16x2(uint32_t w0, uint32_t w1) {
-  const float a = 1.5f - __uint_as_float((w0 >> 9) + 0x3F800000u);
-  const float b = 1.5f - __uint_as_float((w1 >> 9) + 0x3F800000u);
-  const __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
+  unsigned long long f, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(f) : "r"((w0 >> 9) + 0x3F800000u), "r"((w1 >> 9) + 0x3F800000u));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(0x3FC000003FC00000ull /* 1.5, 1.5 */), "l"(f));
+  uint32_t h;
+  asm("{\n\t.reg .f32 a, b;\n\tmov.b64 {a, b}, %1;\n\tcvt.rn.f16x2.f32 %0, b, a;\n\t}" : "=r"(h) : "l"(d));
+  return h;
 }
 
 // The four dithers of channels 4*group .. 4*group+3 of (slot, layer, kv_head).
