@@ -49,12 +49,23 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
   const int seq = static_cast<int>(gw / a.Hq), qh = static_cast<int>(gw % a.Hq);
   const int kvh = qh / a.G, row = qh % a.G;
   const int unit = seq * a.Hkv + kvh;
-  // inputs of the call are read before the wait; the decode grid's outputs only after it
+  // inputs of the call are read before the wait (the decode grid's outputs only after it): the
+  // sequence's page range [c0, c1) and the total cB, by the decode's own clamping of the lengths
   const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
+  int c0 = 0, cB = 0;
+  for (int s = lane; s < a.B; s += 32) {
+    const int n = a.prefix_pages + (min(max(a.seq_lens[s], 0), a.max_pages * kPage) + kPage - 1) / kPage;
+    cB += n;
+    if (s < seq) c0 += n;
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    c0 += __shfl_xor_sync(kFull, c0, off);
+    cB += __shfl_xor_sync(kFull, cB, off);
+  }
+  const int c1 = c0 + a.prefix_pages + (total - a.prefix_len + kPage - 1) / kPage;
   float* o = a.out + static_cast<size_t>(gw) * kHeadDim;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's pieces are complete and visible
-  const int32_t* cum = a.ws_cum;
-  const int c0 = cum[seq], c1 = cum[seq + 1], cB = cum[a.B];
   const long long T = static_cast<long long>(a.Hkv) * cB;
   const int P = c1 - c0;
   if (P == 0) {
@@ -201,15 +212,14 @@ int device_smem_optin() {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t cum, stats, acc, total;
+  size_t stats, acc, total;
 };
 
 WsLayout ws_layout(int batch, int hkv, int hq, int w_max) {
   const int G = hq / hkv;
   const size_t slots = static_cast<size_t>(w_max) + static_cast<size_t>(batch) * hkv;
   WsLayout l;
-  l.cum = 0;
-  l.stats = align256(static_cast<size_t>(batch + 1) * 4);
+  l.stats = 0;
   l.acc = l.stats + align256(slots * G * kStatsFloats * sizeof(float));
   l.total = l.acc + align256(slots * G * kHeadDim * sizeof(float));
   return l;
@@ -396,7 +406,6 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
     a.ln_delta_loc = static_cast<float>(
         std::log(mp->delta_req / (static_cast<double>(mp->n_layers) * mp->n_q_heads * mp->n_steps)));
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.ws_cum = reinterpret_cast<int32_t*>(ws + wl.cum);
   a.out = out;
   a.meter_state = meter_state;
   a.meter_on = meter ? 1 : 0;

@@ -74,7 +74,6 @@ struct Args {
   int tier_b;
   float ln_delta_loc;
   int wait_append;   // the preceding grid appends each sequence's newest token (programmatic launch)
-  int32_t* ws_cum;   // [B + 1] prefix sums of pages per sequence (written by CTA 0)
   float* out;        // [B][Hq][128]
   float* meter_state;  // [B][Hq][4] or nullptr
   int meter_on;
@@ -1134,8 +1133,6 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       }
     }
     __syncthreads();
-    if (blockIdx.x == 0)
-      for (int i = threadIdx.x; i <= a.B; i += blockDim.x) a.ws_cum[i] = cum[i];
   }
 
   const long long T = static_cast<long long>(a.Hkv) * cum[a.B];
