@@ -148,6 +148,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     if (global_ns() - t0 > limit_ns) return false;
   }
 }
+// L2 policy for the streamed pages of the live cache when a shared prefix is attended too: each live page
+// is read once, so it goes first when L2 needs room and the prefix pages, read by every sequence, stay
+// resident (measured: +1 % on a 632-token prefix; without a prefix the plain policy is kept).
+__device__ __forceinline__ uint64_t stream_policy(bool evict_first) {
+  uint64_t p;
+  if (evict_first)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -986,15 +1004,17 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     }
     const int ko_bytes = OUTL ? outlier_tile_bytes(a.live.n_out) : 0;
     mbar_arrive_expect_tx(bar, L::koOff + ko_bytes + (VALUE && a.value_on ? kTileBytesVW : 0));
-    bulk_g2s(stage + L::kOff, a.live.k + tile * L::kBytes, L::kBytes, bar);
-    bulk_g2s(stage + L::vOff, a.live.v + tile * L::vBytes, L::vBytes, bar);
-    if (METER) bulk_g2s(stage + L::wOff, a.live.w + tile * kTileBytesW, kTileBytesW, bar);
+    const uint64_t pol = stream_policy(PKF != kNoPrefix && a.prefix_pages > 0);
+    bulk_g2s_hint(stage + L::kOff, a.live.k + tile * L::kBytes, L::kBytes, bar, pol);
+    bulk_g2s_hint(stage + L::vOff, a.live.v + tile * L::vBytes, L::vBytes, bar, pol);
+    if (METER) bulk_g2s_hint(stage + L::wOff, a.live.w + tile * kTileBytesW, kTileBytesW, bar, pol);
     // scale planes are head-major, so consecutive pages of a unit share a 128-byte line
     const size_t stile = static_cast<size_t>(kvh) * a.live.num_pages + d.phys;
     if (fmt_has_scale(KF)) bulk_g2s(stage + L::ksOff, a.live.ks + stile * kTileBytesS, kTileBytesS, bar);
     if (fmt_has_scale(VF)) bulk_g2s(stage + L::vsOff, a.live.vs + stile * kTileBytesS, kTileBytesS, bar);
-    if (OUTL) bulk_g2s(stage + L::koOff, a.live.ko + stile * ko_bytes, ko_bytes, bar);
-    if (METER && VALUE && a.value_on) bulk_g2s(stage + L::vwOff, a.live.vw + stile * kTileBytesVW, kTileBytesVW, bar);
+    if (OUTL) bulk_g2s_hint(stage + L::koOff, a.live.ko + stile * ko_bytes, ko_bytes, bar, pol);
+    if (METER && VALUE && a.value_on)
+      bulk_g2s_hint(stage + L::vwOff, a.live.vw + stile * kTileBytesVW, kTileBytesVW, bar, pol);
   }
 }
 
