@@ -79,12 +79,22 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
     }
     return;
   }
-  const long long W = min(static_cast<long long>(a.w_max), T);
-  const long long b_u = static_cast<long long>(a.Hkv) * c0 + static_cast<long long>(kvh) * P;
-  const long long e_u = b_u + P;
-  // warp w covers pages [T w / W, T (w + 1) / W): the warp holding page x is ((x + 1) W - 1) / T
-  const long long w_lo = ((b_u + 1) * W - 1) / T, w_hi = (e_u * W - 1) / T;
-  const int np = static_cast<int>(w_hi - w_lo + 1);
+  // page indices fit in 32 bits (checked by the host)
+  const int Ti = static_cast<int>(T);
+  const int W = min(a.w_max, Ti);
+  const int b_u = a.Hkv * c0 + kvh * P, e_u = b_u + P;
+  // warp w covers pages [T w / W, T (w + 1) / W); with T = q W + r that start is q w + (r w) / W.  The
+  // warp holding page x: a binary32 estimate of x W / T, corrected against the exact starts.
+  const int qd = Ti / W, rd = Ti % W;
+  auto start_of = [&](int w) { return qd * w + (rd * w) / W; };
+  auto warp_of = [&](int x) {
+    int w = min(W - 1, static_cast<int>(static_cast<float>(x) * (static_cast<float>(W) / static_cast<float>(Ti))));
+    while (w + 1 < W && start_of(w + 1) <= x) ++w;
+    while (w > 0 && start_of(w) > x) --w;
+    return w;
+  };
+  const int w_lo = warp_of(b_u), w_hi = warp_of(e_u - 1);
+  const int np = w_hi - w_lo + 1;
   const size_t p0 = static_cast<size_t>(w_lo) + unit;  // piece slot of the unit's first piece
   auto stats = [&](int i) { return a.ws_stats + ((p0 + i) * a.G + row) * kStatsFloats; };
   auto accp = [&](int i) { return a.ws_acc + ((p0 + i) * a.G + row) * kHeadDim + 4 * lane; };
@@ -96,69 +106,74 @@ __global__ void __launch_bounds__(256) merge_kernel(const Args a) {
 #pragma unroll
   for (int k = 0; k < kU; ++k)
     if (k < np) v[k] = *reinterpret_cast<const float4*>(accp(k));
-  float m = -INFINITY, l = 0.f, mc = -INFINITY, sc = 0.f, mu = -INFINITY, su = 0.f, vr = 0.f, vmax = 0.f;
-  float cmax = 0.f, om = 0.f;
+  // this lane's pieces (lane, lane + 32, ...) merged locally; then one max and one weighted sum over
+  // the lanes.  (m, l), (mc, sc), (mu, su): running max (log2 units) and scaled sums; r (value side) and
+  // u (1 - A^- of the shapes) ride on l's weights.
+  const bool ext = a.value_on | a.shapes_on;
+  float m = -INFINITY, l = 0.f, mc = -INFINITY, sc = 0.f, mu = -INFINITY, su = 0.f, vr = 0.f, om = 0.f;
+  float vmax = 0.f, cmax = 0.f;
   float m_mine = -INFINITY;  // the running max of piece `lane` (pieces < 32), for the weights below
-  // both branches combine (m, l) with the same arithmetic (lse_combine3), so the output does not depend
-  // on whether the extended meter is on
-  if (!(a.value_on | a.shapes_on)) {
-    for (int i = lane; i < np; i += 32) {
-      const float4 s4 = *reinterpret_cast<const float4*>(stats(i));
-      const float2 t2 = *reinterpret_cast<const float2*>(stats(i) + 4);
-      if (i < 32) m_mine = s4.x;
-      lse_combine3(m, l, vr, om, s4.x, s4.y, 0.f, 0.f);
-      lse_combine(mc, sc, s4.z, s4.w);
-      lse_combine(mu, su, t2.x, t2.y);
-    }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      const float m2 = __shfl_xor_sync(kFull, m, off), l2 = __shfl_xor_sync(kFull, l, off);
-      const float c2 = __shfl_xor_sync(kFull, mc, off), s2 = __shfl_xor_sync(kFull, sc, off);
-      const float u2 = __shfl_xor_sync(kFull, mu, off), v2 = __shfl_xor_sync(kFull, su, off);
-      lse_combine3(m, l, vr, om, m2, l2, 0.f, 0.f);
-      lse_combine(mc, sc, c2, s2);
-      lse_combine(mu, su, u2, v2);
-    }
-  } else {  // extended meter: the value side's and the shapes' sums ride on l's weights
-    for (int i = lane; i < np; i += 32) {
-      const float4 s4 = *reinterpret_cast<const float4*>(stats(i));
-      const float4 t4 = *reinterpret_cast<const float4*>(stats(i) + 4);
+  for (int i = lane; i < np; i += 32) {
+    const float4 s4 = *reinterpret_cast<const float4*>(stats(i));
+    const float2 t2 = *reinterpret_cast<const float2*>(stats(i) + 4);
+    float r2 = 0.f, u2 = 0.f;
+    if (ext) {
+      const float2 q2 = *reinterpret_cast<const float2*>(stats(i) + 6);
       const float2 e2 = *reinterpret_cast<const float2*>(stats(i) + 8);
-      if (i < 32) m_mine = s4.x;
-      lse_combine3(m, l, vr, om, s4.x, s4.y, t4.z, e2.y);
-      lse_combine(mc, sc, s4.z, s4.w);
-      lse_combine(mu, su, t4.x, t4.y);
-      vmax = fmaxf(vmax, t4.w);
+      r2 = q2.x;
+      u2 = e2.y;
+      vmax = fmaxf(vmax, q2.y);
       cmax = fmaxf(cmax, e2.x);
     }
+    if (i < 32) m_mine = s4.x;
+    lse_combine3(m, l, vr, om, s4.x, s4.y, r2, u2);
+    lse_combine(mc, sc, s4.z, s4.w);
+    lse_combine(mu, su, t2.x, t2.y);
+  }
+  // the maxima over the lanes, then every lane's sums rescaled to them and added up
+  float gm = m, gc = mc, gu = mu;
 #pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      const float m2 = __shfl_xor_sync(kFull, m, off), l2 = __shfl_xor_sync(kFull, l, off);
-      const float r2 = __shfl_xor_sync(kFull, vr, off), x2 = __shfl_xor_sync(kFull, vmax, off);
-      const float o2 = __shfl_xor_sync(kFull, om, off), y2 = __shfl_xor_sync(kFull, cmax, off);
-      const float c2 = __shfl_xor_sync(kFull, mc, off), s2 = __shfl_xor_sync(kFull, sc, off);
-      const float u2 = __shfl_xor_sync(kFull, mu, off), v2 = __shfl_xor_sync(kFull, su, off);
-      lse_combine3(m, l, vr, om, m2, l2, r2, o2);
-      lse_combine(mc, sc, c2, s2);
-      lse_combine(mu, su, u2, v2);
-      vmax = fmaxf(vmax, x2);
-      cmax = fmaxf(cmax, y2);
+  for (int off = 16; off; off >>= 1) {
+    gm = fmaxf(gm, __shfl_xor_sync(kFull, gm, off));
+    gc = fmaxf(gc, __shfl_xor_sync(kFull, gc, off));
+    gu = fmaxf(gu, __shfl_xor_sync(kFull, gu, off));
+  }
+  {
+    const float wl = m == -INFINITY ? 0.f : ex2(m - gm);
+    const float wc = mc == -INFINITY ? 0.f : ex2(mc - gc);
+    const float wu = mu == -INFINITY ? 0.f : ex2(mu - gu);
+    l *= wl; vr *= wl; om *= wl; sc *= wc; su *= wu;
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    l += __shfl_xor_sync(kFull, l, off);
+    sc += __shfl_xor_sync(kFull, sc, off);
+    if (a.tier_b) su += __shfl_xor_sync(kFull, su, off);
+    if (ext) {
+      vr += __shfl_xor_sync(kFull, vr, off);
+      om += __shfl_xor_sync(kFull, om, off);
+      vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, off));
+      cmax = fmaxf(cmax, __shfl_xor_sync(kFull, cmax, off));
     }
   }
+  m = gm; mc = gc; mu = gu;
+  if (!a.tier_b) { mu = -INFINITY; su = 0.f; }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float wt_mine = m_mine == -INFINITY ? 0.f : ex2(m_mine - m);
 #pragma unroll
   for (int k = 0; k < kU; ++k) {
-    const float mk = __shfl_sync(kFull, m_mine, k);
-    if (k < np && mk != -INFINITY) {
-      const float wt = ex2(mk - m);
+    const float wt = __shfl_sync(kFull, wt_mine, k);
+    if (k < np && wt != 0.f) {
       acc.x += v[k].x * wt; acc.y += v[k].y * wt; acc.z += v[k].z * wt; acc.w += v[k].w * wt;
     }
   }
   for (int i = kU; i < np; ++i) {  // units split over more than kU warps (few, long sequences)
-    const float mi = stats(i)[0];
-    if (mi != -INFINITY) {
+    const float wt = i < 32 ? __shfl_sync(kFull, wt_mine, i) : [&] {
+      const float mi = stats(i)[0];
+      return mi == -INFINITY ? 0.f : ex2(mi - m);
+    }();
+    if (wt != 0.f) {
       const float4 vi = *reinterpret_cast<const float4*>(accp(i));
-      const float wt = ex2(mi - m);
       acc.x += vi.x * wt; acc.y += vi.y * wt; acc.z += vi.z * wt; acc.w += vi.w * wt;
     }
   }
@@ -373,6 +388,10 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   if (sms <= 0 || smem_max <= 0) return KVQ_ERR_CUDA;
   const WsLayout wl = ws_layout(batch, hkv, num_q_heads, sms * kMaxWarps);
   if (ws_bytes < wl.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  // page indices of the flattened (unit, page) space are 32-bit
+  if (static_cast<long long>(batch) * hkv * ((prefix && prefix_len > 0 ? (prefix_len + kPage - 1) / kPage : 0) +
+                                             static_cast<long long>(max_pages_per_seq)) > 0x7FFFFFFFll)
+    return KVQ_ERR_INVALID_ARG;
 
   const bool has_prefix = prefix && prefix_len > 0;
   const int pkf = has_prefix ? prefix->k_fmt : kNoPrefix;
