@@ -222,6 +222,9 @@ size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t nu
  *       ([W] Sec. 4.3 Prop. 1 and the det-tanh shape), NaN when KVQ_TIER_S is off.
  * workspace_dev / ws_bytes: scratch of at least kvq_decode_workspace_size().
  * An empty sequence (no prefix, seq_len 0) yields out = 0 and ln(A-1) = -inf.
+ * Returns KVQ_ERR_INVALID_ARG (nothing launched) when batch * num_kv_heads *
+ * (prefix pages + max_pages_per_seq) exceeds 2^31 - 1: pages of the call are
+ * indexed with 32-bit integers.
  */
 kvq_status kvq_decode_attn(const kvq_cache* cache, const kvq_cache* prefix, int32_t prefix_len,
                            const void* q_dev, int32_t q_dtype, int32_t batch, int32_t num_q_heads,

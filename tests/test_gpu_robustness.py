@@ -142,3 +142,27 @@ def test_bounded_wait_reports_timeout_and_context_survives(kvq):
     kvq.debug_encode(2, x, out)
     torch.cuda.synchronize()
     assert out.view(torch.float16).float().cpu().equal(x.cpu())
+
+
+def test_page_index_range_refused(kvq):
+    """Calls whose flattened (sequence, kv head, page) space would not fit 32-bit page indices are refused
+    on the host (KVQ_ERR_INVALID_ARG) before any launch; the block table is never read."""
+    import ctypes
+
+    dev = torch.device("cuda")
+    B, Hkv, Hq = 2, 8, 32
+    cache = kvq.PagedCache("bf16", "bf16", Hkv, 4, device=dev)
+    q = torch.zeros((B, Hq, 128), device=dev)
+    out = torch.empty((B, Hq, 128), device=dev)
+    bt = torch.zeros((B, 4), dtype=torch.int32, device=dev)
+    lens = torch.ones(B, dtype=torch.int32, device=dev)
+    ws = torch.empty(kvq.decode_workspace_size(B, Hkv, Hq), dtype=torch.uint8, device=dev)
+    d = cache.desc()
+    max_pages = (1 << 31) // (B * Hkv) + 1  # B * Hkv * max_pages > 2^31 - 1
+    rc = kvq.lib().kvq_decode_attn(ctypes.byref(d), None, 0, q.data_ptr(), 0, B, Hq, bt.data_ptr(), max_pages,
+                                   lens.data_ptr(), 1.0 / 128 ** 0.5, None, out.data_ptr(), None, ws.data_ptr(),
+                                   ws.numel(), None, None)
+    assert rc == 1  # KVQ_ERR_INVALID_ARG
+    # a normal call on the same buffers still runs
+    kvq.decode_attn(cache, q, bt, lens, out, ws)
+    torch.cuda.synchronize()
