@@ -15,6 +15,9 @@ Everything is float64 and follows WitCert (arXiv 2607.28699):
   varsigma_t^2 = (1/d) sum_c q_c^2 s_{c,t}^2 / 12, delta_loc = delta_req/(L*H*T);
   with one scale per (token, kv head) this is
   u_t = sm_scale * ||q|| * s_t * sqrt(2 ln(2S/delta_loc) / 12) (§6.2.2 hoists the sqrt).
+  This library's dither lies on a 1024-point grid (oracle.philox), so the rounding
+  error of each element has a mean of at most 2^-11 LSB; the radius adds that
+  deterministic part, sm_scale * s_t * ||q||_1 * 2^-11.
 * §4.3: meter = min(1, 1/2 (A^2 - 1)); the raw value (kept as a log score
   ln(1/2 (A^2 - 1))) is a risk score with no guarantee above 1.
 * "Compress the shared cartridge", "One kernel spans cartridge and live KV":
@@ -45,6 +48,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
+from .philox import subtractive_error_bias_bound
 from .quant import HEAD_DIM, N_BANDS
 
 __all__ = [
@@ -116,11 +120,21 @@ def tier_a_radius(q: np.ndarray, w: np.ndarray, sm_scale: float) -> np.ndarray:
 
 def tier_b_radius(q: np.ndarray, s_k: np.ndarray, sm_scale: float, seq_len: int,
                   delta_req: float, n_layers: int, n_q_heads: int, n_steps: int) -> np.ndarray:
-    """u_t = sm_scale ||q|| s_t sqrt(2 ln(2S/delta_loc)/12), delta_loc = delta_req/(L H T) (WitCert §4.2)."""
+    """Tier B radius of every token (WitCert §4.2), delta_loc = delta_req/(L H T):
+
+        u_t = sm_scale s_t (||q|| sqrt(2 ln(2S/delta_loc)/12) + ||q||_1 beta),  beta = 2^-11.
+
+    The first term is the page's sub-Gaussian radius (the hoisted square root of §6.2.2).  The
+    second covers the dither grid: with xi uniform on 1024 points instead of the continuum, each
+    element's rounding error has a mean of at most beta in LSB units (its centred part keeps the
+    variance proxy 1/12), so the error's mean contributes at most s_t ||q||_1 beta to eps_t.
+    """
     delta_loc = delta_req / (n_layers * n_q_heads * n_steps)
     kappa = math.sqrt(2.0 * math.log(2.0 * seq_len / delta_loc) / 12.0)
-    qn = float(np.sqrt(np.sum(np.asarray(q, dtype=np.float64) ** 2)))
-    return sm_scale * qn * kappa * np.asarray(s_k, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    qn = float(np.sqrt(np.sum(q ** 2)))
+    q1 = float(np.sum(np.abs(q)))
+    return sm_scale * (qn * kappa + q1 * subtractive_error_bias_bound()) * np.asarray(s_k, dtype=np.float64)
 
 
 FP16_REL = 2.0 ** -11   # |RN_fp16(x) - x| <= 2^-11 |RN_fp16(x)| for normal results ...

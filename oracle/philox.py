@@ -23,17 +23,29 @@ After every round the key is bumped by the two Weyl constants.  Ten rounds
 give Philox4x32-10.  The constants are the published ones: M0 = 0xD2511F53,
 M1 = 0xCD9E8D57, W0 = 0x9E3779B9 (golden ratio), W1 = 0xBB67AE85 (sqrt(3)-1).
 
-Dither contract (this library's reading; the pages fix only the tuple and
-the distribution):
+Dither contract (this library's reading; the pages fix only the tuple, the
+generator and the distribution):
 
     key     = (seed mod 2**32, seed >> 32)
-    counter = (slot, layer, kv_head, channel >> 2)
-    word    = output word (channel & 3) of that call
-    xi      = ((word >> 8) + 1/2) * 2**-24 - 1/2
+    counter = (slot, layer, kv_head, channel >> 3)
+    word    = output word ((channel >> 1) & 3) of that call
+    field   = bits 0..9 of the word for an even channel, bits 16..25 for an odd one
+    xi      = field * 2**-10 - 1/2
 
-so each call serves four consecutive channels, xi lies on the 2**24-point
-mid-point grid of (-1/2, 1/2) (symmetric, mean exactly 0, every value exact in
-binary32), and the key and value planes of a token share the same xi.
+so each call serves eight consecutive channels (two per output word; the pages
+reuse every output word of a call, here each word carries two dithers), xi is
+uniform on the 1024-point grid {-1/2, -1/2 + 2**-10, ..., 1/2 - 2**-10} of
+[-1/2, 1/2), every value is exact in fp16 (hence in binary32), and the key and
+value planes of a token share the same xi.  The grid is what makes the read
+side exact: xi + 3/2 = 1 + field * 2**-10 is the fp16 number whose mantissa is
+the field, so -xi = 3/2 - (that number) and the decode's fp16 tensor-core
+operands carry the write side's xi itself, not a rounding of it.  What the grid costs is stated by
+``subtractive_error_bias_bound``: for any input, the dithered rounding error
+rint(y + xi) - (y + xi) takes 1024 equally spaced values spanning one unit, so
+its mean lies within 2**-11 of 0 (a continuous uniform xi gives exactly 0), and
+its centred part is sub-Gaussian with variance proxy at most 1/12 (the moment
+generating function of an N-point centred grid, sinh(l/2) / (N sinh(l/(2N))),
+never exceeds the continuous one, sinh(l/2) / (l/2)).
 
 Parity status: pinned.  ``philox4x32_10`` agrees word for word with the CUDA
 toolkit's own Philox4x32-10 generator (cuRAND device API, four seeds, seven
@@ -45,13 +57,15 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["PHILOX_M0", "PHILOX_M1", "PHILOX_W0", "PHILOX_W1", "philox4x32_10", "dither"]
+__all__ = ["PHILOX_M0", "PHILOX_M1", "PHILOX_W0", "PHILOX_W1", "DITHER_BITS", "philox4x32_10", "dither",
+           "dither_fields", "subtractive_error_bias_bound"]
 
 PHILOX_M0 = 0xD2511F53
 PHILOX_M1 = 0xCD9E8D57
 PHILOX_W0 = 0x9E3779B9
 PHILOX_W1 = 0xBB67AE85
 _MASK = np.uint64(0xFFFFFFFF)
+DITHER_BITS = 10  # xi lies on a 2**DITHER_BITS-point grid
 
 
 def _mulhilo(m: int, x: np.ndarray):
@@ -88,14 +102,30 @@ def dither_words(seed: int, layer: int, kv_head, slot, channel):
     channel = np.asarray(channel, dtype=np.int64)
     kv_head = np.asarray(kv_head, dtype=np.uint64)
     slot, kv_head, channel = np.broadcast_arrays(slot, kv_head, channel)
-    words = philox4x32_10((slot, np.uint64(layer), kv_head, (channel >> 2).astype(np.uint64)), key)
-    lane = channel & 3
-    out = np.choose(lane, words)
+    words = philox4x32_10((slot, np.uint64(layer), kv_head, (channel >> 3).astype(np.uint64)), key)
+    out = np.choose((channel >> 1) & 3, words)
     return out.astype(np.uint64)
 
 
-def dither(seed: int, layer: int, kv_head, slot, channel) -> np.ndarray:
-    """Dither values xi in (-1/2, 1/2) for broadcastable (kv_head, slot, channel) arrays (float64, exact)."""
+def dither_fields(seed: int, layer: int, kv_head, slot, channel) -> np.ndarray:
+    """The 10-bit field of the Philox word that is the dither of (layer, kv_head, slot, channel)."""
+    channel = np.asarray(channel, dtype=np.int64)
     w = dither_words(seed, layer, kv_head, slot, channel)
-    n = (w >> np.uint64(8)).astype(np.float64)
-    return (n + 0.5) * 2.0 ** -24 - 0.5
+    shift = (np.broadcast_to(channel, w.shape) & 1).astype(np.uint64) * np.uint64(16)
+    return (w >> shift) & np.uint64((1 << DITHER_BITS) - 1)
+
+
+def dither(seed: int, layer: int, kv_head, slot, channel) -> np.ndarray:
+    """Dither values xi in [-1/2, 1/2) for broadcastable (kv_head, slot, channel) arrays (float64, exact)."""
+    k = dither_fields(seed, layer, kv_head, slot, channel).astype(np.float64)
+    return k * 2.0 ** -DITHER_BITS - 0.5
+
+
+def subtractive_error_bias_bound() -> float:
+    """Largest |E[rint(y + xi) - (y + xi)]| over inputs y when xi is uniform on the dither grid.
+
+    For fixed y the 2**DITHER_BITS values of y + xi are equally spaced by 2**-DITHER_BITS over one
+    unit, so the rounding errors are the same grid shifted into [-1/2, 1/2]; its mean is within
+    half a grid step of 0.
+    """
+    return 2.0 ** -(DITHER_BITS + 1)

@@ -9,7 +9,13 @@ missing key bump, a wrong output-word mapping) breaks:
 * the inverse uses the key schedule and multipliers in the opposite order, so
   a round written with swapped output words fails it;
 * uniformity, independence and avalanche statistics;
-* the dither values lie on the documented grid and are symmetric.
+* the dither values lie on the documented 1024-point grid, are exact in fp16,
+  come from the documented bit fields of the documented words, and are
+  uniform (chi-square) with the two fields of a word independent;
+* the subtractively dithered rounding error on that grid: its mean over the
+  grid is within 2^-11 of 0 for every input (exhaustive over the grid), and
+  its centred moment generating function stays below exp(l^2/24), the
+  variance proxy 1/12 that Tier B uses.
 """
 import numpy as np
 import pytest
@@ -110,14 +116,74 @@ def test_dither_grid_range_and_moments():
     ch = np.arange(128)[None, :]
     xi = P.dither(0xABCDEF0123, layer=5, kv_head=2, slot=slots, channel=ch)
     assert xi.shape == (20_000, 128)
-    assert np.all(xi > -0.5) and np.all(xi < 0.5)
-    n = (xi + 0.5) * 2**24 - 0.5
-    assert np.array_equal(n, np.round(n))          # on the mid-point grid
-    assert np.all(np.float32(xi) == xi)             # exact in binary32
-    assert abs(xi.mean()) < 3 * np.sqrt(1 / 12 / xi.size)
-    assert abs(xi.var() - 1 / 12) < 0.002
-    # the grid is symmetric: the extreme values are +-(1/2 - 2^-25)
-    assert (0.5 - 2**-25) in {abs(v) for v in (-0.5 + 2**-25, 0.5 - 2**-25)}
+    assert np.all(xi >= -0.5) and np.all(xi < 0.5)
+    n = (xi + 0.5) * 1024
+    assert np.array_equal(n, np.round(n))                        # on the 2^-10 grid
+    assert np.all(np.float16(xi).astype(np.float64) == xi)       # exact in fp16
+    # xi + 3/2 is the fp16 number 1 + field / 1024: its bit pattern is 0x3C00 | field
+    f = P.dither_fields(0xABCDEF0123, 5, 2, slots, ch)
+    assert np.array_equal(np.float16(xi + 1.5).view(np.uint16).astype(np.uint64), np.uint64(0x3C00) | f)
+    # grid mean -2^-11, variance (1 - 2^-20) / 12
+    assert abs(xi.mean() + 2**-11) < 3 * np.sqrt(1 / 12 / xi.size)
+    assert abs(xi.var() - (1 - 2**-20) / 12) < 0.002
+    counts = np.bincount(n.astype(np.int64).ravel(), minlength=1024)
+    expect = xi.size / 1024
+    chi2 = float(np.sum((counts - expect) ** 2 / expect))
+    assert chi2 < 1023 + 5 * np.sqrt(2 * 1023)                  # ~5 sigma of chi-square(1023)
+
+
+def test_dither_fields_of_one_word_are_independent():
+    slots = np.arange(200_000)
+    a = P.dither_fields(17, 3, 1, slots, 6)        # bits 0..9 of word 3 ...
+    b = P.dither_fields(17, 3, 1, slots, 7)        # ... and bits 16..25 of the same word
+    w = P.dither_words(17, 3, 1, slots, 6)
+    assert np.array_equal(a, w & np.uint64(0x3FF)) and np.array_equal(b, (w >> np.uint64(16)) & np.uint64(0x3FF))
+    joint = np.bincount(((a >> np.uint64(5)) * np.uint64(32) + (b >> np.uint64(5))).astype(np.int64), minlength=1024)
+    expect = slots.size / 1024
+    chi2 = float(np.sum((joint - expect) ** 2 / expect))
+    assert chi2 < 1023 + 5 * np.sqrt(2 * 1023)
+    assert abs(np.corrcoef(a.astype(np.float64), b.astype(np.float64))[0, 1]) < 0.01
+
+
+def _grid_errors(y):
+    """rint(fp32(y + xi)) - (y + xi) for every xi of the grid (float64, exact), y [..] fp32 -> [.., 1024]."""
+    xi = np.arange(1024) * 2.0**-10 - 0.5
+    y = np.asarray(y, dtype=np.float32).astype(np.float64)[..., None]
+    y2 = (y + xi).astype(np.float32).astype(np.float64)
+    return np.rint(y2) - (y + xi)
+
+
+def test_subtractive_error_bias_exhaustive_over_the_grid():
+    rng = np.random.default_rng(5)
+    ys = np.concatenate([
+        rng.uniform(-126.5, 126.5, 4000),
+        np.arange(-126.5, 127.0, 0.5),                            # half-integers and integers
+        np.arange(-4, 4, 2.0**-12),                               # inputs on and off the dither grid
+        np.array([0.0, 2.0**-30, -2.0**-30, 126.5, -126.5, 0.5 - 2.0**-11, 0.25 + 2.0**-13]),
+    ]).astype(np.float32)
+    e = _grid_errors(ys)
+    # subtractive dither: |error| <= 1/2 LSB, up to the binary32 rounding of y + xi
+    assert np.all(np.abs(e) <= 0.5 + 2.0**-24)
+    mu = e.mean(axis=-1)
+    bound = P.subtractive_error_bias_bound()
+    assert bound == 2.0**-11
+    assert np.max(np.abs(mu)) <= bound * (1 + 1e-9) + 2.0**-24   # within half a grid step
+    assert np.max(np.abs(mu)) > 0.9 * bound                      # and the bound is reached: the grid does bias
+    # the errors are the grid itself, shifted: sorted, consecutive gaps of 2^-10
+    gaps = np.diff(np.sort(e[: 4000], axis=-1), axis=-1)
+    assert np.allclose(gaps, 2.0**-10, rtol=0, atol=2.0**-20)
+
+
+def test_subtractive_error_centred_mgf_proxy():
+    rng = np.random.default_rng(6)
+    e = _grid_errors(rng.uniform(-126.5, 126.5, 500).astype(np.float32))
+    c = e - e.mean(axis=-1, keepdims=True)
+    for lam in (0.1, 1.0, 3.0, 8.0, 20.0):
+        mgf = np.exp(lam * c).mean(axis=-1)
+        assert np.all(mgf <= np.exp(lam * lam / 24) * (1 + 1e-12))
+        # and equals the closed form of the centred N-point grid, sinh(l/2) / (N sinh(l / 2N))
+        closed = np.sinh(lam / 2) / (1024 * np.sinh(lam / 2048))
+        assert np.allclose(mgf, closed, rtol=1e-9)
 
 
 def test_dither_stream_is_keyed_by_every_coordinate():
@@ -126,15 +192,19 @@ def test_dither_stream_is_keyed_by_every_coordinate():
     assert not np.array_equal(base, P.dither(99, 2, 0, np.arange(1000), 0))   # layer
     assert not np.array_equal(base, P.dither(99, 1, 1, np.arange(1000), 0))   # kv head
     assert not np.array_equal(base, P.dither(99, 1, 0, np.arange(1, 1001), 0))  # slot
-    # the four channels of one call come from the four output words, in order
+    # the eight channels of one call: channel c <- word c >> 1, bits 0..9 (c even) or 16..25 (c odd)
     w = P.philox4x32_10((np.arange(5, dtype=np.uint64), np.uint64(1), np.uint64(0), np.uint64(0)), (99, 0))
-    for c in range(4):
+    for c in range(8):
         xi = P.dither(99, 1, 0, np.arange(5), c)
-        assert np.array_equal(xi, ((w[c] >> np.uint64(8)).astype(np.float64) + 0.5) * 2**-24 - 0.5)
+        field = (w[c >> 1] >> np.uint64(16 * (c & 1))) & np.uint64(0x3FF)
+        assert np.array_equal(xi, field.astype(np.float64) / 1024 - 0.5)
+    # channel 8 starts the next call
+    w1 = P.philox4x32_10((np.arange(5, dtype=np.uint64), np.uint64(1), np.uint64(0), np.uint64(1)), (99, 0))
+    assert np.array_equal(P.dither(99, 1, 0, np.arange(5), 8), (w1[0] & np.uint64(0x3FF)).astype(np.float64) / 1024 - 0.5)
     # stream uniqueness: distinct (slot, layer, head, channel-group) tuples give distinct words
     slots = np.repeat(np.arange(64), 32 * 2)
     heads = np.tile(np.repeat(np.arange(2), 32), 64)
-    groups = np.tile(np.arange(32), 128)
+    groups = np.tile(np.arange(32), 128)   # (16 calls per row; any 32 distinct groups serve the check)
     words = P.philox4x32_10((slots.astype(np.uint64), np.uint64(3), heads.astype(np.uint64), groups.astype(np.uint64)), (5, 6))
     packed = set(zip(*(v.tolist() for v in words)))
     assert len(packed) == slots.size
