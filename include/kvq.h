@@ -176,8 +176,11 @@ size_t kvq_sizeof(int32_t which);
  *   INT8_DITHER: s = fp16_rn(fp32(amax / 126.5)), code = clamp(rint(fp32(fp32(x / s) + xi)), -127, 127)
  * (amax = 0 stores scale 0 and zero codes).  The dither xi comes from
  * Philox4x32-10 with key (seed low 32 bits, seed high 32 bits), counter
- * (slot, layer, kv_head, c >> 2), output word c & 3, xi = ((w >> 8) + 1/2) *
- * 2^-24 - 1/2; the K and V planes of a token share it ([W] Sec. 6.2.1, 6.2.3).
+ * (slot, layer, kv_head, c >> 3), output word (c >> 1) & 3, of which bits
+ * 0..9 (c even) or 16..25 (c odd) form the field f, xi = f * 2^-10 - 1/2: a
+ * 1024-point grid of [-1/2, 1/2) whose values are exact in fp16, so the
+ * decode's fp16 operands carry exactly the xi used here.  The K and V planes
+ * of a token share it ([W] Sec. 6.2.1, 6.2.3).
  * Device errors: KVQ_ERR_DEVICE_BOUNDS (slot beyond the cache; the token is
  * skipped), KVQ_ERR_NONFINITE_INPUT (non-finite input or fp16 scale overflow;
  * the token is written), KVQ_ERR_RANGE (a value scale above
@@ -213,8 +216,9 @@ size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t nu
  *   (KVQ_METER_STATE_FLOATS):
  *   [0] ln(A - 1) of Tier A, A = sum_t p~_t e^{c_t}, c_t = sm_scale *
  *       sum_b ||q_b|| w_{t,b} ([W] Thm. 1, Thm. 2); -inf when A = 1;
- *   [1] ln(A_B - 1) of Tier B, u_t = sm_scale ||q|| s_t sqrt(2 ln(2S/delta_loc)/12)
- *       ([W] Sec. 4.2), NaN when Tier B is off;
+ *   [1] ln(A_B - 1) of Tier B, u_t = sm_scale s_t (||q|| sqrt(2 ln(2S/delta_loc)/12)
+ *       + ||q||_1 2^-11) ([W] Sec. 4.2; the second term bounds the mean of the dithered
+ *       rounding error on the 1024-point dither grid), NaN when Tier B is off;
  *   [2] log-sum-exp of the compressed logits (natural log); [3] tokens attended S;
  *   [4] R = sum_t p~_t rho^v_t and [5] Vmax = max_t ||v_t|| from the value
  *       witness ([W] Sec. 3), NaN when KVQ_TIER_V is off (0 for an empty sequence);

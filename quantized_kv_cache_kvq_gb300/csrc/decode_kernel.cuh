@@ -393,6 +393,7 @@ struct QFrag {
   bool has_lo;
   float cm_scale;    // c_t = cm_scale * (W . QN)  (natural units)
   float alpha_b[2];  // Tier B: u_t = alpha_b[h] * s_t for heads 2c, 2c+1 (natural units)
+  float s_init[2];   // INT8 keys: 3/2 sum_c q_c (fp16 query as the key products use it), heads 2c, 2c+1
   // fixed-channel outlier bypass: B fragment of the bypassed channels (head g; fp16 hi / lo), and the
   // Tier B terms of heads 2c, 2c+1: u_t += beta_o[h] ||k_hat_{t,O}|| + gamma_o[h]
   uint32_t qo_hi[2], qo_lo[2];
@@ -472,6 +473,7 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
   };
   const bool fp32q = !a.q_bf16;
   bool any_lo = false;
+  float qsum = 0.f;  // sum of this lane's fp16 query channels (K8 family)
   auto put = [&](int kb, const float* x) {  // channels x[0..3] of k-step kb: b0 <- x0, x1; b1 <- x2, x3
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -486,6 +488,7 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
         f.hi[kb][h] = pack_f16(x0, x1);
         const float2 r = unpack_f16(f.hi[kb][h]);
         lo = pack_f16(x0 - r.x, x1 - r.y);
+        qsum += r.x + r.y;
       }
       if (fp32q) {
         f.lo[(kb * 2 + h) * 32 + lane] = lo;
@@ -523,6 +526,13 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     }
   }
   f.has_lo = __any_sync(kFull, any_lo);
+  {
+    // the key products of dithered INT8 pages multiply -(xi + 3/2) by the fp16 query, so their
+    // accumulator starts at 3/2 sum_c q_c (heads 2c and 2c + 1; the sum lives on the lanes of row g)
+    const float qs_g = row_sum4(qsum);
+    f.s_init[0] = 1.5f * __shfl_sync(kFull, qs_g, 8 * c);
+    f.s_init[1] = 1.5f * __shfl_sync(kFull, qs_g, 8 * c + 4);
+  }
   __syncwarp();
   if (METER) {
     // band b = 4c + i holds channels 16c + 4i + {0..3} and 64 + 16c + 4i + {0..3}
@@ -533,6 +543,7 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     load8(64 + 16 * c + 8, w1);
     float qn[4];
     float sq_all = 0.f, sq_int8 = 0.f;  // ||q||^2 and, with the bypass, its INT8-channel part
+    float l1 = 0.f;                      // ||q||_1 over the INT8 channels (Tier B's dither-grid term)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float* u = (i < 2) ? (u0 + 4 * i) : (u1 + 4 * (i - 2));
@@ -544,8 +555,10 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
         s = __fmaf_rn(w[e], w[e], s);
         if (OUTL) {
           const int bit = 4 * i + e;  // channel 16c + bit (u) and 64 + 16c + bit (w)
-          if (!((omask[0] >> bit) & 1u)) s8 = __fmaf_rn(u[e], u[e], s8);
-          if (!((omask[1] >> bit) & 1u)) s8 = __fmaf_rn(w[e], w[e], s8);
+          if (!((omask[0] >> bit) & 1u)) { s8 = __fmaf_rn(u[e], u[e], s8); l1 += fabsf(u[e]); }
+          if (!((omask[1] >> bit) & 1u)) { s8 = __fmaf_rn(w[e], w[e], s8); l1 += fabsf(w[e]); }
+        } else {
+          l1 += fabsf(u[e]) + fabsf(w[e]);
         }
       }
       qn[i] = sqrtf(s);
@@ -573,11 +586,14 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     f.cm_scale = a.sm_scale * ldexpf(1.f, e2);
     // ||q_g|| lives on the lanes of row g; the C fragment needs heads 2c and 2c+1
     // the dither term uses the query on the INT8 channels only (the bypassed ones leave the variance)
+    // u_t = sm_scale s_t (||q|| kappa + ||q||_1 2^-11): the sub-Gaussian radius of WitCert Sec. 4.2 plus
+    // the largest mean of the dithered rounding error on the 1024-point dither grid (2^-11 LSB)
     const float qnorm_g = sqrtf(row_sum4(OUTL ? sq_int8 : sq_all));
+    const float l1_g = row_sum4(l1);
     const float kappa = sqrtf(2.f * (logf(2.f * static_cast<float>(seq_total)) - a.ln_delta_loc) / 12.f);
-    const float q0 = __shfl_sync(kFull, qnorm_g, 8 * c), q1 = __shfl_sync(kFull, qnorm_g, 8 * c + 4);
-    f.alpha_b[0] = a.sm_scale * q0 * kappa;
-    f.alpha_b[1] = a.sm_scale * q1 * kappa;
+    const float b_g = __fmaf_rn(qnorm_g, kappa, l1_g * 0.00048828125f /* 2^-11 */);
+    f.alpha_b[0] = a.sm_scale * __shfl_sync(kFull, b_g, 8 * c);
+    f.alpha_b[1] = a.sm_scale * __shfl_sync(kFull, b_g, 8 * c + 4);
   }
   if (OUTL) {
     // bypassed channels: B fragment columns 2c, 2c + 1 (pair c) and, when m > 4, 2c + 8, 2c + 9 (pair c + 4)
@@ -686,6 +702,9 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       ph = philox_head(pl.layer, static_cast<uint32_t>(kvh), pl.rk0, pl.rk1);
       pt0 = philox_slot(phys * kPage + g, ph, pl.rk0, pl.rk1);
       pt1 = philox_slot(phys * kPage + g + 8, ph, pl.rk0, pl.rk1);
+      // the dither products below use -(xi + 3/2); the accumulator starts at 3/2 sum_c q_c to undo it
+      S[0] = S[2] = f.s_init[0];
+      S[1] = S[3] = f.s_init[1];
     }
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
@@ -693,6 +712,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       const uint4 k1 = lds128(st + L::kOff + ((2 + jj) * 32 + lane) * 16);
       const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
       const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
+      uint4 d0{}, d1{};  // Philox words of tokens g and g + 8, channels 64jj + 16c + 8(sidx >> 1) + {0..7}
 #pragma unroll
       for (int sidx = 0; sidx < 4; ++sidx) {
         uint32_t a0, a1, a2, a3;
@@ -708,20 +728,27 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         mma_f16_4(S, a0, a1, a2, a3, f.hi[kb][0], f.hi[kb][1]);
         if (f.has_lo) mma_f16_4(S, a0, a1, a2, a3, f.lo[(2 * kb) * 32 + lane], f.lo[(2 * kb + 1) * 32 + lane]);
         if (KDITHER) {
-          // subtract xi . q: the dither of tokens g and g + 8, channels 64jj + 16c + 4sidx + {0..3}
-          const uint32_t grp = 16 * jj + 4 * c + sidx;
-          const uint4 w0 = philox_finish(grp, pt0, ph, pl.rk0, pl.rk1);
-          const uint4 w1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
-          const uint32_t n00 = neg_dither_f16x2(w0.x, w0.y), n01 = neg_dither_f16x2(w0.z, w0.w);
-          const uint32_t n10 = neg_dither_f16x2(w1.x, w1.y), n11 = neg_dither_f16x2(w1.z, w1.w);
-          mma_f16_4(S, n00, n10, n01, n11, f.hi[kb][0], f.hi[kb][1]);
-          if (VDITHER) {
-            // stage minus the dither for the value side: token-major fp16 tile, 16-byte chunks xor-swizzled
-            const int ch = 64 * jj + 16 * c + 4 * sidx;
-            const int off = (((ch >> 3) ^ g) << 4) + (ch & 7) * 2;
-            *reinterpret_cast<uint2*>(xi_tile + g * 256 + off) = make_uint2(n00, n01);
-            *reinterpret_cast<uint2*>(xi_tile + (g + 8) * 256 + off) = make_uint2(n10, n11);
+          // one Philox call per token serves two k-steps: words x, y (channels +0..3) for even sidx,
+          // z, w (+4..7) for odd sidx; each word holds the dither of two channels (a0 / a2 pairs)
+          if ((sidx & 1) == 0) {
+            const uint32_t grp = 8 * jj + 2 * c + (sidx >> 1);
+            d0 = philox_finish(grp, pt0, ph, pl.rk0, pl.rk1);
+            d1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
+            if (VDITHER) {
+              // minus the dither for the value side: token-major fp16 tile, 16-byte chunks xor-swizzled by row
+              const int off = ((8 * jj + 2 * c + (sidx >> 1)) ^ g) << 4;
+              *reinterpret_cast<uint4*>(xi_tile + g * 256 + off) =
+                  make_uint4(neg_dither_f16x2(d0.x), neg_dither_f16x2(d0.y), neg_dither_f16x2(d0.z),
+                             neg_dither_f16x2(d0.w));
+              *reinterpret_cast<uint4*>(xi_tile + (g + 8) * 256 + off) =
+                  make_uint4(neg_dither_f16x2(d1.x), neg_dither_f16x2(d1.y), neg_dither_f16x2(d1.z),
+                             neg_dither_f16x2(d1.w));
+            }
           }
+          const uint32_t e0 = (sidx & 1) ? d0.z : d0.x, e2 = (sidx & 1) ? d0.w : d0.y;
+          const uint32_t e1 = (sidx & 1) ? d1.z : d1.x, e3 = (sidx & 1) ? d1.w : d1.y;
+          mma_f16_4(S, neg_shifted_dither_f16x2(e0), neg_shifted_dither_f16x2(e1), neg_shifted_dither_f16x2(e2),
+                    neg_shifted_dither_f16x2(e3), f.hi[kb][0], f.hi[kb][1]);
         }
       }
     }

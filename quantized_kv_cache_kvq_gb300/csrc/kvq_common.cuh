@@ -116,7 +116,7 @@ __device__ __forceinline__ uint4 philox4x32_10_rk(uint4 x, const uint32_t (&k0)[
 }
 
 // The decode regenerates, per page and lane, Philox4x32-10 of the counters (slot, layer, kv_head,
-// grp) for two slots and eight channel groups.  In the first three rounds several products depend
+// grp) for two slots and four groups of eight channels.  In the first three rounds several products depend
 // only on (layer, kv_head) or only on the slot; they are computed once (PhiloxHead per page,
 // PhiloxSlot per token) and each call finishes with two products in rounds 1-2 and seven full
 // rounds.  With (H, L) the high and low words of a product and y, z, w the counters after rounds
@@ -169,31 +169,39 @@ __device__ __forceinline__ uint4 philox_finish(uint32_t grp, const PhiloxSlot& t
   return x;
 }
 
-// Dither value of a Philox output word: ((w >> 8) + 1/2) * 2^-24 - 1/2, exact in binary32.
-__device__ __forceinline__ float dither_from_word(uint32_t w) {
-  return __fmaf_rn(static_cast<float>(w >> 8), 5.9604644775390625e-8f /* 2^-24 */,
-                   -0.49999997019767761f /* 2^-25 - 1/2 */);
+// Dither contract: the call (slot, layer, kv_head, channel >> 3) serves eight channels; output word
+// (channel >> 1) & 3 carries two of them, the even channel in bits 0..9 and the odd one in bits 16..25,
+// and xi = field * 2^-10 - 1/2 (a 1024-point grid of [-1/2, 1/2), every value exact in fp16).
+constexpr uint32_t kDitherFields = 0x03FF03FFu;
+
+// Dither of a 10-bit field: exact in binary32.
+__device__ __forceinline__ float dither_of_field(uint32_t field) {
+  return __fmaf_rn(static_cast<float>(field), 0.0009765625f /* 2^-10 */, -0.5f);
 }
 
-// Minus the dither of two words, rounded to an fp16 pair (low half from w0): the decode's tensor-core
-// operand.  The top 23 bits m = w >> 9 are placed in the mantissa of a float f = 1 + m 2^-23 (no
-// int-to-float conversion); 3/2 - f is exact and exceeds -xi = 1/2 - ((w >> 8) + 1/2) 2^-24 by
-// (bit 8 of w + 1/2) 2^-24 <= 1.5 * 2^-24, far below the fp16 rounding that follows.
-// Both subtractions run as one packed binary32 instruction (each lane rounded like the scalar one).
-__device__ __forceinline__ uint32_t neg_dither_f16x2(uint32_t w0, uint32_t w1) {
-  unsigned long long f, d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(f) : "r"((w0 >> 9) + 0x3F800000u), "r"((w1 >> 9) + 0x3F800000u));
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(0x3FC000003FC00000ull /* 1.5, 1.5 */), "l"(f));
-  uint32_t h;
-  asm("{\n\t.reg .f32 a, b;\n\tmov.b64 {a, b}, %1;\n\tcvt.rn.f16x2.f32 %0, b, a;\n\t}" : "=r"(h) : "l"(d));
-  return h;
+// The decode's key operand of a word: the fp16 pair -(xi + 3/2) = -(1 + field 2^-10) of its two
+// channels (low half: even channel), made by one logic operation -- the field is the mantissa, the
+// sign and exponent bits are those of -1.  The key products add 3/2 sum_c q_c back through the
+// accumulator's initial value.
+__device__ __forceinline__ uint32_t neg_shifted_dither_f16x2(uint32_t w) {
+  return (w & kDitherFields) | 0xBC00BC00u;
 }
 
-// The four dithers of channels 4*group .. 4*group+3 of (slot, layer, kv_head).
-__device__ __forceinline__ float4 dither4(uint32_t slot, uint32_t layer, uint32_t kv_head, uint32_t group,
+// Minus the dither of a word's two channels as an fp16 pair: -xi = 3/2 - (1 + field 2^-10), exact.
+__device__ __forceinline__ uint32_t neg_dither_f16x2(uint32_t w) {
+  const uint32_t m = neg_shifted_dither_f16x2(w);
+  const __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&m), __half2(__half(1.5f), __half(1.5f)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// The four dithers of channels 4*quad .. 4*quad+3 of (slot, layer, kv_head): half of the call
+// (slot, layer, kv_head, quad >> 1).
+__device__ __forceinline__ float4 dither4(uint32_t slot, uint32_t layer, uint32_t kv_head, uint32_t quad,
                                           uint32_t k0, uint32_t k1) {
-  const uint4 w = philox4x32_10(make_uint4(slot, layer, kv_head, group), k0, k1);
-  return make_float4(dither_from_word(w.x), dither_from_word(w.y), dither_from_word(w.z), dither_from_word(w.w));
+  const uint4 w = philox4x32_10(make_uint4(slot, layer, kv_head, quad >> 1), k0, k1);
+  const uint32_t a = (quad & 1u) ? w.z : w.x, b = (quad & 1u) ? w.w : w.y;
+  return make_float4(dither_of_field(a & 0x3FFu), dither_of_field((a >> 16) & 0x3FFu), dither_of_field(b & 0x3FFu),
+                     dither_of_field((b >> 16) & 0x3FFu));
 }
 
 // ---------------------------------------------------------------------------------------------
