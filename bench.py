@@ -59,9 +59,18 @@ def parse():
     p.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
     p.add_argument("--value-side", action="store_true",
                    help="meter the value side too (value witness read, output-error bound from kvq_meter)")
+    p.add_argument("--shapes", action="store_true",
+                   help="alternative bound shapes too (two-sided meter and det-tanh from kvq_meter)")
+    p.add_argument("--gate", action="store_true",
+                   help="gate support too: per-page contributions from kvq_decode_attn_ex and a kvq_gate plan per layer")
+    p.add_argument("--bypass", type=int, default=0, metavar="M",
+                   help="INT8 keys: M massive RoPE pairs per (layer, kv head) injected (x30) and kept in fp16 by the "
+                        "fixed-channel bypass")
     p.add_argument("--separate-append", action="store_true",
                    help="kvq_append + kvq_decode_attn per layer instead of the fused kvq_decode_attn_append")
     p.add_argument("--layers", type=int, default=0, help="override layer count (profiling only; not a bench line)")
+    p.add_argument("--batch", type=int, default=0,
+                   help="override the batch (the first sequences of the workload; profiling only, not a bench line)")
     p.add_argument("--resident-layers", type=int, default=0,
                    help="keep only this many layers' caches in HBM and run every layer call on cache l %% R "
                         "(for workloads whose caches exceed HBM; each call still streams a full layer)")
@@ -72,16 +81,17 @@ CODE_BYTES = {"bf16": 2, "e4m3": 1, "e4m3s": 1, "int8": 1}
 HAS_SCALE = {"bf16": 0, "e4m3": 0, "e4m3s": 1, "int8": 1}
 
 
-def token_head_bytes(k_fmt, v_fmt, meter=True, value_side=False) -> int:
+def token_head_bytes(k_fmt, v_fmt, meter=True, value_side=False, bypass=0) -> int:
     """Bytes one token of one kv head costs the decode: K and V codes, fp16 scales, 32-byte witness
-    (+ the 4-byte value witness with the value side of the output bound)."""
+    (+ the 4-byte value witness with the value side of the output bound, + the fp16 key outlier tile of
+    the fixed-channel bypass: 8 columns for up to 4 pairs, 16 for up to 8)."""
     return (128 * (CODE_BYTES[k_fmt] + CODE_BYTES[v_fmt]) + 2 * (HAS_SCALE[k_fmt] + HAS_SCALE[v_fmt]) + 32 * meter
-            + 4 * value_side)
+            + 4 * value_side + (0 if not bypass else 16 if bypass <= 4 else 32))
 
 
 def step_bytes(w, lens, value_side=False) -> int:
     """Algorithmic bytes of one decode step: live tokens once per (layer, kv head), the prefix once per layer."""
-    live = int(np.sum(lens)) * token_head_bytes(w.k_fmt, w.v_fmt, value_side=value_side)
+    live = int(np.sum(lens)) * token_head_bytes(w.k_fmt, w.v_fmt, value_side=value_side, bypass=w.bypass_pairs)
     pre = (w.prefix_len * token_head_bytes(w.prefix_k_fmt, w.prefix_v_fmt, value_side=value_side)
            if w.prefix_len else 0)
     return w.n_layers * w.n_kv_heads * (live + pre)
@@ -114,8 +124,12 @@ def issue_peak_winst_per_s(sm_mhz: float = GB300_MAX_SM_MHZ) -> float:
     return GB300_SMS * GB300_SCHEDULERS_PER_SM * sm_mhz * 1e6
 
 
-def traffic_record(workload: str):
+def traffic_record(workload: str, variant: bool = False):
+    """The ncu record of the plain decode kernel of a workload; none for variants (value side, bound
+    shapes, gate support, bypass: other kernel instances or extra outputs)."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if variant:
+        return None
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -188,9 +202,11 @@ class ClockSampler:
 class Model:
     """All layers' caches of one workload, filled through kvq_append, plus the step's buffers."""
 
-    def __init__(self, w, device, seed_base=0, n_layers=None, resident=0, value_side=False):
+    def __init__(self, w, device, seed_base=0, n_layers=None, resident=0, value_side=False, shapes=False,
+                 gate=False):
         self.separate_append = False
         self.value_side = value_side
+        self.gate = gate
         import torch
 
         import quantized_kv_cache_kvq_gb300 as kvq
@@ -218,8 +234,10 @@ class Model:
                            enumerate(self.lens)]).to(device)
         for l in range(self.R):
             g.manual_seed(W.unit_seed(w, 100_000 + 1000 * seed_base + l))
+            opairs = torch.from_numpy(W.bypass_pair_table(w, l)).to(device) if w.bypass_pairs else None
             c = kvq.PagedCache(w.k_fmt, w.v_fmt, Hkv, self.num_pages, layer=l,
-                               seed=(0x5EED << 20) + 97 * l + seed_base, value_witness=value_side)
+                               seed=(0x5EED << 20) + 97 * l + seed_base, value_witness=value_side,
+                               outlier_pairs=opairs)
             chunk = 1 << 18
             for a in range(0, total, chunk):
                 b = min(total, a + chunk)
@@ -249,8 +267,18 @@ class Model:
         self.ranking = (torch.empty((B, self.L * Hq), dtype=torch.int32, device=device)
                         if w.n_outliers else None)
         self.ws = torch.empty(kvq.decode_workspace_size(B, Hkv, Hq), dtype=torch.uint8, device=device)
-        tiers = kvq.TIER_A | (kvq.TIER_B if w.tier_b else 0) | (kvq.TIER_V if value_side else 0)
+        tiers = (kvq.TIER_A | (kvq.TIER_B if w.tier_b else 0) | (kvq.TIER_V if value_side else 0)
+                 | (kvq.TIER_S if shapes else 0))
         self.out_bound = torch.empty((self.L, B, Hq), device=device) if value_side else None
+        self.two_sided = torch.empty((self.L, B, Hq), device=device) if shapes else None
+        self.det_tanh = torch.empty((self.L, B, Hq), device=device) if shapes else None
+        # gate support: per-page log contributions to A - 1 of every (sequence, query head), and the greedy
+        # page-in plan's length per (layer, sequence, query head)
+        self.contrib = self.n_page_in = None
+        if gate:
+            stride = int(pages.max()) + (w.prefix_len + W.PAGE - 1) // W.PAGE
+            self.contrib = torch.empty((self.L, B, Hq, stride), device=device)
+            self.n_page_in = torch.empty((self.L, B, Hq), dtype=torch.int32, device=device)
         self.mp = kvq.meter_params(tiers, w.n_layers, Hq, w.n_steps, w.delta_req, w.tau)
         torch.cuda.synchronize()
         if self.err.item() != 0:
@@ -270,7 +298,10 @@ class Model:
             if events is not None:
                 events[l][0].record()
                 kvq.debug_time_decode(events[l][2], events[l][3])
-            if self.separate_append:
+            if self.gate:
+                kvq.decode_attn_ex(self.caches[c], q[l], self.bt, self.seq_lens, self.out[l], self.ws, k_new=k_new[l],
+                                   v_new=v_new[l], page_log_contrib=self.contrib[l], **kw)
+            elif self.separate_append:
                 kvq.decode_attn(self.caches[c], q[l], self.bt, self.seq_lens, self.out[l], self.ws, **kw)
             else:
                 kvq.decode_attn_append(self.caches[c], k_new[l], v_new[l], q[l], self.bt, self.seq_lens, self.out[l],
@@ -278,11 +309,15 @@ class Model:
             if events is not None:
                 events[l][1].record()
                 kvq.debug_time_decode(None, None)
+            if self.gate:
+                kvq.gate(self.contrib[l], self.state[l], self.seq_lens, w.prefix_len, w.tau, self.n_page_in[l])
         kvq.meter(self.state, self.L, w.batch, w.n_q_heads, self.mp, self.meter_a, self.raw_a, self.counts,
-                  cert_b=self.cert_b, ranking=self.ranking, out_bound=self.out_bound)
+                  cert_b=self.cert_b, ranking=self.ranking, out_bound=self.out_bound, two_sided=self.two_sided,
+                  det_tanh=self.det_tanh)
 
     def launches_per_step(self) -> int:
-        return self.L * (3 if self.separate_append else 2) + 1 + (1 if self.ranking is not None else 0)
+        return (self.L * (3 if self.separate_append else 2) + 1 + (1 if self.ranking is not None else 0)
+                + (self.L if self.gate else 0))
 
 
 def run_gpu(args, w):
@@ -303,7 +338,8 @@ def run_gpu(args, w):
     resident = args.resident_layers
     if not resident and w.name == "ragged_paged":
         resident = 4  # 36 layers of this workload need ~413 GB of cache: rotate 4 resident layers
-    m = Model(w, dev, seed_base=rank, n_layers=args.layers or None, resident=resident, value_side=args.value_side)
+    m = Model(w, dev, seed_base=rank, n_layers=args.layers or None, resident=resident, value_side=args.value_side,
+              shapes=args.shapes, gate=args.gate)
     m.separate_append = args.separate_append
     per_step_bytes = step_bytes(w, m.lens, value_side=args.value_side) * m.L // w.n_layers
 
@@ -364,7 +400,7 @@ def run_gpu(args, w):
     layer_bytes = per_step_bytes / m.L
     achieved = layer_bytes / (statistics.mean(layer_ms) * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    tr = traffic_record(w.name)
+    tr = traffic_record(w.name, variant=bool(args.value_side or args.shapes or args.gate or w.bypass_pairs))
     attended = float(np.sum(m.lens) + w.prefix_len * w.batch) * m.L * w.n_kv_heads
     res = dict(value=value, ms_step=ms_step, achieved=achieved, graph=graph is not None, layer_ms_mean=statistics.mean(layer_ms),
                call_ms_mean=statistics.mean(call_ms),
@@ -547,6 +583,12 @@ def workload_config(w):
 def main():
     args = parse()
     w = W.WORKLOADS[args.workload]
+    if args.bypass:
+        if w.k_fmt != "int8" or w.prefix_len:
+            raise SystemExit("--bypass needs a workload with INT8-dithered keys and no shared prefix")
+        w = W.reduced(w, massive_pairs=args.bypass, massive_scale=30.0, bypass_pairs=args.bypass)
+    if args.batch:
+        w = W.reduced(w, batch=args.batch)
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -564,12 +606,19 @@ def main():
             "launch_mode": "cuda_graph" if r["graph"] else "eager"}
     if args.value_side:
         line["config"]["meter"] += " + value side (output-error bound)"
+    if args.shapes:
+        line["config"]["meter"] += " + alternative bound shapes (two-sided, det-tanh)"
+    if args.gate:
+        line["config"]["meter"] += " + gate support (per-page contributions, greedy page-in plan per layer)"
+    if w.bypass_pairs:
+        line["config"]["layout"] += (f" + fixed-channel key bypass of {w.bypass_pairs} massive RoPE pairs "
+                                     f"(x{w.massive_scale:g}, fp16)")
     if r["resident"] < (args.layers or w.n_layers):
         line["config"]["resident_layers"] = r["resident"]
     if "e2e" in r:
         line["e2e"] = r["e2e"]
-    if args.layers:
-        line["note"] = f"profiling run with {args.layers} layers: not a bench line"
+    if args.layers or args.batch:
+        line["note"] = (f"profiling run with {args.layers or w.n_layers} layers, batch {w.batch}: not a bench line")
     if r["world"] == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line))

@@ -632,9 +632,11 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
 // 2c + (v & 1); x[v]: its logit (log2 units, -inf for padding); p[v] = 2^{x - mnew}.
 // Fast form (mc == m): sum += sum_v p (e^r - 1), rescaled with the softmax's alpha.
 // General form: own running max of x + r log2e, terms 2^{x + r log2e - max} (1 - e^{-r}).
-__device__ __forceinline__ void accumulate_meter(const float (&r)[4], const float (&x)[4], const float (&p)[4],
+// Returns true for the fast form, whose per-head terms of this lane's two tokens (p (e^r - 1) summed
+// over tokens g and g + 8, under the softmax max) go to `terms` when it is given.
+__device__ __forceinline__ bool accumulate_meter(const float (&r)[4], const float (&x)[4], const float (&p)[4],
                                                  const float (&alpha)[2], const float (&mnew)[2], float (&mc)[2],
-                                                 float (&sc)[2], bool& slow) {
+                                                 float (&sc)[2], bool& slow, float* terms = nullptr) {
   const float rmax = __uint_as_float(__reduce_max_sync(
       kFull, __float_as_uint(fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3])))));  // r >= 0: bit order = value order
   slow = slow || !(rmax <= kFastRadius);
@@ -646,7 +648,8 @@ __device__ __forceinline__ void accumulate_meter(const float (&r)[4], const floa
     f2_unpack(f2_fma(f2_pack(sc[0], sc[1]), f2_pack(alpha[0], alpha[1]), t), sc[0], sc[1]);
     mc[0] = mnew[0];
     mc[1] = mnew[1];
-    return;
+    if (terms) f2_unpack(t, terms[0], terms[1]);
+    return true;
   }
   float z[4];
 #pragma unroll
@@ -662,6 +665,7 @@ __device__ __forceinline__ void accumulate_meter(const float (&r)[4], const floa
       mc[h] = mc_new;
     }
   }
+  return false;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -855,7 +859,8 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     f2_unpack(f2_mul(f2_pack(C[2], C[3]), f2_splat(f.cm_scale)), cv[2], cv[3]);
 #pragma unroll
     for (int v = 0; v < 4; ++v) cv[v] = fmaxf(cv[v], 0.f);
-    accumulate_meter(cv, x, p, alpha, mnew, s.mc, s.sc, s.slow_a);
+    float pt[2];
+    const bool fast_a = accumulate_meter(cv, x, p, alpha, mnew, s.mc, s.sc, s.slow_a, cdst ? pt : nullptr);
     if (vstate && (ext & kExtShapes)) {
       // alternative shapes (WitCert Sec. 4.3 Prop. 1; det-tanh): max_t c_t and sum_t e^{x_t - m} (1 - e^{-c_t})
       float4 w4 = *reinterpret_cast<const float4*>(vstate + 8 * lane + 4);
@@ -865,8 +870,18 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       w4.w = __fmaf_rn(p[3], one_minus_exp_neg(cv[3]), __fmaf_rn(p[1], one_minus_exp_neg(cv[1]), w4.w * alpha[1]));
       *reinterpret_cast<float4*>(vstate + 8 * lane + 4) = w4;
     }
-    if (vstate && cdst) {
-      // gate support (WitCert Sec. 6.3.5): ln sum_{t in page} e^{x_t} (e^{c_t} - 1) for heads 2c, 2c + 1
+    if (vstate && cdst && fast_a) {
+      // gate support (WitCert Sec. 6.3.5): ln sum_{t in page} e^{x_t} (e^{c_t} - 1) for heads 2c, 2c + 1, from
+      // the fast meter form's terms 2^{x_t - m} (e^{c_t} - 1) (m: the softmax's running max, log2 units)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float sum = col_sum8(pt[h]);
+        const int head = 2 * (lane & 3) + h;
+        if ((lane >> 2) == 0 && head < G)
+          cdst[static_cast<size_t>(head) * cstride] = sum > 0.f ? logf(sum) + mnew[h] * kLn2 : -INFINITY;
+      }
+    } else if (vstate && cdst) {
+      // the same in the general form (a radius above the fast form's range): per-page log-sum-exp
       float t[4];
 #pragma unroll
       for (int v = 0; v < 4; ++v)

@@ -8,6 +8,8 @@
 // that is the output-error bound 2 meter Vmax + R.  Sec. 4.3 Prop. 1: TV <= 1/2 (A/A^- - A^-/A), and
 // neither this nor 1/2 (A^2 - 1) dominates, so the two-sided meter is the minimum; the det-tanh shape
 // TV <= tanh(max |eps|) uses the largest radius.
+#include <cmath>
+
 #include "kvq_common.cuh"
 
 namespace kvq {
@@ -113,23 +115,55 @@ __global__ void __launch_bounds__(512) rank_kernel(const float* __restrict__ raw
 
 constexpr int kMaxGatePages = 16384;
 
-// Greedy block page-in (WitCert Sec. 6.3.5): one block per (sequence, query head) cell.  The cell's
-// page contributions exp(lc - lse) are sorted in shared memory (bitonic; descending, ties to the lower
-// page index) and walked in double precision until A - 1 is at most sqrt(1 + 2 tau) - 1.
-__global__ void __launch_bounds__(512) gate_kernel(const float* __restrict__ lc, int stride,
-                                                   const float* __restrict__ state, int hq,
-                                                   const int32_t* __restrict__ seq_lens, int prefix_pages, float tau,
-                                                   int32_t* __restrict__ n_out, int32_t* __restrict__ list,
-                                                   int max_list) {
+// Float-float sums (an unevaluated pair hi + lo of binary32 numbers, Knuth's TwoSum): prefix sums of up to
+// 16384 contributions to ~2^-44 relative with FP32 arithmetic only (double precision is slow on this part).
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float e = ((a.hi - (s - bb)) + (b.hi - bb)) + (a.lo + b.lo);
+  const float h = s + e;
+  return FF{h, e - (h - s)};
+}
+
+// Greedy block page-in (WitCert Sec. 6.3.5): one block per (sequence, query head) cell.  A cell whose
+// meter is already within tau gets the empty plan at once.  The plan is the first k with
+// (A - 1) - S_k <= target = sqrt(1 + 2 tau) - 1, S_k the sum of the k largest page contributions
+// exp(lc - lse) (descending, ties to the lower page index; all P pages when no k reaches the target).
+// Short plans (the usual case) take the largest remaining page up to kGateQuick times by a block arg-max
+// and sum in float-float; longer ones (known as soon as the deficit exceeds the largest contribution
+// left times the rounds left) sort all pages in shared memory (bitonic) and scan the prefix sums
+// (per-thread chunks, then a block scan).
+constexpr int kGateThreads = 512;
+constexpr int kGateQuick = 16;
+__global__ void __launch_bounds__(kGateThreads) gate_kernel(const float* __restrict__ lc, int stride,
+                                                            const float* __restrict__ state, int hq,
+                                                            const int32_t* __restrict__ seq_lens, int prefix_pages,
+                                                            float target, int32_t* __restrict__ n_out,
+                                                            int32_t* __restrict__ list, int max_list) {
   extern __shared__ __align__(16) float key[];
+  __shared__ FF wsum[kGateThreads / 32];
+  __shared__ float wv[kGateThreads / 32];
+  __shared__ int wi[kGateThreads / 32], quick[kGateQuick];
+  __shared__ int k_shared;
   const int cell = blockIdx.x, seq = cell / hq;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int len = max(seq_lens[seq], 0);
   const int P = min(min(prefix_pages + (len + 15) / 16, kMaxGatePages), stride);  // never past the row
+  const float la = state[static_cast<size_t>(cell) * KVQ_METER_STATE_FLOATS];
+  const float am1 = la == -INFINITY ? 0.f : expf(la);
+  if (!(am1 > target) || P == 0) {  // already within tau (or nothing to page in): the empty plan
+    if (threadIdx.x == 0) n_out[cell] = 0;
+    if (list)
+      for (int i = threadIdx.x; i < max_list; i += blockDim.x) list[static_cast<size_t>(cell) * max_list + i] = -1;
+    return;
+  }
   int n2 = 1;
   while (n2 < P) n2 <<= 1;
   int* idx = reinterpret_cast<int*>(key + n2);
   const float lse = state[static_cast<size_t>(cell) * KVQ_METER_STATE_FLOATS + 2];
-  const float la = state[static_cast<size_t>(cell) * KVQ_METER_STATE_FLOATS];
   for (int i = threadIdx.x; i < n2; i += blockDim.x) {
     float k = -1.f;  // padding sorts last
     if (i < P) {
@@ -138,6 +172,53 @@ __global__ void __launch_bounds__(512) gate_kernel(const float* __restrict__ lc,
     }
     key[i] = k;
     idx[i] = i;
+  }
+  if (threadIdx.x == 0) k_shared = P;
+  __syncthreads();
+  {
+    // short plans: repeated arg-max over the pages not yet taken (each thread reads only its own pages)
+    FF S{0.f, 0.f};
+    for (int k = 0; k < min(P, kGateQuick); ++k) {
+      float bv = -1.f;
+      int bi = 0x7fffffff;
+      for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        const float v = key[i];
+        if (v > bv) { bv = v; bi = i; }  // ascending i: ties keep the lower index
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) { wv[warp] = bv; wi[warp] = bi; }
+      __syncthreads();
+      bv = wv[0];
+      bi = wi[0];
+      for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w)
+        if (wv[w] > bv || (wv[w] == bv && wi[w] < bi)) { bv = wv[w]; bi = wi[w]; }
+      __syncthreads();  // every warp has read wv / wi before the next round writes them
+      if (threadIdx.x == static_cast<unsigned>(bi) % blockDim.x) key[bi] = -1.f;  // taken (its owner's page)
+      if (threadIdx.x == 0) quick[k] = bi;
+      S = ff_add(S, FF{bv, 0.f});
+      if ((am1 - S.hi) - S.lo <= target || k + 1 == P) {  // uniform: every thread holds the same S
+        __syncthreads();
+        const int n = k + 1;
+        if (threadIdx.x == 0) n_out[cell] = n;
+        if (list)
+          for (int i = threadIdx.x; i < max_list; i += blockDim.x)
+            list[static_cast<size_t>(cell) * max_list + i] = i < n ? quick[i] : -1;
+        return;
+      }
+      // every page left contributes at most bv: when the deficit exceeds what the rounds left can remove,
+      // the plan is longer than kGateQuick pages; sort at once (the sort computes the same plan)
+      if ((am1 - S.hi) - S.lo - target > static_cast<float>(kGateQuick - k - 1) * bv) break;
+    }
+  }
+  // a longer plan: start again from all pages and sort them
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    const float v = lc[static_cast<size_t>(cell) * stride + i];
+    key[i] = v == -INFINITY ? 0.f : expf(v - lse);
   }
   __syncthreads();
   auto before = [&](int a, int b) { return key[a] > key[b] || (key[a] == key[b] && idx[a] < idx[b]); };
@@ -153,19 +234,32 @@ __global__ void __launch_bounds__(512) gate_kernel(const float* __restrict__ lc,
       __syncthreads();
     }
   }
-  __shared__ int k_shared;
-  if (threadIdx.x == 0) {
-    const double target = sqrt(1.0 + 2.0 * static_cast<double>(tau)) - 1.0;
-    double rest = la == -INFINITY ? 0.0 : exp(static_cast<double>(la));
-    int k = 0;
-    while (rest > target && k < P) rest -= static_cast<double>(key[k++]);
-    k_shared = k;
-    n_out[cell] = k;
+  // thread t owns sorted positions [b0, b1); its exclusive prefix comes from a block scan of chunk sums
+  const int per = (P + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(P, static_cast<int>(threadIdx.x) * per), b1 = min(P, b0 + per);
+  FF part{0.f, 0.f};
+  for (int i = b0; i < b1; ++i) part = ff_add(part, FF{key[i], 0.f});
+  FF incl = part;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const FF t{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+    if (lane >= o) incl = ff_add(t, incl);
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  FF S{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};  // lanes before this one
+  if (lane == 0) S = FF{0.f, 0.f};
+  for (int w = 0; w < warp; ++w) S = ff_add(wsum[w], S);
+  for (int k = b0; k < b1; ++k) {  // the first k (pages 0..k-1 taken) that reaches the target
+    if ((am1 - S.hi) - S.lo <= target) { atomicMin(&k_shared, k); break; }
+    S = ff_add(S, FF{key[k], 0.f});
   }
   __syncthreads();
+  const int k = k_shared;
+  if (threadIdx.x == 0) n_out[cell] = k;
   if (list)
     for (int i = threadIdx.x; i < max_list; i += blockDim.x)
-      list[static_cast<size_t>(cell) * max_list + i] = i < k_shared ? idx[i] : -1;
+      list[static_cast<size_t>(cell) * max_list + i] = i < k ? idx[i] : -1;
 }
 
 }  // namespace
@@ -180,15 +274,20 @@ extern "C" kvq_status kvq_gate(const float* lc, int32_t stride, const float* sta
   if (batch == 0) return KVQ_OK;
   if (!lc || !state || !seq_lens || !n_page_in || (page_list && max_list == 0)) return KVQ_ERR_INVALID_ARG;
   static int configured = 0;
-  const int smem = kMaxGatePages * 8;  // keys and indices
   if (!configured) {
-    if (cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxGatePages * 8) !=
+        cudaSuccess)
       return KVQ_ERR_CUDA;
     configured = 1;
   }
+  // keys and indices of the largest row a cell can have (a row holds at most `stride` pages)
+  int n2 = 1;
+  while (n2 < stride && n2 < kMaxGatePages) n2 <<= 1;
+  const int smem = n2 * 8;
   const int prefix_pages = (prefix_len + 15) / 16;
-  gate_kernel<<<static_cast<unsigned>(static_cast<long long>(batch) * hq), 512, smem,
-                reinterpret_cast<cudaStream_t>(stream)>>>(lc, stride, state, hq, seq_lens, prefix_pages, tau, n_page_in,
+  const float target = static_cast<float>(std::sqrt(1.0 + 2.0 * static_cast<double>(tau)) - 1.0);  // meter <= tau
+  gate_kernel<<<static_cast<unsigned>(static_cast<long long>(batch) * hq), kGateThreads, smem,
+                reinterpret_cast<cudaStream_t>(stream)>>>(lc, stride, state, hq, seq_lens, prefix_pages, target, n_page_in,
                                                            page_list, max_list);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

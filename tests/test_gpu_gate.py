@@ -145,3 +145,42 @@ def test_zero_witness_removes_the_page_contribution(kvq):
     for h in range(w.n_q_heads):
         drop = math.exp(b_lc[0, h, page] - b_ms[0, h, 2])
         assert math.exp(a_ms[0, h, 0]) == pytest.approx(math.exp(b_ms[0, h, 0]) - drop, rel=1e-4)
+
+
+def test_gate_plan_lengths_short_and_long(kvq):
+    # kvq_gate alone on synthetic contributions, with A - 1 placed so that the shortest greedy prefix has a
+    # chosen length per cell: 0 (already within tau), short plans, plans past the first 16 pages, and none
+    # reaching the target (all pages).  Some contributions are exact duplicates (equal inputs), which must
+    # come in page order.  Expected plans: the oracle's greedy page-in on the float64 contributions.
+    from oracle.meter import greedy_page_in
+
+    rng = np.random.default_rng(17)
+    B, Hq, P = 2, 8, 300
+    keys = rng.uniform(1.0, 3.0, size=(B, Hq, P))
+    keys[:, :, 40:60] = keys[:, :, 20:40]               # duplicates: pages 40..59 equal pages 20..39
+    lc = np.log(keys).astype(np.float32)
+    k64 = np.exp(lc.astype(np.float64))                  # the contributions the kernel sees (lse = 0)
+    tau = 1e-3
+    target = math.sqrt(1 + 2 * tau) - 1                  # far below every contribution: no boundary is close
+    want = [0, 1, 2, 3, 15, 16, 17, 40, 299, 300, 5, 16, 0, 33, 7, 300]
+    am1 = np.empty((B, Hq))
+    for cell, k in enumerate(want):
+        s, h = divmod(cell, Hq)
+        srt = np.sort(k64[s, h])[::-1]
+        am1[s, h] = (srt[:k].sum() + 0.5 * target) if k < P else srt.sum() + 2.0
+    state = np.zeros((B, Hq, 8), dtype=np.float32)
+    state[..., 0] = np.log(am1)
+    lens = torch.full((B,), P * 16, dtype=torch.int32, device="cuda")
+    n_in = torch.empty((B, Hq), dtype=torch.int32, device="cuda")
+    lst = torch.empty((B, Hq, 64), dtype=torch.int32, device="cuda")
+    kvq.gate(torch.from_numpy(lc).cuda(), torch.from_numpy(state).cuda(), lens, 0, tau, n_in, lst)
+    n_in, lst = n_in.cpu().numpy(), lst.cpu().numpy()
+    for cell, k in enumerate(want):
+        s, h = divmod(cell, Hq)
+        # A - 1 as the kernel reads it (binary32 state)
+        ref_k, ref_list = greedy_page_in(k64[s, h], float(np.exp(np.float64(state[s, h, 0]))), tau, max_pages=64)
+        assert ref_k == k
+        assert int(n_in[s, h]) == k, (cell, int(n_in[s, h]), k)
+        m = min(k, 64)
+        assert np.array_equal(lst[s, h, :m], ref_list[:m]), cell
+        assert np.all(lst[s, h, m:] == -1)
