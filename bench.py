@@ -621,6 +621,11 @@ def main():
         line["note"] = (f"profiling run with {args.layers or w.n_layers} layers, batch {w.batch}: not a bench line")
     if r["world"] == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
+        extra = [n for n, on in (("value side", args.value_side), ("bound shapes", args.shapes),
+                                 ("gate support", args.gate), ("outlier bypass", w.bypass_pairs)) if on]
+        if extra:
+            line["cpu_baseline"]["sample"] += (f"; the plain decode of this workload (the oracle sample leaves out the "
+                                               f"{', '.join(extra)} work of the GPU line)")
     print(json.dumps(line))
 
 
