@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const float* __restr
     if (i < P) {
       const float v = lc[static_cast<size_t>(cell) * stride + i];
       k = v == -INFINITY ? 0.f : expf(v - lse);
+      if (!(k >= 0.f)) k = 0.f;  // NaN (non-finite inputs, reported by the decode): no contribution
     }
     key[i] = k;
     idx[i] = i;
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const float* __restr
       for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w)
         if (wv[w] > bv || (wv[w] == bv && wi[w] < bi)) { bv = wv[w]; bi = wi[w]; }
       __syncthreads();  // every warp has read wv / wi before the next round writes them
+      if (bi >= P) break;  // no page left to take (cannot happen with finite keys): the sort path decides
       if (threadIdx.x == static_cast<unsigned>(bi) % blockDim.x) key[bi] = -1.f;  // taken (its owner's page)
       if (threadIdx.x == 0) quick[k] = bi;
       S = ff_add(S, FF{bv, 0.f});
@@ -218,7 +220,8 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(const float* __restr
   // a longer plan: start again from all pages and sort them
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
     const float v = lc[static_cast<size_t>(cell) * stride + i];
-    key[i] = v == -INFINITY ? 0.f : expf(v - lse);
+    const float k = v == -INFINITY ? 0.f : expf(v - lse);
+    key[i] = k >= 0.f ? k : 0.f;
   }
   __syncthreads();
   auto before = [&](int a, int b) { return key[a] > key[b] || (key[a] == key[b] && idx[a] < idx[b]); };

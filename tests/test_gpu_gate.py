@@ -184,3 +184,41 @@ def test_gate_plan_lengths_short_and_long(kvq):
         m = min(k, 64)
         assert np.array_equal(lst[s, h, :m], ref_list[:m]), cell
         assert np.all(lst[s, h, m:] == -1)
+
+
+def test_gate_plan_with_non_finite_contributions(kvq):
+    # a NaN contribution (from non-finite inputs, which the decode reports) counts as none; -inf is an
+    # empty page.  Cells: all NaN (no plan reaches the target: every page), half NaN, NaN next to -inf.
+    from oracle.meter import greedy_page_in
+
+    rng = np.random.default_rng(23)
+    B, Hq, P = 1, 4, 40
+    keys = rng.uniform(1.0, 3.0, size=(B, Hq, P))
+    lc = np.log(keys).astype(np.float32)
+    lc[0, 0, :] = np.nan
+    lc[0, 1, ::2] = np.nan
+    lc[0, 2, :5] = np.nan
+    lc[0, 2, 5:10] = -np.inf
+    k64 = np.exp(lc.astype(np.float64))
+    k64[~np.isfinite(k64)] = 0.0   # NaN -> none, exp(-inf) = 0 already
+    tau = 1e-3
+    target = math.sqrt(1 + 2 * tau) - 1
+    want = [P, 3, 4, 0]
+    am1 = np.empty((B, Hq))
+    for h, k in enumerate(want):
+        srt = np.sort(k64[0, h])[::-1]
+        am1[0, h] = (srt[:k].sum() + 0.5 * target) if h else 5.0
+    state = np.zeros((B, Hq, 8), dtype=np.float32)
+    state[..., 0] = np.log(am1)
+    lens = torch.full((B,), P * 16, dtype=torch.int32, device="cuda")
+    n_in = torch.empty((B, Hq), dtype=torch.int32, device="cuda")
+    lst = torch.empty((B, Hq, 64), dtype=torch.int32, device="cuda")
+    kvq.gate(torch.from_numpy(lc).cuda(), torch.from_numpy(state).cuda(), lens, 0, tau, n_in, lst)
+    torch.cuda.synchronize()
+    n_in, lst = n_in.cpu().numpy(), lst.cpu().numpy()
+    for h, k in enumerate(want):
+        ref_k, ref_list = greedy_page_in(k64[0, h], float(np.exp(np.float64(state[0, h, 0]))), tau, max_pages=64)
+        assert ref_k == k and int(n_in[0, h]) == k, (h, int(n_in[0, h]), k)
+        if h:  # with distinct finite keys the order is unique (the all-NaN cell ties every page)
+            assert np.array_equal(lst[0, h, :k], ref_list[:k])
+        assert np.all(lst[0, h, min(k, 64):] == -1)
