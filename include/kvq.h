@@ -303,6 +303,8 @@ kvq_status kvq_decode_attn_ex(const kvq_cache* cache, const void* k_new_dev, con
  * n_page_in_dev: [batch][num_q_heads] int32, the list's length (0 when the meter is already <= tau).
  * page_list_dev (nullable): [batch][num_q_heads][max_list] int32, the first min(n, max_list) pages of
  *   the list in order, -1 after them.
+ * A NaN contribution (non-finite inputs, which the decode reports in its error word) counts as none;
+ * a cell whose ln(A - 1) is NaN gets the empty plan.
  */
 kvq_status kvq_gate(const float* page_log_contrib_dev, int32_t contrib_stride, const float* meter_state_dev,
                     int32_t batch, int32_t num_q_heads, const int32_t* seq_lens_dev, int32_t prefix_len, float tau,

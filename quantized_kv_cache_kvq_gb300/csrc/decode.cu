@@ -198,7 +198,6 @@ using namespace kvq::dec;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 
 int device_sm_count() {
   static int cache[kMaxDevices] = {0};

@@ -1337,17 +1337,21 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
 namespace kvq {
 namespace dec {
 
-// Host launcher of one instantiation (the dynamic shared-memory limit is raised once per kernel).
+// Host launcher of one instantiation (the dynamic shared-memory limit is raised once per kernel and device:
+// the setting belongs to the device's context).
 // `programmatic`: launch as a programmatic dependent of the preceding grid in the stream (the
 // fused append), which the kernel waits for where it reads that grid's output.
 template <int KF, int VF, int PKF, int PVF, int NW, bool METER, bool VALUE, bool OUTL>
 cudaError_t launch_decode(const Args& a, int grid, size_t smem, cudaStream_t s, bool programmatic) {
   auto kern = decode_split_kernel<KF, VF, PKF, PVF, NW, METER, VALUE, OUTL>;
-  static size_t configured = 0;  // largest dynamic smem size set so far
-  if (smem > configured) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static size_t configured[kMaxDevices] = {};  // largest dynamic smem size set so far, per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || smem > configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    configured = smem;
+    if (dev >= 0 && dev < kMaxDevices) configured[dev] = smem;
   }
   if (!programmatic) {
     kern<<<grid, NW * 32, smem, s>>>(a);

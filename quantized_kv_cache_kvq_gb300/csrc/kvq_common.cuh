@@ -67,6 +67,9 @@ __host__ __device__ __forceinline__ int ko_offset(int t, int col, bool wide) {
 // value witness: k = 0 rho^v, k = 1 ||v||; lane g of the decode reads tokens g and g + 8 as one 8-byte word
 __host__ __device__ __forceinline__ int vw_offset(int t, int k) { return 8 * (t & 7) + 4 * k + 2 * (t >> 3); }
 
+// Devices a process can drive (per-device caches of attributes and of kernel settings).
+constexpr int kMaxDevices = 64;
+
 // ---------------------------------------------------------------------------------------------
 // Device error word: the first error code wins.
 __device__ __forceinline__ void report(int32_t* err, int code) {

@@ -276,12 +276,14 @@ extern "C" kvq_status kvq_gate(const float* lc, int32_t stride, const float* sta
   if (batch < 0 || hq <= 0 || prefix_len < 0 || stride <= 0 || !(tau >= 0.f) || max_list < 0) return KVQ_ERR_INVALID_ARG;
   if (batch == 0) return KVQ_OK;
   if (!lc || !state || !seq_lens || !n_page_in || (page_list && max_list == 0)) return KVQ_ERR_INVALID_ARG;
-  static int configured = 0;
-  if (!configured) {
+  static bool configured[kMaxDevices] = {};  // the limit is a setting of each device's context
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
     if (cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxGatePages * 8) !=
         cudaSuccess)
       return KVQ_ERR_CUDA;
-    configured = 1;
+    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
   }
   // keys and indices of the largest row a cell can have (a row holds at most `stride` pages)
   int n2 = 1;
