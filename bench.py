@@ -59,6 +59,9 @@ def parse():
     p.add_argument("--eager", action="store_true", help="launch the step eagerly instead of replaying a CUDA graph")
     p.add_argument("--value-side", action="store_true",
                    help="meter the value side too (value witness read, output-error bound from kvq_meter)")
+    p.add_argument("--meter-off", action="store_true",
+                   help="decode without the meter (no witness read, no kvq_meter): the meter's marginal cost, as "
+                        "time per step against the default")
     p.add_argument("--shapes", action="store_true",
                    help="alternative bound shapes too (two-sided meter and det-tanh from kvq_meter)")
     p.add_argument("--gate", action="store_true",
@@ -89,10 +92,11 @@ def token_head_bytes(k_fmt, v_fmt, meter=True, value_side=False, bypass=0) -> in
             + 4 * value_side + (0 if not bypass else 16 if bypass <= 4 else 32))
 
 
-def step_bytes(w, lens, value_side=False) -> int:
+def step_bytes(w, lens, value_side=False, meter=True) -> int:
     """Algorithmic bytes of one decode step: live tokens once per (layer, kv head), the prefix once per layer."""
-    live = int(np.sum(lens)) * token_head_bytes(w.k_fmt, w.v_fmt, value_side=value_side, bypass=w.bypass_pairs)
-    pre = (w.prefix_len * token_head_bytes(w.prefix_k_fmt, w.prefix_v_fmt, value_side=value_side)
+    live = int(np.sum(lens)) * token_head_bytes(w.k_fmt, w.v_fmt, meter=meter, value_side=value_side,
+                                                bypass=w.bypass_pairs)
+    pre = (w.prefix_len * token_head_bytes(w.prefix_k_fmt, w.prefix_v_fmt, meter=meter, value_side=value_side)
            if w.prefix_len else 0)
     return w.n_layers * w.n_kv_heads * (live + pre)
 
@@ -203,8 +207,9 @@ class Model:
     """All layers' caches of one workload, filled through kvq_append, plus the step's buffers."""
 
     def __init__(self, w, device, seed_base=0, n_layers=None, resident=0, value_side=False, shapes=False,
-                 gate=False):
+                 gate=False, meter=True):
         self.separate_append = False
+        self.meter_on = meter
         self.value_side = value_side
         self.gate = gate
         import torch
@@ -291,8 +296,9 @@ class Model:
         v_new = self.v_new if v_new is None else v_new
         for l in range(self.L):
             c = l % self.R
-            kw = dict(prefix=self.prefixes[c], prefix_len=w.prefix_len, sm_scale=SM_SCALE, meter=self.mp,
-                      meter_state=self.state[l], err=self.err)
+            kw = dict(prefix=self.prefixes[c], prefix_len=w.prefix_len, sm_scale=SM_SCALE,
+                      meter=self.mp if self.meter_on else None, meter_state=self.state[l] if self.meter_on else None,
+                      err=self.err)
             if self.separate_append:
                 kvq.append(self.caches[c], k_new[l], v_new[l], self.new_slots, self.err)
             if events is not None:
@@ -311,13 +317,15 @@ class Model:
                 kvq.debug_time_decode(None, None)
             if self.gate:
                 kvq.gate(self.contrib[l], self.state[l], self.seq_lens, w.prefix_len, w.tau, self.n_page_in[l])
+        if not self.meter_on:
+            return
         kvq.meter(self.state, self.L, w.batch, w.n_q_heads, self.mp, self.meter_a, self.raw_a, self.counts,
                   cert_b=self.cert_b, ranking=self.ranking, out_bound=self.out_bound, two_sided=self.two_sided,
                   det_tanh=self.det_tanh)
 
     def launches_per_step(self) -> int:
-        return (self.L * (3 if self.separate_append else 2) + 1 + (1 if self.ranking is not None else 0)
-                + (self.L if self.gate else 0))
+        meter = (1 + (1 if self.ranking is not None else 0)) if self.meter_on else 0
+        return self.L * (3 if self.separate_append else 2) + meter + (self.L if self.gate else 0)
 
 
 def run_gpu(args, w):
@@ -338,10 +346,12 @@ def run_gpu(args, w):
     resident = args.resident_layers
     if not resident and w.name == "ragged_paged":
         resident = 4  # 36 layers of this workload need ~413 GB of cache: rotate 4 resident layers
+    if args.meter_off and (args.value_side or args.shapes or args.gate):
+        raise SystemExit("--meter-off excludes the meter's extensions")
     m = Model(w, dev, seed_base=rank, n_layers=args.layers or None, resident=resident, value_side=args.value_side,
-              shapes=args.shapes, gate=args.gate)
+              shapes=args.shapes, gate=args.gate, meter=not args.meter_off)
     m.separate_append = args.separate_append
-    per_step_bytes = step_bytes(w, m.lens, value_side=args.value_side) * m.L // w.n_layers
+    per_step_bytes = step_bytes(w, m.lens, value_side=args.value_side, meter=not args.meter_off) * m.L // w.n_layers
 
     def barrier():
         if world > 1:
@@ -400,7 +410,8 @@ def run_gpu(args, w):
     layer_bytes = per_step_bytes / m.L
     achieved = layer_bytes / (statistics.mean(layer_ms) * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    tr = traffic_record(w.name, variant=bool(args.value_side or args.shapes or args.gate or w.bypass_pairs))
+    tr = traffic_record(w.name, variant=bool(args.value_side or args.shapes or args.gate or w.bypass_pairs
+                                             or args.meter_off))
     attended = float(np.sum(m.lens) + w.prefix_len * w.batch) * m.L * w.n_kv_heads
     res = dict(value=value, ms_step=ms_step, achieved=achieved, graph=graph is not None, layer_ms_mean=statistics.mean(layer_ms),
                call_ms_mean=statistics.mean(call_ms),
@@ -467,8 +478,9 @@ def run_e2e(args, m, per_step_bytes, world, use_graph=True):
         else:
             m.step(dq, dk, dv)
         ho.copy_(m.out, non_blocking=True)
-        hm.copy_(m.meter_a, non_blocking=True)
-        hc.copy_(m.counts, non_blocking=True)
+        if m.meter_on:
+            hm.copy_(m.meter_a, non_blocking=True)
+            hc.copy_(m.counts, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         one()
@@ -479,7 +491,7 @@ def run_e2e(args, m, per_step_bytes, world, use_graph=True):
         torch.cuda.current_stream().synchronize()  # the host reads the step's result
     el = (time.perf_counter() - t0) / args.steps
     h2d = (hq.numel() * hq.element_size() + hk.numel() * 4 + hv.numel() * 4)
-    d2h = ho.numel() * 4 + hm.numel() * 4 + 16
+    d2h = ho.numel() * 4 + ((hm.numel() * 4 + 16) if m.meter_on else 0)
     return {"value": per_step_bytes * world / el / 1e9, "unit": "GB/s", "ms_per_step": el * 1e3,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
@@ -604,6 +616,8 @@ def main():
             "roofline": roofline_of(r, w, args),
             "gpu_launches": r["launches"], "clocks": r["clocks"], "meter_counts": r["counts"],
             "launch_mode": "cuda_graph" if r["graph"] else "eager"}
+    if args.meter_off:
+        line["config"]["meter"] = "off (no witness read, no kvq_meter)"
     if args.value_side:
         line["config"]["meter"] += " + value side (output-error bound)"
     if args.shapes:
