@@ -190,6 +190,24 @@ kvq_status kvq_append(const kvq_cache* cache, const void* k_dev, const void* v_d
                       const int32_t* slot_mapping_dev, int32_t num_tokens, int32_t* err_word_dev,
                       kvq_stream_t stream);
 
+/*
+ * kvq_append_rope -- kvq_append of keys that arrive pre-RoPE: the rotary position embedding is applied
+ * on append ([W] Sec. 6.2.3 write path; [C] the cache keeps keys post-RoPE), and the rotated binary32
+ * key is the exact key of the witness.
+ * k_pre_dev: [num_tokens][num_kv_heads][128] pre-RoPE keys (in_dtype as for kvq_append).
+ * positions_dev: [num_tokens] int32 absolute position of each token.
+ * cos_sin_dev: [max_position][128] fp32, 16-byte aligned, caller-owned: at row p, cos(p theta_j) for
+ *   j = 0..63, then sin(p theta_j), theta_j = theta^(-2j/128) (the model's cos/sin cache).
+ * Half-split pairs (channel j with j + 64): x' = fl(fl(x c) - fl(y s)), y' = fl(fl(y c) + fl(x s)) in
+ * binary32, each product and sum rounded once (no fused multiply-add).
+ * Device errors: those of kvq_append, and KVQ_ERR_DEVICE_BOUNDS for a position outside
+ * [0, max_position) (the token is skipped).
+ */
+kvq_status kvq_append_rope(const kvq_cache* cache, const void* k_pre_dev, const void* v_dev, int32_t in_dtype,
+                           const int32_t* positions_dev, const float* cos_sin_dev, int32_t max_position,
+                           const int32_t* slot_mapping_dev, int32_t num_tokens, int32_t* err_word_dev,
+                           kvq_stream_t stream);
+
 /* Workspace bytes kvq_decode_attn needs for (batch, num_kv_heads, num_q_heads) on the current device. */
 size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t num_q_heads);
 

@@ -30,6 +30,7 @@ __all__ = [
     "decode_attn",
     "decode_attn_noalloc",
     "decode_workspace_size",
+    "append_rope",
     "meter",
     "debug_dither",
     "debug_encode",
@@ -119,6 +120,9 @@ def load(path: str = LIB_PATH):
     L.kvq_tile_bytes.argtypes = [c_int32, c_int32]
     L.kvq_append.restype = c_int32
     L.kvq_append.argtypes = [POINTER(_Cache), c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_void_p]
+    L.kvq_append_rope.restype = c_int32
+    L.kvq_append_rope.argtypes = [POINTER(_Cache), c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_void_p,
+                                  c_int32, c_void_p, c_void_p]
     L.kvq_decode_workspace_size.restype = c_size_t
     L.kvq_decode_workspace_size.argtypes = [c_int32, c_int32, c_int32]
     L.kvq_decode_attn.restype = c_int32
@@ -246,6 +250,21 @@ def append(cache: PagedCache, k: torch.Tensor, v: torch.Tensor, slot_mapping: to
     d = cache.desc()
     _check(lib().kvq_append(ctypes.byref(d), k.data_ptr(), v.data_ptr(), DTYPE[k.dtype], slot_mapping.data_ptr(),
                             int(k.shape[0]), _ptr(err), _stream(stream)), "kvq_append")
+
+
+def append_rope(cache: PagedCache, k_pre: torch.Tensor, v: torch.Tensor, positions: torch.Tensor,
+                cos_sin: torch.Tensor, slot_mapping: torch.Tensor, err: torch.Tensor | None = None, stream=None):
+    """kvq_append_rope: rotate the pre-RoPE keys k_pre [n, Hkv, 128] at ``positions`` [n] with the fp32 table
+    ``cos_sin`` [max_position, 128] (cos of the 64 pair angles, then their sin), then quantize as kvq_append."""
+    assert k_pre.is_contiguous() and v.is_contiguous() and k_pre.dtype == v.dtype and k_pre.shape == v.shape
+    assert slot_mapping.dtype == torch.int32 and slot_mapping.is_contiguous()
+    assert positions.dtype == torch.int32 and positions.is_contiguous() and positions.numel() == k_pre.shape[0]
+    assert cos_sin.dtype == torch.float32 and cos_sin.is_contiguous() and cos_sin.dim() == 2 and cos_sin.shape[1] == HEAD_DIM
+    d = cache.desc()
+    _check(lib().kvq_append_rope(ctypes.byref(d), k_pre.data_ptr(), v.data_ptr(), DTYPE[k_pre.dtype],
+                                 positions.data_ptr(), cos_sin.data_ptr(), int(cos_sin.shape[0]),
+                                 slot_mapping.data_ptr(), int(k_pre.shape[0]), _ptr(err), _stream(stream)),
+           "kvq_append_rope")
 
 
 def decode_workspace_size(batch: int, num_kv_heads: int, num_q_heads: int) -> int:

@@ -11,11 +11,35 @@
 namespace kvq {
 namespace {
 
-template <int KF, int VF>
+// RoPE-on-append (kvq_append_rope): the caller's binary32 cos/sin table and each token's position.
+struct RopeArgs {
+  const int32_t* positions;
+  const float* cos_sin;  // [max_pos][128]: cos of pairs 0..63, then their sin
+  int max_pos;
+};
+
+// Rotate this lane's four key channels (half-split pairs: channel j with j + 64, j = 0..63; lanes 0..15
+// hold channels 0..63, lanes 16..31 their partners).  Each channel is two rounded products and one
+// rounded sum, no fused multiply-add: x' = x c - y s, y' = y c + x s.
+__device__ __forceinline__ void rope_rotate4(float k[4], const float* row, int lane) {
+  const int j0 = 4 * (lane & 15);
+  const float4 cs = *reinterpret_cast<const float4*>(row + j0);
+  const float4 sn = *reinterpret_cast<const float4*>(row + kHeadDim / 2 + j0);
+  const float c[4] = {cs.x, cs.y, cs.z, cs.w}, s[4] = {sn.x, sn.y, sn.z, sn.w};
+  float partner[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) partner[e] = __shfl_xor_sync(0xffffffffu, k[e], 16);
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    k[e] = lane < 16 ? __fsub_rn(__fmul_rn(k[e], c[e]), __fmul_rn(partner[e], s[e]))
+                     : __fadd_rn(__fmul_rn(k[e], c[e]), __fmul_rn(partner[e], s[e]));
+}
+
+template <int KF, int VF, bool ROPE = false>
 __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __restrict__ kin,
                                                      const void* __restrict__ vin, int in_bf16,
                                                      const int32_t* __restrict__ slots, int num_tokens,
-                                                     int32_t* err) {
+                                                     int32_t* err, RopeArgs rope) {
   const int lane = threadIdx.x & 31;
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int H = c.num_kv_heads;
@@ -32,6 +56,14 @@ __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __
   }
   float k[4], v[4];
   load_row4(kin, vin, in_bf16, static_cast<size_t>(row) * kHeadDim + lane * 4, k, v);
+  if (ROPE) {  // the key arrives pre-RoPE: rotate it at the token's position (one position per warp)
+    const int pos = rope.positions[tok];
+    if (pos < 0 || pos >= rope.max_pos) {
+      if (lane == 0) report(err, KVQ_ERR_DEVICE_BOUNDS);
+      return;
+    }
+    rope_rotate4(k, rope.cos_sin + static_cast<size_t>(pos) * kHeadDim, lane);
+  }
   const RowCodes rc = quantize_row<KF, VF>(k, v, static_cast<uint32_t>(slot), static_cast<uint32_t>(c.layer),
                                            static_cast<uint32_t>(head), c.dither_seed, c.v_witness != nullptr,
                                            c.n_outlier_pairs > 0 ? c.outlier_pairs + head * c.n_outlier_pairs : nullptr,
@@ -111,17 +143,22 @@ struct NewestArgs {
 
 template <int KF, int VF>
 cudaError_t launch_append(const kvq_cache& c, const void* k, const void* v, int in_bf16, const int32_t* slots,
-                          int n, int32_t* err, cudaStream_t s) {
+                          int n, int32_t* err, cudaStream_t s, const RopeArgs* rope) {
   const long long rows = static_cast<long long>(n) * c.num_kv_heads;
   const int threads = 256;
   const long long blocks = (rows * 32 + threads - 1) / threads;
-  append_kernel<KF, VF><<<static_cast<unsigned>(blocks), threads, 0, s>>>(c, k, v, in_bf16, slots, n, err);
+  if (rope)
+    append_kernel<KF, VF, true><<<static_cast<unsigned>(blocks), threads, 0, s>>>(c, k, v, in_bf16, slots, n, err,
+                                                                                  *rope);
+  else
+    append_kernel<KF, VF, false><<<static_cast<unsigned>(blocks), threads, 0, s>>>(c, k, v, in_bf16, slots, n, err,
+                                                                                   RopeArgs{nullptr, nullptr, 0});
   return cudaGetLastError();
 }
 
 template <int KF, int VF>
 cudaError_t launch_any(const kvq_cache& c, const void* k, const void* v, int in_bf16, const int32_t* slots, int n,
-                       int32_t* err, cudaStream_t s, const NewestArgs* newest) {
+                       int32_t* err, cudaStream_t s, const NewestArgs* newest, const RopeArgs* rope) {
   const int threads = 256;
   if (newest) {
     const long long rows = static_cast<long long>(newest->batch) * c.num_kv_heads;
@@ -130,17 +167,17 @@ cudaError_t launch_any(const kvq_cache& c, const void* k, const void* v, int in_
         c, k, v, in_bf16, newest->block_table, newest->max_pages, newest->seq_lens, newest->batch, err);
     return cudaGetLastError();
   }
-  return launch_append<KF, VF>(c, k, v, in_bf16, slots, n, err, s);
+  return launch_append<KF, VF>(c, k, v, in_bf16, slots, n, err, s, rope);
 }
 
 template <int KF>
 cudaError_t dispatch_v(int vf, const kvq_cache& c, const void* k, const void* v, int b, const int32_t* sl, int n,
-                       int32_t* e, cudaStream_t s, const NewestArgs* nw = nullptr) {
+                       int32_t* e, cudaStream_t s, const NewestArgs* nw = nullptr, const RopeArgs* rp = nullptr) {
   switch (vf) {
-    case KVQ_FMT_BF16: return launch_any<KF, KVQ_FMT_BF16>(c, k, v, b, sl, n, e, s, nw);
-    case KVQ_FMT_E4M3: return launch_any<KF, KVQ_FMT_E4M3>(c, k, v, b, sl, n, e, s, nw);
-    case KVQ_FMT_E4M3_SCALED: return launch_any<KF, KVQ_FMT_E4M3_SCALED>(c, k, v, b, sl, n, e, s, nw);
-    case KVQ_FMT_INT8_DITHER: return launch_any<KF, KVQ_FMT_INT8_DITHER>(c, k, v, b, sl, n, e, s, nw);
+    case KVQ_FMT_BF16: return launch_any<KF, KVQ_FMT_BF16>(c, k, v, b, sl, n, e, s, nw, rp);
+    case KVQ_FMT_E4M3: return launch_any<KF, KVQ_FMT_E4M3>(c, k, v, b, sl, n, e, s, nw, rp);
+    case KVQ_FMT_E4M3_SCALED: return launch_any<KF, KVQ_FMT_E4M3_SCALED>(c, k, v, b, sl, n, e, s, nw, rp);
+    case KVQ_FMT_INT8_DITHER: return launch_any<KF, KVQ_FMT_INT8_DITHER>(c, k, v, b, sl, n, e, s, nw, rp);
   }
   return cudaErrorInvalidValue;
 }
@@ -219,9 +256,11 @@ extern "C" size_t kvq_sizeof(int32_t which) {
   return 0;
 }
 
-extern "C" kvq_status kvq_append(const kvq_cache* c, const void* k, const void* v, int32_t in_dtype,
-                                 const int32_t* slot_mapping, int32_t num_tokens, int32_t* err,
-                                 kvq_stream_t stream) {
+namespace {
+// The checks of kvq_append and kvq_append_rope, then the launch (rope: nullptr for post-RoPE keys).
+kvq_status append_impl(const kvq_cache* c, const void* k, const void* v, int32_t in_dtype,
+                       const int32_t* slot_mapping, int32_t num_tokens, int32_t* err, kvq_stream_t stream,
+                       const RopeArgs* rope) {
   if (!c || num_tokens < 0 || (in_dtype != KVQ_DTYPE_F32 && in_dtype != KVQ_DTYPE_BF16)) return KVQ_ERR_INVALID_ARG;
   if (c->k_fmt < 0 || c->k_fmt > 3 || c->v_fmt < 0 || c->v_fmt > 3) return KVQ_ERR_UNSUPPORTED_LAYOUT;
   if (c->num_kv_heads <= 0 || c->num_pages < 0 || c->reserved != 0) return KVQ_ERR_INVALID_ARG;
@@ -237,16 +276,44 @@ extern "C" kvq_status kvq_append(const kvq_cache* c, const void* k, const void* 
     if (c->k_fmt != KVQ_FMT_INT8_DITHER) return KVQ_ERR_UNSUPPORTED_LAYOUT;
     if (!c->outlier_pairs || !c->k_outlier || !aligned16(c->k_outlier)) return KVQ_ERR_INVALID_ARG;
   }
+  if (rope && (!rope->positions || !rope->cos_sin || !aligned16(rope->cos_sin) || rope->max_pos <= 0))
+    return KVQ_ERR_INVALID_ARG;
   const int in_bf16 = in_dtype == KVQ_DTYPE_BF16;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;
+  const NewestArgs* no_newest = nullptr;
   switch (c->k_fmt) {
-    case KVQ_FMT_BF16: e = dispatch_v<KVQ_FMT_BF16>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s); break;
-    case KVQ_FMT_E4M3: e = dispatch_v<KVQ_FMT_E4M3>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s); break;
-    case KVQ_FMT_E4M3_SCALED: e = dispatch_v<KVQ_FMT_E4M3_SCALED>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s); break;
-    case KVQ_FMT_INT8_DITHER: e = dispatch_v<KVQ_FMT_INT8_DITHER>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s); break;
+    case KVQ_FMT_BF16:
+      e = dispatch_v<KVQ_FMT_BF16>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s, no_newest, rope);
+      break;
+    case KVQ_FMT_E4M3:
+      e = dispatch_v<KVQ_FMT_E4M3>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s, no_newest, rope);
+      break;
+    case KVQ_FMT_E4M3_SCALED:
+      e = dispatch_v<KVQ_FMT_E4M3_SCALED>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s, no_newest,
+                                          rope);
+      break;
+    case KVQ_FMT_INT8_DITHER:
+      e = dispatch_v<KVQ_FMT_INT8_DITHER>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s, no_newest,
+                                          rope);
+      break;
   }
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" kvq_status kvq_append(const kvq_cache* c, const void* k, const void* v, int32_t in_dtype,
+                                 const int32_t* slot_mapping, int32_t num_tokens, int32_t* err,
+                                 kvq_stream_t stream) {
+  return append_impl(c, k, v, in_dtype, slot_mapping, num_tokens, err, stream, nullptr);
+}
+
+extern "C" kvq_status kvq_append_rope(const kvq_cache* c, const void* k_pre, const void* v, int32_t in_dtype,
+                                      const int32_t* positions, const float* cos_sin, int32_t max_position,
+                                      const int32_t* slot_mapping, int32_t num_tokens, int32_t* err,
+                                      kvq_stream_t stream) {
+  const RopeArgs rope{positions, cos_sin, max_position};
+  return append_impl(c, k_pre, v, in_dtype, slot_mapping, num_tokens, err, stream, &rope);
 }
 
 namespace kvq {
