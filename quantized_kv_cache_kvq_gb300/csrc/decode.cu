@@ -400,7 +400,6 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   const Pick pk = pick(cache->k_fmt, cache->v_fmt, pkf, pvf, meter, ext_meter, outl);
   if (!pk.launch) return KVQ_ERR_UNSUPPORTED_LAYOUT;
   const int nw = pk.warps;
-  const int w_max = sms * nw;
 
   Args a{};
   a.live = planes_of(cache);
@@ -433,7 +432,6 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   a.contrib_stride = contrib ? extras->contrib_stride : 0;
   a.ws_stats = reinterpret_cast<float*>(ws + wl.stats);
   a.ws_acc = reinterpret_cast<float*>(ws + wl.acc);
-  a.w_max = w_max;
   a.err = err_word;
 
   // stage size: the larger of the two segments' page footprints (16-byte multiple by construction)
@@ -443,14 +441,23 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   const int cum_bytes = ((batch + 1) * 4 + 127) & ~127;
   const int lo_bytes = q_dtype == KVQ_DTYPE_F32 ? kQloBytes : 0;
   const bool ext = ext_meter;  // the extended-meter kernel variant and its per-lane state
-  const int fixed = cum_bytes + nw * ((xi ? kXiScratch : 0) + lo_bytes + (ext ? kVStateBytes : 0) + kMaxStages * 8);
-  const int budget = smem_max - 1024 - fixed;
-  int stages = budget / (nw * sb);
-  if (stages > kMaxStages) stages = kMaxStages;
+  // warps that stream pages: the layout's warps per CTA, fewer when their two page stages do not fit shared
+  // memory (large pages with an fp32 query's low parts)
+  const int per_warp_fixed = (xi ? kXiScratch : 0) + lo_bytes + (ext ? kVStateBytes : 0) + kMaxStages * 8;
+  int nwa = nw, stages = 0;
+  for (; nwa >= 4; --nwa) {
+    stages = (smem_max - 1024 - cum_bytes - nwa * per_warp_fixed) / (nwa * sb);
+    if (stages >= 2) break;
+  }
   if (stages < 2) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  if (stages > kMaxStages) stages = kMaxStages;
+  const int w_max = sms * nwa;
+  a.w_max = w_max;
+  a.nwa = nwa;
   a.stages = stages;
   a.stage_bytes = sb;
-  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(nw) * stages * sb;
+  const int fixed = cum_bytes + nwa * per_warp_fixed;
+  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(nwa) * stages * sb;
 
   if (fused_append) {
     // the newest tokens first; the decode is a programmatic dependent of that grid and waits for it

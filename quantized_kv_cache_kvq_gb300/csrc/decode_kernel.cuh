@@ -84,6 +84,7 @@ struct Args {
   float* ws_stats;   // [slots][G][8]
   float* ws_acc;     // [slots][G][128]
   int w_max;
+  int nwa;           // warps per CTA that stream pages (<= NW: fewer when NW warps' stages do not fit shared memory)
   int stages;
   int stage_bytes;
   int32_t* err;
@@ -1200,7 +1201,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
 
   const long long T = static_cast<long long>(a.Hkv) * cum[a.B];
   const long long W = min(static_cast<long long>(a.w_max), T);
-  const int wid = blockIdx.x * NW + warp;
+  if (warp >= a.nwa) return;  // no block-wide barrier follows
+  const int wid = blockIdx.x * a.nwa + warp;
   if (wid >= W) return;
   const long long x_begin = T * wid / W, x_end = T * (wid + 1) / W;
   const int n = static_cast<int>(x_end - x_begin);

@@ -82,6 +82,11 @@ def test_fp32_query_path(kvq):
     inp = make_inputs(wi)
     gpu = run_case_gpu(wi, inputs=inp)
     _check(wi, gpu, reference_case(wi, inputs=inp))
+    # shared K16/V8 prefix + BF16 suffix: both segments' page bodies with the low-part products
+    wc = W.reduced(CASES["cartridge"], q_dtype="f32")
+    inp = make_inputs(wc)
+    gpu = run_case_gpu(wc, inputs=inp)
+    _check(wc, gpu, reference_case(wc, inputs=inp))
 
 
 def test_empty_and_single_token_sequences(kvq):
