@@ -128,6 +128,12 @@ def issue_peak_winst_per_s(sm_mhz: float = GB300_MAX_SM_MHZ) -> float:
     return GB300_SMS * GB300_SCHEDULERS_PER_SM * sm_mhz * 1e6
 
 
+def runs_a_variant(args, w) -> bool:
+    """True when a switch or the workload runs another decode instance than the plain one the ncu records
+    describe (value side, bound shapes, gate support, key outlier bypass, meter off)."""
+    return bool(args.value_side or args.shapes or args.gate or w.bypass_pairs or args.meter_off)
+
+
 def traffic_record(workload: str, variant: bool = False):
     """The ncu record of the plain decode kernel of a workload; none for variants (value side, bound
     shapes, gate support, bypass: other kernel instances or extra outputs)."""
@@ -410,8 +416,7 @@ def run_gpu(args, w):
     layer_bytes = per_step_bytes / m.L
     achieved = layer_bytes / (statistics.mean(layer_ms) * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
-    tr = traffic_record(w.name, variant=bool(args.value_side or args.shapes or args.gate or w.bypass_pairs
-                                             or args.meter_off))
+    tr = traffic_record(w.name, variant=runs_a_variant(args, w))
     attended = float(np.sum(m.lens) + w.prefix_len * w.batch) * m.L * w.n_kv_heads
     res = dict(value=value, ms_step=ms_step, achieved=achieved, graph=graph is not None, layer_ms_mean=statistics.mean(layer_ms),
                call_ms_mean=statistics.mean(call_ms),
