@@ -17,7 +17,9 @@ Everything is float64 and follows WitCert (arXiv 2607.28699):
   u_t = sm_scale * ||q|| * s_t * sqrt(2 ln(2S/delta_loc) / 12) (§6.2.2 hoists the sqrt).
   This library's dither lies on a 1024-point grid (oracle.philox), so the rounding
   error of each element has a mean of at most 2^-11 LSB; the radius adds that
-  deterministic part, sm_scale * s_t * ||q||_1 * 2^-11.
+  deterministic part, sm_scale * s_t * ||q||_1 * 2^-11.  With one scale per group of
+  G_c channels (§6.2.3), varsigma_t keeps the per-channel sum:
+  u_t = sm_scale (kappa sqrt(sum_g ||q_g||^2 s_{g,t}^2) + 2^-11 sum_g ||q_g||_1 s_{g,t}).
 * §4.3: meter = min(1, 1/2 (A^2 - 1)); the raw value (kept as a log score
   ln(1/2 (A^2 - 1))) is a risk score with no guarantee above 1.
 * "Compress the shared cartridge", "One kernel spans cartridge and live KV":
@@ -61,6 +63,7 @@ __all__ = [
     "tier_a_radius",
     "tier_b_radius",
     "tier_b_radius_bypass",
+    "tier_b_radius_groups",
     "log_a_minus_1",
     "meter_from_log_am1",
     "raw_log_score",
@@ -135,6 +138,27 @@ def tier_b_radius(q: np.ndarray, s_k: np.ndarray, sm_scale: float, seq_len: int,
     qn = float(np.sqrt(np.sum(q ** 2)))
     q1 = float(np.sum(np.abs(q)))
     return sm_scale * (qn * kappa + q1 * subtractive_error_bias_bound()) * np.asarray(s_k, dtype=np.float64)
+
+
+def tier_b_radius_groups(q: np.ndarray, s_kg: np.ndarray, sm_scale: float, seq_len: int,
+                         delta_req: float, n_layers: int, n_q_heads: int, n_steps: int) -> np.ndarray:
+    """Tier B radius with one key scale per token per channel group (WitCert §4.2 with the per-channel
+    scales of §6.2.3): s_kg [S, n_groups], group g = channels [g G_c, (g + 1) G_c), G_c = 128 / n_groups.
+
+        u_t = sm_scale (kappa sqrt(sum_c q_c^2 s_{g(c),t}^2) + 2^-11 sum_c |q_c| s_{g(c),t}),
+        kappa = sqrt(2 ln(2S/delta_loc) / 12),
+
+    the sub-Gaussian radius of sum_c q_c s_{g(c),t} (code_c - xi_c - x_c / s_{g(c),t}) (independent
+    per-channel errors with variance proxy s^2 / 12) plus the dither grid's bias bound per channel.
+    """
+    delta_loc = delta_req / (n_layers * n_q_heads * n_steps)
+    kappa = math.sqrt(2.0 * math.log(2.0 * seq_len / delta_loc) / 12.0)
+    s = np.asarray(s_kg, dtype=np.float64)
+    n_groups = s.shape[-1]
+    qg = np.asarray(q, dtype=np.float64).reshape(n_groups, HEAD_DIM // n_groups)
+    q2 = np.sum(qg * qg, axis=-1)          # ||q_g||^2
+    q1 = np.sum(np.abs(qg), axis=-1)       # ||q_g||_1
+    return sm_scale * (kappa * np.sqrt((s * s) @ q2) + subtractive_error_bias_bound() * (s @ q1))
 
 
 FP16_REL = 2.0 ** -11   # |RN_fp16(x) - x| <= 2^-11 |RN_fp16(x)| for normal results ...

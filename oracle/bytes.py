@@ -5,14 +5,18 @@
   without scales or metadata: BF16 K16/V16 144 KiB, K16/V8 and K8/V16 108 KiB,
   K8/V8 72 KiB; 12,628 tokens and a 632-position cartridge scale those linearly.
 * WitCert §4.1: the witness costs 2B = 32 bytes per token per kv head (B = 16, fp16).
-* WitCert §6.2.3: one fp16 scale per (token, kv head) per channel group.
+* WitCert §6.2.3: one fp16 scale per (token, kv head) per channel group.  Its Table 4
+  prices the scale granularities of 8-bit K and V per token per kv head against fp16
+  K+V (512 B): a 256-token block scale per channel, and per-token scales over groups
+  of 16, 32 or 128 (one scalar) channels; G_c = 32 stores 136 B per side.
 
 The decode path must read, per token and kv head: the key codes, the value
 codes, their scales when the format has one, and (meter on) the witness.
 """
 from __future__ import annotations
 
-__all__ = ["CODE_BYTES", "payload_bytes_per_token", "kv_bytes_per_token_head", "decode_step_bytes"]
+__all__ = ["CODE_BYTES", "payload_bytes_per_token", "kv_bytes_per_token_head", "decode_step_bytes",
+           "int8_side_bytes", "scale_granularity_saving"]
 
 CODE_BYTES = {"bf16": 2, "e4m3": 1, "e4m3s": 1, "int8": 1}
 HAS_SCALE = {"bf16": False, "e4m3": False, "e4m3s": True, "int8": True}
@@ -46,3 +50,20 @@ def decode_step_bytes(batch: int, n_layers: int, n_kv_heads: int, seq_lens, k_fm
         pp = kv_bytes_per_token_head(prefix_k_fmt, prefix_v_fmt, meter)
         total += n_layers * n_kv_heads * prefix_len * pp
     return total
+
+
+def int8_side_bytes(granularity: str, group: int = 32, block: int = 256, head_dim: int = 128) -> float:
+    """Bytes per token per kv head of one 8-bit side (K or V) with fp16 scales at a granularity:
+    'token' (one scale per group of ``group`` channels of the token; group = head_dim is one scalar)
+    or 'block' (one scale per channel shared by ``block`` tokens)."""
+    if granularity == "token":
+        assert head_dim % group == 0
+        return head_dim + SCALE_BYTES * (head_dim // group)
+    if granularity == "block":
+        return head_dim + SCALE_BYTES * head_dim / block
+    raise ValueError(granularity)
+
+
+def scale_granularity_saving(k_plus_v_bytes: float, head_dim: int = 128) -> float:
+    """Fraction of fp16 K+V (4 head_dim bytes per token per kv head) that a layout saves."""
+    return 1.0 - k_plus_v_bytes / (2 * 2 * head_dim)

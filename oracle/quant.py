@@ -18,7 +18,9 @@ Rules taken from the pages
   one it was rounded from.
 * WitCert §6.2.3: with token-granular paging the scale is per token (per
   channel group); the workloads here use one group of 128 channels per
-  (token, kv head).
+  (token, kv head).  ``quantize_int8_groups`` is the page's default granularity,
+  one fp16 scale per token per group of G_c = 32 channels (§6.2.3, Table 4);
+  each group follows the INT8 rules above with its own amax.
 * WitCert §4.1, eq. (2): the witness w_{t,b} = ||r_{t,b}|| is the Euclidean
   norm of the key residual r = k_hat - k over band b, stored in fp16.  Bands are
   B = 16 contiguous groups of RoPE frequency pairs (4 pairs = 8 coordinates each).
@@ -42,6 +44,9 @@ Readings where the pages are silent
 * The fp16 witness is rounded up, so it never under-states the residual norm.
 * FP8-scaled values use s = fp16_rn(fp32(amax / 448)) and code = e4m3(fp32(v / s))
   (round-to-nearest-even, saturating at +-448).
+* A channel group is G_c contiguous channels in storage order, group g = channels
+  [g G_c, (g + 1) G_c); with half-split RoPE a pair's two channels fall in groups
+  g and g + 64 / G_c.  The scales of a row are stored group by group.
 """
 from __future__ import annotations
 
@@ -69,6 +74,8 @@ __all__ = [
     "bypass_channels",
     "quantize_int8_bypass",
     "dequantize_int8_bypass",
+    "quantize_int8_groups",
+    "dequantize_int8_groups",
     "band_norms",
 ]
 
@@ -170,6 +177,38 @@ def dequantize_int8_bypass(codes, scale_bits, outlier_bits, xi, pairs) -> np.nda
     xh = dequantize(codes, scale_bits, "int8", xi)
     xh[..., bypass_channels(pairs)] = fp16_value(outlier_bits)
     return xh
+
+
+def quantize_int8_groups(x32: np.ndarray, xi: np.ndarray, group: int = 32):
+    """Subtractively dithered INT8 with one fp16 scale per token per group of ``group`` contiguous
+    channels (WitCert §6.2.3, Table 4: token x G_c-channel groups, G_c = 32 by default).
+
+    Every group is quantized as its own row: s_g = fp16_rn(fp32(amax_g / 126.5)), y = fp32(x / s_g),
+    y2 = fp32(y + xi), code = clamp(round_half_even(y2), -127, 127); a group whose scale is 0 stores
+    all-zero codes.  Returns ``(codes [..., 128] int8, scale_bits [..., 128 / group] uint16, valid [...])``,
+    ``valid`` False for a non-finite input or any group scale that overflows fp16.
+    """
+    x = np.asarray(x32, dtype=np.float32)
+    assert x.shape[-1] == HEAD_DIM and HEAD_DIM % group == 0 and xi.shape == x.shape
+    n_groups = HEAD_DIM // group
+    xg = x.reshape(x.shape[:-1] + (n_groups, group))
+    finite = np.all(np.isfinite(x), axis=-1)
+    s_bits = _scale_bits(np.max(np.abs(xg), axis=-1), INT8_DIVISOR)
+    s = fp16_value(s_bits)
+    valid = finite & np.all(np.isfinite(s), axis=-1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = f32(xg.astype(np.float64) / s[..., None])
+        y2 = f32(y.astype(np.float64) + np.asarray(xi, dtype=np.float64).reshape(xg.shape))
+        code = np.clip(np.rint(y2.astype(np.float64)), -INT8_QMAX, INT8_QMAX)
+    code = np.where((s == 0)[..., None] | ~np.isfinite(code), 0, code)
+    return code.reshape(x.shape).astype(np.int8), s_bits, valid
+
+
+def dequantize_int8_groups(codes: np.ndarray, scale_bits: np.ndarray, xi: np.ndarray) -> np.ndarray:
+    """x_hat_c = s_{g(c)} (code_c - xi_c), g(c) = c // G_c with G_c = 128 / scale_bits.shape[-1] (exact)."""
+    group = HEAD_DIM // scale_bits.shape[-1]
+    s = np.repeat(fp16_value(scale_bits), group, axis=-1)
+    return s * (np.asarray(codes).astype(np.float64) - np.asarray(xi, dtype=np.float64))
 
 
 def dequantize(codes: np.ndarray, scale_bits: np.ndarray | None, fmt: str, xi: np.ndarray | None = None):
