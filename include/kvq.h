@@ -63,7 +63,11 @@ typedef enum kvq_fmt {
   KVQ_FMT_BF16 = 0,        /* bfloat16, round-to-nearest-even; no scale                                  */
   KVQ_FMT_E4M3 = 1,        /* FP8 E4M3 raw cast, round-to-nearest-even, saturating at +-448; no scale     */
   KVQ_FMT_E4M3_SCALED = 2, /* FP8 E4M3 of x / s, s = fp16(amax / 448) per (token, kv head)               */
-  KVQ_FMT_INT8_DITHER = 3  /* subtractively dithered INT8: code = rint(x/s + xi), s = fp16(amax / 126.5) */
+  KVQ_FMT_INT8_DITHER = 3, /* subtractively dithered INT8: code = rint(x/s + xi), s = fp16(amax / 126.5) */
+  KVQ_FMT_INT8_DITHER_G32 = 4 /* the same with one scale per token per group of 32 channels: channels
+                                 32g..32g+31 use s_g = fp16(amax_g / 126.5) ([W] Sec. 6.2.3, Table 4,
+                                 G_c = 32); keys and values of one cache both in this format, no prefix,
+                                 no key outlier bypass */
 } kvq_fmt;
 
 /* Element type of the key / value / query inputs. */
@@ -87,11 +91,16 @@ typedef enum kvq_dtype { KVQ_DTYPE_F32 = 0, KVQ_DTYPE_BF16 = 1 } kvq_dtype;
  * shared-memory loads):
  *   K, 16-bit (4096 B):  16*(((t>>3)*4 + (c>>5))*32 + (t&7)*4 + ((c>>3)&3)) + 2*(c&7)
  *   K,  8-bit (2048 B):  16*(((t>>3)*2 + (c>>6))*32 + (t&7)*4 + ((c>>4)&3)) + (c&15)
+ *   K,  8-bit, 32-channel scale groups (2048 B; every tensor-core k-step inside one group):
+ *                        16*(((t>>3)*2 + (c>>6))*32 + (t&7)*4 + ((c>>3)&3))
+ *                        + 4*(2*((c>>5)&1) + ((c>>2)&1)) + (c&3)
  *   V, 16-bit (4096 B):  16*(32*(c>>4) + 4*(c&7) + ((t&7)>>1)) + 4*(2*(t>>3) + ((c>>3)&1)) + 2*(t&1)
  *   V,  8-bit (2048 B):  16*(32*(c>>5) + 4*(c&7) + ((t&7)>>1)) + 8*((c>>4)&1)
  *                        + 2*(2*(t>>3) + ((c>>3)&1)) + (t&1)
  *   witness (512 B, fp16 bits):  16*(4*(t&7) + (b>>2)) + 8*(t>>3) + 2*(b&3)
  *   scale   (32 B,  fp16 bits):  2*(2*(t&7) + (t>>3))
+ *   scale, 32-channel groups (128 B, fp16 bits; group g = channels 32g..32g+31):
+ *                        16*(t&7) + 4*g + 2*(t>>3)
  *   value witness (64 B, fp16 bits):  8*(t&7) + 4*k + 2*(t>>3), k = 0: rho^v_t =
  *                        ||v_hat_t - v_t||, k = 1: ||v_t|| (both rounded up; [W] Sec. 3,
  *                        the output bound ||y - y_hat|| <= 2 TV max_t ||v_t|| + sum_t p~_t rho^v_t)

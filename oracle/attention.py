@@ -234,7 +234,8 @@ def decode_head(q: np.ndarray, k_exact: np.ndarray, k_hat: np.ndarray, v_hat: np
 
     q [H, 128] (the query values exactly as the kernel reads them), k_exact
     [S, 128] (the binary32 post-RoPE keys), k_hat / v_hat [S, 128] (exact
-    dequantized cache), w [S, 16] (witness values), s_k [S] (key scales, Tier B),
+    dequantized cache), w [S, 16] (witness values), s_k [S] (key scales, Tier B; [S, n_groups] for
+    one scale per token per channel group, WitCert §6.2.3),
     tier_b = dict(delta_req, n_layers, n_q_heads, n_steps) or None, vw [S, 2] (value witness
     values: rho^v, ||v||) or None, v_exact [S, 128] (the binary32 values) or None, bypass =
     dict(channels [2m], values [S, 2m]) for keys stored with the fixed-channel outlier bypass (Tier B).
@@ -262,6 +263,8 @@ def decode_head(q: np.ndarray, k_exact: np.ndarray, k_hat: np.ndarray, v_hat: np
         if tier_b is not None:
             if bypass is not None:
                 u = tier_b_radius_bypass(q[h], s_k, bypass["values"], bypass["channels"], sm_scale, S, **tier_b)
+            elif np.ndim(s_k) == 2:
+                u = tier_b_radius_groups(q[h], s_k, sm_scale, S, **tier_b)
             else:
                 u = tier_b_radius(q[h], s_k, sm_scale, S, **tier_b)
             lb[h] = log_a_minus_1(log_pt[h], u)

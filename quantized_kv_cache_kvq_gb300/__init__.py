@@ -42,7 +42,8 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("KVQ_LIB") or os.path.join(_HERE, "libkvq.so")
 
-FMT = {"bf16": 0, "e4m3": 1, "e4m3s": 2, "int8": 3}
+FMT = {"bf16": 0, "e4m3": 1, "e4m3s": 2, "int8": 3, "int8g32": 4}
+SCALE_TILE_BYTES = {"e4m3s": 32, "int8": 32, "int8g32": 128}  # fp16 scales of a page's 16 tokens
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 TIER_A, TIER_B, TIER_V, TIER_S = 1, 2, 4, 8
 METER_STATE_FLOATS = 8  # floats per (sequence, query head) cell of meter_state
@@ -214,8 +215,8 @@ class PagedCache:
         z = dict(dtype=torch.uint8, device=device)
         self.k = torch.zeros((n, kb), **z)
         self.v = torch.zeros((n, vb), **z)
-        self.k_scale = torch.zeros((n, 32), **z) if k_fmt in ("e4m3s", "int8") else None
-        self.v_scale = torch.zeros((n, 32), **z) if v_fmt in ("e4m3s", "int8") else None
+        self.k_scale = torch.zeros((n, SCALE_TILE_BYTES[k_fmt]), **z) if k_fmt in SCALE_TILE_BYTES else None
+        self.v_scale = torch.zeros((n, SCALE_TILE_BYTES[v_fmt]), **z) if v_fmt in SCALE_TILE_BYTES else None
         self.witness = torch.zeros((n, 512), **z) if witness else None
         self.v_witness = torch.zeros((n, 64), **z) if value_witness else None
         # fixed-channel key outlier bypass: [num_kv_heads, m] int32 RoPE pairs (INT8-dithered keys)

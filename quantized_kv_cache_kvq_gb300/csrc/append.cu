@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __
   const size_t stile = static_cast<size_t>(head) * c.num_pages + page;  // scale planes are head-major
   store_row<KF, VF>(rc, t, static_cast<uint8_t*>(c.k_data) + tile * tile_bytes_k(KF),
                     static_cast<uint8_t*>(c.v_data) + tile * tile_bytes_v(VF),
-                    fmt_has_scale(KF) ? reinterpret_cast<uint8_t*>(c.k_scale) + stile * kTileBytesS : nullptr,
-                    fmt_has_scale(VF) ? reinterpret_cast<uint8_t*>(c.v_scale) + stile * kTileBytesS : nullptr,
+                    fmt_has_scale(KF) ? reinterpret_cast<uint8_t*>(c.k_scale) + stile * tile_bytes_s(KF) : nullptr,
+                    fmt_has_scale(VF) ? reinterpret_cast<uint8_t*>(c.v_scale) + stile * tile_bytes_s(VF) : nullptr,
                     reinterpret_cast<uint8_t*>(c.witness) + tile * kTileBytesW,
                     c.v_witness ? reinterpret_cast<uint8_t*>(c.v_witness) + stile * kTileBytesVW : nullptr,
                     c.n_outlier_pairs > 0
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(256) append_newest_kernel(kvq_cache c, const v
   const size_t stile = static_cast<size_t>(head) * c.num_pages + page;
   store_row<KF, VF>(rc, t, static_cast<uint8_t*>(c.k_data) + tile * tile_bytes_k(KF),
                     static_cast<uint8_t*>(c.v_data) + tile * tile_bytes_v(VF),
-                    fmt_has_scale(KF) ? reinterpret_cast<uint8_t*>(c.k_scale) + stile * kTileBytesS : nullptr,
-                    fmt_has_scale(VF) ? reinterpret_cast<uint8_t*>(c.v_scale) + stile * kTileBytesS : nullptr,
+                    fmt_has_scale(KF) ? reinterpret_cast<uint8_t*>(c.k_scale) + stile * tile_bytes_s(KF) : nullptr,
+                    fmt_has_scale(VF) ? reinterpret_cast<uint8_t*>(c.v_scale) + stile * tile_bytes_s(VF) : nullptr,
                     reinterpret_cast<uint8_t*>(c.witness) + tile * kTileBytesW,
                     c.v_witness ? reinterpret_cast<uint8_t*>(c.v_witness) + stile * kTileBytesVW : nullptr,
                     c.n_outlier_pairs > 0
@@ -173,13 +173,18 @@ cudaError_t launch_any(const kvq_cache& c, const void* k, const void* v, int in_
 template <int KF>
 cudaError_t dispatch_v(int vf, const kvq_cache& c, const void* k, const void* v, int b, const int32_t* sl, int n,
                        int32_t* e, cudaStream_t s, const NewestArgs* nw = nullptr, const RopeArgs* rp = nullptr) {
-  switch (vf) {
-    case KVQ_FMT_BF16: return launch_any<KF, KVQ_FMT_BF16>(c, k, v, b, sl, n, e, s, nw, rp);
-    case KVQ_FMT_E4M3: return launch_any<KF, KVQ_FMT_E4M3>(c, k, v, b, sl, n, e, s, nw, rp);
-    case KVQ_FMT_E4M3_SCALED: return launch_any<KF, KVQ_FMT_E4M3_SCALED>(c, k, v, b, sl, n, e, s, nw, rp);
-    case KVQ_FMT_INT8_DITHER: return launch_any<KF, KVQ_FMT_INT8_DITHER>(c, k, v, b, sl, n, e, s, nw, rp);
+  if constexpr (KF == KVQ_FMT_INT8_DITHER_G32) {  // group-scaled INT8 keys go with group-scaled INT8 values only
+    return vf == KVQ_FMT_INT8_DITHER_G32 ? launch_any<KF, KVQ_FMT_INT8_DITHER_G32>(c, k, v, b, sl, n, e, s, nw, rp)
+                                         : cudaErrorInvalidValue;
+  } else {
+    switch (vf) {
+      case KVQ_FMT_BF16: return launch_any<KF, KVQ_FMT_BF16>(c, k, v, b, sl, n, e, s, nw, rp);
+      case KVQ_FMT_E4M3: return launch_any<KF, KVQ_FMT_E4M3>(c, k, v, b, sl, n, e, s, nw, rp);
+      case KVQ_FMT_E4M3_SCALED: return launch_any<KF, KVQ_FMT_E4M3_SCALED>(c, k, v, b, sl, n, e, s, nw, rp);
+      case KVQ_FMT_INT8_DITHER: return launch_any<KF, KVQ_FMT_INT8_DITHER>(c, k, v, b, sl, n, e, s, nw, rp);
+    }
+    return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;
 }
 
 // zero the witness (and value witness) of repaired slots: one thread per (slot, kv head)
@@ -234,12 +239,12 @@ using namespace kvq;
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 extern "C" size_t kvq_tile_bytes(int32_t fmt, int32_t plane) {
-  if (fmt < KVQ_FMT_BF16 || fmt > KVQ_FMT_INT8_DITHER) return 0;
+  if (fmt < KVQ_FMT_BF16 || fmt > KVQ_FMT_INT8_DITHER_G32) return 0;
   switch (plane) {
     case 0: return static_cast<size_t>(tile_bytes_k(fmt));
     case 1: return static_cast<size_t>(tile_bytes_v(fmt));
     case 2:
-    case 3: return fmt_has_scale(fmt) ? static_cast<size_t>(kTileBytesS) : 0;
+    case 3: return fmt_has_scale(fmt) ? static_cast<size_t>(tile_bytes_s(fmt)) : 0;
     case 4: return static_cast<size_t>(kTileBytesW);
     case 5: return static_cast<size_t>(kTileBytesVW);
     case 6: return fmt == KVQ_FMT_INT8_DITHER ? static_cast<size_t>(outlier_tile_bytes(4)) : 0;
@@ -262,7 +267,8 @@ kvq_status append_impl(const kvq_cache* c, const void* k, const void* v, int32_t
                        const int32_t* slot_mapping, int32_t num_tokens, int32_t* err, kvq_stream_t stream,
                        const RopeArgs* rope) {
   if (!c || num_tokens < 0 || (in_dtype != KVQ_DTYPE_F32 && in_dtype != KVQ_DTYPE_BF16)) return KVQ_ERR_INVALID_ARG;
-  if (c->k_fmt < 0 || c->k_fmt > 3 || c->v_fmt < 0 || c->v_fmt > 3) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  if (c->k_fmt < 0 || c->k_fmt > 4 || c->v_fmt < 0 || c->v_fmt > 4) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  if ((c->k_fmt == KVQ_FMT_INT8_DITHER_G32) != (c->v_fmt == KVQ_FMT_INT8_DITHER_G32)) return KVQ_ERR_UNSUPPORTED_LAYOUT;
   if (c->num_kv_heads <= 0 || c->num_pages < 0 || c->reserved != 0) return KVQ_ERR_INVALID_ARG;
   if (num_tokens == 0) return KVQ_OK;
   if (!k || !v || !slot_mapping || !c->k_data || !c->v_data || !c->witness) return KVQ_ERR_INVALID_ARG;
@@ -297,6 +303,10 @@ kvq_status append_impl(const kvq_cache* c, const void* k, const void* v, int32_t
       e = dispatch_v<KVQ_FMT_INT8_DITHER>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s, no_newest,
                                           rope);
       break;
+    case KVQ_FMT_INT8_DITHER_G32:
+      e = dispatch_v<KVQ_FMT_INT8_DITHER_G32>(c->v_fmt, *c, k, v, in_bf16, slot_mapping, num_tokens, err, s,
+                                              no_newest, rope);
+      break;
   }
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
@@ -327,6 +337,8 @@ cudaError_t launch_append_newest(const kvq_cache& c, const void* k, const void* 
     case KVQ_FMT_E4M3: return dispatch_v<KVQ_FMT_E4M3>(c.v_fmt, c, k, v, in_bf16, nullptr, 0, err, s, &nw);
     case KVQ_FMT_E4M3_SCALED: return dispatch_v<KVQ_FMT_E4M3_SCALED>(c.v_fmt, c, k, v, in_bf16, nullptr, 0, err, s, &nw);
     case KVQ_FMT_INT8_DITHER: return dispatch_v<KVQ_FMT_INT8_DITHER>(c.v_fmt, c, k, v, in_bf16, nullptr, 0, err, s, &nw);
+    case KVQ_FMT_INT8_DITHER_G32:
+      return dispatch_v<KVQ_FMT_INT8_DITHER_G32>(c.v_fmt, c, k, v, in_bf16, nullptr, 0, err, s, &nw);
   }
   return cudaErrorInvalidValue;
 }

@@ -245,13 +245,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // witness tile with the value side on.
 int page_bytes(int kf, int vf, bool meter, bool value, bool outl = false) {
   return tile_bytes_k(kf) + tile_bytes_v(vf) + (meter ? kTileBytesW : 0) + (value ? kTileBytesVW : 0) +
-         (fmt_has_scale(kf) ? kTileBytesS : 0) + (fmt_has_scale(vf) ? kTileBytesS : 0) +
+         (fmt_has_scale(kf) ? tile_bytes_s(kf) : 0) + (fmt_has_scale(vf) ? tile_bytes_s(vf) : 0) +
          (outl ? outlier_tile_bytes(kMaxOutlierPairs) : 0);
 }
 
 kvq_status check_cache(const kvq_cache* c, bool meter) {
   if (!c) return KVQ_ERR_INVALID_ARG;
-  if (c->k_fmt < 0 || c->k_fmt > 3 || c->v_fmt < 0 || c->v_fmt > 3) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  if (c->k_fmt < 0 || c->k_fmt > 4 || c->v_fmt < 0 || c->v_fmt > 4) return KVQ_ERR_UNSUPPORTED_LAYOUT;
+  if (fmt_group_scales(c->k_fmt) != fmt_group_scales(c->v_fmt)) return KVQ_ERR_UNSUPPORTED_LAYOUT;
   if (c->num_kv_heads <= 0 || c->num_pages < 0 || c->reserved != 0) return KVQ_ERR_INVALID_ARG;
   if (!c->k_data || !c->v_data || !aligned16(c->k_data) || !aligned16(c->v_data)) return KVQ_ERR_INVALID_ARG;
   if (fmt_has_scale(c->k_fmt) && (!c->k_scale || !aligned16(c->k_scale))) return KVQ_ERR_INVALID_ARG;
@@ -373,7 +374,7 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
         return KVQ_ERR_INVALID_ARG;
     }
     if (mp->tiers & KVQ_TIER_B) {
-      if (cache->k_fmt != KVQ_FMT_INT8_DITHER || (prefix && prefix_len > 0)) return KVQ_ERR_INVALID_ARG;
+      if (!fmt_is_int8(cache->k_fmt) || (prefix && prefix_len > 0)) return KVQ_ERR_INVALID_ARG;
       if (!(mp->delta_req > 0.0 && mp->delta_req < 1.0) || mp->n_layers <= 0 || mp->n_q_heads <= 0 || mp->n_steps <= 0)
         return KVQ_ERR_INVALID_ARG;
     }
@@ -437,13 +438,15 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   // stage size: the larger of the two segments' page footprints (16-byte multiple by construction)
   int sb = page_bytes(cache->k_fmt, cache->v_fmt, meter, a.value_on, outl);
   if (has_prefix) sb = std::max(sb, page_bytes(prefix->k_fmt, prefix->v_fmt, meter, a.value_on));
-  const bool xi = cache->k_fmt == KVQ_FMT_INT8_DITHER && cache->v_fmt == KVQ_FMT_INT8_DITHER;
+  const bool xi = fmt_is_int8(cache->k_fmt) && fmt_is_int8(cache->v_fmt);
+  const bool gs = fmt_group_scales(cache->k_fmt);
   const int cum_bytes = ((batch + 1) * 4 + 127) & ~127;
   const int lo_bytes = q_dtype == KVQ_DTYPE_F32 ? kQloBytes : 0;
   const bool ext = ext_meter;  // the extended-meter kernel variant and its per-lane state
   // warps that stream pages: the layout's warps per CTA, fewer when their two page stages do not fit shared
   // memory (large pages with an fp32 query's low parts)
-  const int per_warp_fixed = (xi ? kXiScratch : 0) + lo_bytes + (ext ? kVStateBytes : 0) + kMaxStages * 8;
+  const int per_warp_fixed =
+      (xi ? kXiScratch : 0) + lo_bytes + (ext ? kVStateBytes : 0) + (gs ? kGqBytes : 0) + kMaxStages * 8;
   int nwa = nw, stages = 0;
   for (; nwa >= 4; --nwa) {
     stages = (smem_max - 1024 - cum_bytes - nwa * per_warp_fixed) / (nwa * sb);

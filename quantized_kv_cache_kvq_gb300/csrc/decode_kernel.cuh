@@ -40,6 +40,10 @@ constexpr int kXiScratch = 16 * 128 * 2;  // per-warp fp16 dither tile (INT8 val
 // value side (sum_t e^{x_t - m} rho^v_t for heads 2c and 2c + 1, rescaled with l; max_t ||v_t||; 0) and
 // alternative bound shapes (max_t c_t for heads 2c, 2c + 1; sum_t e^{x_t - m} (1 - e^{-c_t}) for both heads).
 constexpr int kVStateBytes = 32 * 32;
+// Group-scaled INT8 keys: per-warp table of the query's per-group terms, [kind][group][head] floats:
+// kind 0 = 3/2 sum_c q_c (the fp16 query the key products use), 1 = (sm_scale kappa)^2 ||q_g||^2,
+// 2 = sm_scale 2^-11 ||q_g||_1 (Tier B), for the 4 groups of 32 channels and the 8 heads of a unit.
+constexpr int kGqBytes = 3 * 4 * 8 * 4;
 constexpr int kExtValue = 1, kExtShapes = 2, kExtContrib = 4;
 constexpr int kStatsFloats = 12;  // per (piece, head): m l mc sc | mu su vr vmax | cmax om 0 0
 constexpr unsigned kFull = 0xffffffffu;
@@ -99,8 +103,8 @@ struct Layout {
   static constexpr int vOff = kBytes;
   static constexpr int wOff = kBytes + vBytes;
   static constexpr int ksOff = wOff + (METER ? kTileBytesW : 0);
-  static constexpr int vsOff = ksOff + (fmt_has_scale(KF) ? kTileBytesS : 0);
-  static constexpr int koOff = vsOff + (fmt_has_scale(VF) ? kTileBytesS : 0);
+  static constexpr int vsOff = ksOff + (fmt_has_scale(KF) ? tile_bytes_s(KF) : 0);
+  static constexpr int koOff = vsOff + (fmt_has_scale(VF) ? tile_bytes_s(VF) : 0);
   // the value witness tile follows; it is copied (and the stage sized for it) only with the value
   // side on, so stages without it keep their size
   static constexpr int vwOff = koOff + (OUTL ? outlier_tile_bytes(kMaxOutlierPairs) : 0);
@@ -395,6 +399,7 @@ struct QFrag {
   float cm_scale;    // c_t = cm_scale * (W . QN)  (natural units)
   float alpha_b[2];  // Tier B: u_t = alpha_b[h] * s_t for heads 2c, 2c+1 (natural units)
   float s_init[2];   // INT8 keys: 3/2 sum_c q_c (fp16 query as the key products use it), heads 2c, 2c+1
+  float* gq;         // group-scaled INT8 keys: the warp's per-group query table (kGqBytes)
   // fixed-channel outlier bypass: B fragment of the bypassed channels (head g; fp16 hi / lo), and the
   // Tier B terms of heads 2c, 2c+1: u_t += beta_o[h] ||k_hat_{t,O}|| + gamma_o[h]
   uint32_t qo_hi[2], qo_lo[2];
@@ -431,7 +436,9 @@ __device__ __forceinline__ void reset_state(SoftState& s) {
 // the INT8 fragments, gathered into qo_hi / qo_lo (column 2i <- channel pairs[i], 2i + 1 <- pairs[i] + 64;
 // B fragment of m16n8k8, or m16n8k16 when m > 4), and Tier B splits ||q|| into the INT8 part (alpha_b)
 // and the bypassed part (beta_o, gamma_o: the deterministic bound of the fp16 rounding).
-template <bool K16, bool METER, bool OUTL = false>
+// GS: group-scaled INT8 keys: the 16-bit family's channel order (k-steps 2j, 2j + 1 hold scale group j)
+// with fp16 fragments, and the per-group table f.gq.
+template <bool K16, bool METER, bool OUTL = false, bool GS = false>
 __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const bool real = g < a.G;
@@ -497,14 +504,24 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
       }
     }
   };
-  if (K16) {
+  float gsum[4], gsq[4], gl1[4];  // GS: this lane's part of group j's fp16 sum, ||q||^2 and ||q||_1
+  if (K16 || GS) {
     // k-step 2j + s <- channels 32j + 8c + 4s + {0..3}
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float v[8];
       load8(32 * j + 8 * c, v);
+      if (GS) qsum = 0.f;
       put(2 * j, v);
       put(2 * j + 1, v + 4);
+      if (GS) {
+        gsum[j] = qsum;
+        float sq = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { sq = __fmaf_rn(v[e], v[e], sq); l1 += fabsf(v[e]); }
+        gsq[j] = sq;
+        gl1[j] = l1;
+      }
     }
   } else {
     // k-step 4jj + s <- channels 64jj + 16c + 4s + {0..3}
@@ -627,6 +644,21 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     f.gamma_o[0] = a.sm_scale * o0 * rt * 0x1p-25f;
     f.gamma_o[1] = a.sm_scale * o1 * rt * 0x1p-25f;
   }
+  if (GS) {
+    // the per-group table, one entry per (kind, group, head g) from the lanes of row g
+    const float kap = METER ? sqrtf(2.f * (logf(2.f * static_cast<float>(seq_total)) - a.ln_delta_loc) / 12.f) : 0.f;
+    const float ka = a.sm_scale * kap;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float s1 = row_sum4(gsum[j]), s2 = row_sum4(gsq[j]), s3 = row_sum4(gl1[j]);
+      if (c == 0) {
+        f.gq[(0 * 4 + j) * 8 + g] = 1.5f * s1;
+        f.gq[(1 * 4 + j) * 8 + g] = ka * ka * s2;
+        f.gq[(2 * 4 + j) * 8 + g] = a.sm_scale * 0x1p-11f * s3;
+      }
+    }
+    __syncwarp();
+  }
 }
 
 // One page of a meter sum.  r[v]: radius (c_t or u_t, natural units) of token g + 8(v >> 1) for head
@@ -683,8 +715,10 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   using L = Layout<KF, VF, METER, OUTL>;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   constexpr bool K16 = fmt_is_16bit(KF);
-  constexpr bool KDITHER = KF == KVQ_FMT_INT8_DITHER;
-  constexpr bool VDITHER = VF == KVQ_FMT_INT8_DITHER;
+  constexpr bool KDITHER = fmt_is_int8(KF);
+  constexpr bool VDITHER = fmt_is_int8(VF);
+  constexpr bool GS = fmt_group_scales(KF);  // keys and values both group-scaled INT8
+  static_assert(fmt_group_scales(KF) == fmt_group_scales(VF), "group-scaled keys go with group-scaled values");
 
   // ---------------- S^T = K . Q^T: rows are tokens g (a0, a2) and g + 8 (a1, a3)
   float S[4] = {0.f, 0.f, 0.f, 0.f};
@@ -699,6 +733,54 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         const uint32_t* lo = f.lo + lane;
         mma_bf16_4(S, k0.x, k1.x, k0.y, k1.y, lo[(4 * j + 0) * 32], lo[(4 * j + 1) * 32]);
         mma_bf16_4(S, k0.z, k1.z, k0.w, k1.w, lo[(4 * j + 2) * 32], lo[(4 * j + 3) * 32]);
+      }
+    }
+  } else if (GS) {
+    // group-scaled INT8 keys: k-step kb = 4jj + sidx holds channels 32gr + 8c + 4(sidx & 1) + {0..3} of scale
+    // group gr = 2jj + (sidx >> 1); group gr's product T (started at 3/2 sum of its q, undoing the -(xi + 3/2)
+    // of the dither products) is multiplied by the token scales of the group into S
+    const PhiloxHead ph = philox_head(pl.layer, static_cast<uint32_t>(kvh), pl.rk0, pl.rk1);
+    const PhiloxSlot pt0 = philox_slot(phys * kPage + g, ph, pl.rk0, pl.rk1);
+    const PhiloxSlot pt1 = philox_slot(phys * kPage + g + 8, ph, pl.rk0, pl.rk1);
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const uint4 k0 = lds128(st + L::kOff + (jj * 32 + lane) * 16);
+      const uint4 k1 = lds128(st + L::kOff + ((2 + jj) * 32 + lane) * 16);
+      const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
+      const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int gr = 2 * jj + half;
+        const float2 ti = *reinterpret_cast<const float2*>(f.gq + gr * 8 + 2 * c);
+        float T[4] = {ti.x, ti.y, ti.x, ti.y};
+        // one Philox call per token: the dither of this lane's 8 channels 32gr + 8c + {0..7} of the group
+        const uint32_t grp = 8 * jj + 4 * half + c;
+        const uint4 d0 = philox_finish(grp, pt0, ph, pl.rk0, pl.rk1);
+        const uint4 d1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
+        if (VDITHER) {
+          const int off = (grp ^ g) << 4;
+          *reinterpret_cast<uint4*>(xi_tile + g * 256 + off) =
+              make_uint4(neg_dither_f16x2(d0.x), neg_dither_f16x2(d0.y), neg_dither_f16x2(d0.z), neg_dither_f16x2(d0.w));
+          *reinterpret_cast<uint4*>(xi_tile + (g + 8) * 256 + off) =
+              make_uint4(neg_dither_f16x2(d1.x), neg_dither_f16x2(d1.y), neg_dither_f16x2(d1.z), neg_dither_f16x2(d1.w));
+        }
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const int sidx = 2 * half + s2, kb = 4 * jj + sidx;
+          const uint32_t x0 = w0[sidx] ^ 0x80808080u, x1 = w1[sidx] ^ 0x80808080u;
+          const uint32_t a0 = s8x2_to_f16x2(x0, 0), a2 = s8x2_to_f16x2(x0, 1);
+          const uint32_t a1 = s8x2_to_f16x2(x1, 0), a3 = s8x2_to_f16x2(x1, 1);
+          mma_f16_4(T, a0, a1, a2, a3, f.hi[kb][0], f.hi[kb][1]);
+          if (LO && f.has_lo) mma_f16_4(T, a0, a1, a2, a3, f.lo[(2 * kb) * 32 + lane], f.lo[(2 * kb + 1) * 32 + lane]);
+          const uint32_t e0 = s2 ? d0.z : d0.x, e2 = s2 ? d0.w : d0.y;
+          const uint32_t e1 = s2 ? d1.z : d1.x, e3 = s2 ? d1.w : d1.y;
+          mma_f16_4(T, neg_shifted_dither_f16x2(e0), neg_shifted_dither_f16x2(e1), neg_shifted_dither_f16x2(e2),
+                    neg_shifted_dither_f16x2(e3), f.hi[kb][0], f.hi[kb][1]);
+        }
+        // scales of group gr for tokens g (low half) and g + 8 (high half)
+        const float2 sg = unpack_f16(*reinterpret_cast<const uint32_t*>(st + L::ksOff + 16 * g + 4 * gr));
+        f2_unpack(f2_fma(f2_pack(T[0], T[1]), f2_splat(sg.x), f2_pack(S[0], S[1])), S[0], S[1]);
+        f2_unpack(f2_fma(f2_pack(T[2], T[3]), f2_splat(sg.y), f2_pack(S[2], S[3])), S[2], S[3]);
       }
     }
   } else {
@@ -790,12 +872,12 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   }
 
   // ---------------- per-token scales of tokens g and g + 8
-  float sk[2] = {1.f, 1.f}, sv[2] = {1.f, 1.f};
-  if (fmt_has_scale(KF)) {
+  float sk[2] = {1.f, 1.f}, sv[2] = {1.f, 1.f};  // (group scales are applied in the products instead)
+  if (fmt_has_scale(KF) && !GS) {
     const float2 a = unpack_f16(*reinterpret_cast<const uint32_t*>(st + L::ksOff + 4 * g));
     sk[0] = a.x; sk[1] = a.y;
   }
-  if (fmt_has_scale(VF)) {
+  if (fmt_has_scale(VF) && !GS) {
     const float2 a = unpack_f16(*reinterpret_cast<const uint32_t*>(st + L::vsOff + 4 * g));
     sv[0] = a.x; sv[1] = a.y;
   }
@@ -805,7 +887,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   f2x xp[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    const float sc = fmt_has_scale(KF) ? qk_scale * sk[r] : qk_scale;
+    const float sc = fmt_has_scale(KF) && !GS ? qk_scale * sk[r] : qk_scale;
     f2x base = f2_splat(r ? xb1 : xb0);
     if (OUTL) base = f2_fma(f2_pack(So[2 * r], So[2 * r + 1]), f2_splat(qk_scale), base);
     xp[r] = f2_fma(f2_pack(S[2 * r], S[2 * r + 1]), f2_splat(sc), base);
@@ -899,9 +981,28 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     }
     if (KDITHER && tier_b) {
       float uv[4];
-      const f2x ab = f2_pack(f.alpha_b[0], f.alpha_b[1]);
-      f2_unpack(f2_mul(ab, f2_splat(sk[0])), uv[0], uv[1]);
-      f2_unpack(f2_mul(ab, f2_splat(sk[1])), uv[2], uv[3]);
+      if (GS) {
+        // u_t = sqrt(sum_g (sm_scale kappa)^2 ||q_g||^2 s_{g,t}^2) + sum_g sm_scale 2^-11 ||q_g||_1 s_{g,t}
+        // (v = 2r + h: token g + 8r, head 2c + h)
+        float var[4] = {0.f, 0.f, 0.f, 0.f}, bias[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int gr = 0; gr < kScaleGroups; ++gr) {
+          const float2 A2 = *reinterpret_cast<const float2*>(f.gq + (4 + gr) * 8 + 2 * c);
+          const float2 B1 = *reinterpret_cast<const float2*>(f.gq + (8 + gr) * 8 + 2 * c);
+          const float2 sg = unpack_f16(*reinterpret_cast<const uint32_t*>(st + L::ksOff + 16 * g + 4 * gr));
+          const float q0 = sg.x * sg.x, q1 = sg.y * sg.y;
+          var[0] = __fmaf_rn(A2.x, q0, var[0]); var[1] = __fmaf_rn(A2.y, q0, var[1]);
+          var[2] = __fmaf_rn(A2.x, q1, var[2]); var[3] = __fmaf_rn(A2.y, q1, var[3]);
+          bias[0] = __fmaf_rn(B1.x, sg.x, bias[0]); bias[1] = __fmaf_rn(B1.y, sg.x, bias[1]);
+          bias[2] = __fmaf_rn(B1.x, sg.y, bias[2]); bias[3] = __fmaf_rn(B1.y, sg.y, bias[3]);
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) uv[v] = sqrtf(var[v]) + bias[v];
+      } else {
+        const f2x ab = f2_pack(f.alpha_b[0], f.alpha_b[1]);
+        f2_unpack(f2_mul(ab, f2_splat(sk[0])), uv[0], uv[1]);
+        f2_unpack(f2_mul(ab, f2_splat(sk[1])), uv[2], uv[3]);
+      }
       if (OUTL) {
 #pragma unroll
         for (int v = 0; v < 4; ++v) uv[v] = __fmaf_ru(f.beta_o[v & 1], kon[v >> 1], uv[v]) + f.gamma_o[v & 1];
@@ -916,7 +1017,35 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   float pw[4];
   f2_unpack(f2_mul(f2_pack(p[0], p[1]), f2_splat(kPvShift * sv[0])), pw[0], pw[1]);
   f2_unpack(f2_mul(f2_pack(p[2], p[3]), f2_splat(kPvShift * sv[1])), pw[2], pw[3]);
-  if (!fmt_is_16bit(VF)) {
+  if (GS) {
+    // group-scaled INT8 values: the 32 channels of word block mm are scale group mm, so its two m-tiles take
+    // P'^T built with the group's token scales; the dither product of the same m-tiles follows
+    __syncwarp();  // the dither tile written in the key loop
+#pragma unroll
+    for (int mm = 0; mm < 4; ++mm) {
+      const float2 sg = unpack_f16(*reinterpret_cast<const uint32_t*>(st + L::vsOff + 16 * g + 4 * mm));
+      float pg[4];
+      f2_unpack(f2_mul(f2_pack(p[0], p[1]), f2_splat(kPvShift * sg.x)), pg[0], pg[1]);
+      f2_unpack(f2_mul(f2_pack(p[2], p[3]), f2_splat(kPvShift * sg.y)), pg[2], pg[3]);
+      const uint32_t b0 = movmatrix_trans(pack_f16(pg[0], pg[1]));
+      const uint32_t b1 = movmatrix_trans(pack_f16(pg[2], pg[3]));
+      const uint4 vb = lds128(st + L::vOff + (mm * 32 + lane) * 16);
+      const uint32_t words[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t x0 = words[2 * half] ^ 0x80808080u, x1 = words[2 * half + 1] ^ 0x80808080u;
+        mma_f16_4(s.o[2 * mm + half], s8x2_to_f16x2(x0, 0), s8x2_to_f16x2(x0, 1), s8x2_to_f16x2(x1, 0),
+                  s8x2_to_f16x2(x1, 1), b0, b1);
+        const int mt = 2 * mm + half;
+        const int mat = lane >> 3, r8 = lane & 7;
+        const int row = ((mat >> 1) << 3) + r8;
+        const int chunk = (2 * mt + (mat & 1)) ^ (row & 7);
+        uint32_t fr[4];
+        ldmatrix_x4_trans(fr, xi_tile + row * 256 + chunk * 16);
+        mma_f16_4(s.o[mt], fr[0], fr[1], fr[2], fr[3], b0, b1);
+      }
+    }
+  } else if (!fmt_is_16bit(VF)) {
     const uint32_t b0 = movmatrix_trans(pack_f16(pw[0], pw[1]));
     const uint32_t b1 = movmatrix_trans(pack_f16(pw[2], pw[3]));
 #pragma unroll
@@ -1035,8 +1164,8 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     bulk_g2s(stage + L::vOff, a.pre.v + tile * L::vBytes, L::vBytes, bar);
     if (METER) bulk_g2s(stage + L::wOff, a.pre.w + tile * kTileBytesW, kTileBytesW, bar);
     const size_t stile = static_cast<size_t>(kvh) * a.pre.num_pages + d.phys;
-    if (fmt_has_scale(pk)) bulk_g2s(stage + L::ksOff, a.pre.ks + stile * kTileBytesS, kTileBytesS, bar);
-    if (fmt_has_scale(pv)) bulk_g2s(stage + L::vsOff, a.pre.vs + stile * kTileBytesS, kTileBytesS, bar);
+    if (fmt_has_scale(pk)) bulk_g2s(stage + L::ksOff, a.pre.ks + stile * tile_bytes_s(pk), tile_bytes_s(pk), bar);
+    if (fmt_has_scale(pv)) bulk_g2s(stage + L::vsOff, a.pre.vs + stile * tile_bytes_s(pv), tile_bytes_s(pv), bar);
     if (METER && VALUE && a.value_on) bulk_g2s(stage + L::vwOff, a.pre.vw + stile * kTileBytesVW, kTileBytesVW, bar);
   } else {
     using L = Layout<KF, VF, METER, OUTL>;
@@ -1054,8 +1183,8 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     if (METER) bulk_g2s_hint(stage + L::wOff, a.live.w + tile * kTileBytesW, kTileBytesW, bar, pol);
     // scale planes are head-major, so consecutive pages of a unit share a 128-byte line
     const size_t stile = static_cast<size_t>(kvh) * a.live.num_pages + d.phys;
-    if (fmt_has_scale(KF)) bulk_g2s(stage + L::ksOff, a.live.ks + stile * kTileBytesS, kTileBytesS, bar);
-    if (fmt_has_scale(VF)) bulk_g2s(stage + L::vsOff, a.live.vs + stile * kTileBytesS, kTileBytesS, bar);
+    if (fmt_has_scale(KF)) bulk_g2s(stage + L::ksOff, a.live.ks + stile * tile_bytes_s(KF), tile_bytes_s(KF), bar);
+    if (fmt_has_scale(VF)) bulk_g2s(stage + L::vsOff, a.live.vs + stile * tile_bytes_s(VF), tile_bytes_s(VF), bar);
     if (OUTL) bulk_g2s_hint(stage + L::koOff, a.live.ko + stile * ko_bytes, ko_bytes, bar, pol);
     if (METER && VALUE && a.value_on)
       bulk_g2s_hint(stage + L::vwOff, a.live.vw + stile * kTileBytesVW, kTileBytesVW, bar, pol);
@@ -1122,7 +1251,7 @@ __device__ void zero_tail(uint8_t* st, int nvalid, bool vw_on, bool ko_wide = fa
   for (int e = lane; e < n; e += 32) {
     const int t = nvalid + e / kHeadDim, c = e % kHeadDim;
     if (fmt_is_16bit(KF)) *reinterpret_cast<uint16_t*>(st + L::kOff + k16_offset(t, c)) = 0;
-    else st[L::kOff + k8_offset(t, c)] = 0;
+    else st[L::kOff + (fmt_group_scales(KF) ? k8g_offset(t, c) : k8_offset(t, c))] = 0;
     if (fmt_is_16bit(VF)) *reinterpret_cast<uint16_t*>(st + L::vOff + v16_offset(t, c)) = 0;
     else st[L::vOff + v8_offset(t, c)] = 0;
   }
@@ -1131,8 +1260,16 @@ __device__ void zero_tail(uint8_t* st, int nvalid, bool vw_on, bool ko_wide = fa
     if (METER) *reinterpret_cast<uint16_t*>(st + L::wOff + w_offset(t, b)) = 0;
   }
   for (int t = nvalid + lane; t < kPage; t += 32) {
-    if (fmt_has_scale(KF)) *reinterpret_cast<uint16_t*>(st + L::ksOff + s_offset(t)) = 0;
-    if (fmt_has_scale(VF)) *reinterpret_cast<uint16_t*>(st + L::vsOff + s_offset(t)) = 0;
+    if (fmt_group_scales(KF)) {
+      for (int gr = 0; gr < kScaleGroups; ++gr) *reinterpret_cast<uint16_t*>(st + L::ksOff + gs_offset(t, gr)) = 0;
+    } else if (fmt_has_scale(KF)) {
+      *reinterpret_cast<uint16_t*>(st + L::ksOff + s_offset(t)) = 0;
+    }
+    if (fmt_group_scales(VF)) {
+      for (int gr = 0; gr < kScaleGroups; ++gr) *reinterpret_cast<uint16_t*>(st + L::vsOff + gs_offset(t, gr)) = 0;
+    } else if (fmt_has_scale(VF)) {
+      *reinterpret_cast<uint16_t*>(st + L::vsOff + s_offset(t)) = 0;
+    }
     if (METER && VALUE && vw_on) {
       *reinterpret_cast<uint16_t*>(st + L::vwOff + vw_offset(t, 0)) = 0;
       *reinterpret_cast<uint16_t*>(st + L::vwOff + vw_offset(t, 1)) = 0;
@@ -1154,7 +1291,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   // let the merge grid (programmatic dependent launch) be scheduled as soon as SMs free up
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr bool K16 = fmt_is_16bit(KF);
-  constexpr bool XI = (KF == KVQ_FMT_INT8_DITHER && VF == KVQ_FMT_INT8_DITHER);
+  constexpr bool XI = fmt_is_int8(KF) && fmt_is_int8(VF);
+  constexpr bool GS = fmt_group_scales(KF);
   int32_t* cum = reinterpret_cast<int32_t*>(smem);
   const int cum_bytes = ((a.B + 1) * 4 + 127) & ~127;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1211,12 +1349,15 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   const int lo_bytes = a.q_bf16 ? 0 : kQloBytes;
   static_assert(METER || !VALUE, "the extended meter rides on the meter");
   const int v_bytes = VALUE ? kVStateBytes : 0;
-  const int per_warp = a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes + v_bytes + kMaxStages * 8;
+  const int gq_bytes = GS ? kGqBytes : 0;
+  const int per_warp =
+      a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes + v_bytes + gq_bytes + kMaxStages * 8;
   uint8_t* wbase = smem + cum_bytes + warp * per_warp;
   uint8_t* xi_tile = wbase + a.stages * a.stage_bytes;
   float* vstate = VALUE ? reinterpret_cast<float*>(xi_tile + (XI ? kXiScratch : 0) + lo_bytes) : nullptr;
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(wbase + a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes + v_bytes);
+  float* gq = GS ? reinterpret_cast<float*>(xi_tile + (XI ? kXiScratch : 0) + lo_bytes + v_bytes) : nullptr;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + a.stages * a.stage_bytes + (XI ? kXiScratch : 0) + lo_bytes +
+                                               v_bytes + gq_bytes);
   if (vstate) {
     *reinterpret_cast<float4*>(vstate + 8 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
     *reinterpret_cast<float4*>(vstate + 8 * lane + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1240,6 +1381,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   QFrag f;
   f.lo = reinterpret_cast<uint32_t*>(wbase + a.stages * a.stage_bytes + (XI ? kXiScratch : 0));
   f.has_lo = false;
+  f.gq = gq;
   SoftState s;
   reset_state(s);
   int unit = -1;
@@ -1265,7 +1407,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       unit = u;
       const int seq = u / a.Hkv, kvh = u % a.Hkv;
       const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
-      load_q<K16, METER, OUTL>(a, seq, kvh, total, f);
+      load_q<K16, METER, OUTL, GS>(a, seq, kvh, total, f);
       if (VALUE && a.page_contrib) {
         // this unit's row of contributions, and the global index of its first page
         unit_x0 = static_cast<long long>(a.Hkv) * cum[seq] + static_cast<long long>(kvh) * (cum[seq + 1] - cum[seq]);
@@ -1297,7 +1439,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
         // one test per page instead of one per k-step (measured: FP8 raw -5.7 %, cartridge -1.0 % per
         // launch); the INT8-dithered body keeps its per-k-step test, which schedules better there (+4.5 %
         // with the split)
-        if (KF == KVQ_FMT_INT8_DITHER || f.has_lo)
+        if (fmt_is_int8(KF) || f.has_lo)
           process_page<KF, VF, METER, OUTL, true>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f,
                                                   s, qk_scale, a.tier_b != 0, vstate, ext,
                                                   crow ? crow + (x_begin + j - unit_x0) : nullptr, a.contrib_stride,

@@ -24,13 +24,21 @@ constexpr float kPvShift = 256.0f;
 constexpr float kPvShiftInv = 1.0f / 256.0f;
 
 __host__ __device__ constexpr bool fmt_is_16bit(int f) { return f == KVQ_FMT_BF16; }
+// subtractively dithered INT8, with one scale per token or one per token and 32-channel group
+__host__ __device__ constexpr bool fmt_is_int8(int f) {
+  return f == KVQ_FMT_INT8_DITHER || f == KVQ_FMT_INT8_DITHER_G32;
+}
+__host__ __device__ constexpr bool fmt_group_scales(int f) { return f == KVQ_FMT_INT8_DITHER_G32; }
 __host__ __device__ constexpr bool fmt_has_scale(int f) {
-  return f == KVQ_FMT_E4M3_SCALED || f == KVQ_FMT_INT8_DITHER;
+  return f == KVQ_FMT_E4M3_SCALED || fmt_is_int8(f);
 }
 __host__ __device__ constexpr int tile_bytes_k(int f) { return fmt_is_16bit(f) ? 4096 : 2048; }
 __host__ __device__ constexpr int tile_bytes_v(int f) { return fmt_is_16bit(f) ? 4096 : 2048; }
 constexpr int kTileBytesW = 512;
 constexpr int kTileBytesS = 32;
+constexpr int kScaleGroup = 32;                        // channels per scale group (group-scaled INT8)
+constexpr int kScaleGroups = kHeadDim / kScaleGroup;   // 4
+__host__ __device__ constexpr int tile_bytes_s(int f) { return fmt_group_scales(f) ? kTileBytesS * kScaleGroups : kTileBytesS; }
 constexpr int kTileBytesVW = 64;  // value witness: (rho^v, ||v||) per token
 constexpr int kMaxOutlierPairs = 8;
 // key outlier tile: 16 tokens x 8 fp16 columns (m <= 4) or x 16 (m <= 8), tensor-core A-fragment order
@@ -48,6 +56,12 @@ __host__ __device__ __forceinline__ int k16_offset(int t, int c) {
 __host__ __device__ __forceinline__ int k8_offset(int t, int c) {
   return 16 * ((((t >> 3) * 2 + (c >> 6)) * 32) + (t & 7) * 4 + ((c >> 4) & 3)) + (c & 15);
 }
+// 8-bit keys with 32-channel scale groups: the 16-bit family's k-step order (k-step 2j + s <- channels
+// 32j + 8c + 4s + {0..3} of lane c), so that every tensor-core k-step lies inside one scale group
+__host__ __device__ __forceinline__ int k8g_offset(int t, int c) {
+  return 16 * ((((t >> 3) * 2 + (c >> 6)) * 32) + (t & 7) * 4 + ((c >> 3) & 3)) + 4 * (2 * ((c >> 5) & 1) + ((c >> 2) & 1)) +
+         (c & 3);
+}
 __host__ __device__ __forceinline__ int v16_offset(int t, int c) {
   return 16 * (32 * (c >> 4) + 4 * (c & 7) + ((t & 7) >> 1)) + 4 * (2 * (t >> 3) + ((c >> 3) & 1)) + 2 * (t & 1);
 }
@@ -59,6 +73,8 @@ __host__ __device__ __forceinline__ int w_offset(int t, int b) {
   return 16 * (4 * (t & 7) + (b >> 2)) + 8 * (t >> 3) + 2 * (b & 3);
 }
 __host__ __device__ __forceinline__ int s_offset(int t) { return 2 * (2 * (t & 7) + (t >> 3)); }
+// group scales: lane g of the decode reads the four groups of tokens g and g + 8 as one 16-byte word
+__host__ __device__ __forceinline__ int gs_offset(int t, int grp) { return 16 * (t & 7) + 4 * grp + 2 * (t >> 3); }
 // key outlier column col of token t (m16n8k8 A fragment for m <= 4, m16n8k16 for m <= 8)
 __host__ __device__ __forceinline__ int ko_offset(int t, int col, bool wide) {
   return wide ? 16 * (4 * (t & 7) + ((col & 7) >> 1)) + 8 * (col >> 3) + 4 * (t >> 3) + 2 * (col & 1)

@@ -4,8 +4,9 @@
 //
 // WitCert (arXiv 2607.28699) Sec. 4.2 "Subtractive dither": x_hat = s (round(x/s + xi) - xi),
 // s = amax / (Q - 1/2), Q = 127.  Sec. 6.2.1: quantize with the stored fp16 scale.  Sec. 6.2.3:
-// one scale per token (per channel group; here the whole 128-channel head), dither keyed by the
-// slot.  Sec. 4.1 eq. (2): the witness w_{t,b} = ||r_{t,b}|| over 16 bands of RoPE pairs, fp16.
+// one scale per token per channel group (the whole 128-channel head, or groups of 32 channels, the
+// 8 lanes 8g..8g+7), dither keyed by the slot.  Sec. 4.1 eq. (2): the witness w_{t,b} = ||r_{t,b}||
+// over 16 bands of RoPE pairs, fp16.
 // "Compress the shared cartridge": BF16 keys, FP8 E4M3 values (K16/V8), E4M3 keys (K8/V8).
 #pragma once
 
@@ -29,7 +30,7 @@ __device__ __forceinline__ void store_k4(uint8_t* tile, int t, int c0, const uin
     *reinterpret_cast<uint2*>(tile + k16_offset(t, c0)) = w;  // c0 % 4 == 0: 8-byte aligned
   } else {
     const uint32_t w = codes[0] | (codes[1] << 8) | (codes[2] << 16) | (codes[3] << 24);
-    *reinterpret_cast<uint32_t*>(tile + k8_offset(t, c0)) = w;
+    *reinterpret_cast<uint32_t*>(tile + (fmt_group_scales(FMT) ? k8g_offset(t, c0) : k8_offset(t, c0))) = w;
   }
 }
 
@@ -49,8 +50,20 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+// max over the 8 lanes of one 32-channel scale group
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = 4; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// the amax a lane's scale is taken over: its 32-channel group or the whole row
+template <int FMT>
+__device__ __forceinline__ float scale_amax(float v) {
+  return fmt_group_scales(FMT) ? group_max(v) : warp_max(v);
+}
 
-// Quantize 4 channels of one row.  `amax` is the row's max |x| (exact), `xi` the dither (INT8).
+// Quantize 4 channels of one row.  `amax` is the max |x| (exact) over the channels that share this
+// lane's scale (the row, or its 32-channel group), `xi` the dither (INT8).
 // Returns codes (bit patterns) and the scale bits; fills the residual bounds when WANT_RES.
 template <int FMT, bool WANT_RES>
 __device__ __forceinline__ void quantize4(const float x[4], float amax, const float xi[4], uint32_t codes[4],
@@ -75,12 +88,12 @@ __device__ __forceinline__ void quantize4(const float x[4], float amax, const fl
     }
     return;
   }
-  const float divisor = (FMT == KVQ_FMT_INT8_DITHER) ? 126.5f : 448.0f;
+  const float divisor = fmt_is_int8(FMT) ? 126.5f : 448.0f;
   const __half s16 = __float2half_rn(__fdiv_rn(amax, divisor));
   scale_bits = __half_as_ushort(s16);
   const float s = __half2float(s16);
   if (!(s <= 65504.0f)) flags |= 1;  // fp16 overflow (or NaN amax)
-  if (FMT == KVQ_FMT_INT8_DITHER) {
+  if (fmt_is_int8(FMT)) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       int code = 0;
@@ -136,7 +149,7 @@ __device__ __forceinline__ void load_row4(const void* kin, const void* vin, int 
 // One row's stored form, as held by the lanes of the warp.
 struct RowCodes {
   uint32_t kc[4], vc[4];  // this lane's four K and V codes
-  uint16_t ks, vs;        // scale bits (formats with a scale)
+  uint16_t ks, vs;        // scale bits (formats with a scale; with group scales, this lane's group)
   uint16_t wb;            // witness bits of band `lane` (lanes 0..15)
   uint16_t vrho, vnorm;   // value witness bits: ||v_hat - v|| and ||v||, rounded up (warp-uniform)
   uint16_t kob[4];        // fp16 bits of this lane's bypassed key channels ...
@@ -159,7 +172,7 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
   for (int i = 0; i < 4; ++i) finite = finite && isfinite(k[i]) && isfinite(v[i]);
   finite = __all_sync(0xffffffffu, finite);
   float xi[4] = {0.f, 0.f, 0.f, 0.f};
-  if (KF == KVQ_FMT_INT8_DITHER || VF == KVQ_FMT_INT8_DITHER) {
+  if (fmt_is_int8(KF) || fmt_is_int8(VF)) {
     const float4 d = dither4(slot, layer, head, static_cast<uint32_t>(lane), static_cast<uint32_t>(seed),
                              static_cast<uint32_t>(seed >> 32));
     xi[0] = d.x; xi[1] = d.y; xi[2] = d.z; xi[3] = d.w;
@@ -181,9 +194,10 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
     float a = 0.f;  // bypassed channels are left out of the amax
 #pragma unroll
     for (int e = 0; e < 4; ++e) a = rc.kocol[e] < 0 ? fmaxf(a, fabsf(k[e])) : a;
-    kamax = warp_max(a);
+    kamax = scale_amax<KF>(a);
   }
-  if (fmt_has_scale(VF)) vamax = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+  if (fmt_has_scale(VF))
+    vamax = scale_amax<VF>(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
   int flags = 0;
   Quantized4 qk, qv;
   rc.ks = 0;
@@ -205,7 +219,9 @@ __device__ __forceinline__ RowCodes quantize_row(const float k[4], const float v
   }
   if (__any_sync(0xffffffffu, (flags & 1) != 0)) flags |= 1;  // an overflowing bypassed channel flags the row
   if (bad_pair) flags |= 4;
-  if (fmt_has_scale(VF) && __half2float(__ushort_as_half(rc.vs)) > KVQ_MAX_VALUE_SCALE) flags |= 2;
+  // every group's value scale is checked (with group scales the lanes hold different ones)
+  if (__any_sync(0xffffffffu, fmt_has_scale(VF) && __half2float(__ushort_as_half(rc.vs)) > KVQ_MAX_VALUE_SCALE))
+    flags |= 2;
   // Witness: upper bound of each band norm.  Lane l holds channels 4l..4l+3, all in band l % 16;
   // lanes l and l + 16 share a band (channels 4b..4b+3 and 64+4b..64+4b+3).
   float ss = 0.0f;
@@ -251,8 +267,12 @@ __device__ __forceinline__ void store_row(const RowCodes& rc, int t, uint8_t* kt
   store_k4<KF>(ktile, t, lane * 4, rc.kc);
   store_v4<VF>(vtile, t, lane * 4, rc.vc);
   if (lane == 0) {
-    if (fmt_has_scale(KF) && kstile) *reinterpret_cast<uint16_t*>(kstile + s_offset(t)) = rc.ks;
-    if (fmt_has_scale(VF) && vstile) *reinterpret_cast<uint16_t*>(vstile + s_offset(t)) = rc.vs;
+    if (fmt_has_scale(KF) && !fmt_group_scales(KF) && kstile) *reinterpret_cast<uint16_t*>(kstile + s_offset(t)) = rc.ks;
+    if (fmt_has_scale(VF) && !fmt_group_scales(VF) && vstile) *reinterpret_cast<uint16_t*>(vstile + s_offset(t)) = rc.vs;
+  }
+  if ((lane & 7) == 0) {  // group scales: lane 8g holds group g's
+    if (fmt_group_scales(KF) && kstile) *reinterpret_cast<uint16_t*>(kstile + gs_offset(t, lane >> 3)) = rc.ks;
+    if (fmt_group_scales(VF) && vstile) *reinterpret_cast<uint16_t*>(vstile + gs_offset(t, lane >> 3)) = rc.vs;
   }
   if (wtile && lane < 16) *reinterpret_cast<uint16_t*>(wtile + w_offset(t, lane)) = rc.wb;
   if (vwtile && lane == 0) {

@@ -7,8 +7,8 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["k_offsets", "v_offsets", "w_offsets", "s_offsets", "vw_offsets", "ko_offsets", "unpack_k", "unpack_v",
-           "unpack_w", "unpack_s", "unpack_vw", "unpack_ko"]
+__all__ = ["k_offsets", "v_offsets", "w_offsets", "s_offsets", "gs_offsets", "vw_offsets", "ko_offsets", "unpack_k",
+           "unpack_v", "unpack_w", "unpack_s", "unpack_gs", "unpack_vw", "unpack_ko"]
 
 
 def k_offsets(fmt: str) -> np.ndarray:
@@ -17,6 +17,9 @@ def k_offsets(fmt: str) -> np.ndarray:
     c = np.arange(128)[None, :]
     if fmt == "bf16":
         return 16 * ((((t >> 3) * 4 + (c >> 5)) * 32) + (t & 7) * 4 + ((c >> 3) & 3)) + 2 * (c & 7)
+    if fmt == "int8g32":   # 32-channel scale groups: every tensor-core k-step inside one group
+        return (16 * ((((t >> 3) * 2 + (c >> 6)) * 32) + (t & 7) * 4 + ((c >> 3) & 3))
+                + 4 * (2 * ((c >> 5) & 1) + ((c >> 2) & 1)) + (c & 3))
     return 16 * ((((t >> 3) * 2 + (c >> 6)) * 32) + (t & 7) * 4 + ((c >> 4) & 3)) + (c & 15)
 
 
@@ -38,6 +41,13 @@ def w_offsets() -> np.ndarray:
 def s_offsets() -> np.ndarray:
     t = np.arange(16)
     return 2 * (2 * (t & 7) + (t >> 3))
+
+
+def gs_offsets() -> np.ndarray:
+    """[16 tokens, 4 groups] byte offsets in a group-scale tile (group g = channels 32g..32g+31)."""
+    t = np.arange(16)[:, None]
+    g = np.arange(4)[None, :]
+    return 16 * (t & 7) + 4 * g + 2 * (t >> 3)
 
 
 def vw_offsets() -> np.ndarray:
@@ -84,6 +94,12 @@ def unpack_s(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:
     """scale plane (head-major tiles: head * num_pages + page) -> fp16 bits [pages, heads, 16 tokens]."""
     tiles = tiles.reshape(num_kv_heads, -1, tiles.shape[-1]).transpose(1, 0, 2)
     return _gather16(tiles, s_offsets())
+
+
+def unpack_gs(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:
+    """group-scale plane (head-major tiles) -> fp16 bits [pages, heads, 16 tokens, 4 groups]."""
+    tiles = tiles.reshape(num_kv_heads, -1, tiles.shape[-1]).transpose(1, 0, 2)
+    return _gather16(tiles, gs_offsets())
 
 
 def unpack_vw(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:

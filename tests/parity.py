@@ -16,8 +16,8 @@ import workloads as W
 from oracle import attention as OA
 from oracle.encoders import fp16_value
 from oracle.philox import dither
-from oracle.quant import (bypass_channels, dequantize, dequantize_int8_bypass, quantize, quantize_int8_bypass,
-                          value_witness_bits, witness_bits)
+from oracle.quant import (bypass_channels, dequantize, dequantize_int8_bypass, dequantize_int8_groups, quantize,
+                          quantize_int8_bypass, quantize_int8_groups, value_witness_bits, witness_bits)
 
 SM_SCALE = float(np.float32(1.0 / math.sqrt(128)))
 PREFIX_SEED_UNIT = 777_777
@@ -53,6 +53,9 @@ def make_inputs(w, layer: int = 0):
 
 
 def _oracle_quant_rows(x32, fmt, xi):
+    if fmt == "int8g32":   # one scale per token per 32-channel group: sb [..., 4]
+        codes, sb, valid = quantize_int8_groups(x32, xi, group=32)
+        return codes, sb, dequantize_int8_groups(codes, sb, xi), valid
     codes, sb, valid = quantize(x32, fmt, xi if fmt == "int8" else None)
     xh = dequantize(codes, sb, fmt, xi if fmt == "int8" else None)
     return codes, sb, xh, valid

@@ -51,6 +51,10 @@ def test_host_entry_points(lib):
     assert kvq.tile_bytes("int8", 1) == 2048 and kvq.tile_bytes("bf16", 1) == 4096
     assert kvq.tile_bytes("int8", 2) == 32 and kvq.tile_bytes("bf16", 2) == 0
     assert kvq.tile_bytes("e4m3s", 3) == 32 and kvq.tile_bytes("e4m3", 4) == 512
+    # INT8 with 32-channel scale groups: 8-bit tiles, 4 fp16 scales per token, no key outlier tile
+    assert kvq.tile_bytes("int8g32", 0) == 2048 and kvq.tile_bytes("int8g32", 1) == 2048
+    assert kvq.tile_bytes("int8g32", 2) == 128 and kvq.tile_bytes("int8g32", 3) == 128
+    assert kvq.tile_bytes("int8g32", 6) == 0 and kvq.tile_bytes("int8g32", 7) == 0
 
 
 def test_struct_sizes_match_c():

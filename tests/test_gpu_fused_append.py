@@ -20,6 +20,8 @@ from tests.parity import SM_SCALE, make_inputs, reference_case  # noqa: E402
 CASES = {
     "cartridge": lambda: W.reduced(W.WORKLOADS["qwen3_8b_cartridge"], batch=3, seq_len=77),
     "int8": lambda: W.reduced(W.WORKLOADS["int8_7b_certified"], batch=3, seq_len=150),
+    "int8g32": lambda: W.reduced(W.WORKLOADS["int8_7b_certified"], batch=3, seq_len=150, k_fmt="int8g32",
+                                 v_fmt="int8g32"),
     "fp8raw": lambda: W.reduced(W.WORKLOADS["fp8_raw_stress"], batch=2, seq_len=100),
     "ragged": lambda: W.reduced(W.WORKLOADS["ragged_paged"], batch=5, ragged=(1, 300)),
 }
