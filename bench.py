@@ -69,6 +69,9 @@ def parse():
     p.add_argument("--bypass", type=int, default=0, metavar="M",
                    help="INT8 keys: M massive RoPE pairs per (layer, kv head) injected (x30) and kept in fp16 by the "
                         "fixed-channel bypass")
+    p.add_argument("--int8-groups", action="store_true",
+                   help="INT8 keys and values with one fp16 scale per token per 32-channel group (WitCert 6.2.3, "
+                        "G_c = 32) instead of one per token")
     p.add_argument("--separate-append", action="store_true",
                    help="kvq_append + kvq_decode_attn per layer instead of the fused kvq_decode_attn_append")
     p.add_argument("--layers", type=int, default=0, help="override layer count (profiling only; not a bench line)")
@@ -80,15 +83,15 @@ def parse():
     return p.parse_args()
 
 
-CODE_BYTES = {"bf16": 2, "e4m3": 1, "e4m3s": 1, "int8": 1}
-HAS_SCALE = {"bf16": 0, "e4m3": 0, "e4m3s": 1, "int8": 1}
+CODE_BYTES = {"bf16": 2, "e4m3": 1, "e4m3s": 1, "int8": 1, "int8g32": 1}
+SCALE_BYTES = {"bf16": 0, "e4m3": 0, "e4m3s": 2, "int8": 2, "int8g32": 8}   # fp16 scales per token per kv head
 
 
 def token_head_bytes(k_fmt, v_fmt, meter=True, value_side=False, bypass=0) -> int:
     """Bytes one token of one kv head costs the decode: K and V codes, fp16 scales, 32-byte witness
     (+ the 4-byte value witness with the value side of the output bound, + the fp16 key outlier tile of
     the fixed-channel bypass: 8 columns for up to 4 pairs, 16 for up to 8)."""
-    return (128 * (CODE_BYTES[k_fmt] + CODE_BYTES[v_fmt]) + 2 * (HAS_SCALE[k_fmt] + HAS_SCALE[v_fmt]) + 32 * meter
+    return (128 * (CODE_BYTES[k_fmt] + CODE_BYTES[v_fmt]) + SCALE_BYTES[k_fmt] + SCALE_BYTES[v_fmt] + 32 * meter
             + 4 * value_side + (0 if not bypass else 16 if bypass <= 4 else 32))
 
 
@@ -130,8 +133,9 @@ def issue_peak_winst_per_s(sm_mhz: float = GB300_MAX_SM_MHZ) -> float:
 
 def runs_a_variant(args, w) -> bool:
     """True when a switch or the workload runs another decode instance than the plain one the ncu records
-    describe (value side, bound shapes, gate support, key outlier bypass, meter off)."""
-    return bool(args.value_side or args.shapes or args.gate or w.bypass_pairs or args.meter_off)
+    describe (value side, bound shapes, gate support, key outlier bypass, meter off, group scales)."""
+    return bool(args.value_side or args.shapes or args.gate or w.bypass_pairs or args.meter_off
+                or getattr(args, "int8_groups", False))
 
 
 def traffic_record(workload: str, variant: bool = False):
@@ -604,6 +608,11 @@ def main():
         if w.k_fmt != "int8" or w.prefix_len:
             raise SystemExit("--bypass needs a workload with INT8-dithered keys and no shared prefix")
         w = W.reduced(w, massive_pairs=args.bypass, massive_scale=30.0, bypass_pairs=args.bypass)
+    if args.int8_groups:
+        if w.k_fmt != "int8" or w.v_fmt != "int8" or w.prefix_len or w.bypass_pairs:
+            raise SystemExit("--int8-groups needs a workload with INT8-dithered keys and values, no shared prefix "
+                             "and no outlier bypass")
+        w = W.reduced(w, k_fmt="int8g32", v_fmt="int8g32")
     if args.batch:
         w = W.reduced(w, batch=args.batch)
     if args.impl == "reference":

@@ -18,10 +18,11 @@ from __future__ import annotations
 __all__ = ["CODE_BYTES", "payload_bytes_per_token", "kv_bytes_per_token_head", "decode_step_bytes",
            "int8_side_bytes", "scale_granularity_saving"]
 
-CODE_BYTES = {"bf16": 2, "e4m3": 1, "e4m3s": 1, "int8": 1}
-HAS_SCALE = {"bf16": False, "e4m3": False, "e4m3s": True, "int8": True}
+CODE_BYTES = {"bf16": 2, "e4m3": 1, "e4m3s": 1, "int8": 1, "int8g32": 1}
+HAS_SCALE = {"bf16": False, "e4m3": False, "e4m3s": True, "int8": True, "int8g32": True}
+SCALE_GROUPS = {"e4m3s": 1, "int8": 1, "int8g32": 4}   # fp16 scales per (token, kv head)
 WITNESS_BYTES = 32   # 16 bands x fp16
-SCALE_BYTES = 2      # one fp16 per (token, kv head)
+SCALE_BYTES = 2      # one fp16 scale
 
 
 def payload_bytes_per_token(k_fmt: str, v_fmt: str, n_layers: int, n_kv_heads: int, head_dim: int = 128) -> int:
@@ -32,7 +33,7 @@ def payload_bytes_per_token(k_fmt: str, v_fmt: str, n_layers: int, n_kv_heads: i
 def kv_bytes_per_token_head(k_fmt: str, v_fmt: str, meter: bool = True, head_dim: int = 128) -> int:
     """Bytes the decode path reads per token per kv head: codes, scales, and the witness when metered."""
     b = head_dim * (CODE_BYTES[k_fmt] + CODE_BYTES[v_fmt])
-    b += SCALE_BYTES * (int(HAS_SCALE[k_fmt]) + int(HAS_SCALE[v_fmt]))
+    b += SCALE_BYTES * (SCALE_GROUPS.get(k_fmt, 0) + SCALE_GROUPS.get(v_fmt, 0))
     if meter:
         b += WITNESS_BYTES
     return b

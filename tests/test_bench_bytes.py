@@ -41,6 +41,16 @@ def test_survey_table_of_bytes_per_token_head():
     assert bench.token_head_bytes("e4m3", "e4m3") == 288
 
 
+def test_group_scaled_int8_bytes():
+    # one fp16 scale per token per 32-channel group: 136 B per side (WitCert 6.2.3), plus the 32-byte witness
+    assert bench.token_head_bytes("int8g32", "int8g32", meter=False) == 2 * OB.int8_side_bytes("token", group=32) == 272
+    assert bench.token_head_bytes("int8g32", "int8g32") == OB.kv_bytes_per_token_head("int8g32", "int8g32") == 304
+    w = W.reduced(W.WORKLOADS["int8_7b_certified"], k_fmt="int8g32", v_fmt="int8g32")
+    lens = W.seq_lengths(w)
+    assert bench.step_bytes(w, lens) == OB.decode_step_bytes(w.batch, w.n_layers, w.n_kv_heads, lens, "int8g32",
+                                                             "int8g32")
+
+
 def test_payload_table_of_the_page():
     g = json.load(open(GOLDEN))
     L, H, d = g["model"]["n_layers"], g["model"]["n_kv_heads"], g["model"]["head_dim"]

@@ -68,7 +68,7 @@ def test_issue_roofline_with_an_alu_record():
 
 
 def test_every_switch_counts_as_a_variant():
-    base = dict(value_side=False, shapes=False, gate=False, meter_off=False)
+    base = dict(value_side=False, shapes=False, gate=False, meter_off=False, int8_groups=False)
     w = bench.W.WORKLOADS["qwen3_8b_cartridge"]
     assert not bench.runs_a_variant(argparse.Namespace(**base), w)
     for k in base:
