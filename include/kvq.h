@@ -141,7 +141,7 @@ typedef struct kvq_cache {
 
 /* Meter configuration ([W] Sec. 4.2 request-level budget, Sec. 4.3 saturation). */
 typedef struct kvq_meter_params {
-  uint32_t tiers;     /* bit 0: Tier A witness bound; bit 1: Tier B dither certificate (INT8 keys only);
+  uint32_t tiers;     /* bit 0: Tier A witness bound; bit 1: Tier B dither certificate (INT8 keys only, either scale layout);
                          bit 2: value side of the output-error bound; bit 3: alternative bound shapes
                          (two-sided, det-tanh); bits 2 and 3 require Tier A                          */
   int32_t n_layers;   /* L in delta_loc = delta_req / (L * H * T)                                      */
@@ -183,7 +183,9 @@ size_t kvq_sizeof(int32_t which);
  * the key residual k_hat - k, rounded up ([W] Sec. 4.1, eq. (2)).  Scales:
  *   E4M3_SCALED: s = fp16_rn(fp32(amax / 448)),  code = e4m3_rn_satfinite(fp32(x / s))
  *   INT8_DITHER: s = fp16_rn(fp32(amax / 126.5)), code = clamp(rint(fp32(fp32(x / s) + xi)), -127, 127)
- * (amax = 0 stores scale 0 and zero codes).  The dither xi comes from
+ *   INT8_DITHER_G32: the same per group of 32 channels (amax and s of channels 32g..32g+31; [W] Sec. 6.2.3)
+ * (amax = 0 stores scale 0 and zero codes).  A cache whose keys are INT8_DITHER_G32 must have
+ * INT8_DITHER_G32 values and vice versa, and has no outlier bypass (else KVQ_ERR_UNSUPPORTED_LAYOUT).  The dither xi comes from
  * Philox4x32-10 with key (seed low 32 bits, seed high 32 bits), counter
  * (slot, layer, kv_head, c >> 3), output word (c >> 1) & 3, of which bits
  * 0..9 (c even) or 16..25 (c odd) form the field f, xi = f * 2^-10 - 1/2: a
@@ -245,7 +247,9 @@ size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t nu
  *       sum_b ||q_b|| w_{t,b} ([W] Thm. 1, Thm. 2); -inf when A = 1;
  *   [1] ln(A_B - 1) of Tier B, u_t = sm_scale s_t (||q|| sqrt(2 ln(2S/delta_loc)/12)
  *       + ||q||_1 2^-11) ([W] Sec. 4.2; the second term bounds the mean of the dithered
- *       rounding error on the 1024-point dither grid), NaN when Tier B is off;
+ *       rounding error on the 1024-point dither grid); with 32-channel group scales
+ *       u_t = sm_scale (kappa sqrt(sum_g ||q_g||^2 s_{g,t}^2) + 2^-11 sum_g ||q_g||_1 s_{g,t}),
+ *       kappa = sqrt(2 ln(2S/delta_loc)/12); NaN when Tier B is off;
  *   [2] log-sum-exp of the compressed logits (natural log); [3] tokens attended S;
  *   [4] R = sum_t p~_t rho^v_t and [5] Vmax = max_t ||v_t|| from the value
  *       witness ([W] Sec. 3), NaN when KVQ_TIER_V is off (0 for an empty sequence);
