@@ -176,3 +176,52 @@ def test_key_outlier_tile_layout(m):
             assert offs[g + 8, 2 * c] == base + 4 and offs[g + 8, 2 * c + 1] == base + 6
             if cols == 16:
                 assert offs[g, 2 * c + 8] == base + 8 and offs[g + 8, 2 * c + 9] == base + 14
+
+
+def test_group_scaled_int8_layouts():
+    """INT8 with 32-channel scale groups: the key tile is a bijection, lane (g, c)'s 16-byte word (nt, jj) holds
+    token 8nt + g in the 16-bit family's k-step order (byte 4 sidx + e <- channel 32 (2jj + (sidx >> 1)) + 8c
+    + 4 (sidx & 1) + e), so the 16 channels of every k-step lie in one group; the group-scale tile is a
+    bijection and lane g reads the four groups of tokens g and g + 8 as one 16-byte word."""
+    from quantized_kv_cache_kvq_gb300 import layout as L
+
+    ko = L.k_offsets("int8g32")
+    assert sorted(ko.ravel().tolist()) == list(range(2048))
+    for nt in range(2):
+        for jj in range(2):
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                word = ((nt * 2 + jj) * 32 + lane) * 16
+                for sidx in range(4):
+                    for e in range(4):
+                        ch = 32 * (2 * jj + (sidx >> 1)) + 8 * c + 4 * (sidx & 1) + e
+                        assert ko[8 * nt + g, ch] == word + 4 * sidx + e
+    for jj in range(2):
+        for sidx in range(4):   # k-step kb = 4jj + sidx: the channels of its 4 lanes c share one group
+            chans = [32 * (2 * jj + (sidx >> 1)) + 8 * c + 4 * (sidx & 1) + e for c in range(4) for e in range(4)]
+            assert len({ch // 32 for ch in chans}) == 1
+            # the same channels as k-step 4jj + sidx of the 16-bit family (k-step 2j + s <- 32j + 8c + 4s + e)
+            j, s = 2 * jj + (sidx >> 1), sidx & 1
+            assert chans == [32 * j + 8 * c + 4 * s + e for c in range(4) for e in range(4)]
+    go = L.gs_offsets()
+    assert sorted((go // 2).ravel().tolist()) == list(range(64))
+    for g in range(8):
+        assert [go[g, k] for k in range(4)] == [16 * g + 4 * k for k in range(4)]
+        assert [go[g + 8, k] for k in range(4)] == [16 * g + 4 * k + 2 for k in range(4)]
+
+
+def test_group_scaled_int8_layout_combinations_refused_on_host(lib):
+    import quantized_kv_cache_kvq_gb300 as kvq
+
+    fake = 16  # aligned, never dereferenced: the layout checks come before any device work
+    def cache(kf, vf, m=0):
+        return kvq._Cache(k_fmt=kf, v_fmt=vf, num_kv_heads=2, num_pages=1, k_data=fake, v_data=fake, k_scale=fake,
+                          v_scale=fake, witness=fake, outlier_pairs=fake if m else None, n_outlier_pairs=m,
+                          k_outlier=fake if m else None)
+    G32, I8, BF = kvq.FMT["int8g32"], kvq.FMT["int8"], kvq.FMT["bf16"]
+    for kf, vf in ((G32, I8), (I8, G32), (BF, G32), (G32, BF)):
+        c = cache(kf, vf)
+        assert lib.kvq_append(ctypes.byref(c), fake, fake, 0, fake, 1, None, None) == 2, (kf, vf)
+    c = cache(G32, G32, m=2)   # no outlier bypass with group scales
+    assert lib.kvq_append(ctypes.byref(c), fake, fake, 0, fake, 1, None, None) == 2
+    assert lib.kvq_tile_bytes(5, 0) == 0    # no format 5
