@@ -26,6 +26,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -42,7 +43,7 @@ import workloads as W  # noqa: E402
 METRIC = "decode-attn KV GB/s (% of GB300 HBM peak) with meter on; attended tok/s"
 SM_SCALE = float(np.float32(1.0 / math.sqrt(128)))
 # device sources of decode_split_kernel (the roofline kernel): its recorded DRAM traffic is valid only
-# for the exact sources it was captured from
+# for the code it was captured from (comments and blank lines aside)
 KERNEL_SOURCES = ["quantized_kv_cache_kvq_gb300/csrc/decode_kernel.cuh", "quantized_kv_cache_kvq_gb300/csrc/kvq_common.cuh",
                   "quantized_kv_cache_kvq_gb300/csrc/decode_instances.inc"]
 
@@ -104,11 +105,25 @@ def step_bytes(w, lens, value_side=False, meter=True) -> int:
     return w.n_layers * w.n_kv_heads * (live + pre)
 
 
-def kernel_hash() -> str:
+def code_only(text: str) -> str:
+    """C++ source without comments and blank lines: what decides the compiled kernel (an edit of a comment
+    leaves the recorded counters valid)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
+def kernel_hash(read=None) -> str:
+    """Fingerprint of the decode kernel's code; ``read(path)`` returns a source's text (default: the working
+    tree)."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        if read is None:
+            with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(code_only(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -6,8 +6,9 @@
 // laid end to end and cut into equal contiguous ranges, one per warp of a persistent grid (a warp
 // range may cross unit boundaries).  Each warp streams its pages through its own ring of shared-
 // memory stages filled by bulk asynchronous copies (cp.async.bulk + mbarrier complete_tx), runs
-// q.K^T, the witness dot product and P.V on tensor cores (mma.sync m16n8k16; the GQA group fills
-// the M = 16 rows), keeps one online-softmax state and the meter accumulators per query head, and
+// q.K^T, the witness dot product and P.V on tensor cores (mma.sync m16n8k16; the page's 16 tokens
+// are the M rows and the GQA group of up to 8 query heads the N columns), keeps one online-softmax
+// state and the meter accumulators per query head, and
 // writes a partial (m, l, acc, meter sums) for every (warp, unit) piece it covered.  The merge
 // kernel combines the pieces of each unit with log-sum-exp weights -- WitCert Sec. 6.2.2: the
 // certificate A is a p~-weighted average, so per-split values merged under the same LSE weights
@@ -18,7 +19,9 @@
 //     A - 1 = sum_t e^{x_t} (e^{c_t} - 1) / sum_t e^{x_t} = sum_t e^{x_t + c_t} (1 - e^{-c_t}) / sum_t e^{x_t}
 // as a running maximum and a scaled sum of e^{x_t + c_t - max} (1 - e^{-c_t}), i.e. in the log
 // domain, so c is never clipped and A never overflows; Tier B does the same with
-// u_t = sm_scale ||q|| s_t sqrt(2 ln(2S/delta_loc) / 12).
+// u_t = sm_scale s_t (||q|| kappa + ||q||_1 2^-11), kappa = sqrt(2 ln(2S/delta_loc) / 12) (the second
+// term covers the dither grid's bias), or with one scale per 32-channel group
+// u_t = sm_scale (kappa sqrt(sum_g ||q_g||^2 s_{g,t}^2) + 2^-11 sum_g ||q_g||_1 s_{g,t}).
 #pragma once
 
 #include "kvq_common.cuh"

@@ -76,3 +76,17 @@ def test_every_switch_counts_as_a_variant():
     # the --bypass switch turns the INT8 workload into one with a fixed-channel key bypass
     x = bench.W.reduced(bench.W.WORKLOADS["int8_7b_certified"], massive_pairs=4, massive_scale=30.0, bypass_pairs=4)
     assert bench.runs_a_variant(argparse.Namespace(**base), x)
+
+
+def test_kernel_fingerprint_ignores_comments_only():
+    code = "int f(int x) {\n  return x + 1;  // one\n}\n"
+    assert bench.code_only(code) == bench.code_only("/* header\n spanning lines */\n" + code.replace("// one", "// two"))
+    assert bench.code_only(code) == bench.code_only(code.replace("\n}", "\n\n   \n}"))
+    assert bench.code_only(code) != bench.code_only(code.replace("x + 1", "x + 2"))
+    texts = {f: open(os.path.join(ROOT, f), encoding="utf-8").read() for f in bench.KERNEL_SOURCES}
+    assert bench.kernel_hash(lambda f: texts[f]) == bench.kernel_hash()
+    f0 = bench.KERNEL_SOURCES[0]
+    edited = dict(texts, **{f0: texts[f0] + "\n// a trailing comment\n"})
+    assert bench.kernel_hash(lambda f: edited[f]) == bench.kernel_hash()
+    edited = dict(texts, **{f0: texts[f0] + "\nstatic int kvq_unused_probe;\n"})
+    assert bench.kernel_hash(lambda f: edited[f]) != bench.kernel_hash()
