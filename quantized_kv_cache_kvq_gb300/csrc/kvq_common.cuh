@@ -46,10 +46,12 @@ __host__ __device__ constexpr int outlier_tile_bytes(int m) { return m <= 0 ? 0 
 
 // ---------------------------------------------------------------------------------------------
 // Tile layouts (byte offsets inside one (page, kv head) tile; see include/kvq.h).
-// K tiles hold, per 16-byte word, one token and 8 (16-bit) or 16 (8-bit) consecutive channels:
-// the A fragments of S^T = K . Q^T.  V tiles hold, per lane of a 16-channel block, the tokens
-// 2c, 2c+1, 2c+8, 2c+9 of channels g and g+8: the A fragments of O^T = V^T . P^T.  Scales hold
-// tokens t and t+8 side by side (the two tokens a lane owns in S^T).
+// K tiles hold, per 16-byte word, one token and 8 (16-bit) or 16 (8-bit) channels -- consecutive,
+// or with 32-channel scale groups four runs of 4 from two groups -- the A fragments of S^T = K . Q^T.
+// V tiles hold, per lane of a 16-channel block, the tokens 2c, 2c+1, 2c+8, 2c+9 of channels g and
+// g+8: the A fragments of O^T = V^T . P^T.  Scales hold tokens t and t+8 side by side (the two
+// tokens a lane owns in S^T), one pair per 4-byte word and, with group scales, the four groups of
+// that pair in one 16-byte word.
 __host__ __device__ __forceinline__ int k16_offset(int t, int c) {
   return 16 * ((((t >> 3) * 4 + (c >> 5)) * 32) + (t & 7) * 4 + ((c >> 3) & 3)) + 2 * (c & 7);
 }
