@@ -636,6 +636,11 @@ def main():
     r = run_gpu(args, w)
     if r["rank"] != 0:
         return
+    print(json.dumps(bench_line(args, w, r)))
+
+
+def bench_line(args, w, r) -> dict:
+    """The JSON object of one bench run (rank 0) from run_gpu's result ``r``."""
     line = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": r["world"], "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
@@ -669,7 +674,7 @@ def main():
         if extra:
             line["cpu_baseline"]["sample"] += (f"; the plain decode of this workload (the oracle sample leaves out the "
                                                f"{', '.join(extra)} work of the GPU line)")
-    print(json.dumps(line))
+    return line
 
 
 if __name__ == "__main__":

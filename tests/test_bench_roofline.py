@@ -90,3 +90,73 @@ def test_kernel_fingerprint_ignores_comments_only():
     assert bench.kernel_hash(lambda f: edited[f]) == bench.kernel_hash()
     edited = dict(texts, **{f0: texts[f0] + "\nstatic int kvq_unused_probe;\n"})
     assert bench.kernel_hash(lambda f: edited[f]) != bench.kernel_hash()
+
+
+def _fake_run(w, traffic, e2e=True):
+    per_step = bench.step_bytes(w, bench.W.seq_lengths(w))
+    r = {"value": per_step / 5e-3 / 1e9, "ms_step": 5.0, "achieved": 6000.0, "graph": True, "layer_ms_mean": 0.14,
+         "call_ms_mean": 0.15, "layer_ms_median": 0.14, "peak": 6788.3, "peak_kind": "measured", "traffic": traffic,
+         "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}, "launches": 3 * 36 * 10 + 10,
+         "attended": 1.0e9, "per_step_bytes": per_step, "world": 1, "rank": 0, "counts": [0, 0, 0, 0],
+         "resident": w.n_layers}
+    if e2e:
+        r["e2e"] = {"value": 0.97 * r["value"], "unit": "GB/s", "h2d_bytes_per_step": 123, "d2h_bytes_per_step": 45}
+    return r
+
+
+def test_bench_line_carries_the_contract_keys(monkeypatch):
+    import sys
+
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--steps", "10", "--warmup", "3", "--no-cpu-baseline"])
+    args = bench.parse()
+    w = bench.W.WORKLOADS[args.workload]
+    rec = bench.traffic_record(w.name)
+    line = bench.bench_line(args, w, _fake_run(w, rec))
+    json.dumps(line)   # serialisable
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "roofline", "clocks", "gpu_launches", "e2e"):
+        assert k in line, k
+    assert line["n_gpus"] == 1 and line["steps"] == 10 and line["warmup"] == 3 and line["higher_is_better"] is True
+    assert line["scaling"] == "weak" and line["vs_baseline"] is None and line["data"] == "synthetic"
+    assert line["config"]["workload"] == "qwen3_8b_cartridge" and "l2" in line["config"]
+    ro = line["roofline"]
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in ro, k
+    assert ro["frac"] == pytest.approx(ro["achieved"] / ro["peak"])
+    assert ro["traffic"] == (rec["bytes_per_launch"] if rec else None)
+    assert set(line["e2e"]) >= {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
+    assert set(line["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    assert line["gpu_launches"] > 0 and "note" not in line and "cpu_baseline" not in line
+
+
+def test_bench_line_of_a_switch_and_a_profiling_run(monkeypatch):
+    import sys
+
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "int8_7b_certified", "--int8-groups", "--layers", "2",
+                                      "--no-cpu-baseline", "--no-e2e"])
+    args = bench.parse()
+    w = bench.W.reduced(bench.W.WORKLOADS["int8_7b_certified"], k_fmt="int8g32", v_fmt="int8g32")
+    line = bench.bench_line(args, w, _fake_run(w, bench.traffic_record(w.name, variant=bench.runs_a_variant(args, w)),
+                                               e2e=False))
+    assert line["roofline"]["traffic"] is None and line["roofline"]["bound"] == "hbm"
+    assert "not a bench line" in line["note"] and line["config"]["layout"] == "K int8g32 / V int8g32"
+
+
+def test_cpu_baseline_object():
+    w = bench.W.reduced(bench.W.WORKLOADS["tiny"], seq_len=256)
+    cb = bench.cpu_baseline(w, budget_s=0.2)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0 and cb["cores"] >= 1
+    assert "units of layer 0 at full context" in cb["sample"]
+
+
+def test_bench_line_cpu_baseline_branch(monkeypatch):
+    import sys
+
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--value-side"])
+    monkeypatch.setattr(bench, "cpu_baseline", lambda w: {"value": 0.03, "unit": "GB/s", "cores": 16, "kind": "oracle",
+                                                          "sample": "s"})
+    args = bench.parse()
+    w = bench.W.WORKLOADS[args.workload]
+    line = bench.bench_line(args, w, _fake_run(w, None))
+    assert line["cpu_baseline"]["kind"] == "oracle" and "value side" in line["cpu_baseline"]["sample"]
+    assert "value side" in line["config"]["meter"]
