@@ -44,8 +44,13 @@ METRIC = "decode-attn KV GB/s (% of GB300 HBM peak) with meter on; attended tok/
 SM_SCALE = float(np.float32(1.0 / math.sqrt(128)))
 # device sources of decode_split_kernel (the roofline kernel): its recorded DRAM traffic is valid only
 # for the code it was captured from (comments and blank lines aside)
+# and for its launch plan (decode.cu picks the warps per CTA, the stage count and the split plan) and build
+# flags (build.py)
 KERNEL_SOURCES = ["quantized_kv_cache_kvq_gb300/csrc/decode_kernel.cuh", "quantized_kv_cache_kvq_gb300/csrc/kvq_common.cuh",
-                  "quantized_kv_cache_kvq_gb300/csrc/decode_instances.inc"]
+                  "quantized_kv_cache_kvq_gb300/csrc/decode_instances.inc", "quantized_kv_cache_kvq_gb300/csrc/decode.cu",
+                  "quantized_kv_cache_kvq_gb300/build.py"]
+# the second workload the default run times after the headline (same steps and warm-up)
+SECOND_WORKLOAD = "int8_7b_certified"
 
 
 def parse():
@@ -78,6 +83,8 @@ def parse():
     p.add_argument("--layers", type=int, default=0, help="override layer count (profiling only; not a bench line)")
     p.add_argument("--batch", type=int, default=0,
                    help="override the batch (the first sequences of the workload; profiling only, not a bench line)")
+    p.add_argument("--no-second", action="store_true",
+                   help=f"time only the headline workload (the default run also times {SECOND_WORKLOAD} after it)")
     p.add_argument("--resident-layers", type=int, default=0,
                    help="keep only this many layers' caches in HBM and run every layer call on cache l %% R "
                         "(for workloads whose caches exceed HBM; each call still streams a full layer)")
@@ -137,13 +144,30 @@ def measured_peaks():
 
 
 # Issue roofline of a path bound by integer arithmetic and instruction issue (the INT8-dithered decode
-# regenerates every element's dither with Philox4x32-10): each of a GB300's 152 SMs has 4 schedulers
-# that each issue at most one warp-instruction per clock, at most 2070 MHz.
-GB300_SMS, GB300_SCHEDULERS_PER_SM, GB300_MAX_SM_MHZ = 152, 4, 2070.0
+# regenerates every element's dither with Philox4x32-10): each SM has 4 schedulers that each issue at most
+# one warp-instruction per clock.  The SM count is the device's (cudaDevAttrMultiProcessorCount through
+# torch) and the clock its maximum SM clock as nvidia-smi reports it during the run; the GB300 figures below
+# (152 SMs, 2070 MHz) stand in only where the device cannot be asked (CPU tests).
+SCHEDULERS_PER_SM = 4
+FALLBACK_SMS, FALLBACK_MAX_SM_MHZ = 152, 2070.0
 
 
-def issue_peak_winst_per_s(sm_mhz: float = GB300_MAX_SM_MHZ) -> float:
-    return GB300_SMS * GB300_SCHEDULERS_PER_SM * sm_mhz * 1e6
+def issue_peak_winst_per_s(sms: int, sm_mhz: float) -> float:
+    return sms * SCHEDULERS_PER_SM * sm_mhz * 1e6
+
+
+def max_sm_mhz(clocks: dict) -> tuple[float, str]:
+    """The SM clock ceiling for the issue peak: nvidia-smi's clocks.max.sm sampled during the run, else the
+    measured figure in MEASURED_PEAKS.json, else the GB300 maximum."""
+    if clocks and clocks.get("sm_max_mhz"):
+        return float(clocks["sm_max_mhz"]), "nvidia-smi clocks.max.sm during the run"
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("sm_max_mhz"):
+            return float(d["sm_max_mhz"]), "MEASURED_PEAKS.json sm_max_mhz"
+    return FALLBACK_MAX_SM_MHZ, "GB300 maximum SM clock (fallback)"
 
 
 def runs_a_variant(args, w) -> bool:
@@ -186,11 +210,20 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                                          "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
+
+    def wait_started(self, limit_s: float = 3.0):
+        """Return once nvidia-smi has written its first sample (or after ``limit_s``)."""
+        t0 = time.perf_counter()
+        while self.proc is not None and time.perf_counter() - t0 < limit_s:
+            self.fh.flush()
+            if os.path.exists(self.path) and os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.02)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -232,7 +265,7 @@ class Model:
     """All layers' caches of one workload, filled through kvq_append, plus the step's buffers."""
 
     def __init__(self, w, device, seed_base=0, n_layers=None, resident=0, value_side=False, shapes=False,
-                 gate=False, meter=True):
+                 gate=False, meter=True, lens=None):
         self.separate_append = False
         self.meter_on = meter
         self.value_side = value_side
@@ -245,7 +278,8 @@ class Model:
         self.L = n_layers or w.n_layers
         self.R = min(self.L, resident) if resident else self.L   # caches resident in HBM
         B, Hkv, Hq = w.batch, w.n_kv_heads, w.n_q_heads
-        self.lens = W.seq_lengths(w)
+        self.lens = W.seq_lengths(w) if lens is None else np.asarray(lens, dtype=np.int64)
+        assert len(self.lens) == B
         pages = (self.lens + W.PAGE - 1) // W.PAGE
         bt = W.block_table_for(w, self.lens)
         self.num_pages = int(pages.sum())
@@ -353,16 +387,50 @@ class Model:
         return self.L * (3 if self.separate_append else 2) + meter + (self.L if self.gate else 0)
 
 
-def run_gpu(args, w):
+def rank_share(w, rank: int, world: int):
+    """This rank's sequences of the job: the global batch is world x w.batch sequences (weak scaling: the
+    per-GPU work stays one workload's batch), assigned to ranks by ``dist.shard_sequences`` (balanced
+    attended tokens, deterministic).  Returns (the rank's workload, its live lengths, its global sequence
+    indices).  The units are independent, so no collective touches the data path."""
+    from quantized_kv_cache_kvq_gb300.dist import shard_sequences
+
+    if world == 1:
+        lens = W.seq_lengths(w)
+        return w, lens, np.arange(len(lens))
+    lens_g = W.seq_lengths(W.reduced(w, batch=w.batch * world))
+    idx = shard_sequences(lens_g, world, prefix_len=w.prefix_len)[rank]
+    return W.reduced(w, batch=len(idx)), lens_g[idx], idx
+
+
+def job_totals(per_rank, counts, world: int, cpu_group=None):
+    """Sum the ranks' per-step figures (step bytes, attended tokens, ...) and meter counters over the ranks
+    (host-side, after the timed region)."""
+    vals = [float(x) for x in np.atleast_1d(per_rank)]
+    if world == 1:
+        return vals, [int(c) for c in counts]
+    import torch
+    import torch.distributed as dist
+
+    from quantized_kv_cache_kvq_gb300.dist import reduce_meter_counts
+
+    t = torch.tensor(vals, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=cpu_group)
+    return t.tolist(), [int(c) for c in reduce_meter_counts(counts, group=cpu_group).tolist()]
+
+
+def run_gpu(args, w, init_dist=True):
     import torch
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    cpu_group = None
     if world > 1:
         import torch.distributed as dist
 
-        dist.init_process_group("nccl")
+        if init_dist and not dist.is_initialized():
+            dist.init_process_group("nccl")
+        cpu_group = dist.new_group(backend="gloo")  # host-side sums (meter counters, step bytes)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import quantized_kv_cache_kvq_gb300 as kvq
@@ -373,10 +441,12 @@ def run_gpu(args, w):
         resident = 4  # 36 layers of this workload need ~413 GB of cache: rotate 4 resident layers
     if args.meter_off and (args.value_side or args.shapes or args.gate):
         raise SystemExit("--meter-off excludes the meter's extensions")
-    m = Model(w, dev, seed_base=rank, n_layers=args.layers or None, resident=resident, value_side=args.value_side,
-              shapes=args.shapes, gate=args.gate, meter=not args.meter_off)
+    wr, lens, _ = rank_share(w, rank, world)
+    m = Model(wr, dev, seed_base=rank, n_layers=args.layers or None, resident=resident, value_side=args.value_side,
+              shapes=args.shapes, gate=args.gate, meter=not args.meter_off, lens=lens)
     m.separate_append = args.separate_append
-    per_step_bytes = step_bytes(w, m.lens, value_side=args.value_side, meter=not args.meter_off) * m.L // w.n_layers
+    per_step_bytes = step_bytes(wr, m.lens, value_side=args.value_side, meter=not args.meter_off) * m.L // w.n_layers
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     def barrier():
         if world > 1:
@@ -397,6 +467,13 @@ def run_gpu(args, w):
         barrier()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        # the sampler needs a moment to start; untimed steps keep the GPU loaded meanwhile, so the samples
+        # bracket the timed region under the same load
+        clk.wait_started()
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 0.3:
+            graph.replay() if graph is not None else m.step()
+            torch.cuda.synchronize()
         barrier()
         start.record()
         for s in range(args.steps):
@@ -429,24 +506,24 @@ def run_gpu(args, w):
     if m.err.item() != 0:
         raise RuntimeError(f"device error {kvq.STATUS.get(m.err.item())}")
     ms_step = ms / args.steps
-    value = per_step_bytes * world / (ms_step * 1e-3) / 1e9
+    rank_attended = float(np.sum(m.lens) + w.prefix_len * wr.batch) * m.L * w.n_kv_heads
+    (job_bytes, attended), job_counts = job_totals([per_step_bytes, rank_attended], m.counts.cpu().tolist(), world,
+                                                   cpu_group)
+    value = job_bytes / (ms_step * 1e-3) / 1e9
     layer_ms = [e[2].elapsed_time(e[3]) for st in events for e in st]
     call_ms = [e[0].elapsed_time(e[1]) for st in events for e in st]
     layer_bytes = per_step_bytes / m.L
     achieved = layer_bytes / (statistics.mean(layer_ms) * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     tr = traffic_record(w.name, variant=runs_a_variant(args, w))
-    attended = float(np.sum(m.lens) + w.prefix_len * w.batch) * m.L * w.n_kv_heads
     res = dict(value=value, ms_step=ms_step, achieved=achieved, graph=graph is not None, layer_ms_mean=statistics.mean(layer_ms),
                call_ms_mean=statistics.mean(call_ms),
                layer_ms_median=statistics.median(layer_ms), peak=peak, peak_kind=peak_kind, traffic=tr,
                clocks=clk.summary(), launches=m.launches_per_step() * args.steps, attended=attended,
-               per_step_bytes=per_step_bytes, world=world, rank=rank, counts=m.counts.cpu().tolist(),
-               resident=m.R)
+               per_step_bytes=per_step_bytes, world=world, rank=rank, counts=job_counts, sms=sms,
+               resident=m.R, job_bytes=job_bytes, rank_batch=wr.batch)
     if not args.no_e2e:
-        res["e2e"] = run_e2e(args, m, per_step_bytes, world, use_graph=graph is not None)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+        res["e2e"] = run_e2e(args, m, per_step_bytes, world, use_graph=graph is not None, cpu_group=cpu_group)
     return res
 
 
@@ -465,11 +542,14 @@ def roofline_of(r, w, args) -> dict:
     if not rec or rec.get("bound") != "alu":
         return hbm
     achieved = rec["warp_inst_per_launch"] / launch_s
-    peak = issue_peak_winst_per_s()
+    sms = int(r.get("sms") or FALLBACK_SMS)
+    mhz, mhz_src = max_sm_mhz(r.get("clocks"))
+    peak = issue_peak_winst_per_s(sms, mhz)
+    sms_src = "the device's SM count" if r.get("sms") else "GB300 SM count (fallback)"
     out = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "warp-instructions/s", "frac": achieved / peak,
            "traffic": rec["bytes_per_launch"], "kernel": hbm["kernel"],
-           "peak_source": f"{GB300_SMS} SMs x {GB300_SCHEDULERS_PER_SM} schedulers x 1 warp-instruction/clock x "
-                          f"{GB300_MAX_SM_MHZ:.0f} MHz",
+           "peak_source": f"{sms} SMs ({sms_src}) x {SCHEDULERS_PER_SM} schedulers x 1 warp-instruction/clock x "
+                          f"{mhz:.0f} MHz ({mhz_src})",
            "warp_inst_per_launch": rec["warp_inst_per_launch"],
            "hbm_achieved_gbs": r["achieved"], "hbm_frac": r["achieved"] / r["peak"],
            "algorithmic_bytes_per_launch": hbm["algorithmic_bytes_per_launch"],
@@ -477,7 +557,7 @@ def roofline_of(r, w, args) -> dict:
     return out
 
 
-def run_e2e(args, m, per_step_bytes, world, use_graph=True):
+def run_e2e(args, m, per_step_bytes, world, use_graph=True, cpu_group=None):
     """Same metric through the public API with pinned host buffers and copies in the timed region."""
     torch = m.torch
     hq = torch.empty(m.q.shape, dtype=m.q.dtype, pin_memory=True).copy_(m.q)
@@ -516,7 +596,15 @@ def run_e2e(args, m, per_step_bytes, world, use_graph=True):
     el = (time.perf_counter() - t0) / args.steps
     h2d = (hq.numel() * hq.element_size() + hk.numel() * 4 + hv.numel() * 4)
     d2h = ho.numel() * 4 + ((hm.numel() * 4 + 16) if m.meter_on else 0)
-    return {"value": per_step_bytes * world / el / 1e9, "unit": "GB/s", "ms_per_step": el * 1e3,
+    job_bytes = per_step_bytes
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([el], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX, group=cpu_group)
+        el = float(t.item())
+        (job_bytes,), _ = job_totals([per_step_bytes], [0, 0, 0, 0], world, cpu_group)
+    return {"value": job_bytes / el / 1e9, "unit": "GB/s", "ms_per_step": el * 1e3,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
@@ -562,7 +650,8 @@ def oracle_units(w, n_units: int, seed_base: int = 0):
     return total_bytes, elapsed
 
 
-def host_threads() -> int:
+def blas_threads() -> int:
+    """Threads of the BLAS pool the oracle's matrix products run on."""
     try:
         import threadpoolctl
 
@@ -573,12 +662,17 @@ def host_threads() -> int:
         return os.cpu_count() or 1
 
 
+def host_cores() -> dict:
+    """The host's logical CPUs (os.cpu_count()) and the BLAS threads the oracle actually used."""
+    return {"cores": os.cpu_count() or 1, "blas_threads": blas_threads()}
+
+
 def cpu_baseline(w, budget_s: float = 15.0):
     """Oracle GB/s on a bounded sample: as many full-context units as fit in ~budget_s."""
     b1, t1 = oracle_units(w, 1)
     n = max(1, min(4 * w.n_kv_heads, int(budget_s / max(t1, 1e-3))))
     b, t = oracle_units(w, n, seed_base=1)
-    return {"value": b / t / 1e9, "unit": "GB/s", "cores": host_threads(), "kind": "oracle",
+    return {"value": b / t / 1e9, "unit": "GB/s", **host_cores(), "kind": "oracle",
             "sample": f"{n} (sequence, kv head) units of layer 0 at full context ({w.name}): float64 oracle "
                       f"dequantize + compressed/exact attention + TV + meter; {b / 1e6:.1f} MB of KV in {t:.1f} s"}
 
@@ -599,21 +693,42 @@ def run_reference(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": host_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "GB/s", **host_cores(), "kind": "oracle",
                              "sample": f"each step: one (sequence, kv head) unit of layer 0 at full context"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
 
-def workload_config(w):
-    lens = W.seq_lengths(w)
-    cfg = {"workload": w.name, "batch": w.batch, "layers": w.n_layers, "kv_heads": w.n_kv_heads,
+def workload_config(w, world: int = 1):
+    """The workload of a line: with N ranks the job is a global batch of N x w.batch sequences, sharded by
+    balanced attended tokens (``dist.shard_sequences``)."""
+    lens = W.seq_lengths(W.reduced(w, batch=w.batch * world))
+    cfg = {"workload": w.name, "batch": w.batch * world, "layers": w.n_layers, "kv_heads": w.n_kv_heads,
            "q_heads": w.n_q_heads, "head_dim": 128, "page_size": 16,
            "layout": f"K {w.k_fmt} / V {w.v_fmt}", "meter": "tier A" + (" + tier B" if w.tier_b else ""),
            "context_tokens": int(lens.mean()) + w.prefix_len, "l2": "inputs larger than L2 (no flush)"}
+    if world > 1:
+        cfg["batch_per_gpu"] = w.batch
+        cfg["parallelism"] = f"dp{world}: sequences sharded across ranks by attended tokens, no data-path collective"
     if w.prefix_len:
         cfg["prefix"] = f"{w.prefix_len} shared tokens, K {w.prefix_k_fmt} / V {w.prefix_v_fmt}, sink x{w.sink_scale:g}"
     return cfg
+
+
+def times_second_workload(args) -> bool:
+    """The default run (the headline workload with no switch) also times the second target workload."""
+    return (args.workload == "qwen3_8b_cartridge" and not args.no_second and not args.layers and not args.batch
+            and not args.resident_layers and not args.separate_append and not args.eager
+            and not runs_a_variant(args, W.WORKLOADS[args.workload]) and not args.bypass)
+
+
+def second_object(args, w, r) -> dict:
+    """The second target workload's figures, timed in the same process after the headline with the same
+    steps and warm-up: its own value, step time, roofline (issue and HBM), clocks, e2e and cpu baseline."""
+    line = bench_line(args, w, r)
+    keep = ("value", "unit", "ms_per_step", "pct_of_hbm_peak", "attended_kv_tok_per_s", "seq_tok_per_s", "roofline",
+            "clocks", "e2e", "config", "gpu_launches", "meter_counts", "launch_mode", "cpu_baseline")
+    return {k: line[k] for k in keep if k in line}
 
 
 def main():
@@ -634,18 +749,33 @@ def main():
         run_reference(args, w)
         return
     r = run_gpu(args, w)
-    if r["rank"] != 0:
-        return
-    print(json.dumps(bench_line(args, w, r)))
+    line = bench_line(args, w, r) if r["rank"] == 0 else None
+    if times_second_workload(args):
+        import gc
+
+        import torch
+
+        gc.collect()
+        torch.cuda.empty_cache()   # the headline's caches are released before the second workload's are built
+        w2 = W.WORKLOADS[SECOND_WORKLOAD]
+        r2 = run_gpu(args, w2)
+        if line is not None:
+            line[SECOND_WORKLOAD] = second_object(args, w2, r2)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line))
 
 
 def bench_line(args, w, r) -> dict:
     """The JSON object of one bench run (rank 0) from run_gpu's result ``r``."""
     line = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": r["world"], "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w, r["world"]),
             "pct_of_hbm_peak": 100.0 * r["value"] / r["world"] / r["peak"],
-            "attended_kv_tok_per_s": r["attended"] * r["world"] / (r["ms_step"] * 1e-3),
+            "attended_kv_tok_per_s": r["attended"] / (r["ms_step"] * 1e-3),
             "seq_tok_per_s": w.batch * r["world"] / (r["ms_step"] * 1e-3),
             "roofline": roofline_of(r, w, args),
             "gpu_launches": r["launches"], "clocks": r["clocks"], "meter_counts": r["counts"],

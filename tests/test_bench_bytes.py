@@ -33,7 +33,7 @@ def test_token_head_bytes_match_the_oracle(k_fmt, v_fmt):
         assert bench.token_head_bytes(k_fmt, v_fmt, bypass=m) == base + extra
 
 
-def test_survey_table_of_bytes_per_token_head():
+def test_bytes_per_token_head_of_each_layout():
     # K16/V8 418 B, BF16/BF16 544 B, INT8-dither 292 B, K8/V8 raw 288 B (witness and scales included)
     assert bench.token_head_bytes("bf16", "e4m3s") == 418
     assert bench.token_head_bytes("bf16", "bf16") == 544
@@ -69,7 +69,7 @@ def test_step_bytes_match_the_oracle(name):
     assert bench.step_bytes(w, lens) == want
 
 
-def test_cartridge_step_is_the_surveyed_30_gb():
+def test_cartridge_step_is_30_gb():
     w = W.WORKLOADS["qwen3_8b_cartridge"]
     b = bench.step_bytes(w, W.seq_lengths(w))
     # 36 x (16 x 11,996 x 8 x 544 + 632 x 8 x 418) bytes

@@ -3,14 +3,16 @@
 * a committed ncu record is used only while its hash is the current decode sources' hash (else the bench
   line carries `traffic` null), and a used record is consistent (bytes, no re-reads);
 * a record marked "alu" turns the roofline into the issue roofline (warp-instructions per second against
-  152 SMs x 4 schedulers x 1 per clock x 2070 MHz) with the HBM figures alongside; without a record the
-  roofline is the HBM one against the measured copy peak and `traffic` is null;
+  the device's SMs x 4 schedulers x 1 per clock x its maximum SM clock) with the HBM figures alongside;
+  without a record the roofline is the HBM one against the measured copy peak and `traffic` is null;
+* the default run carries the second target workload; N ranks shard a global batch of N x B sequences;
 * runs with a switch (value side, shapes, gate, bypass, meter off) never reuse the plain kernel's record.
 """
 import argparse
 import json
 import os
 
+import numpy as np
 import pytest
 
 import bench
@@ -61,10 +63,21 @@ def test_issue_roofline_with_an_alu_record():
     r = bench.roofline_of(_result(layer_ms=0.5, traffic=rec), w, _args())
     assert r["bound"] == "alu" and r["unit"] == "warp-instructions/s"
     assert r["achieved"] == pytest.approx(600_000_000 / 0.5e-3)
-    assert r["peak"] == pytest.approx(152 * 4 * 2070e6)
+    # no device figures in the result: the GB300 fallback (or the measured maximum clock) is named
+    assert r["peak"] == pytest.approx(152 * 4 * bench.max_sm_mhz(None)[0] * 1e6)
+    assert "fallback" in r["peak_source"]
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
     assert r["traffic"] == 510_000_000
     assert r["hbm_achieved_gbs"] == 1000.0 and r["hbm_frac"] == pytest.approx(1000.0 / 6788.3)
+
+
+def test_issue_peak_uses_the_device_sm_count_and_sampled_clock():
+    w = bench.W.WORKLOADS["int8_7b_certified"]
+    rec = {"bound": "alu", "warp_inst_per_launch": 600_000_000, "bytes_per_launch": 510_000_000}
+    res = dict(_result(layer_ms=0.5, traffic=rec), sms=148, clocks={"sm_mhz": 1800.0, "sm_max_mhz": 1965.0})
+    r = bench.roofline_of(res, w, _args())
+    assert r["peak"] == pytest.approx(148 * 4 * 1965e6)
+    assert "148 SMs (the device's SM count)" in r["peak_source"] and "clocks.max.sm" in r["peak_source"]
 
 
 def test_every_switch_counts_as_a_variant():
@@ -145,8 +158,48 @@ def test_bench_line_of_a_switch_and_a_profiling_run(monkeypatch):
 def test_cpu_baseline_object():
     w = bench.W.reduced(bench.W.WORKLOADS["tiny"], seq_len=256)
     cb = bench.cpu_baseline(w, budget_s=0.2)
-    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0 and cb["cores"] >= 1
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0
+    assert cb["cores"] == os.cpu_count() and cb["blas_threads"] >= 1
     assert "units of layer 0 at full context" in cb["sample"]
+
+
+def test_default_run_carries_the_second_target_workload(monkeypatch):
+    import sys
+
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--steps", "10", "--warmup", "3", "--no-cpu-baseline"])
+    args = bench.parse()
+    assert bench.times_second_workload(args)
+    w2 = bench.W.WORKLOADS[bench.SECOND_WORKLOAD]
+    rec = {"bound": "alu", "warp_inst_per_launch": 500_000_000, "bytes_per_launch": 2_456_000_000}
+    obj = bench.second_object(args, w2, dict(_fake_run(w2, rec), sms=152))
+    json.dumps(obj)
+    for k in ("value", "unit", "ms_per_step", "roofline", "clocks", "e2e", "config"):
+        assert k in obj, k
+    assert obj["config"]["workload"] == "int8_7b_certified" and obj["config"]["meter"] == "tier A + tier B"
+    assert obj["roofline"]["bound"] == "alu" and "hbm_frac" in obj["roofline"]
+    # a switch, a profiling shape or another workload times only what was asked for
+    for extra in (["--value-side"], ["--layers", "2"], ["--batch", "4"], ["--workload", "tiny"], ["--no-second"],
+                  ["--eager"], ["--separate-append"]):
+        monkeypatch.setattr(sys, "argv", ["bench.py", *extra])
+        assert not bench.times_second_workload(bench.parse()), extra
+
+
+@pytest.mark.parametrize("name", ["qwen3_8b_cartridge", "ragged_paged"])
+def test_rank_shares_partition_the_global_batch(name):
+    w = bench.W.WORKLOADS[name]
+    w1, lens1, idx1 = bench.rank_share(w, 0, 1)
+    assert w1 is w and np.array_equal(lens1, bench.W.seq_lengths(w)) and np.array_equal(idx1, np.arange(w.batch))
+    for world in (2, 4):
+        lens_g = bench.W.seq_lengths(bench.W.reduced(w, batch=w.batch * world))
+        shares = [bench.rank_share(w, r, world) for r in range(world)]
+        allidx = np.sort(np.concatenate([s[2] for s in shares]))
+        assert np.array_equal(allidx, np.arange(w.batch * world))           # every sequence on exactly one rank
+        for wr, lens, idx in shares:
+            assert wr.batch == len(idx) and np.array_equal(lens, lens_g[idx])
+        if name == "qwen3_8b_cartridge":
+            assert all(s[0].batch == w.batch for s in shares)                # fixed lengths: equal shares
+        cfg = bench.workload_config(w, world)
+        assert cfg["batch"] == w.batch * world and cfg["batch_per_gpu"] == w.batch and "dp" in cfg["parallelism"]
 
 
 def test_bench_line_cpu_baseline_branch(monkeypatch):

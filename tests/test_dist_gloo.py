@@ -64,3 +64,46 @@ def test_two_rank_gloo_reduce():
     assert sorted(shards[0] + shards[1]) == list(range(16))
     for _, _, tot in res:
         assert tot == [8, 0, 1, 16 * 32]
+
+
+def _bench_rank(rank, world, port, q):
+    """One rank of bench.py's multi-GPU path, host side: its share of the global batch and the job totals."""
+    import torch.distributed as dist
+
+    import bench
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w = bench.W.WORKLOADS["ragged_paged"]
+    wr, lens, idx = bench.rank_share(w, rank, world)
+    step = bench.step_bytes(wr, lens)
+    counts = [rank, 0, 0, int(wr.batch) * w.n_layers * w.n_q_heads]
+    (tot_bytes, tot_tokens), tot_counts = bench.job_totals([step, float(lens.sum())], counts, world)
+    q.put((rank, idx.tolist(), step, tot_bytes, tot_tokens, tot_counts))
+    dist.destroy_process_group()
+
+
+def test_two_rank_bench_path():
+    """bench.py --gpus 2 on CPU ranks: the global batch is split by shard_sequences, the step bytes and meter
+    counters are summed over the ranks, and the totals equal those of the whole global batch."""
+    import bench
+
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_bench_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    w = bench.W.WORKLOADS["ragged_paged"]
+    wg = bench.W.reduced(w, batch=2 * w.batch)
+    lens_g = bench.W.seq_lengths(wg)
+    assert sorted(res[0][1] + res[1][1]) == list(range(2 * w.batch))
+    for _, _, _, tot_bytes, tot_tokens, tot_counts in res:
+        assert tot_bytes == res[0][2] + res[1][2] == bench.step_bytes(wg, lens_g)
+        assert tot_tokens == float(lens_g.sum())
+        assert tot_counts == [1, 0, 0, 2 * w.batch * w.n_layers * w.n_q_heads]
