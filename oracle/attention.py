@@ -203,7 +203,8 @@ def meter_from_log_am1(lam1) -> np.ndarray:
 def raw_log_score(lam1) -> np.ndarray:
     """ln(1/2 (A^2 - 1)) = ln(A-1) + ln(A+1) - ln 2, finite for any finite ln(A-1) (WitCert §4.3)."""
     lam1 = np.asarray(lam1, dtype=np.float64)
-    return lam1 + np.logaddexp(math.log(2.0), lam1) - math.log(2.0)
+    with np.errstate(invalid="ignore"):   # NaN states (non-finite inputs) stay NaN
+        return lam1 + np.logaddexp(math.log(2.0), lam1) - math.log(2.0)
 
 
 @dataclass

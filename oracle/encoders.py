@@ -117,7 +117,8 @@ def fp16_bits(x: np.ndarray, mode: str = "rne") -> np.ndarray:
     10 fraction bits, smallest normal 2**-14, subnormal spacing 2**-24.
     Overflow follows IEEE: round-to-nearest overflows to inf at or above
     65520 (the midpoint past 65504); round-up overflows to inf above 65504
-    (and a negative value never rounds up to -inf).
+    (and a finite negative value never rounds up to -inf); an infinity converts
+    to the infinity of its sign in either mode.
     """
     x = np.asarray(x, dtype=np.float64)
     r = round_to_grid(x, 10, -14, mode)
@@ -127,7 +128,8 @@ def fp16_bits(x: np.ndarray, mode: str = "rne") -> np.ndarray:
         r = np.where(over, np.where(sign, -np.inf, np.inf), r)
     elif mode == "ru":
         r = np.where(r > _FP16_MAX, np.inf, r)
-        r = np.where(r < -_FP16_MAX, -_FP16_MAX, r)
+        # a finite value below -65504 rounds up to -65504; -inf itself converts to -inf
+        r = np.where((r < -_FP16_MAX) & np.isfinite(r), -_FP16_MAX, r)
     else:
         raise ValueError(mode)
     # r is exactly representable in binary16 (or +-inf/nan): the numpy cast of an

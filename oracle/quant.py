@@ -41,7 +41,8 @@ Readings where the pages are silent
   once): t = fp32(amax / 126.5) (or / 448), s = fp16_rn(t), y = fp32(x / s),
   y2 = fp32(y + xi), code = clamp(round_half_even(y2), -127, 127).
 * amax = 0 (or a scale that rounds to fp16 zero) stores scale 0 and all-zero codes.
-* The fp16 witness is rounded up, so it never under-states the residual norm.
+* The fp16 witness is the exact residual norm rounded up, so it never under-states
+  it: the smallest binary16 value whose square is at least the exact sum of squares.
 * FP8-scaled values use s = fp16_rn(fp32(amax / 448)) and code = e4m3(fp32(v / s))
   (round-to-nearest-even, saturating at +-448).
 * A channel group is G_c contiguous channels in storage order, group g = channels
@@ -77,6 +78,7 @@ __all__ = [
     "quantize_int8_groups",
     "dequantize_int8_groups",
     "band_norms",
+    "norm_fp16_ru_bits",
 ]
 
 HEAD_DIM = 128
@@ -236,19 +238,97 @@ def band_norms(r: np.ndarray) -> np.ndarray:
     return np.sqrt(np.sum(lo * lo, axis=-1) + np.sum(hi * hi, axis=-1))
 
 
-def value_witness_bits(v_hat: np.ndarray, v32: np.ndarray) -> np.ndarray:
-    """Value witness [..., 2] fp16 (round-up) patterns: (||v_hat - v||, ||v||) over the 128 channels.
+_SQ16 = None
 
-    Rounded up so that neither the value reconstruction error nor the value norm is under-stated.
+
+def _fp16_squares() -> np.ndarray:
+    """h * h for every non-negative binary16 value h, in bit-pattern order 0x0000 .. 0x7C00 (+inf last).
+
+    Positive binary16 values increase with their bit pattern, and the square of a value with 11
+    significant bits is exact in float64, so the table is an exact, increasing list of squares.
     """
+    global _SQ16
+    if _SQ16 is None:
+        h = fp16_value(np.arange(0x7C01, dtype=np.uint16))
+        _SQ16 = h * h
+    return _SQ16
+
+
+def norm_fp16_ru_bits(a_hat: np.ndarray, a: np.ndarray) -> np.ndarray:
+    """binary16 pattern of ||a_hat - a|| over the last axis, rounded up, of the EXACT norm.
+
+    The result is the smallest non-negative binary16 value h (+inf above 65504) with
+    h^2 >= sum_i (a_hat_i - a_i)^2, the sum taken in exact arithmetic.  a_hat and a hold exact
+    values (a binary32 input, a decoded code).  Rows with a non-finite input give the NaN pattern.
+
+    The comparison is made first against a float64 bracket [T_lo, T_hi] of the exact sum of
+    squares (TwoSum gives each difference exactly as d + e; the relative error of sum d^2 is below
+    (n + 4) 2^-52 for n terms; the bracket is twice that wide).  A row whose bracket holds no
+    binary16 square between h's predecessor and h is decided by it; any other row is decided in
+    exact rational arithmetic (``fractions.Fraction``).
+    """
+    x = np.asarray(a_hat, dtype=np.float64)
+    y = np.asarray(a, dtype=np.float64)
+    x, y = np.broadcast_arrays(x, y)
+    n = x.shape[-1]
+    finite = np.all(np.isfinite(x) & np.isfinite(y), axis=-1)
+    xs = np.where(np.isfinite(x) & np.isfinite(y), x, 0.0)
+    ys = np.where(np.isfinite(x) & np.isfinite(y), y, 0.0)
+    d = xs - ys
+    # TwoSum(xs, -ys): d + e == xs - ys exactly
+    bp = d - xs
+    e = (xs - (d - bp)) + (-ys - bp)
+    exact_zero = np.all((d == 0) & (e == 0), axis=-1)
+    T = np.sum(d * d, axis=-1)
+    eps = (n + 4) * 2.0 ** -52
+    t_lo, t_hi = T * (1.0 - 2 * eps), T * (1.0 + 2 * eps)
+    sq = _fp16_squares()
+    hi = np.searchsorted(sq, t_hi, side="left")
+    lo = np.searchsorted(sq, t_lo, side="left")
+    out = hi.astype(np.int64)
+    pred = np.maximum(hi - 1, 0)
+    decided = (hi == 0) | (sq[pred] < t_lo)
+    out = np.where(exact_zero, 0, out)
+    todo = np.flatnonzero(~decided & ~exact_zero & finite)
+    if todo.size:
+        from fractions import Fraction
+
+        shape = out.shape
+        out = out.reshape(-1)
+        flat_x, flat_y = xs.reshape(-1, n), ys.reshape(-1, n)
+        lo_f, hi_f = lo.reshape(-1), hi.reshape(-1)
+        for i in todo:
+            t_exact = sum((Fraction(float(u)) - Fraction(float(v))) ** 2 for u, v in zip(flat_x[i], flat_y[i]))
+            k = int(lo_f[i])   # the answer lies in [lo, hi]: sq[lo - 1] < t_lo <= t_exact <= t_hi <= sq[hi]
+            while k < int(hi_f[i]) and Fraction(float(sq[k])) < t_exact:
+                k += 1
+            out[i] = k
+        out = out.reshape(shape)
+    out = np.where(finite, out, 0x7E00)
+    return out.astype(np.uint16)
+
+
+def _band_view(x: np.ndarray) -> np.ndarray:
+    """[..., 128] -> [..., 16 bands, 8]: band b holds channels 4b..4b+3 and 64+4b..64+4b+3."""
+    half = HEAD_DIM // 2
+    per = half // N_BANDS
+    lo = x[..., :half].reshape(x.shape[:-1] + (N_BANDS, per))
+    hi = x[..., half:].reshape(x.shape[:-1] + (N_BANDS, per))
+    return np.concatenate([lo, hi], axis=-1)
+
+
+def value_witness_bits(v_hat: np.ndarray, v32: np.ndarray) -> np.ndarray:
+    """Value witness [..., 2] fp16 (round-up) patterns: (||v_hat - v||, ||v||) over the 128 channels, each
+    the exact norm rounded up, so that neither the value reconstruction error nor the value norm is
+    under-stated."""
     v = np.asarray(v32, dtype=np.float32).astype(np.float64)
-    r = np.asarray(v_hat, dtype=np.float64) - v
-    rho = np.sqrt(np.sum(r * r, axis=-1))
-    vn = np.sqrt(np.sum(v * v, axis=-1))
-    return np.stack([fp16_bits(rho, "ru"), fp16_bits(vn, "ru")], axis=-1)
+    vh = np.asarray(v_hat, dtype=np.float64)
+    return np.stack([norm_fp16_ru_bits(vh, v), norm_fp16_ru_bits(v, np.zeros_like(v))], axis=-1)
 
 
 def witness_bits(k_hat: np.ndarray, k32: np.ndarray) -> np.ndarray:
-    """fp16 (round-up) patterns of the band norms of r = k_hat - k (WitCert §4.1, eq. (2))."""
-    r = np.asarray(k_hat, dtype=np.float64) - np.asarray(k32, dtype=np.float32).astype(np.float64)
-    return fp16_bits(band_norms(r), "ru")
+    """fp16 patterns of the band norms of r = k_hat - k (WitCert §4.1, eq. (2)): each the exact
+    norm of the band's residual, rounded up."""
+    kh = np.asarray(k_hat, dtype=np.float64)
+    k = np.asarray(k32, dtype=np.float32).astype(np.float64)
+    return norm_fp16_ru_bits(_band_view(kh), _band_view(k))

@@ -61,6 +61,9 @@ def test_fp16_ru_is_smallest_upper_bound():
     # overflow past the largest finite value rounds up to +inf
     assert np.isinf(fp16_value(fp16_bits(np.array([65504.5]), "ru")))[0]
     assert fp16_value(fp16_bits(np.array([-70000.0]), "ru"))[0] == -65504.0
+    # infinities convert to themselves in both modes (IEEE 754 conversion of an infinity)
+    for mode in ("rne", "ru"):
+        assert list(fp16_bits(np.array([np.inf, -np.inf]), mode)) == [0x7C00, 0xFC00]
 
 
 def test_e4m3_decoder_matches_torch_for_all_codes():

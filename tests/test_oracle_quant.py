@@ -7,8 +7,11 @@ What pins what:
   is the one quantized with (a row whose amax makes fp32 and fp16 scales differ).
 * E4M3 scaled: reconstruction error <= half an E4M3 step at each value.
 * BF16 keys: residual <= 2^-9 relative; bf16-representable keys give witness 0.
-* Witness: the smallest fp16 at or above the exact band norm (checked with
-  exact rational arithmetic on a sample); band membership by RoPE pairs.
+* Witness and value witness: the smallest fp16 at or above the exact norm, equal
+  to a binary search in exact rationals on random rows (binary32 subnormals to
+  1e35), on near-ties built to defeat the float64 bracket (h^2 + tiny, exact
+  squares, a 3-4-5 triple), at the overflow edge and for non-finite rows; band
+  membership by RoPE pairs.
 * Lemma 1 (RoPE band unitarity): the band norms of a rotated residual equal
   those of the unrotated one.
 """
@@ -138,3 +141,93 @@ def test_nonfinite_and_overflow_rows_flagged():
     _, _, valid = quantize(x, "e4m3s")
     # 3e7 / 448 = 66,964 is past the fp16 round-to-nearest overflow threshold 65,520
     assert list(valid) == [False, False, True]
+
+
+# ------------------------------------------------------------------ exact norms rounded up to fp16
+def _fp16_ru_norm_brute(a_hat, a):
+    """The definition in exact rationals: the smallest non-negative binary16 value (bit pattern) whose
+    square is at least sum (a_hat - a)^2; +inf (0x7C00) when none is."""
+    t = sum((Fraction(float(u)) - Fraction(float(v))) ** 2 for u, v in zip(a_hat, a))
+    lo, hi = 0, 0x7C00        # binary search over the increasing positive binary16 patterns
+    while lo < hi:
+        mid = (lo + hi) // 2
+        h = Fraction(float(np.uint16(mid).view(np.float16)))
+        if h * h >= t:
+            hi = mid
+        else:
+            lo = mid + 1
+    return lo
+
+
+def _brute_rows(xh, x):
+    return np.array([_fp16_ru_norm_brute(u, v) for u, v in zip(xh.reshape(-1, xh.shape[-1]),
+                                                               x.reshape(-1, x.shape[-1]))]).reshape(xh.shape[:-1])
+
+
+@pytest.mark.parametrize("n", [1, 8, 128])
+def test_exact_norm_matches_rational_brute_force(n):
+    from oracle.quant import norm_fp16_ru_bits
+
+    rng = np.random.default_rng(n)
+    rows = 300 if n < 128 else 60
+    # magnitudes from binary32 subnormals to 1e35, mixed within rows
+    mag = 10.0 ** rng.uniform(-44, 35, (rows, n))
+    x = (rng.standard_normal((rows, n)) * mag).astype(np.float32).astype(np.float64)
+    xh = np.where(rng.random((rows, n)) < 0.5, x, (x * (1 + rng.standard_normal((rows, n)) * 1e-3)).astype(np.float32))
+    got = norm_fp16_ru_bits(xh, x)
+    assert np.array_equal(got, _brute_rows(xh, x))
+
+
+def test_exact_norm_decides_near_ties_exactly():
+    """Rows whose float64 bracket holds an fp16 square: the answer still follows the exact sum."""
+    from oracle.quant import norm_fp16_ru_bits
+
+    cases, want = [], []
+    for hb in (0x0001, 0x03FF, 0x1C00, 0x3555, 0x3C00, 0x7BFE):
+        h = float(np.uint16(hb).view(np.float16))
+        tiny = h * 2.0 ** -70
+        cases.append([h, tiny, 0.0]); want.append(hb + 1)     # h^2 + tiny^2 > h^2: the next fp16 value
+        cases.append([h, 0.0, 0.0]); want.append(hb)          # exactly h
+        cases.append([0.0, h, 0.0]); want.append(hb)
+    # 3-4-5: (3u)^2 + (4u)^2 = (5u)^2 exactly
+    u = 2.0 ** -12
+    cases.append([3 * u, 4 * u, 0.0]); want.append(int(np.float16(5 * u).view(np.uint16)))
+    cases.append([3 * u, 4 * u, u * 2.0 ** -40]); want.append(int(np.float16(5 * u).view(np.uint16)) + 1)
+    cases.append([0.0, 0.0, 0.0]); want.append(0)
+    cases.append([65504.0, 0.0, 0.0]); want.append(0x7BFF)
+    cases.append([65504.0, 1e-3, 0.0]); want.append(0x7C00)   # above the largest finite: +inf
+    cases.append([2.0 ** -149, 0.0, 0.0]); want.append(1)     # any positive norm below 2^-24 rounds up to it
+    xh = np.array(cases)
+    got = norm_fp16_ru_bits(xh, np.zeros_like(xh))
+    assert list(got) == want
+    assert np.array_equal(got, _brute_rows(xh, np.zeros_like(xh)))
+    # the same as residuals of nearby binary32 pairs (the difference itself carries the small term)
+    a = np.float64(np.float32(1.0 + 2.0 ** -20))
+    r = a - 1.0                       # 2^-20, an fp16 value
+    xh2 = np.array([[a, 1.0 + 2.0 ** -23, 2.0 ** -60]])
+    x2 = np.array([[1.0, 1.0, 0.0]])
+    assert np.array_equal(norm_fp16_ru_bits(xh2, x2), _brute_rows(xh2, x2))
+    assert norm_fp16_ru_bits(np.array([[a]]), np.array([[1.0]]))[0] == np.float16(r).view(np.uint16)
+
+
+def test_witness_and_value_witness_are_exact_norms():
+    from oracle.quant import value_witness_bits
+
+    k = _rows(40, 8)
+    xi = dither(5, 2, 1, np.arange(40)[:, None], np.arange(128)[None, :])
+    codes, sb, _ = quantize(k, "int8", xi)
+    kh = dequantize(codes, sb, "int8", xi)
+    w = witness_bits(kh, k)
+    bands = [[4 * b + i for i in range(4)] + [64 + 4 * b + i for i in range(4)] for b in range(16)]
+    for t in range(0, 40, 9):
+        assert [int(v) for v in w[t]] == [_fp16_ru_norm_brute(kh[t, idx], k[t, idx].astype(np.float64))
+                                          for idx in bands]
+    vw = value_witness_bits(kh, k)
+    for t in range(0, 40, 13):
+        assert int(vw[t, 0]) == _fp16_ru_norm_brute(kh[t], k[t].astype(np.float64))
+        assert int(vw[t, 1]) == _fp16_ru_norm_brute(k[t].astype(np.float64), np.zeros(128))
+    # a non-finite row gives the NaN pattern (the library flags such rows)
+    bad = k.copy()
+    bad[0, 5] = np.inf                     # channel 5 lies in band 1
+    wb = witness_bits(kh, bad)
+    assert wb[0, 1] == 0x7E00 and np.array_equal(np.delete(wb[0], 1), np.delete(w[0], 1))
