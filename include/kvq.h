@@ -41,6 +41,9 @@ extern "C" {
 #define KVQ_PAGE_SIZE 16
 #define KVQ_N_BANDS 16
 #define KVQ_MAX_GROUP 8
+/* Largest num_kv_heads and batch kvq_decode_attn accepts (larger values: KVQ_ERR_INVALID_ARG). */
+#define KVQ_MAX_KV_HEADS 128
+#define KVQ_MAX_BATCH 1024
 #define KVQ_VERSION 1
 
 /* A cudaStream_t, declared without the CUDA headers. */
@@ -111,6 +114,9 @@ typedef enum kvq_dtype { KVQ_DTYPE_F32 = 0, KVQ_DTYPE_BF16 = 1 } kvq_dtype;
  *     ([W] Sec. 6.2.5 fixed-channel outlier bypass: a fixed set of m RoPE pairs per
  *     (layer, kv head) is stored in fp16 (round to nearest even) and left out of the
  *     INT8 amax; the INT8 code of a bypassed channel is 0).  Head-major like the scales.
+ * INT8 codes (both INT8 formats) are stored offset binary: the byte is code + 128
+ * (code 0 is 0x80), so that the decode turns a byte into an fp16 operand with one
+ * byte permute.
  * Band b holds the RoPE frequency pairs 4b..4b+3 of the half-split pairing
  * (pair j = channels j and j+64), i.e. channels 4b..4b+3 and 64+4b..64+4b+3
  * ([W] Sec. 4.1, eq. (2)).

@@ -36,7 +36,7 @@ __device__ __forceinline__ void rope_rotate4(float k[4], const float* row, int l
 }
 
 template <int KF, int VF, bool ROPE = false>
-__global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __restrict__ kin,
+__global__ void __launch_bounds__(256, 1) append_kernel(kvq_cache c, const void* __restrict__ kin,
                                                      const void* __restrict__ vin, int in_bf16,
                                                      const int32_t* __restrict__ slots, int num_tokens,
                                                      int32_t* err, RopeArgs rope) {
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) append_kernel(kvq_cache c, const void* __
 // table), one warp per (sequence, kv head); launched ahead of a decode that waits for it only where
 // it reads those pages (programmatic dependent launch).
 template <int KF, int VF>
-__global__ void __launch_bounds__(256) append_newest_kernel(kvq_cache c, const void* __restrict__ kin,
+__global__ void __launch_bounds__(256, 1) append_newest_kernel(kvq_cache c, const void* __restrict__ kin,
                                                             const void* __restrict__ vin, int in_bf16,
                                                             const int32_t* __restrict__ block_table, int max_pages,
                                                             const int32_t* __restrict__ seq_lens, int batch,

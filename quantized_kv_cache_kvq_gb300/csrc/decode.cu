@@ -361,6 +361,7 @@ kvq_status decode_impl(const kvq_cache* cache, const void* k_new, const void* v_
   }
   if (prefix_len < 0 || (prefix_len > 0 && !prefix)) return KVQ_ERR_INVALID_ARG;
   const int hkv = cache->num_kv_heads;
+  if (hkv > KVQ_MAX_KV_HEADS) return KVQ_ERR_INVALID_ARG;
   if (batch < 0 || batch > kMaxBatch || num_q_heads <= 0 || num_q_heads % hkv) return KVQ_ERR_INVALID_ARG;
   const int G = num_q_heads / hkv;
   if (G > kMaxGroup) return KVQ_ERR_UNSUPPORTED_LAYOUT;

@@ -34,7 +34,9 @@ namespace dec {
 constexpr int kMaxWarps = 16;
 constexpr int kQloBytes = 8 * 2 * 32 * 4;  // per-warp low parts of an fp32 query (only when q is fp32)
 constexpr int kMaxStages = 16;
-constexpr int kMaxBatch = 1024;  // sequences per call (prefix sums live in shared memory)
+constexpr int kMaxBatch = KVQ_MAX_BATCH;  // sequences per call (prefix sums live in shared memory; 16 bits of a
+                                         // page descriptor)
+static_assert(KVQ_MAX_KV_HEADS <= 128 && KVQ_MAX_BATCH <= 65536, "page descriptor fields");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr int kNoPrefix = -1;
@@ -251,10 +253,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
   asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(w));
   return r;
 }
-// two int8 codes (bytes sel: 0 -> bytes 0,1; 1 -> bytes 2,3 of w) -> f16x2 (exact):
-// 0x6400 | (b ^ 0x80) is the fp16 value 1024 + b + 128.
-__device__ __forceinline__ uint32_t s8x2_to_f16x2(uint32_t w_xor80, int sel) {
-  const uint32_t h = __byte_perm(w_xor80, 0x64646464u, sel ? 0x4342 : 0x4140);
+// INT8 codes are stored offset binary (byte = code + 128).  Two of them (sel: 0 -> bytes 0,1; 1 -> bytes
+// 2,3 of w) -> f16x2 of code + 1152 (exact): 0x6400 | byte is the fp16 value 1024 + byte.  The products
+// that take these operands remove the 1152 offset in their accumulator (keys: its initial value; values:
+// one product with a constant operand).
+constexpr uint32_t kInt8BiasF16x2 = 0xE480E480u;  // fp16 pair (-1152, -1152)
+__device__ __forceinline__ uint32_t u8x2_to_f16x2_biased(uint32_t w, int sel) {
+  return __byte_perm(w, 0x64646464u, sel ? 0x4342 : 0x4140);
+}
+// the same without the offset: f16x2 of the two codes themselves (exact)
+__device__ __forceinline__ uint32_t u8x2_to_f16x2(uint32_t w, int sel) {
+  const uint32_t h = u8x2_to_f16x2_biased(w, sel);
   const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2(__half(1152.f), __half(1152.f)));
   return *reinterpret_cast<const uint32_t*>(&v);
 }
@@ -401,7 +410,8 @@ struct QFrag {
   bool has_lo;
   float cm_scale;    // c_t = cm_scale * (W . QN)  (natural units)
   float alpha_b[2];  // Tier B: u_t = alpha_b[h] * s_t for heads 2c, 2c+1 (natural units)
-  float s_init[2];   // INT8 keys: 3/2 sum_c q_c (fp16 query as the key products use it), heads 2c, 2c+1
+  float s_init[2];   // INT8 keys: 3/2 sum_c q_c - 1152 sum_c (q_c + lo_c) (fp16 query parts as the key products
+                     // use them: the dither operand's 3/2 and the code operand's 1152 offsets), heads 2c, 2c+1
   float* gq;         // group-scaled INT8 keys: the warp's per-group query table (kGqBytes)
   // fixed-channel outlier bypass: B fragment of the bypassed channels (head g; fp16 hi / lo), and the
   // Tier B terms of heads 2c, 2c+1: u_t += beta_o[h] ||k_hat_{t,O}|| + gamma_o[h]
@@ -414,6 +424,7 @@ struct SoftState {
   float mc[2], sc[2];  // Tier A accumulator: reference max (log2 units) and scaled sum
   float mu[2], su[2];  // Tier B accumulator
   float o[8][4];       // O^T fragments of the 8 channel blocks
+  float pv[2];         // INT8 values: lane-partial sum of the fp16 P' weights per head (for the 3/2 correction)
   // While every radius seen in the unit is <= kFastRadius the meter sums share the softmax's
   // reference max (mc == m): sum p_t (e^{c_t} - 1).  The first larger radius switches the unit to
   // the general form with its own running max (warp-uniform, sticky until the unit ends).
@@ -424,6 +435,7 @@ __device__ __forceinline__ void reset_state(SoftState& s) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     s.m[h] = -INFINITY; s.l[h] = 0.f; s.mc[h] = -INFINITY; s.sc[h] = 0.f; s.mu[h] = -INFINITY; s.su[h] = 0.f;
+    s.pv[h] = 0.f;
   }
   s.slow_a = false;
   s.slow_b = false;
@@ -485,6 +497,7 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
   const bool fp32q = !a.q_bf16;
   bool any_lo = false;
   float qsum = 0.f;  // sum of this lane's fp16 query channels (K8 family)
+  float lsum = 0.f;  // sum of their fp16 low parts (fp32 queries)
   auto put = [&](int kb, const float* x) {  // channels x[0..3] of k-step kb: b0 <- x0, x1; b1 <- x2, x3
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -500,6 +513,10 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
         const float2 r = unpack_f16(f.hi[kb][h]);
         lo = pack_f16(x0 - r.x, x1 - r.y);
         qsum += r.x + r.y;
+        if (fp32q) {
+          const float2 rl = unpack_f16(lo);
+          lsum += rl.x + rl.y;
+        }
       }
       if (fp32q) {
         f.lo[(kb * 2 + h) * 32 + lane] = lo;
@@ -514,11 +531,11 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     for (int j = 0; j < 4; ++j) {
       float v[8];
       load8(32 * j + 8 * c, v);
-      if (GS) qsum = 0.f;
+      if (GS) qsum = lsum = 0.f;
       put(2 * j, v);
       put(2 * j + 1, v + 4);
       if (GS) {
-        gsum[j] = qsum;
+        gsum[j] = 1.5f * qsum - 1152.f * (qsum + lsum);
         float sq = 0.f, l1 = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) { sq = __fmaf_rn(v[e], v[e], sq); l1 += fabsf(v[e]); }
@@ -548,11 +565,12 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
   }
   f.has_lo = __any_sync(kFull, any_lo);
   {
-    // the key products of dithered INT8 pages multiply -(xi + 3/2) by the fp16 query, so their
-    // accumulator starts at 3/2 sum_c q_c (heads 2c and 2c + 1; the sum lives on the lanes of row g)
-    const float qs_g = row_sum4(qsum);
-    f.s_init[0] = 1.5f * __shfl_sync(kFull, qs_g, 8 * c);
-    f.s_init[1] = 1.5f * __shfl_sync(kFull, qs_g, 8 * c + 4);
+    // the key products of dithered INT8 pages multiply -(xi + 3/2) by the fp16 query and the codes, as
+    // code + 1152, by its fp16 high and low parts, so their accumulator starts at 3/2 sum_c q_c -
+    // 1152 sum_c (q_c + lo_c) (heads 2c and 2c + 1; the sums live on the lanes of row g)
+    const float qs_g = row_sum4(1.5f * qsum - 1152.f * (qsum + lsum));
+    f.s_init[0] = __shfl_sync(kFull, qs_g, 8 * c);
+    f.s_init[1] = __shfl_sync(kFull, qs_g, 8 * c + 4);
   }
   __syncwarp();
   if (METER) {
@@ -655,7 +673,7 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     for (int j = 0; j < 4; ++j) {
       const float s1 = row_sum4(gsum[j]), s2 = row_sum4(gsq[j]), s3 = row_sum4(gl1[j]);
       if (c == 0) {
-        f.gq[(0 * 4 + j) * 8 + g] = 1.5f * s1;
+        f.gq[(0 * 4 + j) * 8 + g] = s1;  // 3/2 sum q - 1152 sum (q + lo) of the group (see gsum)
         f.gq[(1 * 4 + j) * 8 + g] = ka * ka * s2;
         f.gq[(2 * 4 + j) * 8 + g] = a.sm_scale * 0x1p-11f * s3;
       }
@@ -754,7 +772,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int gr = 2 * jj + half;
-        const float2 ti = *reinterpret_cast<const float2*>(f.gq + gr * 8 + 2 * c);
+        const float2 ti = *reinterpret_cast<const float2*>(f.gq + gr * 8 + 2 * c);  // undoes the 3/2, 1152 offsets
         float T[4] = {ti.x, ti.y, ti.x, ti.y};
         // one Philox call per token: the dither of this lane's 8 channels 32gr + 8c + {0..7} of the group
         const uint32_t grp = 8 * jj + 4 * half + c;
@@ -770,9 +788,8 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
           const int sidx = 2 * half + s2, kb = 4 * jj + sidx;
-          const uint32_t x0 = w0[sidx] ^ 0x80808080u, x1 = w1[sidx] ^ 0x80808080u;
-          const uint32_t a0 = s8x2_to_f16x2(x0, 0), a2 = s8x2_to_f16x2(x0, 1);
-          const uint32_t a1 = s8x2_to_f16x2(x1, 0), a3 = s8x2_to_f16x2(x1, 1);
+          const uint32_t a0 = u8x2_to_f16x2_biased(w0[sidx], 0), a2 = u8x2_to_f16x2_biased(w0[sidx], 1);
+          const uint32_t a1 = u8x2_to_f16x2_biased(w1[sidx], 0), a3 = u8x2_to_f16x2_biased(w1[sidx], 1);
           mma_f16_4(T, a0, a1, a2, a3, f.hi[kb][0], f.hi[kb][1]);
           if (LO && f.has_lo) mma_f16_4(T, a0, a1, a2, a3, f.lo[(2 * kb) * 32 + lane], f.lo[(2 * kb + 1) * 32 + lane]);
           const uint32_t e0 = s2 ? d0.z : d0.x, e2 = s2 ? d0.w : d0.y;
@@ -793,7 +810,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       ph = philox_head(pl.layer, static_cast<uint32_t>(kvh), pl.rk0, pl.rk1);
       pt0 = philox_slot(phys * kPage + g, ph, pl.rk0, pl.rk1);
       pt1 = philox_slot(phys * kPage + g + 8, ph, pl.rk0, pl.rk1);
-      // the dither products below use -(xi + 3/2); the accumulator starts at 3/2 sum_c q_c to undo it
+      // the products below use code + 1152 and -(xi + 3/2); the accumulator's initial value undoes both offsets
       S[0] = S[2] = f.s_init[0];
       S[1] = S[3] = f.s_init[1];
     }
@@ -803,14 +820,15 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       const uint4 k1 = lds128(st + L::kOff + ((2 + jj) * 32 + lane) * 16);
       const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
       const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
-      uint4 d0{}, d1{};  // Philox words of tokens g and g + 8, channels 64jj + 16c + 8(sidx >> 1) + {0..7}
+      // key operand words -(xi + 3/2) of tokens g and g + 8 (channel pairs of channels 64jj + 16c + 8(sidx >> 1)
+      // + {0..7}), made from the Philox words; the value side reads the same words from the dither tile
+      uint4 n0{}, n1{};
 #pragma unroll
       for (int sidx = 0; sidx < 4; ++sidx) {
         uint32_t a0, a1, a2, a3;
         if (KDITHER) {
-          const uint32_t x0 = w0[sidx] ^ 0x80808080u, x1 = w1[sidx] ^ 0x80808080u;
-          a0 = s8x2_to_f16x2(x0, 0); a2 = s8x2_to_f16x2(x0, 1);
-          a1 = s8x2_to_f16x2(x1, 0); a3 = s8x2_to_f16x2(x1, 1);
+          a0 = u8x2_to_f16x2_biased(w0[sidx], 0); a2 = u8x2_to_f16x2_biased(w0[sidx], 1);
+          a1 = u8x2_to_f16x2_biased(w1[sidx], 0); a3 = u8x2_to_f16x2_biased(w1[sidx], 1);
         } else {
           a0 = e4m3x2_to_f16x2(w0[sidx] & 0xFFFFu); a2 = e4m3x2_to_f16x2(w0[sidx] >> 16);
           a1 = e4m3x2_to_f16x2(w1[sidx] & 0xFFFFu); a3 = e4m3x2_to_f16x2(w1[sidx] >> 16);
@@ -823,23 +841,22 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
           // z, w (+4..7) for odd sidx; each word holds the dither of two channels (a0 / a2 pairs)
           if ((sidx & 1) == 0) {
             const uint32_t grp = 8 * jj + 2 * c + (sidx >> 1);
-            d0 = philox_finish(grp, pt0, ph, pl.rk0, pl.rk1);
-            d1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
+            const uint4 d0 = philox_finish(grp, pt0, ph, pl.rk0, pl.rk1);
+            const uint4 d1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
+            n0 = make_uint4(neg_shifted_dither_f16x2(d0.x), neg_shifted_dither_f16x2(d0.y),
+                            neg_shifted_dither_f16x2(d0.z), neg_shifted_dither_f16x2(d0.w));
+            n1 = make_uint4(neg_shifted_dither_f16x2(d1.x), neg_shifted_dither_f16x2(d1.y),
+                            neg_shifted_dither_f16x2(d1.z), neg_shifted_dither_f16x2(d1.w));
             if (VDITHER) {
-              // minus the dither for the value side: token-major fp16 tile, 16-byte chunks xor-swizzled by row
+              // the value side's dither operand -(xi + 3/2): token-major fp16 tile, 16-byte chunks xor-swizzled by row
               const int off = ((8 * jj + 2 * c + (sidx >> 1)) ^ g) << 4;
-              *reinterpret_cast<uint4*>(xi_tile + g * 256 + off) =
-                  make_uint4(neg_dither_f16x2(d0.x), neg_dither_f16x2(d0.y), neg_dither_f16x2(d0.z),
-                             neg_dither_f16x2(d0.w));
-              *reinterpret_cast<uint4*>(xi_tile + (g + 8) * 256 + off) =
-                  make_uint4(neg_dither_f16x2(d1.x), neg_dither_f16x2(d1.y), neg_dither_f16x2(d1.z),
-                             neg_dither_f16x2(d1.w));
+              *reinterpret_cast<uint4*>(xi_tile + g * 256 + off) = n0;
+              *reinterpret_cast<uint4*>(xi_tile + (g + 8) * 256 + off) = n1;
             }
           }
-          const uint32_t e0 = (sidx & 1) ? d0.z : d0.x, e2 = (sidx & 1) ? d0.w : d0.y;
-          const uint32_t e1 = (sidx & 1) ? d1.z : d1.x, e3 = (sidx & 1) ? d1.w : d1.y;
-          mma_f16_4(S, neg_shifted_dither_f16x2(e0), neg_shifted_dither_f16x2(e1), neg_shifted_dither_f16x2(e2),
-                    neg_shifted_dither_f16x2(e3), f.hi[kb][0], f.hi[kb][1]);
+          const uint32_t e0 = (sidx & 1) ? n0.z : n0.x, e2 = (sidx & 1) ? n0.w : n0.y;
+          const uint32_t e1 = (sidx & 1) ? n1.z : n1.x, e3 = (sidx & 1) ? n1.w : n1.y;
+          mma_f16_4(S, e0, e1, e2, e3, f.hi[kb][0], f.hi[kb][1]);
         }
       }
     }
@@ -1036,9 +1053,9 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       const uint32_t words[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const uint32_t x0 = words[2 * half] ^ 0x80808080u, x1 = words[2 * half + 1] ^ 0x80808080u;
-        mma_f16_4(s.o[2 * mm + half], s8x2_to_f16x2(x0, 0), s8x2_to_f16x2(x0, 1), s8x2_to_f16x2(x1, 0),
-                  s8x2_to_f16x2(x1, 1), b0, b1);
+        const uint32_t x0 = words[2 * half], x1 = words[2 * half + 1];
+        mma_f16_4(s.o[2 * mm + half], u8x2_to_f16x2(x0, 0), u8x2_to_f16x2(x0, 1), u8x2_to_f16x2(x1, 0),
+                  u8x2_to_f16x2(x1, 1), b0, b1);
         const int mt = 2 * mm + half;
         const int mat = lane >> 3, r8 = lane & 7;
         const int row = ((mat >> 1) << 3) + r8;
@@ -1049,8 +1066,17 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       }
     }
   } else if (!fmt_is_16bit(VF)) {
-    const uint32_t b0 = movmatrix_trans(pack_f16(pw[0], pw[1]));
-    const uint32_t b1 = movmatrix_trans(pack_f16(pw[2], pw[3]));
+    const uint32_t h01 = pack_f16(pw[0], pw[1]), h23 = pack_f16(pw[2], pw[3]);
+    const uint32_t b0 = movmatrix_trans(h01);
+    const uint32_t b1 = movmatrix_trans(h23);
+    if (VDITHER) {
+      // the operands below are code + 1152 (removed per page by a product with the constant -1152) and
+      // -(xi + 3/2), whose 3/2 comes back as 3/2 sum_t P'_t per head when the piece is written: the lane's
+      // part of that sum (tokens g, g + 8), rescaled like the accumulators
+      const float2 q01 = unpack_f16(h01), q23 = unpack_f16(h23);
+      f2_unpack(f2_fma(f2_pack(s.pv[0], s.pv[1]), f2_pack(alpha[0], alpha[1]), f2_pack(q01.x + q23.x, q01.y + q23.y)),
+                s.pv[0], s.pv[1]);
+    }
 #pragma unroll
     for (int mm = 0; mm < 4; ++mm) {
       const uint4 vb = lds128(st + L::vOff + (mm * 32 + lane) * 16);
@@ -1060,18 +1086,18 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         const uint32_t u0 = words[2 * half], u1 = words[2 * half + 1];
         uint32_t a0, a1, a2, a3;
         if (VDITHER) {
-          const uint32_t x0 = u0 ^ 0x80808080u, x1 = u1 ^ 0x80808080u;
-          a0 = s8x2_to_f16x2(x0, 0); a1 = s8x2_to_f16x2(x0, 1);
-          a2 = s8x2_to_f16x2(x1, 0); a3 = s8x2_to_f16x2(x1, 1);
+          a0 = u8x2_to_f16x2_biased(u0, 0); a1 = u8x2_to_f16x2_biased(u0, 1);
+          a2 = u8x2_to_f16x2_biased(u1, 0); a3 = u8x2_to_f16x2_biased(u1, 1);
         } else {
           a0 = e4m3x2_to_f16x2(u0 & 0xFFFFu); a1 = e4m3x2_to_f16x2(u0 >> 16);
           a2 = e4m3x2_to_f16x2(u1 & 0xFFFFu); a3 = e4m3x2_to_f16x2(u1 >> 16);
         }
         mma_f16_4(s.o[2 * mm + half], a0, a1, a2, a3, b0, b1);
+        if (VDITHER) mma_f16_4(s.o[2 * mm + half], kInt8BiasF16x2, kInt8BiasF16x2, kInt8BiasF16x2, kInt8BiasF16x2, b0, b1);
       }
     }
     if (VDITHER) {
-      // add (-xi)^T . P'^T: A fragments of the (negated) dither tile by transposed 8x8 loads
+      // add (-(xi + 3/2))^T . P'^T: A fragments of the dither tile by transposed 8x8 loads
       __syncwarp();
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
@@ -1103,10 +1129,13 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
 // Page descriptors: lane l of a chunk describes page x0 + l of the warp's range.
 struct Desc {
   int32_t phys;   // physical page in its cache (-1: out of range, skipped)
-  uint32_t info;  // unit (bits 0..22) | nvalid (bits 23..27) | prefix segment (bit 28) | present (bit 29)
-                  // | last live page of the unit (bit 30)
+  uint32_t info;  // kv head (bits 0..6) | sequence (bits 7..22) | nvalid (bits 23..27) | prefix segment (bit 28)
+                  // | present (bit 29) | last live page of the unit (bit 30)
 };
-__device__ __forceinline__ int d_unit(uint32_t i) { return static_cast<int>(i & 0x7FFFFFu); }
+// the unit's (sequence, kv head) pair as one key, and its parts
+__device__ __forceinline__ uint32_t d_ukey(uint32_t i) { return i & 0x7FFFFFu; }
+__device__ __forceinline__ int d_kvh(uint32_t i) { return static_cast<int>(i & 0x7Fu); }
+__device__ __forceinline__ int d_seq(uint32_t i) { return static_cast<int>((i >> 7) & 0xFFFFu); }
 __device__ __forceinline__ int d_nvalid(uint32_t i) { return static_cast<int>((i >> 23) & 31u); }
 __device__ __forceinline__ bool d_prefix(uint32_t i) { return (i >> 28) & 1u; }
 __device__ __forceinline__ bool d_present(uint32_t i) { return (i >> 29) & 1u; }
@@ -1126,7 +1155,6 @@ __device__ __forceinline__ Desc make_desc(const Args& a, const int32_t* cum, lon
   const int P = cum[s + 1] - cum[s];
   const int kvh = static_cast<int>(r / P);
   const int p = static_cast<int>(r - static_cast<long long>(kvh) * P);
-  const int unit = s * a.Hkv + kvh;
   int nvalid, phys;
   uint32_t pre = 0;
   if (p < a.prefix_pages) {
@@ -1145,7 +1173,8 @@ __device__ __forceinline__ Desc make_desc(const Args& a, const int32_t* cum, lon
   }
   const uint32_t last = (!pre && p == P - 1) ? 1u : 0u;
   d.phys = phys;
-  d.info = static_cast<uint32_t>(unit) | (static_cast<uint32_t>(nvalid) << 23) | (pre << 28) | (1u << 29) | (last << 30);
+  d.info = static_cast<uint32_t>(kvh) | (static_cast<uint32_t>(s) << 7) | (static_cast<uint32_t>(nvalid) << 23) |
+           (pre << 28) | (1u << 29) | (last << 30);
   return d;
 }
 
@@ -1156,7 +1185,7 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
     mbar_arrive(bar);
     return;
   }
-  const int kvh = d_unit(d.info) % a.Hkv;
+  const int kvh = d_kvh(d.info);
   const bool pre = d_prefix(d.info);
   if (PKF != kNoPrefix && pre) {
     using L = Layout<(PKF < 0 ? 0 : PKF), (PVF < 0 ? 0 : PVF), METER>;
@@ -1195,14 +1224,17 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
 }
 
 // Partial of one (warp, unit) piece: per real head, (m, l, mc, sc, mu, su) and the 128 O^T values.
+// PV: the value products used the dither operand -(xi + 3/2); 3/2 sum_t P'_t of each head is added back here.
+template <bool PV>
 __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftState& s, float* vstate) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  float l[2], sc[2], su[2], vr[2] = {0.f, 0.f};
+  float l[2], sc[2], su[2], vr[2] = {0.f, 0.f}, corr[2] = {0.f, 0.f};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     l[h] = col_sum8(s.l[h]);
     sc[h] = col_sum8(s.sc[h]);
     su[h] = col_sum8(s.su[h]);
+    if (PV) corr[h] = 1.5f * col_sum8(s.pv[h]);
   }
   float vmax = 0.f, cmax[2] = {0.f, 0.f}, om[2] = {0.f, 0.f};
   if (vstate) {
@@ -1228,8 +1260,8 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
       float* acc = a.ws_acc + (slot * a.G + head) * kHeadDim;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        acc[16 * mt + g] = s.o[mt][h];
-        acc[16 * mt + g + 8] = s.o[mt][2 + h];
+        acc[16 * mt + g] = PV ? s.o[mt][h] + corr[h] : s.o[mt][h];
+        acc[16 * mt + g + 8] = PV ? s.o[mt][2 + h] + corr[h] : s.o[mt][2 + h];
       }
       if (g == 0) {
         float* st = a.ws_stats + (slot * a.G + head) * kStatsFloats;
@@ -1253,10 +1285,11 @@ __device__ void zero_tail(uint8_t* st, int nvalid, bool vw_on, bool ko_wide = fa
   const int n = (kPage - nvalid) * kHeadDim;
   for (int e = lane; e < n; e += 32) {
     const int t = nvalid + e / kHeadDim, c = e % kHeadDim;
+    // INT8 codes are offset binary: 0x80 is code 0
     if (fmt_is_16bit(KF)) *reinterpret_cast<uint16_t*>(st + L::kOff + k16_offset(t, c)) = 0;
-    else st[L::kOff + (fmt_group_scales(KF) ? k8g_offset(t, c) : k8_offset(t, c))] = 0;
+    else st[L::kOff + (fmt_group_scales(KF) ? k8g_offset(t, c) : k8_offset(t, c))] = fmt_is_int8(KF) ? 0x80 : 0;
     if (fmt_is_16bit(VF)) *reinterpret_cast<uint16_t*>(st + L::vOff + v16_offset(t, c)) = 0;
-    else st[L::vOff + v8_offset(t, c)] = 0;
+    else st[L::vOff + v8_offset(t, c)] = fmt_is_int8(VF) ? 0x80 : 0;
   }
   for (int e = lane; e < (kPage - nvalid) * kBands; e += 32) {
     const int t = nvalid + e / kBands, b = e % kBands;
@@ -1296,6 +1329,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   constexpr bool K16 = fmt_is_16bit(KF);
   constexpr bool XI = fmt_is_int8(KF) && fmt_is_int8(VF);
   constexpr bool GS = fmt_group_scales(KF);
+  constexpr bool PV = XI && !GS;  // value products with the -(xi + 3/2) dither operand
   int32_t* cum = reinterpret_cast<int32_t*>(smem);
   const int cum_bytes = ((a.B + 1) * 4 + 127) & ~127;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1387,7 +1421,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   f.gq = gq;
   SoftState s;
   reset_state(s);
-  int unit = -1;
+  int unit = -1;               // the current unit's index (sequence * Hkv + kv head)
+  uint32_t ukey = 0xFFFFFFFFu;  // and its descriptor key
   long long unit_x0 = 0;   // gate support: global index of the current unit's first page
   float* crow = nullptr;   // gate support: the current unit's contribution row
   const float qk_scale = a.sm_scale * kLog2e;
@@ -1404,11 +1439,11 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
     }
     const int32_t phys = __shfl_sync(kFull, cur.phys, j & 31);
     const uint32_t info = __shfl_sync(kFull, cur.info, j & 31);
-    const int u = d_unit(info);
-    if (u != unit) {
-      if (unit >= 0) { write_piece(a, static_cast<size_t>(wid) + unit, s, vstate); reset_state(s); }
-      unit = u;
-      const int seq = u / a.Hkv, kvh = u % a.Hkv;
+    if (d_ukey(info) != ukey) {
+      if (unit >= 0) { write_piece<PV>(a, static_cast<size_t>(wid) + unit, s, vstate); reset_state(s); }
+      ukey = d_ukey(info);
+      const int seq = d_seq(info), kvh = d_kvh(info);
+      unit = seq * a.Hkv + kvh;
       const int total = a.prefix_len + min(max(a.seq_lens[seq], 0), a.max_pages * kPage);
       load_q<K16, METER, OUTL, GS>(a, seq, kvh, total, f);
       if (VALUE && a.page_contrib) {
@@ -1421,7 +1456,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
     if (!__all_sync(kFull, mbar_wait(&bars[stage], parity))) { ok = false; timeout_at = j; break; }
     uint8_t* st = wbase + stage * a.stage_bytes;
     if (phys >= 0) {
-      const int kvh = u % a.Hkv;
+      const int kvh = d_kvh(info);
       const int nvalid = d_nvalid(info);
       const float xb0 = g8 < nvalid ? 0.f : -INFINITY, xb1 = g8 + 8 < nvalid ? 0.f : -INFINITY;
       if (PKF != kNoPrefix && d_prefix(info)) {
@@ -1475,7 +1510,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
       (void)mbar_wait(&bars[k % a.stages], static_cast<uint32_t>((k / a.stages) & 1));
     return;
   }
-  if (unit >= 0) write_piece(a, static_cast<size_t>(wid) + unit, s, vstate);
+  if (unit >= 0) write_piece<PV>(a, static_cast<size_t>(wid) + unit, s, vstate);
 }
 
 }  // namespace dec

@@ -7,7 +7,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["k_offsets", "v_offsets", "w_offsets", "s_offsets", "gs_offsets", "vw_offsets", "ko_offsets", "unpack_k",
+__all__ = ["int8_codes", "k_offsets", "v_offsets", "w_offsets", "s_offsets", "gs_offsets", "vw_offsets", "ko_offsets", "unpack_k",
            "unpack_v", "unpack_w", "unpack_s", "unpack_gs", "unpack_vw", "unpack_ko"]
 
 
@@ -71,17 +71,27 @@ def _gather16(tiles: np.ndarray, offs: np.ndarray) -> np.ndarray:
     return u16[..., offs // 2]
 
 
+def int8_codes(stored: np.ndarray) -> np.ndarray:
+    """INT8 codes of offset-binary stored bytes (byte = code + 128)."""
+    return (np.asarray(stored, dtype=np.uint8) ^ np.uint8(0x80)).view(np.int8)
+
+
 def unpack_k(tiles: np.ndarray, fmt: str, num_kv_heads: int) -> np.ndarray:
-    """K plane bytes [pages*heads, tile] -> codes [pages, heads, 16, 128] (uint16 bf16 bits / uint8)."""
+    """K plane bytes [pages*heads, tile] -> codes [pages, heads, 16, 128] (uint16 bf16 bits / uint8 e4m3 bits /
+    int8 codes)."""
     tiles = tiles.reshape(-1, num_kv_heads, tiles.shape[-1])
     offs = k_offsets(fmt)
-    return _gather16(tiles, offs) if fmt == "bf16" else tiles[..., offs]
+    if fmt == "bf16":
+        return _gather16(tiles, offs)
+    return int8_codes(tiles[..., offs]) if fmt.startswith("int8") else tiles[..., offs]
 
 
 def unpack_v(tiles: np.ndarray, fmt: str, num_kv_heads: int) -> np.ndarray:
     tiles = tiles.reshape(-1, num_kv_heads, tiles.shape[-1])
     offs = v_offsets(fmt)
-    return _gather16(tiles, offs) if fmt == "bf16" else tiles[..., offs]
+    if fmt == "bf16":
+        return _gather16(tiles, offs)
+    return int8_codes(tiles[..., offs]) if fmt.startswith("int8") else tiles[..., offs]
 
 
 def unpack_w(tiles: np.ndarray, num_kv_heads: int) -> np.ndarray:

@@ -2,7 +2,7 @@
 
 INT8-dithered keys with m RoPE pairs per (layer, kv head) stored in fp16 and left out of the INT8
 amax.  Bars: codes, scales and the fp16 outlier values bit-exact with the oracle (bypassed codes 0);
-witness sound and at most one fp16 step above the oracle's; decode output within 2e-3 and both
+witness bit-exact (the exact band norm rounded up to fp16); decode output within 2e-3 and both
 meters' ln(A - 1) within 1e-4 of the oracle (Tier B with the deterministic fp16 term of the bypassed
 channels), meter >= exact TV; and the page's Table 5 effect on the GPU: the same massive-pair
 workload meters far lower with the bypass than without.
@@ -64,8 +64,7 @@ def test_append_bypass_bit_exact(kvq, m):
     w = L.unpack_w(cache.witness.cpu().numpy(), hkv)[pg, :, t]
     exact = band_norms(ref["kh"] - k.astype(np.float64))
     assert np.all(fp16_value(w) >= exact)
-    d = w.astype(np.int64) - ref["w16"].astype(np.int64)
-    assert np.all((d == 0) | (d == 1))
+    assert np.array_equal(w, ref["w16"])
 
 
 @pytest.mark.parametrize("m,q_dtype", [(4, "bf16"), (8, "bf16"), (4, "f32")])

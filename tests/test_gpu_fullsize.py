@@ -4,8 +4,9 @@ benchmark times (same grid, same persistent split plan, same workspace), checked
 
 Sampled units include the first and last sequence, the longest and the shortest (ragged), so the
 prefix/suffix boundary, partial last pages and random page permutations are all exercised.  Bar: the
-append codes and scales of the sampled units are bit-exact; outputs within 2e-3 relative; ln(A - 1)
-(Tier A, and Tier B where enabled) within 1e-4; meter never below the exact TV.
+append's K and V codes, K and V scales and witness of the sampled units are bit-exact (the shared
+prefix's too); outputs within 2e-3 relative; ln(A - 1) (Tier A, and Tier B where enabled) within 1e-4;
+meter never below the exact TV.
 """
 import math
 
@@ -20,6 +21,36 @@ import workloads as W  # noqa: E402
 from oracle import attention as OA  # noqa: E402
 from oracle.encoders import fp16_value  # noqa: E402
 from tests.parity import SM_SCALE, oracle_cache_rows  # noqa: E402
+
+
+def _host_planes(cache):
+    return {n: (getattr(cache, n).cpu().numpy() if getattr(cache, n) is not None else None)
+            for n in ("k", "v", "k_scale", "v_scale", "witness")}
+
+
+def _check_stored(planes, num_pages, hkv, h, slots, k_fmt, v_fmt, rows):
+    """Codes, scales and witness the GPU stored for kv head h at ``slots`` equal the oracle's ``rows``."""
+    from quantized_kv_cache_kvq_gb300 import layout as L
+
+    pg, t = slots // 16, slots % 16
+
+    def head_tiles(plane, head_major):
+        tiles = plane.reshape(hkv, num_pages, -1)[h] if head_major else plane.reshape(num_pages, hkv, -1)[:, h]
+        return tiles.reshape(num_pages, -1)
+
+    kc = L.unpack_k(head_tiles(planes["k"], False), k_fmt, 1)[pg, 0, t]
+    vc = L.unpack_v(head_tiles(planes["v"], False), v_fmt, 1)[pg, 0, t]
+    for got, ref in ((kc, rows["kc"][:, 0]), (vc, rows["vc"][:, 0])):
+        assert np.array_equal(got, ref.view(got.dtype) if ref.dtype != got.dtype else ref)
+    w16 = L.unpack_w(head_tiles(planes["witness"], False), 1)[pg, 0, t]
+    assert np.array_equal(w16, rows["w16"][:, 0])
+    for side, fmt in (("k", k_fmt), ("v", v_fmt)):
+        ref = rows[f"{side}sb"]
+        if ref is None:
+            continue
+        tiles = head_tiles(planes[f"{side}_scale"], True)
+        got = (L.unpack_gs if fmt == "int8g32" else L.unpack_s)(tiles, 1)[pg, 0, t]
+        assert np.array_equal(got, ref[:, 0])
 
 
 def _sample_units(w, lens):
@@ -80,16 +111,21 @@ def test_fullsize_sampled_parity(name):
     assert err.item() == 0
     out_h, ms_h = out.cpu().numpy().astype(np.float64), ms.cpu().numpy().astype(np.float64)
     q_h = q.float().cpu().numpy().astype(np.float64)
-    kplane = cache.k.cpu().numpy()
+    planes = _host_planes(cache)
+    if prefix is not None:   # the shared prefix's stored rows, every kv head
+        pplanes = _host_planes(prefix)
+        npp = (w.prefix_len + 15) // 16
+        pslots = np.arange(w.prefix_len)
+        for h in range(Hkv):
+            prow = oracle_cache_rows(pre[0][:, h:h + 1], pre[1][:, h:h + 1], pslots, w.prefix_k_fmt, w.prefix_v_fmt,
+                                     pre[2], layer, heads=[h])
+            _check_stored(pplanes, npp, Hkv, h, pslots, w.prefix_k_fmt, w.prefix_v_fmt, prow)
     for s, h in units:
         k32, v32, slots = keep[s]
         k1, v1 = k32[:, h:h + 1], v32[:, h:h + 1]
         rows = oracle_cache_rows(k1, v1, slots, w.k_fmt, w.v_fmt, seed, layer, heads=[h])
-        # append bit-exactness on the sampled unit
-        tiles = kplane.reshape(num_pages, Hkv, -1)[:, h:h + 1]
-        kc = L.unpack_k(tiles.reshape(num_pages, -1), w.k_fmt, 1)[slots // 16, 0, slots % 16]
-        ref_kc = rows["kc"][:, 0]
-        assert np.array_equal(kc, ref_kc.view(kc.dtype) if ref_kc.dtype != kc.dtype else ref_kc)
+        # append bit-exactness on the sampled unit: codes, scales, witness
+        _check_stored(planes, num_pages, Hkv, h, slots, w.k_fmt, w.v_fmt, rows)
         kk, kh, vh, ww = k1[:, 0], rows["kh"][:, 0], rows["vh"][:, 0], fp16_value(rows["w16"][:, 0])
         sk = fp16_value(rows["ksb"][:, 0]) if rows["ksb"] is not None else None
         if pre is not None:
