@@ -15,11 +15,11 @@ Everything is float64 and follows WitCert (arXiv 2607.28699):
   varsigma_t^2 = (1/d) sum_c q_c^2 s_{c,t}^2 / 12, delta_loc = delta_req/(L*H*T);
   with one scale per (token, kv head) this is
   u_t = sm_scale * ||q|| * s_t * sqrt(2 ln(2S/delta_loc) / 12) (§6.2.2 hoists the sqrt).
-  This library's dither lies on a 1024-point grid (oracle.philox), so the rounding
-  error of each element has a mean of at most 2^-11 LSB; the radius adds that
-  deterministic part, sm_scale * s_t * ||q||_1 * 2^-11.  With one scale per group of
+  This library's dither lies on a 256-point grid (oracle.philox), so the rounding
+  error of each element has a mean of at most 2^-9 LSB; the radius adds that
+  deterministic part, sm_scale * s_t * ||q||_1 * 2^-9.  With one scale per group of
   G_c channels (§6.2.3), varsigma_t keeps the per-channel sum:
-  u_t = sm_scale (kappa sqrt(sum_g ||q_g||^2 s_{g,t}^2) + 2^-11 sum_g ||q_g||_1 s_{g,t}).
+  u_t = sm_scale (kappa sqrt(sum_g ||q_g||^2 s_{g,t}^2) + 2^-9 sum_g ||q_g||_1 s_{g,t}).
 * §4.3: meter = min(1, 1/2 (A^2 - 1)); the raw value (kept as a log score
   ln(1/2 (A^2 - 1))) is a risk score with no guarantee above 1.
 * "Compress the shared cartridge", "One kernel spans cartridge and live KV":
@@ -125,10 +125,10 @@ def tier_b_radius(q: np.ndarray, s_k: np.ndarray, sm_scale: float, seq_len: int,
                   delta_req: float, n_layers: int, n_q_heads: int, n_steps: int) -> np.ndarray:
     """Tier B radius of every token (WitCert §4.2), delta_loc = delta_req/(L H T):
 
-        u_t = sm_scale s_t (||q|| sqrt(2 ln(2S/delta_loc)/12) + ||q||_1 beta),  beta = 2^-11.
+        u_t = sm_scale s_t (||q|| sqrt(2 ln(2S/delta_loc)/12) + ||q||_1 beta),  beta = 2^-9.
 
     The first term is the page's sub-Gaussian radius (the hoisted square root of §6.2.2).  The
-    second covers the dither grid: with xi uniform on 1024 points instead of the continuum, each
+    second covers the dither grid: with xi uniform on 256 points instead of the continuum, each
     element's rounding error has a mean of at most beta in LSB units (its centred part keeps the
     variance proxy 1/12), so the error's mean contributes at most s_t ||q||_1 beta to eps_t.
     """
@@ -145,7 +145,7 @@ def tier_b_radius_groups(q: np.ndarray, s_kg: np.ndarray, sm_scale: float, seq_l
     """Tier B radius with one key scale per token per channel group (WitCert §4.2 with the per-channel
     scales of §6.2.3): s_kg [S, n_groups], group g = channels [g G_c, (g + 1) G_c), G_c = 128 / n_groups.
 
-        u_t = sm_scale (kappa sqrt(sum_c q_c^2 s_{g(c),t}^2) + 2^-11 sum_c |q_c| s_{g(c),t}),
+        u_t = sm_scale (kappa sqrt(sum_c q_c^2 s_{g(c),t}^2) + 2^-9 sum_c |q_c| s_{g(c),t}),
         kappa = sqrt(2 ln(2S/delta_loc) / 12),
 
     the sub-Gaussian radius of sum_c q_c s_{g(c),t} (code_c - xi_c - x_c / s_{g(c),t}) (independent

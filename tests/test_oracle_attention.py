@@ -117,8 +117,8 @@ def _mp_decode(q, k, kh, vh, w16, sm, s_k=None, tb=None):
             dl = mp.mpf(tb["delta_req"]) / (tb["n_layers"] * tb["n_q_heads"] * tb["n_steps"])
             kappa = mp.sqrt(2 * mp.log(2 * S / dl) / 12)
             qn = mp.sqrt(mp.fsum(v * v for v in qq))
-            q1 = mp.fsum(abs(mp.mpf(float(x))) for x in q[h])   # the dither grid's bias term, 2^-11 ||q||_1
-            u = [mp.mpf(sm) * (qn * kappa + q1 * mp.mpf(2) ** -11) * mp.mpf(float(s_k[t])) for t in range(S)]
+            q1 = mp.fsum(abs(mp.mpf(float(x))) for x in q[h])   # the dither grid's bias term, 2^-9 ||q||_1
+            u = [mp.mpf(sm) * (qn * kappa + q1 * mp.mpf(2) ** -9) * mp.mpf(float(s_k[t])) for t in range(S)]
             bm1 = mp.fsum(pc[t] * mp.expm1(u[t]) for t in range(S))
             r["lamb"] = mp.log(bm1)
         res.append(r)
@@ -239,27 +239,27 @@ def test_delta_budget_and_tier_b_constant():
     g = _golden("delta_budget.json")
     den = g["n_layers"] * g["n_q_heads"] * g["n_steps"]
     assert round(den / 1e5, 1) == g["denominator_printed_approx"] / 1e5
-    # radius factor: u_t / (sm_scale s_t) = ||q|| sqrt(2 ln(2S/delta_loc)/12) + ||q||_1 2^-11
+    # radius factor: u_t / (sm_scale s_t) = ||q|| sqrt(2 ln(2S/delta_loc)/12) + ||q||_1 2^-9
     kappa = math.sqrt(2 * math.log(2 * 32768 * den / 1e-3) / 12)
     u = A.tier_b_radius(np.ones(128) / math.sqrt(128), np.array([1.0]), 1.0, 32768, 1e-3, 28, 28, 256)
-    assert u[0] == pytest.approx(kappa + math.sqrt(128) * 2.0**-11, rel=1e-14)
+    assert u[0] == pytest.approx(kappa + math.sqrt(128) * 2.0**-9, rel=1e-14)
     # a one-hot query has ||q||_1 = ||q||; the grid term scales with s_t and sm_scale like the rest
     e = np.zeros(128)
     e[37] = -2.0
     u = A.tier_b_radius(e, np.array([0.5, 3.0]), 0.25, 32768, 1e-3, 28, 28, 256)
-    assert np.allclose(u, 0.25 * 2.0 * (kappa + 2.0**-11) * np.array([0.5, 3.0]), rtol=1e-14)
+    assert np.allclose(u, 0.25 * 2.0 * (kappa + 2.0**-9) * np.array([0.5, 3.0]), rtol=1e-14)
 
 
 def test_tier_b_grid_term_covers_the_dither_bias():
     # the worst case of the grid's bias, built by hand: every channel's input sits where the error mean
-    # is largest, and the query's signs follow the bias, so the mean of eps_t is s ||q||_1 2^-11 exactly
+    # is largest, and the query's signs follow the bias, so the mean of eps_t is s ||q||_1 2^-9 exactly
     from oracle.philox import subtractive_error_bias_bound
-    xi = np.arange(1024) * 2.0**-10 - 0.5
+    xi = np.arange(256) * 2.0**-8 - 0.5
     y = np.float32(0.25)                               # on the grid: y + xi hits 1/2 once, rint takes it to 0
     err = np.rint(np.float64(y) + xi) - (np.float64(y) + xi)
-    assert err.min() == -0.5 and err.max() == 0.5 - 2.0**-10
+    assert err.min() == -0.5 and err.max() == 0.5 - 2.0**-8
     # off the grid by half a step the errors form the symmetric mid-point grid: no bias
-    y_mid = np.float64(0.25 + 2.0**-11)
+    y_mid = np.float64(0.25 + 2.0**-9)
     assert (np.rint(y_mid + xi) - (y_mid + xi)).mean() == 0.0
     mu = err.mean()
     assert abs(mu) == pytest.approx(subtractive_error_bias_bound(), rel=1e-12)
@@ -267,7 +267,7 @@ def test_tier_b_grid_term_covers_the_dither_bias():
     q = np.abs(rng.standard_normal(128)) * np.sign(mu)
     s = 0.75
     mean_eps = s * mu * np.sum(q)
-    assert abs(mean_eps) == pytest.approx(s * np.sum(np.abs(q)) * 2.0**-11, rel=1e-12)
+    assert abs(mean_eps) == pytest.approx(s * np.sum(np.abs(q)) * 2.0**-9, rel=1e-12)
     u = A.tier_b_radius(q, np.array([s]), 1.0, 1000, 1e-3, 1, 1, 1)
     noise_only = s * np.linalg.norm(q) * math.sqrt(2 * math.log(2 * 1000 / 1e-3) / 12)
     assert u[0] - noise_only == pytest.approx(abs(mean_eps), rel=1e-12)

@@ -9,11 +9,12 @@ missing key bump, a wrong output-word mapping) breaks:
 * the inverse uses the key schedule and multipliers in the opposite order, so
   a round written with swapped output words fails it;
 * uniformity, independence and avalanche statistics;
-* the dither values lie on the documented 1024-point grid, are exact in fp16,
+* the dither values lie on the documented 256-point grid, are exact in fp16,
   come from the documented bit fields of the documented words, and are
-  uniform (chi-square) with the two fields of a word independent;
+  uniform (chi-square) with the four fields of a word disjoint (together they
+  rebuild the word) and pairwise independent;
 * the subtractively dithered rounding error on that grid: its mean over the
-  grid is within 2^-11 of 0 for every input (exhaustive over the grid), and
+  grid is within 2^-9 of 0 for every input (exhaustive over the grid), and
   its centred moment generating function stays below exp(l^2/24), the
   variance proxy 1/12 that Tier B uses.
 """
@@ -117,37 +118,50 @@ def test_dither_grid_range_and_moments():
     xi = P.dither(0xABCDEF0123, layer=5, kv_head=2, slot=slots, channel=ch)
     assert xi.shape == (20_000, 128)
     assert np.all(xi >= -0.5) and np.all(xi < 0.5)
-    n = (xi + 0.5) * 1024
-    assert np.array_equal(n, np.round(n))                        # on the 2^-10 grid
+    n = (xi + 0.5) * 256
+    assert np.array_equal(n, np.round(n))                        # on the 2^-8 grid
     assert np.all(np.float16(xi).astype(np.float64) == xi)       # exact in fp16
-    # xi + 3/2 is the fp16 number 1 + field / 1024: its bit pattern is 0x3C00 | field
+    # xi + 3/2 is the fp16 number 1 + field / 256: its bit pattern is 0x3C00 | field << 2
     f = P.dither_fields(0xABCDEF0123, 5, 2, slots, ch)
-    assert np.array_equal(np.float16(xi + 1.5).view(np.uint16).astype(np.uint64), np.uint64(0x3C00) | f)
-    # grid mean -2^-11, variance (1 - 2^-20) / 12
-    assert abs(xi.mean() + 2**-11) < 3 * np.sqrt(1 / 12 / xi.size)
-    assert abs(xi.var() - (1 - 2**-20) / 12) < 0.002
-    counts = np.bincount(n.astype(np.int64).ravel(), minlength=1024)
-    expect = xi.size / 1024
+    assert np.array_equal(np.float16(xi + 1.5).view(np.uint16).astype(np.uint64), np.uint64(0x3C00) | (f << np.uint64(2)))
+    # grid mean -2^-9, variance (1 - 2^-16) / 12
+    assert abs(xi.mean() + 2**-9) < 3 * np.sqrt(1 / 12 / xi.size)
+    assert abs(xi.var() - (1 - 2**-16) / 12) < 0.002
+    counts = np.bincount(n.astype(np.int64).ravel(), minlength=256)
+    expect = xi.size / 256
     chi2 = float(np.sum((counts - expect) ** 2 / expect))
-    assert chi2 < 1023 + 5 * np.sqrt(2 * 1023)                  # ~5 sigma of chi-square(1023)
+    assert chi2 < 255 + 5 * np.sqrt(2 * 255)                    # ~5 sigma of chi-square(255)
 
 
-def test_dither_fields_of_one_word_are_independent():
+def test_dither_fields_of_one_word_are_disjoint_and_independent():
     slots = np.arange(200_000)
-    a = P.dither_fields(17, 3, 1, slots, 6)        # bits 0..9 of word 3 ...
-    b = P.dither_fields(17, 3, 1, slots, 7)        # ... and bits 16..25 of the same word
-    w = P.dither_words(17, 3, 1, slots, 6)
-    assert np.array_equal(a, w & np.uint64(0x3FF)) and np.array_equal(b, (w >> np.uint64(16)) & np.uint64(0x3FF))
-    joint = np.bincount(((a >> np.uint64(5)) * np.uint64(32) + (b >> np.uint64(5))).astype(np.int64), minlength=1024)
-    expect = slots.size / 1024
-    chi2 = float(np.sum((joint - expect) ** 2 / expect))
-    assert chi2 < 1023 + 5 * np.sqrt(2 * 1023)
-    assert abs(np.corrcoef(a.astype(np.float64), b.astype(np.float64))[0, 1]) < 0.01
+    w = P.dither_words(17, 3, 1, slots, 12)                       # word 3 of the call: channels 12..15
+    fields = [P.dither_fields(17, 3, 1, slots, c) for c in (12, 13, 14, 15)]
+    rot = ((w >> np.uint64(8)) | (w << np.uint64(24))) & np.uint64(0xFFFFFFFF)
+    m = np.uint64(0xFF)
+    assert np.array_equal(fields[0], (w >> np.uint64(2)) & m) and np.array_equal(fields[1], (w >> np.uint64(18)) & m)
+    assert np.array_equal(fields[2], (rot >> np.uint64(2)) & m) and np.array_equal(fields[3], (rot >> np.uint64(18)) & m)
+    # the four fields are 32 disjoint bits of the word: together they rebuild it
+    back = ((fields[0] << np.uint64(2)) | (fields[1] << np.uint64(18)) | (fields[2] << np.uint64(10))
+            | ((fields[3] & np.uint64(0x3F)) << np.uint64(26)) | (fields[3] >> np.uint64(6)))
+    assert np.array_equal(back, w)
+    for i in range(4):
+        for j in range(i + 1, 4):
+            a, b = fields[i], fields[j]
+            joint = np.bincount(((a >> np.uint64(3)) * np.uint64(32) + (b >> np.uint64(3))).astype(np.int64),
+                                minlength=1024)
+            expect = slots.size / 1024
+            chi2 = float(np.sum((joint - expect) ** 2 / expect))
+            assert chi2 < 1023 + 5 * np.sqrt(2 * 1023)
+            assert abs(np.corrcoef(a.astype(np.float64), b.astype(np.float64))[0, 1]) < 0.01
+
+
+N_GRID = 1 << P.DITHER_BITS
 
 
 def _grid_errors(y):
-    """rint(fp32(y + xi)) - (y + xi) for every xi of the grid (float64, exact), y [..] fp32 -> [.., 1024]."""
-    xi = np.arange(1024) * 2.0**-10 - 0.5
+    """rint(fp32(y + xi)) - (y + xi) for every xi of the grid (float64, exact), y [..] fp32 -> [.., 256]."""
+    xi = np.arange(N_GRID) * 2.0**-8 - 0.5
     y = np.asarray(y, dtype=np.float32).astype(np.float64)[..., None]
     y2 = (y + xi).astype(np.float32).astype(np.float64)
     return np.rint(y2) - (y + xi)
@@ -159,19 +173,19 @@ def test_subtractive_error_bias_exhaustive_over_the_grid():
         rng.uniform(-126.5, 126.5, 4000),
         np.arange(-126.5, 127.0, 0.5),                            # half-integers and integers
         np.arange(-4, 4, 2.0**-12),                               # inputs on and off the dither grid
-        np.array([0.0, 2.0**-30, -2.0**-30, 126.5, -126.5, 0.5 - 2.0**-11, 0.25 + 2.0**-13]),
+        np.array([0.0, 2.0**-30, -2.0**-30, 126.5, -126.5, 0.5 - 2.0**-9, 0.25 + 2.0**-11]),
     ]).astype(np.float32)
     e = _grid_errors(ys)
     # subtractive dither: |error| <= 1/2 LSB, up to the binary32 rounding of y + xi
     assert np.all(np.abs(e) <= 0.5 + 2.0**-24)
     mu = e.mean(axis=-1)
     bound = P.subtractive_error_bias_bound()
-    assert bound == 2.0**-11
+    assert bound == 2.0**-9
     assert np.max(np.abs(mu)) <= bound * (1 + 1e-9) + 2.0**-24   # within half a grid step
     assert np.max(np.abs(mu)) > 0.9 * bound                      # and the bound is reached: the grid does bias
-    # the errors are the grid itself, shifted: sorted, consecutive gaps of 2^-10
+    # the errors are the grid itself, shifted: sorted, consecutive gaps of 2^-8
     gaps = np.diff(np.sort(e[: 4000], axis=-1), axis=-1)
-    assert np.allclose(gaps, 2.0**-10, rtol=0, atol=2.0**-20)
+    assert np.allclose(gaps, 2.0**-8, rtol=0, atol=2.0**-20)
 
 
 def test_subtractive_error_centred_mgf_proxy():
@@ -182,7 +196,7 @@ def test_subtractive_error_centred_mgf_proxy():
         mgf = np.exp(lam * c).mean(axis=-1)
         assert np.all(mgf <= np.exp(lam * lam / 24) * (1 + 1e-12))
         # and equals the closed form of the centred N-point grid, sinh(l/2) / (N sinh(l / 2N))
-        closed = np.sinh(lam / 2) / (1024 * np.sinh(lam / 2048))
+        closed = np.sinh(lam / 2) / (N_GRID * np.sinh(lam / (2 * N_GRID)))
         assert np.allclose(mgf, closed, rtol=1e-9)
 
 
@@ -192,15 +206,19 @@ def test_dither_stream_is_keyed_by_every_coordinate():
     assert not np.array_equal(base, P.dither(99, 2, 0, np.arange(1000), 0))   # layer
     assert not np.array_equal(base, P.dither(99, 1, 1, np.arange(1000), 0))   # kv head
     assert not np.array_equal(base, P.dither(99, 1, 0, np.arange(1, 1001), 0))  # slot
-    # the eight channels of one call: channel c <- word c >> 1, bits 0..9 (c even) or 16..25 (c odd)
+    # the sixteen channels of one call: channel c <- word c >> 2; fields at bits 2..9 / 18..25 of the word
+    # (c = 0, 1 mod 4) and of the word rotated right by 8 bits (c = 2, 3 mod 4)
     w = P.philox4x32_10((np.arange(5, dtype=np.uint64), np.uint64(1), np.uint64(0), np.uint64(0)), (99, 0))
-    for c in range(8):
+    for c in range(16):
         xi = P.dither(99, 1, 0, np.arange(5), c)
-        field = (w[c >> 1] >> np.uint64(16 * (c & 1))) & np.uint64(0x3FF)
-        assert np.array_equal(xi, field.astype(np.float64) / 1024 - 0.5)
-    # channel 8 starts the next call
+        word = w[c >> 2]
+        src = ((word >> np.uint64(8)) | (word << np.uint64(24))) & np.uint64(0xFFFFFFFF) if c & 2 else word
+        field = (src >> np.uint64(18 if c & 1 else 2)) & np.uint64(0xFF)
+        assert np.array_equal(xi, field.astype(np.float64) / 256 - 0.5)
+    # channel 16 starts the next call
     w1 = P.philox4x32_10((np.arange(5, dtype=np.uint64), np.uint64(1), np.uint64(0), np.uint64(1)), (99, 0))
-    assert np.array_equal(P.dither(99, 1, 0, np.arange(5), 8), (w1[0] & np.uint64(0x3FF)).astype(np.float64) / 1024 - 0.5)
+    assert np.array_equal(P.dither(99, 1, 0, np.arange(5), 16),
+                          ((w1[0] >> np.uint64(2)) & np.uint64(0xFF)).astype(np.float64) / 256 - 0.5)
     # stream uniqueness: distinct (slot, layer, head, channel-group) tuples give distinct words
     slots = np.repeat(np.arange(64), 32 * 2)
     heads = np.tile(np.repeat(np.arange(2), 32), 64)
