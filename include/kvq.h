@@ -193,11 +193,12 @@ size_t kvq_sizeof(int32_t which);
  * (amax = 0 stores scale 0 and zero codes).  A cache whose keys are INT8_DITHER_G32 must have
  * INT8_DITHER_G32 values and vice versa, and has no outlier bypass (else KVQ_ERR_UNSUPPORTED_LAYOUT).  The dither xi comes from
  * Philox4x32-10 with key (seed low 32 bits, seed high 32 bits), counter
- * (slot, layer, kv_head, c >> 3), output word (c >> 1) & 3, of which bits
- * 0..9 (c even) or 16..25 (c odd) form the field f, xi = f * 2^-10 - 1/2: a
- * 1024-point grid of [-1/2, 1/2) whose values are exact in fp16, so the
- * decode's fp16 operands carry exactly the xi used here.  The K and V planes
- * of a token share it ([W] Sec. 6.2.1, 6.2.3).
+ * (slot, layer, kv_head, c >> 4), output word w = (c >> 2) & 3; the 8-bit
+ * field f of channel c is bits 2..9 of w (c = 0 mod 4), bits 18..25 of w
+ * (1 mod 4), bits 2..9 (2 mod 4) or 18..25 (3 mod 4) of w rotated right by 8
+ * bits, and xi = f * 2^-8 - 1/2: a 256-point grid of [-1/2, 1/2) whose values
+ * are exact in fp16, so the decode's fp16 operands carry exactly the xi used
+ * here.  The K and V planes of a token share it ([W] Sec. 6.2.1, 6.2.3).
  * Device errors: KVQ_ERR_DEVICE_BOUNDS (slot beyond the cache; the token is
  * skipped), KVQ_ERR_NONFINITE_INPUT (non-finite input or fp16 scale overflow;
  * the token is written), KVQ_ERR_RANGE (a value scale above
@@ -252,9 +253,9 @@ size_t kvq_decode_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t nu
  *   [0] ln(A - 1) of Tier A, A = sum_t p~_t e^{c_t}, c_t = sm_scale *
  *       sum_b ||q_b|| w_{t,b} ([W] Thm. 1, Thm. 2); -inf when A = 1;
  *   [1] ln(A_B - 1) of Tier B, u_t = sm_scale s_t (||q|| sqrt(2 ln(2S/delta_loc)/12)
- *       + ||q||_1 2^-11) ([W] Sec. 4.2; the second term bounds the mean of the dithered
- *       rounding error on the 1024-point dither grid); with 32-channel group scales
- *       u_t = sm_scale (kappa sqrt(sum_g ||q_g||^2 s_{g,t}^2) + 2^-11 sum_g ||q_g||_1 s_{g,t}),
+ *       + ||q||_1 2^-9) ([W] Sec. 4.2; the second term bounds the mean of the dithered
+ *       rounding error on the 256-point dither grid); with 32-channel group scales
+ *       u_t = sm_scale (kappa sqrt(sum_g ||q_g||^2 s_{g,t}^2) + 2^-9 sum_g ||q_g||_1 s_{g,t}),
  *       kappa = sqrt(2 ln(2S/delta_loc)/12); NaN when Tier B is off;
  *   [2] log-sum-exp of the compressed logits (natural log); [3] tokens attended S;
  *   [4] R = sum_t p~_t rho^v_t and [5] Vmax = max_t ||v_t|| from the value
@@ -369,8 +370,13 @@ kvq_status kvq_zero_witness(const kvq_cache* cache, const int32_t* slots_dev, in
  * scratch is a file-scope device array of KVQ_STATIC_WORKSPACE_BYTES (16 MiB)
  * inside the library, which every GPU that loads the library holds until the
  * process exits.  The first call on a device looks up that array's device
- * address (with that device current), so make the first call on each device
- * before any stream capture.  Calls whose workspace need
+ * address (with that device current); with lazy module loading that lookup may
+ * also be when the driver loads the library's device code and reserves the
+ * array, so on a device without 16 MiB free that first call can return
+ * KVQ_ERR_CUDA.  Make the first call on each device at start-up, before any
+ * stream capture.  The address is kept for the life of the process: a device
+ * reset (cudaDeviceReset) invalidates it, and the library does not support
+ * this entry point after one.  Calls whose workspace need
  * (kvq_decode_workspace_size) exceeds KVQ_STATIC_WORKSPACE_BYTES return
  * KVQ_ERR_WORKSPACE_TOO_SMALL without enqueuing work.  The call itself
  * allocates nothing (no cudaMalloc / cudaFree, no allocating library call).

@@ -19,9 +19,9 @@
 //     A - 1 = sum_t e^{x_t} (e^{c_t} - 1) / sum_t e^{x_t} = sum_t e^{x_t + c_t} (1 - e^{-c_t}) / sum_t e^{x_t}
 // as a running maximum and a scaled sum of e^{x_t + c_t - max} (1 - e^{-c_t}), i.e. in the log
 // domain, so c is never clipped and A never overflows; Tier B does the same with
-// u_t = sm_scale s_t (||q|| kappa + ||q||_1 2^-11), kappa = sqrt(2 ln(2S/delta_loc) / 12) (the second
+// u_t = sm_scale s_t (||q|| kappa + ||q||_1 2^-9), kappa = sqrt(2 ln(2S/delta_loc) / 12) (the second
 // term covers the dither grid's bias), or with one scale per 32-channel group
-// u_t = sm_scale (kappa sqrt(sum_g ||q_g||^2 s_{g,t}^2) + 2^-11 sum_g ||q_g||_1 s_{g,t}).
+// u_t = sm_scale (kappa sqrt(sum_g ||q_g||^2 s_{g,t}^2) + 2^-9 sum_g ||q_g||_1 s_{g,t}).
 #pragma once
 
 #include "kvq_common.cuh"
@@ -47,7 +47,7 @@ constexpr int kXiScratch = 16 * 128 * 2;  // per-warp fp16 dither tile (INT8 val
 constexpr int kVStateBytes = 32 * 32;
 // Group-scaled INT8 keys: per-warp table of the query's per-group terms, [kind][group][head] floats:
 // kind 0 = 3/2 sum_c q_c (the fp16 query the key products use), 1 = (sm_scale kappa)^2 ||q_g||^2,
-// 2 = sm_scale 2^-11 ||q_g||_1 (Tier B), for the 4 groups of 32 channels and the 8 heads of a unit.
+// 2 = sm_scale 2^-9 ||q_g||_1 (Tier B), for the 4 groups of 32 channels and the 8 heads of a unit.
 constexpr int kGqBytes = 3 * 4 * 8 * 4;
 constexpr int kExtValue = 1, kExtShapes = 2, kExtContrib = 4;
 constexpr int kStatsFloats = 12;  // per (piece, head): m l mc sc | mu su vr vmax | cmax om 0 0
@@ -625,12 +625,12 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     f.cm_scale = a.sm_scale * ldexpf(1.f, e2);
     // ||q_g|| lives on the lanes of row g; the C fragment needs heads 2c and 2c+1
     // the dither term uses the query on the INT8 channels only (the bypassed ones leave the variance)
-    // u_t = sm_scale s_t (||q|| kappa + ||q||_1 2^-11): the sub-Gaussian radius of WitCert Sec. 4.2 plus
-    // the largest mean of the dithered rounding error on the 1024-point dither grid (2^-11 LSB)
+    // u_t = sm_scale s_t (||q|| kappa + ||q||_1 2^-9): the sub-Gaussian radius of WitCert Sec. 4.2 plus
+    // the largest mean of the dithered rounding error on the 256-point dither grid (2^-9 LSB)
     const float qnorm_g = sqrtf(row_sum4(OUTL ? sq_int8 : sq_all));
     const float l1_g = row_sum4(l1);
     const float kappa = sqrtf(2.f * (logf(2.f * static_cast<float>(seq_total)) - a.ln_delta_loc) / 12.f);
-    const float b_g = __fmaf_rn(qnorm_g, kappa, l1_g * 0.00048828125f /* 2^-11 */);
+    const float b_g = __fmaf_rn(qnorm_g, kappa, l1_g * 0.001953125f /* 2^-9 */);
     f.alpha_b[0] = a.sm_scale * __shfl_sync(kFull, b_g, 8 * c);
     f.alpha_b[1] = a.sm_scale * __shfl_sync(kFull, b_g, 8 * c + 4);
   }
@@ -675,7 +675,7 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
       if (c == 0) {
         f.gq[(0 * 4 + j) * 8 + g] = s1;  // 3/2 sum q - 1152 sum (q + lo) of the group (see gsum)
         f.gq[(1 * 4 + j) * 8 + g] = ka * ka * s2;
-        f.gq[(2 * 4 + j) * 8 + g] = a.sm_scale * 0x1p-11f * s3;
+        f.gq[(2 * 4 + j) * 8 + g] = a.sm_scale * 0x1p-9f * s3;
       }
     }
     __syncwarp();
@@ -774,16 +774,23 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         const int gr = 2 * jj + half;
         const float2 ti = *reinterpret_cast<const float2*>(f.gq + gr * 8 + 2 * c);  // undoes the 3/2, 1152 offsets
         float T[4] = {ti.x, ti.y, ti.x, ti.y};
-        // one Philox call per token: the dither of this lane's 8 channels 32gr + 8c + {0..7} of the group
-        const uint32_t grp = 8 * jj + 4 * half + c;
+        // one Philox call per token serves this lane's 8 channels 32gr + 8c + {0..7}: words 2(c & 1) and
+        // 2(c & 1) + 1 of the call (slot, layer, kv head, (32gr + 8c) >> 4)
+        const uint32_t grp = 2 * gr + (c >> 1);
         const uint4 d0 = philox_finish(grp, pt0, ph, pl.rk0, pl.rk1);
         const uint4 d1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
+        const uint32_t u0 = (c & 1) ? d0.z : d0.x, v0 = (c & 1) ? d0.w : d0.y;  // token g: channels +0..3, +4..7
+        const uint32_t u1 = (c & 1) ? d1.z : d1.x, v1 = (c & 1) ? d1.w : d1.y;  // token g + 8
+        const uint32_t n0[4] = {neg_shifted_dither_lo_f16x2(u0), neg_shifted_dither_hi_f16x2(u0),
+                                neg_shifted_dither_lo_f16x2(v0), neg_shifted_dither_hi_f16x2(v0)};
+        const uint32_t n1[4] = {neg_shifted_dither_lo_f16x2(u1), neg_shifted_dither_hi_f16x2(u1),
+                                neg_shifted_dither_lo_f16x2(v1), neg_shifted_dither_hi_f16x2(v1)};
         if (VDITHER) {
-          const int off = (grp ^ g) << 4;
+          const int off = ((4 * gr + c) ^ g) << 4;
           *reinterpret_cast<uint4*>(xi_tile + g * 256 + off) =
-              make_uint4(neg_dither_f16x2(d0.x), neg_dither_f16x2(d0.y), neg_dither_f16x2(d0.z), neg_dither_f16x2(d0.w));
+              make_uint4(neg_dither_f16x2(n0[0]), neg_dither_f16x2(n0[1]), neg_dither_f16x2(n0[2]), neg_dither_f16x2(n0[3]));
           *reinterpret_cast<uint4*>(xi_tile + (g + 8) * 256 + off) =
-              make_uint4(neg_dither_f16x2(d1.x), neg_dither_f16x2(d1.y), neg_dither_f16x2(d1.z), neg_dither_f16x2(d1.w));
+              make_uint4(neg_dither_f16x2(n1[0]), neg_dither_f16x2(n1[1]), neg_dither_f16x2(n1[2]), neg_dither_f16x2(n1[3]));
         }
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
@@ -792,10 +799,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
           const uint32_t a1 = u8x2_to_f16x2_biased(w1[sidx], 0), a3 = u8x2_to_f16x2_biased(w1[sidx], 1);
           mma_f16_4(T, a0, a1, a2, a3, f.hi[kb][0], f.hi[kb][1]);
           if (LO && f.has_lo) mma_f16_4(T, a0, a1, a2, a3, f.lo[(2 * kb) * 32 + lane], f.lo[(2 * kb + 1) * 32 + lane]);
-          const uint32_t e0 = s2 ? d0.z : d0.x, e2 = s2 ? d0.w : d0.y;
-          const uint32_t e1 = s2 ? d1.z : d1.x, e3 = s2 ? d1.w : d1.y;
-          mma_f16_4(T, neg_shifted_dither_f16x2(e0), neg_shifted_dither_f16x2(e1), neg_shifted_dither_f16x2(e2),
-                    neg_shifted_dither_f16x2(e3), f.hi[kb][0], f.hi[kb][1]);
+          mma_f16_4(T, n0[2 * s2], n1[2 * s2], n0[2 * s2 + 1], n1[2 * s2 + 1], f.hi[kb][0], f.hi[kb][1]);
         }
         // scales of group gr for tokens g (low half) and g + 8 (high half)
         const float2 sg = unpack_f16(*reinterpret_cast<const uint32_t*>(st + L::ksOff + 16 * g + 4 * gr));
@@ -804,6 +808,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       }
     }
   } else {
+    float S2[4] = {0.f, 0.f, 0.f, 0.f};  // the dither products: a second accumulator chain, added at the end
     PhiloxHead ph{};
     PhiloxSlot pt0{}, pt1{};
     if (KDITHER) {
@@ -820,9 +825,13 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       const uint4 k1 = lds128(st + L::kOff + ((2 + jj) * 32 + lane) * 16);
       const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
       const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
-      // key operand words -(xi + 3/2) of tokens g and g + 8 (channel pairs of channels 64jj + 16c + 8(sidx >> 1)
-      // + {0..7}), made from the Philox words; the value side reads the same words from the dither tile
-      uint4 n0{}, n1{};
+      // one Philox call per token serves this lane's 16 channels 64jj + 16c + {0..15} (the call (slot, layer, kv
+      // head, 4jj + c)); word sidx holds the k-step's channels 64jj + 16c + 4 sidx + {0..3}
+      uint4 d0{}, d1{};
+      if (KDITHER) {
+        d0 = philox_finish(4 * jj + c, pt0, ph, pl.rk0, pl.rk1);
+        d1 = philox_finish(4 * jj + c, pt1, ph, pl.rk0, pl.rk1);
+      }
 #pragma unroll
       for (int sidx = 0; sidx < 4; ++sidx) {
         uint32_t a0, a1, a2, a3;
@@ -837,28 +846,28 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         mma_f16_4(S, a0, a1, a2, a3, f.hi[kb][0], f.hi[kb][1]);
         if (LO && f.has_lo) mma_f16_4(S, a0, a1, a2, a3, f.lo[(2 * kb) * 32 + lane], f.lo[(2 * kb + 1) * 32 + lane]);
         if (KDITHER) {
-          // one Philox call per token serves two k-steps: words x, y (channels +0..3) for even sidx,
-          // z, w (+4..7) for odd sidx; each word holds the dither of two channels (a0 / a2 pairs)
-          if ((sidx & 1) == 0) {
-            const uint32_t grp = 8 * jj + 2 * c + (sidx >> 1);
-            const uint4 d0 = philox_finish(grp, pt0, ph, pl.rk0, pl.rk1);
-            const uint4 d1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
-            n0 = make_uint4(neg_shifted_dither_f16x2(d0.x), neg_shifted_dither_f16x2(d0.y),
-                            neg_shifted_dither_f16x2(d0.z), neg_shifted_dither_f16x2(d0.w));
-            n1 = make_uint4(neg_shifted_dither_f16x2(d1.x), neg_shifted_dither_f16x2(d1.y),
-                            neg_shifted_dither_f16x2(d1.z), neg_shifted_dither_f16x2(d1.w));
-            if (VDITHER) {
-              // the value side's dither operand -(xi + 3/2): token-major fp16 tile, 16-byte chunks xor-swizzled by row
-              const int off = ((8 * jj + 2 * c + (sidx >> 1)) ^ g) << 4;
-              *reinterpret_cast<uint4*>(xi_tile + g * 256 + off) = n0;
-              *reinterpret_cast<uint4*>(xi_tile + (g + 8) * 256 + off) = n1;
-            }
+          // the key operand -(xi + 3/2) of channel pairs (+0, +1) and (+2, +3) of tokens g and g + 8
+          const uint32_t w0s = sidx == 0 ? d0.x : sidx == 1 ? d0.y : sidx == 2 ? d0.z : d0.w;
+          const uint32_t w1s = sidx == 0 ? d1.x : sidx == 1 ? d1.y : sidx == 2 ? d1.z : d1.w;
+          const uint32_t e0 = neg_shifted_dither_lo_f16x2(w0s), e2 = neg_shifted_dither_hi_f16x2(w0s);
+          const uint32_t e1 = neg_shifted_dither_lo_f16x2(w1s), e3 = neg_shifted_dither_hi_f16x2(w1s);
+          if (VDITHER && (sidx & 1)) {
+            // the value side's dither operand -(xi + 3/2) of channels 64jj + 16c + 8(sidx >> 1) + {0..7}: token-major
+            // fp16 tile, 16-byte chunks xor-swizzled by row
+            const uint32_t p0 = sidx == 1 ? d0.x : d0.z, p1 = sidx == 1 ? d1.x : d1.z;
+            const int off = ((8 * jj + 2 * c + (sidx >> 1)) ^ g) << 4;
+            *reinterpret_cast<uint4*>(xi_tile + g * 256 + off) =
+                make_uint4(neg_shifted_dither_lo_f16x2(p0), neg_shifted_dither_hi_f16x2(p0), e0, e2);
+            *reinterpret_cast<uint4*>(xi_tile + (g + 8) * 256 + off) =
+                make_uint4(neg_shifted_dither_lo_f16x2(p1), neg_shifted_dither_hi_f16x2(p1), e1, e3);
           }
-          const uint32_t e0 = (sidx & 1) ? n0.z : n0.x, e2 = (sidx & 1) ? n0.w : n0.y;
-          const uint32_t e1 = (sidx & 1) ? n1.z : n1.x, e3 = (sidx & 1) ? n1.w : n1.y;
-          mma_f16_4(S, e0, e1, e2, e3, f.hi[kb][0], f.hi[kb][1]);
+          mma_f16_4(S2, e0, e1, e2, e3, f.hi[kb][0], f.hi[kb][1]);
         }
       }
+    }
+    if (KDITHER) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) S[i] += S2[i];
     }
   }
 
@@ -1002,7 +1011,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     if (KDITHER && tier_b) {
       float uv[4];
       if (GS) {
-        // u_t = sqrt(sum_g (sm_scale kappa)^2 ||q_g||^2 s_{g,t}^2) + sum_g sm_scale 2^-11 ||q_g||_1 s_{g,t}
+        // u_t = sqrt(sum_g (sm_scale kappa)^2 ||q_g||^2 s_{g,t}^2) + sum_g sm_scale 2^-9 ||q_g||_1 s_{g,t}
         // (v = 2r + h: token g + 8r, head 2c + h)
         float var[4] = {0.f, 0.f, 0.f, 0.f}, bias[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll

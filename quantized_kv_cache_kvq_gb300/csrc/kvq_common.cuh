@@ -137,7 +137,7 @@ __device__ __forceinline__ uint4 philox4x32_10_rk(uint4 x, const uint32_t (&k0)[
 }
 
 // The decode regenerates, per page and lane, Philox4x32-10 of the counters (slot, layer, kv_head,
-// grp) for two slots and four groups of eight channels.  In the first three rounds several products depend
+// grp) for two slots and its groups of sixteen channels.  In the first three rounds several products depend
 // only on (layer, kv_head) or only on the slot; they are computed once (PhiloxHead per page,
 // PhiloxSlot per token) and each call finishes with two products in rounds 1-2 and seven full
 // rounds.  With (H, L) the high and low words of a product and y, z, w the counters after rounds
@@ -190,39 +190,42 @@ __device__ __forceinline__ uint4 philox_finish(uint32_t grp, const PhiloxSlot& t
   return x;
 }
 
-// Dither contract: the call (slot, layer, kv_head, channel >> 3) serves eight channels; output word
-// (channel >> 1) & 3 carries two of them, the even channel in bits 0..9 and the odd one in bits 16..25,
-// and xi = field * 2^-10 - 1/2 (a 1024-point grid of [-1/2, 1/2), every value exact in fp16).
-constexpr uint32_t kDitherFields = 0x03FF03FFu;
+// Dither contract: the call (slot, layer, kv_head, channel >> 4) serves sixteen channels; output word
+// w = (channel >> 2) & 3 carries four of them in 8-bit fields: channel 4i at bits 2..9 of w, 4i + 1 at bits
+// 18..25 of w, 4i + 2 and 4i + 3 at bits 2..9 and 18..25 of w rotated right by 8 bits; xi = field * 2^-8 -
+// 1/2 (a 256-point grid of [-1/2, 1/2), every value exact in fp16).
+constexpr uint32_t kDitherFields = 0x03FC03FCu;  // bits 2..9 and 18..25: the fp16 mantissa bits of field * 2^-8
 
-// Dither of a 10-bit field: exact in binary32.
+// Dither of an 8-bit field: exact in binary32.
 __device__ __forceinline__ float dither_of_field(uint32_t field) {
-  return __fmaf_rn(static_cast<float>(field), 0.0009765625f /* 2^-10 */, -0.5f);
+  return __fmaf_rn(static_cast<float>(field), 0.00390625f /* 2^-8 */, -0.5f);
 }
 
-// The decode's key operand of a word: the fp16 pair -(xi + 3/2) = -(1 + field 2^-10) of its two
-// channels (low half: even channel), made by one logic operation -- the field is the mantissa, the
-// sign and exponent bits are those of -1.  The key products add 3/2 sum_c q_c back through the
-// accumulator's initial value.
-__device__ __forceinline__ uint32_t neg_shifted_dither_f16x2(uint32_t w) {
-  return (w & kDitherFields) | 0xBC00BC00u;
+// The decode's key operand for a word's channels 4i, 4i + 1 (lo) or 4i + 2, 4i + 3 (hi): the fp16 pair
+// -(xi + 3/2) = -(1 + field 2^-8) (low half: the lower channel), made by one logic operation -- the field is
+// the mantissa, the sign and exponent bits are those of -1 (plus a rotate for the hi pair).  The key products
+// add 3/2 sum_c q_c back through the accumulator's initial value.
+__device__ __forceinline__ uint32_t neg_shifted_dither_lo_f16x2(uint32_t w) { return (w & kDitherFields) | 0xBC00BC00u; }
+__device__ __forceinline__ uint32_t neg_shifted_dither_hi_f16x2(uint32_t w) {
+  return (__funnelshift_r(w, w, 8) & kDitherFields) | 0xBC00BC00u;
 }
 
-// Minus the dither of a word's two channels as an fp16 pair: -xi = 3/2 - (1 + field 2^-10), exact.
-__device__ __forceinline__ uint32_t neg_dither_f16x2(uint32_t w) {
-  const uint32_t m = neg_shifted_dither_f16x2(w);
-  const __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&m), __half2(__half(1.5f), __half(1.5f)));
+// Minus the dither of a channel pair as an fp16 pair: -xi = 3/2 - (1 + field 2^-8), exact.
+__device__ __forceinline__ uint32_t neg_dither_f16x2(uint32_t shifted) {
+  const __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&shifted), __half2(__half(1.5f), __half(1.5f)));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// The four dithers of channels 4*quad .. 4*quad+3 of (slot, layer, kv_head): half of the call
-// (slot, layer, kv_head, quad >> 1).
+// The four dithers of channels 4*quad .. 4*quad+3 of (slot, layer, kv_head): word quad & 3 of the call
+// (slot, layer, kv_head, quad >> 2).
 __device__ __forceinline__ float4 dither4(uint32_t slot, uint32_t layer, uint32_t kv_head, uint32_t quad,
                                           uint32_t k0, uint32_t k1) {
-  const uint4 w = philox4x32_10(make_uint4(slot, layer, kv_head, quad >> 1), k0, k1);
-  const uint32_t a = (quad & 1u) ? w.z : w.x, b = (quad & 1u) ? w.w : w.y;
-  return make_float4(dither_of_field(a & 0x3FFu), dither_of_field((a >> 16) & 0x3FFu), dither_of_field(b & 0x3FFu),
-                     dither_of_field((b >> 16) & 0x3FFu));
+  const uint4 v = philox4x32_10(make_uint4(slot, layer, kv_head, quad >> 2), k0, k1);
+  const uint32_t q = quad & 3u;
+  const uint32_t w = q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+  const uint32_t r = __funnelshift_r(w, w, 8);
+  return make_float4(dither_of_field((w >> 2) & 0xFFu), dither_of_field((w >> 18) & 0xFFu),
+                     dither_of_field((r >> 2) & 0xFFu), dither_of_field((r >> 18) & 0xFFu));
 }
 
 // ---------------------------------------------------------------------------------------------
