@@ -194,9 +194,8 @@ size_t kvq_sizeof(int32_t which);
  * INT8_DITHER_G32 values and vice versa, and has no outlier bypass (else KVQ_ERR_UNSUPPORTED_LAYOUT).  The dither xi comes from
  * Philox4x32-10 with key (seed low 32 bits, seed high 32 bits), counter
  * (slot, layer, kv_head, c >> 4), output word w = (c >> 2) & 3; the 8-bit
- * field f of channel c is bits 2..9 of w (c = 0 mod 4), bits 18..25 of w
- * (1 mod 4), bits 2..9 (2 mod 4) or 18..25 (3 mod 4) of w rotated right by 8
- * bits, and xi = f * 2^-8 - 1/2: a 256-point grid of [-1/2, 1/2) whose values
+ * field f of channel c is byte (c & 3) of w (bits 8 (c & 3) .. 8 (c & 3) + 7),
+ * and xi = f * 2^-8 - 1/2: a 256-point grid of [-1/2, 1/2) whose values
  * are exact in fp16, so the decode's fp16 operands carry exactly the xi used
  * here.  The K and V planes of a token share it ([W] Sec. 6.2.1, 6.2.3).
  * Device errors: KVQ_ERR_DEVICE_BOUNDS (slot beyond the cache; the token is

@@ -28,27 +28,25 @@ generator and the distribution):
 
     key     = (seed mod 2**32, seed >> 32)
     counter = (slot, layer, kv_head, channel >> 4)
-    word    = output word w = ((channel >> 2) & 3) of that call, r = w rotated right by 8 bits
-    field   = bits 2..9 of w (channel = 0 mod 4), bits 18..25 of w (1 mod 4),
-              bits 2..9 of r (2 mod 4), bits 18..25 of r (3 mod 4)
+    word    = output word w = ((channel >> 2) & 3) of that call
+    field   = byte (channel & 3) of w, i.e. bits 8 (channel & 3) .. 8 (channel & 3) + 7
     xi      = field * 2**-8 - 1/2
 
-so each call serves sixteen consecutive channels (four 8-bit fields per output
-word, 32 disjoint bits of the word; the pages reuse every output word of a
-call, here each word carries four dithers), xi is uniform on the 256-point grid
-{-1/2, -1/2 + 2**-8, ..., 1/2 - 2**-8} of [-1/2, 1/2), every value is exact in
-fp16 (hence in binary32), and the key and value planes of a token share the
-same xi.  The grid is what makes the read side exact: xi + 3/2 = 1 + field *
-2**-8 is the fp16 number whose mantissa bits 2..9 are the field, so it is one
-logic operation on w (or on r) away, -xi = 3/2 - (that number), and the
-decode's fp16 tensor-core operands carry the write side's xi itself, not a
-rounding of it.  What the grid costs is stated by
-``subtractive_error_bias_bound``: for any input, the dithered rounding error
-rint(y + xi) - (y + xi) takes 256 equally spaced values spanning one unit, so
-its mean lies within 2**-9 of 0 (a continuous uniform xi gives exactly 0), and
-its centred part is sub-Gaussian with variance proxy at most 1/12 (the moment
-generating function of an N-point centred grid, sinh(l/2) / (N sinh(l/(2N))),
-never exceeds the continuous one, sinh(l/2) / (l/2)).
+so each call serves sixteen consecutive channels (the four bytes of each output
+word; the pages reuse every output word of a call, here each word carries four
+dithers), xi is uniform on the 256-point grid {-1/2, -1/2 + 2**-8, ..., 1/2 -
+2**-8} of [-1/2, 1/2), every value is exact in fp16 (hence in binary32), and the
+key and value planes of a token share the same xi.  The grid is what makes the
+read side exact: xi + 9/2 = 4 + field * 2**-8 is the fp16 number whose low
+mantissa byte is the field (bit pattern 0x4400 | field), so a byte permutation
+of w gives it, -xi = 9/2 - (that number), and the decode's fp16 tensor-core
+operands carry the write side's xi itself, not a rounding of it.  What the grid
+costs is stated by ``subtractive_error_bias_bound``: for any input, the dithered
+rounding error rint(y + xi) - (y + xi) takes 256 equally spaced values spanning
+one unit, so its mean lies within 2**-9 of 0 (a continuous uniform xi gives
+exactly 0), and its centred part is sub-Gaussian with variance proxy at most
+1/12 (the moment generating function of an N-point centred grid, sinh(l/2) / (N
+sinh(l/(2N))), never exceeds the continuous one, sinh(l/2) / (l/2)).
 
 Parity status: pinned.  ``philox4x32_10`` agrees word for word with the CUDA
 toolkit's own Philox4x32-10 generator (cuRAND device API, four seeds, seven
@@ -111,14 +109,12 @@ def dither_words(seed: int, layer: int, kv_head, slot, channel):
 
 
 def dither_fields(seed: int, layer: int, kv_head, slot, channel) -> np.ndarray:
-    """The 8-bit field of the Philox word that is the dither of (layer, kv_head, slot, channel)."""
+    """The 8-bit field of the Philox word that is the dither of (layer, kv_head, slot, channel): byte
+    (channel & 3) of the word."""
     channel = np.asarray(channel, dtype=np.int64)
     w = dither_words(seed, layer, kv_head, slot, channel)
-    c = np.broadcast_to(channel, w.shape) & 3
-    rot = ((w >> np.uint64(8)) | (w << np.uint64(24))) & _MASK        # w rotated right by 8 bits
-    src = np.where(c >= 2, rot, w)
-    shift = np.where((c & 1) == 1, np.uint64(18), np.uint64(2))
-    return (src >> shift) & np.uint64((1 << DITHER_BITS) - 1)
+    shift = (np.broadcast_to(channel, w.shape) & 3).astype(np.uint64) * np.uint64(8)
+    return (w >> shift) & np.uint64((1 << DITHER_BITS) - 1)
 
 
 def dither(seed: int, layer: int, kv_head, slot, channel) -> np.ndarray:

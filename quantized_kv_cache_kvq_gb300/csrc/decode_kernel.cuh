@@ -46,7 +46,7 @@ constexpr int kXiScratch = 16 * 128 * 2;  // per-warp fp16 dither tile (INT8 val
 // alternative bound shapes (max_t c_t for heads 2c, 2c + 1; sum_t e^{x_t - m} (1 - e^{-c_t}) for both heads).
 constexpr int kVStateBytes = 32 * 32;
 // Group-scaled INT8 keys: per-warp table of the query's per-group terms, [kind][group][head] floats:
-// kind 0 = 3/2 sum_c q_c (the fp16 query the key products use), 1 = (sm_scale kappa)^2 ||q_g||^2,
+// kind 0 = 9/2 sum_c q_c (the fp16 query the key products use), 1 = (sm_scale kappa)^2 ||q_g||^2,
 // 2 = sm_scale 2^-9 ||q_g||_1 (Tier B), for the 4 groups of 32 channels and the 8 heads of a unit.
 constexpr int kGqBytes = 3 * 4 * 8 * 4;
 constexpr int kExtValue = 1, kExtShapes = 2, kExtContrib = 4;
@@ -410,8 +410,8 @@ struct QFrag {
   bool has_lo;
   float cm_scale;    // c_t = cm_scale * (W . QN)  (natural units)
   float alpha_b[2];  // Tier B: u_t = alpha_b[h] * s_t for heads 2c, 2c+1 (natural units)
-  float s_init[2];   // INT8 keys: 3/2 sum_c q_c - 1152 sum_c (q_c + lo_c) (fp16 query parts as the key products
-                     // use them: the dither operand's 3/2 and the code operand's 1152 offsets), heads 2c, 2c+1
+  float s_init[2];   // INT8 keys: 9/2 sum_c q_c - 1152 sum_c (q_c + lo_c) (fp16 query parts as the key products
+                     // use them: the dither operand's 9/2 and the code operand's 1152 offsets), heads 2c, 2c+1
   float* gq;         // group-scaled INT8 keys: the warp's per-group query table (kGqBytes)
   // fixed-channel outlier bypass: B fragment of the bypassed channels (head g; fp16 hi / lo), and the
   // Tier B terms of heads 2c, 2c+1: u_t += beta_o[h] ||k_hat_{t,O}|| + gamma_o[h]
@@ -424,7 +424,7 @@ struct SoftState {
   float mc[2], sc[2];  // Tier A accumulator: reference max (log2 units) and scaled sum
   float mu[2], su[2];  // Tier B accumulator
   float o[8][4];       // O^T fragments of the 8 channel blocks
-  float pv[2];         // INT8 values: lane-partial sum of the fp16 P' weights per head (for the 3/2 correction)
+  float pv[2];         // INT8 values: lane-partial sum of the fp16 P' weights per head (for the 9/2 correction)
   // While every radius seen in the unit is <= kFastRadius the meter sums share the softmax's
   // reference max (mc == m): sum p_t (e^{c_t} - 1).  The first larger radius switches the unit to
   // the general form with its own running max (warp-uniform, sticky until the unit ends).
@@ -535,7 +535,7 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
       put(2 * j, v);
       put(2 * j + 1, v + 4);
       if (GS) {
-        gsum[j] = 1.5f * qsum - 1152.f * (qsum + lsum);
+        gsum[j] = kDitherOffset * qsum - 1152.f * (qsum + lsum);
         float sq = 0.f, l1 = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) { sq = __fmaf_rn(v[e], v[e], sq); l1 += fabsf(v[e]); }
@@ -565,10 +565,10 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
   }
   f.has_lo = __any_sync(kFull, any_lo);
   {
-    // the key products of dithered INT8 pages multiply -(xi + 3/2) by the fp16 query and the codes, as
-    // code + 1152, by its fp16 high and low parts, so their accumulator starts at 3/2 sum_c q_c -
+    // the key products of dithered INT8 pages multiply -(xi + 9/2) by the fp16 query and the codes, as
+    // code + 1152, by its fp16 high and low parts, so their accumulator starts at 9/2 sum_c q_c -
     // 1152 sum_c (q_c + lo_c) (heads 2c and 2c + 1; the sums live on the lanes of row g)
-    const float qs_g = row_sum4(1.5f * qsum - 1152.f * (qsum + lsum));
+    const float qs_g = row_sum4(kDitherOffset * qsum - 1152.f * (qsum + lsum));
     f.s_init[0] = __shfl_sync(kFull, qs_g, 8 * c);
     f.s_init[1] = __shfl_sync(kFull, qs_g, 8 * c + 4);
   }
@@ -673,7 +673,7 @@ __device__ void load_q(const Args& a, int seq, int kvh, int seq_total, QFrag& f)
     for (int j = 0; j < 4; ++j) {
       const float s1 = row_sum4(gsum[j]), s2 = row_sum4(gsq[j]), s3 = row_sum4(gl1[j]);
       if (c == 0) {
-        f.gq[(0 * 4 + j) * 8 + g] = s1;  // 3/2 sum q - 1152 sum (q + lo) of the group (see gsum)
+        f.gq[(0 * 4 + j) * 8 + g] = s1;  // 9/2 sum q - 1152 sum (q + lo) of the group (see gsum)
         f.gq[(1 * 4 + j) * 8 + g] = ka * ka * s2;
         f.gq[(2 * 4 + j) * 8 + g] = a.sm_scale * 0x1p-9f * s3;
       }
@@ -758,7 +758,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     }
   } else if (GS) {
     // group-scaled INT8 keys: k-step kb = 4jj + sidx holds channels 32gr + 8c + 4(sidx & 1) + {0..3} of scale
-    // group gr = 2jj + (sidx >> 1); group gr's product T (started at 3/2 sum of its q, undoing the -(xi + 3/2)
+    // group gr = 2jj + (sidx >> 1); group gr's product T (started at 9/2 sum of its q, undoing the -(xi + 9/2)
     // of the dither products) is multiplied by the token scales of the group into S
     const PhiloxHead ph = philox_head(pl.layer, static_cast<uint32_t>(kvh), pl.rk0, pl.rk1);
     const PhiloxSlot pt0 = philox_slot(phys * kPage + g, ph, pl.rk0, pl.rk1);
@@ -772,7 +772,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int gr = 2 * jj + half;
-        const float2 ti = *reinterpret_cast<const float2*>(f.gq + gr * 8 + 2 * c);  // undoes the 3/2, 1152 offsets
+        const float2 ti = *reinterpret_cast<const float2*>(f.gq + gr * 8 + 2 * c);  // undoes the 9/2, 1152 offsets
         float T[4] = {ti.x, ti.y, ti.x, ti.y};
         // one Philox call per token serves this lane's 8 channels 32gr + 8c + {0..7}: words 2(c & 1) and
         // 2(c & 1) + 1 of the call (slot, layer, kv head, (32gr + 8c) >> 4)
@@ -781,10 +781,10 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         const uint4 d1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
         const uint32_t u0 = (c & 1) ? d0.z : d0.x, v0 = (c & 1) ? d0.w : d0.y;  // token g: channels +0..3, +4..7
         const uint32_t u1 = (c & 1) ? d1.z : d1.x, v1 = (c & 1) ? d1.w : d1.y;  // token g + 8
-        const uint32_t n0[4] = {neg_shifted_dither_lo_f16x2(u0), neg_shifted_dither_hi_f16x2(u0),
-                                neg_shifted_dither_lo_f16x2(v0), neg_shifted_dither_hi_f16x2(v0)};
-        const uint32_t n1[4] = {neg_shifted_dither_lo_f16x2(u1), neg_shifted_dither_hi_f16x2(u1),
-                                neg_shifted_dither_lo_f16x2(v1), neg_shifted_dither_hi_f16x2(v1)};
+        const uint32_t n0[4] = {neg_offset_dither_lo_f16x2(u0), neg_offset_dither_hi_f16x2(u0),
+                                neg_offset_dither_lo_f16x2(v0), neg_offset_dither_hi_f16x2(v0)};
+        const uint32_t n1[4] = {neg_offset_dither_lo_f16x2(u1), neg_offset_dither_hi_f16x2(u1),
+                                neg_offset_dither_lo_f16x2(v1), neg_offset_dither_hi_f16x2(v1)};
         if (VDITHER) {
           const int off = ((4 * gr + c) ^ g) << 4;
           *reinterpret_cast<uint4*>(xi_tile + g * 256 + off) =
@@ -815,7 +815,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       ph = philox_head(pl.layer, static_cast<uint32_t>(kvh), pl.rk0, pl.rk1);
       pt0 = philox_slot(phys * kPage + g, ph, pl.rk0, pl.rk1);
       pt1 = philox_slot(phys * kPage + g + 8, ph, pl.rk0, pl.rk1);
-      // the products below use code + 1152 and -(xi + 3/2); the accumulator's initial value undoes both offsets
+      // the products below use code + 1152 and -(xi + 9/2); the accumulator's initial value undoes both offsets
       S[0] = S[2] = f.s_init[0];
       S[1] = S[3] = f.s_init[1];
     }
@@ -846,20 +846,20 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         mma_f16_4(S, a0, a1, a2, a3, f.hi[kb][0], f.hi[kb][1]);
         if (LO && f.has_lo) mma_f16_4(S, a0, a1, a2, a3, f.lo[(2 * kb) * 32 + lane], f.lo[(2 * kb + 1) * 32 + lane]);
         if (KDITHER) {
-          // the key operand -(xi + 3/2) of channel pairs (+0, +1) and (+2, +3) of tokens g and g + 8
+          // the key operand -(xi + 9/2) of channel pairs (+0, +1) and (+2, +3) of tokens g and g + 8
           const uint32_t w0s = sidx == 0 ? d0.x : sidx == 1 ? d0.y : sidx == 2 ? d0.z : d0.w;
           const uint32_t w1s = sidx == 0 ? d1.x : sidx == 1 ? d1.y : sidx == 2 ? d1.z : d1.w;
-          const uint32_t e0 = neg_shifted_dither_lo_f16x2(w0s), e2 = neg_shifted_dither_hi_f16x2(w0s);
-          const uint32_t e1 = neg_shifted_dither_lo_f16x2(w1s), e3 = neg_shifted_dither_hi_f16x2(w1s);
+          const uint32_t e0 = neg_offset_dither_lo_f16x2(w0s), e2 = neg_offset_dither_hi_f16x2(w0s);
+          const uint32_t e1 = neg_offset_dither_lo_f16x2(w1s), e3 = neg_offset_dither_hi_f16x2(w1s);
           if (VDITHER && (sidx & 1)) {
-            // the value side's dither operand -(xi + 3/2) of channels 64jj + 16c + 8(sidx >> 1) + {0..7}: token-major
+            // the value side's dither operand -(xi + 9/2) of channels 64jj + 16c + 8(sidx >> 1) + {0..7}: token-major
             // fp16 tile, 16-byte chunks xor-swizzled by row
             const uint32_t p0 = sidx == 1 ? d0.x : d0.z, p1 = sidx == 1 ? d1.x : d1.z;
             const int off = ((8 * jj + 2 * c + (sidx >> 1)) ^ g) << 4;
             *reinterpret_cast<uint4*>(xi_tile + g * 256 + off) =
-                make_uint4(neg_shifted_dither_lo_f16x2(p0), neg_shifted_dither_hi_f16x2(p0), e0, e2);
+                make_uint4(neg_offset_dither_lo_f16x2(p0), neg_offset_dither_hi_f16x2(p0), e0, e2);
             *reinterpret_cast<uint4*>(xi_tile + (g + 8) * 256 + off) =
-                make_uint4(neg_shifted_dither_lo_f16x2(p1), neg_shifted_dither_hi_f16x2(p1), e1, e3);
+                make_uint4(neg_offset_dither_lo_f16x2(p1), neg_offset_dither_hi_f16x2(p1), e1, e3);
           }
           mma_f16_4(S2, e0, e1, e2, e3, f.hi[kb][0], f.hi[kb][1]);
         }
@@ -1080,7 +1080,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     const uint32_t b1 = movmatrix_trans(h23);
     if (VDITHER) {
       // the operands below are code + 1152 (removed per page by a product with the constant -1152) and
-      // -(xi + 3/2), whose 3/2 comes back as 3/2 sum_t P'_t per head when the piece is written: the lane's
+      // -(xi + 9/2), whose 9/2 comes back as 9/2 sum_t P'_t per head when the piece is written: the lane's
       // part of that sum (tokens g, g + 8), rescaled like the accumulators
       const float2 q01 = unpack_f16(h01), q23 = unpack_f16(h23);
       f2_unpack(f2_fma(f2_pack(s.pv[0], s.pv[1]), f2_pack(alpha[0], alpha[1]), f2_pack(q01.x + q23.x, q01.y + q23.y)),
@@ -1106,7 +1106,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
       }
     }
     if (VDITHER) {
-      // add (-(xi + 3/2))^T . P'^T: A fragments of the dither tile by transposed 8x8 loads
+      // add (-(xi + 9/2))^T . P'^T: A fragments of the dither tile by transposed 8x8 loads
       __syncwarp();
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
@@ -1233,7 +1233,7 @@ __device__ __forceinline__ void issue_page(const Args& a, uint8_t* stage, uint64
 }
 
 // Partial of one (warp, unit) piece: per real head, (m, l, mc, sc, mu, su) and the 128 O^T values.
-// PV: the value products used the dither operand -(xi + 3/2); 3/2 sum_t P'_t of each head is added back here.
+// PV: the value products used the dither operand -(xi + 9/2); 9/2 sum_t P'_t of each head is added back here.
 template <bool PV>
 __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftState& s, float* vstate) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
@@ -1243,7 +1243,7 @@ __device__ __forceinline__ void write_piece(const Args& a, size_t slot, SoftStat
     l[h] = col_sum8(s.l[h]);
     sc[h] = col_sum8(s.sc[h]);
     su[h] = col_sum8(s.su[h]);
-    if (PV) corr[h] = 1.5f * col_sum8(s.pv[h]);
+    if (PV) corr[h] = kDitherOffset * col_sum8(s.pv[h]);
   }
   float vmax = 0.f, cmax[2] = {0.f, 0.f}, om[2] = {0.f, 0.f};
   if (vstate) {
@@ -1338,7 +1338,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   constexpr bool K16 = fmt_is_16bit(KF);
   constexpr bool XI = fmt_is_int8(KF) && fmt_is_int8(VF);
   constexpr bool GS = fmt_group_scales(KF);
-  constexpr bool PV = XI && !GS;  // value products with the -(xi + 3/2) dither operand
+  constexpr bool PV = XI && !GS;  // value products with the -(xi + 9/2) dither operand
   int32_t* cum = reinterpret_cast<int32_t*>(smem);
   const int cum_bytes = ((a.B + 1) * 4 + 127) & ~127;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

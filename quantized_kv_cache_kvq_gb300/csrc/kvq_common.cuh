@@ -191,41 +191,38 @@ __device__ __forceinline__ uint4 philox_finish(uint32_t grp, const PhiloxSlot& t
 }
 
 // Dither contract: the call (slot, layer, kv_head, channel >> 4) serves sixteen channels; output word
-// w = (channel >> 2) & 3 carries four of them in 8-bit fields: channel 4i at bits 2..9 of w, 4i + 1 at bits
-// 18..25 of w, 4i + 2 and 4i + 3 at bits 2..9 and 18..25 of w rotated right by 8 bits; xi = field * 2^-8 -
-// 1/2 (a 256-point grid of [-1/2, 1/2), every value exact in fp16).
-constexpr uint32_t kDitherFields = 0x03FC03FCu;  // bits 2..9 and 18..25: the fp16 mantissa bits of field * 2^-8
+// w = (channel >> 2) & 3 carries four of them, one per byte: channel 4i + j in byte j of w; xi = byte * 2^-8 - 1/2
+// (a 256-point grid of [-1/2, 1/2), every value exact in fp16).
 
 // Dither of an 8-bit field: exact in binary32.
 __device__ __forceinline__ float dither_of_field(uint32_t field) {
   return __fmaf_rn(static_cast<float>(field), 0.00390625f /* 2^-8 */, -0.5f);
 }
 
-// The decode's key operand for a word's channels 4i, 4i + 1 (lo) or 4i + 2, 4i + 3 (hi): the fp16 pair
-// -(xi + 3/2) = -(1 + field 2^-8) (low half: the lower channel), made by one logic operation -- the field is
-// the mantissa, the sign and exponent bits are those of -1 (plus a rotate for the hi pair).  The key products
-// add 3/2 sum_c q_c back through the accumulator's initial value.
-__device__ __forceinline__ uint32_t neg_shifted_dither_lo_f16x2(uint32_t w) { return (w & kDitherFields) | 0xBC00BC00u; }
-__device__ __forceinline__ uint32_t neg_shifted_dither_hi_f16x2(uint32_t w) {
-  return (__funnelshift_r(w, w, 8) & kDitherFields) | 0xBC00BC00u;
-}
+// The decode's dither operand of a word's channels 4i, 4i + 1 (lo) or 4i + 2, 4i + 3 (hi): the fp16 pair
+// -(xi + 9/2) = -(4 + byte 2^-8), whose bit pattern is 0xC400 | byte (low half: the lower channel), made by one
+// byte permutation of the word with the constant 0xC4 bytes.  The products add 9/2 sum back through the
+// accumulators' initial values (keys) or a lazy per-head correction (values).
+constexpr float kDitherOffset = 4.5f;
+constexpr uint32_t kDitherHighBytes = 0xC4C4C4C4u;
+__device__ __forceinline__ uint32_t neg_offset_dither_lo_f16x2(uint32_t w) { return __byte_perm(w, kDitherHighBytes, 0x4140); }
+__device__ __forceinline__ uint32_t neg_offset_dither_hi_f16x2(uint32_t w) { return __byte_perm(w, kDitherHighBytes, 0x4342); }
 
-// Minus the dither of a channel pair as an fp16 pair: -xi = 3/2 - (1 + field 2^-8), exact.
-__device__ __forceinline__ uint32_t neg_dither_f16x2(uint32_t shifted) {
-  const __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&shifted), __half2(__half(1.5f), __half(1.5f)));
+// Minus the dither of a channel pair as an fp16 pair: -xi = 9/2 - (4 + byte 2^-8), exact.
+__device__ __forceinline__ uint32_t neg_dither_f16x2(uint32_t op) {
+  const __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&op), __half2(__half(kDitherOffset), __half(kDitherOffset)));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// The four dithers of channels 4*quad .. 4*quad+3 of (slot, layer, kv_head): word quad & 3 of the call
-// (slot, layer, kv_head, quad >> 2).
+// The four dithers of channels 4*quad .. 4*quad+3 of (slot, layer, kv_head): the bytes of word quad & 3 of the
+// call (slot, layer, kv_head, quad >> 2).
 __device__ __forceinline__ float4 dither4(uint32_t slot, uint32_t layer, uint32_t kv_head, uint32_t quad,
                                           uint32_t k0, uint32_t k1) {
   const uint4 v = philox4x32_10(make_uint4(slot, layer, kv_head, quad >> 2), k0, k1);
   const uint32_t q = quad & 3u;
   const uint32_t w = q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
-  const uint32_t r = __funnelshift_r(w, w, 8);
-  return make_float4(dither_of_field((w >> 2) & 0xFFu), dither_of_field((w >> 18) & 0xFFu),
-                     dither_of_field((r >> 2) & 0xFFu), dither_of_field((r >> 18) & 0xFFu));
+  return make_float4(dither_of_field(w & 0xFFu), dither_of_field((w >> 8) & 0xFFu),
+                     dither_of_field((w >> 16) & 0xFFu), dither_of_field(w >> 24));
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -77,7 +77,7 @@ def test_fp32_query_path(kvq):
     gpu = run_case_gpu(w8, inputs=inp)
     _check(w8, gpu, reference_case(w8, inputs=inp))
     # dithered INT8 with Tier B: the key products add the query's low part, the dither products and their
-    # 3/2 sum_c q_c start value use the high part
+    # 9/2 sum_c q_c start value use the high part
     wi = W.reduced(CASES["int8"], q_dtype="f32")
     inp = make_inputs(wi)
     gpu = run_case_gpu(wi, inputs=inp)

@@ -98,7 +98,7 @@ def test_decode_group_scales_parity(kvq, name):
 
 
 def test_decode_group_scales_fp32_query(kvq):
-    # the key products add the query's low part; the dither products and each group's 3/2 sum start value use
+    # the key products add the query's low part; the dither products and each group's 9/2 sum start value use
     # the high part
     w = W.reduced(CASES["int8g32"], q_dtype="f32", seq_len=300)
     inp = make_inputs(w)

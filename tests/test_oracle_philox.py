@@ -121,9 +121,10 @@ def test_dither_grid_range_and_moments():
     n = (xi + 0.5) * 256
     assert np.array_equal(n, np.round(n))                        # on the 2^-8 grid
     assert np.all(np.float16(xi).astype(np.float64) == xi)       # exact in fp16
-    # xi + 3/2 is the fp16 number 1 + field / 256: its bit pattern is 0x3C00 | field << 2
+    # xi + 9/2 is the fp16 number 4 + field / 256: its bit pattern is 0x4400 | field (-(xi + 9/2): 0xC400 | field)
     f = P.dither_fields(0xABCDEF0123, 5, 2, slots, ch)
-    assert np.array_equal(np.float16(xi + 1.5).view(np.uint16).astype(np.uint64), np.uint64(0x3C00) | (f << np.uint64(2)))
+    assert np.array_equal(np.float16(xi + 4.5).view(np.uint16).astype(np.uint64), np.uint64(0x4400) | f)
+    assert np.array_equal(np.float16(-(xi + 4.5)).view(np.uint16).astype(np.uint64), np.uint64(0xC400) | f)
     # grid mean -2^-9, variance (1 - 2^-16) / 12
     assert abs(xi.mean() + 2**-9) < 3 * np.sqrt(1 / 12 / xi.size)
     assert abs(xi.var() - (1 - 2**-16) / 12) < 0.002
@@ -137,13 +138,12 @@ def test_dither_fields_of_one_word_are_disjoint_and_independent():
     slots = np.arange(200_000)
     w = P.dither_words(17, 3, 1, slots, 12)                       # word 3 of the call: channels 12..15
     fields = [P.dither_fields(17, 3, 1, slots, c) for c in (12, 13, 14, 15)]
-    rot = ((w >> np.uint64(8)) | (w << np.uint64(24))) & np.uint64(0xFFFFFFFF)
-    m = np.uint64(0xFF)
-    assert np.array_equal(fields[0], (w >> np.uint64(2)) & m) and np.array_equal(fields[1], (w >> np.uint64(18)) & m)
-    assert np.array_equal(fields[2], (rot >> np.uint64(2)) & m) and np.array_equal(fields[3], (rot >> np.uint64(18)) & m)
+    # the fields are the word's bytes, lowest first: via the little-endian byte view of the words
+    as_bytes = w.astype(np.uint32).astype("<u4").view(np.uint8).reshape(-1, 4)
+    for i in range(4):
+        assert np.array_equal(fields[i], as_bytes[:, i].astype(np.uint64))
     # the four fields are 32 disjoint bits of the word: together they rebuild it
-    back = ((fields[0] << np.uint64(2)) | (fields[1] << np.uint64(18)) | (fields[2] << np.uint64(10))
-            | ((fields[3] & np.uint64(0x3F)) << np.uint64(26)) | (fields[3] >> np.uint64(6)))
+    back = fields[0] + fields[1] * np.uint64(256) + fields[2] * np.uint64(65536) + fields[3] * np.uint64(16777216)
     assert np.array_equal(back, w)
     for i in range(4):
         for j in range(i + 1, 4):
@@ -206,19 +206,16 @@ def test_dither_stream_is_keyed_by_every_coordinate():
     assert not np.array_equal(base, P.dither(99, 2, 0, np.arange(1000), 0))   # layer
     assert not np.array_equal(base, P.dither(99, 1, 1, np.arange(1000), 0))   # kv head
     assert not np.array_equal(base, P.dither(99, 1, 0, np.arange(1, 1001), 0))  # slot
-    # the sixteen channels of one call: channel c <- word c >> 2; fields at bits 2..9 / 18..25 of the word
-    # (c = 0, 1 mod 4) and of the word rotated right by 8 bits (c = 2, 3 mod 4)
+    # the sixteen channels of one call: channel c <- byte c & 3 of word c >> 2
     w = P.philox4x32_10((np.arange(5, dtype=np.uint64), np.uint64(1), np.uint64(0), np.uint64(0)), (99, 0))
     for c in range(16):
         xi = P.dither(99, 1, 0, np.arange(5), c)
-        word = w[c >> 2]
-        src = ((word >> np.uint64(8)) | (word << np.uint64(24))) & np.uint64(0xFFFFFFFF) if c & 2 else word
-        field = (src >> np.uint64(18 if c & 1 else 2)) & np.uint64(0xFF)
+        field = (w[c >> 2] // np.uint64(256 ** (c & 3))) % np.uint64(256)
         assert np.array_equal(xi, field.astype(np.float64) / 256 - 0.5)
     # channel 16 starts the next call
     w1 = P.philox4x32_10((np.arange(5, dtype=np.uint64), np.uint64(1), np.uint64(0), np.uint64(1)), (99, 0))
     assert np.array_equal(P.dither(99, 1, 0, np.arange(5), 16),
-                          ((w1[0] >> np.uint64(2)) & np.uint64(0xFF)).astype(np.float64) / 256 - 0.5)
+                          (w1[0] % np.uint64(256)).astype(np.float64) / 256 - 0.5)
     # stream uniqueness: distinct (slot, layer, head, channel-group) tuples give distinct words
     slots = np.repeat(np.arange(64), 32 * 2)
     heads = np.tile(np.repeat(np.arange(2), 32), 64)
