@@ -1491,10 +1491,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
                                                     a.G);
       } else {
         if (nvalid < kPage) zero_tail<KF, VF, METER, VALUE, OUTL>(st, nvalid, a.value_on != 0, a.live.n_out > 4);
-        // one test per page instead of one per k-step (measured: FP8 raw -5.7 %, cartridge -1.0 % per
-        // launch); the INT8-dithered body keeps its per-k-step test, which schedules better there (+4.5 %
-        // with the split)
-        if (fmt_is_int8(KF) || f.has_lo)
+        // one test per page instead of one per k-step (measured per launch: FP8 raw -5.7 %, cartridge -1.0 %,
+        // INT8 -0.9 %: the per-k-step form also loads the query's low parts whether or not it uses them)
+        if (f.has_lo)
           process_page<KF, VF, METER, OUTL, true>(st, xi_tile, xb0, xb1, static_cast<uint32_t>(phys), a.live, kvh, f,
                                                   s, qk_scale, a.tier_b != 0, vstate, ext,
                                                   crow ? crow + (x_begin + j - unit_x0) : nullptr, a.contrib_stride,
