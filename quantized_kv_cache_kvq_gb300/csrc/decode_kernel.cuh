@@ -770,9 +770,10 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
     // group-scaled INT8 keys: k-step kb = 4jj + sidx holds channels 32gr + 8c + 4(sidx & 1) + {0..3} of scale
     // group gr = 2jj + (sidx >> 1); group gr's product T (started at 9/2 sum of its q, undoing the -(xi + 9/2)
     // of the dither products) is multiplied by the token scales of the group into S
+    // lanes c and c ^ 1 use the two halves of the same calls: the even lane makes token g's call, the odd lane
+    // token g + 8's, and each passes its partner the half it needs
     const PhiloxHead ph = philox_head(pl.layer, static_cast<uint32_t>(kvh), pl.rk0, pl.rk1);
-    const PhiloxSlot pt0 = philox_slot(phys * kPage + g, ph, pl.rk0, pl.rk1);
-    const PhiloxSlot pt1 = philox_slot(phys * kPage + g + 8, ph, pl.rk0, pl.rk1);
+    const PhiloxSlot pt = philox_slot(phys * kPage + g + 8 * (c & 1), ph, pl.rk0, pl.rk1);
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
       const uint4 k0 = lds128(st + L::kOff + (jj * 32 + lane) * 16);
@@ -787,10 +788,12 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
         // one Philox call per token serves this lane's 8 channels 32gr + 8c + {0..7}: words 2(c & 1) and
         // 2(c & 1) + 1 of the call (slot, layer, kv head, (32gr + 8c) >> 4)
         const uint32_t grp = 2 * gr + (c >> 1);
-        const uint4 d0 = philox_finish(grp, pt0, ph, pl.rk0, pl.rk1);
-        const uint4 d1 = philox_finish(grp, pt1, ph, pl.rk0, pl.rk1);
-        const uint32_t u0 = (c & 1) ? d0.z : d0.x, v0 = (c & 1) ? d0.w : d0.y;  // token g: channels +0..3, +4..7
-        const uint32_t u1 = (c & 1) ? d1.z : d1.x, v1 = (c & 1) ? d1.w : d1.y;  // token g + 8
+        const uint4 d = philox_finish(grp, pt, ph, pl.rk0, pl.rk1);  // token g (even lanes) or g + 8 (odd lanes)
+        const uint32_t keep0 = (c & 1) ? d.z : d.x, keep1 = (c & 1) ? d.w : d.y;  // this lane's half
+        const uint32_t got0 = __shfl_xor_sync(kFull, (c & 1) ? d.x : d.z, 1);    // the partner's call, this half
+        const uint32_t got1 = __shfl_xor_sync(kFull, (c & 1) ? d.y : d.w, 1);
+        const uint32_t u0 = (c & 1) ? got0 : keep0, v0 = (c & 1) ? got1 : keep1;  // token g: channels +0..3, +4..7
+        const uint32_t u1 = (c & 1) ? keep0 : got0, v1 = (c & 1) ? keep1 : got1;  // token g + 8
         const uint32_t n0[4] = {neg_offset_dither_lo_f16x2(u0), neg_offset_dither_hi_f16x2(u0),
                                 neg_offset_dither_lo_f16x2(v0), neg_offset_dither_hi_f16x2(v0)};
         const uint32_t n1[4] = {neg_offset_dither_lo_f16x2(u1), neg_offset_dither_hi_f16x2(u1),
