@@ -108,13 +108,28 @@ def test_empty_and_single_token_sequences(kvq):
     assert rel.max() <= 2e-3
 
 
-def test_bad_block_table_reported(kvq):
-    w = W.reduced(W.WORKLOADS["tiny"], seq_len=64)
+# one 12-warp layout with branch-issued copies (tiny), one with warp-uniform descriptors (INT8), and the 16-warp
+# raw FP8 layout, whose copy issue predicates the invalid page instead of branching around it
+BAD_BT_CASES = {
+    "tiny": lambda: W.reduced(W.WORKLOADS["tiny"], seq_len=64),
+    "int8": lambda: W.reduced(W.WORKLOADS["int8_7b_certified"], batch=2, seq_len=96),
+    "fp8raw": lambda: W.reduced(W.WORKLOADS["fp8_raw_stress"], batch=2, seq_len=96),
+}
+
+
+@pytest.mark.parametrize("name", list(BAD_BT_CASES))
+def test_bad_block_table_reported(kvq, name):
+    w = BAD_BT_CASES[name]()
     inp = make_inputs(w)
     inp["bt"] = inp["bt"].copy()
     inp["bt"][0, 2] = 10_000  # beyond the cache
     gpu = run_case_gpu(w, inputs=inp)
     assert gpu["err"] == 5  # KVQ_ERR_DEVICE_BOUNDS
+    if w.batch > 1:
+        # the other sequences are untouched by the skipped page
+        ref = reference_case(w, inputs=inp)
+        rel = np.linalg.norm(gpu["out"][1:] - ref["out"][1:], axis=-1) / np.linalg.norm(ref["out"][1:], axis=-1)
+        assert rel.max() <= 2e-3
 
 
 def test_workspace_too_small(kvq):
