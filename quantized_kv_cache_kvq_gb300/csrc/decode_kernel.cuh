@@ -940,7 +940,7 @@ __device__ __forceinline__ void process_page(const uint8_t* st, uint8_t* xi_tile
   // VOTE: the running max moves only when a logit of the page exceeds it, which one vote tells; otherwise the
   // column maxima below would give mnew = m and alpha = 1 exactly, so they are skipped (same results).  Measured per
   // launch: INT8 -2.5 %, group-scaled INT8 -3.2 %, cartridge -0.4 %, ragged +0.3 %; the 16-warp layouts at their
-  // 128-register cap +0.3 % (FP8 raw), so they keep the unconditional form.
+  // 128-register cap +0.3 % (FP8 raw) and the INT8 outlier-bypass body +2.0 %, so those keep the unconditional form.
   float alpha[2] = {1.f, 1.f}, mnew[2] = {s.m[0], s.m[1]};
   const bool grow =
       !VOTE || __any_sync(kFull, (x[0] > s.m[0]) | (x[2] > s.m[0]) | (x[1] > s.m[1]) | (x[3] > s.m[1]));
@@ -1379,7 +1379,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_split_kernel(const Args a) 
   // addresses live on the uniform datapath.  Measured for the 12-warp layouts: INT8 -9.2 % per launch (51 fewer
   // warp-instructions per page), cartridge -1.3 %; for the 16-warp ones +7 % (FP8 raw), so they keep plain values.
   constexpr bool UNI = NW != 16;
-  constexpr bool VOTE = NW != 16;  // the page's max update taken only on a vote (process_page)
+  constexpr bool VOTE = NW != 16 && !OUTL;  // the page's max update taken only on a vote (process_page)
   const int warp = UNI ? static_cast<int>(uniform_u32(threadIdx.x >> 5)) : static_cast<int>(threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
 
